@@ -1,0 +1,540 @@
+"""Benchmark of the GDN layer forward hot path on GB300.
+
+One step = one pass of the forward hot path over one batch of the
+Qwen3.5-4B-shaped GDN layer workload (B=1, T=8192, 16 q/k heads, 32 v heads,
+K=V=128, bf16 inputs, fp32 state): gdn_gate_prep -> gdn_conv1d_varlen (+SiLU,
+Q|K|V channels) -> gdn_chunk_fwd (q/k L2 norm fused).  The segment-parallel
+two-pass (gdn_segment_summary -> gdn_chain_reduce -> gdn_chunk_fwd per
+segment) is measured on the long-context workload (T=131072, 16 heads,
+8 segments) and reported beside it.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host cores instead, on a bounded sample of the same workload.
+Under torchrun every rank runs its own replica of the workload (independent
+layer forwards, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "chunk_gated_delta_rule fwd tokens/s at T=8K,H=32,d=128 bf16; % roofline"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+# ---------------------------------------------------------------- helpers
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:  # noqa: BLE001
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    source="fallback")
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.25)  # first sample before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _kernel_sha() -> str:
+    """Hash of the chunk-kernel sources: a stored ncu traffic figure is valid for these only."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_recurrence_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.startswith("chunk") or fn.endswith(".cuh"):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _stored_traffic(sha: str):
+    """dram read+write bytes per chunk-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "chunk_fwd_qwen35_4b_layer.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if m_sha and m_tr and m_sha.group(1) == sha:
+        return float(m_tr.group(1))
+    return None
+
+
+# ----------------------------------------------------- algorithmic work
+
+def chunk_bytes(wl, n_tok, n_seq, with_h0=False):
+    """HBM bytes one gdn_chunk_fwd must move: q and k once per q/k head, v, o, g, beta
+    once per v-head, h_T (and h0) once per sequence and head."""
+    eb = 2 if wl.dtype == "bf16" else 4
+    per_tok = wl.Hqk * wl.K * eb * 2 + wl.Hv * wl.V * eb * 2 + wl.Hv * 8
+    state = n_seq * wl.Hv * wl.V * wl.K * 4 * (2 if with_h0 else 1)
+    return n_tok * per_tok + state
+
+
+def chunk_flops(wl, n_tok, C=64):
+    """Dense-contraction FLOPs of the chunk form per token and v-head: K K^T, Q K^T and
+    W (6CK), U and P U' (4CV), W S^T, Q S^T and the state update (6KV)."""
+    return n_tok * wl.Hv * (6 * C * wl.K + 4 * C * wl.V + 6 * wl.K * wl.V)
+
+
+def conv_bytes(wl, n_tok):
+    eb = 2 if wl.dtype == "bf16" else 4
+    return n_tok * wl.C * eb * 2 + wl.C * wl.conv_width * eb
+
+
+def gate_bytes(wl, n_tok):
+    eb = 2 if wl.dtype == "bf16" else 4
+    return n_tok * wl.Hv * (2 * eb + 8) + wl.Hv * 8
+
+
+def summary_bytes(wl, n_tok, n_seg):
+    eb = 2 if wl.dtype == "bf16" else 4
+    per_tok = wl.Hqk * wl.K * eb + wl.Hv * wl.V * eb + wl.Hv * 8
+    return n_tok * per_tok + n_seg * wl.Hv * (wl.K * wl.K + wl.V * wl.K) * 4
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_gpu_arm(args, ws, rank, local):
+    import chunked_recurrence_gb300 as crg
+    crg.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl.scaled(seed=wl.seed + 1000 * rank), device=dev, with_direct=False)
+    n_tok, n_seq = inp["n_tok"], inp["n_seq"]
+    cu = inp["cu_seqlens"]
+    if wl.n_samples:  # packed: cu_seqlens derived from position_ids on the device
+        cu_full, cnt = crg.gdn_cu_seqlens_from_position_ids(inp["position_ids"])
+        cu = cu_full[: int(cnt.item()) + 1]
+    bufs = dict(
+        g=torch.empty((n_tok, wl.Hv), device=dev), beta=torch.empty((n_tok, wl.Hv), device=dev),
+        y=torch.empty_like(inp["x"]),
+        o=torch.empty((n_tok, wl.Hv, wl.V), device=dev, dtype=wl.torch_dtype),
+        h_T=torch.empty((n_seq, wl.Hv, wl.V, wl.K), device=dev))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    marks = {}
+
+    def step(record=False):
+        if record:
+            e = [ev() for _ in range(4)]
+            e[0].record(stream)
+        g, beta = crg.gdn_gate_prep(inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
+                                    bufs["g"], bufs["beta"])
+        if record:
+            e[1].record(stream)
+        y = crg.gdn_conv1d_varlen(inp["x"], inp["conv_w"], None, cu,
+                                  None if cu is not None else wl.B, 1, bufs["y"])
+        if record:
+            e[2].record(stream)
+        q, k, v = crg.split_qkv(y, wl.Hqk, wl.Hv, wl.K, wl.V)
+        crg.gdn_chunk_fwd(q, k, v, g, beta, inp["h0"], cu, inp["scale"], True,
+                          B=None if cu is not None else wl.B, o=bufs["o"], h_T=bufs["h_T"])
+        if record:
+            e[3].record(stream)
+            marks.setdefault("ev", []).append(e)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local) if rank == 0 or True else None
+    clocks.start()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.fill_(1)  # L2 flush between steps, outside the per-step events
+        step(record=True)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+
+    per_step = [e[0].elapsed_time(e[3]) for e in marks["ev"]]
+    t_gate = [e[0].elapsed_time(e[1]) for e in marks["ev"]]
+    t_conv = [e[1].elapsed_time(e[2]) for e in marks["ev"]]
+    t_chunk = [e[2].elapsed_time(e[3]) for e in marks["ev"]]
+    step_ms_local = sum(per_step) / len(per_step)
+    step_ms = _max_over_ranks(step_ms_local, ws, dev)
+    tokens_all = _sum_over_ranks(float(n_tok), ws, dev)
+    value = tokens_all / (step_ms * 1e-3)
+
+    peaks = _peaks()
+    chunk_ms = sum(t_chunk) / len(t_chunk)
+    cb = chunk_bytes(wl, n_tok, n_seq, inp["h0"] is not None)
+    cf = chunk_flops(wl, n_tok)
+    achieved = cb / (chunk_ms * 1e-3) / 1e9
+    sha = _kernel_sha()
+    traffic = _stored_traffic(sha)
+    t_hbm = cb / (peaks["hbm_gbs"] * 1e9)
+    t_tc = cf / (peaks["bf16_tflops"] * 1e12)
+    roofline = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "kernel": "gdn_chunk_fwd", "algorithmic_bytes": cb, "algorithmic_flops": cf,
+                "tensor_frac": round(cf / (chunk_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs / bf16_tflops)",
+                "kernel_sha": sha}
+    kernels = {
+        "gdn_gate_prep": _kinfo(sum(t_gate) / len(t_gate), gate_bytes(wl, n_tok), peaks),
+        "gdn_conv1d_varlen": _kinfo(sum(t_conv) / len(t_conv), conv_bytes(wl, n_tok), peaks),
+        "gdn_chunk_fwd": _kinfo(chunk_ms, cb, peaks),
+    }
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws)
+
+    seg = None
+    if not args.no_segment:
+        seg = run_segment_leg(crg, args, dev, stream, peaks)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
+
+    launches_per_step = 3
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; x, a ~N(0,1), conv w ~N(0,0.25), A_log ~U(0,ln16), dt_bias ~U(-1,1))",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hqk": wl.Hqk, "Hv": wl.Hv,
+                   "K": wl.K, "V": wl.V, "conv_channels": wl.C, "conv_width": wl.conv_width,
+                   "chunk": 64, "state": "fp32", "parallelism": f"replicas x{ws}",
+                   "step": "gate_prep + conv1d(SiLU) + chunk_fwd(L2 norm fused)",
+                   "l2": "flushed between steps (512 MiB fill outside the per-step events)"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    if seg is not None:
+        out["segment_parallel"] = seg
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out
+
+
+def _kinfo(ms, nbytes, peaks):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 5), "bytes": nbytes, "achieved_gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+
+
+def run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws):
+    """Same step through the public API, with the step's inputs copied from pinned host
+    memory and its results (o, h_T) read back inside the timed region."""
+    host = {k: inp[k].cpu().pin_memory() for k in ("x", "a", "b")}
+    if inp["h0"] is not None:
+        host["h0"] = inp["h0"].cpu().pin_memory()
+    dev_in = {k: torch.empty_like(inp[k]) for k in host}
+    o_host = torch.empty(bufs["o"].shape, dtype=bufs["o"].dtype).pin_memory()
+    h_host = torch.empty(bufs["h_T"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size() + h_host.numel() * 4
+
+    def one():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        r = crg.layer_fwd(dev_in["x"], inp["conv_w"], dev_in["a"], dev_in["b"], inp["A_log"],
+                          inp["dt_bias"], wl.Hqk, wl.Hv, wl.K, wl.V, dev_in.get("h0"), cu, wl.B,
+                          inp["scale"], bufs=bufs)
+        o_host.copy_(r["o"], non_blocking=True)
+        h_host.copy_(r["h_T"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    _barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(e0.elapsed_time(e1) / n, ws, dev)
+    tok = _sum_over_ranks(float(inp["n_tok"]), ws, dev)
+    return {"value": round(tok / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def run_segment_leg(crg, args, dev, stream, peaks):
+    """Segment-parallel two-pass on the long-context workload (8 segments of 16384)."""
+    wl = synth.WORKLOADS["long_segments"]
+    inp = synth.make_inputs(wl, device=dev, with_front_end=False)
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    g, beta = crg.gdn_gate_prep(inp["a"], inp["b"], inp["A_log"], inp["dt_bias"])
+    bounds = inp["seg_bounds"]
+    n_tok, n_seg = inp["n_tok"], wl.n_seg
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    M = torch.empty((n_seg, wl.Hv, wl.K, wl.K), device=dev)
+    S_loc = torch.empty((n_seg, wl.Hv, wl.V, wl.K), device=dev)
+    S_start = torch.empty_like(S_loc)
+    h_T = torch.empty((wl.Hv, wl.V, wl.K), device=dev)
+    o = torch.empty((n_tok, wl.Hv, wl.V), device=dev, dtype=wl.torch_dtype)
+    o1 = torch.empty_like(o)
+    h1 = torch.empty((1, wl.Hv, wl.V, wl.K), device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    reps = max(2, min(args.steps // 10, 5))
+    t = {"summary": [], "chain": [], "pass2": [], "single": []}
+    for it in range(reps + 1):
+        flush.fill_(1)
+        e = [ev() for _ in range(4)]
+        e[0].record(stream)
+        crg.gdn_segment_summary(k, v, g, beta, bounds, True, M=M, S_local=S_loc)
+        e[1].record(stream)
+        crg.gdn_chain_reduce(M, S_loc, None, S_start, h_T)
+        e[2].record(stream)
+        crg.gdn_chunk_fwd(q, k, v, g, beta, S_start, bounds, inp["scale"], True, o=o,
+                          want_h_T=False)
+        e[3].record(stream)
+        flush.fill_(1)
+        f = [ev(), ev()]
+        f[0].record(stream)
+        crg.gdn_chunk_fwd(q, k, v, g, beta, None, None, inp["scale"], True, B=1, o=o1, h_T=h1)
+        f[1].record(stream)
+        torch.cuda.synchronize()
+        if it == 0:
+            continue  # warm-up
+        t["summary"].append(e[0].elapsed_time(e[1]))
+        t["chain"].append(e[1].elapsed_time(e[2]))
+        t["pass2"].append(e[2].elapsed_time(e[3]))
+        t["single"].append(f[0].elapsed_time(f[1]))
+    m = {k2: sum(v2) / len(v2) for k2, v2 in t.items()}
+    total = m["summary"] + m["chain"] + m["pass2"]
+    rel = float((o.float() - o1.float()).norm() / o1.float().norm())
+    relh = float((h_T - h1[0]).norm() / h1[0].norm())
+    sb = summary_bytes(wl, n_tok, n_seg)
+    cb = chunk_bytes(wl, n_tok, n_seg, with_h0=True)
+    chain_b = n_seg * wl.Hv * (wl.K * wl.K + 2 * wl.V * wl.K) * 4
+    return {"workload": wl.name, "T": wl.T, "H": wl.Hv, "n_seg": n_seg,
+            "tokens_per_s": round(n_tok / (total * 1e-3), 1),
+            "single_pass_tokens_per_s": round(n_tok / (m["single"] * 1e-3), 1),
+            "ms": {k2: round(v2, 4) for k2, v2 in m.items()},
+            "kernels": {"gdn_segment_summary": _kinfo(m["summary"], sb, peaks),
+                        "gdn_chain_reduce": _kinfo(m["chain"], chain_b, peaks),
+                        "gdn_chunk_fwd(pass 2)": _kinfo(m["pass2"], cb, peaks)},
+            "two_pass_vs_single_rel_l2": {"o": rel, "h_T": relh}}
+
+
+# --------------------------------------------------------- CPU oracle legs
+
+def _oracle_sample(wl, inp, n_tok_sample, n_threads):
+    """The fp64 oracle's whole layer forward on the first n_tok_sample tokens (all heads)."""
+    import numpy as np
+
+    import oracle
+    f64 = lambda t: t[:n_tok_sample].detach().cpu().double().numpy()
+    x, a, b = f64(inp["x"]), f64(inp["a"]), f64(inp["b"])
+    w = inp["conv_w"].cpu().double().numpy()
+    A_log, dt = inp["A_log"].cpu().double().numpy(), inp["dt_bias"].cpu().double().numpy()
+    t0 = time.perf_counter()
+    oracle.layer_fwd(x, w, a, b, A_log, dt, wl.Hqk, wl.Hv, wl.K, wl.V, scale=inp["scale"],
+                     n_threads=n_threads)
+    dt_s = time.perf_counter() - t0
+    del np
+    return dt_s
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """Oracle as it stands on the host cores, on a bounded prefix of the workload."""
+    import oracle
+    oracle.build()
+    cores = _cores()
+    n = 256
+    dt = _oracle_sample(wl, inp, n, cores)
+    n_tok = inp["n_tok"]
+    target = int(min(n_tok, max(n, n * budget_s / max(dt, 1e-3))))
+    target = max(64, (target // 64) * 64)
+    dt = _oracle_sample(wl, inp, target, cores)
+    return {"value": round(target / dt, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle layer forward (conv+SiLU, gates, L2 norm, token-by-token "
+                      f"recurrence) on the first {target} of {n_tok} tokens, all {wl.Hv} v-heads, "
+                      f"{cores} threads; {dt:.1f} s"}
+
+
+def run_reference_arm(args, ws, rank):
+    """`--impl reference`: the fp64 CPU oracle on the host cores, per step a bounded
+    sample of the same workload (rank 0 only)."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, device="cpu", with_direct=False)
+    cores = _cores()
+    dt = _oracle_sample(wl, inp, 128, cores)
+    per_step_budget = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = int(min(inp["n_tok"], max(64, 128 * per_step_budget / max(dt, 1e-3))))
+    n = max(64, (n // 64) * 64)
+    for _ in range(args.warmup):
+        _oracle_sample(wl, inp, n, cores)
+    times = [_oracle_sample(wl, inp, n, cores) for _ in range(args.steps)]
+    mean = sum(times) / len(times)
+    value = n / mean
+    sample = (f"fp64 oracle layer forward on the first {n} of {inp['n_tok']} tokens, all "
+              f"{wl.Hv} v-heads, {cores} threads, per step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hqk": wl.Hqk, "Hv": wl.Hv,
+                       "K": wl.K, "V": wl.V, "step": "oracle layer forward, bounded prefix"},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen35_4b_layer", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-segment", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least three warm-up steps
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        out = run_reference_arm(args, ws, rank)
+    else:
+        out = run_gpu_arm(args, ws, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

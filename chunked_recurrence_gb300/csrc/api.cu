@@ -1,0 +1,96 @@
+// api.cu -- argument checking and dispatch of gdn_chunk_fwd / gdn_segment_summary.
+#include "common.cuh"
+
+namespace gdn {
+gdn_status chunk_fwd_simt(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *h0, const int32_t *cu,
+                          const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
+                          cudaStream_t st);
+gdn_status segment_summary_simt(const void *k, const void *v, const float *g, const float *beta,
+                                const int32_t *bounds, int n_seg, const gdn_shape &sh,
+                                uint32_t flags, float *M, float *S_local, cudaStream_t st);
+}  // namespace gdn
+
+using namespace gdn;
+
+namespace {
+
+constexpr size_t kWorkspaceBase = 256;  // status word + padding to keep later regions aligned
+
+// Fills dense strides and checks the shape.  Returns GDN_OK or the error.
+gdn_status normalise_shape(const gdn_shape *in, gdn_shape *out) {
+  if (!in) return GDN_ERR_INVALID_ARG;
+  gdn_shape s = *in;
+  if (s.dtype != GDN_F32 && s.dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (s.B <= 0 || s.T < 0 || s.n_seqs < 0 || s.Hqk <= 0 || s.Hv <= 0 || s.K <= 0 || s.V <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (s.Hv % s.Hqk != 0) return GDN_ERR_INVALID_ARG;
+  if (s.q_stride == 0) s.q_stride = (int64_t)s.Hqk * s.K;
+  if (s.k_stride == 0) s.k_stride = (int64_t)s.Hqk * s.K;
+  if (s.v_stride == 0) s.v_stride = (int64_t)s.Hv * s.V;
+  if (s.q_stride < (int64_t)s.Hqk * s.K || s.k_stride < (int64_t)s.Hqk * s.K ||
+      s.v_stride < (int64_t)s.Hv * s.V)
+    return GDN_ERR_INVALID_ARG;
+  if (!(s.K == 32 || s.K == 64 || s.K == 128)) return GDN_ERR_UNSUPPORTED;
+  if (s.V % 32 != 0 || s.V > 256) return GDN_ERR_UNSUPPORTED;
+  if (s.n_seqs > 65535 || s.Hv > 65535) return GDN_ERR_UNSUPPORTED;
+  *out = s;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape) {
+  gdn_shape s;
+  if (normalise_shape(shape, &s) != GDN_OK) return 0;
+  return kWorkspaceBase;
+}
+
+extern "C" size_t gdn_segment_summary_workspace_bytes(const gdn_shape *shape, int32_t n_seg) {
+  gdn_shape s;
+  if (n_seg < 0 || normalise_shape(shape, &s) != GDN_OK) return 0;
+  return kWorkspaceBase;
+}
+
+extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, const float *h0, const int32_t *cu_seqlens,
+                                    const gdn_shape *shape, float scale, uint32_t flags, void *o,
+                                    float *h_T, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+  gdn_shape s;
+  gdn_status st = normalise_shape(shape, &s);
+  if (st != GDN_OK) return st;
+  if (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_SIMT | GDN_FLAG_O_F32)) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens) {
+    if (s.B != 1 || s.n_seqs < 0) return GDN_ERR_INVALID_ARG;
+  } else if (s.n_seqs != s.B) {
+    return GDN_ERR_INVALID_ARG;
+  }
+  if (!workspace || workspace_bytes < kWorkspaceBase || !aligned(workspace, 256))
+    return GDN_ERR_WORKSPACE;
+  const int64_t n_tok = cu_seqlens ? s.T : (int64_t)s.B * s.T;
+  if (s.n_seqs == 0) return GDN_OK;
+  if (n_tok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+  if (n_tok == 0 && !h_T) return GDN_OK;
+  return chunk_fwd_simt(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
+                        (cudaStream_t)stream);
+}
+
+extern "C" gdn_status gdn_segment_summary(const void *k, const void *v, const float *g,
+                                          const float *beta, const int32_t *seg_bounds,
+                                          int32_t n_seg, const gdn_shape *shape, uint32_t flags,
+                                          float *M, float *S_local, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+  gdn_shape s;
+  gdn_status st = normalise_shape(shape, &s);
+  if (st != GDN_OK) return st;
+  if (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_SIMT)) return GDN_ERR_INVALID_ARG;
+  if (s.B != 1 || n_seg < 0 || n_seg > 65535) return GDN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWorkspaceBase || !aligned(workspace, 256))
+    return GDN_ERR_WORKSPACE;
+  if (n_seg == 0) return GDN_OK;
+  if (!seg_bounds || !M || !S_local) return GDN_ERR_INVALID_ARG;
+  if (s.T > 0 && (!k || !v || !g || !beta)) return GDN_ERR_INVALID_ARG;
+  return segment_summary_simt(k, v, g, beta, seg_bounds, n_seg, s, flags, M, S_local,
+                              (cudaStream_t)stream);
+}

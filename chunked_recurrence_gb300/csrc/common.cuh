@@ -1,0 +1,51 @@
+// common.cuh -- small helpers shared by the libgdn translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;          // tokens per chunk of the UT/WY form
+constexpr float kL2Eps = 1e-6f;     // q/k L2 norm: x / sqrt(sum x^2 + eps)
+
+// device status word written by kernels that detect a problem (first writer wins)
+__device__ __forceinline__ void set_status(int32_t *status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// index of the sequence that holds token t: largest s with cu[s] <= t (n_seqs >= 1)
+__device__ __forceinline__ int seq_of_token(const int32_t *cu, int n_seqs, int64_t t) {
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+inline gdn_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace gdn

@@ -1,0 +1,173 @@
+/*
+ * gdn.h -- C ABI of libgdn: the chunked gated delta rule forward of a Qwen3.5
+ * GatedDeltaNet layer and the steps around it, on one GB300 (sm_103a).
+ *
+ * The method (gated delta rule, Yang, Kautz, Hatamizadeh, "Gated Delta
+ * Networks", ICLR 2025), per v-head h with state S in R^{V x K} kept in fp32:
+ *     S_t = exp(g_t) * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = scale * S_t q_t
+ * "feat: hybrid CP for Qwen3.5 MoE (DeltaNet + attention)", Summary: the layer
+ * is recurrent in a compact per-head state matrix; Approach: a sequence split
+ * only has to pass that state between pieces.
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument is a DEVICE pointer, allocated and owned by the
+ *    caller, unless stated otherwise.  The library never allocates device
+ *    memory, never synchronises the stream, and keeps no per-call state
+ *    between calls beyond a cache of driver entry points.
+ *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream).
+ *  - Argument errors return GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED before
+ *    anything is launched.  A failed launch returns GDN_ERR_CUDA.  Errors that
+ *    only the GPU can see (a bounded wait that gave up, a bad index) are
+ *    written to the status word at the start of the workspace; read it with
+ *    gdn_workspace_status() after the stream has been synchronised.
+ *  - Layouts are token-major and row-major: a token's heads are contiguous,
+ *    and a head's features are contiguous.  "Dense" strides mean the natural
+ *    packed layout.
+ *  - Sequences: with cu_seqlens == NULL the token axis holds B rows of T
+ *    tokens each; with cu_seqlens (int32, n_seqs+1 increasing offsets, first
+ *    0, last = total tokens) it holds n_seqs packed samples and B must be 1
+ *    ("[v1] support GDN Ulysses cp", Key decisions 6: varlen only at batch 1).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* null required pointer, bad size, bad layout */
+  GDN_ERR_UNSUPPORTED = 2, /* valid but not built: e.g. K > 128 */
+  GDN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  GDN_ERR_TIMEOUT = 4,     /* device status: a bounded wait gave up */
+  GDN_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
+  GDN_ERR_BOUNDS = 6       /* device status: an index check failed */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* flags of gdn_chunk_fwd / gdn_segment_summary */
+#define GDN_FLAG_QK_L2NORM 1u  /* normalise q and k to unit L2 norm on load (eps 1e-6 inside the sqrt) */
+#define GDN_FLAG_SIMT 2u       /* force the fp32 CUDA-core kernel (the tensor-core kernel is the default for bf16) */
+#define GDN_FLAG_O_F32 4u      /* write o as fp32 whatever the input dtype (default: o has the input dtype) */
+
+/* Problem shape of the recurrence. */
+typedef struct {
+  int32_t B;        /* batch rows; 1 when cu_seqlens is given */
+  int64_t T;        /* tokens per batch row; total tokens when cu_seqlens is given */
+  int32_t n_seqs;   /* number of sequences: B without cu_seqlens, else len(cu_seqlens) - 1 */
+  int32_t Hqk;      /* q/k heads; v-head h reads q/k head h / (Hv / Hqk) */
+  int32_t Hv;       /* v heads (state heads); a multiple of Hqk */
+  int32_t K;        /* key / query width (32, 64 or 128) */
+  int32_t V;        /* value width (a multiple of 32, at most 256) */
+  int32_t dtype;    /* gdn_dtype of q, k, v and o */
+  int64_t q_stride; /* elements between consecutive tokens of q; 0 = dense (Hqk * K) */
+  int64_t k_stride; /* same for k; 0 = dense (Hqk * K) */
+  int64_t v_stride; /* same for v; 0 = dense (Hv * V) */
+} gdn_shape;
+
+/* Human-readable name of a status code (static string). */
+const char *gdn_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int32_t gdn_version(void);
+
+/* Number of bytes of device workspace gdn_chunk_fwd needs for `shape`
+ * (at least 256: the status word and padding).  0 on a bad shape. */
+size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape);
+
+/* Zero the status word at the start of `workspace` (stream-ordered). */
+gdn_status gdn_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Copy the status word at the start of `workspace` to *status_out (host) and
+ * synchronise `stream`.  *status_out is a gdn_status: GDN_OK when no device
+ * check failed since the last reset. */
+gdn_status gdn_workspace_status(const void *workspace, int32_t *status_out, void *stream);
+
+/* Gate prep of the Qwen3.5 GatedDeltaNet layer ("[v1] support GDN Ulysses
+ * cp", What This PR Does: A_log and dt_bias are per-v-head parameters, a and
+ * b per-token inputs):
+ *     g    = -exp(A_log[h]) * softplus(a + dt_bias[h])
+ *     beta = sigmoid(b)
+ * a, b: [n_tokens, Hv] of ab_dtype; A_log, dt_bias: [Hv] fp32;
+ * g, beta: [n_tokens, Hv] fp32 outputs.  n_tokens may be 0. */
+gdn_status gdn_gate_prep(const void *a, const void *b, int32_t ab_dtype, const float *A_log,
+                         const float *dt_bias, int64_t n_tokens, int32_t Hv, float *g, float *beta,
+                         void *stream);
+
+/* Depthwise causal conv1d over channels with per-sequence zero history
+ * ("[v1] support GDN Ulysses cp", Key decisions 5: the conv is given
+ * cu_seqlens so packed samples never read each other's tokens):
+ *     y[t, c] = act( bias[c] + sum_{j<W} w[c, j] * x[t - W + 1 + j, c] )
+ * where x before the start of t's sequence reads as 0 and act is identity
+ * (act = 0) or SiLU (act = 1).  x, y: [n_tokens, C] (row stride C), w: [C, W],
+ * bias: [C] or NULL, all of `dtype`; accumulation in fp32.  Sequences are
+ * cu_seqlens (n_seqs+1 offsets) or, when cu_seqlens is NULL, n_seqs equal
+ * rows of n_tokens / n_seqs tokens.  1 <= W <= 8.  x and y must not overlap. */
+gdn_status gdn_conv1d_varlen(const void *x, const void *w, const void *bias, int32_t dtype,
+                             const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t C,
+                             int32_t width, int32_t act, void *y, void *stream);
+
+/* The chunked gated delta rule forward (chunk size 64; UT/WY transform inside
+ * each chunk, state passed from chunk to chunk in fp32).
+ *   q, k: [tokens, Hqk, K] (token stride shape->q_stride / k_stride)
+ *   v:    [tokens, Hv, V]  (token stride shape->v_stride)
+ *   g, beta: [tokens, Hv] fp32 (log-decay and write strength, e.g. from gdn_gate_prep)
+ *   h0:   [n_seqs, Hv, V, K] fp32 start states, or NULL for zero
+ *   cu_seqlens: see the conventions above, or NULL
+ *   scale: multiplies o (1/sqrt(K) in Qwen3.5)
+ *   flags: GDN_FLAG_QK_L2NORM, GDN_FLAG_SIMT, GDN_FLAG_O_F32
+ *   o:    [tokens, Hv, V] (dense) of shape->dtype, or fp32 with GDN_FLAG_O_F32; every token written
+ *   h_T:  [n_seqs, Hv, V, K] fp32 final states, or NULL
+ *   workspace: at least gdn_chunk_fwd_workspace_bytes(shape) bytes, 256-byte aligned
+ * A sequence of length 0 leaves h_T = h0 (or 0).  q, k, v, o must not overlap. */
+gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, const float *h0, const int32_t *cu_seqlens,
+                         const gdn_shape *shape, float scale, uint32_t flags, void *o, float *h_T,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Per-segment summary for the segment-parallel two-pass ("Qwen3.5 cp - #1",
+ * Architecture and Patches: the pass that outputs each segment's total
+ * transition M and local state b).  For segment i = [seg_bounds[i],
+ * seg_bounds[i+1]) of the token axis and v-head h, for every start state S:
+ *     S_end = S * M[i, h] + S_local[i, h]
+ *   M:       [n_seg, Hv, K, K] fp32 = prod_t exp(g_t) (I - beta_t k_t k_t^T)
+ *   S_local: [n_seg, Hv, V, K] fp32 = the state reached from 0
+ * shape describes the whole token axis (B must be 1, cu_seqlens is not
+ * taken: segments must lie inside one sequence).  seg_bounds: device int32
+ * [n_seg+1], non-decreasing, inside [0, T]; empty segments give M = I and
+ * S_local = 0.  flags: GDN_FLAG_QK_L2NORM.  workspace as for gdn_chunk_fwd. */
+size_t gdn_segment_summary_workspace_bytes(const gdn_shape *shape, int32_t n_seg);
+gdn_status gdn_segment_summary(const void *k, const void *v, const float *g, const float *beta,
+                               const int32_t *seg_bounds, int32_t n_seg, const gdn_shape *shape,
+                               uint32_t flags, float *M, float *S_local, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/* fp32 chain reduce of the segment summaries ("Qwen3.5 cp - #1",
+ * Architecture: (b, M) chain reduce, fp32):
+ *     S_start[0] = h0 (or 0);  S_start[i+1] = S_start[i] M[i] + S_local[i];  h_T = S_start[n_seg]
+ * M: [n_seg, Hv, K, K], S_local: [n_seg, Hv, V, K], h0: [Hv, V, K] or NULL,
+ * S_start: [n_seg, Hv, V, K] out, h_T: [Hv, V, K] out or NULL; all fp32.
+ * Pass 2 is gdn_chunk_fwd with cu_seqlens = seg_bounds and h0 = S_start. */
+gdn_status gdn_chain_reduce(const float *M, const float *S_local, const float *h0, int32_t n_seg,
+                            int32_t Hv, int32_t K, int32_t V, float *S_start, float *h_T,
+                            void *stream);
+
+/* cu_seqlens from position_ids ("[v1] support GDN Ulysses cp", Key decisions
+ * 4): a sample starts at token 0 and wherever position_ids is 0.
+ * position_ids: [n_tokens] int64; cu_seqlens: [n_tokens + 1] int32 out, of
+ * which the first n_seqs + 1 entries are written; n_seqs: one int32 out on
+ * the device.  n_tokens may be 0 (then n_seqs = 0, cu_seqlens[0] = 0). */
+gdn_status gdn_cu_seqlens_from_position_ids(const int64_t *position_ids, int64_t n_tokens,
+                                            int32_t *cu_seqlens, int32_t *n_seqs, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

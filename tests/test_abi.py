@@ -1,0 +1,131 @@
+"""The C-ABI library builds, loads and exports what include/gdn.h declares;
+host-side argument checks return errors before anything is launched (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_recurrence_gb300 import build as b
+    b.build()
+    import chunked_recurrence_gb300 as crg
+    return crg.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(gdn_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ["gdn_gate_prep", "gdn_conv1d_varlen", "gdn_chunk_fwd", "gdn_segment_summary",
+                 "gdn_chain_reduce", "gdn_cu_seqlens_from_position_ids"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from chunked_recurrence_gb300 import build as b
+    out = subprocess.run(["nm", "-D", "--defined-only", b.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)", out))
+    for name in _declared():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_binding_covers_every_symbol(lib):
+    import chunked_recurrence_gb300 as crg
+    assert set(_declared()) == set(crg.exported_symbols())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.gdn_status_string(0) == b"GDN_OK"
+    assert lib.gdn_status_string(4) == b"GDN_ERR_TIMEOUT"
+    assert lib.gdn_status_string(99) == b"GDN_ERR_UNKNOWN"
+    assert lib.gdn_version() >> 16 == 1
+
+
+def _shape(**kw):
+    import chunked_recurrence_gb300 as crg
+    d = dict(B=1, T=128, n_seqs=1, Hqk=2, Hv=4, K=128, V=128, dtype=1, q_stride=0, k_stride=0,
+             v_stride=0)
+    d.update(kw)
+    return crg.GdnShape(**d)
+
+
+def test_workspace_bytes(lib):
+    assert lib.gdn_chunk_fwd_workspace_bytes(ctypes.byref(_shape())) >= 256
+    assert lib.gdn_chunk_fwd_workspace_bytes(ctypes.byref(_shape(Hv=3))) == 0  # Hv % Hqk
+    assert lib.gdn_chunk_fwd_workspace_bytes(ctypes.byref(_shape(K=96))) == 0
+    assert lib.gdn_segment_summary_workspace_bytes(ctypes.byref(_shape()), 4) >= 256
+
+
+def test_argument_errors_return_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: every call below fails validation first
+    ws = P(0x20000)    # 256-byte aligned
+    sh = _shape()
+    # missing workspace
+    assert lib.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None, ctypes.byref(sh), 1.0, 0,
+                             fake, None, None, 0, None) == 5
+    # misaligned workspace
+    assert lib.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None, ctypes.byref(sh), 1.0, 0,
+                             fake, None, P(0x20004), 256, None) == 5
+    # null q
+    assert lib.gdn_chunk_fwd(None, fake, fake, fake, fake, None, None, ctypes.byref(sh), 1.0, 0,
+                             fake, None, ws, 256, None) == 1
+    # unknown flag bit
+    assert lib.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None, ctypes.byref(sh), 1.0, 64,
+                             fake, None, ws, 256, None) == 1
+    # varlen needs B == 1
+    sh2 = _shape(B=2, n_seqs=2)
+    assert lib.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, fake, ctypes.byref(sh2), 1.0, 0,
+                             fake, None, ws, 256, None) == 1
+    # unsupported widths
+    assert lib.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None,
+                             ctypes.byref(_shape(K=256)), 1.0, 0, fake, None, ws, 256, None) == 2
+    assert lib.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None,
+                             ctypes.byref(_shape(V=48)), 1.0, 0, fake, None, ws, 256, None) == 2
+    # q stride smaller than a token
+    assert lib.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None,
+                             ctypes.byref(_shape(q_stride=100)), 1.0, 0, fake, None, ws, 256,
+                             None) == 1
+    # zero sequences is a no-op
+    assert lib.gdn_chunk_fwd(None, None, None, None, None, None, fake,
+                             ctypes.byref(_shape(n_seqs=0, T=0)), 1.0, 0, None, None, ws, 256,
+                             None) == 0
+    # gate prep / conv / chain reduce / cu_seqlens checks
+    assert lib.gdn_gate_prep(fake, fake, 7, fake, fake, 10, 4, fake, fake, None) == 1
+    assert lib.gdn_gate_prep(None, None, 1, None, None, 0, 4, None, None, None) == 0
+    assert lib.gdn_gate_prep(None, fake, 1, fake, fake, 10, 4, fake, fake, None) == 1
+    assert lib.gdn_conv1d_varlen(fake, fake, None, 1, None, 1, 10, 8, 9, 1, fake, None) == 1
+    assert lib.gdn_conv1d_varlen(fake, fake, None, 1, None, 3, 10, 8, 4, 1, fake, None) == 1
+    assert lib.gdn_conv1d_varlen(fake, fake, None, 1, None, 1, 10, 8, 4, 2, fake, None) == 1
+    assert lib.gdn_chain_reduce(None, None, None, 2, 4, 128, 128, None, None, None) == 1
+    assert lib.gdn_chain_reduce(fake, fake, None, 2, 4, 256, 128, fake, None, None) == 2
+    assert lib.gdn_cu_seqlens_from_position_ids(fake, -1, fake, fake, None) == 1
+    assert lib.gdn_segment_summary(fake, fake, fake, fake, fake, 2, ctypes.byref(_shape(B=2)), 0,
+                                   fake, fake, ws, 256, None) == 1
+    assert lib.gdn_workspace_reset(None, 0, None) == 5
+    assert lib.gdn_workspace_status(None, None, None) == 1
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "chunked_recurrence_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in src and "from oracle" not in src, fn
+                assert "gdn_oracle" not in src, fn
