@@ -5,10 +5,11 @@ namespace gdn {
 gdn_status chunk_fwd_simt(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, const int32_t *cu,
                           const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
-                          cudaStream_t st);
+                          int32_t *status, cudaStream_t st);
 gdn_status segment_summary_simt(const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *bounds, int n_seg, const gdn_shape &sh,
-                                uint32_t flags, float *M, float *S_local, cudaStream_t st);
+                                uint32_t flags, float *M, float *S_local, int32_t *status,
+                                cudaStream_t st);
 }  // namespace gdn
 
 using namespace gdn;
@@ -73,7 +74,7 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   if (n_tok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
   if (n_tok == 0 && !h_T) return GDN_OK;
   return chunk_fwd_simt(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
-                        (cudaStream_t)stream);
+                        (int32_t *)workspace, (cudaStream_t)stream);
 }
 
 extern "C" gdn_status gdn_segment_summary(const void *k, const void *v, const float *g,
@@ -92,5 +93,5 @@ extern "C" gdn_status gdn_segment_summary(const void *k, const void *v, const fl
   if (!seg_bounds || !M || !S_local) return GDN_ERR_INVALID_ARG;
   if (s.T > 0 && (!k || !v || !g || !beta)) return GDN_ERR_INVALID_ARG;
   return segment_summary_simt(k, v, g, beta, seg_bounds, n_seg, s, flags, M, S_local,
-                              (cudaStream_t)stream);
+                              (int32_t *)workspace, (cudaStream_t)stream);
 }

@@ -38,6 +38,8 @@ struct SimtParams {
   const float *g, *beta, *h0;
   const int32_t *cu;  // sequence (or segment) bounds, or null
   int64_t row_T;      // tokens per batch row when cu is null
+  int64_t n_tok;      // tokens on the token axis: every sequence must lie inside it
+  int32_t *status;    // device status word (workspace), set on a bad sequence range
   int Hqk, Hv, K, V;
   int64_t qs, ks, vs;  // token strides (elements)
   float scale;
@@ -84,6 +86,10 @@ __global__ void __launch_bounds__(NT) chunk_simt_kernel(const SimtParams p) {
   } else {
     start = (int64_t)s * p.row_T;
     end = start + p.row_T;
+  }
+  if (start < 0 || end < start || end > p.n_tok) {  // bad cu_seqlens: report, touch nothing
+    if (tid == 0) set_status(p.status, GDN_ERR_BOUNDS);
+    return;
   }
 
   // start state of this block's rows
@@ -303,8 +309,10 @@ namespace gdn {
 gdn_status chunk_fwd_simt(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, const int32_t *cu,
                           const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
-                          cudaStream_t st) {
+                          int32_t *status, cudaStream_t st) {
   SimtParams p{};
+  p.n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
+  p.status = status;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.cu = cu;
   p.row_T = sh.T;
   p.Hqk = sh.Hqk; p.Hv = sh.Hv; p.K = sh.K; p.V = sh.V;
@@ -317,8 +325,11 @@ gdn_status chunk_fwd_simt(const void *q, const void *k, const void *v, const flo
 
 gdn_status segment_summary_simt(const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *bounds, int n_seg, const gdn_shape &sh,
-                                uint32_t flags, float *M, float *S_local, cudaStream_t st) {
+                                uint32_t flags, float *M, float *S_local, int32_t *status,
+                                cudaStream_t st) {
   SimtParams p{};
+  p.n_tok = sh.T;
+  p.status = status;
   p.k = k; p.v = v; p.g = g; p.beta = beta; p.cu = bounds;
   p.Hqk = sh.Hqk; p.Hv = sh.Hv; p.K = sh.K; p.V = sh.V;
   p.qs = sh.q_stride; p.ks = sh.k_stride; p.vs = sh.v_stride;

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(128) conv1d_kernel(const T *__restrict__ x, co
   if (cu) {
     s = seq_of_token(cu, n_seqs, t0);
     while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t0) ++s;  // skip empty sequences
-    start = cu[s];
+    start = max((int64_t)cu[s], (int64_t)0);  // a malformed cu_seqlens never makes a read go negative
     end = cu[s + 1];
   } else {
     start = (t0 / row_T) * row_T;
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(128) conv1d_kernel(const T *__restrict__ x, co
     if (t >= end) {  // a new sequence begins at t: zero history
       if (cu) {
         while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t) ++s;
-        start = cu[s];
+        start = max((int64_t)cu[s], (int64_t)0);
         end = cu[s + 1];
       } else {
         start = t;

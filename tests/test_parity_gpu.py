@@ -251,14 +251,30 @@ def test_resume_through_h0_on_gpu(crg):
     c = make_case([200], 1, 2, 128, 128, "bf16", "mild", True, seed=9)
     o, hT = run_gpu(crg, c)
     t = 77
-    first = dict(c, q=c["q"][:t], k=c["k"][:t], v=c["v"][:t], g=c["g"][:t], beta=c["beta"][:t])
+    first = dict(c, q=c["q"][:t], k=c["k"][:t], v=c["v"][:t], g=c["g"][:t], beta=c["beta"][:t],
+                 cu=torch.tensor([0, t], dtype=torch.int32))
     o1, h1 = run_gpu(crg, first)
     second = dict(c, q=c["q"][t:], k=c["k"][t:], v=c["v"][t:], g=c["g"][t:], beta=c["beta"][t:],
-                  h0=h1)
+                  h0=h1, cu=torch.tensor([0, 200 - t], dtype=torch.int32))
     o2, h2 = run_gpu(crg, second)
     ro, rh = run_oracle(c)
     assert_close(torch.cat([o1, o2]), ro, "bf16", "resumed o")
     assert_close(h2, rh, "bf16", "resumed h_T")
+
+
+def test_bad_cu_seqlens_reported_not_read(crg):
+    """A sequence range past the token axis sets GDN_ERR_BOUNDS in the workspace status
+    word; the kernel's own range check skips the block before any load."""
+    c = make_case([100], 1, 2, 64, 64, "bf16", seed=13)
+    ws = crg.Workspace(4096, DEV)
+    d = lambda t: t.to(DEV)
+    bad = torch.tensor([0, 60, 164], dtype=torch.int32, device=DEV)  # 164 > 100 tokens
+    o = torch.zeros((100, 2, 64), device=DEV, dtype=torch.bfloat16)
+    crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), None, bad,
+                      c["scale"], o=o, workspace=ws)
+    assert ws.status() == 6  # GDN_ERR_BOUNDS
+    ws.reset()
+    assert ws.status() == 0
 
 
 def test_device_status_clean(crg):
@@ -313,8 +329,20 @@ def _layer_case(wl, device="cpu"):
     return inp
 
 
-def _oracle_layer_heads(inp, heads):
-    """Oracle layer forward for a subset of v-heads (conv on just their channels)."""
+def _to_interface(y, dtype):
+    """Round an oracle stage output to the dtype the ABI stores it in between stages."""
+    t = torch.from_numpy(np.ascontiguousarray(y))
+    t = t.to(torch.bfloat16) if dtype == "bf16" else t.to(torch.float32)
+    return t.double().numpy()
+
+
+def _oracle_layer_heads(inp, heads, interface_round=True):
+    """Oracle layer forward for a subset of v-heads (conv on just their channels).
+
+    With interface_round the oracle stores each stage's output in the dtype the
+    ABI passes between stages (the conv output y in the input dtype, g and beta in
+    fp32), rounding its own fp64 values, so that the final comparison measures the
+    chunk kernel's error on the inputs it is given; without it the chain stays fp64."""
     wl = inp["workload"]
     Hqk, Hv, K, V = wl.Hqk, wl.Hv, wl.K, wl.V
     r = Hv // Hqk
@@ -329,10 +357,14 @@ def _oracle_layer_heads(inp, heads):
         xs = to64(x.index_select(1, ci))
         ws = to64(w.index_select(0, ci))
         y = oracle.conv1d(xs, ws, None, cu, 1, B=wl.B)
+        if interface_round:
+            y = _to_interface(y, wl.dtype)
         n = xs.shape[0]
         q, k, v = y[:, :K].reshape(n, 1, K), y[:, K:2 * K].reshape(n, 1, K), y[:, 2 * K:].reshape(n, 1, V)
         g, beta = oracle.gate_prep(to64(inp["a"][:, h:h + 1]), to64(inp["b"][:, h:h + 1]),
                                    to64(inp["A_log"][h:h + 1]), to64(inp["dt_bias"][h:h + 1]))
+        if interface_round:
+            g, beta = _to_interface(g, "f32"), _to_interface(beta, "f32")
         h0 = None if inp["h0"] is None else to64(inp["h0"][:, h:h + 1])
         o, hT = oracle.gdn_fwd(q, k, v, g, beta, h0, cu, inp["scale"], True, B=wl.B)
         outs[h] = (o[:, 0], hT[:, 0])
@@ -376,3 +408,8 @@ def test_reduced_workloads(crg, name):
     for h, (ro, rh) in ref.items():
         assert_close(r["o"][:, h].cpu(), ro, "bf16", f"{name} o head {h}")
         assert_close(r["h_T"][:, h].cpu(), rh, "bf16", f"{name} h_T head {h}")
+    # end to end against the all-fp64 chain: the relative-L2 bar still holds
+    ref64 = _oracle_layer_heads(inp, heads, interface_round=False)
+    for h, (ro, rh) in ref64.items():
+        assert metrics(r["o"][:, h].cpu(), ro)["rel_l2"] <= 5e-3
+        assert metrics(r["h_T"][:, h].cpu(), rh)["rel_l2"] <= 5e-3
