@@ -10,6 +10,12 @@ gdn_status segment_summary_simt(const void *k, const void *v, const float *g, co
                                 const int32_t *bounds, int n_seg, const gdn_shape &sh,
                                 uint32_t flags, float *M, float *S_local, int32_t *status,
                                 cudaStream_t st);
+bool chunk_tc_supported(const void *q, const void *k, const void *v, const gdn_shape &sh);
+size_t chunk_tc_workspace_bytes(const gdn_shape &sh, int64_t n_tok);
+gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const float *h0, const int32_t *cu,
+                        const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
+                        void *workspace, size_t ws_bytes, cudaStream_t st);
 }  // namespace gdn
 
 using namespace gdn;
@@ -41,9 +47,14 @@ gdn_status normalise_shape(const gdn_shape *in, gdn_shape *out) {
 
 }  // namespace
 
+// The tensor-core path (bf16, K = 128) keeps T = (I + A)^-1 diag(beta) of every
+// chunk and v-head in the workspace between its two kernels.
+bool tc_shape(const gdn_shape &s) { return s.dtype == GDN_BF16 && s.K == 128 && s.V % 32 == 0; }
+
 extern "C" size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape) {
   gdn_shape s;
   if (normalise_shape(shape, &s) != GDN_OK) return 0;
+  if (tc_shape(s)) return chunk_tc_workspace_bytes(s, (int64_t)s.B * s.T);
   return kWorkspaceBase;
 }
 
@@ -73,6 +84,9 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   if (s.n_seqs == 0) return GDN_OK;
   if (n_tok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
   if (n_tok == 0 && !h_T) return GDN_OK;
+  if (!(flags & GDN_FLAG_SIMT) && n_tok > 0 && tc_shape(s) && chunk_tc_supported(q, k, v, s))
+    return chunk_fwd_tc(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T, workspace,
+                        workspace_bytes, (cudaStream_t)stream);
   return chunk_fwd_simt(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
                         (int32_t *)workspace, (cudaStream_t)stream);
 }
