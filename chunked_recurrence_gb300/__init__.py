@@ -54,6 +54,8 @@ _SIGS = {
                           ctypes.c_int),
     "gdn_chunk_fwd": ([_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(GdnShape), _F32, _U32, _P, _P,
                        _P, _SZ, _P], ctypes.c_int),
+    "gdn_chunk_fwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(GdnShape), _F32, _U32,
+                               _P, _P, _P], ctypes.c_int),
     "gdn_segment_summary": ([_P, _P, _P, _P, _P, _I32, ctypes.POINTER(GdnShape), _U32, _P, _P,
                              _P, _SZ, _P], ctypes.c_int),
     "gdn_chain_reduce": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
@@ -260,6 +262,25 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm
                                 _ptr(cu_seqlens), ctypes.byref(sh), float(scale), flags, _ptr(o),
                                 _ptr(h_T), ws.ptr(), ws.nbytes, _stream(v, stream)),
            "gdn_chunk_fwd")
+    return o, h_T
+
+
+def gdn_chunk_fwd_noalloc(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm_qk=True,
+                          B=None, o=None, h_T=None, stream=None):
+    """gdn_chunk_fwd without a workspace, for callers that cannot allocate device
+    memory: the library's fixed 16 MiB device scratch array is used instead.
+    Outputs must then be passed in (o, h_T); shapes whose scratch does not fit
+    raise GdnError (GDN_ERR_WORKSPACE)."""
+    _need_cuda(q, k, v, g, beta, h0, cu_seqlens)
+    sh = make_shape(q, k, v, cu_seqlens, B)
+    if scale is None:
+        scale = sh.K ** -0.5
+    flags = GDN_FLAG_QK_L2NORM if l2norm_qk else 0
+    assert o is not None, "gdn_chunk_fwd_noalloc writes into caller-provided o"
+    _check(load().gdn_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                        _ptr(cu_seqlens), ctypes.byref(sh), float(scale), flags,
+                                        _ptr(o), _ptr(h_T), _stream(v, stream)),
+           "gdn_chunk_fwd_noalloc")
     return o, h_T
 
 

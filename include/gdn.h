@@ -132,6 +132,32 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
                          const gdn_shape *shape, float scale, uint32_t flags, void *o, float *h_T,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/* gdn_chunk_fwd for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this call; it exists for users of this library whose
+ * host application owns the whole device memory pool (an inference server or
+ * engine plugin with a fixed budget and its own allocator), or whose code path
+ * may not take the device-wide synchronisation of cudaMalloc/cudaFree.
+ *
+ * Arguments, layouts, results and error codes are those of gdn_chunk_fwd
+ * without the workspace: the scratch lives in a 16 MiB file-scope device
+ * array inside libgdn, held by every GPU that loads the library until the
+ * process exits.  The call allocates nothing.
+ *  - Size limit: the scratch gdn_chunk_fwd_workspace_bytes(shape) reports must
+ *    fit in 16 MiB; larger shapes return GDN_ERR_WORKSPACE before anything runs
+ *    (on the bf16, K = 128 path that is 256 + 8320 * Hv * (n_seqs + ceil(tokens/64))
+ *    bytes, e.g. 2048 tokens x 32 v-heads or 8192 tokens x 8 v-heads).
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array and clears its status word
+ *    first; calls that overlap on the GPU (different streams, no ordering)
+ *    race on it and must not be issued.  Device-side status (bad sequence
+ *    ranges, timeouts) is not readable through this entry point. */
+gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const float *h0, const int32_t *cu_seqlens,
+                                 const gdn_shape *shape, float scale, uint32_t flags, void *o,
+                                 float *h_T, void *stream);
+
 /* Per-segment summary for the segment-parallel two-pass ("Qwen3.5 cp - #1",
  * Architecture and Patches: the pass that outputs each segment's total
  * transition M and local state b).  For segment i = [seg_bounds[i],

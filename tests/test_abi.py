@@ -121,6 +121,18 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.gdn_workspace_status(None, None, None) == 1
 
 
+def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
+    """gdn_chunk_fwd_noalloc checks the scratch it needs against its fixed 16 MiB
+    array before any CUDA call: a million tokens x 4 v-heads (~545 MB) is refused."""
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced
+    big = _shape(T=1 << 20)
+    assert lib.gdn_chunk_fwd_noalloc(fake, fake, fake, fake, fake, None, None, ctypes.byref(big),
+                                     1.0, 1, fake, None, None) == 5  # GDN_ERR_WORKSPACE
+    assert lib.gdn_chunk_fwd_noalloc(fake, fake, fake, fake, fake, None, None,
+                                     ctypes.byref(_shape(Hv=3)), 1.0, 1, fake, None, None) == 1
+
+
 def test_product_package_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "chunked_recurrence_gb300")
     for dirpath, _, files in os.walk(pkg):
