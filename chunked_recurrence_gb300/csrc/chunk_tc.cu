@@ -246,23 +246,36 @@ __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
         X[i * kAP + lt] = (i > lt) ? bh[i] * expf(gh[i] - gl) * KK[i * kAP + lt] : 0.f;
     }
     __syncthreads();
-    // X = (I + A)^-1 by forward substitution, row by row, one column a thread;
-    // rows < i of X already replaced A's rows.
-    for (int i = 1; i < C; ++i) {
-      float x = 0.f;
-      if (active && lt < i) {
-        x = X[i * kAP + lt];
-        for (int m = lt + 1; m < i; ++m) x = fmaf(X[i * kAP + m], X[m * kAP + lt], x);
-      }
-      __syncthreads();
-      if (active && lt < i) X[i * kAP + lt] = -x;
-      __syncthreads();
-    }
-    // T row lt = X row lt scaled by beta per column (unit diagonal -> beta), packed fp32
+    // X = (I + A)^-1, one column per thread, held in registers: x_r = delta_rc - sum_{j<r} A_rj x_j.
+    // Every thread walks the same (r, j) sequence, so the A_rj reads are warp-wide broadcasts and
+    // no barrier is needed; entries above the diagonal of the column are zero and add nothing.
     if (active) {
-      float *dst = p.T + ((size_t)slot * p.Hv + hv) * kTPacked + lt * (lt + 1) / 2;
-      for (int c0 = 0; c0 < lt; ++c0) dst[c0] = X[lt * kAP + c0] * bh[c0];
-      dst[lt] = bh[lt];
+      float x[C];
+#pragma unroll
+      for (int r = 0; r < C; ++r) x[r] = 0.f;
+      x[0] = (lt == 0) ? 1.f : 0.f;
+#pragma unroll
+      for (int r = 1; r < C; ++r) {
+        const float *Ar = X + r * kAP;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int j = 0; j + 3 < r; j += 4) {
+          a0 = fmaf(Ar[j], x[j], a0);
+          a1 = fmaf(Ar[j + 1], x[j + 1], a1);
+          a2 = fmaf(Ar[j + 2], x[j + 2], a2);
+          a3 = fmaf(Ar[j + 3], x[j + 3], a3);
+        }
+#pragma unroll
+        for (int j = r & ~3; j < r; ++j) a0 = fmaf(Ar[j], x[j], a0);
+        x[r] = (r == lt) ? 1.f : -((a0 + a1) + (a2 + a3));
+      }
+      // T[r][lt] = x_r beta_lt for r >= lt (x_lt = 1 gives the diagonal beta_lt), packed rows;
+      // for a fixed r the 32 lanes write 32 consecutive floats.
+      float *dst = p.T + ((size_t)slot * p.Hv + hv) * kTPacked;
+      const float bl = bh[lt];
+#pragma unroll
+      for (int r = 0; r < C; ++r)
+        if (r >= lt) dst[r * (r + 1) / 2 + lt] = x[r] * bl;
     }
     __syncthreads();
   }
@@ -294,7 +307,7 @@ constexpr uint32_t OFF_TL = 99328;      // 8 KB T lo
 constexpr uint32_t OFF_TPH = 107520;    // 8 KB T diag(b/|k|) hi
 constexpr uint32_t OFF_TPL = 115712;    // 8 KB T diag(b/|k|) lo
 constexpr uint32_t OFF_NW = 123904;     // 16 KB -W              [fb][64][128 B]
-constexpr uint32_t OFF_QT = 140288;     // 16 KB scale diag(b/|q|) q
+constexpr uint32_t OFF_QT = 140288;     // 16 KB (unused)
 constexpr uint32_t OFF_PT = 156672;     // 8 KB  P without its diagonal [64][128 B]
 constexpr uint32_t OFF_ST = 164864;     // 8 KB  S^T (bf16)      [128 feat][32 v] SW64
 constexpr uint32_t OFF_UP = 173056;     // 4 KB  U' hi           [64 tok][32 v] SW64
@@ -305,7 +318,8 @@ constexpr uint32_t kTcSmem = 189440 + 1024;
 constexpr uint32_t kStageBytes = 4 * 8192 + 4096 + (uint32_t)kTBytes;  // k, q (2 boxes each), v, T
 
 // TMEM columns
-constexpr uint32_t COL_QK = 0, COL_W = 64, COL_U = 192, COL_O = 224, COL_S = 256, kTmemCols = 512;
+constexpr uint32_t COL_QK = 0, COL_W = 64, COL_U = 192, COL_O = 224, COL_S = 256, COL_OB = 288,
+                   kTmemCols = 512;
 
 __device__ __forceinline__ void put_bf16(uint8_t *tile, int row, int col, float x) {
   *reinterpret_cast<__nv_bfloat16 *>(tile + sw128_off(row, col)) = __float2bfloat16_rn(x);
@@ -318,7 +332,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t bar_tma[2], bar_mma;
   __shared__ uint32_t tbase;
-  __shared__ float gam[C], bex[C], dec[C], kinv[C], qinv[C];
+  __shared__ float gam[C], gl2[C], bex[C], dec[C], kinv[C], qinv[C], alpha[C];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int v0 = blockIdx.x * BVT, h = blockIdx.y, s = blockIdx.z;
@@ -346,9 +360,6 @@ __global__ void __launch_bounds__(NT, 1)
     tmem_alloc(&tbase, kTmemCols);
     tmem_relinquish();
   }
-  // the four T tiles keep a zero upper triangle: clear them once
-  for (uint32_t i = tid; i < 4 * 8192 / 16; i += NT)
-    reinterpret_cast<uint4 *>(sm + OFF_TH)[i] = make_uint4(0, 0, 0, 0);
   // fp32 state, transposed: thread f holds S[v0 + v][f] for v < 32
   float S[BVT];
   const float *h0p = p.h0 ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0) * KD + tid : nullptr;
@@ -406,6 +417,9 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_after();
   };
 
+  // g of the first chunk; later chunks' g is loaded one chunk ahead
+  float gnext = 0.f;
+  if (n_chunks > 0 && tid < C && start + tid < end) gnext = p.g[(start + tid) * p.Hv + h];
   const bool lane_row = lane < 16;      // rows of M = 64 results: lanes 0-15 of each quarter
   const int mrow = warp * 16 + lane;    // the token row this thread holds in M = 64 results
   const int row = mrow & 63;            // in-range index for the threads without a row
@@ -424,7 +438,11 @@ __global__ void __launch_bounds__(NT, 1)
       tma_inflight[st ^ 1] = true;
     }
     // ---- gates of this chunk: gamma (cumsum), b = exp(gamma), d = exp(gamma_last - gamma)
-    if (tid < C) gam[tid] = tid < n ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
+    if (tid < C) gam[tid] = gnext;
+    if (ci + 1 < n_chunks && tid < C) {
+      const int64_t t1 = t0 + C;
+      gnext = (t1 + tid < end) ? p.g[(t1 + tid) * p.Hv + h] : 0.f;
+    }
     __syncthreads();
     if (warp == 0) {
       const float g0 = gam[2 * lane], g1 = gam[2 * lane + 1];
@@ -438,6 +456,8 @@ __global__ void __launch_bounds__(NT, 1)
       const float ga = incl - g1, gb = incl;
       gam[2 * lane] = ga;
       gam[2 * lane + 1] = gb;
+      gl2[2 * lane] = ga * 1.4426950408889634f;
+      gl2[2 * lane + 1] = gb * 1.4426950408889634f;
       bex[2 * lane] = expf(ga);
       bex[2 * lane + 1] = expf(gb);
       dec[2 * lane] = expf(last - ga);
@@ -474,39 +494,42 @@ __global__ void __launch_bounds__(NT, 1)
         kinv[r] = inv;
       } else {
         qinv[r] = inv;
-        const float sc = p.scale * bex[r] * inv;
-#pragma unroll
-        for (int fb = 0; fb < 2; ++fb)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(rowbase + fb * 16384 + sw128_off(r, j * 8));
-            const uint32_t *w = reinterpret_cast<const uint32_t *>(&u);
-            uint4 b;
-            uint32_t *bw = reinterpret_cast<uint32_t *>(&b);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = unpack_bf16(w[e]);
-              bw[e] = pack_bf16(f.x * sc, f.y * sc);
-            }
-            *reinterpret_cast<uint4 *>(sm + OFF_QT + fb * 8192 + sw128_off(r, j * 8)) = b;
-          }
+        alpha[r] = p.scale * bex[r] * inv;
       }
     }
     __syncthreads();
-    // ---- T (fp32, packed) -> bf16 hi/lo tiles of T and of T diag(b / |k|)
-    for (int idx = tid; idx < kTPacked; idx += NT) {
-      int i = (int)((sqrtf(8.f * (float)idx + 1.f) - 1.f) * 0.5f);
-      while ((i + 1) * (i + 2) / 2 <= idx) ++i;
-      while (i * (i + 1) / 2 > idx) --i;
-      const int j = idx - i * (i + 1) / 2;
-      const float t = tp[idx];
-      const float th = __bfloat162float(__float2bfloat16_rn(t));
-      const float t2 = t * bex[j] * kinv[j];
-      const float t2h = __bfloat162float(__float2bfloat16_rn(t2));
-      put_bf16(sm + OFF_TH, i, j, th);
-      put_bf16(sm + OFF_TL, i, j, t - th);
-      put_bf16(sm + OFF_TPH, i, j, t2h);
-      put_bf16(sm + OFF_TPL, i, j, t2 - t2h);
+    // ---- T (fp32, packed) -> bf16 hi/lo tiles of T and of T diag(b / |k|); thread = (row, 32 columns)
+    {
+      const int r = tid & 63, cb = (tid >> 6) * 32;
+      const float *trow = tp + r * (r + 1) / 2;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c0 = cb + q * 8;
+        uint32_t wh[4], wl[4], xh[4], xl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float t[2], t2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = c0 + 2 * e + u;
+            t[u] = (c <= r) ? trow[c] : 0.f;
+            t2[u] = t[u] * bex[c] * kinv[c];
+          }
+          const float h0 = __bfloat162float(__float2bfloat16_rn(t[0]));
+          const float h1 = __bfloat162float(__float2bfloat16_rn(t[1]));
+          const float g0 = __bfloat162float(__float2bfloat16_rn(t2[0]));
+          const float g1 = __bfloat162float(__float2bfloat16_rn(t2[1]));
+          wh[e] = pack_bf16(h0, h1);
+          wl[e] = pack_bf16(t[0] - h0, t[1] - h1);
+          xh[e] = pack_bf16(g0, g1);
+          xl[e] = pack_bf16(t2[0] - g0, t2[1] - g1);
+        }
+        const uint32_t off = sw128_off(r, c0);
+        *reinterpret_cast<uint4 *>(sm + OFF_TH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(sm + OFF_TL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        *reinterpret_cast<uint4 *>(sm + OFF_TPH + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+        *reinterpret_cast<uint4 *>(sm + OFF_TPL + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+      }
     }
     sync_smem_for_mma();
     // ---- state-independent MMAs: Q K^T, W = T diag(b/|k|) K (hi + lo), U = T V (hi + lo)
@@ -537,7 +560,7 @@ __global__ void __launch_bounds__(NT, 1)
     //      in fp32; -W -> bf16 tile
     float pdiag = 0.f;
     {
-      const float gr = gam[row], qr = p.scale * qinv[row];
+      const float gr2 = gl2[row], qr = p.scale * qinv[row];
 #pragma unroll
       for (int c0 = 0; c0 < C; c0 += 16) {
         float v[16];
@@ -548,8 +571,8 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int j0 = c0 + 2 * e, j1 = j0 + 1;
-            const float a = (j0 < mrow) ? qr * kinv[j0] * expf(gr - gam[j0]) * v[2 * e] : 0.f;
-            const float b = (j1 < mrow) ? qr * kinv[j1] * expf(gr - gam[j1]) * v[2 * e + 1] : 0.f;
+            const float a = (j0 < mrow) ? qr * kinv[j0] * exp2f(gr2 - gl2[j0]) * v[2 * e] : 0.f;
+            const float b = (j1 < mrow) ? qr * kinv[j1] * exp2f(gr2 - gl2[j1]) * v[2 * e + 1] : 0.f;
             if (j0 == mrow) pdiag = qr * kinv[j0] * v[2 * e];
             if (j1 == mrow) pdiag = qr * kinv[j1] * v[2 * e + 1];
             w[e] = pack_bf16(a, b);
@@ -574,7 +597,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
     sync_smem_for_mma();
-    // ---- state chain, round 1: U' = U - W S^T ; O = scale diag(b/|q|) Q S^T
+    // ---- state chain, round 1: U' = U - W S^T ; Q S^T (raw q; scale b / |q| applied per row later)
     if (tid == 0) {
       const uint32_t id = idesc_bf16(64, BVT, false, true);
 #pragma unroll
@@ -582,7 +605,8 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
         const uint64_t bs = smem_desc(sb + OFF_ST + ks * 1024, 2048, 512, 4);
         umma_bf16(tm + COL_U, smem_desc(sb + OFF_NW + off, 16, 1024, 2), bs, id, 1);
-        umma_bf16(tm + COL_O, smem_desc(sb + OFF_QT + off, 16, 1024, 2), bs, id, ks > 0);
+        const uint32_t qoff = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
+        umma_bf16(tm + COL_O, smem_desc(qk_a + qoff, 16, 1024, 2), bs, id, ks > 0);
       }
     }
     commit_mma();
@@ -628,8 +652,8 @@ __global__ void __launch_bounds__(NT, 1)
       for (int ks = 0; ks < C / 16; ++ks) {
         const uint64_t pa = smem_desc(sb + OFF_PT + ks * 32, 16, 1024, 2);
         const uint64_t ka = smem_desc(qk_a + ks * 2048, 16384, 1024, 2);
-        umma_bf16(tm + COL_O, pa, smem_desc(sb + OFF_UP + ks * 1024, 2048, 512, 4), id_o, 1);
-        umma_bf16(tm + COL_O, pa, smem_desc(sb + OFF_UPL + ks * 1024, 2048, 512, 4), id_o, 1);
+        umma_bf16(tm + COL_OB, pa, smem_desc(sb + OFF_UP + ks * 1024, 2048, 512, 4), id_o, ks > 0);
+        umma_bf16(tm + COL_OB, pa, smem_desc(sb + OFF_UPL + ks * 1024, 2048, 512, 4), id_o, 1);
         umma_bf16(tm + COL_S, ka, smem_desc(sb + OFF_DU + ks * 1024, 2048, 512, 4), id_s, ks > 0);
         umma_bf16(tm + COL_S, ka, smem_desc(sb + OFF_DUL + ks * 1024, 2048, 512, 4), id_s, 1);
       }
@@ -639,18 +663,20 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_after();
     {
       const float blast = bex[C - 1];
-      float ds[BVT], ov[BVT];
+      float ds[BVT], ov[BVT], ob[BVT];
       tmem_ld16(tl + COL_S, *reinterpret_cast<float(*)[16]>(ds));
       tmem_ld16(tl + COL_S + 16, *reinterpret_cast<float(*)[16]>(ds + 16));
       tmem_ld16(tl + COL_O, *reinterpret_cast<float(*)[16]>(ov));
       tmem_ld16(tl + COL_O + 16, *reinterpret_cast<float(*)[16]>(ov + 16));
+      tmem_ld16(tl + COL_OB, *reinterpret_cast<float(*)[16]>(ob));
+      tmem_ld16(tl + COL_OB + 16, *reinterpret_cast<float(*)[16]>(ob + 16));
       tmem_wait_ld();
 #pragma unroll
       for (int v = 0; v < BVT; ++v) S[v] = fmaf(blast, S[v], ds[v]);
       write_state_bf16();
       if (lane_row && mrow < n) {
 #pragma unroll
-        for (int v = 0; v < BVT; ++v) ov[v] = fmaf(pdiag, up[v], ov[v]);
+        for (int v = 0; v < BVT; ++v) ov[v] = fmaf(alpha[mrow], ov[v], fmaf(pdiag, up[v], ob[v]));
         const size_t off = (size_t)(t0 + mrow) * o_tok_stride + (size_t)h * p.V + v0;
         if (p.o_f32) {
           float4 *dst = reinterpret_cast<float4 *>((float *)p.o + off);
@@ -677,6 +703,540 @@ __global__ void __launch_bounds__(NT, 1)
     float *dst = p.hT + (((size_t)s * p.Hv + h) * p.V + v0) * KD + tid;
 #pragma unroll
     for (int v = 0; v < BVT; ++v) dst[(size_t)v * KD] = S[v];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, kTmemCols);
+}
+
+// ======================================== warp-specialised main kernel
+//
+// Two warpgroups per block (256 threads) overlap consecutive chunks:
+//  * WG0 (warps 0-3) prepares chunk c+1's state-independent operands: gates,
+//    1/|k| and 1/|q|, the bf16 hi/lo split of T and T diag(b/|k|), the MMAs
+//    Q K^T, W = T diag(b/|k|) K and U = T V, then the bf16 tiles P (strictly
+//    lower) and -W.  It hands them over through double-buffered shared memory
+//    and TMEM, signalling `full[b]`.
+//  * WG1 (warps 4-7) runs chunk c's state chain: U' = U - W S^T and Q S^T,
+//    the U' epilogue, P U' and K^T diag(d/|k|) U', then the fp32 state update
+//    and the output, signalling `empty[b]` when chunk c's buffers may be reused.
+// Raw k | q tiles sit in a 3-stage TMA ring (both groups read them); v tiles
+// in a 2-stage ring of WG0; T is prefetched from global into registers one
+// chunk ahead.
+
+constexpr int NT2 = 256;
+constexpr uint32_t W_KQ = 0;                 // 3 stages x 32 KB: [fb][rows 0-63 k | 64-127 q][128 B]
+constexpr uint32_t W_V = 98304;              // 2 x 4 KB: [64 tok][32 v] SW64
+constexpr uint32_t W_TH = 106496, W_TL = 114688, W_TPH = 122880, W_TPL = 131072;  // 4 x 8 KB, SW128
+constexpr uint32_t W_NW = 139264;            // 2 x 16 KB: -W [fb][64][128 B]
+constexpr uint32_t W_PT = 172032;            // 2 x 8 KB: P (strictly lower) [64][128 B]
+constexpr uint32_t W_ST = 188416;            // 8 KB: S^T bf16 [128 feat][32 v] SW64
+constexpr uint32_t W_UP = 196608, W_DU = 200704, W_UPL = 204800, W_DUL = 208896;  // 4 x 4 KB, SW64
+constexpr uint32_t kWsSmem = 212992 + 1024;
+constexpr uint32_t WC_QK = 0, WC_W = 64, WC_U = 192, WC_OA = 256, WC_OB = 288, WC_S = 320;
+
+struct WsShared {
+  uint64_t kq_full[3], v_full[2], pre_done, chain_done, out_done, full[2], empty[2];
+  uint32_t tbase;
+  int abort;
+  int kq_issued[3], kq_seen[3], v_issued[2], v_seen[2];
+  int pre_inflight, chain_inflight, out_inflight;
+  uint32_t ph_pre, ph_chain, ph_out;
+  float gam[C], gl2[C], bex[C], dec[C], kinv[C], qinv[C];  // WG0 working set
+  float dk[2][C], alpha[2][C], pdiag[2][C], blast[2];      // handed to WG1 per buffer
+  int nvalid[2];
+};
+
+__global__ void __launch_bounds__(NT2, 1)
+    chunk_ws_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  __shared__ WsShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wg = tid >> 7, wt = tid & 127, quarter = warp & 3;
+  const int v0 = blockIdx.x * BVT, h = blockIdx.y, s = blockIdx.z;
+  const int qh = h / (p.Hv / p.Hqk);
+  int64_t start, end;
+  seq_range(p.cu, p.row_T, s, start, end);
+  if (start < 0 || end < start || end > p.n_tok) {
+    if (tid == 0) set_status(p.status, GDN_ERR_BOUNDS);
+    return;
+  }
+  const int n_chunks = (int)((end - start + C - 1) / C);
+  const int64_t sbase = (int64_t)s + start / C;
+  const uint32_t sb = smem_u32(sm);
+  volatile int *abort_flag = &sh.abort;
+
+  auto issue_kq = [&](int ci, int st) {  // raw k and q tiles of chunk ci into ring stage st
+    const int32_t t0 = (int32_t)(start + (int64_t)ci * C);
+    uint8_t *qk = sm + W_KQ + st * 32768;
+    mbar_arrive_expect_tx(&sh.kq_full[st], 4 * 8192);
+    tma_load_3d(qk, &tm_k, &sh.kq_full[st], 0, qh, t0);
+    tma_load_3d(qk + 16384, &tm_k, &sh.kq_full[st], 64, qh, t0);
+    tma_load_3d(qk + 8192, &tm_q, &sh.kq_full[st], 0, qh, t0);
+    tma_load_3d(qk + 16384 + 8192, &tm_q, &sh.kq_full[st], 64, qh, t0);
+    sh.kq_issued[st] += 1;
+  };
+  auto issue_v = [&](int ci, int vb) {
+    const int32_t t0 = (int32_t)(start + (int64_t)ci * C);
+    mbar_arrive_expect_tx(&sh.v_full[vb], 4096);
+    tma_load_3d(sm + W_V + vb * 4096, &tm_v, &sh.v_full[vb], v0, h, t0);
+    sh.v_issued[vb] += 1;
+  };
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, GDN_ERR_TIMEOUT);
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&sh.kq_full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 1);
+      sh.v_issued[i] = sh.v_seen[i] = 0;
+    }
+    mbar_init(&sh.pre_done, 1);
+    mbar_init(&sh.chain_done, 1);
+    mbar_init(&sh.out_done, 1);
+    for (int i = 0; i < 3; ++i) sh.kq_issued[i] = sh.kq_seen[i] = 0;
+    sh.abort = 0;
+    sh.pre_inflight = sh.chain_inflight = sh.out_inflight = 0;
+    sh.ph_pre = sh.ph_chain = sh.ph_out = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    for (int ci = 0; ci < 3 && ci < n_chunks; ++ci) issue_kq(ci, ci);
+    if (n_chunks > 0) issue_v(0, 0);
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh.tbase, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = sh.tbase;
+  const uint32_t tl = tm + ((uint32_t)(quarter * 32) << 16);  // this warp's lane quarter
+  const bool lane_row = lane < 16;                             // M = 64 rows: lanes 0-15 of a quarter
+  const int mrow = quarter * 16 + lane;
+
+  if (wg == 0) {
+    // ===================================================== WG0: operands
+    float gnext = 0.f;
+    if (n_chunks > 0 && wt < C && start + wt < end) gnext = p.g[(start + wt) * p.Hv + h];
+    const int tr = wt & 63, tcb = (wt >> 6) * 32;  // T row and 32-column half of this thread
+    float tpre[32];
+    auto load_T = [&](int ci) {
+      const float *trow = p.T + ((size_t)(sbase + ci) * p.Hv + h) * kTPacked + tr * (tr + 1) / 2;
+#pragma unroll
+      for (int u = 0; u < 32; ++u) tpre[u] = (tcb + u <= tr) ? trow[tcb + u] : 0.f;
+    };
+    if (n_chunks > 0) load_T(0);
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int b = ci & 1, st = ci % 3;
+      const int64_t t0 = start + (int64_t)ci * C;
+      const int n = (int)min((int64_t)C, end - t0);
+      const uint32_t qk_a = sb + W_KQ + st * 32768;
+      const uint8_t *qk = sm + W_KQ + st * 32768;
+      // chunk ci-2's buffers (same parity) must be released by WG1
+      {
+        const bool ok = ci < 2 || mbar_wait_abortable(&sh.empty[b], ((ci - 2) >> 1) & 1, kSpin, abort_flag);
+        if (named_bar_any(1, 128, !ok)) {
+          if (wt == 0) fail();
+          break;
+        }
+      }
+      if (wt == 0 && ci + 1 < n_chunks) issue_v(ci + 1, (ci + 1) & 1);
+      // ---- gates
+      if (wt < C) sh.gam[wt] = gnext;
+      if (ci + 1 < n_chunks && wt < C) {
+        const int64_t t1 = t0 + C;
+        gnext = (t1 + wt < end) ? p.g[(t1 + wt) * p.Hv + h] : 0.f;
+      }
+      named_bar_sync(1, 128);
+      if (warp == 0) {
+        const float g0 = sh.gam[2 * lane], g1 = sh.gam[2 * lane + 1];
+        float incl = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        const float last = __shfl_sync(0xffffffffu, incl, 31);
+        const float ga = incl - g1, gb = incl;
+        sh.gam[2 * lane] = ga;
+        sh.gam[2 * lane + 1] = gb;
+        sh.gl2[2 * lane] = ga * 1.4426950408889634f;
+        sh.gl2[2 * lane + 1] = gb * 1.4426950408889634f;
+        sh.bex[2 * lane] = expf(ga);
+        sh.bex[2 * lane + 1] = expf(gb);
+        sh.dec[2 * lane] = expf(last - ga);
+        sh.dec[2 * lane + 1] = expf(last - gb);
+        if (lane == 31) sh.blast[b] = expf(last);
+      }
+      // ---- this chunk's k | q and v tiles
+      {
+        bool ok = mbar_wait_abortable(&sh.kq_full[st], (ci / 3) & 1, kSpin, abort_flag);
+        ok = ok && mbar_wait_abortable(&sh.v_full[b], (ci >> 1) & 1, kSpin, abort_flag);
+        if (named_bar_any(1, 128, !ok)) {
+          if (wt == 0) fail();
+          break;
+        }
+        if (wt == 0) {
+          sh.kq_seen[st] += 1;
+          sh.v_seen[b] += 1;
+        }
+      }
+      named_bar_sync(1, 128);
+      // ---- 1/|k|, 1/|q|; alpha = scale b / |q|
+      {
+        const int r = wt & 63;
+        const bool isq = wt >= 64;
+        const uint8_t *rowbase = qk + (isq ? 8192 : 0);
+        float ss = 0.f;
+#pragma unroll
+        for (int fb = 0; fb < 2; ++fb)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(rowbase + fb * 16384 + sw128_off(r, j * 8));
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = unpack_bf16(w[e]);
+              ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+            }
+          }
+        const float inv = p.l2norm ? 1.f / sqrtf(ss + kL2Eps) : 1.f;
+        if (!isq) {
+          sh.kinv[r] = inv;
+        } else {
+          sh.qinv[r] = inv;
+          sh.alpha[b][r] = p.scale * sh.bex[r] * inv;
+        }
+      }
+      named_bar_sync(1, 128);
+      if (wt < C) sh.dk[b][wt] = sh.dec[wt] * sh.kinv[wt];
+      // ---- T and T diag(b/|k|) as bf16 hi/lo tiles (row tr, columns tcb..tcb+31)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c0 = tcb + q * 8;
+        uint32_t wh[4], wl[4], xh[4], xl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c0 + 2 * e;
+          const float t_0 = tpre[q * 8 + 2 * e], t_1 = tpre[q * 8 + 2 * e + 1];
+          const float u_0 = t_0 * sh.bex[c] * sh.kinv[c], u_1 = t_1 * sh.bex[c + 1] * sh.kinv[c + 1];
+          const float h0 = __bfloat162float(__float2bfloat16_rn(t_0));
+          const float h1 = __bfloat162float(__float2bfloat16_rn(t_1));
+          const float g0 = __bfloat162float(__float2bfloat16_rn(u_0));
+          const float g1 = __bfloat162float(__float2bfloat16_rn(u_1));
+          wh[e] = pack_bf16(h0, h1);
+          wl[e] = pack_bf16(t_0 - h0, t_1 - h1);
+          xh[e] = pack_bf16(g0, g1);
+          xl[e] = pack_bf16(u_0 - g0, u_1 - g1);
+        }
+        const uint32_t off = sw128_off(tr, c0);
+        *reinterpret_cast<uint4 *>(sm + W_TH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4 *>(sm + W_TL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        *reinterpret_cast<uint4 *>(sm + W_TPH + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+        *reinterpret_cast<uint4 *>(sm + W_TPL + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+      }
+      if (ci + 1 < n_chunks) load_T(ci + 1);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      tc_fence_after();
+      // ---- Q K^T, W = T diag(b/|k|) K, U = T V (hi + lo)
+      if (wt == 0) {
+        const uint32_t id_qk = idesc_bf16(64, 64, false, false);
+#pragma unroll
+        for (int ks = 0; ks < KD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          umma_bf16(tm + WC_QK, smem_desc(qk_a + 8192 + off, 16, 1024, 2),
+                    smem_desc(qk_a + off, 16, 1024, 2), id_qk, ks > 0);
+        }
+        const uint32_t id_w = idesc_bf16(64, 128, false, true);
+        const uint32_t id_u = idesc_bf16(64, BVT, false, true);
+        const uint32_t v_a = sb + W_V + b * 4096;
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t kb = smem_desc(qk_a + ks * 2048, 16384, 1024, 2);
+          const uint64_t vb = smem_desc(v_a + ks * 1024, 2048, 512, 4);
+          umma_bf16(tm + WC_W, smem_desc(sb + W_TPH + ks * 32, 16, 1024, 2), kb, id_w, ks > 0);
+          umma_bf16(tm + WC_W, smem_desc(sb + W_TPL + ks * 32, 16, 1024, 2), kb, id_w, 1);
+          umma_bf16(tm + WC_U + b * BVT, smem_desc(sb + W_TH + ks * 32, 16, 1024, 2), vb, id_u, ks > 0);
+          umma_bf16(tm + WC_U + b * BVT, smem_desc(sb + W_TL + ks * 32, 16, 1024, 2), vb, id_u, 1);
+        }
+        umma_commit(&sh.pre_done);
+        sh.pre_inflight = 1;
+      }
+      {
+        const bool ok = mbar_wait_abortable(&sh.pre_done, ci & 1, kSpin, abort_flag);
+        if (named_bar_any(1, 128, !ok)) {
+          if (wt == 0) fail();
+          break;
+        }
+      }
+      if (wt == 0) {
+        sh.pre_inflight = 0;
+        sh.ph_pre = (ci + 1) & 1;
+      }
+      tc_fence_after();
+      // ---- P (strictly lower, bf16) with its diagonal kept in fp32; -W (bf16)
+      {
+        const int row = mrow & 63;
+        const float gr2 = sh.gl2[row], qr = p.scale * sh.qinv[row];
+        uint8_t *pt = sm + W_PT + b * 8192;
+        float v[64];
+#pragma unroll
+        for (int c0 = 0; c0 < C; c0 += 16) tmem_ld16(tl + WC_QK + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+        tmem_wait_ld();
+        if (lane_row) {
+#pragma unroll
+          for (int c0 = 0; c0 < C; c0 += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j0 = c0 + 2 * e, j1 = j0 + 1;
+              const float a = (j0 < mrow) ? qr * sh.kinv[j0] * exp2f(gr2 - sh.gl2[j0]) * v[j0] : 0.f;
+              const float bb = (j1 < mrow) ? qr * sh.kinv[j1] * exp2f(gr2 - sh.gl2[j1]) * v[j1] : 0.f;
+              w[e] = pack_bf16(a, bb);
+            }
+            *reinterpret_cast<uint4 *>(pt + sw128_off(mrow, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          float vd = 0.f;
+#pragma unroll
+          for (int j = 0; j < C; ++j) vd = (j == mrow) ? v[j] : vd;
+          sh.pdiag[b][mrow] = qr * sh.kinv[mrow] * vd;
+        }
+        uint8_t *nw = sm + W_NW + b * 16384;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 16)
+            tmem_ld16(tl + WC_W + half * 64 + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+          tmem_wait_ld();
+          if (lane_row) {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) w[e] = pack_bf16(-v[c0 + 2 * e], -v[c0 + 2 * e + 1]);
+              *reinterpret_cast<uint4 *>(nw + half * 8192 + sw128_off(mrow, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      if (wt == 0) sh.nvalid[b] = n;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (wt == 0) mbar_arrive(&sh.full[b]);
+    }
+  } else {
+    // ===================================================== WG1: state chain
+    float S[BVT];
+    {
+      const float *h0p = p.h0 ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0) * KD + wt : nullptr;
+#pragma unroll
+      for (int v = 0; v < BVT; ++v) S[v] = h0p ? h0p[(size_t)v * KD] : 0.f;
+    }
+    auto write_state_bf16 = [&]() {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 o = make_uint4(pack_bf16(S[q * 8 + 0], S[q * 8 + 1]), pack_bf16(S[q * 8 + 2], S[q * 8 + 3]),
+                             pack_bf16(S[q * 8 + 4], S[q * 8 + 5]), pack_bf16(S[q * 8 + 6], S[q * 8 + 7]));
+        *reinterpret_cast<uint4 *>(sm + W_ST + sw64_off(wt, q * 8)) = o;
+      }
+    };
+    write_state_bf16();
+    fence_proxy_async_smem();
+    named_bar_sync(2, 128);
+    const size_t o_tok_stride = (size_t)p.Hv * p.V;
+    uint32_t ph_chain = 0;
+    bool ok_all = true;
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int b = ci & 1, st = ci % 3;
+      const int64_t t0 = start + (int64_t)ci * C;
+      const uint32_t qk_a = sb + W_KQ + st * 32768;
+      {
+        const bool ok = mbar_wait_abortable(&sh.full[b], (ci >> 1) & 1, kSpin, abort_flag);
+        if (named_bar_any(2, 128, !ok)) {
+          if (wt == 0) fail();
+          ok_all = false;
+          break;
+        }
+      }
+      tc_fence_after();
+      // ---- round 1: U' = U - W S^T ; Q S^T
+      if (wt == 0) {
+        const uint32_t id = idesc_bf16(64, BVT, false, true);
+#pragma unroll
+        for (int ks = 0; ks < KD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
+          umma_bf16(tm + WC_U + b * BVT, smem_desc(sb + W_NW + b * 16384 + off, 16, 1024, 2),
+                    smem_desc(sb + W_ST + ks * 1024, 2048, 512, 4), id, 1);
+        }
+        umma_commit(&sh.chain_done);  // the state path waits for U' only
+        sh.chain_inflight = 1;
+#pragma unroll
+        for (int ks = 0; ks < KD / 16; ++ks) {
+          const uint32_t qoff = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
+          umma_bf16(tm + WC_OA, smem_desc(qk_a + qoff, 16, 1024, 2),
+                    smem_desc(sb + W_ST + ks * 1024, 2048, 512, 4), id, ks > 0);
+        }
+      }
+      {
+        const bool ok = mbar_wait_abortable(&sh.chain_done, ph_chain, kSpin, abort_flag);
+        if (named_bar_any(2, 128, !ok)) {
+          if (wt == 0) fail();
+          ok_all = false;
+          break;
+        }
+      }
+      ph_chain ^= 1u;
+      tc_fence_after();
+      float up[BVT];
+      tmem_ld16(tl + WC_U + b * BVT, *reinterpret_cast<float(*)[16]>(up));
+      tmem_ld16(tl + WC_U + b * BVT + 16, *reinterpret_cast<float(*)[16]>(up + 16));
+      tmem_wait_ld();
+      if (lane_row) {
+        const float dr = sh.dk[b][mrow];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c0 = q * 8;
+          uint32_t uh[4], ul[4], dh[4], dl[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = up[c0 + 2 * e], bb = up[c0 + 2 * e + 1];
+            const float ah = __bfloat162float(__float2bfloat16_rn(a));
+            const float bh = __bfloat162float(__float2bfloat16_rn(bb));
+            uh[e] = pack_bf16(ah, bh);
+            ul[e] = pack_bf16(a - ah, bb - bh);
+            const float da = dr * a, db = dr * bb;
+            const float dah = __bfloat162float(__float2bfloat16_rn(da));
+            const float dbh = __bfloat162float(__float2bfloat16_rn(db));
+            dh[e] = pack_bf16(dah, dbh);
+            dl[e] = pack_bf16(da - dah, db - dbh);
+          }
+          const uint32_t off = sw64_off(mrow, c0);
+          *reinterpret_cast<uint4 *>(sm + W_UP + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+          *reinterpret_cast<uint4 *>(sm + W_UPL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
+          *reinterpret_cast<uint4 *>(sm + W_DU + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
+          *reinterpret_cast<uint4 *>(sm + W_DUL + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(2, 128);
+      tc_fence_after();
+      // ---- round 2: P U' (hi + lo) ; dS^T = K^T diag(d/|k|) U' (hi + lo)
+      if (wt == 0) {
+        const uint32_t id_o = idesc_bf16(64, BVT, false, true);
+        const uint32_t id_s = idesc_bf16(128, BVT, true, true);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t ka = smem_desc(qk_a + ks * 2048, 16384, 1024, 2);
+          umma_bf16(tm + WC_S, ka, smem_desc(sb + W_DU + ks * 1024, 2048, 512, 4), id_s, ks > 0);
+          umma_bf16(tm + WC_S, ka, smem_desc(sb + W_DUL + ks * 1024, 2048, 512, 4), id_s, 1);
+        }
+        umma_commit(&sh.chain_done);  // the state update waits for dS^T only
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t pa = smem_desc(sb + W_PT + b * 8192 + ks * 32, 16, 1024, 2);
+          umma_bf16(tm + WC_OB, pa, smem_desc(sb + W_UP + ks * 1024, 2048, 512, 4), id_o, ks > 0);
+          umma_bf16(tm + WC_OB, pa, smem_desc(sb + W_UPL + ks * 1024, 2048, 512, 4), id_o, 1);
+        }
+        umma_commit(&sh.out_done);  // Q S^T and P U' of this chunk
+        sh.out_inflight = 1;
+      }
+      {
+        const bool ok = mbar_wait_abortable(&sh.chain_done, ph_chain, kSpin, abort_flag);
+        if (named_bar_any(2, 128, !ok)) {
+          if (wt == 0) fail();
+          ok_all = false;
+          break;
+        }
+      }
+      ph_chain ^= 1u;
+      if (wt == 0) sh.chain_inflight = 0;
+      tc_fence_after();
+      {
+        const float blast = sh.blast[b];
+        float ds[BVT];
+        tmem_ld16(tl + WC_S, *reinterpret_cast<float(*)[16]>(ds));
+        tmem_ld16(tl + WC_S + 16, *reinterpret_cast<float(*)[16]>(ds + 16));
+        tmem_wait_ld();
+#pragma unroll
+        for (int v = 0; v < BVT; ++v) S[v] = fmaf(blast, S[v], ds[v]);
+        write_state_bf16();
+      }
+      {
+        const bool ok = mbar_wait_abortable(&sh.out_done, sh.ph_out, kSpin, abort_flag);
+        if (named_bar_any(2, 128, !ok)) {
+          if (wt == 0) fail();
+          ok_all = false;
+          break;
+        }
+        if (wt == 0) {
+          sh.ph_out ^= 1u;
+          sh.out_inflight = 0;
+        }
+      }
+      tc_fence_after();
+      {
+        float oa[BVT], ob[BVT];
+        tmem_ld16(tl + WC_OA, *reinterpret_cast<float(*)[16]>(oa));
+        tmem_ld16(tl + WC_OA + 16, *reinterpret_cast<float(*)[16]>(oa + 16));
+        tmem_ld16(tl + WC_OB, *reinterpret_cast<float(*)[16]>(ob));
+        tmem_ld16(tl + WC_OB + 16, *reinterpret_cast<float(*)[16]>(ob + 16));
+        tmem_wait_ld();
+        if (lane_row && mrow < sh.nvalid[b]) {
+          const float al = sh.alpha[b][mrow], pd = sh.pdiag[b][mrow];
+#pragma unroll
+          for (int v = 0; v < BVT; ++v) oa[v] = fmaf(al, oa[v], fmaf(pd, up[v], ob[v]));
+          const size_t off = (size_t)(t0 + mrow) * o_tok_stride + (size_t)h * p.V + v0;
+          if (p.o_f32) {
+            float4 *dst = reinterpret_cast<float4 *>((float *)p.o + off);
+#pragma unroll
+            for (int q = 0; q < BVT / 4; ++q) dst[q] = make_float4(oa[4 * q], oa[4 * q + 1], oa[4 * q + 2], oa[4 * q + 3]);
+          } else {
+            uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)p.o + off);
+#pragma unroll
+            for (int q = 0; q < BVT / 8; ++q)
+              dst[q] = make_uint4(pack_bf16(oa[8 * q], oa[8 * q + 1]), pack_bf16(oa[8 * q + 2], oa[8 * q + 3]),
+                                  pack_bf16(oa[8 * q + 4], oa[8 * q + 5]), pack_bf16(oa[8 * q + 6], oa[8 * q + 7]));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(2, 128);
+      if (wt == 0) {
+        mbar_arrive(&sh.empty[b]);
+        if (ci + 3 < n_chunks) issue_kq(ci + 3, st);
+      }
+    }
+    if (ok_all && p.hT) {
+      float *dst = p.hT + (((size_t)s * p.Hv + h) * p.V + v0) * KD + wt;
+#pragma unroll
+      for (int v = 0; v < BVT; ++v) dst[(size_t)v * KD] = S[v];
+    }
+    if (wt == 0) sh.ph_chain = ph_chain;
+  }
+  __syncthreads();
+  if (tid == 0 && sh.abort) {
+    // let copies and MMAs still in flight land before shared memory and TMEM are released
+    for (int i = 0; i < 3; ++i)
+      if (sh.kq_issued[i] > sh.kq_seen[i]) (void)mbar_wait(&sh.kq_full[i], sh.kq_seen[i] & 1, kSpin);
+    for (int i = 0; i < 2; ++i)
+      if (sh.v_issued[i] > sh.v_seen[i]) (void)mbar_wait(&sh.v_full[i], sh.v_seen[i] & 1, kSpin);
+    if (sh.pre_inflight) (void)mbar_wait(&sh.pre_done, sh.ph_pre, kSpin);
+    if (sh.chain_inflight) (void)mbar_wait(&sh.chain_done, sh.ph_chain, kSpin);
+    if (sh.out_inflight) (void)mbar_wait(&sh.out_done, sh.ph_out, kSpin);
   }
   tc_fence_before();
   __syncthreads();
@@ -784,10 +1344,10 @@ gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float
   tp.o_f32 = (flags & GDN_FLAG_O_F32) ? 1 : 0;
   tp.hT = h_T;
   tp.status = status;
-  if (cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kTcSmem) != cudaSuccess)
+  if (cudaFuncSetAttribute(chunk_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kWsSmem) != cudaSuccess)
     return GDN_ERR_CUDA;
-  chunk_tc_kernel<<<dim3(sh.V / BVT, sh.Hv, sh.n_seqs), NT, kTcSmem, st>>>(mq, mk, mv, tp);
+  chunk_ws_kernel<<<dim3(sh.V / BVT, sh.Hv, sh.n_seqs), NT2, kWsSmem, st>>>(mq, mk, mv, tp);
   return launch_status();
 }
 

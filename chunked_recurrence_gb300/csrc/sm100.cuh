@@ -62,6 +62,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   return false;
 }
 
+// Like mbar_wait, but also gives up as soon as *abort (set by another warp
+// that hit a failure) becomes non-zero.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t parity, uint32_t max_iters,
+                                                    volatile int *abort) {
+  for (uint32_t i = 0; i < max_iters; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (i > 64) __nanosleep(32);
+  }
+  return false;
+}
+
+// Barrier among `count` threads (a multiple of 32) using hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Barrier among `count` threads on hardware barrier `id` that also ORs `pred`
+// across them: every participant gets the same answer.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
