@@ -295,6 +295,9 @@ struct TcParams {
   int o_f32;
   float *hT;
   int32_t *status;
+  // segment-summary mode: state columns [0, K) are M (start I, v = 0), [K, K + V) S_local
+  int summary;
+  float *M, *S_local;
 };
 
 // dynamic shared memory map (offsets from a 1024-aligned base)
@@ -767,6 +770,11 @@ __global__ void __launch_bounds__(NT2, 1)
   const int64_t sbase = (int64_t)s + start / C;
   const uint32_t sb = smem_u32(sm);
   volatile int *abort_flag = &sh.abort;
+  // summary mode: M's columns see v = 0 (their v tiles stay zero and are never loaded);
+  // S_local's columns read v at column v0 - K
+  const bool m_cols = p.summary && v0 < KD;
+  const bool load_v = !m_cols;
+  const int vcol = p.summary ? v0 - KD : v0;
 
   auto issue_kq = [&](int ci, int st) {  // raw k and q tiles of chunk ci into ring stage st
     const int32_t t0 = (int32_t)(start + (int64_t)ci * C);
@@ -781,7 +789,7 @@ __global__ void __launch_bounds__(NT2, 1)
   auto issue_v = [&](int ci, int vb) {
     const int32_t t0 = (int32_t)(start + (int64_t)ci * C);
     mbar_arrive_expect_tx(&sh.v_full[vb], 4096);
-    tma_load_3d(sm + W_V + vb * 4096, &tm_v, &sh.v_full[vb], v0, h, t0);
+    tma_load_3d(sm + W_V + vb * 4096, &tm_v, &sh.v_full[vb], vcol, h, t0);
     sh.v_issued[vb] += 1;
   };
   auto fail = [&]() {
@@ -809,8 +817,10 @@ __global__ void __launch_bounds__(NT2, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     for (int ci = 0; ci < 3 && ci < n_chunks; ++ci) issue_kq(ci, ci);
-    if (n_chunks > 0) issue_v(0, 0);
+    if (n_chunks > 0 && load_v) issue_v(0, 0);
   }
+  if (m_cols)  // v = 0 for M's columns: both v buffers stay zero
+    for (int i = tid; i < 2 * 4096 / 16; i += NT2) reinterpret_cast<uint4 *>(sm + W_V)[i] = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     tmem_alloc(&sh.tbase, kTmemCols);
     tmem_relinquish();
@@ -849,7 +859,7 @@ __global__ void __launch_bounds__(NT2, 1)
           break;
         }
       }
-      if (wt == 0 && ci + 1 < n_chunks) issue_v(ci + 1, (ci + 1) & 1);
+      if (wt == 0 && ci + 1 < n_chunks && load_v) issue_v(ci + 1, (ci + 1) & 1);
       // ---- gates
       if (wt < C) sh.gam[wt] = gnext;
       if (ci + 1 < n_chunks && wt < C) {
@@ -880,14 +890,14 @@ __global__ void __launch_bounds__(NT2, 1)
       // ---- this chunk's k | q and v tiles
       {
         bool ok = mbar_wait_abortable(&sh.kq_full[st], (ci / 3) & 1, kSpin, abort_flag);
-        ok = ok && mbar_wait_abortable(&sh.v_full[b], (ci >> 1) & 1, kSpin, abort_flag);
+        if (load_v) ok = ok && mbar_wait_abortable(&sh.v_full[b], (ci >> 1) & 1, kSpin, abort_flag);
         if (named_bar_any(1, 128, !ok)) {
           if (wt == 0) fail();
           break;
         }
         if (wt == 0) {
           sh.kq_seen[st] += 1;
-          sh.v_seen[b] += 1;
+          if (load_v) sh.v_seen[b] += 1;
         }
       }
       named_bar_sync(1, 128);
@@ -1039,8 +1049,11 @@ __global__ void __launch_bounds__(NT2, 1)
   } else {
     // ===================================================== WG1: state chain
     float S[BVT];
-    {
-      const float *h0p = p.h0 ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0) * KD + wt : nullptr;
+    if (m_cols) {  // M starts at the identity: S[v0 + v][f] = (v0 + v == f)
+#pragma unroll
+      for (int v = 0; v < BVT; ++v) S[v] = (v0 + v == wt) ? 1.f : 0.f;
+    } else {
+      const float *h0p = (p.h0 && !p.summary) ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0) * KD + wt : nullptr;
 #pragma unroll
       for (int v = 0; v < BVT; ++v) S[v] = h0p ? h0p[(size_t)v * KD] : 0.f;
     }
@@ -1083,7 +1096,7 @@ __global__ void __launch_bounds__(NT2, 1)
         umma_commit(&sh.chain_done);  // the state path waits for U' only
         sh.chain_inflight = 1;
 #pragma unroll
-        for (int ks = 0; ks < KD / 16; ++ks) {
+        for (int ks = 0; ks < (p.summary ? 0 : KD / 16); ++ks) {
           const uint32_t qoff = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
           umma_bf16(tm + WC_OA, smem_desc(qk_a + qoff, 16, 1024, 2),
                     smem_desc(sb + W_ST + ks * 1024, 2048, 512, 4), id, ks > 0);
@@ -1145,13 +1158,15 @@ __global__ void __launch_bounds__(NT2, 1)
         }
         umma_commit(&sh.chain_done);  // the state update waits for dS^T only
 #pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks) {
+        for (int ks = 0; ks < (p.summary ? 0 : C / 16); ++ks) {
           const uint64_t pa = smem_desc(sb + W_PT + b * 8192 + ks * 32, 16, 1024, 2);
           umma_bf16(tm + WC_OB, pa, smem_desc(sb + W_UP + ks * 1024, 2048, 512, 4), id_o, ks > 0);
           umma_bf16(tm + WC_OB, pa, smem_desc(sb + W_UPL + ks * 1024, 2048, 512, 4), id_o, 1);
         }
-        umma_commit(&sh.out_done);  // Q S^T and P U' of this chunk
-        sh.out_inflight = 1;
+        if (!p.summary) {
+          umma_commit(&sh.out_done);  // Q S^T and P U' of this chunk
+          sh.out_inflight = 1;
+        }
       }
       {
         const bool ok = mbar_wait_abortable(&sh.chain_done, ph_chain, kSpin, abort_flag);
@@ -1174,7 +1189,7 @@ __global__ void __launch_bounds__(NT2, 1)
         for (int v = 0; v < BVT; ++v) S[v] = fmaf(blast, S[v], ds[v]);
         write_state_bf16();
       }
-      {
+      if (!p.summary) {
         const bool ok = mbar_wait_abortable(&sh.out_done, sh.ph_out, kSpin, abort_flag);
         if (named_bar_any(2, 128, !ok)) {
           if (wt == 0) fail();
@@ -1194,7 +1209,7 @@ __global__ void __launch_bounds__(NT2, 1)
         tmem_ld16(tl + WC_OB, *reinterpret_cast<float(*)[16]>(ob));
         tmem_ld16(tl + WC_OB + 16, *reinterpret_cast<float(*)[16]>(ob + 16));
         tmem_wait_ld();
-        if (lane_row && mrow < sh.nvalid[b]) {
+        if (!p.summary && lane_row && mrow < sh.nvalid[b]) {
           const float al = sh.alpha[b][mrow], pd = sh.pdiag[b][mrow];
 #pragma unroll
           for (int v = 0; v < BVT; ++v) oa[v] = fmaf(al, oa[v], fmaf(pd, up[v], ob[v]));
@@ -1220,7 +1235,12 @@ __global__ void __launch_bounds__(NT2, 1)
         if (ci + 3 < n_chunks) issue_kq(ci + 3, st);
       }
     }
-    if (ok_all && p.hT) {
+    if (ok_all && p.summary) {
+      float *dst = m_cols ? p.M + (((size_t)s * p.Hv + h) * KD + v0) * KD + wt
+                          : p.S_local + (((size_t)s * p.Hv + h) * p.V + vcol) * KD + wt;
+#pragma unroll
+      for (int v = 0; v < BVT; ++v) dst[(size_t)v * KD] = S[v];
+    } else if (ok_all && p.hT) {
       float *dst = p.hT + (((size_t)s * p.Hv + h) * p.V + v0) * KD + wt;
 #pragma unroll
       for (int v = 0; v < BVT; ++v) dst[(size_t)v * KD] = S[v];
@@ -1290,43 +1310,43 @@ size_t chunk_tc_workspace_bytes(const gdn_shape &sh, int64_t n_tok) {
   return kWsHeader + n_slots(n_tok, sh.n_seqs) * (size_t)sh.Hv * kTBytes;
 }
 
-gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float *g,
-                        const float *beta, const float *h0, const int32_t *cu,
-                        const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
-                        void *workspace, size_t ws_bytes, cudaStream_t st) {
-  const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
-  if (ws_bytes < chunk_tc_workspace_bytes(sh, n_tok)) return GDN_ERR_WORKSPACE;
+// Both kernels of the tensor-core path: the prep kernel (T for every chunk and
+// v-head into the workspace), then the warp-specialised chunk kernel over
+// (state-column tiles, v-heads, sequences).
+static gdn_status run_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  const float *h0, const int32_t *cu, int n_seqs, int64_t n_tok, const gdn_shape &sh,
+                  float scale, uint32_t flags, void *o, float *h_T, bool summary, float *M,
+                  float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st) {
+  const size_t slots = n_slots(n_tok, n_seqs);
+  if (ws_bytes < kWsHeader + slots * (size_t)sh.Hv * kTBytes) return GDN_ERR_WORKSPACE;
+  if (slots > 2147483647ULL) return GDN_ERR_UNSUPPORTED;
   int32_t *status = (int32_t *)workspace;
   float *Tws = (float *)((uint8_t *)workspace + kWsHeader);
-  const size_t slots = n_slots(n_tok, sh.n_seqs);
   const int l2 = (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0;
-  if (n_tok > 0) {
-    PrepParams pp{};
-    pp.k = (const __nv_bfloat16 *)k;
-    pp.ks = sh.k_stride;
-    pp.g = g;
-    pp.beta = beta;
-    pp.cu = cu;
-    pp.row_T = sh.T;
-    pp.n_tok = n_tok;
-    pp.n_seqs = sh.n_seqs;
-    pp.Hqk = sh.Hqk;
-    pp.Hv = sh.Hv;
-    pp.l2norm = l2;
-    pp.T = Tws;
-    pp.status = status;
-    if (cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPrepSmem) != cudaSuccess)
-      return GDN_ERR_CUDA;
-    if (slots > 2147483647ULL) return GDN_ERR_UNSUPPORTED;
-    chunk_prep_kernel<<<dim3((unsigned)slots, sh.Hqk), NT, kPrepSmem, st>>>(pp);
-    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-  }
+  PrepParams pp{};
+  pp.k = (const __nv_bfloat16 *)k;
+  pp.ks = sh.k_stride;
+  pp.g = g;
+  pp.beta = beta;
+  pp.cu = cu;
+  pp.row_T = sh.T;
+  pp.n_tok = n_tok;
+  pp.n_seqs = n_seqs;
+  pp.Hqk = sh.Hqk;
+  pp.Hv = sh.Hv;
+  pp.l2norm = l2;
+  pp.T = Tws;
+  pp.status = status;
+  if (cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kPrepSmem) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  chunk_prep_kernel<<<dim3((unsigned)slots, sh.Hqk), NT, kPrepSmem, st>>>(pp);
+  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   CUtensorMap mq, mk, mv;
-  const int64_t map_tok = n_tok > 0 ? n_tok : 1;
-  if (!make_map3(&mq, q ? q : k, KD, sh.Hqk, map_tok, sh.q_stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map3(&mk, k, KD, sh.Hqk, map_tok, sh.k_stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map3(&mv, v, sh.V, sh.Hv, map_tok, sh.v_stride, BVT, CU_TENSOR_MAP_SWIZZLE_64B))
+  if (!make_map3(&mq, q, KD, sh.Hqk, n_tok, summary ? sh.k_stride : sh.q_stride, 64,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map3(&mk, k, KD, sh.Hqk, n_tok, sh.k_stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map3(&mv, v, sh.V, sh.Hv, n_tok, sh.v_stride, BVT, CU_TENSOR_MAP_SWIZZLE_64B))
     return GDN_ERR_CUDA;
   TcParams tp{};
   tp.cu = cu;
@@ -1344,11 +1364,31 @@ gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float
   tp.o_f32 = (flags & GDN_FLAG_O_F32) ? 1 : 0;
   tp.hT = h_T;
   tp.status = status;
+  tp.summary = summary ? 1 : 0;
+  tp.M = M;
+  tp.S_local = S_local;
   if (cudaFuncSetAttribute(chunk_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kWsSmem) != cudaSuccess)
     return GDN_ERR_CUDA;
-  chunk_ws_kernel<<<dim3(sh.V / BVT, sh.Hv, sh.n_seqs), NT2, kWsSmem, st>>>(mq, mk, mv, tp);
+  const int cols = summary ? KD + sh.V : sh.V;
+  chunk_ws_kernel<<<dim3(cols / BVT, sh.Hv, n_seqs), NT2, kWsSmem, st>>>(mq, mk, mv, tp);
   return launch_status();
+}
+
+gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const float *h0, const int32_t *cu,
+                        const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
+                        void *workspace, size_t ws_bytes, cudaStream_t st) {
+  const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
+  return run_tc(q, k, v, g, beta, h0, cu, sh.n_seqs, n_tok, sh, scale, flags, o, h_T, false,
+                nullptr, nullptr, workspace, ws_bytes, st);
+}
+
+gdn_status summary_tc(const void *k, const void *v, const float *g, const float *beta,
+                      const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
+                      float *M, float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st) {
+  return run_tc(k, k, v, g, beta, nullptr, bounds, n_seg, sh.T, sh, 1.f, flags, nullptr, nullptr,
+                true, M, S_local, workspace, ws_bytes, st);
 }
 
 }  // namespace gdn

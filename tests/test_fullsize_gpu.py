@@ -1,0 +1,139 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+Each test builds the workload on the GPU from the seeded generator, runs the
+same calls bench.py makes, and compares sampled heads (or sequence x head
+pairs) against the fp64 oracle computed for exactly those outputs.  The
+segment-parallel workload also checks, for every head, that the two-pass
+result equals the single pass on the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.parity import assert_close, metrics, to64
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def crg():
+    import chunked_recurrence_gb300 as m
+    m.load()
+    return m
+
+
+def _bf16_round(y):
+    return torch.from_numpy(np.ascontiguousarray(y)).to(torch.bfloat16).double().numpy()
+
+
+def _f32_round(y):
+    return np.asarray(y, dtype=np.float32).astype(np.float64)
+
+
+def _oracle_layer(inp, cu_host, seqs, heads, n_threads=None):
+    """Oracle layer forward for v-heads `heads` (all their q/k/v channels) over the
+    sequences `seqs`, with each stage's output stored in the ABI's dtype."""
+    wl = inp["workload"]
+    Hqk, K, V = wl.Hqk, wl.K, wl.V
+    r = wl.Hv // Hqk
+    x, w = inp["x"], inp["conv_w"]
+    out = {}
+    for h in heads:
+        qh = h // r
+        cols = (list(range(qh * K, (qh + 1) * K)) + list(range(Hqk * K + qh * K, Hqk * K + (qh + 1) * K))
+                + list(range(2 * Hqk * K + h * V, 2 * Hqk * K + (h + 1) * V)))
+        ci = torch.tensor(cols, device=x.device)
+        for s in seqs:
+            a, b = int(cu_host[s]), int(cu_host[s + 1])
+            xs = to64(x[a:b].index_select(1, ci))
+            ws = to64(w.index_select(0, ci))
+            y = _bf16_round(oracle.conv1d(xs, ws, None, None, 1))
+            n = b - a
+            q = y[:, :K].reshape(n, 1, K)
+            k = y[:, K:2 * K].reshape(n, 1, K)
+            v = y[:, 2 * K:].reshape(n, 1, V)
+            g, beta = oracle.gate_prep(to64(inp["a"][a:b, h:h + 1]), to64(inp["b"][a:b, h:h + 1]),
+                                       to64(inp["A_log"][h:h + 1]), to64(inp["dt_bias"][h:h + 1]))
+            g, beta = _f32_round(g), _f32_round(beta)
+            h0 = None if inp["h0"] is None else to64(inp["h0"][s:s + 1, h:h + 1])
+            o, hT = oracle.gdn_fwd(q, k, v, g, beta, h0, None, inp["scale"], True,
+                                   n_threads=n_threads)
+            out[(s, h)] = (o[:, 0], hT[0, 0])
+    return out
+
+
+def _run_layer(crg, inp, cu):
+    wl = inp["workload"]
+    r = crg.layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
+                      wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"])
+    torch.cuda.synchronize()
+    return r
+
+
+def _check(r, ref, cu_host, what):
+    for (s, h), (ro, rh) in ref.items():
+        a, b = int(cu_host[s]), int(cu_host[s + 1])
+        assert_close(r["o"][a:b, h].cpu(), ro, "bf16", f"{what} o seq {s} head {h}")
+        assert_close(r["h_T"][s, h].cpu(), rh, "bf16", f"{what} h_T seq {s} head {h}")
+
+
+def test_qwen35_4b_layer_full(crg):
+    inp = synth.make_inputs("qwen35_4b_layer", device=DEV, with_direct=False)
+    r = _run_layer(crg, inp, None)
+    cu = np.array([0, inp["n_tok"]])
+    ref = _oracle_layer(inp, cu, [0], [0, 13, 31])
+    _check(r, ref, cu, "4B layer")
+
+
+def test_packed_full(crg):
+    inp = synth.make_inputs("packed", device=DEV, with_direct=False)
+    cu_full, cnt = crg.gdn_cu_seqlens_from_position_ids(inp["position_ids"])
+    n = int(cnt.item())
+    cu = cu_full[: n + 1]
+    cu_host = cu.cpu().numpy()
+    assert n == 12 and np.array_equal(cu_host, inp["cu_seqlens"].cpu().numpy())
+    r = _run_layer(crg, inp, cu)
+    ref = _oracle_layer(inp, cu_host, [0, 5, 11], [1, 30])
+    _check(r, ref, cu_host, "packed")
+
+
+def test_train_batch_full(crg):
+    inp = synth.make_inputs("train_batch", device=DEV, with_direct=False)
+    r = _run_layer(crg, inp, None)
+    wl = inp["workload"]
+    cu = np.arange(wl.B + 1) * wl.T
+    ref = _oracle_layer(inp, cu, [0, 7], [2, 63])
+    _check(r, ref, cu, "train batch")
+
+
+def test_long_segments_full(crg):
+    """Segment two-pass at T = 131072 in 8 segments: equal to the single pass on
+    every head, and both equal to the oracle on sampled heads."""
+    wl = synth.WORKLOADS["long_segments"]
+    inp = synth.make_inputs(wl, device=DEV, with_front_end=False)
+    g, beta = crg.gdn_gate_prep(inp["a"], inp["b"], inp["A_log"], inp["dt_bias"])
+    bounds = inp["seg_bounds"]
+    o2, h2 = crg.segment_parallel_fwd(inp["q"], inp["k"], inp["v"], g, beta, bounds,
+                                      scale=inp["scale"])
+    o1, h1 = crg.gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], g, beta, None, None, inp["scale"],
+                               True, B=1)
+    torch.cuda.synchronize()
+    for h in range(wl.Hv):
+        m = metrics(o2[:, h].float(), o1[:, h].float())
+        assert m["rel_l2"] <= 5e-3, (h, m)
+        assert metrics(h2[h], h1[0, h])["rel_l2"] <= 5e-3
+    heads = [0, 9]
+    ix = torch.tensor(heads, device=DEV)
+    sel = lambda t: to64(t.index_select(1, ix))
+    ro, rh = oracle.gdn_fwd(sel(inp["q"]), sel(inp["k"]), sel(inp["v"]), sel(g), sel(beta), None,
+                            None, inp["scale"], True)  # both heads in parallel (one job each)
+    for j, h in enumerate(heads):
+        assert_close(o1[:, h].cpu(), ro[:, j], "bf16", f"single pass o head {h}")
+        assert_close(h1[0, h].cpu(), rh[0, j], "bf16", f"single pass h_T head {h}")
+        assert_close(o2[:, h].cpu(), ro[:, j], "bf16", f"two-pass o head {h}")
+        assert_close(h2[h].cpu(), rh[0, j], "bf16", f"two-pass h_T head {h}")
