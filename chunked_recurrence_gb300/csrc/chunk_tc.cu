@@ -97,8 +97,10 @@ struct PrepParams {
   int32_t *status;
 };
 
-constexpr int kAP = C + 1;  // padded fp32 row of the A / X matrices
-constexpr size_t kPrepSmem = 1024 + 16384 + sizeof(float) * (C * kAP * 3 + 5 * C);
+constexpr int kAP = C + 4;  // fp32 row of the A / X matrices, padded to keep rows 16-byte aligned
+// dynamic shared memory: 1024 alignment slack + the bf16 k tile (16 KB) + fp32 KK, X0, X1
+// (3 x 64 x kAP) + gamma, beta (2 x 64 each), 1/|k| (64) and exp(g) (2 x 64) = 7 x 64 floats
+constexpr size_t kPrepSmem = 1024 + 16384 + sizeof(float) * (C * kAP * 3 + 7 * C);
 
 __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
   extern __shared__ uint8_t smraw[];
@@ -110,6 +112,7 @@ __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
   float *gm = X1 + C * kAP;                        // [2][64] gamma per half
   float *bt = gm + 2 * C;                          // [2][64] beta per half
   float *kinv = bt + 2 * C;                        // [64] 1 / |k| per token
+  float *al = kinv + C;                            // [2][64] exp(g) per half
   __shared__ uint64_t bar;
   __shared__ uint32_t tbase;
 
@@ -199,6 +202,11 @@ __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
     const bool has_row = lane < 16;
     const int r = warp * 16 + lane;
     const float ir = has_row ? kinv[r] : 0.f;
+    // shared loads before any store: interleaved, each load would wait for the previous
+    // store (the compiler cannot rule out aliasing between the two arrays)
+    float kv[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) kv[c] = kinv[c];
 #pragma unroll
     for (int c0 = 0; c0 < C; c0 += 16) {
       float v[16];
@@ -206,7 +214,7 @@ __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
       tmem_wait_ld();
       if (has_row)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) KK[r * kAP + c0 + i] = v[i] * ir * kinv[c0 + i];
+        for (int i = 0; i < 16; ++i) KK[r * kAP + c0 + i] = v[i] * ir * kv[c0 + i];
     }
   }
   tc_fence_before();
@@ -217,13 +225,15 @@ __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
   const int rh = p.Hv / p.Hqk;
   const int half = tid >> 6, lt = tid & 63;
   float *X = half ? X1 : X0;
-  float *gh = gm + half * C, *bh = bt + half * C;
+  float *gh = gm + half * C, *bh = bt + half * C, *ah = al + half * C;
   for (int j0 = 0; j0 < rh; j0 += 2) {
     const int j = j0 + half;
     const bool active = j < rh;  // uniform per half (64 threads)
     const int hv = qh * rh + (active ? j : 0);
     if (active) {
-      gh[lt] = lt < n ? p.g[(t0 + lt) * p.Hv + hv] : 0.f;
+      const float gv = lt < n ? p.g[(t0 + lt) * p.Hv + hv] : 0.f;
+      gh[lt] = gv;
+      ah[lt] = expf(gv);  // per-token decay exp(g)
       bh[lt] = lt < n ? p.beta[(t0 + lt) * p.Hv + hv] : 0.f;
     }
     __syncthreads();
@@ -241,9 +251,17 @@ __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
     __syncthreads();
     // column lt of A: A[i][lt] = beta_i exp(gamma_i - gamma_lt) (k_hat_i . k_hat_lt), i > lt
     if (active) {
-      const float gl = gh[lt];
-      for (int i = 0; i < C; ++i)
-        X[i * kAP + lt] = (i > lt) ? bh[i] * expf(gh[i] - gl) * KK[i * kAP + lt] : 0.f;
+      // exp(gamma_i - gamma_lt) = prod_{m = lt+1..i} exp(g_m): a running product down the
+      // column; all loads come before the stores (see the K K^T unpacking above)
+      float col[C];
+      float gp = 1.f;
+#pragma unroll
+      for (int i = 0; i < C; ++i) {
+        if (i > lt) gp *= ah[i];
+        col[i] = (i > lt) ? bh[i] * gp * KK[i * kAP + lt] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < C; ++i) X[i * kAP + lt] = col[i];
     }
     __syncthreads();
     // X = (I + A)^-1, one column per thread, held in registers: x_r = delta_rc - sum_{j<r} A_rj x_j.
@@ -256,17 +274,16 @@ __global__ void __launch_bounds__(NT) chunk_prep_kernel(const PrepParams p) {
       x[0] = (lt == 0) ? 1.f : 0.f;
 #pragma unroll
       for (int r = 1; r < C; ++r) {
-        const float *Ar = X + r * kAP;
+        const float4 *Ar = reinterpret_cast<const float4 *>(X + r * kAP);  // rows are 16-byte aligned
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int j = 0; j + 3 < r; j += 4) {
-          a0 = fmaf(Ar[j], x[j], a0);
-          a1 = fmaf(Ar[j + 1], x[j + 1], a1);
-          a2 = fmaf(Ar[j + 2], x[j + 2], a2);
-          a3 = fmaf(Ar[j + 3], x[j + 3], a3);
+        for (int j = 0; j < r; j += 4) {  // columns < 64 of row r; entries past r are not used
+          const float4 a = Ar[j >> 2];
+          a0 = fmaf(a.x, x[j], a0);
+          if (j + 1 < r) a1 = fmaf(a.y, x[j + 1], a1);
+          if (j + 2 < r) a2 = fmaf(a.z, x[j + 2], a2);
+          if (j + 3 < r) a3 = fmaf(a.w, x[j + 3], a3);
         }
-#pragma unroll
-        for (int j = r & ~3; j < r; ++j) a0 = fmaf(Ar[j], x[j], a0);
         x[r] = (r == lt) ? 1.f : -((a0 + a1) + (a2 + a3));
       }
       // T[r][lt] = x_r beta_lt for r >= lt (x_lt = 1 gives the diagonal beta_lt), packed rows;
@@ -745,7 +762,7 @@ struct WsShared {
   int kq_issued[3], kq_seen[3], v_issued[2], v_seen[2];
   int pre_inflight, chain_inflight, out_inflight;
   uint32_t ph_pre, ph_chain, ph_out;
-  float gam[C], gl2[C], bex[C], dec[C], kinv[C], qinv[C];  // WG0 working set
+  float gam[C], gl2[C], bex[C], dec[C], kinv[C], qinv[C], alf[C + 1];  // WG0 working set
   float dk[2][C], alpha[2][C], pdiag[2][C], blast[2];      // handed to WG1 per buffer
   int nvalid[2];
 };
@@ -853,7 +870,8 @@ __global__ void __launch_bounds__(NT2, 1)
       const uint8_t *qk = sm + W_KQ + st * 32768;
       // chunk ci-2's buffers (same parity) must be released by WG1
       {
-        const bool ok = ci < 2 || mbar_wait_abortable(&sh.empty[b], ((ci - 2) >> 1) & 1, kSpin, abort_flag);
+        // one thread polls; the others wait in the hardware barrier of the vote below
+        const bool ok = ci < 2 || wt != 0 || mbar_wait_abortable(&sh.empty[b], ((ci - 2) >> 1) & 1, kSpin, abort_flag);
         if (named_bar_any(1, 128, !ok)) {
           if (wt == 0) fail();
           break;
@@ -885,12 +903,17 @@ __global__ void __launch_bounds__(NT2, 1)
         sh.bex[2 * lane + 1] = expf(gb);
         sh.dec[2 * lane] = expf(last - ga);
         sh.dec[2 * lane + 1] = expf(last - gb);
-        if (lane == 31) sh.blast[b] = expf(last);
+        sh.alf[2 * lane] = expf(g0);  // per-token decay exp(g)
+        sh.alf[2 * lane + 1] = expf(g1);
+        if (lane == 31) {
+          sh.blast[b] = expf(last);
+          sh.alf[C] = 1.f;
+        }
       }
       // ---- this chunk's k | q and v tiles
       {
-        bool ok = mbar_wait_abortable(&sh.kq_full[st], (ci / 3) & 1, kSpin, abort_flag);
-        if (load_v) ok = ok && mbar_wait_abortable(&sh.v_full[b], (ci >> 1) & 1, kSpin, abort_flag);
+        bool ok = wt != 0 || mbar_wait_abortable(&sh.kq_full[st], (ci / 3) & 1, kSpin, abort_flag);
+        if (load_v) ok = ok && (wt != 0 || mbar_wait_abortable(&sh.v_full[b], (ci >> 1) & 1, kSpin, abort_flag));
         if (named_bar_any(1, 128, !ok)) {
           if (wt == 0) fail();
           break;
@@ -929,16 +952,20 @@ __global__ void __launch_bounds__(NT2, 1)
       }
       named_bar_sync(1, 128);
       if (wt < C) sh.dk[b][wt] = sh.dec[wt] * sh.kinv[wt];
-      // ---- T and T diag(b/|k|) as bf16 hi/lo tiles (row tr, columns tcb..tcb+31)
+      // ---- T and T diag(b/|k|) as bf16 hi/lo tiles (row tr, columns tcb..tcb+31);
+      //      the column factors are read before any tile store: interleaved, every shared
+      //      load would wait for the preceding store (the compiler cannot rule out aliasing)
+      float cf[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) cf[u] = sh.bex[tcb + u] * sh.kinv[tcb + u];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int c0 = tcb + q * 8;
         uint32_t wh[4], wl[4], xh[4], xl[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int c = c0 + 2 * e;
           const float t_0 = tpre[q * 8 + 2 * e], t_1 = tpre[q * 8 + 2 * e + 1];
-          const float u_0 = t_0 * sh.bex[c] * sh.kinv[c], u_1 = t_1 * sh.bex[c + 1] * sh.kinv[c + 1];
+          const float u_0 = t_0 * cf[q * 8 + 2 * e], u_1 = t_1 * cf[q * 8 + 2 * e + 1];
           const float h0 = __bfloat162float(__float2bfloat16_rn(t_0));
           const float h1 = __bfloat162float(__float2bfloat16_rn(t_1));
           const float g0 = __bfloat162float(__float2bfloat16_rn(u_0));
@@ -984,7 +1011,7 @@ __global__ void __launch_bounds__(NT2, 1)
         sh.pre_inflight = 1;
       }
       {
-        const bool ok = mbar_wait_abortable(&sh.pre_done, ci & 1, kSpin, abort_flag);
+        const bool ok = wt != 0 || mbar_wait_abortable(&sh.pre_done, ci & 1, kSpin, abort_flag);
         if (named_bar_any(1, 128, !ok)) {
           if (wt == 0) fail();
           break;
@@ -998,46 +1025,47 @@ __global__ void __launch_bounds__(NT2, 1)
       // ---- P (strictly lower, bf16) with its diagonal kept in fp32; -W (bf16)
       {
         const int row = mrow & 63;
-        const float gr2 = sh.gl2[row], qr = p.scale * sh.qinv[row];
+        const float qr = p.scale * sh.qinv[row];
         uint8_t *pt = sm + W_PT + b * 8192;
-        float v[64];
+        uint8_t *nw = sm + W_NW + b * 16384;
+        // Q K^T and the first half of W in one TMEM round trip, the second half of W in another
+        float qk[64], w64[64];
+        tmem_ld64(tl + WC_QK, qk);
+        tmem_ld64(tl + WC_W, w64);
+        tmem_wait_ld();
+        if (lane_row) {
+          // Gamma_{r,j} = exp(gamma_r - gamma_j) = prod_{i=j+1..r} exp(g_i) for j < r: a running
+          // product walking j downwards, one multiply per column and no exponential.  All shared
+          // loads come before the stores (see the T conversion).
+          float gprod = 1.f, vd = 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < C; c0 += 16) tmem_ld16(tl + WC_QK + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+          for (int j = C - 1; j >= 0; --j) {
+            const float aj = sh.alf[j + 1], kj = sh.kinv[j];
+            vd = (j == mrow) ? qk[j] : vd;
+            if (j < mrow) gprod *= aj;
+            qk[j] = (j < mrow) ? qr * kj * gprod * qk[j] : 0.f;
+          }
+          const float pdv = qr * sh.kinv[mrow] * vd;
+#pragma unroll
+          for (int c0 = 0; c0 < C; c0 += 8)
+            *reinterpret_cast<uint4 *>(pt + sw128_off(mrow, c0)) =
+                make_uint4(pack_bf16(qk[c0], qk[c0 + 1]), pack_bf16(qk[c0 + 2], qk[c0 + 3]),
+                           pack_bf16(qk[c0 + 4], qk[c0 + 5]), pack_bf16(qk[c0 + 6], qk[c0 + 7]));
+          sh.pdiag[b][mrow] = pdv;
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 8)
+            *reinterpret_cast<uint4 *>(nw + sw128_off(mrow, c0)) =
+                make_uint4(pack_bf16(-w64[c0], -w64[c0 + 1]), pack_bf16(-w64[c0 + 2], -w64[c0 + 3]),
+                           pack_bf16(-w64[c0 + 4], -w64[c0 + 5]), pack_bf16(-w64[c0 + 6], -w64[c0 + 7]));
+        }
+        tmem_ld64(tl + WC_W + 64, w64);
         tmem_wait_ld();
         if (lane_row) {
 #pragma unroll
-          for (int c0 = 0; c0 < C; c0 += 8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j0 = c0 + 2 * e, j1 = j0 + 1;
-              const float a = (j0 < mrow) ? qr * sh.kinv[j0] * exp2f(gr2 - sh.gl2[j0]) * v[j0] : 0.f;
-              const float bb = (j1 < mrow) ? qr * sh.kinv[j1] * exp2f(gr2 - sh.gl2[j1]) * v[j1] : 0.f;
-              w[e] = pack_bf16(a, bb);
-            }
-            *reinterpret_cast<uint4 *>(pt + sw128_off(mrow, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          float vd = 0.f;
-#pragma unroll
-          for (int j = 0; j < C; ++j) vd = (j == mrow) ? v[j] : vd;
-          sh.pdiag[b][mrow] = qr * sh.kinv[mrow] * vd;
-        }
-        uint8_t *nw = sm + W_NW + b * 16384;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16)
-            tmem_ld16(tl + WC_W + half * 64 + c0, *reinterpret_cast<float(*)[16]>(v + c0));
-          tmem_wait_ld();
-          if (lane_row) {
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 8) {
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) w[e] = pack_bf16(-v[c0 + 2 * e], -v[c0 + 2 * e + 1]);
-              *reinterpret_cast<uint4 *>(nw + half * 8192 + sw128_off(mrow, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
+          for (int c0 = 0; c0 < 64; c0 += 8)
+            *reinterpret_cast<uint4 *>(nw + 8192 + sw128_off(mrow, c0)) =
+                make_uint4(pack_bf16(-w64[c0], -w64[c0 + 1]), pack_bf16(-w64[c0 + 2], -w64[c0 + 3]),
+                           pack_bf16(-w64[c0 + 4], -w64[c0 + 5]), pack_bf16(-w64[c0 + 6], -w64[c0 + 7]));
         }
       }
       if (wt == 0) sh.nvalid[b] = n;
@@ -1076,7 +1104,7 @@ __global__ void __launch_bounds__(NT2, 1)
       const int64_t t0 = start + (int64_t)ci * C;
       const uint32_t qk_a = sb + W_KQ + st * 32768;
       {
-        const bool ok = mbar_wait_abortable(&sh.full[b], (ci >> 1) & 1, kSpin, abort_flag);
+        const bool ok = wt != 0 || mbar_wait_abortable(&sh.full[b], (ci >> 1) & 1, kSpin, abort_flag);
         if (named_bar_any(2, 128, !ok)) {
           if (wt == 0) fail();
           ok_all = false;
@@ -1103,7 +1131,7 @@ __global__ void __launch_bounds__(NT2, 1)
         }
       }
       {
-        const bool ok = mbar_wait_abortable(&sh.chain_done, ph_chain, kSpin, abort_flag);
+        const bool ok = wt != 0 || mbar_wait_abortable(&sh.chain_done, ph_chain, kSpin, abort_flag);
         if (named_bar_any(2, 128, !ok)) {
           if (wt == 0) fail();
           ok_all = false;
@@ -1169,7 +1197,7 @@ __global__ void __launch_bounds__(NT2, 1)
         }
       }
       {
-        const bool ok = mbar_wait_abortable(&sh.chain_done, ph_chain, kSpin, abort_flag);
+        const bool ok = wt != 0 || mbar_wait_abortable(&sh.chain_done, ph_chain, kSpin, abort_flag);
         if (named_bar_any(2, 128, !ok)) {
           if (wt == 0) fail();
           ok_all = false;
@@ -1190,7 +1218,7 @@ __global__ void __launch_bounds__(NT2, 1)
         write_state_bf16();
       }
       if (!p.summary) {
-        const bool ok = mbar_wait_abortable(&sh.out_done, sh.ph_out, kSpin, abort_flag);
+        const bool ok = wt != 0 || mbar_wait_abortable(&sh.out_done, sh.ph_out, kSpin, abort_flag);
         if (named_bar_any(2, 128, !ok)) {
           if (wt == 0) fail();
           ok_all = false;
