@@ -46,6 +46,7 @@ _SIGS = {
     "gdn_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "gdn_version": ([], _I32),
     "gdn_chunk_fwd_workspace_bytes": ([ctypes.POINTER(GdnShape)], _SZ),
+    "gdn_chunk_fwd_min_workspace_bytes": ([ctypes.POINTER(GdnShape)], _SZ),
     "gdn_segment_summary_workspace_bytes": ([ctypes.POINTER(GdnShape), _I32], _SZ),
     "gdn_workspace_reset": ([_P, _SZ, _P], ctypes.c_int),
     "gdn_workspace_status": ([_P, ctypes.POINTER(_I32), _P], ctypes.c_int),
@@ -232,6 +233,10 @@ def _workspace_for(nbytes, device):
 
 def gdn_chunk_fwd_workspace_bytes(shape: GdnShape) -> int:
     return int(load().gdn_chunk_fwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_chunk_fwd_min_workspace_bytes(shape: GdnShape) -> int:
+    return int(load().gdn_chunk_fwd_min_workspace_bytes(ctypes.byref(shape)))
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm_qk=True,

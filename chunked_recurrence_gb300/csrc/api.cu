@@ -12,6 +12,12 @@ gdn_status segment_summary_simt(const void *k, const void *v, const float *g, co
                                 cudaStream_t st);
 bool chunk_tc_supported(const void *q, const void *k, const void *v, const gdn_shape &sh);
 size_t chunk_tc_workspace_bytes(const gdn_shape &sh, int64_t n_tok);
+bool chunk_scan_supported(const void *q, const void *k, const void *v, const gdn_shape &sh);
+size_t chunk_scan_workspace_bytes(const gdn_shape &sh, int64_t n_tok);
+gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *h0, const int32_t *cu,
+                          const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
+                          void *workspace, size_t ws_bytes, cudaStream_t st);
 gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float *g,
                         const float *beta, const float *h0, const int32_t *cu,
                         const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
@@ -50,11 +56,23 @@ gdn_status normalise_shape(const gdn_shape *in, gdn_shape *out) {
 
 }  // namespace
 
-// The tensor-core path (bf16, K = 128) keeps T = (I + A)^-1 diag(beta) of every
-// chunk and v-head in the workspace between its two kernels.
+// The tensor-core path (bf16, K = 128) keeps per-chunk operands in the workspace
+// between its two kernels.  With room for every chunk's full operand record
+// (gdn_chunk_fwd_workspace_bytes) the split operand/scan kernels run; with at
+// least the compact size (gdn_chunk_fwd_min_workspace_bytes: only T of every
+// chunk) the older kernel pair that rebuilds the operands inside the scan runs.
 bool tc_shape(const gdn_shape &s) { return s.dtype == GDN_BF16 && s.K == 128 && s.V % 32 == 0; }
+bool scan_shape(const gdn_shape &s) { return tc_shape(s) && s.V % 64 == 0 && s.V <= 256; }
 
 extern "C" size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape) {
+  gdn_shape s;
+  if (normalise_shape(shape, &s) != GDN_OK) return 0;
+  if (scan_shape(s)) return chunk_scan_workspace_bytes(s, (int64_t)s.B * s.T);
+  if (tc_shape(s)) return chunk_tc_workspace_bytes(s, (int64_t)s.B * s.T);
+  return kWorkspaceBase;
+}
+
+extern "C" size_t gdn_chunk_fwd_min_workspace_bytes(const gdn_shape *shape) {
   gdn_shape s;
   if (normalise_shape(shape, &s) != GDN_OK) return 0;
   if (tc_shape(s)) return chunk_tc_workspace_bytes(s, (int64_t)s.B * s.T);
@@ -92,9 +110,14 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   if (s.n_seqs == 0) return GDN_OK;
   if (n_tok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
   if (n_tok == 0 && !h_T) return GDN_OK;
-  if (!(flags & GDN_FLAG_SIMT) && n_tok > 0 && tc_shape(s) && chunk_tc_supported(q, k, v, s))
+  if (!(flags & GDN_FLAG_SIMT) && n_tok > 0 && tc_shape(s) && chunk_tc_supported(q, k, v, s)) {
+    if (scan_shape(s) && chunk_scan_supported(q, k, v, s) &&
+        workspace_bytes >= chunk_scan_workspace_bytes(s, n_tok))
+      return chunk_fwd_scan(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T, workspace,
+                            workspace_bytes, (cudaStream_t)stream);
     return chunk_fwd_tc(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T, workspace,
                         workspace_bytes, (cudaStream_t)stream);
+  }
   return chunk_fwd_simt(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
                         (int32_t *)workspace, (cudaStream_t)stream);
 }

@@ -1,0 +1,884 @@
+// chunk_scan.cu -- tensor-core path of gdn_chunk_fwd split by dependence on the
+// state: a fully parallel operand kernel, then a lean state scan.
+//
+// The chunk form of the gated delta rule ("Gated Delta Networks", chunkwise
+// algorithm; the UT/WY transform), per chunk of C = 64 tokens, v-head h and
+// start state S (V x K, fp32), with unit-norm keys and queries:
+//   gamma = inclusive cumsum of g,  b = exp(gamma),  d = exp(gamma_last - gamma)
+//   A  = strictly-lower(diag(beta) K_hat K_hat^T * Gamma),  Gamma_ij = exp(gamma_i - gamma_j)
+//   T  = (I + A)^-1 diag(beta)
+//   W  = T diag(b) K_hat,  U = T V                          (state-independent)
+//   U' = U - W S^T                                          (state step 1)
+//   O  = scale diag(b) Q_hat S^T + P U',  P = scale (Q_hat K_hat^T * Gamma), j <= i
+//   S <- b_last S + U'^T diag(d) K_hat                      (state step 2)
+//
+// chunk_operand_kernel (one block per chunk x v-head, all chunks at once)
+// computes everything that does not depend on S and stores it in a record of
+// the workspace laid out as the scan kernel's shared-memory tiles:
+//   -W (bf16, K-major 128-byte-swizzled images, two 64-feature halves), P
+//   without its diagonal (bf16, same layout), U (fp32, 32-column slices) and
+//   the vectors alpha = scale b / |q|, diag(P) (fp32), d / |k| and b_last.
+// chunk_scan_kernel (one block per sequence x v-head x 32 value columns) then
+// walks the chunks with three small tcgen05 MMA groups per chunk:
+//   [Q; -W] S^T                   (M = 128: raw q rows, then -W rows)
+//   K^T [dU'_hi | dU'_lo]         (M = 128 key features, N = 2 x 32)
+//   [P; -] [U'_hi | U'_lo]        (rows 0-63 used)
+// with the fp32 state in registers (one key feature per thread) and a bf16
+// copy of S^T in shared memory as the MMA operand.
+//
+// Precision: q and k enter the MMAs as their exact bf16 values (1/|q|, 1/|k|
+// applied in fp32); T enters as a hi + lo pair of bf16 matrices; U' and
+// diag(d/|k|) U' enter as hi + lo pairs; the diagonal of P stays fp32.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "chunk_common.cuh"
+#include "common.cuh"
+#include "sm100.cuh"
+
+using namespace gdn;
+using namespace gdn::sm100;
+
+namespace {
+
+constexpr int C = kChunk;   // 64 tokens per chunk
+constexpr int KD = 128;     // key width of this path
+constexpr int VS = 32;      // value columns per scan block
+constexpr uint32_t kSpin = 1u << 22;  // bounded waits before reporting a timeout
+constexpr size_t kHeader = 256;       // status word + padding
+
+// ------------------------------------------------------------ records
+// One record per (chunk slot, v-head), 1 KB aligned pieces:
+constexpr uint32_t REC_NW = 0;       // -W: [2 feature halves][64 rows][128 B] bf16, SW128 images
+constexpr uint32_t REC_P = 16384;    // P (strictly lower): [64 rows][128 B] bf16, SW128 image
+constexpr uint32_t REC_VEC = 24576;  // alpha[64], pdiag[64], dk[64] fp32, b_last, n
+constexpr uint32_t REC_U = 25600;    // U: [V / 32 slices][64 tokens][32] fp32
+constexpr uint32_t VEC_ALPHA = 0, VEC_PDIAG = 64, VEC_DK = 128, VEC_BLAST = 192, VEC_N = 193;  // floats
+
+__host__ __device__ constexpr size_t rec_bytes(int V) { return (size_t)REC_U + (size_t)V * C * 4; }
+
+// ============================================================ operand kernel
+
+struct OpParams {
+  const __nv_bfloat16 *q, *k, *v;
+  int64_t qs, ks, vs;  // token strides (elements)
+  const float *g, *beta;
+  const int32_t *cu;
+  int64_t row_T, n_tok;
+  int n_seqs, Hqk, Hv, l2norm;
+  float scale;
+  uint8_t *rec;
+  size_t rec_bytes;
+  int32_t *status;
+};
+
+constexpr int kXP = C + 4;  // fp32 row of A / T, padded (rows stay 16-byte aligned)
+constexpr uint32_t OP_KQ = 0;      // [2 halves][128 rows][128 B]: rows 0-63 raw k, 64-127 raw q
+constexpr uint32_t OP_VT = 32768;  // raw v: [V / 64 blocks][64 tokens][128 B], SW128
+__host__ __device__ constexpr uint32_t op_x(int V) { return OP_VT + (uint32_t)V * 128; }
+__host__ __device__ constexpr uint32_t op_tt(int V) { return op_x(V) + 18432; }  // 64 x kXP floats
+// T hi, T lo, T diag(b/|k|) hi, lo: 4 x [64 rows][128 B] SW128
+__host__ __device__ constexpr uint32_t op_smem(int V) { return op_tt(V) + 32768 + 1024; }
+
+// Column lt (>= R0) of X = (I + A)^-1 by forward substitution, held in registers:
+// x_r = delta_r,lt - sum_{j<r} A_rj x_j.  Every lane walks the same (r, j) sequence, so
+// the A_rj reads are warp-wide broadcasts; all columns of the warp are >= R0, so rows
+// and terms below R0 are zero and skipped.
+template <int R0>
+__device__ __forceinline__ void solve_column(const float *X, int lt, float (&x)[C]) {
+#pragma unroll
+  for (int r = 0; r < C; ++r) x[r] = 0.f;
+  x[R0] = (lt == R0) ? 1.f : 0.f;
+#pragma unroll
+  for (int r = R0 + 1; r < C; ++r) {
+    const float4 *Ar = reinterpret_cast<const float4 *>(X + r * kXP);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int j = R0; j < r; j += 4) {
+      const float4 a = Ar[j >> 2];
+      a0 = fmaf(a.x, x[j], a0);
+      if (j + 1 < r) a1 = fmaf(a.y, x[j + 1], a1);
+      if (j + 2 < r) a2 = fmaf(a.z, x[j + 2], a2);
+      if (j + 3 < r) a3 = fmaf(a.w, x[j + 3], a3);
+    }
+    x[r] = (r == lt) ? 1.f : -((a0 + a1) + (a2 + a3));
+  }
+}
+
+template <int V>
+__global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
+  constexpr int NVB = V / 64;                       // 64-column blocks of v
+  constexpr uint32_t kCols = (128 + V <= 256) ? 256u : 512u;
+  extern __shared__ uint8_t smraw[];
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  __shared__ float gam[C], bex[C], dec[C], alf[C + 1], kinv[C], qinv[C], bet[C];
+  __shared__ float blast_s;
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tbase;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = (int)(blockIdx.x % (unsigned)p.Hv);
+  const int64_t slot = blockIdx.x / (unsigned)p.Hv;
+  const int qh = h / (p.Hv / p.Hqk);
+  int lo = 0, hi = p.n_seqs - 1;  // sequence of this slot: largest s with slot_base(s) <= slot
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (slot_base(p.cu, p.row_T, mid) <= slot) lo = mid; else hi = mid - 1;
+  }
+  const int s = lo;
+  int64_t start, end;
+  seq_range(p.cu, p.row_T, s, start, end);
+  if (start < 0 || end < start || end > p.n_tok) {
+    if (tid == 0) set_status(p.status, GDN_ERR_BOUNDS);
+    return;
+  }
+  const int64_t c = slot - slot_base(p.cu, p.row_T, s);
+  const int64_t t0 = start + c * C;
+  if (c < 0 || t0 >= end) return;  // slot past this sequence's last chunk: never read
+  const int n = (int)min((int64_t)C, end - t0);
+  uint8_t *rec = p.rec + ((size_t)slot * p.Hv + h) * p.rec_bytes;
+  float *vec = reinterpret_cast<float *>(rec + REC_VEC);
+  float *X = reinterpret_cast<float *>(sm + op_x(V));
+  uint8_t *TT = sm + op_tt(V);
+
+  // ---- raw k, q and v rows (two threads per token) into swizzled tiles; gates; norms
+  {
+    const int r = tid >> 1, hf = tid & 1;
+    const bool valid = r < n;
+    const int64_t tok = t0 + r;
+    uint4 kr[8], qr[8], vr[4 * NVB];
+    if (valid) {
+      const uint4 *ks = reinterpret_cast<const uint4 *>(p.k + tok * p.ks + (int64_t)qh * KD + hf * 64);
+      const uint4 *qs = reinterpret_cast<const uint4 *>(p.q + tok * p.qs + (int64_t)qh * KD + hf * 64);
+      const uint4 *vs = reinterpret_cast<const uint4 *>(p.v + tok * p.vs + (int64_t)h * V + hf * (V / 2));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        kr[j] = __ldg(ks + j);
+        qr[j] = __ldg(qs + j);
+      }
+#pragma unroll
+      for (int j = 0; j < 4 * NVB; ++j) vr[j] = __ldg(vs + j);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) kr[j] = qr[j] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < 4 * NVB; ++j) vr[j] = make_uint4(0, 0, 0, 0);
+    }
+    if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
+    else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t *wk = reinterpret_cast<const uint32_t *>(&kr[j]);
+      const uint32_t *wq = reinterpret_cast<const uint32_t *>(&qr[j]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 a = unpack_bf16(wk[e]), b = unpack_bf16(wq[e]);
+        sk = fmaf(a.x, a.x, fmaf(a.y, a.y, sk));
+        sq = fmaf(b.x, b.x, fmaf(b.y, b.y, sq));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      *reinterpret_cast<uint4 *>(sm + OP_KQ + hf * 16384 + sw128_off(r, j * 8)) = kr[j];
+      *reinterpret_cast<uint4 *>(sm + OP_KQ + hf * 16384 + 8192 + sw128_off(r, j * 8)) = qr[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 4 * NVB; ++j) {
+      const int col = hf * (V / 2) + j * 8;
+      *reinterpret_cast<uint4 *>(sm + OP_VT + (col >> 6) * 8192 + sw128_off(r, col & 63)) = vr[j];
+    }
+    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    if (hf == 0) {
+      kinv[r] = p.l2norm ? 1.f / sqrtf(sk + kL2Eps) : 1.f;
+      qinv[r] = p.l2norm ? 1.f / sqrtf(sq + kL2Eps) : 1.f;
+    }
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(&tbase, kCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = tbase;
+  const uint32_t kq_a = smem_u32(sm + OP_KQ);
+  // ---- [K; Q] K^T: M = 128 (k rows, then q rows), N = 64, K = 128 on the tensor core
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+    for (int ks = 0; ks < KD / 16; ++ks) {
+      const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+      umma_bf16(tm, smem_desc(kq_a + off, 16, 1024, 2), smem_desc(kq_a + off, 16, 1024, 2), id, ks > 0);
+    }
+    umma_commit(&bar);
+  }
+  // ---- gates: inclusive cumsum of g and the exponentials the chunk form uses
+  if (warp == 0) {
+    const float g0 = gam[2 * lane], g1 = gam[2 * lane + 1];
+    float incl = g0 + g1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const float last = __shfl_sync(0xffffffffu, incl, 31);
+    const float ga = incl - g1, gb = incl;
+    gam[2 * lane] = ga;
+    gam[2 * lane + 1] = gb;
+    bex[2 * lane] = expf(ga);
+    bex[2 * lane + 1] = expf(gb);
+    dec[2 * lane] = expf(last - ga);
+    dec[2 * lane + 1] = expf(last - gb);
+    alf[2 * lane] = expf(g0);
+    alf[2 * lane + 1] = expf(g1);
+    if (lane == 31) {
+      blast_s = expf(last);
+      alf[C] = 1.f;
+    }
+  }
+  __syncthreads();
+  if (tid < C) {
+    vec[VEC_ALPHA + tid] = p.scale * bex[tid] * qinv[tid];
+    vec[VEC_DK + tid] = (tid < n) ? dec[tid] * kinv[tid] : 0.f;
+    if (tid == 0) {
+      vec[VEC_BLAST] = blast_s;
+      reinterpret_cast<int *>(vec)[VEC_N] = n;
+    }
+  }
+  {
+    const bool ok = tid != 0 || mbar_wait(&bar, 0, kSpin);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
+      (void)mbar_wait(&bar, 0, kSpin);  // an MMA still in flight lands before TMEM is freed
+      tc_fence_before();
+      __syncthreads();
+      if (warp == 0) tmem_dealloc(tm, kCols);
+      return;
+    }
+  }
+  tc_fence_after();
+  // ---- rows of K K^T (lanes 0-63) become rows of A; rows of Q K^T (lanes 64-127) rows of P
+  {
+    const int i = tid & 63;
+    const bool isq = tid >= 64;
+    float r64[64];
+    tmem_ld64(tm + ((uint32_t)(warp * 32) << 16), r64);
+    tmem_wait_ld();
+    const float bi = isq ? p.scale * qinv[i] : bet[i] * kinv[i];
+    // Gamma_ij = prod_{m=j+1..i} exp(g_m) for j < i: a running product walking j down.
+    // Every shared load comes before the stores below (interleaved, each load would wait for
+    // the previous store: the compiler cannot rule out aliasing).
+    float gprod = 1.f, vd = 0.f;
+#pragma unroll
+    for (int j = C - 1; j >= 0; --j) {
+      const float aj = alf[j + 1], kj = kinv[j];
+      vd = (j == i) ? r64[j] : vd;
+      if (j < i) gprod *= aj;
+      r64[j] = (j < i) ? bi * kj * gprod * r64[j] : 0.f;
+    }
+    if (!isq) {
+      float4 *xr = reinterpret_cast<float4 *>(X + i * kXP);
+#pragma unroll
+      for (int m = 0; m < C / 4; ++m) xr[m] = make_float4(r64[4 * m], r64[4 * m + 1], r64[4 * m + 2], r64[4 * m + 3]);
+    } else {
+      const float pd = bi * kinv[i] * vd;
+      uint8_t *pimg = rec + REC_P;
+#pragma unroll
+      for (int c0 = 0; c0 < C; c0 += 8)
+        *reinterpret_cast<uint4 *>(pimg + sw128_off(i, c0)) =
+            make_uint4(pack_bf16(r64[c0], r64[c0 + 1]), pack_bf16(r64[c0 + 2], r64[c0 + 3]),
+                       pack_bf16(r64[c0 + 4], r64[c0 + 5]), pack_bf16(r64[c0 + 6], r64[c0 + 7]));
+      vec[VEC_PDIAG + i] = pd;
+    }
+  }
+  __syncthreads();
+  // ---- T = (I + A)^-1 diag(beta): one column per thread of warps 0-1
+  float x[C];
+  if (warp == 0) solve_column<0>(X, tid, x);
+  else if (warp == 1) solve_column<32>(X, tid, x);
+  __syncthreads();  // every read of A is done: T overwrites it
+  if (warp < 2) {
+    const float bl = bet[tid];
+#pragma unroll
+    for (int r = 0; r < C; ++r) X[r * kXP + tid] = (r >= tid) ? x[r] * bl : 0.f;
+  }
+  __syncthreads();
+  // ---- T and T diag(b/|k|) as bf16 hi/lo K-major tiles (row r, columns cb..cb+31)
+  {
+    const int r = tid >> 1, cb = (tid & 1) * 32;
+    float t[32], cf[32];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float4 a = reinterpret_cast<const float4 *>(X + r * kXP + cb)[m];
+      t[4 * m] = a.x;
+      t[4 * m + 1] = a.y;
+      t[4 * m + 2] = a.z;
+      t[4 * m + 3] = a.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 32; ++u) cf[u] = bex[cb + u] * kinv[cb + u];
+#pragma unroll
+    for (int q8 = 0; q8 < 4; ++q8) {
+      uint32_t wh[4], wl[4], xh[4], xl[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int u = q8 * 8 + 2 * e;
+        const float t_0 = t[u], t_1 = t[u + 1];
+        const float u_0 = t_0 * cf[u], u_1 = t_1 * cf[u + 1];
+        const float h0 = __bfloat162float(__float2bfloat16_rn(t_0));
+        const float h1 = __bfloat162float(__float2bfloat16_rn(t_1));
+        const float g0 = __bfloat162float(__float2bfloat16_rn(u_0));
+        const float g1 = __bfloat162float(__float2bfloat16_rn(u_1));
+        wh[e] = pack_bf16(h0, h1);
+        wl[e] = pack_bf16(t_0 - h0, t_1 - h1);
+        xh[e] = pack_bf16(g0, g1);
+        xl[e] = pack_bf16(u_0 - g0, u_1 - g1);
+      }
+      const uint32_t off = sw128_off(r, cb + q8 * 8);
+      *reinterpret_cast<uint4 *>(TT + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+      *reinterpret_cast<uint4 *>(TT + 8192 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      *reinterpret_cast<uint4 *>(TT + 16384 + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+      *reinterpret_cast<uint4 *>(TT + 24576 + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // ---- W = T diag(b/|k|) K (TMEM columns 0-127) and U = T V (columns 128..128+V), hi + lo
+  if (tid == 0) {
+    const uint32_t tt_a = smem_u32(TT), vt_a = smem_u32(sm + OP_VT);
+    const uint32_t id_w = idesc_bf16(64, 128, false, true);
+    const uint32_t id_u = idesc_bf16(64, V, false, true);
+#pragma unroll
+    for (int ks = 0; ks < C / 16; ++ks) {
+      const uint64_t kb = smem_desc(kq_a + ks * 2048, 16384, 1024, 2);
+      const uint64_t vb = smem_desc(vt_a + ks * 2048, 8192, 1024, 2);
+      umma_bf16(tm, smem_desc(tt_a + 16384 + ks * 32, 16, 1024, 2), kb, id_w, ks > 0);
+      umma_bf16(tm, smem_desc(tt_a + 24576 + ks * 32, 16, 1024, 2), kb, id_w, 1);
+      umma_bf16(tm + 128, smem_desc(tt_a + ks * 32, 16, 1024, 2), vb, id_u, ks > 0);
+      umma_bf16(tm + 128, smem_desc(tt_a + 8192 + ks * 32, 16, 1024, 2), vb, id_u, 1);
+    }
+    umma_commit(&bar);
+  }
+  {
+    const bool ok = tid != 0 || mbar_wait(&bar, 1, kSpin);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
+      (void)mbar_wait(&bar, 1, kSpin);
+      tc_fence_before();
+      __syncthreads();
+      if (warp == 0) tmem_dealloc(tm, kCols);
+      return;
+    }
+  }
+  tc_fence_after();
+  // ---- drain: rows of an M = 64 result sit in lanes 0-15 of each 32-lane quarter
+  {
+    const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
+    const int r = warp * 16 + lane;
+    const bool has_row = lane < 16;
+    float w64[64];
+#pragma unroll
+    for (int fb = 0; fb < 2; ++fb) {
+      tmem_ld64(tl + fb * 64, w64);
+      tmem_wait_ld();
+      if (has_row) {
+        uint8_t *dst = rec + REC_NW + fb * 8192;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 8)
+          *reinterpret_cast<uint4 *>(dst + sw128_off(r, c0)) =
+              make_uint4(pack_bf16(-w64[c0], -w64[c0 + 1]), pack_bf16(-w64[c0 + 2], -w64[c0 + 3]),
+                         pack_bf16(-w64[c0 + 4], -w64[c0 + 5]), pack_bf16(-w64[c0 + 6], -w64[c0 + 7]));
+      }
+    }
+#pragma unroll
+    for (int vb = 0; vb < NVB; ++vb) {
+      tmem_ld64(tl + 128 + vb * 64, w64);
+      tmem_wait_ld();
+      if (has_row) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + (size_t)(2 * vb + half) * 8192 + r * 128);
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            dst[m] = make_float4(w64[half * 32 + 4 * m], w64[half * 32 + 4 * m + 1],
+                                 w64[half * 32 + 4 * m + 2], w64[half * 32 + 4 * m + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, kCols);
+}
+
+// ============================================================ scan kernel
+
+struct ScanParams {
+  const int32_t *cu;
+  int64_t row_T, n_tok;
+  int Hqk, Hv, V;
+  const float *h0;
+  const uint8_t *rec;
+  size_t rec_bytes;
+  void *o;
+  int o_f32;
+  float *hT;
+  int32_t *status;
+};
+
+constexpr int NTS = 320;  // warps 0-7 epilogues, warp 8 copies, warp 9 MMAs
+// one stage of chunk operands (offsets inside the stage; each stage is 1 KB aligned)
+constexpr uint32_t ST_AQW = 0;      // [2 halves][128 rows][128 B]: rows 0-63 raw q, rows 64-127 -W
+constexpr uint32_t ST_K = 32768;    // [2 halves][64 tokens][128 B] raw k
+constexpr uint32_t ST_P = 49152;    // [64][128 B] P; the 8 KB after it stand in as the unused
+                                    // rows 64-127 of the M = 128 operand
+constexpr uint32_t ST_U = 57344;    // [64 tokens][32] fp32 U slice
+constexpr uint32_t ST_VEC = 65536;  // alpha, pdiag, dk, b_last, n
+constexpr uint32_t kStage = 66560;
+constexpr uint32_t kStageTx = 16384 + 16384 + 16384 + 8192 + 8192 + 1024;
+constexpr uint32_t SC_ST = 2 * kStage;     // S^T bf16 [128 features][32 values] SW64
+constexpr uint32_t SC_UP = SC_ST + 8192;   // 2 x [U'_hi | U'_lo] [64 tokens][64] SW128
+constexpr uint32_t SC_DU = SC_UP + 16384;  // [dU'_hi | dU'_lo] [64 tokens][64] SW128
+constexpr uint32_t kScanSmem = SC_DU + 8192 + 1024;
+// TMEM columns
+constexpr uint32_t TC_A = 0;    // 2 x 32: q S^T in lanes 0-63, -W S^T in lanes 64-127
+constexpr uint32_t TC_O = 64;   // 2 x 64: [P U'_hi | P U'_lo] in lanes 0-63
+constexpr uint32_t TC_S = 192;  // 64: [K^T dU'_hi | K^T dU'_lo], one lane per key feature
+constexpr uint32_t kScanCols = 256;
+
+struct ScanShared {
+  uint64_t full[2], empty[2], ga, b1, b2[2], epa, epb;
+  uint32_t tbase;
+  int abort;
+  int fills[2];          // loads issued into each stage
+  uint64_t *mma_bar;     // barrier of the last MMA commit and its phase parity
+  uint32_t mma_par;
+};
+
+// Every lane waits (bounded); the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  const bool ok = mbar_wait_abortable(bar, parity, kSpin, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(NTS, 1)
+    chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const ScanParams p) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  __shared__ ScanShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int v0 = blockIdx.x * VS, h = blockIdx.y, s = blockIdx.z;
+  const int qh = h / (p.Hv / p.Hqk);
+  int64_t start, end;
+  seq_range(p.cu, p.row_T, s, start, end);
+  if (start < 0 || end < start || end > p.n_tok) {
+    if (tid == 0) set_status(p.status, GDN_ERR_BOUNDS);
+    return;
+  }
+  const int n_chunks = (int)((end - start + C - 1) / C);
+  const int64_t sbase = (int64_t)s + start / C;
+  const uint32_t sb = smem_u32(sm);
+  volatile int *abort_flag = &sh.abort;
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 256);
+      mbar_init(&sh.b2[i], 1);
+      sh.fills[i] = 0;
+    }
+    mbar_init(&sh.ga, 1);
+    mbar_init(&sh.b1, 1);
+    mbar_init(&sh.epa, 128);
+    mbar_init(&sh.epb, 256);
+    sh.abort = 0;
+    sh.mma_bar = nullptr;
+    sh.mma_par = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh.tbase, kScanCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = sh.tbase;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, GDN_ERR_TIMEOUT);
+  };
+
+  if (warp == 8) {
+    // ===================================================== copies
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      for (int ci = 0; ci < n_chunks; ++ci) {
+        const int st = ci & 1;
+        if (ci >= 2 && !mbar_wait_abortable(&sh.empty[st], ((ci - 2) >> 1) & 1, kSpin, abort_flag)) {
+          fail();
+          break;
+        }
+        const int32_t t0 = (int32_t)(start + (int64_t)ci * C);
+        const uint8_t *r = p.rec + ((size_t)(sbase + ci) * p.Hv + h) * p.rec_bytes;
+        uint8_t *sg = sm + st * kStage;
+        uint64_t *fb = &sh.full[st];
+        mbar_arrive_expect_tx(fb, kStageTx);
+        tma_load_3d(sg + ST_AQW, &tm_q, fb, 0, qh, t0);
+        tma_load_3d(sg + ST_AQW + 16384, &tm_q, fb, 64, qh, t0);
+        bulk_load(sg + ST_AQW + 8192, r + REC_NW, 8192, fb);
+        bulk_load(sg + ST_AQW + 24576, r + REC_NW + 8192, 8192, fb);
+        tma_load_3d(sg + ST_K, &tm_k, fb, 0, qh, t0);
+        tma_load_3d(sg + ST_K + 8192, &tm_k, fb, 64, qh, t0);
+        bulk_load(sg + ST_P, r + REC_P, 8192, fb);
+        bulk_load(sg + ST_U, r + REC_U + (size_t)(v0 / VS) * 8192, 8192, fb);
+        bulk_load(sg + ST_VEC, r + REC_VEC, 1024, fb);
+        sh.fills[st] += 1;
+      }
+    }
+  } else if (warp == 9) {
+    // ===================================================== MMAs
+    if (lane == 0) {
+      const uint32_t id_a = idesc_bf16(128, VS, false, true);
+      const uint32_t id_s = idesc_bf16(128, 64, true, true);
+      const uint32_t id_o = idesc_bf16(128, 64, false, true);
+      for (int ci = 0; ci < n_chunks; ++ci) {
+        const int st = ci & 1, ab = ci & 1;
+        if (!mbar_wait_abortable(&sh.full[st], (ci >> 1) & 1, kSpin, abort_flag) ||
+            !mbar_wait_abortable(&sh.epb, ci & 1, kSpin, abort_flag)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sg = sb + st * kStage;
+        // [q; -W] S^T
+#pragma unroll
+        for (int ks = 0; ks < KD / 16; ++ks)
+          umma_bf16(tm + TC_A + ab * 32,
+                    smem_desc(sg + ST_AQW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2),
+                    smem_desc(sb + SC_ST + ks * 1024, 2048, 512, 4), id_a, ks > 0);
+        umma_commit(&sh.ga);
+        sh.mma_bar = &sh.ga;
+        sh.mma_par = ci & 1;
+        if (!mbar_wait_abortable(&sh.epa, ci & 1, kSpin, abort_flag)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        // K^T [dU'_hi | dU'_lo]: the state path
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          umma_bf16(tm + TC_S, smem_desc(sg + ST_K + ks * 2048, 8192, 1024, 2),
+                    smem_desc(sb + SC_DU + ks * 2048, 8192, 1024, 2), id_s, ks > 0);
+        umma_commit(&sh.b1);
+        // [P; -] [U'_hi | U'_lo]: the output path
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          umma_bf16(tm + TC_O + ab * 64, smem_desc(sg + ST_P + ks * 32, 16, 1024, 2),
+                    smem_desc(sb + SC_UP + ab * 8192 + ks * 2048, 8192, 1024, 2), id_o, ks > 0);
+        umma_commit(&sh.b2[ab]);
+        sh.mma_bar = &sh.b2[ab];
+        sh.mma_par = (ci >> 1) & 1;
+      }
+    }
+  } else {
+    // ===================================================== epilogues (warps 0-7)
+    // warp w reads TMEM lanes 32 (w % 4) .. +31 and handles value columns 16 (w / 4) .. +15
+    const int quarter = warp & 3, hc = warp >> 2;
+    const uint32_t lq = (uint32_t)(quarter * 32) << 16;
+    const int f = quarter * 32 + lane;  // key feature of this thread's state row
+    const int cb = hc * 16;             // first value column of this thread (inside the block)
+    float S[16];
+    {
+      const float *h0p = p.h0 ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0 + cb) * KD + f : nullptr;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) S[j] = h0p ? h0p[(size_t)j * KD] : 0.f;
+    }
+    auto write_state = [&]() {
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+        *reinterpret_cast<uint4 *>(sm + SC_ST + sw64_off(f, cb + 8 * m)) =
+            make_uint4(pack_bf16(S[8 * m], S[8 * m + 1]), pack_bf16(S[8 * m + 2], S[8 * m + 3]),
+                       pack_bf16(S[8 * m + 4], S[8 * m + 5]), pack_bf16(S[8 * m + 6], S[8 * m + 7]));
+    };
+    write_state();
+    fence_proxy_async_smem();
+    mbar_arrive(&sh.epb);
+    const size_t o_tok = (size_t)p.Hv * p.V;
+    bool ok = true;
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int st = ci & 1, ab = ci & 1;
+      const uint8_t *sg = sm + st * kStage;
+      const float *vec = reinterpret_cast<const float *>(sg + ST_VEC);
+      if (!warp_wait(&sh.full[st], (ci >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (quarter >= 2) {
+        // ---- U' = U - W S^T for tokens i (lanes 64-127); hi/lo and diag(d/|k|) hi/lo tiles
+        if (!warp_wait(&sh.ga, ci & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int i = (quarter - 2) * 32 + lane;
+        float a[16];
+        tmem_ld16(tm + lq + TC_A + ab * 32 + cb, a);
+        const float4 *ur = reinterpret_cast<const float4 *>(sg + ST_U + i * 128 + cb * 4);
+        float u[16];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 t = ur[m];
+          u[4 * m] = t.x;
+          u[4 * m + 1] = t.y;
+          u[4 * m + 2] = t.z;
+          u[4 * m + 3] = t.w;
+        }
+        const float dk = vec[VEC_DK + i];
+        tmem_wait_ld();
+        uint32_t uh[8], ul[8], dh[8], dl[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x0 = a[2 * e] + u[2 * e], x1 = a[2 * e + 1] + u[2 * e + 1];
+          const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+          const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+          uh[e] = pack_bf16(h0, h1);
+          ul[e] = pack_bf16(x0 - h0, x1 - h1);
+          const float y0 = dk * x0, y1 = dk * x1;
+          const float k0 = __bfloat162float(__float2bfloat16_rn(y0));
+          const float k1 = __bfloat162float(__float2bfloat16_rn(y1));
+          dh[e] = pack_bf16(k0, k1);
+          dl[e] = pack_bf16(y0 - k0, y1 - k1);
+        }
+        uint8_t *up = sm + SC_UP + ab * 8192;
+        uint8_t *du = sm + SC_DU;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t oh = sw128_off(i, cb + 8 * m), ol = sw128_off(i, 32 + cb + 8 * m);
+          *reinterpret_cast<uint4 *>(up + oh) = make_uint4(uh[4 * m], uh[4 * m + 1], uh[4 * m + 2], uh[4 * m + 3]);
+          *reinterpret_cast<uint4 *>(up + ol) = make_uint4(ul[4 * m], ul[4 * m + 1], ul[4 * m + 2], ul[4 * m + 3]);
+          *reinterpret_cast<uint4 *>(du + oh) = make_uint4(dh[4 * m], dh[4 * m + 1], dh[4 * m + 2], dh[4 * m + 3]);
+          *reinterpret_cast<uint4 *>(du + ol) = make_uint4(dl[4 * m], dl[4 * m + 1], dl[4 * m + 2], dl[4 * m + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sh.epa);
+      }
+      // ---- S <- b_last S + dS (fp32), and its bf16 copy for the next chunk's MMAs
+      if (!warp_wait(&sh.b1, ci & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        float dh[16], dl[16];
+        tmem_ld16(tm + lq + TC_S + cb, dh);
+        tmem_ld16(tm + lq + TC_S + 32 + cb, dl);
+        const float bl = vec[VEC_BLAST];
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[j] = fmaf(bl, S[j], dh[j] + dl[j]);
+        write_state();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sh.epb);
+      }
+      if (quarter < 2) {
+        // ---- o = alpha (q S^T) + P U' + diag(P) U' for tokens i (lanes 0-63)
+        if (!warp_wait(&sh.b2[ab], (ci >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int i = quarter * 32 + lane;
+        float qs[16], ph[16], pl[16];
+        tmem_ld16(tm + lq + TC_A + ab * 32 + cb, qs);
+        tmem_ld16(tm + lq + TC_O + ab * 64 + cb, ph);
+        tmem_ld16(tm + lq + TC_O + ab * 64 + 32 + cb, pl);
+        const uint8_t *up = sm + SC_UP + ab * 8192;
+        float uo[16];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint4 hv = *reinterpret_cast<const uint4 *>(up + sw128_off(i, cb + 8 * m));
+          const uint4 lv = *reinterpret_cast<const uint4 *>(up + sw128_off(i, 32 + cb + 8 * m));
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, lw[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = unpack_bf16(hw[e]), b = unpack_bf16(lw[e]);
+            uo[8 * m + 2 * e] = a.x + b.x;
+            uo[8 * m + 2 * e + 1] = a.y + b.y;
+          }
+        }
+        const float al = vec[VEC_ALPHA + i], pd = vec[VEC_PDIAG + i];
+        const int64_t t0 = start + (int64_t)ci * C;
+        const int nv = (int)min((int64_t)C, end - t0);
+        tmem_wait_ld();
+        float ov[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ov[j] = fmaf(al, qs[j], fmaf(pd, uo[j], ph[j] + pl[j]));
+        if (i < nv) {
+          const size_t off = (size_t)(t0 + i) * o_tok + (size_t)h * p.V + v0 + cb;
+          if (p.o_f32) {
+            float4 *dst = reinterpret_cast<float4 *>((float *)p.o + off);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) dst[m] = make_float4(ov[4 * m], ov[4 * m + 1], ov[4 * m + 2], ov[4 * m + 3]);
+          } else {
+            uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)p.o + off);
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+              dst[m] = make_uint4(pack_bf16(ov[8 * m], ov[8 * m + 1]), pack_bf16(ov[8 * m + 2], ov[8 * m + 3]),
+                                  pack_bf16(ov[8 * m + 4], ov[8 * m + 5]), pack_bf16(ov[8 * m + 6], ov[8 * m + 7]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.empty[st]);
+    }
+    if (!ok && lane == 0) fail();
+    if (ok && p.hT) {
+      float *dst = p.hT + (((size_t)s * p.Hv + h) * p.V + v0 + cb) * KD + f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) dst[(size_t)j * KD] = S[j];
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && sh.abort) {
+    // copies and MMAs still in flight land before shared memory and TMEM are released
+    for (int i = 0; i < 2; ++i)
+      if (sh.fills[i] > 0) (void)mbar_wait(&sh.full[i], (sh.fills[i] - 1) & 1, kSpin);
+    if (sh.mma_bar) (void)mbar_wait(sh.mma_bar, sh.mma_par, kSpin);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tm, kScanCols);
+}
+
+// ============================================================ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [n_tok][heads][128] bf16 map with token stride `tok_stride` elements; 64 x 64 boxes, SW128.
+bool make_qk_map(CUtensorMap *m, const void *base, int heads, int64_t n_tok, int64_t tok_stride) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)heads, (cuuint64_t)n_tok};
+  cuuint64_t strides[2] = {(cuuint64_t)KD * 2, (cuuint64_t)tok_stride * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int V>
+gdn_status launch_operands(const OpParams &op, size_t slots, cudaStream_t st) {
+  const size_t smem = op_smem(V);
+  if (cudaFuncSetAttribute(chunk_operand_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  const size_t blocks = slots * (size_t)op.Hv;
+  if (blocks > 2147483647ULL) return GDN_ERR_UNSUPPORTED;
+  chunk_operand_kernel<V><<<(unsigned)blocks, 128, smem, st>>>(op);
+  return launch_status();
+}
+
+}  // namespace
+
+namespace gdn {
+
+// The split path handles bf16, K = 128 and V a multiple of 64 up to 256.
+bool chunk_scan_supported(const void *q, const void *k, const void *v, const gdn_shape &sh) {
+  if (sh.dtype != GDN_BF16 || sh.K != KD || sh.V % 64 != 0 || sh.V > 256) return false;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return false;
+  if ((sh.q_stride * 2) % 16 || (sh.k_stride * 2) % 16 || (sh.v_stride * 2) % 16) return false;
+  const int64_t n_tok = (int64_t)sh.B * sh.T;
+  return n_tok < (1LL << 31);
+}
+
+size_t chunk_scan_workspace_bytes(const gdn_shape &sh, int64_t n_tok) {
+  return kHeader + n_slots(n_tok, sh.n_seqs) * (size_t)sh.Hv * rec_bytes(sh.V);
+}
+
+gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *h0, const int32_t *cu,
+                          const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
+                          void *workspace, size_t ws_bytes, cudaStream_t st) {
+  const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
+  const int n_seqs = sh.n_seqs;
+  const size_t slots = n_slots(n_tok, n_seqs);
+  if (ws_bytes < chunk_scan_workspace_bytes(sh, n_tok)) return GDN_ERR_WORKSPACE;
+  int32_t *status = (int32_t *)workspace;
+  OpParams op{};
+  op.q = (const __nv_bfloat16 *)q;
+  op.k = (const __nv_bfloat16 *)k;
+  op.v = (const __nv_bfloat16 *)v;
+  op.qs = sh.q_stride;
+  op.ks = sh.k_stride;
+  op.vs = sh.v_stride;
+  op.g = g;
+  op.beta = beta;
+  op.cu = cu;
+  op.row_T = sh.T;
+  op.n_tok = n_tok;
+  op.n_seqs = n_seqs;
+  op.Hqk = sh.Hqk;
+  op.Hv = sh.Hv;
+  op.l2norm = (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0;
+  op.scale = scale;
+  op.rec = (uint8_t *)workspace + kHeader;
+  op.rec_bytes = rec_bytes(sh.V);
+  op.status = status;
+  gdn_status r;
+  switch (sh.V) {
+    case 64: r = launch_operands<64>(op, slots, st); break;
+    case 128: r = launch_operands<128>(op, slots, st); break;
+    case 192: r = launch_operands<192>(op, slots, st); break;
+    case 256: r = launch_operands<256>(op, slots, st); break;
+    default: return GDN_ERR_UNSUPPORTED;
+  }
+  if (r != GDN_OK) return r;
+  CUtensorMap mq, mk;
+  if (!make_qk_map(&mq, q, sh.Hqk, n_tok, sh.q_stride) || !make_qk_map(&mk, k, sh.Hqk, n_tok, sh.k_stride))
+    return GDN_ERR_CUDA;
+  ScanParams sp{};
+  sp.cu = cu;
+  sp.row_T = sh.T;
+  sp.n_tok = n_tok;
+  sp.Hqk = sh.Hqk;
+  sp.Hv = sh.Hv;
+  sp.V = sh.V;
+  sp.h0 = h0;
+  sp.rec = op.rec;
+  sp.rec_bytes = op.rec_bytes;
+  sp.o = o;
+  sp.o_f32 = (flags & GDN_FLAG_O_F32) ? 1 : 0;
+  sp.hT = h_T;
+  sp.status = status;
+  if (cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kScanSmem) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  chunk_scan_kernel<<<dim3(sh.V / VS, sh.Hv, n_seqs), NTS, kScanSmem, st>>>(mq, mk, sp);
+  return launch_status();
+}
+
+}  // namespace gdn

@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "sm100.cuh"
+#include "chunk_common.cuh"
 
 using namespace gdn;
 using namespace gdn::sm100;
@@ -56,33 +57,6 @@ constexpr uint32_t kSpin = 1u << 22;  // bounded waits (~0.2 s) before reporting
 constexpr size_t kWsHeader = 256;
 constexpr int kTPacked = C * (C + 1) / 2;                  // 2080 floats
 constexpr size_t kTBytes = (size_t)kTPacked * sizeof(float);  // 8320 bytes, a multiple of 16
-
-inline size_t n_slots(int64_t n_tok, int n_seqs) { return (size_t)n_seqs + (size_t)((n_tok + C - 1) / C); }
-
-__device__ __forceinline__ void seq_range(const int32_t *cu, int64_t row_T, int s, int64_t &start,
-                                          int64_t &end) {
-  if (cu) {
-    start = cu[s];
-    end = cu[s + 1];
-  } else {
-    start = (int64_t)s * row_T;
-    end = start + row_T;
-  }
-}
-
-__device__ __forceinline__ int64_t slot_base(const int32_t *cu, int64_t row_T, int s) {
-  const int64_t st = cu ? (int64_t)cu[s] : (int64_t)s * row_T;
-  return (int64_t)s + st / C;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&u);
-  return __bfloat1622float2(h);
-}
 
 // ============================================================ prep kernel
 

@@ -16,8 +16,10 @@ namespace {
 
 // Scratch for gdn_chunk_fwd_noalloc: 16 MiB, held by every GPU that loads the
 // library until the process exits.  On the tensor-core path (bf16, K = 128)
-// this bounds the problem size: 256 + 8320 * Hv * (n_seqs + ceil(tokens / 64))
-// bytes must fit, e.g. 2048 tokens x 32 v-heads, or 8192 tokens x 8 v-heads.
+// this bounds the problem size: the compact workspace, 256 + 8320 * Hv *
+// (n_seqs + ceil(tokens / 64)) bytes, must fit, e.g. 2048 tokens x 32 v-heads
+// or 8192 tokens x 8 v-heads.  gdn_chunk_fwd then takes the path that fits in
+// 16 MiB: the split operand/scan kernels for small shapes, else the compact pair.
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -48,7 +50,7 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const 
                                             const int32_t *cu_seqlens, const gdn_shape *shape,
                                             float scale, uint32_t flags, void *o, float *h_T,
                                             void *stream) {
-  const size_t need = gdn_chunk_fwd_workspace_bytes(shape);
+  const size_t need = gdn_chunk_fwd_min_workspace_bytes(shape);
   if (need == 0) return GDN_ERR_INVALID_ARG;          // bad shape (same checks as gdn_chunk_fwd)
   if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;  // beyond the fixed scratch
   void *scratch = nullptr;

@@ -78,9 +78,19 @@ const char *gdn_status_string(int status);
 /* ABI version: (major << 16) | minor. */
 int32_t gdn_version(void);
 
-/* Number of bytes of device workspace gdn_chunk_fwd needs for `shape`
- * (at least 256: the status word and padding).  0 on a bad shape. */
+/* Number of bytes of device workspace gdn_chunk_fwd needs for `shape` on its
+ * fastest path (at least 256: the status word and padding).  0 on a bad shape.
+ * On the tensor-core path (bf16, K = 128, V a multiple of 64 up to 256) this
+ * holds one operand record per chunk and v-head: 256 + (n_seqs +
+ * ceil(tokens / 64)) * Hv * (25600 + 256 V) bytes. */
 size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape);
+
+/* The smallest workspace gdn_chunk_fwd accepts for `shape`.  Between this and
+ * gdn_chunk_fwd_workspace_bytes the tensor-core path keeps only T of every
+ * chunk (256 + 8320 * Hv * (n_seqs + ceil(tokens / 64)) bytes) and rebuilds the
+ * other operands inside its scan kernel: same results, slower.  0 on a bad
+ * shape. */
+size_t gdn_chunk_fwd_min_workspace_bytes(const gdn_shape *shape);
 
 /* Zero the status word at the start of `workspace` (stream-ordered). */
 gdn_status gdn_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
@@ -142,10 +152,11 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
  * without the workspace: the scratch lives in a 16 MiB file-scope device
  * array inside libgdn, held by every GPU that loads the library until the
  * process exits.  The call allocates nothing.
- *  - Size limit: the scratch gdn_chunk_fwd_workspace_bytes(shape) reports must
- *    fit in 16 MiB; larger shapes return GDN_ERR_WORKSPACE before anything runs
- *    (on the bf16, K = 128 path that is 256 + 8320 * Hv * (n_seqs + ceil(tokens/64))
- *    bytes, e.g. 2048 tokens x 32 v-heads or 8192 tokens x 8 v-heads).
+ *  - Size limit: gdn_chunk_fwd_min_workspace_bytes(shape) must fit in 16 MiB;
+ *    larger shapes return GDN_ERR_WORKSPACE before anything runs (on the bf16,
+ *    K = 128 path that is 256 + 8320 * Hv * (n_seqs + ceil(tokens/64)) bytes,
+ *    e.g. 2048 tokens x 32 v-heads or 8192 tokens x 8 v-heads).  Shapes whose
+ *    gdn_chunk_fwd_workspace_bytes also fits take the faster path.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress); make that first call
  *    before any stream capture.
