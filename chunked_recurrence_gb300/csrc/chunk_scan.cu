@@ -23,6 +23,7 @@
 //   [Q; -W] S^T                   (M = 128: raw q rows, then -W rows)
 //   K^T [dU'_hi | dU'_lo]         (M = 128 key features, N = 2 x 32)
 //   [P; -] [U'_hi | U'_lo]        (rows 0-63 used)
+// Operands of three chunks are in flight (TMA and bulk copies) ahead of the scan.
 // with the fp32 state in registers (one key feature per thread) and a bf16
 // copy of S^T in shared memory as the MMA operand.
 //
@@ -72,43 +73,134 @@ struct OpParams {
   int32_t *status;
 };
 
-constexpr int kXP = C + 4;  // fp32 row of A / T, padded (rows stay 16-byte aligned)
-constexpr uint32_t OP_KQ = 0;      // [2 halves][128 rows][128 B]: rows 0-63 raw k, 64-127 raw q
+constexpr int kXP = C + 4;  // fp32 row of A, padded (rows stay 16-byte aligned)
+constexpr uint32_t OP_KQ = 0;      // [2 halves][128 rows][128 B]: rows 0-63 raw k, 64-127 raw q;
+                                   // once Q K^T is done, T hi and T lo take the q rows' places
+constexpr uint32_t OP_TH = 8192, OP_TL = 24576;
 constexpr uint32_t OP_VT = 32768;  // raw v: [V / 64 blocks][64 tokens][128 B], SW128
+// A, then (I + A)^-1 in place, then the T diag(b/|k|) hi / lo tiles
 __host__ __device__ constexpr uint32_t op_x(int V) { return OP_VT + (uint32_t)V * 128; }
-__host__ __device__ constexpr uint32_t op_tt(int V) { return op_x(V) + 18432; }  // 64 x kXP floats
-// T hi, T lo, T diag(b/|k|) hi, lo: 4 x [64 rows][128 B] SW128
-__host__ __device__ constexpr uint32_t op_smem(int V) { return op_tt(V) + 32768 + 1024; }
+__host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + 18432 + 1024; }
 
-// Column lt (>= R0) of X = (I + A)^-1 by forward substitution, held in registers:
-// x_r = delta_r,lt - sum_{j<r} A_rj x_j.  Every lane walks the same (r, j) sequence, so
-// the A_rj reads are warp-wide broadcasts; all columns of the warp are >= R0, so rows
-// and terms below R0 are zero and skipped.
-template <int R0>
-__device__ __forceinline__ void solve_column(const float *X, int lt, float (&x)[C]) {
+// Y = (I + A)^-1 for the strictly lower 64 x 64 A held in X (fp32, row stride kXP), in
+// place, by 16 x 16 blocks: the diagonal blocks by forward substitution, then the
+// blocks below them one block-diagonal d = I - J at a time,
+//   Y_IJ = -Y_II sum_{K=J}^{I-1} A_IK Y_KJ.
+// A's blocks below the diagonal stay in place (later sums read them); Y_II replaces
+// A_II, and Y_IJ (J < I) is kept in the unused upper block (J, I), so Y_KJ (K >= J) is
+// X[16 J + m][16 K + c] in every case.  A 16 x 16 result is computed by 16 threads,
+// each a 4 x 4 tile in registers.
+__device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
+  float y[16];
+  const int b = (tid >> 4) * 16, cc = tid & 15;
+  if (tid < C) {
 #pragma unroll
-  for (int r = 0; r < C; ++r) x[r] = 0.f;
-  x[R0] = (lt == R0) ? 1.f : 0.f;
+    for (int r = 0; r < 16; ++r) {
+      const float4 *ar = reinterpret_cast<const float4 *>(X + (b + r) * kXP + b);
+      float acc = 0.f;
 #pragma unroll
-  for (int r = R0 + 1; r < C; ++r) {
-    const float4 *Ar = reinterpret_cast<const float4 *>(X + r * kXP);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int j = R0; j < r; j += 4) {
-      const float4 a = Ar[j >> 2];
-      a0 = fmaf(a.x, x[j], a0);
-      if (j + 1 < r) a1 = fmaf(a.y, x[j + 1], a1);
-      if (j + 2 < r) a2 = fmaf(a.z, x[j + 2], a2);
-      if (j + 3 < r) a3 = fmaf(a.w, x[j + 3], a3);
+      for (int j4 = 0; j4 < 4; ++j4) {
+        if (4 * j4 < r) {
+          const float4 a = ar[j4];
+          acc = fmaf(a.x, y[4 * j4], acc);
+          if (4 * j4 + 1 < r) acc = fmaf(a.y, y[4 * j4 + 1], acc);
+          if (4 * j4 + 2 < r) acc = fmaf(a.z, y[4 * j4 + 2], acc);
+          if (4 * j4 + 3 < r) acc = fmaf(a.w, y[4 * j4 + 3], acc);
+        }
+      }
+      y[r] = (r == cc) ? 1.f : -acc;  // rows above cc sum only zeros
     }
-    x[r] = (r == lt) ? 1.f : -((a0 + a1) + (a2 + a3));
+  }
+  __syncthreads();  // every read of A_II is done
+  if (tid < C) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) X[(b + r) * kXP + b + cc] = y[r];
+  }
+  __syncthreads();
+  const int t = tid & 15, tr = (t >> 2) * 4, tc = (t & 3) * 4;
+#pragma unroll 1
+  for (int d = 1; d < 4; ++d) {
+    const bool act = tid < 16 * (4 - d);
+    const int I = d + (tid >> 4), J = I - d;
+    float z[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
+    if (act) {
+#pragma unroll 1
+      for (int K = J; K < I; ++K) {
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          float4 a[4], yv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            a[i] = *reinterpret_cast<const float4 *>(X + (16 * I + tr + i) * kXP + 16 * K + 4 * m4);
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm)
+            yv[mm] = *reinterpret_cast<const float4 *>(X + (16 * J + 4 * m4 + mm) * kXP + 16 * K + tc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+              z[i][0] = fmaf(ai[mm], yv[mm].x, z[i][0]);
+              z[i][1] = fmaf(ai[mm], yv[mm].y, z[i][1]);
+              z[i][2] = fmaf(ai[mm], yv[mm].z, z[i][2]);
+              z[i][3] = fmaf(ai[mm], yv[mm].w, z[i][3]);
+            }
+          }
+        }
+      }
+      // the sum goes to block (J, I), which no sum of this block-diagonal reads
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(X + (16 * J + tr + i) * kXP + 16 * I + tc) =
+            make_float4(z[i][0], z[i][1], z[i][2], z[i][3]);
+    }
+    __syncthreads();
+    if (act) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
+#pragma unroll
+      for (int m4 = 0; m4 < 4; ++m4) {
+        float4 a[4], zv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          a[i] = *reinterpret_cast<const float4 *>(X + (16 * I + tr + i) * kXP + 16 * I + 4 * m4);
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm)
+          zv[mm] = *reinterpret_cast<const float4 *>(X + (16 * J + 4 * m4 + mm) * kXP + 16 * I + tc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            z[i][0] = fmaf(ai[mm], zv[mm].x, z[i][0]);
+            z[i][1] = fmaf(ai[mm], zv[mm].y, z[i][1]);
+            z[i][2] = fmaf(ai[mm], zv[mm].z, z[i][2]);
+            z[i][3] = fmaf(ai[mm], zv[mm].w, z[i][3]);
+          }
+        }
+      }
+    }
+    __syncthreads();  // every thread has read its sums: Y_IJ replaces them
+    if (act) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(X + (16 * J + tr + i) * kXP + 16 * I + tc) =
+            make_float4(-z[i][0], -z[i][1], -z[i][2], -z[i][3]);
+    }
+    __syncthreads();
   }
 }
 
 template <int V>
 __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
   constexpr int NVB = V / 64;                       // 64-column blocks of v
-  constexpr uint32_t kCols = (128 + V <= 256) ? 256u : 512u;
+  constexpr uint32_t kCols = (V <= 128) ? 128u : 256u;
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   __shared__ float gam[C], bex[C], dec[C], alf[C + 1], kinv[C], qinv[C], bet[C];
@@ -138,7 +230,6 @@ __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
   uint8_t *rec = p.rec + ((size_t)slot * p.Hv + h) * p.rec_bytes;
   float *vec = reinterpret_cast<float *>(rec + REC_VEC);
   float *X = reinterpret_cast<float *>(sm + op_x(V));
-  uint8_t *TT = sm + op_tt(V);
 
   // ---- raw k, q and v rows (two threads per token) into swizzled tiles; gates; norms
   {
@@ -298,31 +389,36 @@ __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
     }
   }
   __syncthreads();
-  // ---- T = (I + A)^-1 diag(beta): one column per thread of warps 0-1
-  float x[C];
-  if (warp == 0) solve_column<0>(X, tid, x);
-  else if (warp == 1) solve_column<32>(X, tid, x);
-  __syncthreads();  // every read of A is done: T overwrites it
-  if (warp < 2) {
-    const float bl = bet[tid];
-#pragma unroll
-    for (int r = 0; r < C; ++r) X[r * kXP + tid] = (r >= tid) ? x[r] * bl : 0.f;
-  }
-  __syncthreads();
-  // ---- T and T diag(b/|k|) as bf16 hi/lo K-major tiles (row r, columns cb..cb+31)
+  // ---- T = (I + A)^-1 diag(beta)
+  invert_unit_lower(X, tid);
+  // ---- T and T diag(b/|k|) as bf16 hi/lo K-major tiles (row r, columns cb..cb+31): T's
+  //      tiles replace the raw q rows (Q K^T no longer needs them), T diag(b/|k|)'s tiles
+  //      replace A once every thread has read its row of the inverse
   {
-    const int r = tid >> 1, cb = (tid & 1) * 32;
+    const int r = tid >> 1, cb = (tid & 1) * 32, I = r >> 4;
     float t[32], cf[32];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float4 a = reinterpret_cast<const float4 *>(X + r * kXP + cb)[m];
-      t[4 * m] = a.x;
-      t[4 * m + 1] = a.y;
-      t[4 * m + 2] = a.z;
-      t[4 * m + 3] = a.w;
+    for (int g16 = 0; g16 < 2; ++g16) {
+      const int J = (cb >> 4) + g16;
+      // row r of Y_IJ: the diagonal block in place, blocks left of it in upper block (J, I)
+      const float *src = (J == I) ? X + r * kXP + 16 * J : X + (16 * J + (r & 15)) * kXP + 16 * I;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 a = (J <= I) ? reinterpret_cast<const float4 *>(src)[m] : make_float4(0.f, 0.f, 0.f, 0.f);
+        t[16 * g16 + 4 * m] = a.x;
+        t[16 * g16 + 4 * m + 1] = a.y;
+        t[16 * g16 + 4 * m + 2] = a.z;
+        t[16 * g16 + 4 * m + 3] = a.w;
+      }
     }
 #pragma unroll
-    for (int u = 0; u < 32; ++u) cf[u] = bex[cb + u] * kinv[cb + u];
+    for (int u = 0; u < 32; ++u) {
+      const float bu = bet[cb + u];
+      t[u] = (cb + u <= r) ? t[u] * bu : 0.f;
+      cf[u] = bex[cb + u] * kinv[cb + u];
+    }
+    __syncthreads();  // X is free
+    uint8_t *TP = reinterpret_cast<uint8_t *>(X);
 #pragma unroll
     for (int q8 = 0; q8 < 4; ++q8) {
       uint32_t wh[4], wl[4], xh[4], xl[4];
@@ -341,81 +437,93 @@ __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
         xl[e] = pack_bf16(u_0 - g0, u_1 - g1);
       }
       const uint32_t off = sw128_off(r, cb + q8 * 8);
-      *reinterpret_cast<uint4 *>(TT + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-      *reinterpret_cast<uint4 *>(TT + 8192 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-      *reinterpret_cast<uint4 *>(TT + 16384 + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-      *reinterpret_cast<uint4 *>(TT + 24576 + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
+      *reinterpret_cast<uint4 *>(sm + OP_TH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+      *reinterpret_cast<uint4 *>(sm + OP_TL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      *reinterpret_cast<uint4 *>(TP + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
+      *reinterpret_cast<uint4 *>(TP + 8192 + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
     }
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // ---- W = T diag(b/|k|) K (TMEM columns 0-127) and U = T V (columns 128..128+V), hi + lo
-  if (tid == 0) {
-    const uint32_t tt_a = smem_u32(TT), vt_a = smem_u32(sm + OP_VT);
-    const uint32_t id_w = idesc_bf16(64, 128, false, true);
-    const uint32_t id_u = idesc_bf16(64, V, false, true);
+  // ---- W = T diag(b/|k|) K, then U = T V, each hi + lo, in the same TMEM columns
+  const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
+  const int rr = warp * 16 + lane;  // rows of an M = 64 result sit in lanes 0-15 of a quarter
+  const bool has_row = lane < 16;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (tid == 0) {
+      if (pass == 0) {
+        const uint32_t tp_a = smem_u32(X);
+        const uint32_t id_w = idesc_bf16(64, 128, false, true);
 #pragma unroll
-    for (int ks = 0; ks < C / 16; ++ks) {
-      const uint64_t kb = smem_desc(kq_a + ks * 2048, 16384, 1024, 2);
-      const uint64_t vb = smem_desc(vt_a + ks * 2048, 8192, 1024, 2);
-      umma_bf16(tm, smem_desc(tt_a + 16384 + ks * 32, 16, 1024, 2), kb, id_w, ks > 0);
-      umma_bf16(tm, smem_desc(tt_a + 24576 + ks * 32, 16, 1024, 2), kb, id_w, 1);
-      umma_bf16(tm + 128, smem_desc(tt_a + ks * 32, 16, 1024, 2), vb, id_u, ks > 0);
-      umma_bf16(tm + 128, smem_desc(tt_a + 8192 + ks * 32, 16, 1024, 2), vb, id_u, 1);
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t kb = smem_desc(kq_a + ks * 2048, 16384, 1024, 2);
+          umma_bf16(tm, smem_desc(tp_a + ks * 32, 16, 1024, 2), kb, id_w, ks > 0);
+          umma_bf16(tm, smem_desc(tp_a + 8192 + ks * 32, 16, 1024, 2), kb, id_w, 1);
+        }
+      } else {
+        const uint32_t vt_a = smem_u32(sm + OP_VT);
+        const uint32_t id_u = idesc_bf16(64, V, false, true);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t vb = smem_desc(vt_a + ks * 2048, 8192, 1024, 2);
+          umma_bf16(tm, smem_desc(kq_a + OP_TH + ks * 32, 16, 1024, 2), vb, id_u, ks > 0);
+          umma_bf16(tm, smem_desc(kq_a + OP_TL + ks * 32, 16, 1024, 2), vb, id_u, 1);
+        }
+      }
+      umma_commit(&bar);
     }
-    umma_commit(&bar);
-  }
-  {
-    const bool ok = tid != 0 || mbar_wait(&bar, 1, kSpin);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
-      (void)mbar_wait(&bar, 1, kSpin);
-      tc_fence_before();
-      __syncthreads();
-      if (warp == 0) tmem_dealloc(tm, kCols);
-      return;
-    }
-  }
-  tc_fence_after();
-  // ---- drain: rows of an M = 64 result sit in lanes 0-15 of each 32-lane quarter
-  {
-    const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
-    const int r = warp * 16 + lane;
-    const bool has_row = lane < 16;
-    float w64[64];
-#pragma unroll
-    for (int fb = 0; fb < 2; ++fb) {
-      tmem_ld64(tl + fb * 64, w64);
-      tmem_wait_ld();
-      if (has_row) {
-        uint8_t *dst = rec + REC_NW + fb * 8192;
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 8)
-          *reinterpret_cast<uint4 *>(dst + sw128_off(r, c0)) =
-              make_uint4(pack_bf16(-w64[c0], -w64[c0 + 1]), pack_bf16(-w64[c0 + 2], -w64[c0 + 3]),
-                         pack_bf16(-w64[c0 + 4], -w64[c0 + 5]), pack_bf16(-w64[c0 + 6], -w64[c0 + 7]));
+    {
+      const uint32_t par = pass == 0 ? 1u : 0u;  // completions 2 and 3 of the barrier
+      const bool ok = tid != 0 || mbar_wait(&bar, par, kSpin);
+      if (__syncthreads_or(!ok)) {
+        if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
+        (void)mbar_wait(&bar, par, kSpin);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tm, kCols);
+        return;
       }
     }
+    tc_fence_after();
+    float w64[64];
+    if (pass == 0) {  // -W as bf16 K-major images of the two 64-feature halves
 #pragma unroll
-    for (int vb = 0; vb < NVB; ++vb) {
-      tmem_ld64(tl + 128 + vb * 64, w64);
-      tmem_wait_ld();
-      if (has_row) {
+      for (int fb = 0; fb < 2; ++fb) {
+        tmem_ld64(tl + fb * 64, w64);
+        tmem_wait_ld();
+        if (has_row) {
+          uint8_t *dst = rec + REC_NW + fb * 8192;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + (size_t)(2 * vb + half) * 8192 + r * 128);
+          for (int c0 = 0; c0 < 64; c0 += 8)
+            *reinterpret_cast<uint4 *>(dst + sw128_off(rr, c0)) =
+                make_uint4(pack_bf16(-w64[c0], -w64[c0 + 1]), pack_bf16(-w64[c0 + 2], -w64[c0 + 3]),
+                           pack_bf16(-w64[c0 + 4], -w64[c0 + 5]), pack_bf16(-w64[c0 + 6], -w64[c0 + 7]));
+        }
+      }
+    } else {  // U as fp32 32-column slices
 #pragma unroll
-          for (int m = 0; m < 8; ++m)
-            dst[m] = make_float4(w64[half * 32 + 4 * m], w64[half * 32 + 4 * m + 1],
-                                 w64[half * 32 + 4 * m + 2], w64[half * 32 + 4 * m + 3]);
+      for (int vb = 0; vb < NVB; ++vb) {
+        tmem_ld64(tl + vb * 64, w64);
+        tmem_wait_ld();
+        if (has_row) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + (size_t)(2 * vb + half) * 8192 + rr * 128);
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              dst[m] = make_float4(w64[half * 32 + 4 * m], w64[half * 32 + 4 * m + 1],
+                                   w64[half * 32 + 4 * m + 2], w64[half * 32 + 4 * m + 3]);
+          }
         }
       }
     }
+    tc_fence_before();
+    __syncthreads();  // the columns are free for the next pass
+    tc_fence_after();
   }
-  tc_fence_before();
-  __syncthreads();
   if (warp == 0) tmem_dealloc(tm, kCols);
 }
 
@@ -434,7 +542,8 @@ struct ScanParams {
   int32_t *status;
 };
 
-constexpr int NTS = 320;  // warps 0-7 epilogues, warp 8 copies, warp 9 MMAs
+// warps 0-7: state path; 8, 9, 12, 13: outputs; 10: copies; 11: MMAs
+constexpr int NTS = 448;
 // one stage of chunk operands (offsets inside the stage; each stage is 1 KB aligned)
 constexpr uint32_t ST_AQW = 0;      // [2 halves][128 rows][128 B]: rows 0-63 raw q, rows 64-127 -W
 constexpr uint32_t ST_K = 32768;    // [2 halves][64 tokens][128 B] raw k
@@ -444,24 +553,34 @@ constexpr uint32_t ST_U = 57344;    // [64 tokens][32] fp32 U slice
 constexpr uint32_t ST_VEC = 65536;  // alpha, pdiag, dk, b_last, n
 constexpr uint32_t kStage = 66560;
 constexpr uint32_t kStageTx = 16384 + 16384 + 16384 + 8192 + 8192 + 1024;
-constexpr uint32_t SC_ST = 2 * kStage;     // S^T bf16 [128 features][32 values] SW64
-constexpr uint32_t SC_UP = SC_ST + 8192;   // 2 x [U'_hi | U'_lo] [64 tokens][64] SW128
-constexpr uint32_t SC_DU = SC_UP + 16384;  // [dU'_hi | dU'_lo] [64 tokens][64] SW128
+constexpr int kStages = 3;                 // chunks of operands in flight
+constexpr uint32_t SC_ST = kStages * kStage;  // S^T bf16 [128 features][32 values] SW64
+constexpr uint32_t SC_UP = SC_ST + 8192;      // [U'_hi | U'_lo] [64 tokens][64] SW128
+constexpr uint32_t SC_DU = SC_UP + 8192;      // [dU'_hi | dU'_lo] [64 tokens][64] SW128
 constexpr uint32_t kScanSmem = SC_DU + 8192 + 1024;
 // TMEM columns
-constexpr uint32_t TC_A = 0;    // 2 x 32: q S^T in lanes 0-63, -W S^T in lanes 64-127
-constexpr uint32_t TC_O = 64;   // 2 x 64: [P U'_hi | P U'_lo] in lanes 0-63
-constexpr uint32_t TC_S = 192;  // 64: [K^T dU'_hi | K^T dU'_lo], one lane per key feature
+constexpr uint32_t TC_A = 0;    // 3 x 32: q S^T in lanes 0-63, -W S^T in lanes 64-127
+constexpr uint32_t TC_O = 96;   // 64: [P U'_hi | P U'_lo] in lanes 0-63
+constexpr uint32_t TC_S = 160;  // 64: [K^T dU'_hi | K^T dU'_lo], one lane per key feature
 constexpr uint32_t kScanCols = 256;
 
 struct ScanShared {
-  uint64_t full[2], empty[2], ga, b1, b2[2], epa, epb;
+  uint64_t full[kStages], empty[kStages], ga, b1, b2, epa, epa2, epb, outd;
   uint32_t tbase;
   int abort;
-  int fills[2];          // loads issued into each stage
+  int fills[kStages];    // loads issued into each stage
   uint64_t *mma_bar;     // barrier of the last MMA commit and its phase parity
   uint32_t mma_par;
 };
+
+// x0, x1 as a packed bf16 pair (hi) and the packed bf16 pair of what it leaves (lo).
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<uint32_t *>(&h);
+  lo = *reinterpret_cast<uint32_t *>(&l);
+}
 
 // Every lane waits (bounded); the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -489,16 +608,18 @@ __global__ void __launch_bounds__(NTS, 1)
   const uint32_t sb = smem_u32(sm);
   volatile int *abort_flag = &sh.abort;
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.full[i], 1);
-      mbar_init(&sh.empty[i], 256);
-      mbar_init(&sh.b2[i], 1);
+      mbar_init(&sh.empty[i], 384);
       sh.fills[i] = 0;
     }
     mbar_init(&sh.ga, 1);
     mbar_init(&sh.b1, 1);
+    mbar_init(&sh.b2, 1);
     mbar_init(&sh.epa, 128);
+    mbar_init(&sh.epa2, 128);
     mbar_init(&sh.epb, 256);
+    mbar_init(&sh.outd, 128);
     sh.abort = 0;
     sh.mma_bar = nullptr;
     sh.mma_par = 0;
@@ -517,14 +638,14 @@ __global__ void __launch_bounds__(NTS, 1)
     set_status(p.status, GDN_ERR_TIMEOUT);
   };
 
-  if (warp == 8) {
+  if (warp == 10) {
     // ===================================================== copies
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       for (int ci = 0; ci < n_chunks; ++ci) {
-        const int st = ci & 1;
-        if (ci >= 2 && !mbar_wait_abortable(&sh.empty[st], ((ci - 2) >> 1) & 1, kSpin, abort_flag)) {
+        const int st = ci % kStages;
+        if (ci >= kStages && !mbar_wait_abortable(&sh.empty[st], ((ci - kStages) / kStages) & 1, kSpin, abort_flag)) {
           fail();
           break;
         }
@@ -545,53 +666,78 @@ __global__ void __launch_bounds__(NTS, 1)
         sh.fills[st] += 1;
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 11) {
     // ===================================================== MMAs
     if (lane == 0) {
       const uint32_t id_a = idesc_bf16(128, VS, false, true);
       const uint32_t id_s = idesc_bf16(128, 64, true, true);
       const uint32_t id_o = idesc_bf16(128, 64, false, true);
-      for (int ci = 0; ci < n_chunks; ++ci) {
-        const int st = ci & 1, ab = ci & 1;
-        if (!mbar_wait_abortable(&sh.full[st], (ci >> 1) & 1, kSpin, abort_flag) ||
-            !mbar_wait_abortable(&sh.epb, ci & 1, kSpin, abort_flag)) {
-          fail();
+      // descriptors of stage 0; a byte offset moves a descriptor by offset / 16
+      const uint64_t d_aqw = smem_desc(sb + ST_AQW, 16, 1024, 2);
+      const uint64_t d_st = smem_desc(sb + SC_ST, 2048, 512, 4);
+      const uint64_t d_k = smem_desc(sb + ST_K, 8192, 1024, 2);
+      const uint64_t d_du = smem_desc(sb + SC_DU, 8192, 1024, 2);
+      const uint64_t d_p = smem_desc(sb + ST_P, 16, 1024, 2);
+      const uint64_t d_up = smem_desc(sb + SC_UP, 8192, 1024, 2);
+      int outd_seen = 0;  // outputs known to be done; out_done phases are consumed in order
+      auto outputs_done = [&](int need) {
+        while (outd_seen < need) {
+          if (!mbar_wait_abortable(&sh.outd, outd_seen & 1, kSpin, abort_flag)) return false;
+          ++outd_seen;
+        }
+        return true;
+      };
+      // [P; -] [U'_hi | U'_lo] of chunk cj: the output path, one chunk behind the state path
+      auto issue_b2 = [&](int cj) {
+        if (!mbar_wait_abortable(&sh.epa2, cj & 1, kSpin, abort_flag) || !outputs_done(cj)) return false;
+        tc_fence_after();
+        const uint64_t sj = (uint64_t)((cj % kStages) * kStage) >> 4;
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks)
+          umma_bf16(tm + TC_O, d_p + sj + ((ks * 32) >> 4), d_up + ((ks * 2048) >> 4), id_o, ks > 0);
+        umma_commit(&sh.b2);
+        sh.mma_bar = &sh.b2;
+        sh.mma_par = cj & 1;
+        return true;
+      };
+      bool mok = true;
+      for (int ci = 0; ci < n_chunks && mok; ++ci) {
+        const int st = ci % kStages;
+        // chunk ci's operands, the state after chunk ci-1, and the output of chunk ci-3
+        // (whose accumulator columns [q; -W] S^T reuses) done
+        if (!mbar_wait_abortable(&sh.full[st], (ci / kStages) & 1, kSpin, abort_flag) ||
+            !mbar_wait_abortable(&sh.epb, ci & 1, kSpin, abort_flag) || !outputs_done(ci - 2)) {
+          mok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sg = sb + st * kStage;
+        const uint64_t so = (uint64_t)(st * kStage) >> 4;
         // [q; -W] S^T
 #pragma unroll
         for (int ks = 0; ks < KD / 16; ++ks)
-          umma_bf16(tm + TC_A + ab * 32,
-                    smem_desc(sg + ST_AQW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2),
-                    smem_desc(sb + SC_ST + ks * 1024, 2048, 512, 4), id_a, ks > 0);
+          umma_bf16(tm + TC_A + (ci % 3) * 32, d_aqw + so + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                    d_st + ((ks * 1024) >> 4), id_a, ks > 0);
         umma_commit(&sh.ga);
         sh.mma_bar = &sh.ga;
         sh.mma_par = ci & 1;
-        if (!mbar_wait_abortable(&sh.epa, ci & 1, kSpin, abort_flag)) {
-          fail();
+        if ((ci > 0 && !issue_b2(ci - 1)) || !mbar_wait_abortable(&sh.epa, ci & 1, kSpin, abort_flag)) {
+          mok = false;
           break;
         }
         tc_fence_after();
         // K^T [dU'_hi | dU'_lo]: the state path
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
-          umma_bf16(tm + TC_S, smem_desc(sg + ST_K + ks * 2048, 8192, 1024, 2),
-                    smem_desc(sb + SC_DU + ks * 2048, 8192, 1024, 2), id_s, ks > 0);
+          umma_bf16(tm + TC_S, d_k + so + ((ks * 2048) >> 4), d_du + ((ks * 2048) >> 4), id_s, ks > 0);
         umma_commit(&sh.b1);
-        // [P; -] [U'_hi | U'_lo]: the output path
-#pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks)
-          umma_bf16(tm + TC_O + ab * 64, smem_desc(sg + ST_P + ks * 32, 16, 1024, 2),
-                    smem_desc(sb + SC_UP + ab * 8192 + ks * 2048, 8192, 1024, 2), id_o, ks > 0);
-        umma_commit(&sh.b2[ab]);
-        sh.mma_bar = &sh.b2[ab];
-        sh.mma_par = (ci >> 1) & 1;
+        sh.mma_bar = &sh.b1;
+        sh.mma_par = ci & 1;
       }
+      if (mok && n_chunks > 0) mok = issue_b2(n_chunks - 1);
+      if (!mok) fail();
     }
-  } else {
-    // ===================================================== epilogues (warps 0-7)
+  } else if (warp < 8) {
+    // ===================================================== state path (warps 0-7)
     // warp w reads TMEM lanes 32 (w % 4) .. +31 and handles value columns 16 (w / 4) .. +15
     const int quarter = warp & 3, hc = warp >> 2;
     const uint32_t lq = (uint32_t)(quarter * 32) << 16;
@@ -613,61 +759,48 @@ __global__ void __launch_bounds__(NTS, 1)
     write_state();
     fence_proxy_async_smem();
     mbar_arrive(&sh.epb);
-    const size_t o_tok = (size_t)p.Hv * p.V;
     bool ok = true;
     for (int ci = 0; ci < n_chunks; ++ci) {
-      const int st = ci & 1, ab = ci & 1;
+      const int st = ci % kStages;
       const uint8_t *sg = sm + st * kStage;
       const float *vec = reinterpret_cast<const float *>(sg + ST_VEC);
-      if (!warp_wait(&sh.full[st], (ci >> 1) & 1, abort_flag)) {
+      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, abort_flag)) {
         ok = false;
         break;
       }
+      const int i = (quarter - 2) * 32 + lane;  // token of this lane (warps on lanes 64-127)
+      float x[16];
       if (quarter >= 2) {
-        // ---- U' = U - W S^T for tokens i (lanes 64-127); hi/lo and diag(d/|k|) hi/lo tiles
+        // ---- U' = U - W S^T for tokens i: diag(d/|k|) U' hi/lo for the state path
         if (!warp_wait(&sh.ga, ci & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int i = (quarter - 2) * 32 + lane;
-        float a[16];
-        tmem_ld16(tm + lq + TC_A + ab * 32 + cb, a);
+        tmem_ld16(tm + lq + TC_A + (ci % 3) * 32 + cb, x);
         const float4 *ur = reinterpret_cast<const float4 *>(sg + ST_U + i * 128 + cb * 4);
-        float u[16];
+        float4 u4[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 t = ur[m];
-          u[4 * m] = t.x;
-          u[4 * m + 1] = t.y;
-          u[4 * m + 2] = t.z;
-          u[4 * m + 3] = t.w;
-        }
+        for (int m = 0; m < 4; ++m) u4[m] = ur[m];
         const float dk = vec[VEC_DK + i];
         tmem_wait_ld();
-        uint32_t uh[8], ul[8], dh[8], dl[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float x0 = a[2 * e] + u[2 * e], x1 = a[2 * e + 1] + u[2 * e + 1];
-          const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-          const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-          uh[e] = pack_bf16(h0, h1);
-          ul[e] = pack_bf16(x0 - h0, x1 - h1);
-          const float y0 = dk * x0, y1 = dk * x1;
-          const float k0 = __bfloat162float(__float2bfloat16_rn(y0));
-          const float k1 = __bfloat162float(__float2bfloat16_rn(y1));
-          dh[e] = pack_bf16(k0, k1);
-          dl[e] = pack_bf16(y0 - k0, y1 - k1);
+        for (int m = 0; m < 4; ++m) {
+          x[4 * m] += u4[m].x;
+          x[4 * m + 1] += u4[m].y;
+          x[4 * m + 2] += u4[m].z;
+          x[4 * m + 3] += u4[m].w;
         }
-        uint8_t *up = sm + SC_UP + ab * 8192;
+        uint32_t dh[8], dl[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split_bf16(dk * x[2 * e], dk * x[2 * e + 1], dh[e], dl[e]);
         uint8_t *du = sm + SC_DU;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          const uint32_t oh = sw128_off(i, cb + 8 * m), ol = sw128_off(i, 32 + cb + 8 * m);
-          *reinterpret_cast<uint4 *>(up + oh) = make_uint4(uh[4 * m], uh[4 * m + 1], uh[4 * m + 2], uh[4 * m + 3]);
-          *reinterpret_cast<uint4 *>(up + ol) = make_uint4(ul[4 * m], ul[4 * m + 1], ul[4 * m + 2], ul[4 * m + 3]);
-          *reinterpret_cast<uint4 *>(du + oh) = make_uint4(dh[4 * m], dh[4 * m + 1], dh[4 * m + 2], dh[4 * m + 3]);
-          *reinterpret_cast<uint4 *>(du + ol) = make_uint4(dl[4 * m], dl[4 * m + 1], dl[4 * m + 2], dl[4 * m + 3]);
+          *reinterpret_cast<uint4 *>(du + sw128_off(i, cb + 8 * m)) =
+              make_uint4(dh[4 * m], dh[4 * m + 1], dh[4 * m + 2], dh[4 * m + 3]);
+          *reinterpret_cast<uint4 *>(du + sw128_off(i, 32 + cb + 8 * m)) =
+              make_uint4(dl[4 * m], dl[4 * m + 1], dl[4 * m + 2], dl[4 * m + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -692,53 +825,25 @@ __global__ void __launch_bounds__(NTS, 1)
         tc_fence_before();
         mbar_arrive(&sh.epb);
       }
-      if (quarter < 2) {
-        // ---- o = alpha (q S^T) + P U' + diag(P) U' for tokens i (lanes 0-63)
-        if (!warp_wait(&sh.b2[ab], (ci >> 1) & 1, abort_flag)) {
+      if (quarter >= 2) {
+        // ---- U' hi/lo for the output path, once the previous chunk's output has read its tile
+        if (ci > 0 && !warp_wait(&sh.outd, (ci - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const int i = quarter * 32 + lane;
-        float qs[16], ph[16], pl[16];
-        tmem_ld16(tm + lq + TC_A + ab * 32 + cb, qs);
-        tmem_ld16(tm + lq + TC_O + ab * 64 + cb, ph);
-        tmem_ld16(tm + lq + TC_O + ab * 64 + 32 + cb, pl);
-        const uint8_t *up = sm + SC_UP + ab * 8192;
-        float uo[16];
+        uint32_t uh[8], ul[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split_bf16(x[2 * e], x[2 * e + 1], uh[e], ul[e]);
+        uint8_t *up = sm + SC_UP;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          const uint4 hv = *reinterpret_cast<const uint4 *>(up + sw128_off(i, cb + 8 * m));
-          const uint4 lv = *reinterpret_cast<const uint4 *>(up + sw128_off(i, 32 + cb + 8 * m));
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, lw[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 a = unpack_bf16(hw[e]), b = unpack_bf16(lw[e]);
-            uo[8 * m + 2 * e] = a.x + b.x;
-            uo[8 * m + 2 * e + 1] = a.y + b.y;
-          }
+          *reinterpret_cast<uint4 *>(up + sw128_off(i, cb + 8 * m)) =
+              make_uint4(uh[4 * m], uh[4 * m + 1], uh[4 * m + 2], uh[4 * m + 3]);
+          *reinterpret_cast<uint4 *>(up + sw128_off(i, 32 + cb + 8 * m)) =
+              make_uint4(ul[4 * m], ul[4 * m + 1], ul[4 * m + 2], ul[4 * m + 3]);
         }
-        const float al = vec[VEC_ALPHA + i], pd = vec[VEC_PDIAG + i];
-        const int64_t t0 = start + (int64_t)ci * C;
-        const int nv = (int)min((int64_t)C, end - t0);
-        tmem_wait_ld();
-        float ov[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) ov[j] = fmaf(al, qs[j], fmaf(pd, uo[j], ph[j] + pl[j]));
-        if (i < nv) {
-          const size_t off = (size_t)(t0 + i) * o_tok + (size_t)h * p.V + v0 + cb;
-          if (p.o_f32) {
-            float4 *dst = reinterpret_cast<float4 *>((float *)p.o + off);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) dst[m] = make_float4(ov[4 * m], ov[4 * m + 1], ov[4 * m + 2], ov[4 * m + 3]);
-          } else {
-            uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)p.o + off);
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-              dst[m] = make_uint4(pack_bf16(ov[8 * m], ov[8 * m + 1]), pack_bf16(ov[8 * m + 2], ov[8 * m + 3]),
-                                  pack_bf16(ov[8 * m + 4], ov[8 * m + 5]), pack_bf16(ov[8 * m + 6], ov[8 * m + 7]));
-          }
-        }
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.epa2);
       }
       tc_fence_before();
       mbar_arrive(&sh.empty[st]);
@@ -749,11 +854,73 @@ __global__ void __launch_bounds__(NTS, 1)
 #pragma unroll
       for (int j = 0; j < 16; ++j) dst[(size_t)j * KD] = S[j];
     }
+  } else {
+    // ===================================================== outputs (warps 8, 9, 12, 13)
+    // o = alpha (q S^T) + P U' + diag(P) U' for tokens i = lanes 0-63
+    const int quarter = warp & 3, hc = (warp >> 2) & 1;
+    const uint32_t lq = (uint32_t)(quarter * 32) << 16;
+    const int cb = hc * 16;
+    const int i = quarter * 32 + lane;
+    const size_t o_tok = (size_t)p.Hv * p.V;
+    bool ok = true;
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int st = ci % kStages;
+      const uint8_t *sg = sm + st * kStage;
+      const float *vec = reinterpret_cast<const float *>(sg + ST_VEC);
+      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, abort_flag) || !warp_wait(&sh.b2, ci & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float qs[16], ph[16], pl[16];
+      tmem_ld16(tm + lq + TC_A + (ci % 3) * 32 + cb, qs);
+      tmem_ld16(tm + lq + TC_O + cb, ph);
+      tmem_ld16(tm + lq + TC_O + 32 + cb, pl);
+      const uint8_t *up = sm + SC_UP;
+      float uo[16];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint4 hv = *reinterpret_cast<const uint4 *>(up + sw128_off(i, cb + 8 * m));
+        const uint4 lv = *reinterpret_cast<const uint4 *>(up + sw128_off(i, 32 + cb + 8 * m));
+        const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, lw[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = unpack_bf16(hw[e]), b = unpack_bf16(lw[e]);
+          uo[8 * m + 2 * e] = a.x + b.x;
+          uo[8 * m + 2 * e + 1] = a.y + b.y;
+        }
+      }
+      const float al = vec[VEC_ALPHA + i], pd = vec[VEC_PDIAG + i];
+      const int64_t t0 = start + (int64_t)ci * C;
+      const int nv = (int)min((int64_t)C, end - t0);
+      tmem_wait_ld();
+      float ov[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ov[j] = fmaf(al, qs[j], fmaf(pd, uo[j], ph[j] + pl[j]));
+      if (i < nv) {
+        const size_t off = (size_t)(t0 + i) * o_tok + (size_t)h * p.V + v0 + cb;
+        if (p.o_f32) {
+          float4 *dst = reinterpret_cast<float4 *>((float *)p.o + off);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) dst[m] = make_float4(ov[4 * m], ov[4 * m + 1], ov[4 * m + 2], ov[4 * m + 3]);
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)p.o + off);
+#pragma unroll
+          for (int m = 0; m < 2; ++m)
+            dst[m] = make_uint4(pack_bf16(ov[8 * m], ov[8 * m + 1]), pack_bf16(ov[8 * m + 2], ov[8 * m + 3]),
+                                pack_bf16(ov[8 * m + 4], ov[8 * m + 5]), pack_bf16(ov[8 * m + 6], ov[8 * m + 7]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.outd);
+      mbar_arrive(&sh.empty[st]);
+    }
+    if (!ok && lane == 0) fail();
   }
   __syncthreads();
   if (tid == 0 && sh.abort) {
     // copies and MMAs still in flight land before shared memory and TMEM are released
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kStages; ++i)
       if (sh.fills[i] > 0) (void)mbar_wait(&sh.full[i], (sh.fills[i] - 1) & 1, kSpin);
     if (sh.mma_bar) (void)mbar_wait(sh.mma_bar, sh.mma_par, kSpin);
   }
