@@ -53,7 +53,8 @@ constexpr size_t kHeader = 256;       // status word + padding
 constexpr uint32_t REC_NW = 0;       // -W: [2 feature halves][64 rows][128 B] bf16, SW128 images
 constexpr uint32_t REC_P = 16384;    // P (strictly lower): [64 rows][128 B] bf16, SW128 image
 constexpr uint32_t REC_VEC = 24576;  // alpha[64], pdiag[64], dk[64] fp32, b_last, n
-constexpr uint32_t REC_U = 25600;    // U: [V / 32 slices][64 tokens][32] fp32
+constexpr uint32_t REC_U = 25600;    // U: [V / 32 slices][64 tokens][32] fp32; the 16-byte
+                                     // piece m of token row r sits at piece m ^ (r % 8)
 constexpr uint32_t VEC_ALPHA = 0, VEC_PDIAG = 64, VEC_DK = 128, VEC_BLAST = 192, VEC_N = 193;  // floats
 
 __host__ __device__ constexpr size_t rec_bytes(int V) { return (size_t)REC_U + (size_t)V * C * 4; }
@@ -514,7 +515,7 @@ __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
             float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + (size_t)(2 * vb + half) * 8192 + rr * 128);
 #pragma unroll
             for (int m = 0; m < 8; ++m)
-              dst[m] = make_float4(w64[half * 32 + 4 * m], w64[half * 32 + 4 * m + 1],
+              dst[m ^ (rr & 7)] = make_float4(w64[half * 32 + 4 * m], w64[half * 32 + 4 * m + 1],
                                    w64[half * 32 + 4 * m + 2], w64[half * 32 + 4 * m + 3]);
           }
         }
@@ -549,7 +550,7 @@ constexpr uint32_t ST_AQW = 0;      // [2 halves][128 rows][128 B]: rows 0-63 ra
 constexpr uint32_t ST_K = 32768;    // [2 halves][64 tokens][128 B] raw k
 constexpr uint32_t ST_P = 49152;    // [64][128 B] P; the 8 KB after it stand in as the unused
                                     // rows 64-127 of the M = 128 operand
-constexpr uint32_t ST_U = 57344;    // [64 tokens][32] fp32 U slice
+constexpr uint32_t ST_U = 57344;    // [64 tokens][32] fp32 U slice (16-byte pieces swizzled)
 constexpr uint32_t ST_VEC = 65536;  // alpha, pdiag, dk, b_last, n
 constexpr uint32_t kStage = 66560;
 constexpr uint32_t kStageTx = 16384 + 16384 + 16384 + 8192 + 8192 + 1024;
@@ -582,9 +583,15 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uin
   lo = *reinterpret_cast<uint32_t *>(&l);
 }
 
+// One arrival for the whole warp, after every lane's shared-memory writes and fences.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Every lane waits (bounded); the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  const bool ok = mbar_wait_abortable(bar, parity, kSpin, abort);
+  const bool ok = mbar_wait_spin(bar, parity, kSpin, abort);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -610,16 +617,16 @@ __global__ void __launch_bounds__(NTS, 1)
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.full[i], 1);
-      mbar_init(&sh.empty[i], 384);
+      mbar_init(&sh.empty[i], 12);
       sh.fills[i] = 0;
     }
     mbar_init(&sh.ga, 1);
     mbar_init(&sh.b1, 1);
     mbar_init(&sh.b2, 1);
-    mbar_init(&sh.epa, 128);
-    mbar_init(&sh.epa2, 128);
-    mbar_init(&sh.epb, 256);
-    mbar_init(&sh.outd, 128);
+    mbar_init(&sh.epa, 4);  // epilogue barriers count warps: lane 0 arrives for its warp
+    mbar_init(&sh.epa2, 4);
+    mbar_init(&sh.epb, 8);
+    mbar_init(&sh.outd, 4);
     sh.abort = 0;
     sh.mma_bar = nullptr;
     sh.mma_par = 0;
@@ -645,7 +652,7 @@ __global__ void __launch_bounds__(NTS, 1)
       tma_prefetch_desc(&tm_k);
       for (int ci = 0; ci < n_chunks; ++ci) {
         const int st = ci % kStages;
-        if (ci >= kStages && !mbar_wait_abortable(&sh.empty[st], ((ci - kStages) / kStages) & 1, kSpin, abort_flag)) {
+        if (ci >= kStages && !mbar_wait_spin(&sh.empty[st], ((ci - kStages) / kStages) & 1, kSpin, abort_flag)) {
           fail();
           break;
         }
@@ -682,14 +689,14 @@ __global__ void __launch_bounds__(NTS, 1)
       int outd_seen = 0;  // outputs known to be done; out_done phases are consumed in order
       auto outputs_done = [&](int need) {
         while (outd_seen < need) {
-          if (!mbar_wait_abortable(&sh.outd, outd_seen & 1, kSpin, abort_flag)) return false;
+          if (!mbar_wait_spin(&sh.outd, outd_seen & 1, kSpin, abort_flag)) return false;
           ++outd_seen;
         }
         return true;
       };
       // [P; -] [U'_hi | U'_lo] of chunk cj: the output path, one chunk behind the state path
       auto issue_b2 = [&](int cj) {
-        if (!mbar_wait_abortable(&sh.epa2, cj & 1, kSpin, abort_flag) || !outputs_done(cj)) return false;
+        if (!mbar_wait_spin(&sh.epa2, cj & 1, kSpin, abort_flag) || !outputs_done(cj)) return false;
         tc_fence_after();
         const uint64_t sj = (uint64_t)((cj % kStages) * kStage) >> 4;
 #pragma unroll
@@ -705,8 +712,8 @@ __global__ void __launch_bounds__(NTS, 1)
         const int st = ci % kStages;
         // chunk ci's operands, the state after chunk ci-1, and the output of chunk ci-3
         // (whose accumulator columns [q; -W] S^T reuses) done
-        if (!mbar_wait_abortable(&sh.full[st], (ci / kStages) & 1, kSpin, abort_flag) ||
-            !mbar_wait_abortable(&sh.epb, ci & 1, kSpin, abort_flag) || !outputs_done(ci - 2)) {
+        if (!mbar_wait_spin(&sh.full[st], (ci / kStages) & 1, kSpin, abort_flag) ||
+            !mbar_wait_spin(&sh.epb, ci & 1, kSpin, abort_flag) || !outputs_done(ci - 2)) {
           mok = false;
           break;
         }
@@ -720,7 +727,7 @@ __global__ void __launch_bounds__(NTS, 1)
         umma_commit(&sh.ga);
         sh.mma_bar = &sh.ga;
         sh.mma_par = ci & 1;
-        if ((ci > 0 && !issue_b2(ci - 1)) || !mbar_wait_abortable(&sh.epa, ci & 1, kSpin, abort_flag)) {
+        if ((ci > 0 && !issue_b2(ci - 1)) || !mbar_wait_spin(&sh.epa, ci & 1, kSpin, abort_flag)) {
           mok = false;
           break;
         }
@@ -758,7 +765,7 @@ __global__ void __launch_bounds__(NTS, 1)
     };
     write_state();
     fence_proxy_async_smem();
-    mbar_arrive(&sh.epb);
+    warp_arrive(&sh.epb);
     bool ok = true;
     for (int ci = 0; ci < n_chunks; ++ci) {
       const int st = ci % kStages;
@@ -778,10 +785,10 @@ __global__ void __launch_bounds__(NTS, 1)
         }
         tc_fence_after();
         tmem_ld16(tm + lq + TC_A + (ci % 3) * 32 + cb, x);
-        const float4 *ur = reinterpret_cast<const float4 *>(sg + ST_U + i * 128 + cb * 4);
+        const float4 *ur = reinterpret_cast<const float4 *>(sg + ST_U + i * 128);
         float4 u4[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) u4[m] = ur[m];
+        for (int m = 0; m < 4; ++m) u4[m] = ur[((cb >> 2) + m) ^ (i & 7)];  // rows are swizzled
         const float dk = vec[VEC_DK + i];
         tmem_wait_ld();
 #pragma unroll
@@ -804,7 +811,7 @@ __global__ void __launch_bounds__(NTS, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sh.epa);
+        warp_arrive(&sh.epa);
       }
       // ---- S <- b_last S + dS (fp32), and its bf16 copy for the next chunk's MMAs
       if (!warp_wait(&sh.b1, ci & 1, abort_flag)) {
@@ -823,7 +830,7 @@ __global__ void __launch_bounds__(NTS, 1)
         write_state();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sh.epb);
+        warp_arrive(&sh.epb);
       }
       if (quarter >= 2) {
         // ---- U' hi/lo for the output path, once the previous chunk's output has read its tile
@@ -843,10 +850,10 @@ __global__ void __launch_bounds__(NTS, 1)
               make_uint4(ul[4 * m], ul[4 * m + 1], ul[4 * m + 2], ul[4 * m + 3]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&sh.epa2);
+        warp_arrive(&sh.epa2);
       }
       tc_fence_before();
-      mbar_arrive(&sh.empty[st]);
+      warp_arrive(&sh.empty[st]);
     }
     if (!ok && lane == 0) fail();
     if (ok && p.hT) {
@@ -912,8 +919,8 @@ __global__ void __launch_bounds__(NTS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&sh.outd);
-      mbar_arrive(&sh.empty[st]);
+      warp_arrive(&sh.outd);
+      warp_arrive(&sh.empty[st]);
     }
     if (!ok && lane == 0) fail();
   }

@@ -74,6 +74,17 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t pari
   return false;
 }
 
+// Like mbar_wait_abortable for waits on the critical path of a pipeline: no sleep
+// between polls, and *abort is read only every 32 polls.  Still bounded by max_iters.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, uint32_t max_iters,
+                                               volatile int *abort) {
+  for (uint32_t i = 0; i < max_iters; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 31 && *abort) return false;
+  }
+  return false;
+}
+
 // Barrier among `count` threads (a multiple of 32) using hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
