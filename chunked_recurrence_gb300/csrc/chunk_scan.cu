@@ -81,7 +81,9 @@ constexpr uint32_t OP_TH = 8192, OP_TL = 24576;
 constexpr uint32_t OP_VT = 32768;  // raw v: [V / 64 blocks][64 tokens][128 B], SW128
 // A, then (I + A)^-1 in place, then the T diag(b/|k|) hi / lo tiles
 __host__ __device__ constexpr uint32_t op_x(int V) { return OP_VT + (uint32_t)V * 128; }
-__host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + 18432 + 1024; }
+// partial block products of the inversion: 4 x [16][kZP] fp32 after A's 64 x kXP floats
+__host__ __device__ constexpr uint32_t op_zs(int V) { return op_x(V) + 17408; }
+__host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + 22528 + 1024; }
 
 // Y = (I + A)^-1 for the strictly lower 64 x 64 A held in X (fp32, row stride kXP), in
 // place, by 16 x 16 blocks: the diagonal blocks by forward substitution, then the
@@ -89,12 +91,16 @@ __host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + 18432 +
 //   Y_IJ = -Y_II sum_{K=J}^{I-1} A_IK Y_KJ.
 // A's blocks below the diagonal stay in place (later sums read them); Y_II replaces
 // A_II, and Y_IJ (J < I) is kept in the unused upper block (J, I), so Y_KJ (K >= J) is
-// X[16 J + m][16 K + c] in every case.  A 16 x 16 result is computed by 16 threads,
-// each a 4 x 4 tile in registers.
-__device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
+// X[16 J + m][16 K + c] in every case.  Each block product goes to one warp (a 2 x 4
+// tile per lane), the products of a block-diagonal to different warps with their sums
+// parked in ZS, so a level costs two dependent block products whatever its number of
+// terms.  `lw` is this warp's role; blocks resident on one SM pass different roles to
+// the same hardware warp slot so that the work spreads over the SM's four schedulers.
+constexpr int kZP = 20;  // fp32 row of a parked 16 x 16 product, padded against bank conflicts
+__device__ __forceinline__ void invert_unit_lower(float *X, float *ZS, int lw, int lane) {
   float y[16];
-  const int b = (tid >> 4) * 16, cc = tid & 15;
-  if (tid < C) {
+  const int b = lw * 16, cc = lane & 15;
+  if (lane < 16) {  // diagonal block lw, column cc
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const float4 *ar = reinterpret_cast<const float4 *>(X + (b + r) * kXP + b);
@@ -113,69 +119,75 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
     }
   }
   __syncthreads();  // every read of A_II is done
-  if (tid < C) {
+  if (lane < 16) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) X[(b + r) * kXP + b + cc] = y[r];
   }
   __syncthreads();
-  const int t = tid & 15, tr = (t >> 2) * 4, tc = (t & 3) * 4;
+  const int tr = (lane >> 2) * 2, tc = (lane & 3) * 4;  // this lane's 2 x 4 tile
 #pragma unroll 1
   for (int d = 1; d < 4; ++d) {
-    const bool act = tid < 16 * (4 - d);
-    const int I = d + (tid >> 4), J = I - d;
-    float z[4][4];
+    if (lw < (4 - d) * d) {  // product A_IK Y_KJ: block bb (I = d + bb, J = bb), K = J + kk
+      const int bb = lw / d, kk = lw - bb * d;
+      const int I = d + bb, J = bb, K = J + kk;
+      float z[2][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
-    if (act) {
+        for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
 #pragma unroll 1
-      for (int K = J; K < I; ++K) {
+      for (int m4 = 0; m4 < 4; ++m4) {
+        float4 a[2], yv[4];
 #pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-          float4 a[4], yv[4];
+        for (int i = 0; i < 2; ++i)
+          a[i] = *reinterpret_cast<const float4 *>(X + (16 * I + tr + i) * kXP + 16 * K + 4 * m4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            a[i] = *reinterpret_cast<const float4 *>(X + (16 * I + tr + i) * kXP + 16 * K + 4 * m4);
+        for (int mm = 0; mm < 4; ++mm)
+          yv[mm] = *reinterpret_cast<const float4 *>(X + (16 * J + 4 * m4 + mm) * kXP + 16 * K + tc);
 #pragma unroll
-          for (int mm = 0; mm < 4; ++mm)
-            yv[mm] = *reinterpret_cast<const float4 *>(X + (16 * J + 4 * m4 + mm) * kXP + 16 * K + tc);
+        for (int i = 0; i < 2; ++i) {
+          const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-              z[i][0] = fmaf(ai[mm], yv[mm].x, z[i][0]);
-              z[i][1] = fmaf(ai[mm], yv[mm].y, z[i][1]);
-              z[i][2] = fmaf(ai[mm], yv[mm].z, z[i][2]);
-              z[i][3] = fmaf(ai[mm], yv[mm].w, z[i][3]);
-            }
+          for (int mm = 0; mm < 4; ++mm) {
+            z[i][0] = fmaf(ai[mm], yv[mm].x, z[i][0]);
+            z[i][1] = fmaf(ai[mm], yv[mm].y, z[i][1]);
+            z[i][2] = fmaf(ai[mm], yv[mm].z, z[i][2]);
+            z[i][3] = fmaf(ai[mm], yv[mm].w, z[i][3]);
           }
         }
       }
-      // the sum goes to block (J, I), which no sum of this block-diagonal reads
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float4 *>(X + (16 * J + tr + i) * kXP + 16 * I + tc) =
+      for (int i = 0; i < 2; ++i)
+        *reinterpret_cast<float4 *>(ZS + lw * 16 * kZP + (tr + i) * kZP + tc) =
             make_float4(z[i][0], z[i][1], z[i][2], z[i][3]);
     }
     __syncthreads();
-    if (act) {
+    if (lw < 4 - d) {  // Y_IJ = -Y_II (sum of block lw's products), into upper block (J, I)
+      const int I = d + lw, J = lw;
+      float z[2][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
-#pragma unroll
+#pragma unroll 1
       for (int m4 = 0; m4 < 4; ++m4) {
-        float4 a[4], zv[4];
+        float4 a[2], zv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 2; ++i)
           a[i] = *reinterpret_cast<const float4 *>(X + (16 * I + tr + i) * kXP + 16 * I + 4 * m4);
 #pragma unroll
-        for (int mm = 0; mm < 4; ++mm)
-          zv[mm] = *reinterpret_cast<const float4 *>(X + (16 * J + 4 * m4 + mm) * kXP + 16 * I + tc);
+        for (int mm = 0; mm < 4; ++mm) {
+          zv[mm] = *reinterpret_cast<const float4 *>(ZS + (lw * d) * 16 * kZP + (4 * m4 + mm) * kZP + tc);
+          for (int kk = 1; kk < d; ++kk) {
+            const float4 w = *reinterpret_cast<const float4 *>(ZS + (lw * d + kk) * 16 * kZP + (4 * m4 + mm) * kZP + tc);
+            zv[mm].x += w.x;
+            zv[mm].y += w.y;
+            zv[mm].z += w.z;
+            zv[mm].w += w.w;
+          }
+        }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
           const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
 #pragma unroll
           for (int mm = 0; mm < 4; ++mm) {
@@ -186,11 +198,8 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
           }
         }
       }
-    }
-    __syncthreads();  // every thread has read its sums: Y_IJ replaces them
-    if (act) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
         *reinterpret_cast<float4 *>(X + (16 * J + tr + i) * kXP + 16 * I + tc) =
             make_float4(-z[i][0], -z[i][1], -z[i][2], -z[i][3]);
     }
@@ -199,14 +208,16 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
 }
 
 template <int V>
-__global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
+__global__ void __launch_bounds__(128)
+    chunk_operand_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const OpParams p) {
   constexpr int NVB = V / 64;                       // 64-column blocks of v
   constexpr uint32_t kCols = (V <= 128) ? 128u : 256u;
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   __shared__ float gam[C], bex[C], dec[C], alf[C + 1], kinv[C], qinv[C], bet[C];
   __shared__ float blast_s;
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar, ld_bar;
   __shared__ uint32_t tbase;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = (int)(blockIdx.x % (unsigned)p.Hv);
@@ -232,36 +243,50 @@ __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
   float *vec = reinterpret_cast<float *>(rec + REC_VEC);
   float *X = reinterpret_cast<float *>(sm + op_x(V));
 
-  // ---- raw k, q and v rows (two threads per token) into swizzled tiles; gates; norms
+  // ---- raw k, q and v tiles by TMA (rows past the chunk's end hold finite data of the
+  //      next sequence or zeros: beta = 0 there keeps them out of every result); gates
+  if (tid == 0) {
+    mbar_init(&ld_bar, 1);
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int32_t tt = (int32_t)t0;
+    mbar_arrive_expect_tx(&ld_bar, (4 + NVB) * 8192);
+    tma_load_3d(sm + OP_KQ, &tm_k, &ld_bar, 0, qh, tt);
+    tma_load_3d(sm + OP_KQ + 16384, &tm_k, &ld_bar, 64, qh, tt);
+    tma_load_3d(sm + OP_KQ + 8192, &tm_q, &ld_bar, 0, qh, tt);
+    tma_load_3d(sm + OP_KQ + 24576, &tm_q, &ld_bar, 64, qh, tt);
+#pragma unroll
+    for (int nb = 0; nb < NVB; ++nb) tma_load_3d(sm + OP_VT + nb * 8192, &tm_v, &ld_bar, nb * 64, h, tt);
+  }
+  if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
+  else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
+  if (warp == 0) {
+    tmem_alloc(&tbase, kCols);
+    tmem_relinquish();
+  }
+  {
+    const bool ok = tid != 0 || mbar_wait(&ld_bar, 0, kSpin);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
+      (void)mbar_wait(&ld_bar, 0, kSpin);  // the copies land before shared memory is released
+      tc_fence_before();
+      __syncthreads();
+      if (warp == 0) tmem_dealloc(tbase, kCols);
+      return;
+    }
+  }
+  // ---- 1/|k| and 1/|q| from the tiles (two threads per token)
   {
     const int r = tid >> 1, hf = tid & 1;
-    const bool valid = r < n;
-    const int64_t tok = t0 + r;
-    uint4 kr[8], qr[8], vr[4 * NVB];
-    if (valid) {
-      const uint4 *ks = reinterpret_cast<const uint4 *>(p.k + tok * p.ks + (int64_t)qh * KD + hf * 64);
-      const uint4 *qs = reinterpret_cast<const uint4 *>(p.q + tok * p.qs + (int64_t)qh * KD + hf * 64);
-      const uint4 *vs = reinterpret_cast<const uint4 *>(p.v + tok * p.vs + (int64_t)h * V + hf * (V / 2));
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        kr[j] = __ldg(ks + j);
-        qr[j] = __ldg(qs + j);
-      }
-#pragma unroll
-      for (int j = 0; j < 4 * NVB; ++j) vr[j] = __ldg(vs + j);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) kr[j] = qr[j] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < 4 * NVB; ++j) vr[j] = make_uint4(0, 0, 0, 0);
-    }
-    if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
-    else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
     float sk = 0.f, sq = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint32_t *wk = reinterpret_cast<const uint32_t *>(&kr[j]);
-      const uint32_t *wq = reinterpret_cast<const uint32_t *>(&qr[j]);
+      const uint4 kr = *reinterpret_cast<const uint4 *>(sm + OP_KQ + hf * 16384 + sw128_off(r, j * 8));
+      const uint4 qr = *reinterpret_cast<const uint4 *>(sm + OP_KQ + hf * 16384 + 8192 + sw128_off(r, j * 8));
+      const uint32_t wk[4] = {kr.x, kr.y, kr.z, kr.w}, wq[4] = {qr.x, qr.y, qr.z, qr.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 a = unpack_bf16(wk[e]), b = unpack_bf16(wq[e]);
@@ -269,31 +294,12 @@ __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
         sq = fmaf(b.x, b.x, fmaf(b.y, b.y, sq));
       }
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      *reinterpret_cast<uint4 *>(sm + OP_KQ + hf * 16384 + sw128_off(r, j * 8)) = kr[j];
-      *reinterpret_cast<uint4 *>(sm + OP_KQ + hf * 16384 + 8192 + sw128_off(r, j * 8)) = qr[j];
-    }
-#pragma unroll
-    for (int j = 0; j < 4 * NVB; ++j) {
-      const int col = hf * (V / 2) + j * 8;
-      *reinterpret_cast<uint4 *>(sm + OP_VT + (col >> 6) * 8192 + sw128_off(r, col & 63)) = vr[j];
-    }
     sk += __shfl_xor_sync(0xffffffffu, sk, 1);
     sq += __shfl_xor_sync(0xffffffffu, sq, 1);
     if (hf == 0) {
       kinv[r] = p.l2norm ? 1.f / sqrtf(sk + kL2Eps) : 1.f;
       qinv[r] = p.l2norm ? 1.f / sqrtf(sq + kL2Eps) : 1.f;
     }
-  }
-  fence_proxy_async_smem();
-  if (warp == 0) {
-    tmem_alloc(&tbase, kCols);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(128) chunk_operand_kernel(const OpParams p) {
   }
   __syncthreads();
   // ---- T = (I + A)^-1 diag(beta)
-  invert_unit_lower(X, tid);
+  invert_unit_lower(X, reinterpret_cast<float *>(sm + op_zs(V)), (warp + (int)(blockIdx.x & 3u)) & 3, lane);
   // ---- T and T diag(b/|k|) as bf16 hi/lo K-major tiles (row r, columns cb..cb+31): T's
   //      tiles replace the raw q rows (Q K^T no longer needs them), T diag(b/|k|)'s tiles
   //      replace A once every thread has read its row of the inverse
@@ -951,12 +957,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [n_tok][heads][128] bf16 map with token stride `tok_stride` elements; 64 x 64 boxes, SW128.
-bool make_qk_map(CUtensorMap *m, const void *base, int heads, int64_t n_tok, int64_t tok_stride) {
+// [n_tok][heads][width] bf16 map with token stride `tok_stride` elements; 64 x 64 boxes, SW128.
+bool make_tile_map(CUtensorMap *m, const void *base, int width, int heads, int64_t n_tok, int64_t tok_stride) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)heads, (cuuint64_t)n_tok};
-  cuuint64_t strides[2] = {(cuuint64_t)KD * 2, (cuuint64_t)tok_stride * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)heads, (cuuint64_t)n_tok};
+  cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)tok_stride * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
@@ -965,14 +971,15 @@ bool make_qk_map(CUtensorMap *m, const void *base, int heads, int64_t n_tok, int
 }
 
 template <int V>
-gdn_status launch_operands(const OpParams &op, size_t slots, cudaStream_t st) {
+gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const OpParams &op, size_t slots, cudaStream_t st) {
   const size_t smem = op_smem(V);
   if (cudaFuncSetAttribute(chunk_operand_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return GDN_ERR_CUDA;
   const size_t blocks = slots * (size_t)op.Hv;
   if (blocks > 2147483647ULL) return GDN_ERR_UNSUPPORTED;
-  chunk_operand_kernel<V><<<(unsigned)blocks, 128, smem, st>>>(op);
+  chunk_operand_kernel<V><<<(unsigned)blocks, 128, smem, st>>>(mq, mk, mv, op);
   return launch_status();
 }
 
@@ -1022,18 +1029,20 @@ gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const flo
   op.rec = (uint8_t *)workspace + kHeader;
   op.rec_bytes = rec_bytes(sh.V);
   op.status = status;
+  CUtensorMap mq, mk, mv;
+  if (!make_tile_map(&mq, q, KD, sh.Hqk, n_tok, sh.q_stride) ||
+      !make_tile_map(&mk, k, KD, sh.Hqk, n_tok, sh.k_stride) ||
+      !make_tile_map(&mv, v, sh.V, sh.Hv, n_tok, sh.v_stride))
+    return GDN_ERR_CUDA;
   gdn_status r;
   switch (sh.V) {
-    case 64: r = launch_operands<64>(op, slots, st); break;
-    case 128: r = launch_operands<128>(op, slots, st); break;
-    case 192: r = launch_operands<192>(op, slots, st); break;
-    case 256: r = launch_operands<256>(op, slots, st); break;
+    case 64: r = launch_operands<64>(mq, mk, mv, op, slots, st); break;
+    case 128: r = launch_operands<128>(mq, mk, mv, op, slots, st); break;
+    case 192: r = launch_operands<192>(mq, mk, mv, op, slots, st); break;
+    case 256: r = launch_operands<256>(mq, mk, mv, op, slots, st); break;
     default: return GDN_ERR_UNSUPPORTED;
   }
   if (r != GDN_OK) return r;
-  CUtensorMap mq, mk;
-  if (!make_qk_map(&mq, q, sh.Hqk, n_tok, sh.q_stride) || !make_qk_map(&mk, k, sh.Hqk, n_tok, sh.k_stride))
-    return GDN_ERR_CUDA;
   ScanParams sp{};
   sp.cu = cu;
   sp.row_T = sh.T;
