@@ -8,6 +8,10 @@ two-pass (gdn_segment_summary -> gdn_chain_reduce -> gdn_chunk_fwd per
 segment) is measured on the long-context workload (T=131072, 16 heads,
 8 segments) and reported beside it.
 
+gdn_chunk_fwd runs as two kernels (chunk_operand_kernel: every chunk's
+state-independent operands at once; chunk_scan_kernel: the state chain), so a
+step is four launches.  The roofline is reported for the gdn_chunk_fwd call.
+
 Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
 on the host cores instead, on a bounded sample of the same workload.
 Under torchrun every rank runs its own replica of the workload (independent
@@ -294,7 +298,8 @@ def run_gpu_arm(args, ws, rank, local):
     roofline = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "kernel": "gdn_chunk_fwd", "algorithmic_bytes": cb, "algorithmic_flops": cf,
+                "kernel": "gdn_chunk_fwd (chunk_operand_kernel + chunk_scan_kernel)",
+                "algorithmic_bytes": cb, "algorithmic_flops": cf,
                 "tensor_frac": round(cf / (chunk_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs / bf16_tflops)",
                 "kernel_sha": sha}
@@ -315,7 +320,7 @@ def run_gpu_arm(args, ws, rank, local):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
 
-    launches_per_step = 3
+    launches_per_step = 4  # gate prep, conv1d, and gdn_chunk_fwd's operand + scan kernels
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),

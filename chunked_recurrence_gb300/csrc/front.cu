@@ -102,6 +102,16 @@ struct Vec;
 template <>
 struct Vec<__nv_bfloat16, 8> {
   using raw = uint4;
+  __device__ static raw load_raw(const __nv_bfloat16 *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+  __device__ static void cvt(const raw &r, float *f) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(h[i]);
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+  }
   __device__ static void load(const __nv_bfloat16 *p, float *f) {
     const uint4 r = *reinterpret_cast<const uint4 *>(p);
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
@@ -122,6 +132,11 @@ struct Vec<__nv_bfloat16, 8> {
 };
 template <>
 struct Vec<float, 4> {
+  using raw = float4;
+  __device__ static raw load_raw(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+  __device__ static void cvt(const raw &r, float *f) {
+    f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
+  }
   __device__ static void load(const float *p, float *f) {
     const float4 r = *reinterpret_cast<const float4 *>(p);
     f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
@@ -132,12 +147,15 @@ struct Vec<float, 4> {
 };
 template <typename T>
 struct Vec<T, 1> {
+  using raw = T;
+  __device__ static raw load_raw(const T *p) { return *p; }
+  __device__ static void cvt(const raw &r, float *f) { f[0] = to_f32(r); }
   __device__ static void load(const T *p, float *f) { f[0] = to_f32(*p); }
   __device__ static void store(T *p, const float *f) { *p = from_f32<T>(f[0]); }
 };
 
 template <typename T, int VEC, int W>
-__global__ void __launch_bounds__(128) conv1d_kernel(const T *__restrict__ x, const T *__restrict__ w,
+__global__ void __launch_bounds__(128, 5) conv1d_kernel(const T *__restrict__ x, const T *__restrict__ w,
                                                      const T *__restrict__ bias,
                                                      const int32_t *__restrict__ cu, int n_seqs,
                                                      int64_t row_T, int64_t n_tok, int C, int act,
@@ -178,39 +196,52 @@ __global__ void __launch_bounds__(128) conv1d_kernel(const T *__restrict__ x, co
       for (int v = 0; v < VEC; ++v) hist[j][v] = 0.f;
     }
   }
-  for (int64_t t = t0; t < t1; ++t) {
-    if (t >= end) {  // a new sequence begins at t: zero history
-      if (cu) {
-        while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t) ++s;
-        start = max((int64_t)cu[s], (int64_t)0);
-        end = cu[s + 1];
-      } else {
-        start = t;
-        end = t + row_T;
+  // tokens in batches of kAhead: all of a batch's loads are in flight before its first use
+  constexpr int kAhead = 4;
+  for (int64_t tb = t0; tb < t1; tb += kAhead) {
+    typename Vec<T, VEC>::raw raw[kAhead];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u)
+      if (tb + u < t1) raw[u] = Vec<T, VEC>::load_raw(x + (tb + u) * C + c0);
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int64_t t = tb + u;
+      if (t >= t1) break;
+      if (t >= end) {  // a new sequence begins at t: zero history
+        if (cu) {
+          while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t) ++s;
+          start = max((int64_t)cu[s], (int64_t)0);
+          end = cu[s + 1];
+        } else {
+          start = t;
+          end = t + row_T;
+        }
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j)
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) hist[j][v] = 0.f;
       }
+      float cur[VEC], out[VEC];
+      Vec<T, VEC>::cvt(raw[u], cur);
 #pragma unroll
-      for (int j = 0; j < W - 1; ++j)
+      for (int v = 0; v < VEC; ++v) {
+        float acc = bs[v];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) hist[j][v] = 0.f;
-    }
-    float cur[VEC], out[VEC];
-    Vec<T, VEC>::load(x + t * C + c0, cur);
+        for (int j = 0; j < W - 1; ++j) acc = fmaf(wt[j][v], hist[j][v], acc);
+        acc = fmaf(wt[W - 1][v], cur[v], acc);
+        // SiLU with the fast exponential and division: their error (a few ulp of fp32) is
+        // far below the rounding of y to the input dtype
+        out[v] = act ? __fdividef(acc, 1.f + __expf(-acc)) : acc;
+      }
+      Vec<T, VEC>::store(y + t * C + c0, out);
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-      float acc = bs[v];
+      for (int j = 0; j + 1 < W - 1; ++j)
 #pragma unroll
-      for (int j = 0; j < W - 1; ++j) acc = fmaf(wt[j][v], hist[j][v], acc);
-      acc = fmaf(wt[W - 1][v], cur[v], acc);
-      out[v] = act ? acc / (1.f + expf(-acc)) : acc;
-    }
-    Vec<T, VEC>::store(y + t * C + c0, out);
+        for (int v = 0; v < VEC; ++v) hist[j][v] = hist[j + 1][v];
+      if (W > 1) {
 #pragma unroll
-    for (int j = 0; j + 1 < W - 1; ++j)
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) hist[j][v] = hist[j + 1][v];
-    if (W > 1) {
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) hist[W > 1 ? W - 2 : 0][v] = cur[v];
+        for (int v = 0; v < VEC; ++v) hist[W > 1 ? W - 2 : 0][v] = cur[v];
+      }
     }
   }
 }
