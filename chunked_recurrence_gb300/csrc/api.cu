@@ -22,6 +22,10 @@ gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float
                         const float *beta, const float *h0, const int32_t *cu,
                         const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
                         void *workspace, size_t ws_bytes, cudaStream_t st);
+gdn_status summary_scan(const void *k, const void *v, const float *g, const float *beta,
+                        const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
+                        float *M, float *S_local, void *workspace, size_t ws_bytes,
+                        cudaStream_t st);
 gdn_status summary_tc(const void *k, const void *v, const float *g, const float *beta,
                       const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
                       float *M, float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st);
@@ -82,10 +86,10 @@ extern "C" size_t gdn_chunk_fwd_min_workspace_bytes(const gdn_shape *shape) {
 extern "C" size_t gdn_segment_summary_workspace_bytes(const gdn_shape *shape, int32_t n_seg) {
   gdn_shape s;
   if (n_seg < 0 || normalise_shape(shape, &s) != GDN_OK) return 0;
-  if (tc_shape(s)) {  // T of every chunk of every segment, as for gdn_chunk_fwd
+  if (tc_shape(s)) {  // the operand records (or T) of every chunk of every segment
     gdn_shape segs = s;
     segs.n_seqs = n_seg;
-    return chunk_tc_workspace_bytes(segs, s.T);
+    return scan_shape(s) ? chunk_scan_workspace_bytes(segs, s.T) : chunk_tc_workspace_bytes(segs, s.T);
   }
   return kWorkspaceBase;
 }
@@ -137,9 +141,16 @@ extern "C" gdn_status gdn_segment_summary(const void *k, const void *v, const fl
   if (n_seg == 0) return GDN_OK;
   if (!seg_bounds || !M || !S_local) return GDN_ERR_INVALID_ARG;
   if (s.T > 0 && (!k || !v || !g || !beta)) return GDN_ERR_INVALID_ARG;
-  if (!(flags & GDN_FLAG_SIMT) && s.T > 0 && tc_shape(s) && chunk_tc_supported(k, k, v, s))
+  if (!(flags & GDN_FLAG_SIMT) && s.T > 0 && tc_shape(s) && chunk_tc_supported(k, k, v, s)) {
+    gdn_shape segs = s;
+    segs.n_seqs = n_seg;
+    if (scan_shape(s) && chunk_scan_supported(k, k, v, s) &&
+        workspace_bytes >= chunk_scan_workspace_bytes(segs, s.T))
+      return summary_scan(k, v, g, beta, seg_bounds, n_seg, s, flags, M, S_local, workspace,
+                          workspace_bytes, (cudaStream_t)stream);
     return summary_tc(k, v, g, beta, seg_bounds, n_seg, s, flags, M, S_local, workspace,
                       workspace_bytes, (cudaStream_t)stream);
+  }
   return segment_summary_simt(k, v, g, beta, seg_bounds, n_seg, s, flags, M, S_local,
                               (int32_t *)workspace, (cudaStream_t)stream);
 }

@@ -547,6 +547,10 @@ struct ScanParams {
   int o_f32;
   float *hT;
   int32_t *status;
+  // segment-summary mode: state columns [0, K) are M (start I, v = 0), [K, K + V) are
+  // S_local (start 0); no output, q unused
+  int summary;
+  float *M, *S_local;
 };
 
 // warps 0-7: state path; 8, 9, 12, 13: outputs; 10: copies; 11: MMAs
@@ -620,6 +624,9 @@ __global__ void __launch_bounds__(NTS, 1)
   const int64_t sbase = (int64_t)s + start / C;
   const uint32_t sb = smem_u32(sm);
   volatile int *abort_flag = &sh.abort;
+  const bool summary = p.summary != 0;
+  const bool m_cols = summary && v0 < KD;   // columns of M: v = 0, so U = 0 and nothing is loaded
+  const int uslice = (summary ? v0 - KD : v0) / VS;
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.full[i], 1);
@@ -666,15 +673,17 @@ __global__ void __launch_bounds__(NTS, 1)
         const uint8_t *r = p.rec + ((size_t)(sbase + ci) * p.Hv + h) * p.rec_bytes;
         uint8_t *sg = sm + st * kStage;
         uint64_t *fb = &sh.full[st];
-        mbar_arrive_expect_tx(fb, kStageTx);
-        tma_load_3d(sg + ST_AQW, &tm_q, fb, 0, qh, t0);
-        tma_load_3d(sg + ST_AQW + 16384, &tm_q, fb, 64, qh, t0);
+        mbar_arrive_expect_tx(fb, kStageTx - (summary ? 16384u : 0u) - (m_cols ? 8192u : 0u));
+        if (!summary) {  // the summary has no output: the q rows stay unused
+          tma_load_3d(sg + ST_AQW, &tm_q, fb, 0, qh, t0);
+          tma_load_3d(sg + ST_AQW + 16384, &tm_q, fb, 64, qh, t0);
+        }
         bulk_load(sg + ST_AQW + 8192, r + REC_NW, 8192, fb);
         bulk_load(sg + ST_AQW + 24576, r + REC_NW + 8192, 8192, fb);
         tma_load_3d(sg + ST_K, &tm_k, fb, 0, qh, t0);
         tma_load_3d(sg + ST_K + 8192, &tm_k, fb, 64, qh, t0);
         bulk_load(sg + ST_P, r + REC_P, 8192, fb);
-        bulk_load(sg + ST_U, r + REC_U + (size_t)(v0 / VS) * 8192, 8192, fb);
+        if (!m_cols) bulk_load(sg + ST_U, r + REC_U + (size_t)uslice * 8192, 8192, fb);
         bulk_load(sg + ST_VEC, r + REC_VEC, 1024, fb);
         sh.fills[st] += 1;
       }
@@ -719,7 +728,7 @@ __global__ void __launch_bounds__(NTS, 1)
         // chunk ci's operands, the state after chunk ci-1, and the output of chunk ci-3
         // (whose accumulator columns [q; -W] S^T reuses) done
         if (!mbar_wait_spin(&sh.full[st], (ci / kStages) & 1, kSpin, abort_flag) ||
-            !mbar_wait_spin(&sh.epb, ci & 1, kSpin, abort_flag) || !outputs_done(ci - 2)) {
+            !mbar_wait_spin(&sh.epb, ci & 1, kSpin, abort_flag) || (!summary && !outputs_done(ci - 2))) {
           mok = false;
           break;
         }
@@ -733,7 +742,7 @@ __global__ void __launch_bounds__(NTS, 1)
         umma_commit(&sh.ga);
         sh.mma_bar = &sh.ga;
         sh.mma_par = ci & 1;
-        if ((ci > 0 && !issue_b2(ci - 1)) || !mbar_wait_spin(&sh.epa, ci & 1, kSpin, abort_flag)) {
+        if ((!summary && ci > 0 && !issue_b2(ci - 1)) || !mbar_wait_spin(&sh.epa, ci & 1, kSpin, abort_flag)) {
           mok = false;
           break;
         }
@@ -746,7 +755,7 @@ __global__ void __launch_bounds__(NTS, 1)
         sh.mma_bar = &sh.b1;
         sh.mma_par = ci & 1;
       }
-      if (mok && n_chunks > 0) mok = issue_b2(n_chunks - 1);
+      if (mok && !summary && n_chunks > 0) mok = issue_b2(n_chunks - 1);
       if (!mok) fail();
     }
   } else if (warp < 8) {
@@ -757,8 +766,11 @@ __global__ void __launch_bounds__(NTS, 1)
     const int f = quarter * 32 + lane;  // key feature of this thread's state row
     const int cb = hc * 16;             // first value column of this thread (inside the block)
     float S[16];
-    {
-      const float *h0p = p.h0 ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0 + cb) * KD + f : nullptr;
+    if (m_cols) {  // M starts at the identity
+#pragma unroll
+      for (int j = 0; j < 16; ++j) S[j] = (v0 + cb + j == f) ? 1.f : 0.f;
+    } else {
+      const float *h0p = (p.h0 && !summary) ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0 + cb) * KD + f : nullptr;
 #pragma unroll
       for (int j = 0; j < 16; ++j) S[j] = h0p ? h0p[(size_t)j * KD] : 0.f;
     }
@@ -794,7 +806,8 @@ __global__ void __launch_bounds__(NTS, 1)
         const float4 *ur = reinterpret_cast<const float4 *>(sg + ST_U + i * 128);
         float4 u4[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) u4[m] = ur[((cb >> 2) + m) ^ (i & 7)];  // rows are swizzled
+        for (int m = 0; m < 4; ++m)  // rows are swizzled; M's columns have U = 0
+          u4[m] = m_cols ? make_float4(0.f, 0.f, 0.f, 0.f) : ur[((cb >> 2) + m) ^ (i & 7)];
         const float dk = vec[VEC_DK + i];
         tmem_wait_ld();
 #pragma unroll
@@ -838,7 +851,7 @@ __global__ void __launch_bounds__(NTS, 1)
         tc_fence_before();
         warp_arrive(&sh.epb);
       }
-      if (quarter >= 2) {
+      if (quarter >= 2 && !summary) {
         // ---- U' hi/lo for the output path, once the previous chunk's output has read its tile
         if (ci > 0 && !warp_wait(&sh.outd, (ci - 1) & 1, abort_flag)) {
           ok = false;
@@ -862,8 +875,11 @@ __global__ void __launch_bounds__(NTS, 1)
       warp_arrive(&sh.empty[st]);
     }
     if (!ok && lane == 0) fail();
-    if (ok && p.hT) {
-      float *dst = p.hT + (((size_t)s * p.Hv + h) * p.V + v0 + cb) * KD + f;
+    float *dst = nullptr;
+    if (m_cols) dst = p.M + (((size_t)s * p.Hv + h) * KD + v0 + cb) * KD + f;
+    else if (summary) dst = p.S_local + (((size_t)s * p.Hv + h) * p.V + uslice * VS + cb) * KD + f;
+    else if (p.hT) dst = p.hT + (((size_t)s * p.Hv + h) * p.V + v0 + cb) * KD + f;
+    if (ok && dst) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) dst[(size_t)j * KD] = S[j];
     }
@@ -880,7 +896,16 @@ __global__ void __launch_bounds__(NTS, 1)
       const int st = ci % kStages;
       const uint8_t *sg = sm + st * kStage;
       const float *vec = reinterpret_cast<const float *>(sg + ST_VEC);
-      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, abort_flag) || !warp_wait(&sh.b2, ci & 1, abort_flag)) {
+      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (summary) {  // no output: only release the stage
+        tc_fence_before();
+        warp_arrive(&sh.empty[st]);
+        continue;
+      }
+      if (!warp_wait(&sh.b2, ci & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -1000,20 +1025,24 @@ size_t chunk_scan_workspace_bytes(const gdn_shape &sh, int64_t n_tok) {
   return kHeader + n_slots(n_tok, sh.n_seqs) * (size_t)sh.Hv * rec_bytes(sh.V);
 }
 
-gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const float *g,
-                          const float *beta, const float *h0, const int32_t *cu,
-                          const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
-                          void *workspace, size_t ws_bytes, cudaStream_t st) {
-  const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
-  const int n_seqs = sh.n_seqs;
+// Both kernels of the split path over `n_seqs` sequences (cu_seqlens `cu`, or rows of
+// sh.T tokens): the operand records, then the state scan over (value-column blocks,
+// v-heads, sequences).  Summary mode scans the K + V columns of [M; S_local] instead.
+static gdn_status run_scan(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const float *h0, const int32_t *cu, int n_seqs,
+                           int64_t n_tok, const gdn_shape &sh, int64_t q_stride, float scale,
+                           uint32_t flags, void *o, float *h_T, bool summary, float *M,
+                           float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st) {
+  gdn_shape rs = sh;
+  rs.n_seqs = n_seqs;
   const size_t slots = n_slots(n_tok, n_seqs);
-  if (ws_bytes < chunk_scan_workspace_bytes(sh, n_tok)) return GDN_ERR_WORKSPACE;
+  if (ws_bytes < kHeader + slots * (size_t)sh.Hv * rec_bytes(sh.V)) return GDN_ERR_WORKSPACE;
   int32_t *status = (int32_t *)workspace;
   OpParams op{};
   op.q = (const __nv_bfloat16 *)q;
   op.k = (const __nv_bfloat16 *)k;
   op.v = (const __nv_bfloat16 *)v;
-  op.qs = sh.q_stride;
+  op.qs = q_stride;
   op.ks = sh.k_stride;
   op.vs = sh.v_stride;
   op.g = g;
@@ -1030,7 +1059,7 @@ gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const flo
   op.rec_bytes = rec_bytes(sh.V);
   op.status = status;
   CUtensorMap mq, mk, mv;
-  if (!make_tile_map(&mq, q, KD, sh.Hqk, n_tok, sh.q_stride) ||
+  if (!make_tile_map(&mq, q, KD, sh.Hqk, n_tok, q_stride) ||
       !make_tile_map(&mk, k, KD, sh.Hqk, n_tok, sh.k_stride) ||
       !make_tile_map(&mv, v, sh.V, sh.Hv, n_tok, sh.v_stride))
     return GDN_ERR_CUDA;
@@ -1057,11 +1086,33 @@ gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const flo
   sp.o_f32 = (flags & GDN_FLAG_O_F32) ? 1 : 0;
   sp.hT = h_T;
   sp.status = status;
+  sp.summary = summary ? 1 : 0;
+  sp.M = M;
+  sp.S_local = S_local;
   if (cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kScanSmem) != cudaSuccess)
     return GDN_ERR_CUDA;
-  chunk_scan_kernel<<<dim3(sh.V / VS, sh.Hv, n_seqs), NTS, kScanSmem, st>>>(mq, mk, sp);
+  const int cols = summary ? KD + sh.V : sh.V;
+  chunk_scan_kernel<<<dim3(cols / VS, sh.Hv, n_seqs), NTS, kScanSmem, st>>>(mq, mk, sp);
   return launch_status();
+}
+
+gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *h0, const int32_t *cu,
+                          const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
+                          void *workspace, size_t ws_bytes, cudaStream_t st) {
+  const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
+  return run_scan(q, k, v, g, beta, h0, cu, sh.n_seqs, n_tok, sh, sh.q_stride, scale, flags, o,
+                  h_T, false, nullptr, nullptr, workspace, ws_bytes, st);
+}
+
+// gdn_segment_summary on the split path: k stands in for q (no output is formed).
+gdn_status summary_scan(const void *k, const void *v, const float *g, const float *beta,
+                        const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
+                        float *M, float *S_local, void *workspace, size_t ws_bytes,
+                        cudaStream_t st) {
+  return run_scan(k, k, v, g, beta, nullptr, bounds, n_seg, sh.T, sh, sh.k_stride, 1.f, flags,
+                  nullptr, nullptr, true, M, S_local, workspace, ws_bytes, st);
 }
 
 }  // namespace gdn

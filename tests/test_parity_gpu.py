@@ -413,3 +413,43 @@ def test_reduced_workloads(crg, name):
     for h, (ro, rh) in ref64.items():
         assert metrics(r["o"][:, h].cpu(), ro)["rel_l2"] <= 5e-3
         assert metrics(r["h_T"][:, h].cpu(), rh)["rel_l2"] <= 5e-3
+
+
+# ------------------------------------- the compact workspace path (bf16, K = 128)
+
+def _compact_ws(crg, c, n_seqs):
+    sh = crg.make_shape(c["k"], c["k"], c["v"], None, 1)
+    sh.n_seqs = n_seqs
+    return crg.Workspace(crg.gdn_chunk_fwd_min_workspace_bytes(sh), DEV)
+
+
+@pytest.mark.parametrize("lengths,V", [([1000], 128), ([64, 1, 200, 0, 77], 128), ([300], 96)])
+def test_chunk_fwd_compact_workspace(crg, lengths, V):
+    """A workspace of gdn_chunk_fwd_min_workspace_bytes selects the compact kernel pair
+    (only T per chunk kept); its results match the oracle as the split path's do."""
+    c = make_case(lengths, 2, 4, 128, V, "bf16", "mild", True, seed=40 + V)
+    d = lambda t: None if t is None else t.to(DEV)
+    sh = crg.make_shape(c["q"], c["k"], c["v"], d(c["cu"]), c["B"])
+    full, small = crg.gdn_chunk_fwd_workspace_bytes(sh), crg.gdn_chunk_fwd_min_workspace_bytes(sh)
+    assert small <= full
+    ws = crg.Workspace(small, DEV)
+    o, hT = crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]),
+                              d(c["cu"]), c["scale"], True, B=c["B"], workspace=ws)
+    ro, rh = run_oracle(c)
+    assert_close(o.cpu(), ro, "bf16", "compact o")
+    assert_close(hT.cpu(), rh, "bf16", "compact h_T")
+    assert ws.status() == 0
+
+
+def test_segment_summary_compact_workspace(crg):
+    """gdn_segment_summary with only room for T per chunk takes the compact pair."""
+    bounds = [0, 70, 70, 256]
+    c = make_case([256], 2, 4, 128, 128, "bf16", "mild", True, seed=47)
+    b = torch.tensor(bounds, dtype=torch.int32)
+    d = lambda t: t.to(DEV)
+    ws = _compact_ws(crg, c, len(bounds) - 1)
+    M, S = crg.gdn_segment_summary(d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(b), workspace=ws)
+    rM, rS = oracle.segment_summary(to64(c["k"]), to64(c["v"]), to64(c["g"]), to64(c["beta"]),
+                                    np.array(bounds, np.int32), l2norm_qk=True)
+    assert_close(M.cpu(), rM, "bf16", "compact M")
+    assert_close(S.cpu(), rS, "bf16", "compact S_local")
