@@ -78,12 +78,18 @@ constexpr int kXP = C + 4;  // fp32 row of A, padded (rows stay 16-byte aligned)
 constexpr uint32_t OP_KQ = 0;      // [2 halves][128 rows][128 B]: rows 0-63 raw k, 64-127 raw q;
                                    // once Q K^T is done, T hi and T lo take the q rows' places
 constexpr uint32_t OP_TH = 8192, OP_TL = 24576;
-constexpr uint32_t OP_VT = 32768;  // raw v: [V / 64 blocks][64 tokens][128 B], SW128
+// Raw v ([V / 64 blocks][64 tokens][128 B], SW128).  Up to V = 128 it is loaded late, into
+// the k rows once W = T diag(b/|k|) K has read them (blocks 16 KB apart), which keeps a
+// block at 50 KB of shared memory so that four fit on an SM; wider v has its own region.
+__host__ __device__ constexpr bool op_late_v(int V) { return V <= 128; }
+__host__ __device__ constexpr uint32_t op_vt(int V) { return op_late_v(V) ? 0u : 32768u; }
+__host__ __device__ constexpr uint32_t op_vt_stride(int V) { return op_late_v(V) ? 16384u : 8192u; }
 // A, then (I + A)^-1 in place, then the T diag(b/|k|) hi / lo tiles
-__host__ __device__ constexpr uint32_t op_x(int V) { return OP_VT + (uint32_t)V * 128; }
-// partial block products of the inversion: 4 x [16][kZP] fp32 after A's 64 x kXP floats
-__host__ __device__ constexpr uint32_t op_zs(int V) { return op_x(V) + 17408; }
-__host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + 22528 + 1024; }
+__host__ __device__ constexpr uint32_t op_x(int V) { return op_late_v(V) ? 32768u : 32768u + (uint32_t)V * 128; }
+// partial block products of the inversion, 4 x [16][kZP] fp32: in the q rows (free once
+// Q K^T is done, not yet holding T) or after A
+__host__ __device__ constexpr uint32_t op_zs(int V) { return op_late_v(V) ? OP_TH : op_x(V) + 17408; }
+__host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + (op_late_v(V) ? 17408u : 22528u) + 1024; }
 
 // Y = (I + A)^-1 for the strictly lower 64 x 64 A held in X (fp32, row stride kXP), in
 // place, by 16 x 16 blocks: the diagonal blocks by forward substitution, then the
@@ -253,13 +259,14 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   if (tid == 0) {
     const int32_t tt = (int32_t)t0;
-    mbar_arrive_expect_tx(&ld_bar, (4 + NVB) * 8192);
+    mbar_arrive_expect_tx(&ld_bar, (4 + (op_late_v(V) ? 0 : NVB)) * 8192);
     tma_load_3d(sm + OP_KQ, &tm_k, &ld_bar, 0, qh, tt);
     tma_load_3d(sm + OP_KQ + 16384, &tm_k, &ld_bar, 64, qh, tt);
     tma_load_3d(sm + OP_KQ + 8192, &tm_q, &ld_bar, 0, qh, tt);
     tma_load_3d(sm + OP_KQ + 24576, &tm_q, &ld_bar, 64, qh, tt);
+    if (!op_late_v(V))
 #pragma unroll
-    for (int nb = 0; nb < NVB; ++nb) tma_load_3d(sm + OP_VT + nb * 8192, &tm_v, &ld_bar, nb * 64, h, tt);
+      for (int nb = 0; nb < NVB; ++nb) tma_load_3d(sm + op_vt(V) + nb * 8192, &tm_v, &ld_bar, nb * 64, h, tt);
   }
   if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
   else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
@@ -460,6 +467,17 @@ __global__ void __launch_bounds__(128)
   const bool has_row = lane < 16;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
+    if (op_late_v(V) && pass == 1) {
+      const bool ok = tid != 0 || mbar_wait(&ld_bar, 1, kSpin);
+      if (__syncthreads_or(!ok)) {
+        if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
+        (void)mbar_wait(&ld_bar, 1, kSpin);  // the copy lands before shared memory is released
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tm, kCols);
+        return;
+      }
+    }
     if (tid == 0) {
       if (pass == 0) {
         const uint32_t tp_a = smem_u32(X);
@@ -471,11 +489,11 @@ __global__ void __launch_bounds__(128)
           umma_bf16(tm, smem_desc(tp_a + 8192 + ks * 32, 16, 1024, 2), kb, id_w, 1);
         }
       } else {
-        const uint32_t vt_a = smem_u32(sm + OP_VT);
+        const uint32_t vt_a = smem_u32(sm + op_vt(V));
         const uint32_t id_u = idesc_bf16(64, V, false, true);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks) {
-          const uint64_t vb = smem_desc(vt_a + ks * 2048, 8192, 1024, 2);
+          const uint64_t vb = smem_desc(vt_a + ks * 2048, op_vt_stride(V), 1024, 2);
           umma_bf16(tm, smem_desc(kq_a + OP_TH + ks * 32, 16, 1024, 2), vb, id_u, ks > 0);
           umma_bf16(tm, smem_desc(kq_a + OP_TL + ks * 32, 16, 1024, 2), vb, id_u, 1);
         }
@@ -484,7 +502,15 @@ __global__ void __launch_bounds__(128)
     }
     {
       const uint32_t par = pass == 0 ? 1u : 0u;  // completions 2 and 3 of the barrier
-      const bool ok = tid != 0 || mbar_wait(&bar, par, kSpin);
+      bool ok = tid != 0 || mbar_wait(&bar, par, kSpin);
+      if (op_late_v(V) && pass == 0 && tid == 0 && ok) {
+        // W has read the k rows: v goes there while -W drains
+        const int32_t tt = (int32_t)t0;
+        mbar_arrive_expect_tx(&ld_bar, NVB * 8192);
+#pragma unroll
+        for (int nb = 0; nb < NVB; ++nb)
+          tma_load_3d(sm + op_vt(V) + nb * op_vt_stride(V), &tm_v, &ld_bar, nb * 64, h, tt);
+      }
       if (__syncthreads_or(!ok)) {
         if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
         (void)mbar_wait(&bar, par, kSpin);
