@@ -18,18 +18,18 @@
 // a hi + lo pair of bf16 matrices; the diagonal of P (the largest term of
 // the largest outputs) is added in fp32 outside the MMA.
 //
-// Two kernels:
+// This is the compact-workspace pair (only T of every chunk is kept between the
+// kernels; chunk_scan.cu holds the split pair used when the workspace has room
+// for full operand records):
 //  * chunk_prep_kernel (fully parallel over chunk x q/k head): K K^T on the
 //    tensor core, then per v-head the 64 x 64 forward substitution for T in
 //    fp32 on CUDA cores; T is written packed (lower triangle incl. diagonal,
-//    fp32, 8320 bytes per chunk and v-head) to the workspace.  It is the only
-//    state-independent step that is sequential inside a chunk, so it runs off
-//    the state chain.
-//  * chunk_tc_kernel (one block per sequence x v-head x 32 value columns):
-//    walks the chunks in order with the fp32 state transposed in registers
-//    (thread f holds row f of S^T, one TMEM lane per key feature), TMA
-//    prefetching chunk c+1 while chunk c runs, and every contraction on
-//    tcgen05: Q K^T, W, U, U' = U - W S^T, Q S^T, P U', K^T diag(d) U'.
+//    fp32, 8320 bytes per chunk and v-head) to the workspace.
+//  * chunk_ws_kernel (one block per sequence x v-head x 32 value columns):
+//    one warpgroup rebuilds chunk c+1's operands from T while the other walks
+//    the state chain of chunk c, with the fp32 state transposed in registers
+//    (thread f holds row f of S^T, one TMEM lane per key feature) and every
+//    contraction on tcgen05: Q K^T, W, U, U' = U - W S^T, Q S^T, P U', K^T diag(d) U'.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -291,417 +291,7 @@ struct TcParams {
   float *M, *S_local;
 };
 
-// dynamic shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t OFF_QK = 0;          // 2 stages x 32 KB: [fb][rows 0-63 k | 64-127 q][128 B], raw bf16
-constexpr uint32_t OFF_V = 65536;       // 2 stages x 4 KB:  [64 tok][32 v] SW64
-constexpr uint32_t OFF_TP = 73728;      // 2 stages x 8448 B: packed fp32 T
-constexpr uint32_t kTPStride = 8448;
-constexpr uint32_t OFF_TH = 91136;      // 8 KB T hi            [64][128 B] SW128
-constexpr uint32_t OFF_TL = 99328;      // 8 KB T lo
-constexpr uint32_t OFF_TPH = 107520;    // 8 KB T diag(b/|k|) hi
-constexpr uint32_t OFF_TPL = 115712;    // 8 KB T diag(b/|k|) lo
-constexpr uint32_t OFF_NW = 123904;     // 16 KB -W              [fb][64][128 B]
-constexpr uint32_t OFF_QT = 140288;     // 16 KB (unused)
-constexpr uint32_t OFF_PT = 156672;     // 8 KB  P without its diagonal [64][128 B]
-constexpr uint32_t OFF_ST = 164864;     // 8 KB  S^T (bf16)      [128 feat][32 v] SW64
-constexpr uint32_t OFF_UP = 173056;     // 4 KB  U' hi           [64 tok][32 v] SW64
-constexpr uint32_t OFF_DU = 177152;     // 4 KB  diag(d/|k|) U' hi
-constexpr uint32_t OFF_UPL = 181248;    // 4 KB  U' lo
-constexpr uint32_t OFF_DUL = 185344;    // 4 KB  diag(d/|k|) U' lo
-constexpr uint32_t kTcSmem = 189440 + 1024;
-constexpr uint32_t kStageBytes = 4 * 8192 + 4096 + (uint32_t)kTBytes;  // k, q (2 boxes each), v, T
-
-// TMEM columns
-constexpr uint32_t COL_QK = 0, COL_W = 64, COL_U = 192, COL_O = 224, COL_S = 256, COL_OB = 288,
-                   kTmemCols = 512;
-
-__device__ __forceinline__ void put_bf16(uint8_t *tile, int row, int col, float x) {
-  *reinterpret_cast<__nv_bfloat16 *>(tile + sw128_off(row, col)) = __float2bfloat16_rn(x);
-}
-
-__global__ void __launch_bounds__(NT, 1)
-    chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
-  extern __shared__ uint8_t smraw[];
-  uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t bar_tma[2], bar_mma;
-  __shared__ uint32_t tbase;
-  __shared__ float gam[C], gl2[C], bex[C], dec[C], kinv[C], qinv[C], alpha[C];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int v0 = blockIdx.x * BVT, h = blockIdx.y, s = blockIdx.z;
-  const int qh = h / (p.Hv / p.Hqk);
-  int64_t start, end;
-  seq_range(p.cu, p.row_T, s, start, end);
-  if (start < 0 || end < start || end > p.n_tok) {
-    if (tid == 0) set_status(p.status, GDN_ERR_BOUNDS);
-    return;
-  }
-  const int n_chunks = (int)((end - start + C - 1) / C);
-  const int64_t sbase = (int64_t)s + start / C;
-  const uint32_t sb = smem_u32(sm);
-
-  if (tid == 0) {
-    mbar_init(&bar_tma[0], 1);
-    mbar_init(&bar_tma[1], 1);
-    mbar_init(&bar_mma, 1);
-    fence_mbar_init();
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-  }
-  if (warp == 0) {
-    tmem_alloc(&tbase, kTmemCols);
-    tmem_relinquish();
-  }
-  // fp32 state, transposed: thread f holds S[v0 + v][f] for v < 32
-  float S[BVT];
-  const float *h0p = p.h0 ? p.h0 + (((size_t)s * p.Hv + h) * p.V + v0) * KD + tid : nullptr;
-#pragma unroll
-  for (int v = 0; v < BVT; ++v) S[v] = h0p ? h0p[(size_t)v * KD] : 0.f;
-  auto write_state_bf16 = [&]() {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 o = make_uint4(pack_bf16(S[q * 8 + 0], S[q * 8 + 1]), pack_bf16(S[q * 8 + 2], S[q * 8 + 3]),
-                           pack_bf16(S[q * 8 + 4], S[q * 8 + 5]), pack_bf16(S[q * 8 + 6], S[q * 8 + 7]));
-      *reinterpret_cast<uint4 *>(sm + OFF_ST + sw64_off(tid, q * 8)) = o;
-    }
-  };
-  write_state_bf16();
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tm = tbase;
-  const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter
-
-  auto issue_tma = [&](int ci, int st) {
-    const int64_t t0 = start + (int64_t)ci * C;
-    const float *tsrc = p.T + ((size_t)(sbase + ci) * p.Hv + h) * kTPacked;
-    uint8_t *qk = sm + OFF_QK + st * 32768;
-    mbar_arrive_expect_tx(&bar_tma[st], kStageBytes);
-    tma_load_3d(qk, &tm_k, &bar_tma[st], 0, qh, (int32_t)t0);
-    tma_load_3d(qk + 16384, &tm_k, &bar_tma[st], 64, qh, (int32_t)t0);
-    tma_load_3d(qk + 8192, &tm_q, &bar_tma[st], 0, qh, (int32_t)t0);
-    tma_load_3d(qk + 16384 + 8192, &tm_q, &bar_tma[st], 64, qh, (int32_t)t0);
-    tma_load_3d(sm + OFF_V + st * 4096, &tm_v, &bar_tma[st], v0, h, (int32_t)t0);
-    bulk_load(sm + OFF_TP + st * kTPStride, tsrc, (uint32_t)kTBytes, &bar_tma[st]);
-  };
-  if (tid == 0 && n_chunks > 0) issue_tma(0, 0);
-  // what is in flight, tracked identically by every thread (the issuing thread is tid 0)
-  bool tma_inflight[2] = {n_chunks > 0, false};
-  bool mma_inflight = false;
-  uint32_t ph_tma[2] = {0u, 0u}, ph_mma = 0;
-  bool failed = false;
-  auto commit_mma = [&]() {
-    if (tid == 0) umma_commit(&bar_mma);
-    mma_inflight = true;
-  };
-  auto wait_mma = [&]() -> bool {
-    const bool ok = mbar_wait(&bar_mma, ph_mma, kSpin);
-    if (__syncthreads_or(!ok)) return false;
-    ph_mma ^= 1u;
-    mma_inflight = false;
-    return true;
-  };
-  auto sync_smem_for_mma = [&]() {
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  };
-
-  // g of the first chunk; later chunks' g is loaded one chunk ahead
-  float gnext = 0.f;
-  if (n_chunks > 0 && tid < C && start + tid < end) gnext = p.g[(start + tid) * p.Hv + h];
-  const bool lane_row = lane < 16;      // rows of M = 64 results: lanes 0-15 of each quarter
-  const int mrow = warp * 16 + lane;    // the token row this thread holds in M = 64 results
-  const int row = mrow & 63;            // in-range index for the threads without a row
-  const size_t o_tok_stride = (size_t)p.Hv * p.V;
-
-  for (int ci = 0; ci < n_chunks && !failed; ++ci) {
-    const int st = ci & 1;
-    const int64_t t0 = start + (int64_t)ci * C;
-    const int n = (int)min((int64_t)C, end - t0);
-    const uint8_t *qk = sm + OFF_QK + st * 32768;
-    const uint32_t qk_a = sb + OFF_QK + st * 32768;
-    const uint32_t v_a = sb + OFF_V + st * 4096;
-    const float *tp = reinterpret_cast<const float *>(sm + OFF_TP + st * kTPStride);
-    if (ci + 1 < n_chunks) {
-      if (tid == 0) issue_tma(ci + 1, st ^ 1);
-      tma_inflight[st ^ 1] = true;
-    }
-    // ---- gates of this chunk: gamma (cumsum), b = exp(gamma), d = exp(gamma_last - gamma)
-    if (tid < C) gam[tid] = gnext;
-    if (ci + 1 < n_chunks && tid < C) {
-      const int64_t t1 = t0 + C;
-      gnext = (t1 + tid < end) ? p.g[(t1 + tid) * p.Hv + h] : 0.f;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const float g0 = gam[2 * lane], g1 = gam[2 * lane + 1];
-      float incl = g0 + g1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      const float last = __shfl_sync(0xffffffffu, incl, 31);
-      const float ga = incl - g1, gb = incl;
-      gam[2 * lane] = ga;
-      gam[2 * lane + 1] = gb;
-      gl2[2 * lane] = ga * 1.4426950408889634f;
-      gl2[2 * lane + 1] = gb * 1.4426950408889634f;
-      bex[2 * lane] = expf(ga);
-      bex[2 * lane + 1] = expf(gb);
-      dec[2 * lane] = expf(last - ga);
-      dec[2 * lane + 1] = expf(last - gb);
-    }
-    // ---- wait for this chunk's tiles
-    {
-      const bool ok = mbar_wait(&bar_tma[st], ph_tma[st], kSpin);
-      if (__syncthreads_or(!ok)) { failed = true; break; }
-      ph_tma[st] ^= 1u;
-      tma_inflight[st] = false;
-    }
-    // ---- 1/|k| and 1/|q| per token (threads 0-63 k rows, 64-127 q rows);
-    //      q rows also give the bf16 operand scale * b / |q| * q
-    {
-      const int r = tid & 63;
-      const bool isq = tid >= 64;
-      const uint8_t *rowbase = qk + (isq ? 8192 : 0);
-      float ss = 0.f;
-#pragma unroll
-      for (int fb = 0; fb < 2; ++fb)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 u = *reinterpret_cast<const uint4 *>(rowbase + fb * 16384 + sw128_off(r, j * 8));
-          const uint32_t *w = reinterpret_cast<const uint32_t *>(&u);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = unpack_bf16(w[e]);
-            ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-          }
-        }
-      const float inv = p.l2norm ? 1.f / sqrtf(ss + kL2Eps) : 1.f;
-      if (!isq) {
-        kinv[r] = inv;
-      } else {
-        qinv[r] = inv;
-        alpha[r] = p.scale * bex[r] * inv;
-      }
-    }
-    __syncthreads();
-    // ---- T (fp32, packed) -> bf16 hi/lo tiles of T and of T diag(b / |k|); thread = (row, 32 columns)
-    {
-      const int r = tid & 63, cb = (tid >> 6) * 32;
-      const float *trow = tp + r * (r + 1) / 2;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c0 = cb + q * 8;
-        uint32_t wh[4], wl[4], xh[4], xl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float t[2], t2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = c0 + 2 * e + u;
-            t[u] = (c <= r) ? trow[c] : 0.f;
-            t2[u] = t[u] * bex[c] * kinv[c];
-          }
-          const float h0 = __bfloat162float(__float2bfloat16_rn(t[0]));
-          const float h1 = __bfloat162float(__float2bfloat16_rn(t[1]));
-          const float g0 = __bfloat162float(__float2bfloat16_rn(t2[0]));
-          const float g1 = __bfloat162float(__float2bfloat16_rn(t2[1]));
-          wh[e] = pack_bf16(h0, h1);
-          wl[e] = pack_bf16(t[0] - h0, t[1] - h1);
-          xh[e] = pack_bf16(g0, g1);
-          xl[e] = pack_bf16(t2[0] - g0, t2[1] - g1);
-        }
-        const uint32_t off = sw128_off(r, c0);
-        *reinterpret_cast<uint4 *>(sm + OFF_TH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_TL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_TPH + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_TPL + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
-      }
-    }
-    sync_smem_for_mma();
-    // ---- state-independent MMAs: Q K^T, W = T diag(b/|k|) K (hi + lo), U = T V (hi + lo)
-    if (tid == 0) {
-      const uint32_t id_qk = idesc_bf16(64, 64, false, false);
-#pragma unroll
-      for (int ks = 0; ks < KD / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(tm + COL_QK, smem_desc(qk_a + 8192 + off, 16, 1024, 2),
-                  smem_desc(qk_a + off, 16, 1024, 2), id_qk, ks > 0);
-      }
-      const uint32_t id_w = idesc_bf16(64, 128, false, true);
-      const uint32_t id_u = idesc_bf16(64, BVT, false, true);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) {
-        const uint64_t kb = smem_desc(qk_a + ks * 2048, 16384, 1024, 2);
-        const uint64_t vb = smem_desc(v_a + ks * 1024, 2048, 512, 4);
-        umma_bf16(tm + COL_W, smem_desc(sb + OFF_TPH + ks * 32, 16, 1024, 2), kb, id_w, ks > 0);
-        umma_bf16(tm + COL_W, smem_desc(sb + OFF_TPL + ks * 32, 16, 1024, 2), kb, id_w, 1);
-        umma_bf16(tm + COL_U, smem_desc(sb + OFF_TH + ks * 32, 16, 1024, 2), vb, id_u, ks > 0);
-        umma_bf16(tm + COL_U, smem_desc(sb + OFF_TL + ks * 32, 16, 1024, 2), vb, id_u, 1);
-      }
-    }
-    commit_mma();
-    if (!wait_mma()) { failed = true; break; }
-    tc_fence_after();
-    // ---- P = scale (Q_hat K_hat^T * Gamma), strictly lower part -> bf16 tile, diagonal kept
-    //      in fp32; -W -> bf16 tile
-    float pdiag = 0.f;
-    {
-      const float gr2 = gl2[row], qr = p.scale * qinv[row];
-#pragma unroll
-      for (int c0 = 0; c0 < C; c0 += 16) {
-        float v[16];
-        tmem_ld16(tl + COL_QK + c0, v);
-        tmem_wait_ld();
-        if (lane_row) {
-          uint32_t w[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j0 = c0 + 2 * e, j1 = j0 + 1;
-            const float a = (j0 < mrow) ? qr * kinv[j0] * exp2f(gr2 - gl2[j0]) * v[2 * e] : 0.f;
-            const float b = (j1 < mrow) ? qr * kinv[j1] * exp2f(gr2 - gl2[j1]) * v[2 * e + 1] : 0.f;
-            if (j0 == mrow) pdiag = qr * kinv[j0] * v[2 * e];
-            if (j1 == mrow) pdiag = qr * kinv[j1] * v[2 * e + 1];
-            w[e] = pack_bf16(a, b);
-          }
-          *reinterpret_cast<uint4 *>(sm + OFF_PT + sw128_off(mrow, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4 *>(sm + OFF_PT + sw128_off(mrow, c0 + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < KD; c0 += 16) {
-        float v[16];
-        tmem_ld16(tl + COL_W + c0, v);
-        tmem_wait_ld();
-        if (lane_row) {
-          uint32_t w[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) w[e] = pack_bf16(-v[2 * e], -v[2 * e + 1]);
-          const int fb = c0 >> 6, cc = c0 & 63;
-          *reinterpret_cast<uint4 *>(sm + OFF_NW + fb * 8192 + sw128_off(mrow, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4 *>(sm + OFF_NW + fb * 8192 + sw128_off(mrow, cc + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      }
-    }
-    sync_smem_for_mma();
-    // ---- state chain, round 1: U' = U - W S^T ; Q S^T (raw q; scale b / |q| applied per row later)
-    if (tid == 0) {
-      const uint32_t id = idesc_bf16(64, BVT, false, true);
-#pragma unroll
-      for (int ks = 0; ks < KD / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-        const uint64_t bs = smem_desc(sb + OFF_ST + ks * 1024, 2048, 512, 4);
-        umma_bf16(tm + COL_U, smem_desc(sb + OFF_NW + off, 16, 1024, 2), bs, id, 1);
-        const uint32_t qoff = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(tm + COL_O, smem_desc(qk_a + qoff, 16, 1024, 2), bs, id, ks > 0);
-      }
-    }
-    commit_mma();
-    if (!wait_mma()) { failed = true; break; }
-    tc_fence_after();
-    float up[BVT];  // U' row of this thread (fp32), reused for the diagonal term of O
-    tmem_ld16(tl + COL_U, *reinterpret_cast<float(*)[16]>(up));
-    tmem_ld16(tl + COL_U + 16, *reinterpret_cast<float(*)[16]>(up + 16));
-    tmem_wait_ld();
-    if (lane_row) {
-      const float dr = dec[mrow] * kinv[mrow];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c0 = q * 8;
-        uint32_t uh[4], ul[4], dh[4], dl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = up[c0 + 2 * e], b = up[c0 + 2 * e + 1];
-          const float ah = __bfloat162float(__float2bfloat16_rn(a));
-          const float bh = __bfloat162float(__float2bfloat16_rn(b));
-          uh[e] = pack_bf16(ah, bh);
-          ul[e] = pack_bf16(a - ah, b - bh);
-          const float da = dr * a, db = dr * b;
-          const float dah = __bfloat162float(__float2bfloat16_rn(da));
-          const float dbh = __bfloat162float(__float2bfloat16_rn(db));
-          dh[e] = pack_bf16(dah, dbh);
-          dl[e] = pack_bf16(da - dah, db - dbh);
-        }
-        const uint32_t off = sw64_off(mrow, c0);
-        *reinterpret_cast<uint4 *>(sm + OFF_UP + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_UPL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_DU + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-        *reinterpret_cast<uint4 *>(sm + OFF_DUL + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
-      }
-    }
-    sync_smem_for_mma();
-    // ---- state chain, round 2: O += P U' (strictly lower P) ; dS^T = K^T diag(d/|k|) U'
-    //      (U' as a hi + lo pair of bf16 operands)
-    if (tid == 0) {
-      const uint32_t id_o = idesc_bf16(64, BVT, false, true);
-      const uint32_t id_s = idesc_bf16(128, BVT, true, true);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) {
-        const uint64_t pa = smem_desc(sb + OFF_PT + ks * 32, 16, 1024, 2);
-        const uint64_t ka = smem_desc(qk_a + ks * 2048, 16384, 1024, 2);
-        umma_bf16(tm + COL_OB, pa, smem_desc(sb + OFF_UP + ks * 1024, 2048, 512, 4), id_o, ks > 0);
-        umma_bf16(tm + COL_OB, pa, smem_desc(sb + OFF_UPL + ks * 1024, 2048, 512, 4), id_o, 1);
-        umma_bf16(tm + COL_S, ka, smem_desc(sb + OFF_DU + ks * 1024, 2048, 512, 4), id_s, ks > 0);
-        umma_bf16(tm + COL_S, ka, smem_desc(sb + OFF_DUL + ks * 1024, 2048, 512, 4), id_s, 1);
-      }
-    }
-    commit_mma();
-    if (!wait_mma()) { failed = true; break; }
-    tc_fence_after();
-    {
-      const float blast = bex[C - 1];
-      float ds[BVT], ov[BVT], ob[BVT];
-      tmem_ld16(tl + COL_S, *reinterpret_cast<float(*)[16]>(ds));
-      tmem_ld16(tl + COL_S + 16, *reinterpret_cast<float(*)[16]>(ds + 16));
-      tmem_ld16(tl + COL_O, *reinterpret_cast<float(*)[16]>(ov));
-      tmem_ld16(tl + COL_O + 16, *reinterpret_cast<float(*)[16]>(ov + 16));
-      tmem_ld16(tl + COL_OB, *reinterpret_cast<float(*)[16]>(ob));
-      tmem_ld16(tl + COL_OB + 16, *reinterpret_cast<float(*)[16]>(ob + 16));
-      tmem_wait_ld();
-#pragma unroll
-      for (int v = 0; v < BVT; ++v) S[v] = fmaf(blast, S[v], ds[v]);
-      write_state_bf16();
-      if (lane_row && mrow < n) {
-#pragma unroll
-        for (int v = 0; v < BVT; ++v) ov[v] = fmaf(alpha[mrow], ov[v], fmaf(pdiag, up[v], ob[v]));
-        const size_t off = (size_t)(t0 + mrow) * o_tok_stride + (size_t)h * p.V + v0;
-        if (p.o_f32) {
-          float4 *dst = reinterpret_cast<float4 *>((float *)p.o + off);
-#pragma unroll
-          for (int q = 0; q < BVT / 4; ++q) dst[q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
-        } else {
-          uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)p.o + off);
-#pragma unroll
-          for (int q = 0; q < BVT / 8; ++q)
-            dst[q] = make_uint4(pack_bf16(ov[8 * q], ov[8 * q + 1]), pack_bf16(ov[8 * q + 2], ov[8 * q + 3]),
-                                pack_bf16(ov[8 * q + 4], ov[8 * q + 5]), pack_bf16(ov[8 * q + 6], ov[8 * q + 7]));
-        }
-      }
-    }
-    sync_smem_for_mma();
-  }
-  if (failed) {
-    if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
-    // copies or MMAs still in flight land before shared memory and TMEM are released
-    for (int i = 0; i < 2; ++i)
-      if (tma_inflight[i]) (void)mbar_wait(&bar_tma[i], ph_tma[i], kSpin);
-    if (mma_inflight) (void)mbar_wait(&bar_mma, ph_mma, kSpin);
-  } else if (p.hT) {
-    float *dst = p.hT + (((size_t)s * p.Hv + h) * p.V + v0) * KD + tid;
-#pragma unroll
-    for (int v = 0; v < BVT; ++v) dst[(size_t)v * KD] = S[v];
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tm, kTmemCols);
-}
+constexpr uint32_t kTmemCols = 512;
 
 // ======================================== warp-specialised main kernel
 //

@@ -28,12 +28,15 @@ def _inputs(seed, T=1000, Hqk=2, Hv=4, K=128, V=128):
     return [t.to(DEV) for t in (q, k, v, g, beta, h0)]
 
 
-def test_noalloc_matches_gdn_chunk_fwd_twice():
+@pytest.mark.parametrize("T,Hv", [(1000, 4), (4096, 8)])
+def test_noalloc_matches_gdn_chunk_fwd_twice(T, Hv):
+    """(1000, 4): the full operand records fit the 16 MiB array (split kernels);
+    (4096, 8): only the compact workspace fits (compact kernels)."""
     import chunked_recurrence_gb300 as crg
     from tests.parity import assert_close
     crg.load()
     for seed in (101, 202):
-        q, k, v, g, beta, h0 = _inputs(seed)
+        q, k, v, g, beta, h0 = _inputs(seed, T=T, Hv=Hv)
         o_ref, h_ref = crg.gdn_chunk_fwd(q, k, v, g, beta, h0)
         o = torch.empty_like(o_ref)
         h = torch.empty_like(h_ref)
