@@ -352,41 +352,64 @@ def _kinfo(ms, nbytes, peaks):
 
 
 def run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws):
-    """Same step through the public API, with the step's inputs copied from pinned host
-    memory and its results (o, h_T) read back inside the timed region."""
-    host = {k: inp[k].cpu().pin_memory() for k in ("x", "a", "b")}
-    if inp["h0"] is not None:
-        host["h0"] = inp["h0"].cpu().pin_memory()
-    dev_in = {k: torch.empty_like(inp[k]) for k in host}
-    o_host = torch.empty(bufs["o"].shape, dtype=bufs["o"].dtype).pin_memory()
-    h_host = torch.empty(bufs["h_T"].shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = o_host.numel() * o_host.element_size() + h_host.numel() * 4
+    """The same step through the public API (layer_fwd), with each step's inputs copied
+    from pinned host memory and its results (o, h_T) read back inside the timed region.
+    Copies and compute run on three streams with two buffer slots, as a caller that
+    overlaps transfers would drive the API: step i's host->device copy and step i-1's
+    device->host copy overlap the compute of the steps around them."""
+    keys = ["x", "a", "b"] + (["h0"] if inp["h0"] is not None else [])
+    host_in = {k: inp[k].cpu().pin_memory() for k in keys}
+    slots = 2
+    dev_in = [{k: torch.empty_like(inp[k]) for k in keys} for _ in range(slots)]
+    outs = [dict(g=bufs["g"], beta=bufs["beta"], y=bufs["y"], o=torch.empty_like(bufs["o"]),
+                 h_T=torch.empty_like(bufs["h_T"])) for _ in range(slots)]
+    host_out = [(torch.empty(bufs["o"].shape, dtype=bufs["o"].dtype).pin_memory(),
+                 torch.empty(bufs["h_T"].shape, dtype=torch.float32).pin_memory()) for _ in range(slots)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out[0][0].numel() * host_out[0][0].element_size() + host_out[0][1].numel() * 4
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    ev_in, ev_comp, ev_out = [ev() for _ in range(slots)], [ev() for _ in range(slots)], [ev() for _ in range(slots)]
 
-    def one():
-        for k, t in host.items():
-            dev_in[k].copy_(t, non_blocking=True)
-        r = crg.layer_fwd(dev_in["x"], inp["conv_w"], dev_in["a"], dev_in["b"], inp["A_log"],
-                          inp["dt_bias"], wl.Hqk, wl.Hv, wl.K, wl.V, dev_in.get("h0"), cu, wl.B,
-                          inp["scale"], bufs=bufs)
-        o_host.copy_(r["o"], non_blocking=True)
-        h_host.copy_(r["h_T"], non_blocking=True)
+    def one(i):
+        sl = i % slots
+        with torch.cuda.stream(s_in):
+            if i >= slots:
+                s_in.wait_event(ev_comp[sl])  # the slot's inputs were read by step i - 2
+            for k in keys:
+                dev_in[sl][k].copy_(host_in[k], non_blocking=True)
+            ev_in[sl].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in[sl])
+            if i >= slots:
+                s_comp.wait_event(ev_out[sl])  # the slot's outputs were read back
+            d = dev_in[sl]
+            crg.layer_fwd(d["x"], inp["conv_w"], d["a"], d["b"], inp["A_log"], inp["dt_bias"],
+                          wl.Hqk, wl.Hv, wl.K, wl.V, d.get("h0"), cu, wl.B, inp["scale"],
+                          stream=s_comp, bufs=outs[sl])
+            ev_comp[sl].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[sl])
+            host_out[sl][0].copy_(outs[sl]["o"], non_blocking=True)
+            host_out[sl][1].copy_(outs[sl]["h_T"], non_blocking=True)
+            ev_out[sl].record(s_out)
 
-    for _ in range(max(1, args.warmup)):
-        one()
+    for i in range(max(2, args.warmup)):
+        one(i)
     torch.cuda.synchronize()
     n = max(3, min(args.steps, 20))
     _barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        one()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(n):
+        one(i)
+    e1.record(s_out)  # after the last read-back, which follows every step's compute and copies
     torch.cuda.synchronize()
     ms = _max_over_ranks(e0.elapsed_time(e1) / n, ws, dev)
     tok = _sum_over_ranks(float(inp["n_tok"]), ws, dev)
     return {"value": round(tok / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "pipeline": "3 streams (H2D, compute, D2H), 2 buffer slots"}
 
 
 def run_segment_leg(crg, args, dev, stream, peaks):
