@@ -156,14 +156,14 @@ class ClockSampler:
 
 
 def _kernel_sha() -> str:
-    """Hash of the chunk-kernel sources: a stored ncu traffic figure is valid for these only."""
+    """Hash of the sources chunk_operand_kernel and chunk_scan_kernel compile from: a stored
+    ncu traffic figure is valid for these only."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_recurrence_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.startswith("chunk") or fn.endswith(".cuh"):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode())
-                h.update(f.read())
+    for fn in ("chunk_common.cuh", "chunk_scan.cu", "common.cuh", "sm100.cuh"):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
