@@ -84,133 +84,44 @@ constexpr uint32_t OP_TH = 8192, OP_TL = 24576;
 __host__ __device__ constexpr bool op_late_v(int V) { return V <= 128; }
 __host__ __device__ constexpr uint32_t op_vt(int V) { return op_late_v(V) ? 0u : 32768u; }
 __host__ __device__ constexpr uint32_t op_vt_stride(int V) { return op_late_v(V) ? 16384u : 8192u; }
-// A, then (I + A)^-1 in place, then the T diag(b/|k|) hi / lo tiles
+// A, then (I + A)^-1, both row-major (row stride kXP), then the T diag(b/|k|) hi / lo tiles
 __host__ __device__ constexpr uint32_t op_x(int V) { return op_late_v(V) ? 32768u : 32768u + (uint32_t)V * 128; }
-// partial block products of the inversion, 4 x [16][kZP] fp32: in the q rows (free once
-// Q K^T is done, not yet holding T) or after A
-__host__ __device__ constexpr uint32_t op_zs(int V) { return op_late_v(V) ? OP_TH : op_x(V) + 17408; }
-__host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + (op_late_v(V) ? 17408u : 22528u) + 1024; }
+__host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + 17408u + 1024; }
 
-// Y = (I + A)^-1 for the strictly lower 64 x 64 A held in X (fp32, row stride kXP), in
-// place, by 16 x 16 blocks: the diagonal blocks by forward substitution, then the
-// blocks below them one block-diagonal d = I - J at a time,
-//   Y_IJ = -Y_II sum_{K=J}^{I-1} A_IK Y_KJ.
-// A's blocks below the diagonal stay in place (later sums read them); Y_II replaces
-// A_II, and Y_IJ (J < I) is kept in the unused upper block (J, I), so Y_KJ (K >= J) is
-// X[16 J + m][16 K + c] in every case.  Each block product goes to one warp (a 2 x 4
-// tile per lane), the products of a block-diagonal to different warps with their sums
-// parked in ZS, so a level costs two dependent block products whatever its number of
-// terms.  `lw` is this warp's role; blocks resident on one SM pass different roles to
-// the same hardware warp slot so that the work spreads over the SM's four schedulers.
-constexpr int kZP = 20;  // fp32 row of a parked 16 x 16 product, padded against bank conflicts
-__device__ __forceinline__ void invert_unit_lower(float *X, float *ZS, int lw, int lane) {
-  float y[16];
-  const int b = lw * 16, cc = lane & 15;
-  if (lane < 16) {  // diagonal block lw, column cc
+// Y = (I + A)^-1 for the strictly lower 64 x 64 A in X, by forward substitution swept
+// by columns of A: y_i = delta_ij - sum_{k<i} A_ik y_k, and once row k of Y is final every
+// row below it takes the rank-1 term -A_ik Y_kj.  Each thread keeps an 8 x 4 tile of Y in
+// registers: rows rg + 8 m (m = 0..7) and columns 4 cg + c (c = 0..3), with rg = lane % 8
+// and cg = 4 warp + lane / 8, so the eight owners of one column group sit in one warp.
+// Step k reads row k's four values from their owner (lane k % 8 of the group) by shuffle
+// and A_ik for the thread's rows below k (one shared load each, shared by its 4 columns).
+// No barrier between steps.  Y is left in X, row-major, zero above the diagonal.
+__device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
+  const int lane = tid & 31, rg = lane & 7, cg = (tid >> 5) * 4 + (lane >> 3);
+  float y[8][4];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float4 *ar = reinterpret_cast<const float4 *>(X + (b + r) * kXP + b);
-      float acc = 0.f;
+  for (int m = 0; m < 8; ++m)
 #pragma unroll
-      for (int j4 = 0; j4 < 4; ++j4) {
-        if (4 * j4 < r) {
-          const float4 a = ar[j4];
-          acc = fmaf(a.x, y[4 * j4], acc);
-          if (4 * j4 + 1 < r) acc = fmaf(a.y, y[4 * j4 + 1], acc);
-          if (4 * j4 + 2 < r) acc = fmaf(a.z, y[4 * j4 + 2], acc);
-          if (4 * j4 + 3 < r) acc = fmaf(a.w, y[4 * j4 + 3], acc);
-        }
-      }
-      y[r] = (r == cc) ? 1.f : -acc;  // rows above cc sum only zeros
+    for (int c = 0; c < 4; ++c) y[m][c] = (rg + 8 * m == 4 * cg + c) ? 1.f : 0.f;
+  const float *xr = X + rg * kXP;
+#pragma unroll
+  for (int k = 0; k < C - 1; ++k) {
+    float yk[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) yk[c] = __shfl_sync(0xffffffffu, y[k >> 3][c], (k & 7) | (lane & 24));
+    // rows rg + 8 m with m < k / 8 lie above row k: A_ik = 0 there (and A_kk = 0)
+#pragma unroll
+    for (int m = k >> 3; m < 8; ++m) {
+      const float a = xr[8 * m * kXP + k];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) y[m][c] = fmaf(-a, yk[c], y[m][c]);
     }
   }
-  __syncthreads();  // every read of A_II is done
-  if (lane < 16) {
+  __syncthreads();  // every read of A is done
 #pragma unroll
-    for (int r = 0; r < 16; ++r) X[(b + r) * kXP + b + cc] = y[r];
-  }
+  for (int m = 0; m < 8; ++m)
+    *reinterpret_cast<float4 *>(X + (rg + 8 * m) * kXP + 4 * cg) = make_float4(y[m][0], y[m][1], y[m][2], y[m][3]);
   __syncthreads();
-  const int tr = (lane >> 2) * 2, tc = (lane & 3) * 4;  // this lane's 2 x 4 tile
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    if (lw < (4 - d) * d) {  // product A_IK Y_KJ: block bb (I = d + bb, J = bb), K = J + kk
-      const int bb = lw / d, kk = lw - bb * d;
-      const int I = d + bb, J = bb, K = J + kk;
-      float z[2][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
-#pragma unroll 1
-      for (int m4 = 0; m4 < 4; ++m4) {
-        float4 a[2], yv[4];
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          a[i] = *reinterpret_cast<const float4 *>(X + (16 * I + tr + i) * kXP + 16 * K + 4 * m4);
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm)
-          yv[mm] = *reinterpret_cast<const float4 *>(X + (16 * J + 4 * m4 + mm) * kXP + 16 * K + tc);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            z[i][0] = fmaf(ai[mm], yv[mm].x, z[i][0]);
-            z[i][1] = fmaf(ai[mm], yv[mm].y, z[i][1]);
-            z[i][2] = fmaf(ai[mm], yv[mm].z, z[i][2]);
-            z[i][3] = fmaf(ai[mm], yv[mm].w, z[i][3]);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        *reinterpret_cast<float4 *>(ZS + lw * 16 * kZP + (tr + i) * kZP + tc) =
-            make_float4(z[i][0], z[i][1], z[i][2], z[i][3]);
-    }
-    __syncthreads();
-    if (lw < 4 - d) {  // Y_IJ = -Y_II (sum of block lw's products), into upper block (J, I)
-      const int I = d + lw, J = lw;
-      float z[2][4];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
-#pragma unroll 1
-      for (int m4 = 0; m4 < 4; ++m4) {
-        float4 a[2], zv[4];
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          a[i] = *reinterpret_cast<const float4 *>(X + (16 * I + tr + i) * kXP + 16 * I + 4 * m4);
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-          zv[mm] = *reinterpret_cast<const float4 *>(ZS + (lw * d) * 16 * kZP + (4 * m4 + mm) * kZP + tc);
-          for (int kk = 1; kk < d; ++kk) {
-            const float4 w = *reinterpret_cast<const float4 *>(ZS + (lw * d + kk) * 16 * kZP + (4 * m4 + mm) * kZP + tc);
-            zv[mm].x += w.x;
-            zv[mm].y += w.y;
-            zv[mm].z += w.z;
-            zv[mm].w += w.w;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float ai[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            z[i][0] = fmaf(ai[mm], zv[mm].x, z[i][0]);
-            z[i][1] = fmaf(ai[mm], zv[mm].y, z[i][1]);
-            z[i][2] = fmaf(ai[mm], zv[mm].z, z[i][2]);
-            z[i][3] = fmaf(ai[mm], zv[mm].w, z[i][3]);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        *reinterpret_cast<float4 *>(X + (16 * J + tr + i) * kXP + 16 * I + tc) =
-            make_float4(-z[i][0], -z[i][1], -z[i][2], -z[i][3]);
-    }
-    __syncthreads();
-  }
 }
 
 template <int V>
@@ -404,26 +315,20 @@ __global__ void __launch_bounds__(128)
   }
   __syncthreads();
   // ---- T = (I + A)^-1 diag(beta)
-  invert_unit_lower(X, reinterpret_cast<float *>(sm + op_zs(V)), (warp + (int)(blockIdx.x & 3u)) & 3, lane);
+  invert_unit_lower(X, tid);
   // ---- T and T diag(b/|k|) as bf16 hi/lo K-major tiles (row r, columns cb..cb+31): T's
   //      tiles replace the raw q rows (Q K^T no longer needs them), T diag(b/|k|)'s tiles
   //      replace A once every thread has read its row of the inverse
   {
-    const int r = tid >> 1, cb = (tid & 1) * 32, I = r >> 4;
+    const int r = tid & 63, cb = (tid >> 6) * 32;
     float t[32], cf[32];
 #pragma unroll
-    for (int g16 = 0; g16 < 2; ++g16) {
-      const int J = (cb >> 4) + g16;
-      // row r of Y_IJ: the diagonal block in place, blocks left of it in upper block (J, I)
-      const float *src = (J == I) ? X + r * kXP + 16 * J : X + (16 * J + (r & 15)) * kXP + 16 * I;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float4 a = (J <= I) ? reinterpret_cast<const float4 *>(src)[m] : make_float4(0.f, 0.f, 0.f, 0.f);
-        t[16 * g16 + 4 * m] = a.x;
-        t[16 * g16 + 4 * m + 1] = a.y;
-        t[16 * g16 + 4 * m + 2] = a.z;
-        t[16 * g16 + 4 * m + 3] = a.w;
-      }
+    for (int m = 0; m < 8; ++m) {
+      const float4 a = reinterpret_cast<const float4 *>(X + r * kXP + cb)[m];
+      t[4 * m] = a.x;
+      t[4 * m + 1] = a.y;
+      t[4 * m + 2] = a.z;
+      t[4 * m + 3] = a.w;
     }
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
