@@ -31,6 +31,8 @@
 // applied in fp32); T enters as a hi + lo pair of bf16 matrices; U' and
 // diag(d/|k|) U' enter as hi + lo pairs; the diagonal of P stays fp32.
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 #include <math.h>
 
 #include "chunk_common.cuh"
@@ -71,6 +73,7 @@ struct OpParams {
   float scale;
   uint8_t *rec;
   size_t rec_bytes;
+  int64_t n_items;  // chunk slots x v-heads
   int32_t *status;
 };
 
@@ -125,7 +128,7 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
 }
 
 template <int V>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 4)
     chunk_operand_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const OpParams p) {
   constexpr int NVB = V / 64;                       // 64-column blocks of v
@@ -137,8 +140,26 @@ __global__ void __launch_bounds__(128)
   __shared__ uint64_t bar, ld_bar;
   __shared__ uint32_t tbase;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = (int)(blockIdx.x % (unsigned)p.Hv);
-  const int64_t slot = blockIdx.x / (unsigned)p.Hv;
+  // A resident block walks the (chunk slot, v-head) items with the grid's stride: TMEM and
+  // the barriers are set up once, and the phases of the barriers are counted across items.
+  if (tid == 0) {
+    mbar_init(&ld_bar, 1);
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tbase, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = tbase;
+  uint32_t ldp = 0, mp = 0;  // completed phases of ld_bar and bar
+#pragma unroll 1
+  for (int64_t item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+  const int h = (int)(item % p.Hv);
+  const int64_t slot = item / p.Hv;
   const int qh = h / (p.Hv / p.Hqk);
   int lo = 0, hi = p.n_seqs - 1;  // sequence of this slot: largest s with slot_base(s) <= slot
   while (lo < hi) {
@@ -150,11 +171,11 @@ __global__ void __launch_bounds__(128)
   seq_range(p.cu, p.row_T, s, start, end);
   if (start < 0 || end < start || end > p.n_tok) {
     if (tid == 0) set_status(p.status, GDN_ERR_BOUNDS);
-    return;
+    break;
   }
   const int64_t c = slot - slot_base(p.cu, p.row_T, s);
   const int64_t t0 = start + c * C;
-  if (c < 0 || t0 >= end) return;  // slot past this sequence's last chunk: never read
+  if (c < 0 || t0 >= end) continue;  // slot past this sequence's last chunk: never read
   const int n = (int)min((int64_t)C, end - t0);
   uint8_t *rec = p.rec + ((size_t)slot * p.Hv + h) * p.rec_bytes;
   float *vec = reinterpret_cast<float *>(rec + REC_VEC);
@@ -162,12 +183,6 @@ __global__ void __launch_bounds__(128)
 
   // ---- raw k, q and v tiles by TMA (rows past the chunk's end hold finite data of the
   //      next sequence or zeros: beta = 0 there keeps them out of every result); gates
-  if (tid == 0) {
-    mbar_init(&ld_bar, 1);
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
   if (tid == 0) {
     const int32_t tt = (int32_t)t0;
     mbar_arrive_expect_tx(&ld_bar, (4 + (op_late_v(V) ? 0 : NVB)) * 8192);
@@ -181,20 +196,14 @@ __global__ void __launch_bounds__(128)
   }
   if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
   else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
-  if (warp == 0) {
-    tmem_alloc(&tbase, kCols);
-    tmem_relinquish();
-  }
   {
-    const bool ok = tid != 0 || mbar_wait(&ld_bar, 0, kSpin);
+    const bool ok = tid != 0 || mbar_wait(&ld_bar, ldp & 1, kSpin);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
-      (void)mbar_wait(&ld_bar, 0, kSpin);  // the copies land before shared memory is released
-      tc_fence_before();
-      __syncthreads();
-      if (warp == 0) tmem_dealloc(tbase, kCols);
-      return;
+      (void)mbar_wait(&ld_bar, ldp & 1, kSpin);  // the copies land before shared memory is released
+      break;
     }
+    ++ldp;
   }
   // ---- 1/|k| and 1/|q| from the tiles (two threads per token)
   {
@@ -222,7 +231,6 @@ __global__ void __launch_bounds__(128)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tm = tbase;
   const uint32_t kq_a = smem_u32(sm + OP_KQ);
   // ---- [K; Q] K^T: M = 128 (k rows, then q rows), N = 64, K = 128 on the tensor core
   if (tid == 0) {
@@ -268,15 +276,13 @@ __global__ void __launch_bounds__(128)
     }
   }
   {
-    const bool ok = tid != 0 || mbar_wait(&bar, 0, kSpin);
+    const bool ok = tid != 0 || mbar_wait(&bar, mp & 1, kSpin);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
-      (void)mbar_wait(&bar, 0, kSpin);  // an MMA still in flight lands before TMEM is freed
-      tc_fence_before();
-      __syncthreads();
-      if (warp == 0) tmem_dealloc(tm, kCols);
-      return;
+      (void)mbar_wait(&bar, mp & 1, kSpin);  // an MMA still in flight lands before TMEM is freed
+      break;
     }
+    ++mp;
   }
   tc_fence_after();
   // ---- rows of K K^T (lanes 0-63) become rows of A; rows of Q K^T (lanes 64-127) rows of P
@@ -370,18 +376,18 @@ __global__ void __launch_bounds__(128)
   const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
   const int rr = warp * 16 + lane;  // rows of an M = 64 result sit in lanes 0-15 of a quarter
   const bool has_row = lane < 16;
+  bool dead = false;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     if (op_late_v(V) && pass == 1) {
-      const bool ok = tid != 0 || mbar_wait(&ld_bar, 1, kSpin);
+      const bool ok = tid != 0 || mbar_wait(&ld_bar, ldp & 1, kSpin);
       if (__syncthreads_or(!ok)) {
         if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
-        (void)mbar_wait(&ld_bar, 1, kSpin);  // the copy lands before shared memory is released
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tm, kCols);
-        return;
+        (void)mbar_wait(&ld_bar, ldp & 1, kSpin);  // the copy lands before shared memory is released
+        dead = true;
+        break;
       }
+      ++ldp;
     }
     if (tid == 0) {
       if (pass == 0) {
@@ -406,7 +412,7 @@ __global__ void __launch_bounds__(128)
       umma_commit(&bar);
     }
     {
-      const uint32_t par = pass == 0 ? 1u : 0u;  // completions 2 and 3 of the barrier
+      const uint32_t par = mp & 1;
       bool ok = tid != 0 || mbar_wait(&bar, par, kSpin);
       if (op_late_v(V) && pass == 0 && tid == 0 && ok) {
         // W has read the k rows: v goes there while -W drains
@@ -419,11 +425,10 @@ __global__ void __launch_bounds__(128)
       if (__syncthreads_or(!ok)) {
         if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
         (void)mbar_wait(&bar, par, kSpin);
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tm, kCols);
-        return;
+        dead = true;
+        break;
       }
+      ++mp;
     }
     tc_fence_after();
     float w64[64];
@@ -462,6 +467,10 @@ __global__ void __launch_bounds__(128)
     __syncthreads();  // the columns are free for the next pass
     tc_fence_after();
   }
+  if (dead) break;
+  }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) tmem_dealloc(tm, kCols);
 }
 
@@ -931,11 +940,25 @@ gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const C
                            const OpParams &op, size_t slots, cudaStream_t st) {
   const size_t smem = op_smem(V);
   if (cudaFuncSetAttribute(chunk_operand_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+                           (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(chunk_operand_kernel<V>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return GDN_ERR_CUDA;
-  const size_t blocks = slots * (size_t)op.Hv;
-  if (blocks > 2147483647ULL) return GDN_ERR_UNSUPPORTED;
-  chunk_operand_kernel<V><<<(unsigned)blocks, 128, smem, st>>>(mq, mk, mv, op);
+  const size_t items = slots * (size_t)op.Hv;
+  if (items == 0) return GDN_OK;
+  // resident blocks only: each walks the items with the grid's stride
+  int dev = 0, sms = 0, smem_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  // blocks an SM holds: shared memory (dynamic + 2 KB static + 1 KB reserved), at most 4
+  // (128 registers x 128 threads each)
+  const int per_sm = std::max(1, std::min(4, smem_sm / (int)(smem + 3072)));
+  const size_t grid = std::min(items, (size_t)sms * (size_t)per_sm);
+  OpParams q = op;
+  q.n_items = (int64_t)items;
+  chunk_operand_kernel<V><<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, q);
   return launch_status();
 }
 
