@@ -155,7 +155,7 @@ struct Vec<T, 1> {
 };
 
 template <typename T, int VEC, int W>
-__global__ void __launch_bounds__(128, 5) conv1d_kernel(const T *__restrict__ x, const T *__restrict__ w,
+__global__ void __launch_bounds__(128, 4) conv1d_kernel(const T *__restrict__ x, const T *__restrict__ w,
                                                      const T *__restrict__ bias,
                                                      const int32_t *__restrict__ cu, int n_seqs,
                                                      int64_t row_T, int64_t n_tok, int C, int act,
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(128, 5) conv1d_kernel(const T *__restrict__ x,
     }
   }
   // tokens in batches of kAhead: all of a batch's loads are in flight before its first use
-  constexpr int kAhead = 4;
+  constexpr int kAhead = 8;
   for (int64_t tb = t0; tb < t1; tb += kAhead) {
     typename Vec<T, VEC>::raw raw[kAhead];
 #pragma unroll
