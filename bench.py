@@ -6,7 +6,9 @@ K=V=128, bf16 inputs, fp32 state): gdn_gate_prep -> gdn_conv1d_varlen (+SiLU,
 Q|K|V channels) -> gdn_chunk_fwd (q/k L2 norm fused).  The segment-parallel
 two-pass (gdn_segment_summary -> gdn_chain_reduce -> gdn_chunk_fwd per
 segment) is measured on the long-context workload (T=131072, 16 heads,
-8 segments) and reported beside it.
+8 segments) and reported beside it, and one decode step (gate prep and
+gdn_decode_step: conv with the carried inputs, L2 norm, recurrence) for a batch
+of 64 sequences of the same layer continuing from fp32 states.
 
 gdn_chunk_fwd runs as two kernels (chunk_operand_kernel: every chunk's
 state-independent operands at once; chunk_scan_kernel: the state chain), so a
@@ -315,6 +317,9 @@ def run_gpu_arm(args, ws, rank, local):
     seg = None
     if not args.no_segment:
         seg = run_segment_leg(crg, args, dev, stream, peaks)
+    dec = None
+    if not args.no_decode:
+        dec = run_decode_leg(crg, args, dev, stream, peaks)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -340,6 +345,8 @@ def run_gpu_arm(args, ws, rank, local):
     }
     if seg is not None:
         out["segment_parallel"] = seg
+    if dec is not None:
+        out["decode"] = dec
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out
@@ -410,6 +417,41 @@ def run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws):
     return {"value": round(tok / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "pipeline": "3 streams (H2D, compute, D2H), 2 buffer slots"}
+
+
+def run_decode_leg(crg, args, dev, stream, peaks, B=64):
+    """One decode step (gate prep + gdn_decode_step) for a batch of B sequences of the
+    4B-shaped layer, continuing from fp32 states; the states (B x 32 x 128 x 128 fp32) are
+    larger than L2, which is also flushed between steps."""
+    wl = synth.WORKLOADS["qwen35_4b_layer"]
+    d = synth.decode_inputs(B, wl.Hqk, wl.Hv, wl.K, wl.V, wl.conv_width, "bf16", seed=40404, device=dev)
+    x, cs, w, st = d["x"], d["conv_state"], d["conv_w"], d["state"]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    o = torch.empty((B, wl.Hv, wl.V), device=dev, dtype=torch.bfloat16)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    reps = max(5, min(args.steps // 5, 40))
+    ts = []
+    for it in range(reps + 3):
+        flush.fill_(1)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        g, beta = crg.gdn_gate_prep(d["a"], d["b"], d["A_log"], d["dt_bias"])
+        crg.gdn_decode_step(x, cs, w, g, beta, st, wl.Hqk, wl.Hv, wl.K, wl.V, act=1, scale=d["scale"], o=o)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= 3:
+            ts.append(e0.elapsed_time(e1))
+    ms = sum(ts) / len(ts)
+    C = d["C"]
+    nbytes = (2 * B * wl.Hv * wl.V * wl.K * 4            # state read and written
+              + B * C * 2 + 2 * B * (wl.conv_width - 1) * C * 2  # x; conv state read and written
+              + C * wl.conv_width * 2 + B * wl.Hv * wl.V * 2      # conv weights; o
+              + B * wl.Hv * (2 * 2 + 2 * 4))                      # a, b in; g, beta out
+    return {"B": B, "workload": wl.name, "tokens_per_s": round(B / (ms * 1e-3), 1),
+            "ms_per_step": round(ms, 5), "bytes": nbytes,
+            "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "launches_per_step": 3, "steps": len(ts)}
 
 
 def run_segment_leg(crg, args, dev, stream, peaks):
@@ -549,6 +591,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen35_4b_layer", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-segment", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

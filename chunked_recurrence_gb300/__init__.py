@@ -60,6 +60,8 @@ _SIGS = {
     "gdn_segment_summary": ([_P, _P, _P, _P, _P, _I32, ctypes.POINTER(GdnShape), _U32, _P, _P,
                              _P, _SZ, _P], ctypes.c_int),
     "gdn_chain_reduce": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "gdn_decode_step": ([_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                         _F32, _U32, _P, _P], ctypes.c_int),
     "gdn_cu_seqlens_from_position_ids": ([_P, _I64, _P, _P, _P], ctypes.c_int),
 }
 
@@ -144,6 +146,35 @@ def gdn_gate_prep(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
                                 _ptr(dt_bias), n_tok, Hv, _ptr(g), _ptr(beta), _stream(a, stream)),
            "gdn_gate_prep")
     return g, beta
+
+
+def gdn_decode_step(x, conv_state, w, g, beta, state, Hqk, Hv, K, V, bias=None, act=1, scale=None,
+                    l2norm_qk=True, o=None, o_f32=False, stream=None):
+    """One decode step for B sequences: conv1d (+SiLU) of the new token x [B, C] with the carried
+    conv_state [B, W-1, C] (updated in place), q/k L2 norm and the recurrence on state
+    [B, Hv, V, K] fp32 (updated in place); returns o [B, Hv, V]."""
+    _need_cuda(x, conv_state, w, g, beta, state, bias)
+    for n, t in (("x", x), ("w", w), ("g", g), ("beta", beta), ("state", state)):
+        _contig(n, t)
+    B, C = x.shape
+    width = w.shape[1]
+    assert C == 2 * Hqk * K + Hv * V and w.shape[0] == C and w.dtype == x.dtype
+    assert g.dtype == torch.float32 and beta.dtype == torch.float32 and state.dtype == torch.float32
+    assert tuple(state.shape) == (B, Hv, V, K) and tuple(g.shape) == (B, Hv) == tuple(beta.shape)
+    if width > 1:
+        _contig("conv_state", conv_state)
+        assert tuple(conv_state.shape) == (B, width - 1, C) and conv_state.dtype == x.dtype
+    if scale is None:
+        scale = K ** -0.5
+    o_dtype = torch.float32 if o_f32 else x.dtype
+    if o is None:
+        o = torch.empty((B, Hv, V), device=x.device, dtype=o_dtype)
+    assert o.dtype == o_dtype and o.is_contiguous()
+    flags = (GDN_FLAG_QK_L2NORM if l2norm_qk else 0) | (GDN_FLAG_O_F32 if o_f32 else 0)
+    _check(load().gdn_decode_step(_ptr(x), _ptr(conv_state), _ptr(w), _ptr(bias), _dtype_code(x.dtype),
+                                  width, int(act), _ptr(g), _ptr(beta), _ptr(state), B, Hqk, Hv, K, V,
+                                  float(scale), flags, _ptr(o), _stream(x, stream)), "gdn_decode_step")
+    return o
 
 
 def gdn_conv1d_varlen(x, w, bias=None, cu_seqlens=None, n_seqs=None, act=1, y=None, stream=None):

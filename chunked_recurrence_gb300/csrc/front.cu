@@ -22,7 +22,7 @@ extern "C" const char *gdn_status_string(int status) {
   }
 }
 
-extern "C" int32_t gdn_version(void) { return (1 << 16) | 1; }
+extern "C" int32_t gdn_version(void) { return (1 << 16) | 2; }
 
 extern "C" gdn_status gdn_workspace_reset(void *workspace, size_t workspace_bytes, void *stream) {
   if (!workspace || workspace_bytes < sizeof(int32_t)) return GDN_ERR_WORKSPACE;

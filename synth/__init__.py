@@ -170,3 +170,32 @@ def mild_gates(n_tok: int, Hv: int, seed: int, device="cpu"):
     gg = torch.rand((n_tok, Hv), generator=g, device=device) * -0.05
     bb = torch.rand((n_tok, Hv), generator=g, device=device) * 0.6 + 0.2
     return gg, bb
+
+
+def decode_inputs(B: int, Hqk: int, Hv: int, K: int, V: int, width: int, dtype: str, seed: int,
+                  device="cpu", with_bias: bool = False, state_std: float = 0.1) -> dict:
+    """Inputs of one decode step for B sequences: the new token's Q|K|V projections x [B, C],
+    the carried conv inputs conv_state [B, width-1, C], conv_w [C, width] (and bias [C]),
+    a, b [B, Hv], A_log, dt_bias [Hv] fp32 and the recurrent state [B, Hv, V, K] fp32.
+    Distributions as the layer workloads: x, conv_state, a, b ~ N(0, 1), w ~ N(0, 0.5^2),
+    bias ~ N(0, 0.1^2), A_log ~ U(0, ln 16), dt_bias ~ U(-1, 1), state ~ N(0, state_std^2);
+    x, conv_state, w and bias rounded once to `dtype` ("f32" or "bf16")."""
+    dev = torch.device(device)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    C = 2 * Hqk * K + Hv * V
+    g = _gen(seed, dev)
+
+    def normal(shape, std=1.0):
+        return torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std
+
+    out = {"C": C, "scale": K ** -0.5}
+    out["A_log"] = torch.rand((Hv,), generator=g, device=dev) * math.log(16.0)
+    out["dt_bias"] = torch.rand((Hv,), generator=g, device=dev) * 2.0 - 1.0
+    out["a"] = normal((B, Hv)).to(dt)
+    out["b"] = normal((B, Hv)).to(dt)
+    out["conv_w"] = normal((C, width), 0.5).to(dt)
+    out["bias"] = normal((C,), 0.1).to(dt) if with_bias else None
+    out["x"] = normal((B, C)).to(dt)
+    out["conv_state"] = normal((B, max(width - 1, 0), C)).to(dt)
+    out["state"] = normal((B, Hv, V, K), state_std)
+    return out

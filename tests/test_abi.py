@@ -117,6 +117,17 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.gdn_cu_seqlens_from_position_ids(fake, -1, fake, fake, None) == 1
     assert lib.gdn_segment_summary(fake, fake, fake, fake, fake, 2, ctypes.byref(_shape(B=2)), 0,
                                    fake, fake, ws, 256, None) == 1
+    # decode step: x, cs, w, bias, dtype, width, act, g, beta, state, B, Hqk, Hv, K, V, scale, flags, o
+    dec = lib.gdn_decode_step
+    assert dec(fake, fake, fake, None, 7, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
+    assert dec(fake, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 48, 128, 1.0, 1, fake, None) == 1
+    assert dec(fake, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 3, 4, 128, 128, 1.0, 1, fake, None) == 1
+    assert dec(fake, fake, fake, None, 1, 9, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
+    assert dec(fake, fake, fake, None, 1, 4, 2, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
+    assert dec(fake, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 2, fake, None) == 1
+    assert dec(None, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
+    assert dec(fake, None, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
+    assert dec(None, None, None, None, 1, 4, 1, None, None, None, 0, 2, 4, 128, 128, 1.0, 1, None, None) == 0
     assert lib.gdn_workspace_reset(None, 0, None) == 5
     assert lib.gdn_workspace_status(None, None, None) == 1
 
