@@ -54,6 +54,7 @@ def _load():
             _lib.oracle_gate_prep.argtypes = [d, d, d, d, i64, i32, d, d]
             _lib.oracle_conv1d.argtypes = [d, d, d, d, i32, i32, i32, i32, d]
             _lib.oracle_l2norm_rows.argtypes = [d, i64, i32, ctypes.c_double, d]
+            _lib.oracle_gated_rmsnorm.argtypes = [d, d, d, i64, i32, ctypes.c_double, d]
             _lib.oracle_gdn_fwd.argtypes = [d, d, d, d, d, d, d, i32, i32, i32, i32, i32,
                                             ctypes.c_double, i32, ctypes.c_double, d, d, i32]
             _lib.oracle_segment_summary.argtypes = [d, d, d, d, d, i32, i32, i32, i32, i32,
@@ -171,6 +172,17 @@ def chain_reduce(M, S_local, h0=None):
     _load().oracle_chain_reduce(_ptr(M), _ptr(S_local), _ptr(h0), n_seg, Hv, K, V,
                                 _ptr(S_start), _ptr(hT))
     return S_start, hT
+
+
+def gated_rmsnorm(o, z, w=None, eps=1e-6):
+    """y = o / sqrt(mean(o^2) + eps) * w * silu(z) over the last axis (V) of o and z."""
+    o, z = _f64(o), _f64(z)
+    V = o.shape[-1]
+    rows = o.size // V if V else 0
+    w = None if w is None else _f64(w)
+    y = np.empty_like(o)
+    _load().oracle_gated_rmsnorm(_ptr(o), _ptr(z), _ptr(w), rows, V, float(eps), _ptr(y))
+    return y
 
 
 def cu_seqlens_from_position_ids(pos):

@@ -100,6 +100,27 @@ void oracle_l2norm_rows(const double *x, int64_t rows, int n, double eps,
   for (int64_t r = 0; r < rows; ++r) l2_normalise(x + r * n, n, eps, out + r * n);
 }
 
+/* Gated RMS norm of the core's output ("[v1] support GDN Ulysses cp", Design: the layer
+ * applies a norm to the chunk_gated_delta_rule output, and z is one of the layer's
+ * per-token components).  The pages give no formula; the reading taken is the gated
+ * RMS norm over each (token, v-head) row of V values:
+ *    y[v] = o[v] / sqrt(mean_v o^2 + eps) * w[v] * z[v] * sigmoid(z[v])
+ * with w [V] (NULL reads as ones). */
+void oracle_gated_rmsnorm(const double *o, const double *z, const double *w, int64_t rows,
+                          int V, double eps, double *y) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const double *orow = o + r * V, *zrow = z + r * V;
+    double ms = 0.0;
+    for (int v = 0; v < V; ++v) ms += orow[v] * orow[v];
+    ms /= (double)V;
+    const double inv = 1.0 / sqrt(ms + eps);
+    for (int v = 0; v < V; ++v) {
+      const double gate = zrow[v] / (1.0 + exp(-zrow[v]));
+      y[r * V + v] = orow[v] * inv * (w ? w[v] : 1.0) * gate;
+    }
+  }
+}
+
 /* ------------------------------------------------------ thread work queue */
 
 typedef struct {

@@ -41,6 +41,11 @@ MUTANTS = {
                            "acc += S[(int64_t)a * K + m] * Mi[(int64_t)j * K + m];"),
     "chain_local_dropped": ("double acc = Li[(int64_t)a * K + j];", "double acc = 0.0;"),
     "cu_restart_value": ("if (t == 0 || pos[t] == 0)", "if (t == 0 || pos[t] == 1)"),
+    "rmsnorm_sum_not_mean": ("ms /= (double)V;", "ms /= 1.0;"),
+    "rmsnorm_gate_sign": ("zrow[v] / (1.0 + exp(-zrow[v]))", "zrow[v] / (1.0 + exp(zrow[v]))"),
+    "rmsnorm_gate_z_dropped": ("const double gate = zrow[v] / (1.0 + exp(-zrow[v]));",
+                               "const double gate = 1.0 / (1.0 + exp(-zrow[v]));"),
+    "rmsnorm_weight_dropped": ("* (w ? w[v] : 1.0) * gate", "* gate"),
 }
 
 

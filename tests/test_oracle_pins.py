@@ -142,6 +142,41 @@ def test_l2norm_flag_inside_recurrence(oracle_mod):
 
 # -------------------------------------------------- recurrence: brute force
 
+def test_gated_rmsnorm_vs_torch(oracle_mod):
+    """Against torch's rms_norm and silu in float64 ("+ norm" of the layer, read as the
+    gated RMS norm of each (token, v-head) row)."""
+    import torch
+    rng = np.random.default_rng(71)
+    o = rng.standard_normal((5, 3, 48))
+    z = rng.standard_normal((5, 3, 48)) * 2
+    w = rng.standard_normal(48)
+    got = oracle_mod.gated_rmsnorm(o, z, w, eps=1e-6)
+    ot, zt, wt = (torch.from_numpy(a) for a in (o, z, w))
+    ref = (torch.nn.functional.rms_norm(ot, (48,), wt, 1e-6) * torch.nn.functional.silu(zt)).numpy()
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-14)
+    # w = None is a weight of ones
+    assert np.allclose(oracle_mod.gated_rmsnorm(o, z, None), oracle_mod.gated_rmsnorm(o, z, np.ones(48)),
+                       rtol=0, atol=0)
+
+
+def test_gated_rmsnorm_invariants(oracle_mod):
+    rng = np.random.default_rng(72)
+    o = rng.standard_normal((7, 32)) * 3
+    z = rng.standard_normal((7, 32))
+    silu = z / (1 + np.exp(-z))
+    # eps = 0: every row, the gate divided out, has root-mean-square exactly 1
+    y = oracle_mod.gated_rmsnorm(o, z, None, eps=0.0)
+    assert np.allclose(np.sqrt(np.mean((y / silu) ** 2, axis=1)), 1.0, rtol=1e-12)
+    # z = 0 closes the gate; silu(z) - silu(-z) = z
+    assert np.all(oracle_mod.gated_rmsnorm(o, np.zeros_like(z), None) == 0.0)
+    d = oracle_mod.gated_rmsnorm(o, z, None, eps=0.0) - oracle_mod.gated_rmsnorm(o, -z, None, eps=0.0)
+    unit = o / np.sqrt(np.mean(o ** 2, axis=1, keepdims=True))
+    assert np.allclose(d, unit * z, rtol=1e-12, atol=1e-13)
+    # the weight scales each channel
+    w = rng.standard_normal(32)
+    assert np.allclose(oracle_mod.gated_rmsnorm(o, z, w), oracle_mod.gated_rmsnorm(o, z, None) * w, rtol=1e-12)
+
+
 def test_single_step_by_hand(oracle_mod):
     # S1 = S0 (I - beta k k^T) + beta v k^T with S0 = I, k = (0.6, 0.8), beta = 1/2,
     # v = (1, 2), g = 0, q = (1, 0): worked out by hand,
