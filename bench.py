@@ -320,6 +320,7 @@ def run_gpu_arm(args, ws, rank, local):
     dec = None
     if not args.no_decode:
         dec = run_decode_leg(crg, args, dev, stream, peaks)
+        dec["gated_rmsnorm"] = run_norm_leg(crg, args, dev, stream, peaks)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -452,6 +453,31 @@ def run_decode_leg(crg, args, dev, stream, peaks, B=64):
             "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "launches_per_step": 3, "steps": len(ts)}
+
+
+def run_norm_leg(crg, args, dev, stream, peaks):
+    """gdn_gated_rmsnorm over the 4B layer's o (8192 tokens x 32 v-heads x 128, bf16) with z;
+    L2 flushed between calls."""
+    wl = synth.WORKLOADS["qwen35_4b_layer"]
+    d = synth.norm_inputs((wl.T, wl.Hv), wl.V, "bf16", seed=40505, device=dev)
+    y = torch.empty_like(d["o"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    ts = []
+    for it in range(3 + max(5, min(args.steps // 5, 40))):
+        flush.fill_(1)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        crg.gdn_gated_rmsnorm(d["o"], d["z"], d["w"], y=y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= 3:
+            ts.append(e0.elapsed_time(e1))
+    ms = sum(ts) / len(ts)
+    nbytes = 3 * d["o"].numel() * 2 + wl.V * 2
+    out = _kinfo(ms, nbytes, peaks)
+    out["rows"] = wl.T * wl.Hv
+    return out
 
 
 def run_segment_leg(crg, args, dev, stream, peaks):

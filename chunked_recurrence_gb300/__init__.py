@@ -60,6 +60,7 @@ _SIGS = {
     "gdn_segment_summary": ([_P, _P, _P, _P, _P, _I32, ctypes.POINTER(GdnShape), _U32, _P, _P,
                              _P, _SZ, _P], ctypes.c_int),
     "gdn_chain_reduce": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "gdn_gated_rmsnorm": ([_P, _P, _P, _I32, _I64, _I32, _F32, _P, _P], ctypes.c_int),
     "gdn_decode_step": ([_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
                          _F32, _U32, _P, _P], ctypes.c_int),
     "gdn_cu_seqlens_from_position_ids": ([_P, _I64, _P, _P, _P], ctypes.c_int),
@@ -175,6 +176,23 @@ def gdn_decode_step(x, conv_state, w, g, beta, state, Hqk, Hv, K, V, bias=None, 
                                   width, int(act), _ptr(g), _ptr(beta), _ptr(state), B, Hqk, Hv, K, V,
                                   float(scale), flags, _ptr(o), _stream(x, stream)), "gdn_decode_step")
     return o
+
+
+def gdn_gated_rmsnorm(o, z, w=None, eps=1e-6, y=None, stream=None):
+    """y = o / sqrt(mean(o^2) + eps) * w * silu(z) over the last axis (V) of o [..., V]; y may be o."""
+    _need_cuda(o, z, w)
+    _contig("o", o)
+    _contig("z", z)
+    assert z.shape == o.shape and z.dtype == o.dtype
+    V = o.shape[-1]
+    if w is not None:
+        assert w.shape == (V,) and w.dtype == o.dtype
+    y = torch.empty_like(o) if y is None else y
+    assert y.shape == o.shape and y.dtype == o.dtype and y.is_contiguous()
+    rows = o.numel() // V if V else 0
+    _check(load().gdn_gated_rmsnorm(_ptr(o), _ptr(z), _ptr(w), _dtype_code(o.dtype), rows, V, float(eps),
+                                    _ptr(y), _stream(o, stream)), "gdn_gated_rmsnorm")
+    return y
 
 
 def gdn_conv1d_varlen(x, w, bias=None, cu_seqlens=None, n_seqs=None, act=1, y=None, stream=None):

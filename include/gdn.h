@@ -213,6 +213,17 @@ gdn_status gdn_decode_step(const void *x, void *conv_state, const void *w, const
                            int32_t K, int32_t V, float scale, uint32_t flags, void *o,
                            void *stream);
 
+/* Gated RMS norm of the core's output: the layer's "+ norm" after chunk_gated_delta_rule
+ * ("[v1] support GDN Ulysses cp", Design; z is one of the layer's per-token components).
+ * The pages give no formula; the reading taken is, per row r of V values,
+ *     y[r, v] = o[r, v] / sqrt(mean_v o[r, :]^2 + eps) * w[v] * silu(z[r, v])
+ * with rows = tokens x v-heads of o [tokens, Hv, V].
+ *   o, z, y: [n_rows, V] of dtype (dense rows); w: [V] of dtype, or NULL for ones
+ *   eps >= 0 (1e-6 in Qwen3.5); accumulation in fp32.  y may be o (in place); z must not
+ *   overlap y.  n_rows may be 0. */
+gdn_status gdn_gated_rmsnorm(const void *o, const void *z, const void *w, int32_t dtype, int64_t n_rows,
+                             int32_t V, float eps, void *y, void *stream);
+
 /* fp32 chain reduce of the segment summaries ("Qwen3.5 cp - #1",
  * Architecture: (b, M) chain reduce, fp32):
  *     S_start[0] = h0 (or 0);  S_start[i+1] = S_start[i] M[i] + S_local[i];  h_T = S_start[n_seg]

@@ -199,3 +199,15 @@ def decode_inputs(B: int, Hqk: int, Hv: int, K: int, V: int, width: int, dtype: 
     out["conv_state"] = normal((B, max(width - 1, 0), C)).to(dt)
     out["state"] = normal((B, Hv, V, K), state_std)
     return out
+
+
+def norm_inputs(shape, V: int, dtype: str, seed: int, device="cpu", with_weight: bool = True) -> dict:
+    """Inputs of the gated RMS norm: o, z [*shape, V] ~ N(0, 1) and w [V] ~ N(1, 0.1^2),
+    rounded once to `dtype` ("f32" or "bf16")."""
+    dev = torch.device(device)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    g = _gen(seed, dev)
+    o = torch.randn((*shape, V), generator=g, device=dev).to(dt)
+    z = torch.randn((*shape, V), generator=g, device=dev).to(dt)
+    w = (1.0 + 0.1 * torch.randn((V,), generator=g, device=dev)).to(dt) if with_weight else None
+    return {"o": o, "z": z, "w": w}

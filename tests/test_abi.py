@@ -128,6 +128,12 @@ def test_argument_errors_return_before_launch(lib):
     assert dec(None, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
     assert dec(fake, None, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
     assert dec(None, None, None, None, 1, 4, 1, None, None, None, 0, 2, 4, 128, 128, 1.0, 1, None, None) == 0
+    # gated rms norm: o, z, w, dtype, n_rows, V, eps, y
+    assert lib.gdn_gated_rmsnorm(fake, fake, None, 7, 10, 128, 1e-6, fake, None) == 1
+    assert lib.gdn_gated_rmsnorm(fake, fake, None, 1, 10, 0, 1e-6, fake, None) == 1
+    assert lib.gdn_gated_rmsnorm(fake, fake, None, 1, 10, 128, -1.0, fake, None) == 1
+    assert lib.gdn_gated_rmsnorm(None, fake, None, 1, 10, 128, 1e-6, fake, None) == 1
+    assert lib.gdn_gated_rmsnorm(None, None, None, 1, 0, 128, 1e-6, None, None) == 0
     assert lib.gdn_workspace_reset(None, 0, None) == 5
     assert lib.gdn_workspace_status(None, None, None) == 1
 
