@@ -44,6 +44,16 @@ __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, co
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ float qs[K], ks[K], vs[kDecRows];
   __shared__ float red[3][4];
+  // this warp's 8 rows of S, loaded first so that their latency overlaps the conv below
+  constexpr int kRowsPerWarp = kDecRows / 4;
+  float sr[kRowsPerWarp][KPL];
+  float *Sh = S + ((size_t)b * Hv + h) * V * K;
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int v = vb * kDecRows + warp * kRowsPerWarp + r;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) sr[r][j] = v < V ? Sh[(size_t)v * K + lane + 32 * j] : 0.f;
+  }
 
   // conv1d (+ SiLU) of channel c at the sequence's next token, in the prefill conv's order
   auto conv = [&](int c) -> float {
@@ -97,15 +107,6 @@ __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, co
   }
   const float a = __expf(g[(size_t)b * Hv + h]), bt = beta[(size_t)b * Hv + h];
   // rows of S: warp w takes rows 8 w .. 8 w + 7 of this block's 32
-  constexpr int kRowsPerWarp = kDecRows / 4;
-  float sr[kRowsPerWarp][KPL];
-  float *Sh = S + ((size_t)b * Hv + h) * V * K;
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int v = vb * kDecRows + warp * kRowsPerWarp + r;
-#pragma unroll
-    for (int j = 0; j < KPL; ++j) sr[r][j] = v < V ? Sh[(size_t)v * K + lane + 32 * j] : 0.f;
-  }
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
     const int vr = warp * kRowsPerWarp + r, v = vb * kDecRows + vr;
