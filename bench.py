@@ -6,9 +6,10 @@ K=V=128, bf16 inputs, fp32 state): gdn_gate_prep -> gdn_conv1d_varlen (+SiLU,
 Q|K|V channels) -> gdn_chunk_fwd (q/k L2 norm fused).  The segment-parallel
 two-pass (gdn_segment_summary -> gdn_chain_reduce -> gdn_chunk_fwd per
 segment) is measured on the long-context workload (T=131072, 16 heads,
-8 segments) and reported beside it, and one decode step (gate prep and
-gdn_decode_step: conv with the carried inputs, L2 norm, recurrence) for a batch
-of 64 sequences of the same layer continuing from fp32 states.
+8 segments) and reported beside it, and one decode step (gdn_decode_step:
+gates, conv with the carried inputs, L2 norm, recurrence) for a batch
+of 64 sequences of the same layer continuing from fp32 states, and the gated
+RMSNorm of the layer's o.
 
 gdn_chunk_fwd runs as two kernels (chunk_operand_kernel: every chunk's
 state-independent operands at once; chunk_scan_kernel: the state chain), so a
@@ -421,12 +422,14 @@ def run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws):
 
 
 def run_decode_leg(crg, args, dev, stream, peaks, B=64):
-    """One decode step (gate prep + gdn_decode_step) for a batch of B sequences of the
-    4B-shaped layer, continuing from fp32 states; the states (B x 32 x 128 x 128 fp32) are
-    larger than L2, which is also flushed between steps."""
+    """One decode step (gdn_decode_step: gates, conv with the carried inputs, L2 norm,
+    recurrence) for a batch of B sequences of the 4B-shaped layer, continuing from fp32
+    states; the states (B x 32 x 128 x 128 fp32) are larger than L2, which is also flushed
+    between steps."""
     wl = synth.WORKLOADS["qwen35_4b_layer"]
     d = synth.decode_inputs(B, wl.Hqk, wl.Hv, wl.K, wl.V, wl.conv_width, "bf16", seed=40404, device=dev)
-    x, cs, w, st = d["x"], d["conv_state"], d["conv_w"], d["state"]
+    x, w, st = d["x"], d["conv_w"], d["state"]
+    cs, spare = d["conv_state"], torch.empty_like(d["conv_state"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     o = torch.empty((B, wl.Hv, wl.V), device=dev, dtype=torch.bfloat16)
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -436,10 +439,11 @@ def run_decode_leg(crg, args, dev, stream, peaks, B=64):
         flush.fill_(1)
         e0, e1 = ev(), ev()
         e0.record(stream)
-        g, beta = crg.gdn_gate_prep(d["a"], d["b"], d["A_log"], d["dt_bias"])
-        crg.gdn_decode_step(x, cs, w, g, beta, st, wl.Hqk, wl.Hv, wl.K, wl.V, act=1, scale=d["scale"], o=o)
+        _, nxt = crg.gdn_decode_step(x, cs, w, d["a"], d["b"], d["A_log"], d["dt_bias"], st, wl.Hqk, wl.Hv,
+                                     wl.K, wl.V, act=1, scale=d["scale"], o=o, conv_state_out=spare)
         e1.record(stream)
         torch.cuda.synchronize()
+        cs, spare = nxt, cs
         if it >= 3:
             ts.append(e0.elapsed_time(e1))
     ms = sum(ts) / len(ts)
@@ -447,12 +451,12 @@ def run_decode_leg(crg, args, dev, stream, peaks, B=64):
     nbytes = (2 * B * wl.Hv * wl.V * wl.K * 4            # state read and written
               + B * C * 2 + 2 * B * (wl.conv_width - 1) * C * 2  # x; conv state read and written
               + C * wl.conv_width * 2 + B * wl.Hv * wl.V * 2      # conv weights; o
-              + B * wl.Hv * (2 * 2 + 2 * 4))                      # a, b in; g, beta out
+              + B * wl.Hv * 2 * 2)                                # a, b
     return {"B": B, "workload": wl.name, "tokens_per_s": round(B / (ms * 1e-3), 1),
             "ms_per_step": round(ms, 5), "bytes": nbytes,
             "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-            "launches_per_step": 3, "steps": len(ts)}
+            "launches_per_step": 1, "steps": len(ts)}
 
 
 def run_norm_leg(crg, args, dev, stream, peaks):

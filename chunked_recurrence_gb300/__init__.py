@@ -61,8 +61,8 @@ _SIGS = {
                              _P, _SZ, _P], ctypes.c_int),
     "gdn_chain_reduce": ([_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
     "gdn_gated_rmsnorm": ([_P, _P, _P, _I32, _I64, _I32, _F32, _P, _P], ctypes.c_int),
-    "gdn_decode_step": ([_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
-                         _F32, _U32, _P, _P], ctypes.c_int),
+    "gdn_decode_step": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
+                         _I32, _F32, _U32, _P, _P], ctypes.c_int),
     "gdn_cu_seqlens_from_position_ids": ([_P, _I64, _P, _P, _P], ctypes.c_int),
 }
 
@@ -149,22 +149,28 @@ def gdn_gate_prep(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
     return g, beta
 
 
-def gdn_decode_step(x, conv_state, w, g, beta, state, Hqk, Hv, K, V, bias=None, act=1, scale=None,
-                    l2norm_qk=True, o=None, o_f32=False, stream=None):
-    """One decode step for B sequences: conv1d (+SiLU) of the new token x [B, C] with the carried
-    conv_state [B, W-1, C] (updated in place), q/k L2 norm and the recurrence on state
-    [B, Hv, V, K] fp32 (updated in place); returns o [B, Hv, V]."""
-    _need_cuda(x, conv_state, w, g, beta, state, bias)
-    for n, t in (("x", x), ("w", w), ("g", g), ("beta", beta), ("state", state)):
+def gdn_decode_step(x, conv_state, w, a, b, A_log, dt_bias, state, Hqk, Hv, K, V, bias=None, act=1,
+                    scale=None, l2norm_qk=True, o=None, o_f32=False, conv_state_out=None, stream=None):
+    """One decode step for B sequences: the token's gates from a, b [B, Hv], conv1d (+SiLU) of the
+    new token x [B, C] with the carried inputs conv_state [B, W-1, C], q/k L2 norm and the
+    recurrence on state [B, Hv, V, K] fp32 (updated in place).  Returns (o [B, Hv, V],
+    conv_state_out): the carried inputs for the next step, in conv_state_out if given (a
+    buffer other than conv_state), else in a new tensor."""
+    _need_cuda(x, conv_state, w, a, b, A_log, dt_bias, state, bias)
+    for n, t in (("x", x), ("w", w), ("a", a), ("b", b), ("state", state)):
         _contig(n, t)
     B, C = x.shape
     width = w.shape[1]
     assert C == 2 * Hqk * K + Hv * V and w.shape[0] == C and w.dtype == x.dtype
-    assert g.dtype == torch.float32 and beta.dtype == torch.float32 and state.dtype == torch.float32
-    assert tuple(state.shape) == (B, Hv, V, K) and tuple(g.shape) == (B, Hv) == tuple(beta.shape)
-    if width > 1:
-        _contig("conv_state", conv_state)
-        assert tuple(conv_state.shape) == (B, width - 1, C) and conv_state.dtype == x.dtype
+    assert a.dtype == x.dtype == b.dtype and tuple(a.shape) == (B, Hv) == tuple(b.shape)
+    assert A_log.dtype == torch.float32 and dt_bias.dtype == torch.float32 and state.dtype == torch.float32
+    assert tuple(state.shape) == (B, Hv, V, K)
+    _contig("conv_state", conv_state)
+    assert tuple(conv_state.shape) == (B, width - 1, C) and conv_state.dtype == x.dtype
+    if conv_state_out is None:
+        conv_state_out = torch.empty_like(conv_state)
+    assert conv_state_out.shape == conv_state.shape and conv_state_out.is_contiguous()
+    assert width == 1 or conv_state.numel() == 0 or conv_state_out.data_ptr() != conv_state.data_ptr()
     if scale is None:
         scale = K ** -0.5
     o_dtype = torch.float32 if o_f32 else x.dtype
@@ -172,10 +178,13 @@ def gdn_decode_step(x, conv_state, w, g, beta, state, Hqk, Hv, K, V, bias=None, 
         o = torch.empty((B, Hv, V), device=x.device, dtype=o_dtype)
     assert o.dtype == o_dtype and o.is_contiguous()
     flags = (GDN_FLAG_QK_L2NORM if l2norm_qk else 0) | (GDN_FLAG_O_F32 if o_f32 else 0)
-    _check(load().gdn_decode_step(_ptr(x), _ptr(conv_state), _ptr(w), _ptr(bias), _dtype_code(x.dtype),
-                                  width, int(act), _ptr(g), _ptr(beta), _ptr(state), B, Hqk, Hv, K, V,
-                                  float(scale), flags, _ptr(o), _stream(x, stream)), "gdn_decode_step")
-    return o
+    wide = width > 1
+    _check(load().gdn_decode_step(_ptr(x), _ptr(conv_state) if wide else None,
+                                  _ptr(conv_state_out) if wide else None, _ptr(w), _ptr(bias),
+                                  _dtype_code(x.dtype), width, int(act), _ptr(a), _ptr(b), _ptr(A_log),
+                                  _ptr(dt_bias), _ptr(state), B, Hqk, Hv, K, V, float(scale), flags, _ptr(o),
+                                  _stream(x, stream)), "gdn_decode_step")
+    return o, conv_state_out
 
 
 def gdn_gated_rmsnorm(o, z, w=None, eps=1e-6, y=None, stream=None):

@@ -10,13 +10,16 @@
 // The update is done as S <- a S + u k^T with a = exp(g) and u = beta (v - a S k), and
 // o = scale (a S q + u (k^T q)): every row of S is read once and written once.
 //
-// decode_kernel: one block per (32 rows of S, v-head, sequence).  The block forms the
-// conv outputs of its head's q, k and v channels (q and k are shared by Hv / Hqk v-heads
-// and by the V / 32 row blocks; each block recomputes them from the same inputs), rounds
-// them to the storage dtype as the prefill conv stores them, normalises q and k, then each
-// warp streams 8 rows of S: lane l holds S[v][l + 32 j] (coalesced), the two dot products
-// are warp reductions.  State traffic is 2 V K 4 bytes per (sequence, v-head).
-// conv_shift_kernel: afterwards, conv_state <- its last W-2 rows followed by x.
+// decode_kernel: one block per (32 rows of S, v-head, sequence), one launch per step.  The
+// block computes its head's gates, forms the conv outputs of its head's q, k and v channels
+// (q and k are shared by Hv / Hqk v-heads and by the V / 32 row blocks; each block
+// recomputes them from the same inputs), rounds them to the storage dtype as the prefill
+// conv stores them, normalises q and k, then each warp streams 8 rows of S: lane l holds
+// S[v][l + 32 j] (coalesced), the two dot products are warp reductions.  The conv state is
+// double-buffered: the block that owns a channel (its v channels; q and k channels by the
+// first v-head of the group and row block 0) writes that channel's shifted inputs to the
+// output buffer, so no block overwrites what another still reads.  State traffic is
+// 2 V K 4 bytes per (sequence, v-head).
 #include "common.cuh"
 
 using namespace gdn;
@@ -32,9 +35,10 @@ __device__ __forceinline__ float round_to(float x) {
 
 template <typename T, int KPL, int W>
 __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, const T *__restrict__ conv_state,
-                                                     const T *__restrict__ w, const T *__restrict__ bias,
-                                                     int act, const float *__restrict__ g,
-                                                     const float *__restrict__ beta, float *__restrict__ S,
+                                                     T *__restrict__ conv_out, const T *__restrict__ w,
+                                                     const T *__restrict__ bias, int act, const T *__restrict__ ga,
+                                                     const T *__restrict__ gb, const float *__restrict__ A_log,
+                                                     const float *__restrict__ dt_bias, float *__restrict__ S,
                                                      int Hqk, int Hv, int V, int l2norm, float scale,
                                                      int o_f32, void *__restrict__ o) {
   constexpr int K = KPL * 32;
@@ -73,6 +77,21 @@ __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, co
     const int v = vb * kDecRows + tid;
     vs[tid] = v < V ? conv(2 * Hqk * K + h * V + v) : 0.f;
   }
+  // shifted conv inputs of the channels this block owns, into the output buffer
+  if (W > 1) {
+    auto shift = [&](int c) {
+#pragma unroll
+      for (int j = 0; j + 1 < W - 1; ++j)
+        conv_out[((size_t)b * (W - 1) + j) * C + c] = conv_state[((size_t)b * (W - 1) + j + 1) * C + c];
+      conv_out[((size_t)b * (W - 1) + W - 2) * C + c] = x[(size_t)b * C + c];
+    };
+    if (tid < kDecRows && vb * kDecRows + tid < V) shift(2 * Hqk * K + h * V + vb * kDecRows + tid);
+    if (vb == 0 && h % (Hv / Hqk) == 0)
+      for (int i = tid; i < K; i += 128) {
+        shift(qh * K + i);
+        shift(Hqk * K + qh * K + i);
+      }
+  }
   __syncthreads();
   // |q|^2, |k|^2 and k.q over the head's K features
   float sq = 0.f, sk = 0.f, kq = 0.f;
@@ -105,7 +124,9 @@ __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, co
     kr[j] = ks[lane + 32 * j] * kn;
     qr[j] = qs[lane + 32 * j] * qn;
   }
-  const float a = __expf(g[(size_t)b * Hv + h]), bt = beta[(size_t)b * Hv + h];
+  float gv, bt;
+  gdn_gates(to_f32<T>(ga[(size_t)b * Hv + h]), to_f32<T>(gb[(size_t)b * Hv + h]), A_log[h], dt_bias[h], gv, bt);
+  const float a = __expf(gv);
   // rows of S: warp w takes rows 8 w .. 8 w + 7 of this block's 32
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
@@ -134,42 +155,34 @@ __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, co
   }
 }
 
-// conv_state[b] <- rows 1 .. W-2 of conv_state[b], then x[b]
-template <typename T, int W>
-__global__ void conv_shift_kernel(const T *__restrict__ x, T *__restrict__ conv_state, int B, int C) {
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (int64_t)B * C) return;
-  const int64_t b = idx / C, c = idx - b * C;
-  T *st = conv_state + b * (W - 1) * C + c;
-#pragma unroll
-  for (int j = 0; j + 1 < W - 1; ++j) st[(int64_t)j * C] = st[(int64_t)(j + 1) * C];
-  st[(int64_t)(W - 2) * C] = x[b * C + c];
-}
+struct DecArgs {
+  const void *x, *cs_in;
+  void *cs_out;
+  const void *w, *bias;
+  int act;
+  const void *a, *b;
+  const float *A_log, *dt_bias;
+  float *state;
+  int B, Hqk, Hv, V, l2norm, o_f32;
+  float scale;
+  void *o;
+};
 
 template <typename T, int KPL, int W>
-void launch_decode(const void *x, void *conv_state, const void *w, const void *bias, int act,
-                   const float *g, const float *beta, float *state, int B, int Hqk, int Hv, int V,
-                   int l2norm, float scale, int o_f32, void *o, cudaStream_t st) {
-  const dim3 grid((unsigned)((V + kDecRows - 1) / kDecRows), (unsigned)Hv, (unsigned)B);
-  decode_kernel<T, KPL, W><<<grid, 128, 0, st>>>((const T *)x, (const T *)conv_state, (const T *)w,
-                                                 (const T *)bias, act, g, beta, state, Hqk, Hv, V, l2norm,
-                                                 scale, o_f32, o);
-  if (W > 1) {
-    const int C = 2 * Hqk * KPL * 32 + Hv * V;
-    const int64_t n = (int64_t)B * C;
-    conv_shift_kernel<T, (W > 1 ? W : 2)><<<(unsigned)((n + 255) / 256), 256, 0, st>>>((const T *)x, (T *)conv_state, B, C);
-  }
+void launch_decode(const DecArgs &d, cudaStream_t st) {
+  const dim3 grid((unsigned)((d.V + kDecRows - 1) / kDecRows), (unsigned)d.Hv, (unsigned)d.B);
+  decode_kernel<T, KPL, W><<<grid, 128, 0, st>>>((const T *)d.x, (const T *)d.cs_in, (T *)d.cs_out, (const T *)d.w,
+                                                 (const T *)d.bias, d.act, (const T *)d.a, (const T *)d.b, d.A_log,
+                                                 d.dt_bias, d.state, d.Hqk, d.Hv, d.V, d.l2norm, d.scale, d.o_f32,
+                                                 d.o);
 }
 
 template <typename T, int KPL>
-gdn_status dispatch_w(int W, const void *x, void *conv_state, const void *w, const void *bias, int act,
-                      const float *g, const float *beta, float *state, int B, int Hqk, int Hv, int V,
-                      int l2norm, float scale, int o_f32, void *o, cudaStream_t st) {
+gdn_status dispatch_w(int W, const DecArgs &d, cudaStream_t st) {
   switch (W) {
-#define GDN_DEC_W(WW)                                                                              \
-  case WW:                                                                                         \
-    launch_decode<T, KPL, WW>(x, conv_state, w, bias, act, g, beta, state, B, Hqk, Hv, V, l2norm, \
-                              scale, o_f32, o, st);                                                \
+#define GDN_DEC_W(WW)                   \
+  case WW:                              \
+    launch_decode<T, KPL, WW>(d, st);   \
     break;
     GDN_DEC_W(1) GDN_DEC_W(2) GDN_DEC_W(3) GDN_DEC_W(4) GDN_DEC_W(5) GDN_DEC_W(6) GDN_DEC_W(7) GDN_DEC_W(8)
 #undef GDN_DEC_W
@@ -179,14 +192,11 @@ gdn_status dispatch_w(int W, const void *x, void *conv_state, const void *w, con
 }
 
 template <typename T>
-gdn_status dispatch_k(int K, int W, const void *x, void *conv_state, const void *w, const void *bias, int act,
-                      const float *g, const float *beta, float *state, int B, int Hqk, int Hv, int V,
-                      int l2norm, float scale, int o_f32, void *o, cudaStream_t st) {
+gdn_status dispatch_k(int K, int W, const DecArgs &d, cudaStream_t st) {
   switch (K / 32) {
-#define GDN_DEC_K(KP)                                                                                     \
-  case KP:                                                                                                \
-    return dispatch_w<T, KP>(W, x, conv_state, w, bias, act, g, beta, state, B, Hqk, Hv, V, l2norm, scale, \
-                             o_f32, o, st);
+#define GDN_DEC_K(KP) \
+  case KP:            \
+    return dispatch_w<T, KP>(W, d, st);
     GDN_DEC_K(1) GDN_DEC_K(2) GDN_DEC_K(3) GDN_DEC_K(4) GDN_DEC_K(5) GDN_DEC_K(6) GDN_DEC_K(7) GDN_DEC_K(8)
 #undef GDN_DEC_K
     default: return GDN_ERR_UNSUPPORTED;
@@ -195,25 +205,25 @@ gdn_status dispatch_k(int K, int W, const void *x, void *conv_state, const void 
 
 }  // namespace
 
-extern "C" gdn_status gdn_decode_step(const void *x, void *conv_state, const void *w, const void *bias,
-                                      int32_t dtype, int32_t width, int32_t act, const float *g,
-                                      const float *beta, float *state, int32_t B, int32_t Hqk, int32_t Hv,
-                                      int32_t K, int32_t V, float scale, uint32_t flags, void *o,
-                                      void *stream) {
+extern "C" gdn_status gdn_decode_step(const void *x, const void *conv_state_in, void *conv_state_out,
+                                      const void *w, const void *bias, int32_t dtype, int32_t width, int32_t act,
+                                      const void *a, const void *b, const float *A_log, const float *dt_bias,
+                                      float *state, int32_t B, int32_t Hqk, int32_t Hv, int32_t K, int32_t V,
+                                      float scale, uint32_t flags, void *o, void *stream) {
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
   if (B < 0 || Hqk < 1 || Hv < 1 || Hv % Hqk != 0 || V < 1 || K < 32 || K > 256 || K % 32 != 0)
     return GDN_ERR_INVALID_ARG;
   if (width < 1 || width > 8 || (act != 0 && act != 1)) return GDN_ERR_INVALID_ARG;
   if (flags & ~(uint32_t)(GDN_FLAG_QK_L2NORM | GDN_FLAG_O_F32)) return GDN_ERR_INVALID_ARG;
   if (B == 0) return GDN_OK;
-  if (!x || !w || !g || !beta || !state || !o || (width > 1 && !conv_state)) return GDN_ERR_INVALID_ARG;
+  if (!x || !w || !a || !b || !A_log || !dt_bias || !state || !o ||
+      (width > 1 && (!conv_state_in || !conv_state_out || conv_state_in == conv_state_out)))
+    return GDN_ERR_INVALID_ARG;
   if ((int64_t)2 * Hqk * K + (int64_t)Hv * V > 2147483647LL || B > 65535 || Hv > 65535)
     return GDN_ERR_UNSUPPORTED;
-  const int l2 = (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, of = (flags & GDN_FLAG_O_F32) ? 1 : 0;
+  DecArgs d{x, conv_state_in, conv_state_out, w, bias, act, a, b, A_log, dt_bias, state, B, Hqk, Hv, V,
+            (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, (flags & GDN_FLAG_O_F32) ? 1 : 0, scale, o};
   cudaStream_t st = (cudaStream_t)stream;
-  if (dtype == GDN_BF16)
-    return dispatch_k<__nv_bfloat16>(K, width, x, conv_state, w, bias, act, g, beta, state, B, Hqk, Hv, V, l2,
-                                     scale, of, o, st);
-  return dispatch_k<float>(K, width, x, conv_state, w, bias, act, g, beta, state, B, Hqk, Hv, V, l2, scale, of,
-                           o, st);
+  if (dtype == GDN_BF16) return dispatch_k<__nv_bfloat16>(K, width, d, st);
+  return dispatch_k<float>(K, width, d, st);
 }

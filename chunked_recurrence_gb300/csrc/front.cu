@@ -58,10 +58,7 @@ __global__ void __launch_bounds__(256) gate_prep_kernel(const T *__restrict__ a,
       const int64_t i = i0 + u;
       if (i < n) {
         const int h = (int)(i % Hv);
-        const float x = to_f32(a[i]) + dt_bias[h];
-        const float softplus = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
-        g[i] = -expf(A_log[h]) * softplus;
-        beta[i] = 1.f / (1.f + expf(-to_f32(b[i])));
+        gdn_gates(to_f32(a[i]), to_f32(b[i]), A_log[h], dt_bias[h], g[i], beta[i]);
       }
     }
   }

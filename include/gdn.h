@@ -188,29 +188,31 @@ gdn_status gdn_segment_summary(const void *k, const void *v, const float *g, con
 
 /* One decode step of the layer core for B sequences, continuing from their states
  * ("Qwen3.5 cp - #1", Architecture: after the prefill, decode runs the standard
- * recurrent path from the final ssm_state).  For each sequence b, with the new
- * token's Q|K|V projections x[b] and the last W-1 inputs in conv_state[b]:
- *     y[c]  = act( bias[c] + sum_{j<W-1} w[c, j] conv_state[b, j, c] + w[c, W-1] x[b, c] )
+ * recurrent path from the final ssm_state).  For each sequence b, with the new token's
+ * Q|K|V projections x[b], its gate inputs a[b], b[b] and the last W-1 inputs in
+ * conv_state_in[b]:
+ *     g, beta = the gates of gdn_gate_prep (same arithmetic)
+ *     y[c]  = act( bias[c] + sum_{j<W-1} w[c, j] conv_state_in[b, j, c] + w[c, W-1] x[b, c] )
  *             (the conv1d of gdn_conv1d_varlen at the sequence's next token; y rounded
  *             to `dtype` as gdn_conv1d_varlen stores it)
  *     q, k  = y's q and k channels of q/k head h / (Hv / Hqk), L2-normalised with
  *             GDN_FLAG_QK_L2NORM;  v = y's v channels of v-head h
  *     S    <- exp(g) S (I - beta k k^T) + beta v k^T,   o = scale S q
- * and conv_state[b] <- its last W-2 rows followed by x[b].
- *   x:          [B, C] of `dtype`, C = 2 Hqk K + Hv V (q | k | v channels)
- *   conv_state: [B, W-1, C] of `dtype`, in/out (unused when W = 1)
- *   w:          [C, W] of `dtype`;  bias: [C] of `dtype` or NULL;  act: 0 none, 1 SiLU
- *   g, beta:    [B, Hv] fp32 (e.g. from gdn_gate_prep on the token's a, b)
- *   state:      [B, Hv, V, K] fp32, in/out (the layout of gdn_chunk_fwd's h_T)
- *   flags:      GDN_FLAG_QK_L2NORM, GDN_FLAG_O_F32 (any other bit: GDN_ERR_INVALID_ARG)
- *   o:          [B, Hv, V] of `dtype`, or fp32 with GDN_FLAG_O_F32
- * K a multiple of 32 up to 256, V >= 1, 1 <= W <= 8, Hv a multiple of Hqk.  x, o and
- * conv_state must not overlap.  Two launches on `stream`: the step, then the conv-state
- * shift. */
-gdn_status gdn_decode_step(const void *x, void *conv_state, const void *w, const void *bias,
-                           int32_t dtype, int32_t width, int32_t act, const float *g,
-                           const float *beta, float *state, int32_t B, int32_t Hqk, int32_t Hv,
-                           int32_t K, int32_t V, float scale, uint32_t flags, void *o,
+ *     conv_state_out[b] = rows 1 .. W-2 of conv_state_in[b], then x[b]
+ *   x:              [B, C] of `dtype`, C = 2 Hqk K + Hv V (q | k | v channels)
+ *   conv_state_in:  [B, W-1, C] of `dtype`;  conv_state_out: the same shape, a separate
+ *                   buffer (swap the two between steps); both unused when W = 1
+ *   w:              [C, W] of `dtype`;  bias: [C] of `dtype` or NULL;  act: 0 none, 1 SiLU
+ *   a, b:           [B, Hv] of `dtype`;  A_log, dt_bias: [Hv] fp32
+ *   state:          [B, Hv, V, K] fp32, in/out (the layout of gdn_chunk_fwd's h_T)
+ *   flags:          GDN_FLAG_QK_L2NORM, GDN_FLAG_O_F32 (any other bit: GDN_ERR_INVALID_ARG)
+ *   o:              [B, Hv, V] of `dtype`, or fp32 with GDN_FLAG_O_F32
+ * K a multiple of 32 up to 256, V >= 1, 1 <= W <= 8, Hv a multiple of Hqk.  x, o and the
+ * two conv-state buffers must not overlap.  One launch on `stream`. */
+gdn_status gdn_decode_step(const void *x, const void *conv_state_in, void *conv_state_out, const void *w,
+                           const void *bias, int32_t dtype, int32_t width, int32_t act, const void *a,
+                           const void *b, const float *A_log, const float *dt_bias, float *state, int32_t B,
+                           int32_t Hqk, int32_t Hv, int32_t K, int32_t V, float scale, uint32_t flags, void *o,
                            void *stream);
 
 /* Gated RMS norm of the core's output: the layer's "+ norm" after chunk_gated_delta_rule

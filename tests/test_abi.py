@@ -117,17 +117,25 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.gdn_cu_seqlens_from_position_ids(fake, -1, fake, fake, None) == 1
     assert lib.gdn_segment_summary(fake, fake, fake, fake, fake, 2, ctypes.byref(_shape(B=2)), 0,
                                    fake, fake, ws, 256, None) == 1
-    # decode step: x, cs, w, bias, dtype, width, act, g, beta, state, B, Hqk, Hv, K, V, scale, flags, o
+    # decode step: x, cs_in, cs_out, w, bias, dtype, width, act, a, b, A_log, dt_bias, state,
+    #              B, Hqk, Hv, K, V, scale, flags, o
     dec = lib.gdn_decode_step
-    assert dec(fake, fake, fake, None, 7, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
-    assert dec(fake, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 48, 128, 1.0, 1, fake, None) == 1
-    assert dec(fake, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 3, 4, 128, 128, 1.0, 1, fake, None) == 1
-    assert dec(fake, fake, fake, None, 1, 9, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
-    assert dec(fake, fake, fake, None, 1, 4, 2, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
-    assert dec(fake, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 2, fake, None) == 1
-    assert dec(None, fake, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
-    assert dec(fake, None, fake, None, 1, 4, 1, fake, fake, fake, 2, 2, 4, 128, 128, 1.0, 1, fake, None) == 1
-    assert dec(None, None, None, None, 1, 4, 1, None, None, None, 0, 2, 4, 128, 128, 1.0, 1, None, None) == 0
+    def d(**kw):
+        args = dict(x=fake, ci=fake, co=P(0x30000), w=fake, bias=None, dt=1, W=4, act=1, a=fake, b=fake, al=fake,
+                    db=fake, st=fake, B=2, Hqk=2, Hv=4, K=128, V=128, scale=1.0, flags=1, o=fake)
+        args.update(kw)
+        return dec(*args.values(), None)
+    assert d(dt=7) == 1
+    assert d(K=48) == 1
+    assert d(Hqk=3) == 1
+    assert d(W=9) == 1
+    assert d(act=2) == 1
+    assert d(flags=2) == 1
+    assert d(x=None) == 1
+    assert d(ci=None) == 1
+    assert d(co=fake) == 1      # the conv state may not be updated in place
+    assert d(a=None) == 1
+    assert d(B=0, x=None, ci=None, co=None, w=None, a=None, b=None, al=None, db=None, st=None, o=None) == 0
     # gated rms norm: o, z, w, dtype, n_rows, V, eps, y
     assert lib.gdn_gated_rmsnorm(fake, fake, None, 7, 10, 128, 1e-6, fake, None) == 1
     assert lib.gdn_gated_rmsnorm(fake, fake, None, 1, 10, 0, 1e-6, fake, None) == 1

@@ -49,11 +49,12 @@ def oracle_step(d, Hqk, Hv, K, V, width, act, dtype, l2norm=True):
 
 def gpu_step(crg, d, Hqk, Hv, K, V, act, l2norm=True, o_f32=False):
     on = {key: (t.to(DEV) if isinstance(t, torch.Tensor) else t) for key, t in d.items()}
-    g, beta = crg.gdn_gate_prep(on["a"], on["b"], on["A_log"], on["dt_bias"])
-    cs, st = on["conv_state"].clone(), on["state"].clone()
-    o = crg.gdn_decode_step(on["x"], cs, on["conv_w"], g, beta, st, Hqk, Hv, K, V, bias=on["bias"], act=act,
-                            scale=d["scale"], l2norm_qk=l2norm, o_f32=o_f32)
+    cs_in, st = on["conv_state"].clone(), on["state"].clone()
+    o, cs = crg.gdn_decode_step(on["x"], cs_in, on["conv_w"], on["a"], on["b"], on["A_log"], on["dt_bias"], st,
+                                Hqk, Hv, K, V, bias=on["bias"], act=act, scale=d["scale"], l2norm_qk=l2norm,
+                                o_f32=o_f32)
     torch.cuda.synchronize()
+    assert torch.equal(cs_in.cpu(), d["conv_state"])  # the input buffer is only read
     return o, st, cs
 
 
@@ -114,12 +115,14 @@ def test_decode_continues_prefill(crg):
                                 inp["dt_bias"])
     o_pre, state = crg.gdn_chunk_fwd(q, k, v, g, beta, scale=K ** -0.5)
     conv_state = x[T0 - (width - 1): T0].reshape(1, width - 1, -1).contiguous()
+    spare = torch.empty_like(conv_state)
     outs = []
-    for t in range(T0, T0 + T1):
-        gt, bt = crg.gdn_gate_prep(inp["a"][t: t + 1].contiguous(), inp["b"][t: t + 1].contiguous(),
-                                   inp["A_log"], inp["dt_bias"])
-        outs.append(crg.gdn_decode_step(x[t: t + 1].contiguous(), conv_state, w, gt, bt, state, Hqk, Hv, K, V,
-                                        act=1, scale=K ** -0.5))
+    for t in range(T0, T0 + T1):  # the two conv-state buffers swap roles every step
+        o_t, nxt = crg.gdn_decode_step(x[t: t + 1].contiguous(), conv_state, w, inp["a"][t: t + 1].contiguous(),
+                                       inp["b"][t: t + 1].contiguous(), inp["A_log"], inp["dt_bias"], state,
+                                       Hqk, Hv, K, V, act=1, scale=K ** -0.5, conv_state_out=spare)
+        outs.append(o_t)
+        conv_state, spare = nxt, conv_state
     torch.cuda.synchronize()
     o_dec = torch.cat(outs, dim=0)
     assert_close(o_pre, ref["o"][:T0], "bf16", "prefill o")
@@ -130,7 +133,7 @@ def test_decode_continues_prefill(crg):
 def test_decode_step_empty_batch(crg):
     d = synth.decode_inputs(1, 1, 1, 32, 32, 4, "f32", seed=31901)
     x = d["x"][:0].to(DEV)
-    o = crg.gdn_decode_step(x, d["conv_state"][:0].to(DEV), d["conv_w"].to(DEV),
-                            torch.zeros((0, 1), device=DEV), torch.zeros((0, 1), device=DEV),
-                            torch.zeros((0, 1, 32, 32), device=DEV), 1, 1, 32, 32)
+    o, _ = crg.gdn_decode_step(x, d["conv_state"][:0].to(DEV), d["conv_w"].to(DEV), d["a"][:0].to(DEV),
+                               d["b"][:0].to(DEV), d["A_log"].to(DEV), d["dt_bias"].to(DEV),
+                               torch.zeros((0, 1, 32, 32), device=DEV), 1, 1, 32, 32)
     assert o.shape == (0, 1, 32)
