@@ -46,16 +46,6 @@ inline gdn_status launch_status() {
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-// Qwen3.5 gates of one (token, v-head): g = -exp(A_log) softplus(a + dt_bias) (softplus as
-// max(x, 0) + log1p(exp(-|x|))), beta = sigmoid(b).  Shared by gdn_gate_prep and the decode
-// step so that both give the same values.
-__device__ __forceinline__ void gdn_gates(float a, float b, float A_log, float dt_bias, float &g, float &beta) {
-  const float x = a + dt_bias;
-  const float softplus = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
-  g = -expf(A_log) * softplus;
-  beta = 1.f / (1.f + expf(-b));
-}
-
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace gdn

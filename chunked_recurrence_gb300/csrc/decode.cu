@@ -21,6 +21,7 @@
 // output buffer, so no block overwrites what another still reads.  State traffic is
 // 2 V K 4 bytes per (sequence, v-head).
 #include "common.cuh"
+#include "gates.cuh"
 
 using namespace gdn;
 

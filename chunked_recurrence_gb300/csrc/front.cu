@@ -4,6 +4,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "gates.cuh"
 
 using namespace gdn;
 
