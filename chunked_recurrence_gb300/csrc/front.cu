@@ -3,8 +3,11 @@
 // chain reduce of segment summaries, and the small ABI helpers.
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "gates.cuh"
+#include "sm100.cuh"
 
 using namespace gdn;
 
@@ -244,6 +247,221 @@ __global__ void __launch_bounds__(128, 4) conv1d_kernel(const T *__restrict__ x,
   }
 }
 
+// The bf16 conv with its input staged in shared memory.  A block owns 1024 channels (eight
+// a thread) of a run of tokens; whole token rows of those channels (2 KB each) arrive by bulk
+// async copies into a ring of kStages stages of kStageRows rows, each stage with its own
+// mbarrier, so three stages of loads stay in flight while the block computes on the fourth.
+// The run starts W-1 tokens early (at most back to its sequence's start) so the history
+// comes through the same ring.  Runs are sized so that the grid is about one wave of
+// resident blocks.  The conv taps are packed fp32x2 FMAs, in the same order as the scalar
+// chain, and SiLU(x) = x / (1 + e^-x) takes e^-x as 2^(-x log2 e) on the hardware base-2
+// exponential and the division as a hardware reciprocal (both with flush to zero: the
+// results round to bf16 right after).  A wait that gives up (only a failed copy can make it)
+// leaves NaN in the outputs the block did not compute.
+constexpr int kStageRows = 8, kStages = 4, kStagedCols = 1024;
+constexpr uint32_t kStagedSmem = kStages * kStageRows * kStagedCols * 2;
+constexpr uint32_t kConvSpin = 1u << 22;
+
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float hw_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float hw_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int W>
+__global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                               const __nv_bfloat16 *__restrict__ w,
+                                                               const __nv_bfloat16 *__restrict__ bias,
+                                                               const int32_t *__restrict__ cu, int n_seqs,
+                                                               int64_t row_T, int64_t n_tok, int C, int run,
+                                                               int act, __nv_bfloat16 *__restrict__ y) {
+  using namespace gdn::sm100;
+  constexpr int VEC = 8, HW = W > 1 ? W - 1 : 1;
+  constexpr float kLog2e = 1.4426950408889634f;
+  extern __shared__ __align__(128) uint4 ring[];  // [kStages][kStageRows][kStagedCols / 8]
+  __shared__ __align__(8) uint64_t full[kStages];
+  const int tid = threadIdx.x;
+  const int cbase = blockIdx.y * kStagedCols, c0 = cbase + tid * VEC;
+  const bool mine = c0 < C;
+  const uint32_t row_bytes = (uint32_t)min(kStagedCols, C - cbase) * 2;
+  const int64_t t0 = (int64_t)blockIdx.x * run;
+  if (t0 >= n_tok) return;
+  const int64_t t1 = min(t0 + (int64_t)run, n_tok);
+  int s = 0;
+  int64_t start, end;
+  if (cu) {
+    s = seq_of_token(cu, n_seqs, t0);
+    while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t0) ++s;  // skip empty sequences
+    start = max((int64_t)cu[s], (int64_t)0);
+    end = cu[s + 1];
+  } else {
+    start = (t0 / row_T) * row_T;
+    end = start + row_T;
+  }
+  // loaded rows: the history tokens of t0 inside its sequence, then the run
+  const int64_t ts = max(t0 - (W - 1), min(start, t0));
+  const int nst = (int)((t1 - ts + kStageRows - 1) / kStageRows);
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int k) {  // stage k: rows ts + k kStageRows ...
+    const int st = k % kStages;
+    const int64_t a = ts + (int64_t)k * kStageRows;
+    const int m = (int)min((int64_t)kStageRows, t1 - a);
+    mbar_arrive_expect_tx(&full[st], (uint32_t)m * row_bytes);
+    for (int i = 0; i < m; ++i)
+      bulk_load(ring + (st * kStageRows + i) * (kStagedCols / 8), x + (a + i) * C + cbase, row_bytes, &full[st]);
+  };
+  if (tid == 0)
+    for (int k = 0; k < min(kStages, nst); ++k) issue(k);
+  float wt[W][VEC], bs[VEC], hist[HW][VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) wt[j][v] = mine ? to_f32(w[(int64_t)(c0 + v) * W + j]) : 0.f;
+    bs[v] = (mine && bias) ? to_f32(bias[c0 + v]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < HW; ++j) hist[j][v] = 0.f;
+  }
+  int k = 0;
+  for (; k < nst; ++k) {
+    const int st = k % kStages;
+    const bool ok = mbar_wait(&full[st], (uint32_t)(k / kStages) & 1, kConvSpin);
+    if (__syncthreads_or(!ok)) break;
+    const int64_t a = ts + (int64_t)k * kStageRows;
+    const int m = (int)min((int64_t)kStageRows, t1 - a);
+#pragma unroll
+    for (int i = 0; i < kStageRows; ++i) {
+      if (i >= m) break;
+      const int64_t t = a + i;
+      if (t >= end) {  // a new sequence begins at t: zero history
+        if (cu) {
+          while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t) ++s;
+          start = max((int64_t)cu[s], (int64_t)0);
+          end = cu[s + 1];
+        } else {
+          start = t;
+          end = t + row_T;
+        }
+#pragma unroll
+        for (int j = 0; j < HW; ++j)
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) hist[j][v] = 0.f;
+      }
+      float cur[VEC];
+      Vec<__nv_bfloat16, VEC>::cvt(ring[(st * kStageRows + i) * (kStagedCols / 8) + tid], cur);
+      if (t >= t0 && mine) {
+        float out[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; v += 2) {
+          uint64_t acc = f2_pack(bs[v], bs[v + 1]);
+#pragma unroll
+          for (int j = 0; j < W - 1; ++j)
+            acc = f2_fma(f2_pack(wt[j][v], wt[j][v + 1]), f2_pack(hist[j][v], hist[j][v + 1]), acc);
+          acc = f2_fma(f2_pack(wt[W - 1][v], wt[W - 1][v + 1]), f2_pack(cur[v], cur[v + 1]), acc);
+          if (act) {
+            float e0, e1, d0, d1;
+            f2_unpack(f2_mul(acc, f2_pack(-kLog2e, -kLog2e)), e0, e1);
+            f2_unpack(f2_add(f2_pack(hw_exp2(e0), hw_exp2(e1)), f2_pack(1.f, 1.f)), d0, d1);
+            acc = f2_mul(acc, f2_pack(hw_rcp(d0), hw_rcp(d1)));
+          }
+          f2_unpack(acc, out[v], out[v + 1]);
+        }
+        Vec<__nv_bfloat16, VEC>::store(y + t * C + c0, out);
+      }
+      if (W > 1) {
+#pragma unroll
+        for (int j = 0; j + 1 < HW; ++j)
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) hist[j][v] = hist[j + 1][v];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) hist[HW - 1][v] = cur[v];
+      }
+    }
+    __syncthreads();  // every read of stage st is done before it is refilled
+    if (tid == 0 && k + kStages < nst) issue(k + kStages);
+  }
+  if (k < nst) {  // a wait gave up: NaN where nothing was computed, and the copies land first
+    if (mine) {
+      float nan[VEC];
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) nan[v] = __int_as_float(0x7fc00000);
+      for (int64_t t = max(t0, ts + (int64_t)k * kStageRows); t < t1; ++t) Vec<__nv_bfloat16, VEC>::store(y + t * C + c0, nan);
+    }
+    if (tid == 0)
+      for (int j = k; j < min(nst, k + kStages); ++j) (void)mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1, kConvSpin);
+    __syncthreads();
+  }
+}
+
+// Launches the staged bf16 conv; returns false (nothing launched) where it does not apply.
+static bool launch_conv_staged(int W, cudaStream_t st, const __nv_bfloat16 *x, const __nv_bfloat16 *w,
+                               const __nv_bfloat16 *bias, const int32_t *cu, int n_seqs, int64_t row_T,
+                               int64_t n_tok, int C, int act, __nv_bfloat16 *y, gdn_status *status) {
+  int dev = 0, sms = 0, smem_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
+    *status = GDN_ERR_CUDA;
+    return true;
+  }
+  const int64_t ncb = (C + kStagedCols - 1) / kStagedCols;
+  if (ncb > 65535) return false;
+  const int per_sm = std::max(1, std::min(3, smem_sm / (int)(kStagedSmem + 1024)));
+  const int64_t per_wave = std::max<int64_t>(1, (int64_t)sms * per_sm / ncb);  // runs in one wave
+  const int64_t run = std::max<int64_t>(16, (n_tok + per_wave - 1) / per_wave);
+  if (run > 2147483647LL) return false;
+  const dim3 grid((unsigned)((n_tok + run - 1) / run), (unsigned)ncb);
+#define GDN_STAGED_CASE(WW)                                                                          \
+  case WW:                                                                                           \
+    if (cudaFuncSetAttribute(conv1d_staged_kernel<WW>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             (int)kStagedSmem) != cudaSuccess) {                                     \
+      *status = GDN_ERR_CUDA;                                                                        \
+      return true;                                                                                   \
+    }                                                                                                \
+    conv1d_staged_kernel<WW><<<grid, 128, kStagedSmem, st>>>(x, w, bias, cu, n_seqs, row_T, n_tok, C, \
+                                                             (int)run, act, y);                      \
+    break;
+  switch (W) {
+    GDN_STAGED_CASE(1) GDN_STAGED_CASE(2) GDN_STAGED_CASE(3) GDN_STAGED_CASE(4)
+    GDN_STAGED_CASE(5) GDN_STAGED_CASE(6)
+    default: return false;  // wider convs hold more history than fit 3 blocks an SM: the register kernel
+  }
+#undef GDN_STAGED_CASE
+  *status = launch_status();
+  return true;
+}
+
 template <typename T, int VEC>
 static void launch_conv_w(int W, dim3 grid, dim3 block, cudaStream_t st, const T *x, const T *w,
                           const T *bias, const int32_t *cu, int n_seqs, int64_t row_T,
@@ -282,6 +500,10 @@ extern "C" gdn_status gdn_conv1d_varlen(const void *x, const void *w, const void
     const int per = vec ? 8 : 1;
     const dim3 grid((unsigned)runs, (unsigned)((C / per + 127) / 128));
     if (grid.y > 65535u) return GDN_ERR_UNSUPPORTED;
+    gdn_status staged = GDN_OK;
+    if (vec && launch_conv_staged(width, st, (const T *)x, (const T *)w, (const T *)bias, cu_seqlens, n_seqs,
+                                  row_T, n_tokens, C, act, (T *)y, &staged))
+      return staged;
     if (vec)
       launch_conv_w<T, 8>(width, grid, block, st, (const T *)x, (const T *)w, (const T *)bias,
                           cu_seqlens, n_seqs, row_T, n_tokens, C, act, (T *)y);

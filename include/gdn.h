@@ -119,7 +119,10 @@ gdn_status gdn_gate_prep(const void *a, const void *b, int32_t ab_dtype, const f
  * (act = 0) or SiLU (act = 1).  x, y: [n_tokens, C] (row stride C), w: [C, W],
  * bias: [C] or NULL, all of `dtype`; accumulation in fp32.  Sequences are
  * cu_seqlens (n_seqs+1 offsets) or, when cu_seqlens is NULL, n_seqs equal
- * rows of n_tokens / n_seqs tokens.  1 <= W <= 8.  x and y must not overlap. */
+ * rows of n_tokens / n_seqs tokens.  1 <= W <= 8.  x and y must not overlap.
+ * bf16 with C a multiple of 8, W <= 6 and 16-byte aligned x, y stages token rows
+ * through shared memory by bulk async copies; a copy wait that runs out (a failed
+ * copy, never an input error) leaves NaN in the outputs it could not compute. */
 gdn_status gdn_conv1d_varlen(const void *x, const void *w, const void *bias, int32_t dtype,
                              const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t C,
                              int32_t width, int32_t act, void *y, void *stream);

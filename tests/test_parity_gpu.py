@@ -142,6 +142,27 @@ def test_conv_rows_odd_channels_bias(crg, dtype):
     _conv_check(crg, x, w, None, 3, 1, dtype, bias)
 
 
+@pytest.mark.parametrize("width", [1, 3, 4, 6])
+@pytest.mark.parametrize("rows", [False, True])
+def test_conv_staged_multiblock(crg, width, rows):
+    """bf16 with C a multiple of 8 takes the shared-memory staged kernel: two channel blocks
+    (the second ragged, 136 of 1024 channels), runs of many stages that start and end inside
+    sequences, sequences shorter than the history, bias, with and without SiLU."""
+    gen = _cpu_gen(40 + width)
+    C = 1160
+    if rows:
+        cu, n_seqs, n = None, 3, 3 * 1003
+    else:
+        lens = [700, 1, 1, 2, 1500, 0, 3, 796]
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+        n_seqs, n = None, int(cu[-1])
+    x = _round(torch.randn((n, C), generator=gen), "bf16")
+    w = _round(torch.randn((C, width), generator=gen) * 0.5, "bf16")
+    bias = _round(torch.randn(C, generator=gen) * 0.2, "bf16")
+    _conv_check(crg, x, w, cu, n_seqs, 1, "bf16", bias)
+    _conv_check(crg, x, w, cu, n_seqs, 0, "bf16")
+
+
 def test_conv_packed_equals_separate_on_gpu(crg):
     gen = _cpu_gen(4)
     lens = [40, 1, 77]
