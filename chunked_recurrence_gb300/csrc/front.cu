@@ -360,27 +360,12 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
     if (__syncthreads_or(!ok)) break;
     const int64_t a = ts + (int64_t)k * kStageRows;
     const int m = (int)min((int64_t)kStageRows, t1 - a);
-#pragma unroll
-    for (int i = 0; i < kStageRows; ++i) {
-      if (i >= m) break;
-      const int64_t t = a + i;
-      if (t >= end) {  // a new sequence begins at t: zero history
-        if (cu) {
-          while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t) ++s;
-          start = max((int64_t)cu[s], (int64_t)0);
-          end = cu[s + 1];
-        } else {
-          start = t;
-          end = t + row_T;
-        }
-#pragma unroll
-        for (int j = 0; j < HW; ++j)
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) hist[j][v] = 0.f;
-      }
+    const uint4 *rows = ring + st * kStageRows * (kStagedCols / 8) + tid;
+    // one token row: its conv output (when `emit`) and the history shift
+    auto conv_row = [&](const uint4 &raw, int64_t t, bool emit) {
       float cur[VEC];
-      Vec<__nv_bfloat16, VEC>::cvt(ring[(st * kStageRows + i) * (kStagedCols / 8) + tid], cur);
-      if (t >= t0 && mine) {
+      Vec<__nv_bfloat16, VEC>::cvt(raw, cur);
+      if (emit) {
         float out[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; v += 2) {
@@ -406,6 +391,36 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
           for (int v = 0; v < VEC; ++v) hist[j][v] = hist[j + 1][v];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) hist[HW - 1][v] = cur[v];
+      }
+    };
+    if (m == kStageRows && a >= t0 && a + kStageRows <= end && mine) {
+      // the whole stage lies inside one sequence and past the history rows: straight-line
+      // rows with no per-row test, so the rows' arithmetic can interleave
+      uint4 raw[kStageRows];
+#pragma unroll
+      for (int i = 0; i < kStageRows; ++i) raw[i] = rows[i * (kStagedCols / 8)];
+#pragma unroll
+      for (int i = 0; i < kStageRows; ++i) conv_row(raw[i], a + i, true);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kStageRows; ++i) {
+        if (i >= m) break;
+        const int64_t t = a + i;
+        if (t >= end) {  // a new sequence begins at t: zero history
+          if (cu) {
+            while (s + 1 < n_seqs && (int64_t)cu[s + 1] <= t) ++s;
+            start = max((int64_t)cu[s], (int64_t)0);
+            end = cu[s + 1];
+          } else {
+            start = t;
+            end = t + row_T;
+          }
+#pragma unroll
+          for (int j = 0; j < HW; ++j)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) hist[j][v] = 0.f;
+        }
+        conv_row(rows[i * (kStagedCols / 8)], t, t >= t0 && mine);
       }
     }
     __syncthreads();  // every read of stage st is done before it is refilled
