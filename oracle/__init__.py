@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the gated delta rule forward and the steps around it.
+"""fp64 CPU oracle for the gated delta rule forward, its backward and the steps around it.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` leg of ``bench.py`` may import this
@@ -57,6 +57,9 @@ def _load():
             _lib.oracle_gated_rmsnorm.argtypes = [d, d, d, i64, i32, ctypes.c_double, d]
             _lib.oracle_gdn_fwd.argtypes = [d, d, d, d, d, d, d, i32, i32, i32, i32, i32,
                                             ctypes.c_double, i32, ctypes.c_double, d, d, i32]
+            _lib.oracle_gdn_bwd.argtypes = [d, d, d, d, d, d, d, i32, i32, i32, i32, i32,
+                                            ctypes.c_double, i32, ctypes.c_double, d, d, d, d, d,
+                                            d, d, d, i32]
             _lib.oracle_segment_summary.argtypes = [d, d, d, d, d, i32, i32, i32, i32, i32,
                                                     i32, ctypes.c_double, d, d, i32]
             _lib.oracle_chain_reduce.argtypes = [d, d, d, i32, i32, i32, i32, d, d]
@@ -145,6 +148,35 @@ def gdn_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=1.0, l2norm_qk=Fal
                            n_seq, Hqk, Hv, K, V, float(scale), int(bool(l2norm_qk)), eps,
                            _ptr(o), _ptr(hT), _threads(n_threads))
     return o, hT
+
+
+def gdn_bwd(q, k, v, g, beta, do, dhT=None, h0=None, cu_seqlens=None, scale=1.0,
+            l2norm_qk=False, eps=L2_EPS, B=1, n_threads=None):
+    """Gradients of L = sum(do * o) + sum(dhT * hT) for the forward of gdn_fwd.
+
+    Same inputs and layouts as gdn_fwd, plus do: [n_tok, Hv, V] and dhT:
+    [n_seq, Hv, V, K] or None.  Returns (dq, dk, dv, dg, dbeta, dh0); dh0 is the
+    gradient with respect to the start state (zero when h0 is None).
+    """
+    q, k, v, g, beta, do = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta), _f64(do)
+    n_tok, Hqk, K = k.shape
+    Hv, V = v.shape[1], v.shape[2]
+    assert Hv % Hqk == 0 and do.shape == v.shape
+    cu = _cu(cu_seqlens, n_tok, B)
+    n_seq = len(cu) - 1
+    h0 = None if h0 is None else _f64(h0)
+    dhT = None if dhT is None else _f64(dhT)
+    for t in (h0, dhT):
+        if t is not None:
+            assert t.shape == (n_seq, Hv, V, K)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dg, dbeta = np.zeros_like(g), np.zeros_like(beta)
+    dh0 = np.zeros((n_seq, Hv, V, K))
+    _load().oracle_gdn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu),
+                           n_seq, Hqk, Hv, K, V, float(scale), int(bool(l2norm_qk)), eps,
+                           _ptr(do), _ptr(dhT), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                           _ptr(dbeta), _ptr(dh0), _threads(n_threads))
+    return dq, dk, dv, dg, dbeta, dh0
 
 
 def segment_summary(k, v, g, beta, seg_bounds, l2norm_qk=False, eps=L2_EPS, n_threads=None):

@@ -1,6 +1,7 @@
 /*
  * gdn_oracle.c -- plain, slow, token-by-token fp64 CPU oracle for the gated
- * delta rule forward and the steps around it.
+ * delta rule forward, its backward (the exact gradient of that forward) and
+ * the steps around it.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
  * execute this file: it is used by tests/, by __graft_entry__.smoke() and by
@@ -168,6 +169,22 @@ typedef struct {
   double *o, *hT;
 } fwd_ctx;
 
+/* One token's state update, S_t from S_{t-1}: S <- alpha S;  r = v - S k;
+ * S <- S + beta r k^T. */
+static void fwd_token(double *S, const double *kt, const double *vt, double alpha, double bt,
+                      int K, int V) {
+  for (int i = 0; i < V; ++i) {
+    double *row = S + (int64_t)i * K;
+    double pred = 0.0;
+    for (int j = 0; j < K; ++j) {
+      row[j] *= alpha;
+      pred += row[j] * kt[j];
+    }
+    const double r = vt[i] - pred;
+    for (int j = 0; j < K; ++j) row[j] += bt * r * kt[j];
+  }
+}
+
 /* One (sequence, v-head) pair, token by token.  The v-head h reads q/k head
  * h / (Hv / Hqk): each q/k head serves Hv/Hqk consecutive v-heads.
  * Per token, with alpha = exp(g_t):
@@ -198,19 +215,11 @@ static void fwd_job(void *vctx, int64_t job) {
     const double bt = c->beta[t * c->Hv + h];
     const double *vt = c->v + (t * c->Hv + h) * V;
     double *ot = c->o + (t * c->Hv + h) * V;
+    fwd_token(S, kt, vt, alpha, bt, K, V);
     for (int i = 0; i < V; ++i) {
-      double *row = S + (int64_t)i * K;
-      double pred = 0.0;
-      for (int j = 0; j < K; ++j) {
-        row[j] *= alpha;
-        pred += row[j] * kt[j];
-      }
-      const double r = vt[i] - pred;
+      const double *row = S + (int64_t)i * K;
       double out = 0.0;
-      for (int j = 0; j < K; ++j) {
-        row[j] += bt * r * kt[j];
-        out += row[j] * qt[j];
-      }
+      for (int j = 0; j < K; ++j) out += row[j] * qt[j];
       ot[i] = c->scale * out;
     }
   }
@@ -229,6 +238,171 @@ void oracle_gdn_fwd(const double *q, const double *k, const double *v,
                     int n_threads) {
   fwd_ctx c = {q, k, v, g, beta, h0, cu, n_seq, Hqk, Hv, K, V, l2norm, scale, eps, o, hT};
   run_jobs(fwd_job, &c, (int64_t)n_seq * Hv, n_threads);
+}
+
+/* ------------------------------------------------ the recurrence, backward */
+
+/* The backward of the chunked rule is what training runs through the layer
+ * ("[v1] support GDN Ulysses cp", Testing: loss alignment over 2000 training
+ * steps; "feat: hybrid CP for Qwen3.5 MoE (DeltaNet + attention)", Test plan:
+ * forward/backward passes).  The pages give no formula for it, so it is the
+ * exact gradient of the forward above: for upstream gradients dout (of o) and
+ * dhT (of hT), the gradients of
+ *     L = sum_t <dout_t, o_t> + sum <dhT, S_T>
+ * with respect to q, k, v, g, beta and h0, taken back through each token step
+ * of fwd_job in reverse order.  With P = alpha S_{t-1}, r = v - P k,
+ * S_t = P + beta r k^T and o_t = scale S_t q, given dS = dL/dS_t:
+ *     dq   += scale S_t^T dout_t         dS  += scale dout_t q^T
+ *     dbeta = r^T dS k                    dr   = beta dS k,   dv = dr
+ *     dk   += beta dS^T r - P^T dr        dP   = dS - dr k^T
+ *     dg    = alpha <S_{t-1}, dP>         dS_{t-1} = alpha dP
+ * and dh0 = dS_0.  q and k here are the unit-norm vectors when l2norm is set;
+ * their gradients then go back through the norm (l2_backward).  A q/k head
+ * serves Hv/Hqk v-heads, so its gradient is the sum over them. */
+
+typedef struct {
+  const double *q, *k, *v, *g, *beta, *h0, *dout, *dhT;
+  const int32_t *cu;
+  int n_seq, Hqk, Hv, K, V, l2norm;
+  double scale, eps;
+  double *dq, *dk, *dv, *dg, *dbeta, *dh0;
+} bwd_ctx;
+
+enum { kCheckpoint = 64 }; /* tokens between the states kept from the forward */
+
+/* With n = sqrt(|x|^2 + eps) and xh = x / n:  dx = dxh / n - x (x . dxh) / n^3. */
+static void l2_backward(const double *x, const double *dxh, int n, double eps, double *dx) {
+  double ss = 0.0, xd = 0.0;
+  for (int i = 0; i < n; ++i) {
+    ss += x[i] * x[i];
+    xd += x[i] * dxh[i];
+  }
+  const double nn = sqrt(ss + eps);
+  for (int i = 0; i < n; ++i) dx[i] = dxh[i] / nn - x[i] * xd / (nn * nn * nn);
+}
+
+/* One (sequence, q/k head) pair: its Hv/Hqk v-heads one after another.  The
+ * forward keeps the state before every kCheckpoint-th token; the backward
+ * recomputes the states of one block of tokens from there (bit for bit, the
+ * same operations) and walks that block from its last token to its first. */
+static void bwd_job(void *vctx, int64_t job) {
+  const bwd_ctx *c = (const bwd_ctx *)vctx;
+  const int s = (int)(job / c->Hqk), qh = (int)(job % c->Hqk);
+  const int K = c->K, V = c->V, G = c->Hv / c->Hqk, Hv = c->Hv, Hqk = c->Hqk;
+  const int64_t t0 = c->cu[s], n = c->cu[s + 1] - t0, VK = (int64_t)V * K;
+  const int64_t n_ck = n / kCheckpoint + 1;
+  double *ck = (double *)malloc(sizeof(double) * n_ck * VK);
+  double *st = (double *)malloc(sizeof(double) * (kCheckpoint + 1) * VK);
+  double *dS = (double *)malloc(sizeof(double) * VK);
+  double *qn = (double *)malloc(sizeof(double) * (n > 0 ? n : 1) * K);
+  double *kn = (double *)malloc(sizeof(double) * (n > 0 ? n : 1) * K);
+  double *dqn = (double *)calloc((size_t)(n > 0 ? n : 1) * K, sizeof(double));
+  double *dkn = (double *)calloc((size_t)(n > 0 ? n : 1) * K, sizeof(double));
+  double *r = (double *)malloc(sizeof(double) * V), *dr = (double *)malloc(sizeof(double) * V);
+  double *dSk = (double *)malloc(sizeof(double) * V);
+  for (int64_t i = 0; i < n; ++i) {
+    const double *qraw = c->q + ((t0 + i) * Hqk + qh) * K, *kraw = c->k + ((t0 + i) * Hqk + qh) * K;
+    if (c->l2norm) {
+      l2_normalise(qraw, K, c->eps, qn + i * K);
+      l2_normalise(kraw, K, c->eps, kn + i * K);
+    } else {
+      memcpy(qn + i * K, qraw, sizeof(double) * K);
+      memcpy(kn + i * K, kraw, sizeof(double) * K);
+    }
+  }
+  for (int hh = 0; hh < G; ++hh) {
+    const int h = qh * G + hh;
+    /* forward, keeping the checkpoints */
+    if (c->h0) memcpy(st, c->h0 + ((int64_t)s * Hv + h) * VK, sizeof(double) * VK);
+    else memset(st, 0, sizeof(double) * VK);
+    for (int64_t i = 0; i < n; ++i) {
+      if (i % kCheckpoint == 0) memcpy(ck + (i / kCheckpoint) * VK, st, sizeof(double) * VK);
+      const int64_t t = t0 + i;
+      fwd_token(st, kn + i * K, c->v + (t * Hv + h) * V, exp(c->g[t * Hv + h]), c->beta[t * Hv + h], K, V);
+    }
+    if (c->dhT) memcpy(dS, c->dhT + ((int64_t)s * Hv + h) * VK, sizeof(double) * VK);
+    else memset(dS, 0, sizeof(double) * VK);
+    for (int64_t b = (n - 1) / kCheckpoint; n > 0 && b >= 0; --b) {
+      const int64_t i0 = b * kCheckpoint, i1 = (i0 + kCheckpoint < n) ? i0 + kCheckpoint : n;
+      memcpy(st, ck + b * VK, sizeof(double) * VK); /* st[m] = state before token i0 + m */
+      for (int64_t i = i0; i < i1; ++i) {
+        const int64_t t = t0 + i;
+        double *nx = st + (i - i0 + 1) * VK;
+        memcpy(nx, nx - VK, sizeof(double) * VK);
+        fwd_token(nx, kn + i * K, c->v + (t * Hv + h) * V, exp(c->g[t * Hv + h]), c->beta[t * Hv + h], K, V);
+      }
+      for (int64_t i = i1 - 1; i >= i0; --i) {
+        const int64_t t = t0 + i;
+        const double *Sp = st + (i - i0) * VK, *Sn = Sp + VK;
+        const double *qt = qn + i * K, *kt = kn + i * K;
+        const double *vt = c->v + (t * Hv + h) * V, *dot = c->dout + (t * Hv + h) * V;
+        const double alpha = exp(c->g[t * Hv + h]), bt = c->beta[t * Hv + h];
+        double *dqt = dqn + i * K, *dkt = dkn + i * K;
+        /* o_t = scale S_t q */
+        for (int a = 0; a < V; ++a)
+          for (int j = 0; j < K; ++j) {
+            dqt[j] += c->scale * Sn[(int64_t)a * K + j] * dot[a];
+            dS[(int64_t)a * K + j] += c->scale * dot[a] * qt[j];
+          }
+        /* S_t = P + beta r k^T, r = v - P k, P = alpha S_{t-1} */
+        double db = 0.0;
+        for (int a = 0; a < V; ++a) {
+          double pk = 0.0, sk = 0.0;
+          for (int j = 0; j < K; ++j) {
+            pk += (Sp[(int64_t)a * K + j] * alpha) * kt[j];
+            sk += dS[(int64_t)a * K + j] * kt[j];
+          }
+          r[a] = vt[a] - pk;
+          dSk[a] = sk;
+          db += r[a] * sk;
+        }
+        for (int a = 0; a < V; ++a) {
+          dr[a] = bt * dSk[a];
+          c->dv[(t * Hv + h) * V + a] = dr[a];
+        }
+        for (int j = 0; j < K; ++j) {
+          double acc = 0.0;
+          for (int a = 0; a < V; ++a)
+            acc += bt * dS[(int64_t)a * K + j] * r[a] - alpha * Sp[(int64_t)a * K + j] * dr[a];
+          dkt[j] += acc;
+        }
+        double dalpha = 0.0;
+        for (int a = 0; a < V; ++a)
+          for (int j = 0; j < K; ++j) {
+            const double dp = dS[(int64_t)a * K + j] - dr[a] * kt[j];
+            dalpha += Sp[(int64_t)a * K + j] * dp;
+            dS[(int64_t)a * K + j] = alpha * dp;
+          }
+        c->dg[t * Hv + h] = alpha * dalpha;
+        c->dbeta[t * Hv + h] = db;
+      }
+    }
+    if (c->dh0) memcpy(c->dh0 + ((int64_t)s * Hv + h) * VK, dS, sizeof(double) * VK);
+  }
+  for (int64_t i = 0; i < n; ++i) { /* back to the raw q and k */
+    const int64_t off = ((t0 + i) * Hqk + qh) * K;
+    if (c->l2norm) {
+      l2_backward(c->q + off, dqn + i * K, K, c->eps, c->dq + off);
+      l2_backward(c->k + off, dkn + i * K, K, c->eps, c->dk + off);
+    } else {
+      memcpy(c->dq + off, dqn + i * K, sizeof(double) * K);
+      memcpy(c->dk + off, dkn + i * K, sizeof(double) * K);
+    }
+  }
+  free(ck); free(st); free(dS); free(qn); free(kn); free(dqn); free(dkn); free(r); free(dr); free(dSk);
+}
+
+/* Gradients of every input for upstream dout [n_tok, Hv, V] and dhT (may be
+ * NULL: no loss on the final state).  h0 may be NULL (zero start state); dh0
+ * may be NULL.  Outputs have the layouts of the inputs. */
+void oracle_gdn_bwd(const double *q, const double *k, const double *v, const double *g,
+                    const double *beta, const double *h0, const int32_t *cu, int n_seq, int Hqk,
+                    int Hv, int K, int V, double scale, int l2norm, double eps,
+                    const double *dout, const double *dhT, double *dq, double *dk, double *dv,
+                    double *dg, double *dbeta, double *dh0, int n_threads) {
+  bwd_ctx c = {q, k, v, g, beta, h0, dout, dhT, cu, n_seq, Hqk, Hv, K, V, l2norm, scale, eps,
+               dq, dk, dv, dg, dbeta, dh0};
+  run_jobs(bwd_job, &c, (int64_t)n_seq * Hqk, n_threads);
 }
 
 /* -------------------------------------------------- segment summaries */

@@ -23,7 +23,14 @@ MUTANTS = {
     "decay_dropped": ("row[j] *= alpha;", "row[j] *= 1.0;"),
     "residual_sign": ("const double r = vt[i] - pred;", "const double r = vt[i] + pred;"),
     "beta_dropped": ("row[j] += bt * r * kt[j];", "row[j] += r * kt[j];"),
-    "read_before_write": ("out += row[j] * qt[j];", "out += (row[j] - bt * r * kt[j]) * qt[j];"),
+    "read_before_write": ("    fwd_token(S, kt, vt, alpha, bt, K, V);\n    for (int i = 0; i < V; ++i) {\n"
+                          "      const double *row = S + (int64_t)i * K;\n      double out = 0.0;\n"
+                          "      for (int j = 0; j < K; ++j) out += row[j] * qt[j];\n"
+                          "      ot[i] = c->scale * out;\n    }",
+                          "    for (int i = 0; i < V; ++i) {\n"
+                          "      const double *row = S + (int64_t)i * K;\n      double out = 0.0;\n"
+                          "      for (int j = 0; j < K; ++j) out += row[j] * qt[j];\n"
+                          "      ot[i] = c->scale * out;\n    }\n    fwd_token(S, kt, vt, alpha, bt, K, V);"),
     "key_index_shift": ("pred += row[j] * kt[j];", "pred += row[j] * kt[(j + 1) % K];"),
     "scale_dropped": ("ot[i] = c->scale * out;", "ot[i] = out;"),
     "gate_sign": ("g[i] = -exp(A_log[h]) * softplus;", "g[i] = exp(A_log[h]) * softplus;"),
@@ -46,6 +53,20 @@ MUTANTS = {
     "rmsnorm_gate_z_dropped": ("const double gate = zrow[v] / (1.0 + exp(-zrow[v]));",
                                "const double gate = 1.0 / (1.0 + exp(-zrow[v]));"),
     "rmsnorm_weight_dropped": ("* (w ? w[v] : 1.0) * gate", "* gate"),
+    "bwd_key_state_term_dropped": (
+        "acc += bt * dS[(int64_t)a * K + j] * r[a] - alpha * Sp[(int64_t)a * K + j] * dr[a];",
+        "acc += bt * dS[(int64_t)a * K + j] * r[a];"),
+    "bwd_state_decay_dropped": ("dS[(int64_t)a * K + j] = alpha * dp;", "dS[(int64_t)a * K + j] = dp;"),
+    "bwd_dP_sign": ("const double dp = dS[(int64_t)a * K + j] - dr[a] * kt[j];",
+                    "const double dp = dS[(int64_t)a * K + j] + dr[a] * kt[j];"),
+    "bwd_gqa_overwrite": ("dkt[j] += acc;", "dkt[j] = acc;"),
+    "bwd_norm_jacobian_dropped": ("dx[i] = dxh[i] / nn - x[i] * xd / (nn * nn * nn);",
+                                  "dx[i] = dxh[i] / nn;"),
+    "bwd_output_reads_old_state": ("dqt[j] += c->scale * Sn[(int64_t)a * K + j] * dot[a];",
+                                   "dqt[j] += c->scale * Sp[(int64_t)a * K + j] * dot[a];"),
+    "bwd_recompute_from_block_start": ("memcpy(nx, nx - VK, sizeof(double) * VK);",
+                                       "memcpy(nx, st, sizeof(double) * VK);"),
+    "bwd_gate_chain_dropped": ("c->dg[t * Hv + h] = alpha * dalpha;", "c->dg[t * Hv + h] = dalpha;"),
 }
 
 

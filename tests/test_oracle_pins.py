@@ -483,6 +483,102 @@ def test_thread_count_does_not_change_results(oracle_mod):
     np.testing.assert_array_equal(a[1], b[1])
 
 
+# ------------------------------------------------------------ backward
+
+def _fd_check(oracle_mod, args, do, dhT, kw, sample=None, seed=0):
+    """Central differences of L = sum(do * o) + sum(dhT * hT) through the forward oracle
+    (pinned above) against gdn_bwd, on every element or on `sample` random elements of
+    each input."""
+    grads = oracle_mod.gdn_bwd(*args[:5], do, dhT, args[5], **kw)
+
+    def loss(a):
+        o, hT = oracle_mod.gdn_fwd(*a, **kw)
+        return (o * do).sum() + (0.0 if dhT is None else (hT * dhT).sum())
+
+    rng = np.random.default_rng(seed)
+    for ai, (x, gx) in enumerate(zip(args, grads)):
+        if x is None:
+            continue
+        idxs = list(np.ndindex(x.shape))
+        if sample is not None and len(idxs) > sample:
+            idxs = [idxs[i] for i in rng.choice(len(idxs), sample, replace=False)]
+        for idx in idxs:
+            ap = [None if y is None else y.copy() for y in args]
+            am = [None if y is None else y.copy() for y in args]
+            ap[ai][idx] += 1e-6
+            am[ai][idx] -= 1e-6
+            fd = (loss(ap) - loss(am)) / 2e-6
+            assert abs(fd - gx[idx]) <= 1e-6 * (1.0 + abs(fd)), (ai, idx, fd, gx[idx])
+
+
+def test_gdn_bwd_finite_differences(oracle_mod):
+    """Every gradient of every element, two packed sequences, two v-heads sharing one q/k
+    head, a start state and a loss on the final state; with and without the q/k L2 norm."""
+    rng = np.random.default_rng(71)
+    q, k, v, g, beta, h0 = _rand_case(rng, 12, 1, 2, 4, 3, n_seq=2)
+    k = rng.standard_normal(k.shape)  # raw keys, so the norm's Jacobian matters
+    h0 = 0.3 * h0
+    do = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape)
+    cu = np.array([0, 5, 12], dtype=np.int32)
+    for l2 in (True, False):
+        _fd_check(oracle_mod, [q, k, v, g, beta, h0], do, dhT,
+                  dict(cu_seqlens=cu, scale=0.7, l2norm_qk=l2))
+
+
+def test_gdn_bwd_finite_differences_past_a_checkpoint(oracle_mod):
+    """Rows of 70 tokens (longer than the 64 tokens between the states the backward keeps),
+    two q/k heads of two v-heads each, no start state, no loss on the final state."""
+    rng = np.random.default_rng(72)
+    q, k, v, g, beta, _ = _rand_case(rng, 140, 2, 4, 3, 2, mild=True, h0=False)
+    do = rng.standard_normal(v.shape)
+    _fd_check(oracle_mod, [q, k, v, g, beta, None], do, None,
+              dict(B=2, scale=0.5, l2norm_qk=True), sample=25, seed=3)
+
+
+def test_gdn_bwd_single_token_closed_form(oracle_mod):
+    """One token from S_0: S_1 = a S_0 + b (v - a S_0 k) k^T, o = s S_1 q.  By hand:
+    do/dv etc. of L = <do, o> + <dhT, S_1>."""
+    rng = np.random.default_rng(73)
+    K, V = 5, 4
+    q, k, v = rng.standard_normal(K), rng.standard_normal(K), rng.standard_normal(V)
+    S0 = rng.standard_normal((V, K))
+    gg, b, sc = -0.4, 0.6, 0.8
+    a = math.exp(gg)
+    do, D = rng.standard_normal(V), rng.standard_normal((V, K))
+    r = v - a * S0 @ k
+    S1 = a * S0 + b * np.outer(r, k)
+    G = sc * np.outer(do, q) + D                      # dL/dS_1
+    want = {
+        "dq": sc * S1.T @ do,
+        "dv": b * G @ k,
+        "dbeta": r @ G @ k,
+        "dk": b * G.T @ r - a * S0.T @ (b * G @ k),
+        "dh0": a * (G - np.outer(b * G @ k, k)),
+    }
+    want["dg"] = a * np.sum(S0 * want["dh0"] / a)
+    got = oracle_mod.gdn_bwd(q[None, None], k[None, None], v[None, None], np.array([[gg]]),
+                             np.array([[b]]), do[None, None], D[None, None], S0[None, None],
+                             scale=sc)
+    for name, x in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], got):
+        np.testing.assert_allclose(np.asarray(x).reshape(np.shape(want[name])), want[name],
+                                   rtol=1e-12, atol=1e-12, err_msg=name)
+
+
+def test_gdn_bwd_beta_zero(oracle_mod):
+    """With beta = 0 nothing is written: S_t = exp(g_t) S_{t-1}, so v and k get no gradient
+    at all, and dq_t = s exp(G_t) h0^T do_t with G_t the cumulative log decay."""
+    rng = np.random.default_rng(74)
+    q, k, v, g, _, h0 = _rand_case(rng, 9, 1, 1, 4, 3)
+    beta = np.zeros_like(g)
+    do = rng.standard_normal(v.shape)
+    dq, dk, dv, dg, dbeta, dh0 = oracle_mod.gdn_bwd(q, k, v, g, beta, do, None, h0, scale=0.9)
+    assert not dv.any() and not dk.any()
+    G = np.cumsum(g[:, 0])
+    want = 0.9 * np.exp(G)[:, None] * (do[:, 0] @ h0[0, 0])
+    np.testing.assert_allclose(dq[:, 0], want, rtol=1e-12, atol=1e-14)
+
+
 # ----------------------------------------------------- regression fixture
 
 def test_oracle_regression_fixture(oracle_mod):
