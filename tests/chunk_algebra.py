@@ -13,6 +13,11 @@ inclusive cumulative sum of g inside the chunk and b = exp(gamma):
   S1  = b_last S0 + U'^T diag(exp(gamma_last - gamma)) K
 and, split by linearity in S0, S1 = S0 Mc + U^T D K with
   Mc  = b_last I - W^T D K.
+
+chunked_head_bwd takes the same chunk form backward (reverse mode through each
+of the steps above, chunk by chunk from the last).  The state gradient runs as
+the transposed chain dS0 = dS1 Mc^T + (terms local to the chunk), which is what
+a backward scan kernel follows.
 """
 import numpy as np
 
@@ -66,3 +71,88 @@ def chunk_transition(k, g, beta, C):
         Mc = np.exp(gam[-1]) * np.eye(K) - W.T @ (d[:, None] * Kc)
         M = M @ Mc
     return M
+
+
+def chunked_head_bwd(q, k, v, g, beta, S0, scale, C, do, dST):
+    """Gradients (dq, dk, dv, dg, dbeta, dS0) of L = <do, o> + <dST, S_T> for chunked_head.
+
+    The chunk start states come from a forward pass; then, from the last chunk to the
+    first, each step of the chunk form above is taken back in reverse order:
+      S1 = b_last S0 + U'^T D K        O = scale (diag(b) Q S0^T + P U'),  P = (Q K^T) * Gamma
+      U' = U - W S0^T                  W = T diag(b) K,  U = T V,  T = (I + A)^-1 diag(beta)
+      A = strictly-lower(diag(beta) (K K^T) * Gamma)
+    and the gradients of gamma, b = exp(gamma), d = exp(gamma_last - gamma) and Gamma go
+    to g through the cumulative sum (dg_i = sum over j >= i of dgamma_j).
+    """
+    T, K = k.shape
+    starts = []
+    S = np.array(S0, dtype=np.float64, copy=True)
+    for c0 in range(0, T, C):
+        starts.append(S.copy())
+        sl = slice(c0, min(c0 + C, T))
+        S = chunked_head(q[sl], k[sl], v[sl], g[sl], beta[sl], S, scale, C)[1]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dg, dbeta = np.zeros(T), np.zeros(T)
+    dS = np.array(dST, dtype=np.float64, copy=True)
+    for ci in reversed(range(len(starts))):
+        sl = slice(ci * C, min(ci * C + C, T))
+        S = starts[ci]
+        Kc, Qc, Vc, gc, bc = k[sl], q[sl], v[sl], g[sl], beta[sl]
+        n = Kc.shape[0]
+        gam = np.cumsum(gc)
+        b = np.exp(gam)
+        d = np.exp(gam[-1] - gam)
+        G = _gamma_matrix(gam)
+        KK = Kc @ Kc.T
+        A = np.tril(bc[:, None] * KK * G, -1)
+        Z = np.linalg.inv(np.eye(n) + A)
+        Tm = Z * bc[None, :]
+        Kb = b[:, None] * Kc
+        W = Tm @ Kb
+        U = Tm @ Vc
+        Up = U - W @ S.T
+        QK = Qc @ Kc.T
+        P = QK * G
+        Ot = scale * do[sl]
+        db = np.zeros(n)
+        # S1 = b_last S0 + U'^T D K
+        dS0 = b[-1] * dS
+        db[-1] += np.sum(S * dS)
+        dUp = (d[:, None] * Kc) @ dS.T
+        dK = (d[:, None] * Up) @ dS
+        dd = np.einsum("iv,vk,ik->i", Up, dS, Kc)
+        # O = scale (diag(b) Q S0^T + P U')
+        dQ = (b[:, None] * Ot) @ S
+        dS0 += Ot.T @ (b[:, None] * Qc)
+        db += np.einsum("iv,vk,ik->i", Ot, S, Qc)
+        dP = Ot @ Up.T
+        dUp += P.T @ Ot
+        dQ += (dP * G) @ Kc
+        dK += (dP * G).T @ Qc
+        dG = dP * QK
+        # U' = U - W S0^T
+        dW = -dUp @ S
+        dS0 -= dUp.T @ W
+        # W = T diag(b) K, U = T V
+        dT = dW @ Kb.T + dUp @ Vc.T
+        dKb = Tm.T @ dW
+        dK += b[:, None] * dKb
+        db += np.sum(Kc * dKb, axis=1)
+        dV = Tm.T @ dUp
+        # T = Z diag(beta), Z = (I + A)^-1
+        dbt = np.sum(dT * Z, axis=0)
+        dA = np.tril(-Z.T @ (dT * bc[None, :]) @ Z.T, -1)
+        # A = strictly-lower(diag(beta) (K K^T) * Gamma)
+        dbt += np.sum(dA * KK * G, axis=1)
+        dKK = bc[:, None] * dA * G
+        dG += bc[:, None] * dA * KK
+        dK += (dKK + dKK.T) @ Kc
+        # gamma through Gamma, b and d, then g through the cumulative sum
+        dGG = np.tril(dG * G)
+        dgam = dGG.sum(axis=1) - dGG.sum(axis=0) + db * b - dd * d
+        dgam[-1] += np.sum(dd * d)
+        dq[sl], dk[sl], dv[sl] = dQ, dK, dV
+        dg[sl] = np.cumsum(dgam[::-1])[::-1]
+        dbeta[sl] = dbt
+        dS = dS0
+    return dq, dk, dv, dg, dbeta, dS

@@ -368,6 +368,44 @@ def test_chunk_algebra_equals_token_loop(oracle_mod, C, mild):
     np.testing.assert_allclose(Sc, hT[0, 0], rtol=1e-10, atol=1e-12)
 
 
+@pytest.mark.parametrize("C", [1, 16, 64])
+@pytest.mark.parametrize("mild", [False, True])
+def test_chunk_algebra_backward_equals_token_loop(oracle_mod, C, mild):
+    """The chunk form's backward (the blueprint of a backward kernel pair) against the
+    token-by-token backward, which the finite-difference pins hold to the forward."""
+    rng = np.random.default_rng(30 + C)
+    T, K, V = 150, 16, 12
+    q, k, v, g, beta, h0 = _rand_case(rng, T, 1, 1, K, V, mild=mild)
+    if not mild:
+        g = g * 3.0
+    do = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape)
+    ref = oracle_mod.gdn_bwd(q, k, v, g, beta, do, dhT, h0, scale=0.25)
+    got = chunk_algebra.chunked_head_bwd(q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], h0[0, 0],
+                                         0.25, C, do[:, 0], dhT[0, 0])
+    for name, r, x in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], ref, got):
+        r = np.asarray(r).reshape(np.shape(x))
+        np.testing.assert_allclose(x, r, rtol=0, atol=1e-11 * np.abs(r).max(), err_msg=name)
+
+
+def test_chunk_backward_state_chain_is_transposed_transition(oracle_mod):
+    """Over one chunk, dS0 depends on dS1 only through dS1 Mc^T (Mc the chunk's transition),
+    so the state gradient of a backward scan runs the forward chain transposed."""
+    rng = np.random.default_rng(31)
+    T, K, V = 40, 8, 6
+    q, k, v, g, beta, h0 = _rand_case(rng, T, 1, 1, K, V, mild=True)
+    do = rng.standard_normal(v.shape)
+    X = rng.standard_normal((V, K))
+    args = (q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], h0[0, 0], 0.5, 64, do[:, 0])
+    with_x = chunk_algebra.chunked_head_bwd(*args, X)[5]
+    without = chunk_algebra.chunked_head_bwd(*args, np.zeros((V, K)))[5]
+    Mc = chunk_algebra.chunk_transition(k[:, 0], g[:, 0], beta[:, 0], 64)
+    np.testing.assert_allclose(with_x - without, X @ Mc.T, rtol=1e-11, atol=1e-12)
+    # and the token-by-token backward agrees on dh0
+    ref = oracle_mod.gdn_bwd(q, k, v, g, beta, do, X[None, None], h0, scale=0.5)[5]
+    np.testing.assert_allclose(with_x, ref[0, 0], rtol=1e-11, atol=1e-12)
+
+
 # ---------------------------------------------- segment summary and chain
 
 def test_segment_summary_is_the_product(oracle_mod):
