@@ -64,6 +64,9 @@ _SIGS = {
     "gdn_decode_step": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                          _I32, _F32, _U32, _P, _P], ctypes.c_int),
     "gdn_cu_seqlens_from_position_ids": ([_P, _I64, _P, _P, _P], ctypes.c_int),
+    "gdn_chunk_bwd_workspace_bytes": ([ctypes.POINTER(GdnShape)], _SZ),
+    "gdn_chunk_bwd": ([_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(GdnShape), _F32, _U32, _P, _P, _P, _P, _P,
+                       _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
 }
 
 
@@ -326,6 +329,46 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm
                                 _ptr(h_T), ws.ptr(), ws.nbytes, _stream(v, stream)),
            "gdn_chunk_fwd")
     return o, h_T
+
+
+def gdn_chunk_bwd_workspace_bytes(shape: GdnShape) -> int:
+    return int(load().gdn_chunk_bwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, d_o, dh_T=None, h0=None, cu_seqlens=None, scale=None, l2norm_qk=True,
+                  B=None, want_dh0=True, workspace=None, stream=None):
+    """Gradients of <d_o, o> + <dh_T, h_T> for gdn_chunk_fwd's forward with the same inputs.
+
+    d_o [n_tok, Hv, V] and dh_T [n_seqs, Hv, V, K] (or None) are fp32.  Returns
+    (dq, dk, dv, dg, dbeta, dh0), all fp32; dh0 is None when want_dh0 is False.
+    """
+    _need_cuda(q, k, v, g, beta, d_o, dh_T, h0, cu_seqlens)
+    for n, t in (("g", g), ("beta", beta), ("d_o", d_o), ("dh_T", dh_T), ("h0", h0)):
+        _contig(n, t)
+        assert t is None or t.dtype == torch.float32, f"{n} must be fp32"
+    assert q.dtype == k.dtype == v.dtype
+    sh = make_shape(q, k, v, cu_seqlens, B)
+    n_tok = k.shape[0]
+    if scale is None:
+        scale = sh.K ** -0.5
+    dev = v.device
+    dq = torch.empty((n_tok, sh.Hqk, sh.K), device=dev, dtype=torch.float32)
+    dk = torch.empty_like(dq)
+    dv = torch.empty((n_tok, sh.Hv, sh.V), device=dev, dtype=torch.float32)
+    dg = torch.empty((n_tok, sh.Hv), device=dev, dtype=torch.float32)
+    dbeta = torch.empty_like(dg)
+    dh0 = torch.empty((sh.n_seqs, sh.Hv, sh.V, sh.K), device=dev, dtype=torch.float32) if want_dh0 else None
+    nbytes = gdn_chunk_bwd_workspace_bytes(sh)
+    if nbytes == 0:
+        raise GdnError("gdn_chunk_bwd: shape not supported (K 32/64/128, V a multiple of 16 up to 256)")
+    ws = workspace or _workspace_for(nbytes, dev)
+    flags = GDN_FLAG_QK_L2NORM if l2norm_qk else 0
+    _check(load().gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+                                ctypes.byref(sh), float(scale), flags, _ptr(d_o), _ptr(dh_T), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), ws.ptr(), ws.nbytes,
+                                _stream(v, stream)),
+           "gdn_chunk_bwd")
+    return dq, dk, dv, dg, dbeta, dh0
 
 
 def gdn_chunk_fwd_noalloc(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm_qk=True,

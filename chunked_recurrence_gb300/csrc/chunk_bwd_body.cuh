@@ -1,0 +1,416 @@
+// chunk_bwd_body.cuh -- the block body of the fp32 backward of the chunked gated delta rule.
+//
+// Training runs backward through the layer ("[v1] support GDN Ulysses cp", Testing: loss
+// alignment over training steps; "feat: hybrid CP for Qwen3.5 MoE (DeltaNet + attention)",
+// Test plan: forward/backward passes).  This is the exact gradient of the chunk form
+//   gamma = inclusive cumsum of g in the chunk, b = exp(gamma), d = exp(gamma_last - gamma)
+//   A  = strictly-lower(diag(beta) (K K^T) * Gamma),  Gamma_ij = exp(gamma_i - gamma_j)
+//   Z  = (I + A)^-1,  T = Z diag(beta)
+//   U' = T (V - diag(b) K S^T)                  (= T V - W S^T with W = T diag(b) K)
+//   O  = scale (diag(b) Q S^T + P U'),  P = (Q K^T) * Gamma, causal incl. the diagonal
+//   S1 = b_last S + U'^T diag(d) K
+// for upstream gradients dO and dS1, taken back step by step (reverse mode):
+//   dU' = diag(d) K dS1^T + P^T Ot   (Ot = scale dO),  dP = Ot U'^T
+//   dV  = T^T dU',  dT = dU' (V - diag(b) K S^T)^T,   dA = -Z^T (dT diag(beta)) Z^T
+//   dS  = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K
+//   dq  = diag(b) Ot S + (dP * Gamma) K
+//   dk  = diag(d) U' dS1 + (dP * Gamma)^T Q - diag(b) dV S + (dKK + dKK^T) K,
+//         dKK = diag(beta) dA * Gamma
+//   dbeta = colsum(dT * Z) + rowsum(dA * KK * Gamma)
+//   dgamma from Gamma (row sums minus column sums of dGamma * Gamma), b and d; dg is the
+//   reverse cumulative sum of dgamma.
+// Each row of the state evolves on its own given k, g, beta and its column of v, and so
+// does each row of dS.  So a block owns BV rows of one v-head's state: it recomputes its
+// rows' chunk-start states in a forward sweep, then walks the chunks backward carrying its
+// rows of dS.  dv and dh0 of its rows are complete in the block; dq, dk, dg and dbeta are
+// sums over the blocks of a head (and over the v-heads of a q/k head) and are added
+// atomically.
+//
+// The body is written against an executor X with three operations: x.par(n, f) runs f(i)
+// for i in [0, n), the items independent of each other; x.sync() is a block barrier;
+// x.add(p, v) adds v to *p atomically.  The CUDA kernel runs items on threads with
+// __syncthreads(); a host harness runs the same code with plain loops.
+#pragma once
+
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define GDN_BWD_FN __device__ __forceinline__
+#define GDN_BWD_HD __host__ __device__ inline
+#else
+#define GDN_BWD_FN inline
+#define GDN_BWD_HD inline
+#endif
+
+namespace gdn_bwd {
+
+constexpr int C = 64;   // tokens per chunk
+constexpr int BV = 16;  // state rows per block
+constexpr int CP = C + 1, VP = BV + 1;
+constexpr float kEps = 1e-6f;  // q/k L2 norm: x / sqrt(sum x^2 + eps)
+
+struct Params {
+  const void *q, *k, *v;  // q, k [n_tok][Hqk][K] (token strides qs, ks), v [n_tok][Hv][V] (vs)
+  const float *g, *beta;  // [n_tok][Hv]
+  const float *h0;        // [n_seq][Hv][V][K] or null
+  const float *dout;      // [n_tok][Hv][V]
+  const float *dhT;       // [n_seq][Hv][V][K] or null
+  const int32_t *cu;      // sequence bounds, or null: rows of row_T tokens
+  int64_t row_T, n_tok;
+  int Hqk, Hv, K, V;
+  int64_t qs, ks, vs;
+  float scale;
+  int l2norm;
+  float *states;    // [slot][Hv][V][K]: chunk-start states (chunk c of sequence s: slot s + start/C + c)
+  float *dqn, *dkn; // [n_tok][Hqk][K]: gradients of the unit-norm (or raw) q and k, accumulated
+  float *dv;        // [n_tok][Hv][V]
+  float *dg, *dbeta;  // [n_tok][Hv], accumulated
+  float *dh0;       // [n_seq][Hv][V][K] or null
+  int32_t *status;  // set to GDN_ERR_BOUNDS on a bad sequence range
+};
+
+// shared memory of one block, in floats
+GDN_BWD_HD size_t smem_floats(int K) {
+  const size_t KP = (size_t)K + 1;
+  return 2 * C * KP + 2 * BV * KP + 7 * (size_t)C * VP + 6 * (size_t)C * CP + 8 * C;
+}
+
+// ld(ptr, i): element i of a q / k / v array as float
+template <class X, class LD>
+GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, int s) {
+  const int K = p.K, KP = K + 1, V = p.V, Hv = p.Hv;
+  float *Ks = sm;              // [C][KP]  k of the chunk (unit-norm when l2norm)
+  float *Qs = Ks + C * KP;     // [C][KP]  q
+  float *Ss = Qs + C * KP;     // [BV][KP] this block's rows of the chunk-start state
+  float *dSs = Ss + BV * KP;   // [BV][KP] their gradient, carried from the chunk's end
+  float *Vs = dSs + BV * KP;   // [C][VP]  v columns of the block's rows
+  float *Os = Vs + C * VP;     // [C][VP]  scale * dO
+  float *Us = Os + C * VP;     // [C][VP]  U'
+  float *dUs = Us + C * VP;    // [C][VP]  K dS1^T, then dU'
+  float *dVs = dUs + C * VP;   // [C][VP]  dV
+  float *KSs = dVs + C * VP;   // [C][VP]  K S^T
+  float *QSs = KSs + C * VP;   // [C][VP]  Q S^T
+  float *Zm = QSs + C * VP;    // [C][CP]  A, then Z = (I + A)^-1 (unit lower)
+  float *QKm = Zm + C * CP;    // [C][CP]  Q K^T (lower incl. diagonal)
+  float *KKm = QKm + C * CP;   // [C][CP]  K K^T (strictly lower)
+  float *dPm = KKm + C * CP;   // [C][CP]  dP (lower incl. diagonal)
+  float *dTm = dPm + C * CP;   // [C][CP]  dT, then dA, then dKK
+  float *Ym = dTm + C * CP;    // [C][CP]  (dT diag(beta)) Z^T
+  float *gam = Ym + C * CP;    // [C] gamma
+  float *bet = gam + C;        // [C] beta
+  float *bex = bet + C;        // [C] exp(gamma)
+  float *dec = bex + C;        // [C] exp(gamma_last - gamma)
+  float *db = dec + C;         // [C] dL/db
+  float *dd = db + C;          // [C] dL/dd
+  float *dbt = dd + C;         // [C] dL/dbeta
+  float *dgm = dbt + C;        // [C] scratch of the inversion, then dL/dgamma
+
+  const int qh = h / (Hv / p.Hqk), row0 = tile * BV;
+  int64_t start, end;
+  if (p.cu) {
+    start = p.cu[s];
+    end = p.cu[s + 1];
+  } else {
+    start = (int64_t)s * p.row_T;
+    end = start + p.row_T;
+  }
+  if (start < 0 || end < start || end > p.n_tok) {
+    x.fail(p.status);
+    return;
+  }
+  const int64_t slot0 = (int64_t)s + start / C;
+  const int n_chunks = (int)((end - start + C - 1) / C);
+  const size_t VK = (size_t)V * K;
+  auto G = [&](int i, int j) { return expf(gam[i] - gam[j]); };  // j <= i
+
+  // ---- the chunk's inputs and its state-independent matrices (with_q: Q, dO, Q K^T too)
+  auto prep = [&](int64_t t0, int n, bool with_q) {
+    x.par(C * K, [&](int idx) {
+      const int r = idx / K, c = idx % K;
+      const bool in = r < n;
+      Ks[r * KP + c] = in ? ld(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c) : 0.f;
+      if (with_q) Qs[r * KP + c] = in ? ld(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c) : 0.f;
+    });
+    x.par(C * BV, [&](int idx) {
+      const int r = idx / BV, j = idx % BV;
+      const bool in = r < n;
+      Vs[r * VP + j] = in ? ld(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j) : 0.f;
+      if (with_q) Os[r * VP + j] = in ? p.scale * p.dout[((t0 + r) * Hv + h) * V + row0 + j] : 0.f;
+    });
+    x.par(C, [&](int i) {
+      const bool in = i < n;
+      gam[i] = in ? p.g[(t0 + i) * Hv + h] : 0.f;
+      bet[i] = in ? p.beta[(t0 + i) * Hv + h] : 0.f;
+    });
+    x.sync();
+    if (p.l2norm) {
+      x.par(with_q ? 2 * C : C, [&](int r) {
+        float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
+        float ss = 0.f;
+        for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
+        const float inv = 1.f / sqrtf(ss + kEps);
+        for (int c = 0; c < K; ++c) row[c] *= inv;
+      });
+    }
+    if (x.leader())
+      for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
+    x.sync();
+    x.par(C, [&](int i) {
+      bex[i] = expf(gam[i]);
+      dec[i] = expf(gam[C - 1] - gam[i]);
+    });
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      float kk = 0.f, qk = 0.f;
+      if (j < i)
+        for (int c = 0; c < K; ++c) kk = fmaf(Ks[i * KP + c], Ks[j * KP + c], kk);
+      if (with_q && j <= i)
+        for (int c = 0; c < K; ++c) qk = fmaf(Qs[i * KP + c], Ks[j * KP + c], qk);
+      KKm[i * CP + j] = kk;
+      Zm[i * CP + j] = j < i ? bet[i] * expf(gam[i] - gam[j]) * kk : 0.f;
+      if (with_q) QKm[i * CP + j] = qk;
+    });
+    x.sync();
+    // Z = (I + A)^-1 by forward substitution, a row at a time: row i of Z (left of the
+    // diagonal) is -(A_ij + sum_{j<m<i} A_im Z_mj); rows above i already hold Z.
+    for (int i = 1; i < C; ++i) {
+      x.par(i, [&](int j) {
+        float acc = Zm[i * CP + j];
+        for (int m = j + 1; m < i; ++m) acc = fmaf(Zm[i * CP + m], Zm[m * CP + j], acc);
+        dgm[j] = acc;
+      });
+      x.sync();
+      x.par(i, [&](int j) { Zm[i * CP + j] = -dgm[j]; });
+      x.sync();
+    }
+    x.par(C, [&](int i) { Zm[i * CP + i] = 1.f; });
+    // K S^T (and Q S^T)
+    x.par(C * BV, [&](int idx) {
+      const int i = idx / BV, v = idx % BV;
+      float ks = 0.f, qs = 0.f;
+      for (int c = 0; c < K; ++c) ks = fmaf(Ks[i * KP + c], Ss[v * KP + c], ks);
+      KSs[i * VP + v] = ks;
+      if (with_q) {
+        for (int c = 0; c < K; ++c) qs = fmaf(Qs[i * KP + c], Ss[v * KP + c], qs);
+        QSs[i * VP + v] = qs;
+      }
+    });
+    x.sync();
+    // U' = Z diag(beta) (V - diag(b) K S^T)
+    x.par(C * BV, [&](int idx) {
+      const int i = idx / BV, v = idx % BV;
+      float acc = 0.f;
+      for (int j = 0; j <= i; ++j)
+        acc = fmaf(Zm[i * CP + j] * bet[j], Vs[j * VP + v] - bex[j] * KSs[j * VP + v], acc);
+      Us[i * VP + v] = acc;
+    });
+    x.sync();
+  };
+
+  // ---- forward sweep: the chunk-start state of every chunk, for this block's rows
+  x.par(BV * K, [&](int idx) {
+    const int r = idx / K, c = idx % K;
+    Ss[r * KP + c] = p.h0 ? p.h0[((size_t)s * Hv + h) * VK + (size_t)(row0 + r) * K + c] : 0.f;
+  });
+  x.sync();
+  for (int ci = 0; ci < n_chunks; ++ci) {
+    const int64_t t0 = start + (int64_t)ci * C;
+    const int n = (int)(end - t0 < C ? end - t0 : C);
+    float *dst = p.states + ((size_t)(slot0 + ci) * Hv + h) * VK + (size_t)row0 * K;
+    x.par(BV * K, [&](int idx) { dst[(idx / K) * (size_t)K + idx % K] = Ss[(idx / K) * KP + idx % K]; });
+    prep(t0, n, false);
+    // S1 = b_last S + U'^T diag(d) K
+    x.par(BV * K, [&](int idx) {
+      const int v = idx / K, c = idx % K;
+      float acc = 0.f;
+      for (int j = 0; j < C; ++j) acc = fmaf(Us[j * VP + v] * dec[j], Ks[j * KP + c], acc);
+      Ss[v * KP + c] = fmaf(bex[C - 1], Ss[v * KP + c], acc);
+    });
+    x.sync();
+  }
+
+  // ---- backward sweep
+  x.par(BV * K, [&](int idx) {
+    const int r = idx / K, c = idx % K;
+    dSs[r * KP + c] = p.dhT ? p.dhT[((size_t)s * Hv + h) * VK + (size_t)(row0 + r) * K + c] : 0.f;
+  });
+  for (int ci = n_chunks - 1; ci >= 0; --ci) {
+    const int64_t t0 = start + (int64_t)ci * C;
+    const int n = (int)(end - t0 < C ? end - t0 : C);
+    const float *src = p.states + ((size_t)(slot0 + ci) * Hv + h) * VK + (size_t)row0 * K;
+    x.par(BV * K, [&](int idx) { Ss[(idx / K) * KP + idx % K] = src[(idx / K) * (size_t)K + idx % K]; });
+    x.sync();
+    prep(t0, n, true);
+    // K dS1^T; dP = Ot U'^T (lower incl. diagonal)
+    x.par(C * BV, [&](int idx) {
+      const int i = idx / BV, v = idx % BV;
+      float acc = 0.f;
+      for (int c = 0; c < K; ++c) acc = fmaf(Ks[i * KP + c], dSs[v * KP + c], acc);
+      dUs[i * VP + v] = acc;
+    });
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      float acc = 0.f;
+      if (j <= i)
+        for (int v = 0; v < BV; ++v) acc = fmaf(Os[i * VP + v], Us[j * VP + v], acc);
+      dPm[i * CP + j] = acc;
+    });
+    x.sync();
+    // dd_i = U'_i . (K dS1^T)_i;  dU' = diag(d) K dS1^T + P^T Ot
+    x.par(C, [&](int i) {
+      float acc = 0.f;
+      for (int v = 0; v < BV; ++v) acc = fmaf(Us[i * VP + v], dUs[i * VP + v], acc);
+      dd[i] = acc;
+    });
+    x.sync();
+    x.par(C * BV, [&](int idx) {
+      const int i = idx / BV, v = idx % BV;
+      float acc = dec[i] * dUs[i * VP + v];
+      for (int j = i; j < C; ++j) acc = fmaf(QKm[j * CP + i] * G(j, i), Os[j * VP + v], acc);
+      dUs[i * VP + v] = acc;
+    });
+    x.sync();
+    // dV = T^T dU' (complete for these rows); dT = dU' (V - diag(b) K S^T)^T (lower)
+    x.par(C * BV, [&](int idx) {
+      const int i = idx / BV, v = idx % BV;
+      float acc = 0.f;
+      for (int j = i; j < C; ++j) acc = fmaf(Zm[j * CP + i], dUs[j * VP + v], acc);
+      acc *= bet[i];
+      dVs[i * VP + v] = acc;
+      if (i < n) p.dv[((t0 + i) * Hv + h) * V + row0 + v] = acc;
+    });
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      float acc = 0.f;
+      if (j <= i)
+        for (int v = 0; v < BV; ++v) acc = fmaf(dUs[i * VP + v], Vs[j * VP + v] - bex[j] * KSs[j * VP + v], acc);
+      dTm[i * CP + j] = acc;
+    });
+    x.sync();
+    // dbeta from T = Z diag(beta); db; Y = (dT diag(beta)) Z^T
+    x.par(C, [&](int j) {
+      float acc = 0.f;
+      for (int i = j; i < C; ++i) acc = fmaf(dTm[i * CP + j], Zm[i * CP + j], acc);
+      dbt[j] = acc;
+      float b = 0.f;
+      for (int v = 0; v < BV; ++v)
+        b += Os[j * VP + v] * QSs[j * VP + v] - dVs[j * VP + v] * KSs[j * VP + v];
+      if (j == C - 1)
+        for (int idx = 0; idx < BV * K; ++idx) b = fmaf(Ss[(idx / K) * KP + idx % K], dSs[(idx / K) * KP + idx % K], b);
+      db[j] = b;
+    });
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      const int mm = i < j ? i : j;
+      float acc = 0.f;
+      for (int m = 0; m <= mm; ++m) acc = fmaf(dTm[i * CP + m] * bet[m], Zm[j * CP + m], acc);
+      Ym[i * CP + j] = acc;
+    });
+    x.sync();
+    // dA = -Z^T Y, strictly lower (into dT's place)
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      float acc = 0.f;
+      if (j < i)
+        for (int m = i; m < C; ++m) acc = fmaf(Zm[m * CP + i], Ym[m * CP + j], acc);
+      dTm[i * CP + j] = -acc;
+    });
+    x.sync();
+    // dgamma (through Gamma in A and P, b and d) and the rest of dbeta
+    x.par(C, [&](int i) {
+      float rA = 0.f, cA = 0.f, rP = 0.f, cP = 0.f, bA = 0.f;
+      for (int j = 0; j < i; ++j) {
+        const float t = dTm[i * CP + j] * KKm[i * CP + j] * G(i, j);
+        bA += t;
+        rA = fmaf(bet[i], t, rA);
+      }
+      for (int m = i + 1; m < C; ++m) cA = fmaf(bet[m], dTm[m * CP + i] * KKm[m * CP + i] * G(m, i), cA);
+      for (int j = 0; j <= i; ++j) rP = fmaf(dPm[i * CP + j], QKm[i * CP + j] * G(i, j), rP);
+      for (int m = i; m < C; ++m) cP = fmaf(dPm[m * CP + i], QKm[m * CP + i] * G(m, i), cP);
+      dbt[i] += bA;
+      dgm[i] = rP - cP + rA - cA + db[i] * bex[i] - dd[i] * dec[i];
+    });
+    x.sync();
+    if (x.leader()) {
+      float sdd = 0.f;
+      for (int i = 0; i < C; ++i) sdd = fmaf(dd[i], dec[i], sdd);
+      dgm[C - 1] += sdd;
+      for (int i = C - 2; i >= 0; --i) dgm[i] += dgm[i + 1];  // dg = reverse cumsum of dgamma
+    }
+    x.sync();
+    x.par(C, [&](int i) {
+      if (i < n) {
+        x.add(p.dg + (t0 + i) * Hv + h, dgm[i]);
+        x.add(p.dbeta + (t0 + i) * Hv + h, dbt[i]);
+      }
+    });
+    // dKK = diag(beta) dA * Gamma (strictly lower)
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      dTm[i * CP + j] = j < i ? bet[i] * dTm[i * CP + j] * G(i, j) : 0.f;
+    });
+    x.sync();
+    // dq and dk of the chunk's tokens
+    x.par(C * K, [&](int idx) {
+      const int i = idx / K, c = idx % K;
+      if (i >= n) return;
+      float sq = 0.f, sk = 0.f, sv = 0.f;
+      for (int v = 0; v < BV; ++v) {
+        sq = fmaf(Os[i * VP + v], Ss[v * KP + c], sq);
+        sk = fmaf(Us[i * VP + v], dSs[v * KP + c], sk);
+        sv = fmaf(dVs[i * VP + v], Ss[v * KP + c], sv);
+      }
+      float dq = bex[i] * sq, dk = dec[i] * sk - bex[i] * sv;
+      for (int j = 0; j <= i; ++j) dq = fmaf(dPm[i * CP + j] * G(i, j), Ks[j * KP + c], dq);
+      for (int j = i; j < C; ++j) dk = fmaf(dPm[j * CP + i] * G(j, i), Qs[j * KP + c], dk);
+      for (int j = 0; j < i; ++j) dk = fmaf(dTm[i * CP + j], Ks[j * KP + c], dk);
+      for (int j = i + 1; j < C; ++j) dk = fmaf(dTm[j * CP + i], Ks[j * KP + c], dk);
+      const size_t off = ((size_t)(t0 + i) * p.Hqk + qh) * K + c;
+      x.add(p.dqn + off, dq);
+      x.add(p.dkn + off, dk);
+    });
+    x.sync();
+    // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K
+    x.par(BV * K, [&](int idx) {
+      const int v = idx / K, c = idx % K;
+      float acc = bex[C - 1] * dSs[v * KP + c];
+      for (int i = 0; i < C; ++i)
+        acc = fmaf(bex[i], Os[i * VP + v] * Qs[i * KP + c] - dVs[i * VP + v] * Ks[i * KP + c], acc);
+      dSs[v * KP + c] = acc;
+    });
+    x.sync();
+  }
+  if (p.dh0)
+    x.par(BV * K, [&](int idx) {
+      const int r = idx / K, c = idx % K;
+      p.dh0[((size_t)s * Hv + h) * VK + (size_t)(row0 + r) * K + c] = dSs[r * KP + c];
+    });
+}
+
+// Row r of q or k (token t = r / Hqk, head r % Hqk): the gradient of the unit-norm row taken
+// back to the raw row, dx = dxh / n - x (x . dxh) / n^3 with n = sqrt(|x|^2 + eps), or
+// copied when there is no norm.
+template <class LD>
+GDN_BWD_FN void l2_back_row(const void *raw, int64_t stride, int Hqk, int K, int l2norm, LD ld, const float *dn,
+                            float *out, int64_t r) {
+  const int64_t t = r / Hqk, hh = r % Hqk;
+  const int64_t base = t * stride + hh * K;
+  const float *dr = dn + r * K;
+  float *o = out + r * K;
+  if (!l2norm) {
+    for (int c = 0; c < K; ++c) o[c] = dr[c];
+    return;
+  }
+  float ss = 0.f, xd = 0.f;
+  for (int c = 0; c < K; ++c) {
+    const float xv = ld(raw, base + c);
+    ss = fmaf(xv, xv, ss);
+    xd = fmaf(xv, dr[c], xd);
+  }
+  const float nn = sqrtf(ss + kEps), inv = 1.f / nn, inv3 = inv * inv * inv;
+  for (int c = 0; c < K; ++c) o[c] = dr[c] * inv - ld(raw, base + c) * xd * inv3;
+}
+
+}  // namespace gdn_bwd

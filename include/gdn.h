@@ -189,6 +189,31 @@ gdn_status gdn_segment_summary(const void *k, const void *v, const float *g, con
                                uint32_t flags, float *M, float *S_local, void *workspace,
                                size_t workspace_bytes, void *stream);
 
+/* Backward of gdn_chunk_fwd: the gradients that training takes through the layer
+ * ("[v1] support GDN Ulysses cp", Testing: loss alignment over training steps;
+ * "feat: hybrid CP for Qwen3.5 MoE (DeltaNet + attention)", Test plan:
+ * forward/backward passes).  For upstream gradients d_o of o and dh_T of h_T it
+ * writes the exact gradients of L = <d_o, o> + <dh_T, h_T> for the forward of
+ * gdn_chunk_fwd with the same q, k, v, g, beta, h0, cu_seqlens, shape, scale and
+ * flags (GDN_FLAG_QK_L2NORM only): dq, dk [tokens, Hqk, K] (summed over the v-heads
+ * that share a q/k head, and taken back through the L2 norm when it is on), dv
+ * [tokens, Hv, V], dg, dbeta [tokens, Hv], dh0 [n_seqs, Hv, V, K] (may be NULL).
+ * d_o [tokens, Hv, V] and dh_T [n_seqs, Hv, V, K] (NULL: no loss on h_T) are fp32,
+ * as are all outputs; q, k, v are of shape->dtype with the strides of gdn_shape.
+ * K is 32, 64 or 128; V a multiple of 16 up to 256 (else GDN_ERR_UNSUPPORTED).
+ * fp32 CUDA-core kernel: one block per (16 state rows, v-head, sequence) recomputes
+ * its rows' chunk-start states, then walks the chunks backward.  The workspace
+ * (gdn_chunk_bwd_workspace_bytes, 256-byte aligned) holds the status word, the
+ * chunk-start states and the q/k gradient accumulators; a bad cu_seqlens range
+ * sets GDN_ERR_BOUNDS in the status word (gdn_workspace_status).  dq, dk, dg and
+ * dbeta are summed with atomic adds, so their last bits depend on the order. */
+size_t gdn_chunk_bwd_workspace_bytes(const gdn_shape *shape);
+gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         const float *h0, const int32_t *cu_seqlens, const gdn_shape *shape, float scale,
+                         uint32_t flags, const float *d_o, const float *dh_T, float *dq, float *dk, float *dv,
+                         float *dg, float *dbeta, float *dh0, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
 /* One decode step of the layer core for B sequences, continuing from their states
  * ("Qwen3.5 cp - #1", Architecture: after the prefill, decode runs the standard
  * recurrent path from the final ssm_state).  For each sequence b, with the new token's

@@ -1,0 +1,61 @@
+// Host run of the backward's block body (chunked_recurrence_gb300/csrc/chunk_bwd_body.cuh),
+// for the CPU tests: the same code the CUDA kernel runs, with every block and every
+// parallel item executed in order by one thread.  fp32 inputs only.
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "chunk_bwd_body.cuh"
+
+namespace {
+
+struct HostExec {
+  template <class F>
+  void par(int n, F &&f) {
+    for (int i = 0; i < n; ++i) f(i);
+  }
+  void sync() {}
+  bool leader() const { return true; }
+  void add(float *p, float v) { *p += v; }
+  void fail(int32_t *status) {
+    if (status && *status == 0) *status = 6;  // GDN_ERR_BOUNDS
+  }
+};
+
+struct HostLoad {
+  float operator()(const void *p, int64_t i) const { return reinterpret_cast<const float *>(p)[i]; }
+};
+
+}  // namespace
+
+extern "C" int emu_chunk_bwd(const float *q, const float *k, const float *v, const float *g, const float *beta,
+                             const float *h0, const int32_t *cu, int n_seqs, int64_t row_T, int64_t n_tok, int Hqk,
+                             int Hv, int K, int V, float scale, int l2norm, const float *dout, const float *dhT,
+                             float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dh0) {
+  const int64_t n_slots = n_seqs + (n_tok + gdn_bwd::C - 1) / gdn_bwd::C;
+  std::vector<float> states((size_t)n_slots * Hv * V * K), dqn((size_t)n_tok * Hqk * K), dkn(dqn.size());
+  std::vector<float> sm(gdn_bwd::smem_floats(K));
+  if (n_tok > 0) {
+    std::memset(dv, 0, sizeof(float) * (size_t)n_tok * Hv * V);
+    std::memset(dg, 0, sizeof(float) * (size_t)n_tok * Hv);
+    std::memset(dbeta, 0, sizeof(float) * (size_t)n_tok * Hv);
+  }
+  int32_t status = 0;
+  gdn_bwd::Params p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0; p.dout = dout; p.dhT = dhT;
+  p.cu = cu; p.row_T = row_T; p.n_tok = n_tok;
+  p.Hqk = Hqk; p.Hv = Hv; p.K = K; p.V = V;
+  p.qs = (int64_t)Hqk * K; p.ks = (int64_t)Hqk * K; p.vs = (int64_t)Hv * V;
+  p.scale = scale; p.l2norm = l2norm;
+  p.states = states.data(); p.dqn = dqn.data(); p.dkn = dkn.data();
+  p.dv = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0; p.status = &status;
+  HostExec x;
+  for (int s = 0; s < n_seqs; ++s)
+    for (int h = 0; h < Hv; ++h)
+      for (int tile = 0; tile < V / gdn_bwd::BV; ++tile) gdn_bwd::block(x, p, HostLoad{}, sm.data(), tile, h, s);
+  for (int64_t r = 0; r < n_tok * Hqk; ++r) {
+    gdn_bwd::l2_back_row(q, p.qs, Hqk, K, l2norm, HostLoad{}, dqn.data(), dq, r);
+    gdn_bwd::l2_back_row(k, p.ks, Hqk, K, l2norm, HostLoad{}, dkn.data(), dk, r);
+  }
+  return status;
+}

@@ -166,3 +166,32 @@ def test_product_package_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in src and "from oracle" not in src, fn
                 assert "gdn_oracle" not in src, fn
+
+
+def test_chunk_bwd_argument_errors_return_before_launch(lib):
+    """gdn_chunk_bwd's host checks: shape, flags, workspace, pointers; nothing is launched."""
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced
+    ws = P(0x20000)    # 256-byte aligned
+    sh = _shape()
+    need = lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(sh))
+    # states of (1 + 2) chunk slots x 4 heads x 128 x 128 fp32, two q/k accumulators of 128 x 2 x 128
+    assert need == 256 + 3 * 4 * 128 * 128 * 4 + 2 * 128 * 2 * 128 * 4
+    assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(K=96))) == 0
+    assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(V=40))) == 0
+    assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(V=48))) > 0
+
+    def call(q=fake, shape=sh, flags=1, cu=None, w=ws, nbytes=need, dq=fake):
+        return lib.gdn_chunk_bwd(q, fake, fake, fake, fake, None, cu, shape if shape is None else ctypes.byref(shape),
+                                 1.0, flags, fake, None, dq, fake, fake, fake, fake, None, w, nbytes, None)
+    assert call(shape=None) == 1
+    assert call(shape=_shape(K=256)) == 2
+    assert call(shape=_shape(Hv=3)) == 1
+    assert call(flags=2) == 1              # only the L2-norm flag
+    assert call(w=None) == 5
+    assert call(w=P(0x20004)) == 5
+    assert call(nbytes=need - 1) == 5
+    assert call(q=None) == 1
+    assert call(dq=None) == 1
+    assert call(shape=_shape(B=2, n_seqs=2), cu=fake) == 1
+    assert call(q=None, shape=_shape(T=0, n_seqs=0), cu=fake, nbytes=256) == 0  # no sequences: no-op
