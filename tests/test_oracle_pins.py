@@ -617,6 +617,21 @@ def test_gdn_bwd_beta_zero(oracle_mod):
     np.testing.assert_allclose(dq[:, 0], want, rtol=1e-12, atol=1e-14)
 
 
+def test_gdn_bwd_empty_sequence_and_threads(oracle_mod):
+    """An empty sequence maps h0 to h_T unchanged, so its dh0 is dh_T exactly; and the
+    gradients do not depend on how many threads share the (sequence, q/k head) jobs."""
+    rng = np.random.default_rng(75)
+    q, k, v, g, beta, h0 = _rand_case(rng, 30, 2, 4, 6, 5, n_seq=3)
+    do = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape)
+    cu = np.array([0, 0, 12, 30], dtype=np.int32)
+    a = oracle_mod.gdn_bwd(q, k, v, g, beta, do, dhT, h0, cu_seqlens=cu, scale=0.6, n_threads=1)
+    b = oracle_mod.gdn_bwd(q, k, v, g, beta, do, dhT, h0, cu_seqlens=cu, scale=0.6, n_threads=7)
+    np.testing.assert_array_equal(a[5][0], dhT[0])
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
 # ----------------------------------------------------- regression fixture
 
 def test_oracle_regression_fixture(oracle_mod):
