@@ -8,8 +8,6 @@
 // to put gdn_chunk_fwd's scratch (the status word and, on the tensor-core
 // path, the per-chunk T matrices).  This entry point keeps that scratch in a
 // file-scope device array of fixed size instead.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
@@ -23,23 +21,14 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch per device, looked up once per device
-// with that device current.  In host code the array's name is only a host-side
-// stand-in; the kernels must be given this address.
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mutex;
-
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in; the kernels must be given this
+// address.  It is looked up on every call (cudaGetSymbolAddress is cheap), so
+// a device reset or a new primary context never leaves a stale address behind.
 gdn_status scratch_for_current_device(void **out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+  *out = p;
   return GDN_OK;
 }
 

@@ -160,9 +160,9 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
  *    K = 128 path that is 256 + 8320 * Hv * (n_seqs + ceil(tokens/64)) bytes,
  *    e.g. 2048 tokens x 32 v-heads or 8192 tokens x 8 v-heads).  Shapes whose
  *    gdn_chunk_fwd_workspace_bytes also fits take the faster path.
- *  - The first call on a device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress), so it stays valid across device resets and new
+ *    contexts; make the first call on a device before any stream capture.
  *  - Every call on a device shares the one array and clears its status word
  *    first; calls that overlap on the GPU (different streams, no ordering)
  *    race on it and must not be issued.  Device-side status (bad sequence

@@ -137,3 +137,71 @@ def test_long_segments_full(crg):
         assert_close(h1[0, h].cpu(), rh[0, j], "bf16", f"single pass h_T head {h}")
         assert_close(o2[:, h].cpu(), ro[:, j], "bf16", f"two-pass o head {h}")
         assert_close(h2[h].cpu(), rh[0, j], "bf16", f"two-pass h_T head {h}")
+
+
+# ---------------------------------------------------------------- long state memory
+# With the paper's gates the mean decay is exp(-4.4) per token, so whole-tensor errors
+# cannot see a fault in how the state is carried from chunk to chunk.  These run the
+# full-length workloads again with mild gates (g ~ U(-0.05, 0), beta ~ U(0.2, 0.8)):
+# the state then carries over hundreds of tokens, across every chunk and segment start.
+
+def _select_heads(inp, g, beta, heads, r):
+    """q, k of the q/k heads that v-heads `heads` read, and v, g, beta of those v-heads,
+    as fp64 arrays with one q/k head per v-head (the oracle's Hqk = Hv case)."""
+    qk = torch.tensor([h // r for h in heads], device=DEV)
+    vh = torch.tensor(heads, device=DEV)
+    return (to64(inp["q"].index_select(1, qk)), to64(inp["k"].index_select(1, qk)),
+            to64(inp["v"].index_select(1, vh)), to64(g.index_select(1, vh)),
+            to64(beta.index_select(1, vh)))
+
+
+def _windows(starts, n_tok, width):
+    idx = [t for s in starts for t in range(int(s), min(int(s) + width, n_tok))]
+    return np.unique(np.array(idx, dtype=np.int64))
+
+
+@pytest.mark.parametrize("o_f32", [False, True])
+def test_qwen35_4b_layer_mild_gates_full(crg, o_f32):
+    """T = 8192, 16 q/k and 32 v heads: 128 chunks of carried state per head."""
+    wl = synth.WORKLOADS["qwen35_4b_layer"]
+    inp = synth.make_inputs(wl, device=DEV, with_front_end=False)
+    n = inp["n_tok"]
+    g, beta = synth.mild_gates(n, wl.Hv, wl.seed, device=DEV)
+    o, hT = crg.gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], g, beta, None, None, inp["scale"],
+                              True, B=1, o_f32=o_f32)
+    torch.cuda.synchronize()
+    heads = [0, 7, 18, 31]
+    ro, rh = oracle.gdn_fwd(*_select_heads(inp, g, beta, heads, wl.Hv // wl.Hqk), None, None,
+                            inp["scale"], True)
+    win = _windows(range(0, n, 64), n, 16)  # the first 16 tokens after every chunk start
+    for j, h in enumerate(heads):
+        og = o[:, h]
+        assert_close(og.cpu(), ro[:, j], "bf16", f"mild 4B layer o head {h}")
+        assert_close(hT[0, h].cpu(), rh[0, j], "bf16", f"mild 4B layer h_T head {h}")
+        assert_close(og.cpu()[win], ro[win, j], "bf16", f"mild 4B layer chunk-start windows head {h}")
+
+
+def test_long_segments_mild_gates_full(crg):
+    """T = 131072, 16 heads, 8 segments: the single pass carries the state over 2048
+    chunks, the two-pass over 256-chunk segments joined by the fp32 chain reduce."""
+    wl = synth.WORKLOADS["long_segments"]
+    inp = synth.make_inputs(wl, device=DEV, with_front_end=False)
+    n = inp["n_tok"]
+    g, beta = synth.mild_gates(n, wl.Hv, wl.seed, device=DEV)
+    bounds = inp["seg_bounds"]
+    o1, h1 = crg.gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], g, beta, None, None, inp["scale"],
+                               True, B=1)
+    o2, h2 = crg.segment_parallel_fwd(inp["q"], inp["k"], inp["v"], g, beta, bounds,
+                                      scale=inp["scale"])
+    torch.cuda.synchronize()
+    heads = [0, 5, 10, 15]
+    ro, rh = oracle.gdn_fwd(*_select_heads(inp, g, beta, heads, 1), None, None, inp["scale"], True)
+    seg_win = _windows(bounds.cpu().numpy()[:-1], n, 64)  # the first chunk of every segment
+    chunk_win = _windows(range(0, n, 64), n, 16)
+    for j, h in enumerate(heads):
+        for what, o, hT in (("single pass", o1[:, h], h1[0, h]), ("two-pass", o2[:, h], h2[h])):
+            oc = o.cpu()
+            assert_close(oc, ro[:, j], "bf16", f"mild {what} o head {h}")
+            assert_close(hT.cpu(), rh[0, j], "bf16", f"mild {what} h_T head {h}")
+            assert_close(oc[seg_win], ro[seg_win, j], "bf16", f"mild {what} segment-start windows head {h}")
+            assert_close(oc[chunk_win], ro[chunk_win, j], "bf16", f"mild {what} chunk-start windows head {h}")
