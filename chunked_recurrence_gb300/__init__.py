@@ -19,10 +19,13 @@ import torch
 from . import build as _build
 
 GDN_OK = 0
+GDN_ERR_TIMEOUT, GDN_ERR_BOUNDS = 4, 6  # device-side statuses read from a workspace
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_SIMT = 2
 GDN_FLAG_O_F32 = 4
+GDN_FLAG_SPLIT = 8
+GDN_FLAG_TEST_NO_WAIT = 16
 CHUNK = 64
 
 _lib = None
@@ -300,10 +303,22 @@ def gdn_chunk_fwd_min_workspace_bytes(shape: GdnShape) -> int:
     return int(load().gdn_chunk_fwd_min_workspace_bytes(ctypes.byref(shape)))
 
 
+def split_workspace_bytes(shape: GdnShape) -> int:
+    """Workspace of the two-kernel split path (GDN_FLAG_SPLIT): a status header and one
+    operand record of 25600 + 256 V bytes per chunk slot and v-head."""
+    n_tok = shape.T if shape.B == 1 else shape.B * shape.T
+    slots = shape.n_seqs + (n_tok + CHUNK - 1) // CHUNK
+    return 256 + slots * shape.Hv * (25600 + 256 * shape.V)
+
+
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm_qk=True,
                   B=None, simt=False, o=None, h_T=None, want_h_T=True, workspace=None,
-                  stream=None, o_f32=False):
-    """Chunked gated delta rule forward; returns (o [n_tok, Hv, V], h_T [n_seqs, Hv, V, K] or None)."""
+                  stream=None, o_f32=False, split=False, _test_no_wait=False):
+    """Chunked gated delta rule forward; returns (o [n_tok, Hv, V], h_T [n_seqs, Hv, V, K] or None).
+
+    bf16 with K = V = 128 runs the fused persistent kernel; split=True takes the two-kernel
+    split path instead.  _test_no_wait (tests only) makes every bounded wait of the fused
+    kernel give up at once, so the call ends with GDN_ERR_TIMEOUT in the workspace status."""
     _need_cuda(q, k, v, g, beta, h0, cu_seqlens)
     for n, t in (("g", g), ("beta", beta), ("h0", h0)):
         _contig(n, t)
@@ -314,7 +329,8 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm
     if scale is None:
         scale = sh.K ** -0.5
     flags = ((GDN_FLAG_QK_L2NORM if l2norm_qk else 0) | (GDN_FLAG_SIMT if simt else 0)
-             | (GDN_FLAG_O_F32 if o_f32 else 0))
+             | (GDN_FLAG_O_F32 if o_f32 else 0) | (GDN_FLAG_SPLIT if split else 0)
+             | (GDN_FLAG_TEST_NO_WAIT if _test_no_wait else 0))
     o_dtype = torch.float32 if o_f32 else v.dtype
     if o is None:
         o = torch.empty((n_tok, sh.Hv, sh.V), device=v.device, dtype=o_dtype)
@@ -323,7 +339,12 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm
         h_T = torch.empty((sh.n_seqs, sh.Hv, sh.V, sh.K), device=v.device, dtype=torch.float32)
     if h0 is not None:
         assert h0.dtype == torch.float32 and tuple(h0.shape) == (sh.n_seqs, sh.Hv, sh.V, sh.K)
-    ws = workspace or _workspace_for(gdn_chunk_fwd_workspace_bytes(sh), v.device)
+    if workspace is None:
+        nb = gdn_chunk_fwd_workspace_bytes(sh)
+        if split:
+            nb = max(nb, split_workspace_bytes(sh))
+        workspace = _workspace_for(nb, v.device)
+    ws = workspace
     _check(load().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                 _ptr(cu_seqlens), ctypes.byref(sh), float(scale), flags, _ptr(o),
                                 _ptr(h_T), ws.ptr(), ws.nbytes, _stream(v, stream)),

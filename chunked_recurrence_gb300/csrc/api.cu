@@ -1,4 +1,6 @@
 // api.cu -- argument checking and dispatch of gdn_chunk_fwd / gdn_segment_summary.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace gdn {
@@ -26,6 +28,12 @@ gdn_status summary_scan(const void *k, const void *v, const float *g, const floa
                         const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
                         float *M, float *S_local, void *workspace, size_t ws_bytes,
                         cudaStream_t st);
+bool chunk_fused_supported(const void *q, const void *k, const void *v, const gdn_shape &sh);
+size_t chunk_fused_workspace_bytes(const gdn_shape &sh);
+gdn_status chunk_fwd_fused(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const float *h0, const int32_t *cu,
+                           const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
+                           void *workspace, size_t ws_bytes, cudaStream_t st);
 gdn_status summary_tc(const void *k, const void *v, const float *g, const float *beta,
                       const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
                       float *M, float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st);
@@ -68,9 +76,14 @@ gdn_status normalise_shape(const gdn_shape *in, gdn_shape *out) {
 bool tc_shape(const gdn_shape &s) { return s.dtype == GDN_BF16 && s.K == 128 && s.V % 32 == 0; }
 bool scan_shape(const gdn_shape &s) { return tc_shape(s) && s.V % 64 == 0 && s.V <= 256; }
 
+bool fused_shape(const gdn_shape &s) { return s.dtype == GDN_BF16 && s.K == 128 && s.V == 128; }
+
 extern "C" size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape) {
   gdn_shape s;
   if (normalise_shape(shape, &s) != GDN_OK) return 0;
+  // the fused kernel's ring, or the compact pair's T matrices should the fused kernel decline
+  if (fused_shape(s))
+    return std::max(chunk_fused_workspace_bytes(s), chunk_tc_workspace_bytes(s, (int64_t)s.B * s.T));
   if (scan_shape(s)) return chunk_scan_workspace_bytes(s, (int64_t)s.B * s.T);
   if (tc_shape(s)) return chunk_tc_workspace_bytes(s, (int64_t)s.B * s.T);
   return kWorkspaceBase;
@@ -102,7 +115,9 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   gdn_shape s;
   gdn_status st = normalise_shape(shape, &s);
   if (st != GDN_OK) return st;
-  if (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_SIMT | GDN_FLAG_O_F32)) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_SIMT | GDN_FLAG_O_F32 | GDN_FLAG_SPLIT |
+                GDN_FLAG_TEST_NO_WAIT))
+    return GDN_ERR_INVALID_ARG;
   if (cu_seqlens) {
     if (s.B != 1 || s.n_seqs < 0) return GDN_ERR_INVALID_ARG;
   } else if (s.n_seqs != s.B) {
@@ -114,6 +129,13 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   if (s.n_seqs == 0) return GDN_OK;
   if (n_tok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
   if (n_tok == 0 && !h_T) return GDN_OK;
+  if (!(flags & (GDN_FLAG_SIMT | GDN_FLAG_SPLIT)) && n_tok > 0 && chunk_fused_supported(q, k, v, s)) {
+    // the fused kernel; it declines (before launching anything) when the device cannot hold
+    // its grid at once or the workspace is too small for its ring, and the split path runs
+    const gdn_status fs = chunk_fwd_fused(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
+                                          workspace, workspace_bytes, (cudaStream_t)stream);
+    if (fs != GDN_ERR_UNSUPPORTED) return fs;
+  }
   if (!(flags & GDN_FLAG_SIMT) && n_tok > 0 && tc_shape(s) && chunk_tc_supported(q, k, v, s)) {
     if (scan_shape(s) && chunk_scan_supported(q, k, v, s) &&
         workspace_bytes >= chunk_scan_workspace_bytes(s, n_tok))

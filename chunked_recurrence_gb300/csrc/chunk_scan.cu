@@ -922,6 +922,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+namespace gdn {
+
 // [n_tok][heads][width] bf16 map with token stride `tok_stride` elements; 64 x 64 boxes, SW128.
 bool make_tile_map(CUtensorMap *m, const void *base, int width, int heads, int64_t n_tok, int64_t tok_stride) {
   auto enc = encode_fn();
@@ -934,6 +938,10 @@ bool make_tile_map(CUtensorMap *m, const void *base, int width, int heads, int64
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace gdn
+
+namespace {
 
 template <int V>
 gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,

@@ -195,3 +195,18 @@ def test_chunk_bwd_argument_errors_return_before_launch(lib):
     assert call(dq=None) == 1
     assert call(shape=_shape(B=2, n_seqs=2), cu=fake) == 1
     assert call(q=None, shape=_shape(T=0, n_seqs=0), cu=fake, nbytes=256) == 0  # no sequences: no-op
+
+
+def test_flag_values_match_header_and_test_mode_is_off_by_default():
+    """The binding's flag constants are the header's, and no call sets the test-only
+    GDN_FLAG_TEST_NO_WAIT unless asked to."""
+    import inspect
+    import re
+    import chunked_recurrence_gb300 as crg
+    hdr = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    defs = {k: int(v) for k, v in re.findall(r"#define (GDN_FLAG_\w+) (\d+)u", hdr)}
+    for name, val in defs.items():
+        assert getattr(crg, name) == val, name
+    assert inspect.signature(crg.gdn_chunk_fwd).parameters["_test_no_wait"].default is False
+    src = inspect.getsource(crg)
+    assert src.count("GDN_FLAG_TEST_NO_WAIT if _test_no_wait") == 1

@@ -61,10 +61,11 @@ def make_case(lengths, Hqk, Hv, K, V, dtype, gates="paper", h0=False, seed=0, B=
                 scale=K ** -0.5)
 
 
-def run_gpu(crg, c, simt=False, l2norm=True, o_f32=False):
+def run_gpu(crg, c, simt=False, l2norm=True, o_f32=False, split=False):
     d = lambda t: None if t is None else t.to(DEV)
     o, hT = crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]),
-                              d(c["cu"]), c["scale"], l2norm, B=c["B"], simt=simt, o_f32=o_f32)
+                              d(c["cu"]), c["scale"], l2norm, B=c["B"], simt=simt, o_f32=o_f32,
+                              split=split)
     torch.cuda.synchronize()
     return o.cpu(), hT.cpu()
 
@@ -76,8 +77,8 @@ def run_oracle(c, l2norm=True):
                           c["scale"], l2norm, B=c["B"] or 1)
 
 
-def check_case(crg, c, simt=False, l2norm=True, what="", o_f32=False):
-    o, hT = run_gpu(crg, c, simt, l2norm, o_f32)
+def check_case(crg, c, simt=False, l2norm=True, what="", o_f32=False, split=False):
+    o, hT = run_gpu(crg, c, simt, l2norm, o_f32, split)
     ro, rh = run_oracle(c, l2norm)
     mo = assert_close(o, ro, c["dtype"], f"{what} o")
     mh = assert_close(hT, rh, c["dtype"], f"{what} h_T")
@@ -206,22 +207,24 @@ SMALL = [
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{c[5]}-L{len(c[0])}-K{c[3]}-V{c[4]}")
 @pytest.mark.parametrize("gates", ["paper", "mild"])
 @pytest.mark.parametrize("h0", [False, True])
-@pytest.mark.parametrize("simt", [False, True])
-def test_chunk_fwd_small(crg, case, gates, h0, simt):
+@pytest.mark.parametrize("path", ["default", "split", "simt"])
+def test_chunk_fwd_small(crg, case, gates, h0, path):
+    """Every path against the oracle; "default" is the fused kernel for bf16 K = V = 128."""
     lengths, Hqk, Hv, K, V, dtype = case
     c = make_case(lengths, Hqk, Hv, K, V, dtype, gates, h0, seed=len(lengths) * 31 + K + V)
-    mo, mh, o, _, ro, _ = check_case(crg, c, simt=simt, what=f"{case}")
+    mo, mh, o, _, ro, _ = check_case(crg, c, simt=path == "simt", split=path == "split",
+                                     what=f"{case} {path}")
     if gates == "mild" and c["cu"] is not None:
         idx = boundary_windows(c["cu"].numpy())
         assert_close(o[idx], ro[idx], dtype, "boundary windows")
 
 
-@pytest.mark.parametrize("simt", [False, True])
-def test_chunk_fwd_fp32_output_strict_bar(crg, simt):
+@pytest.mark.parametrize("path", ["default", "split", "simt"])
+def test_chunk_fwd_fp32_output_strict_bar(crg, path):
     """bf16 inputs, o written in fp32: the 2e-2 * rms max-abs bar with no storage allowance."""
     for seed, gates in ((287, "paper"), (288, "mild")):
         c = make_case([300, 65], 2, 4, 128, 128, "bf16", gates, True, seed=seed)
-        o, _ = run_gpu(crg, c, simt=simt, o_f32=True)
+        o, _ = run_gpu(crg, c, simt=path == "simt", o_f32=True, split=path == "split")
         assert o.dtype == torch.float32
         ro, _ = run_oracle(c)
         assert_close(o, ro, "bf16", f"fp32-o {gates}")
@@ -474,3 +477,55 @@ def test_segment_summary_compact_workspace(crg):
                                     np.array(bounds, np.int32), l2norm_qk=True)
     assert_close(M.cpu(), rM, "bf16", "compact M")
     assert_close(S.cpu(), rS, "bf16", "compact S_local")
+
+
+# ------------------------------------------------------ fused kernel specifics
+
+FUSED = [
+    # lengths (packed) or rows,         Hqk, Hv, B
+    ([1, 63, 64, 65, 0, 127, 128, 129, 700], 2, 4, None),  # every tail length, an empty sequence
+    ([5000], 1, 1, None),                                    # one long chain
+    ([640], 4, 8, 3),                                        # batch rows, GQA 2:1
+    ([64] * 40, 1, 2, None),                                 # 80 items: chains take several in turn
+]
+
+
+@pytest.mark.parametrize("case", FUSED, ids=lambda c: f"L{len(c[0])}-Hv{c[2]}-B{c[3]}")
+@pytest.mark.parametrize("gates", ["paper", "mild"])
+def test_fused_against_oracle_and_split(crg, case, gates):
+    """The fused kernel against the oracle, and against the split path (the two share no
+    kernel code), with h0, on the tail lengths and item counts that exercise its ring."""
+    lengths, Hqk, Hv, B = case
+    c = make_case(lengths, Hqk, Hv, 128, 128, "bf16", gates, True, seed=90 + len(lengths) + Hv, B=B)
+    o, hT = run_gpu(crg, c)
+    os_, hs = run_gpu(crg, c, split=True)
+    ro, rh = run_oracle(c)
+    assert_close(o, ro, "bf16", "fused o")
+    assert_close(hT, rh, "bf16", "fused h_T")
+    assert_close(os_, ro, "bf16", "split o")
+    assert metrics(o.float(), os_.float())["rel_l2"] <= 5e-3
+    assert metrics(hT, hs)["rel_l2"] <= 5e-3
+    if gates == "mild" and c["cu"] is not None:
+        idx = boundary_windows(c["cu"].numpy(), width=8)
+        assert_close(o[idx], ro[idx], "bf16", "fused chunk-start windows")
+
+
+def test_fused_timeout_reported_then_context_usable(crg):
+    """With every bounded wait told to give up at once, the fused kernel stops and reports
+    GDN_ERR_TIMEOUT in the status word (no trap, no hang); the same context then runs a
+    normal call that matches the oracle."""
+    c = make_case([300, 65], 2, 4, 128, 128, "bf16", "mild", True, seed=77)
+    d = lambda t: None if t is None else t.to(DEV)
+    sh = crg.make_shape(d(c["q"]), d(c["k"]), d(c["v"]), d(c["cu"]))
+    ws = crg.Workspace(crg.gdn_chunk_fwd_workspace_bytes(sh), DEV)
+    ws.reset()
+    crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]), d(c["cu"]),
+                      c["scale"], True, workspace=ws, _test_no_wait=True)
+    assert ws.status() == crg.GDN_ERR_TIMEOUT
+    ws.reset()
+    o, hT = crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]),
+                              d(c["cu"]), c["scale"], True, workspace=ws)
+    assert ws.status() == 0
+    ro, rh = run_oracle(c)
+    assert_close(o.cpu(), ro, "bf16", "o after a timeout")
+    assert_close(hT.cpu(), rh, "bf16", "h_T after a timeout")
