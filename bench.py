@@ -11,9 +11,11 @@ gates, conv with the carried inputs, L2 norm, recurrence) for a batch
 of 64 sequences of the same layer continuing from fp32 states, and the gated
 RMSNorm of the layer's o.
 
-gdn_chunk_fwd runs as two kernels (chunk_operand_kernel: every chunk's
-state-independent operands at once; chunk_scan_kernel: the state chain), so a
+gdn_chunk_fwd runs as two launches: a one-block set-up kernel (the ring flags
+and each chain's schedule) and chunk_fused_kernel, a persistent kernel in which
+per-head state chains are fed by chunk builders through an L2-resident ring; a
 step is four launches.  The roofline is reported for the gdn_chunk_fwd call.
+The two-kernel split path (GDN_FLAG_SPLIT) is timed beside it on the same inputs.
 
 Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
 on the host cores instead, on a bounded sample of the same workload.
@@ -159,11 +161,11 @@ class ClockSampler:
 
 
 def _kernel_sha() -> str:
-    """Hash of the sources chunk_operand_kernel and chunk_scan_kernel compile from: a stored
-    ncu traffic figure is valid for these only."""
+    """Hash of the sources chunk_fused_kernel compiles from: a stored ncu traffic figure is
+    valid for these only."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_recurrence_gb300", "csrc")
-    for fn in ("chunk_common.cuh", "chunk_scan.cu", "common.cuh", "sm100.cuh"):
+    for fn in ("chunk_common.cuh", "chunk_fused.cu", "common.cuh", "sm100.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
@@ -285,32 +287,31 @@ def run_gpu_arm(args, ws, rank, local):
     t_conv = [e[1].elapsed_time(e[2]) for e in marks["ev"]]
     t_chunk = [e[2].elapsed_time(e[3]) for e in marks["ev"]]
     step_ms_local = sum(per_step) / len(per_step)
+    step_ms_median = statistics.median(per_step)
     step_ms = _max_over_ranks(step_ms_local, ws, dev)
     tokens_all = _sum_over_ranks(float(n_tok), ws, dev)
     value = tokens_all / (step_ms * 1e-3)
 
     peaks = _peaks()
     chunk_ms = sum(t_chunk) / len(t_chunk)
+    chunk_ms_median = statistics.median(t_chunk)
     cb = chunk_bytes(wl, n_tok, n_seq, inp["h0"] is not None)
     cf = chunk_flops(wl, n_tok)
-    achieved = cb / (chunk_ms * 1e-3) / 1e9
     sha = _kernel_sha()
     traffic = _stored_traffic(sha)
-    t_hbm = cb / (peaks["hbm_gbs"] * 1e9)
-    t_tc = cf / (peaks["bf16_tflops"] * 1e12)
-    roofline = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
-                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "kernel": "gdn_chunk_fwd (chunk_operand_kernel + chunk_scan_kernel)",
-                "algorithmic_bytes": cb, "algorithmic_flops": cf,
-                "tensor_frac": round(cf / (chunk_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs / bf16_tflops)",
-                "kernel_sha": sha}
+    roofline = roofline_entry(cb, cf, chunk_ms, peaks, traffic)
+    roofline.update({"kernel": "gdn_chunk_fwd (chunk_fused_setup_kernel + chunk_fused_kernel)",
+                     "ms_mean": round(chunk_ms, 5), "ms_median": round(chunk_ms_median, 5),
+                     "kernel_sha": sha})
     kernels = {
         "gdn_gate_prep": _kinfo(sum(t_gate) / len(t_gate), gate_bytes(wl, n_tok), peaks),
         "gdn_conv1d_varlen": _kinfo(sum(t_conv) / len(t_conv), conv_bytes(wl, n_tok), peaks),
         "gdn_chunk_fwd": _kinfo(chunk_ms, cb, peaks),
     }
+
+    q_, k_, v_ = crg.split_qkv(bufs["y"], wl.Hqk, wl.Hv, wl.K, wl.V)
+    paths = time_chunk_paths(crg, q_, k_, v_, bufs["g"], bufs["beta"], inp["h0"], cu,
+                             None if cu is not None else wl.B, inp["scale"], stream, flush)
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws)
@@ -327,10 +328,11 @@ def run_gpu_arm(args, ws, rank, local):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
 
-    launches_per_step = 4  # gate prep, conv1d, and gdn_chunk_fwd's operand + scan kernels
+    launches_per_step = 4  # gate prep, conv1d, and gdn_chunk_fwd's set-up + fused kernels
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "ms_per_step_median": round(step_ms_median, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; x, a ~N(0,1), conv w ~N(0,0.25), A_log ~U(0,ln16), dt_bias ~U(-1,1))",
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hqk": wl.Hqk, "Hv": wl.Hv,
@@ -340,6 +342,7 @@ def run_gpu_arm(args, ws, rank, local):
                    "l2": "flushed between steps (512 MiB fill outside the per-step events)"},
         "roofline": roofline,
         "kernels": kernels,
+        "chunk_fwd_paths": paths,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -351,6 +354,46 @@ def run_gpu_arm(args, ws, rank, local):
         out["decode"] = dec
     if cpu is not None:
         out["cpu_baseline"] = cpu
+    return out
+
+
+def roofline_entry(nbytes, flops, ms, peaks, traffic=None):
+    """Roofline of one call: the bound is the tighter of HBM (algorithmic bytes at the
+    measured copy bandwidth) and the tensor cores (algorithmic FLOPs at the measured bf16
+    rate); `frac` is the fraction of THAT bound's peak, `hbm_frac` and `tensor_frac` both."""
+    t = ms * 1e-3
+    gbs, tfs = nbytes / t / 1e9, flops / t / 1e12
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    hbm = t_hbm >= t_tc
+    return {"bound": "hbm" if hbm else "tensor",
+            "achieved": round(gbs if hbm else tfs, 1),
+            "peak": peaks["hbm_gbs"] if hbm else peaks["bf16_tflops"],
+            "unit": "GB/s" if hbm else "TFLOP/s",
+            "frac": round(max(t_hbm, t_tc) / t, 4), "traffic": traffic,
+            "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "tensor_frac": round(tfs / peaks["bf16_tflops"], 4),
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs / bf16_tflops)"}
+
+
+def time_chunk_paths(crg, q, k, v, g, beta, h0, cu, B, scale, stream, flush, reps=30):
+    """gdn_chunk_fwd on the fused kernel and on the two-kernel split path (GDN_FLAG_SPLIT),
+    same inputs, L2 flushed before each call; median ms of each."""
+    out = {}
+    for name, split in (("fused", False), ("split", True)):
+        ts = []
+        for it in range(reps + 3):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            crg.gdn_chunk_fwd(q, k, v, g, beta, h0, cu, scale, True, B=B, split=split)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 3:
+                ts.append(e0.elapsed_time(e1))
+        out[name + "_ms"] = round(statistics.median(ts), 5)
+    out["speedup"] = round(out["split_ms"] / out["fused_ms"], 3)
     return out
 
 

@@ -63,3 +63,19 @@ def test_rank_helpers_are_identities_on_one_rank():
     assert bench._max_over_ranks(3.5, 1, "cpu") == 3.5
     assert bench._sum_over_ranks(8192.0, 1, "cpu") == 8192.0
     bench._barrier(1)
+
+
+def test_roofline_frac_uses_the_bound_that_applies():
+    """frac is the fraction of the tighter bound's peak: HBM for the headline call, the
+    tensor cores for a contraction-heavy one; both secondary fractions are reported."""
+    peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0, "source": "test"}
+    # 1 GB and 10 GFLOP in 2 ms: HBM time 1 ms > tensor time 0.1 ms -> HBM-bound at 50%
+    r = bench.roofline_entry(1e9, 1e10, 2.0, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 1000.0
+    assert r["frac"] == pytest.approx(0.5) and r["achieved"] == pytest.approx(500.0)
+    assert r["hbm_frac"] == pytest.approx(0.5) and r["tensor_frac"] == pytest.approx(0.05)
+    # 0.1 GB and 200 GFLOP in 4 ms: tensor time 2 ms > HBM time 0.1 ms -> tensor-bound at 50%
+    r = bench.roofline_entry(1e8, 2e11, 4.0, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 100.0
+    assert r["frac"] == pytest.approx(0.5) and r["achieved"] == pytest.approx(50.0)
+    assert r["hbm_frac"] == pytest.approx(0.025)
