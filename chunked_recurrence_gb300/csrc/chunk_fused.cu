@@ -56,7 +56,7 @@ namespace {
 constexpr int C = kChunk;  // 64 tokens per chunk
 constexpr int KD = 128;    // key width
 constexpr int VD = 128;    // value width
-constexpr int NT = 448;    // threads per CTA: 14 warps
+constexpr int NT = 576;    // threads per CTA: 18 warps
 constexpr uint32_t kSpinDefault = 1u << 22;
 constexpr size_t kHeader = 256;  // status word + padding
 
@@ -106,6 +106,7 @@ static_assert(REC_BYTES % 1024 == 0 && REC_SMEM % 16 == 0, "record alignment");
 constexpr int SM_GAM = 0, SM_BEX = 64, SM_DEC = 128, SM_ALF = 192, SM_KINV = 260, SM_QINV = 324,
               SM_BET = 388, SM_ALPHA = 452, SM_DK = 516, SM_MISC = 580;  // misc: blast, unit ints
 constexpr int SM_BAR = 640;  // two mbarriers (8-byte aligned: float index 640 = byte 2560)
+static_assert(SM_MISC + 2 * 8 + 1 <= SM_BAR, "unit words and b_last");
 static_assert(SM_BAR * 4 + 16 <= 3072, "small region");
 
 struct FfCtl {  // at the start of the fused path's control area
@@ -169,19 +170,6 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// 32 lanes x 32 columns of 32-bit data to TMEM (thread i of the warp writes lane quarter + i).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 
@@ -276,6 +264,47 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid, Bar bar) {
 
 // ============================================================ builder lane
 
+// bulk copies shared -> global, tracked per issuing thread in bulk async-groups
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed group has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all but the newest committed group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every committed group has completed its writes
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// decoded unit in the lane's small region (ints): valid (1) or none left (-1), chain, position,
+// v-head, tokens, first token
+constexpr int U_VALID = 0, U_CI = 1, U_POS = 2, U_H = 3, U_N = 4, U_T0 = 5, U_WORDS = 8;
+
+// Claims units until one is real (a chain's stream can be shorter than the longest).
+__device__ __forceinline__ void claim_unit(const FfParams &p, int64_t total, int *u_out) {
+  int valid = -1;
+  Unit un{};
+  int ci = 0, pos = 0;
+  while (!*(volatile int32_t *)&p.ctl->abort) {
+    const int u = atomicAdd(&p.ctl->counter, 1);
+    if ((int64_t)u >= total) break;
+    ci = u % p.n_chain;
+    pos = u / p.n_chain;
+    if (decode_unit(p, ci, pos, un)) {
+      valid = 1;
+      break;
+    }
+  }
+  u_out[U_CI] = ci;
+  u_out[U_POS] = pos;
+  u_out[U_H] = un.h;
+  u_out[U_N] = un.n;
+  u_out[U_T0] = (int)un.t0;
+  u_out[U_VALID] = valid;
+}
+
 __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                              FfParams &p, uint8_t *sm, uint32_t tm, int lane_id) {
   const int tid = threadIdx.x - 128 * lane_id;  // 0..127 inside the lane
@@ -286,20 +315,53 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
   float *gam = smf + SM_GAM, *bex = smf + SM_BEX, *dec = smf + SM_DEC, *alf = smf + SM_ALF;
   float *kinv = smf + SM_KINV, *qinv = smf + SM_QINV, *bet = smf + SM_BET, *alpha = smf + SM_ALPHA;
   float *dk = smf + SM_DK;
-  int *misc = reinterpret_cast<int *>(smf + SM_MISC);
+  int *ucur = reinterpret_cast<int *>(smf + SM_MISC), *unext = ucur + U_WORDS;
+  float *blast_s = smf + SM_MISC + 2 * U_WORDS;
   uint64_t *ld_bar = reinterpret_cast<uint64_t *>(smf + SM_BAR), *mma_bar = ld_bar + 1;
   float *X = reinterpret_cast<float *>(sm + B_X);
   const uint32_t sb = smem_u32(sm);
   const uint32_t lq = (uint32_t)(wq * 32) << 16;
   const uint32_t R0 = tm, R1 = tm + 128;
+  const int64_t total = (int64_t)p.n_chain * (int64_t)p.ctl->maxN;
+  // TMA of a unit's k, q, v tiles (thread 0) and its gates (every thread)
+  auto issue_loads = [&](const int *u) {
+    const int h = u[U_H], n = u[U_N], qh = h / (p.Hv / p.Hqk);
+    const int64_t t0 = u[U_T0];
+    if (tid == 0) {
+      const int32_t tt = (int32_t)t0;
+      mbar_arrive_expect_tx(ld_bar, 6 * 8192);
+      tma_load_3d(sm + B_KQ, tm_k, ld_bar, 0, qh, tt);
+      tma_load_3d(sm + B_KQ + 16384, tm_k, ld_bar, 64, qh, tt);
+      tma_load_3d(sm + B_KQ + 8192, tm_q, ld_bar, 0, qh, tt);
+      tma_load_3d(sm + B_KQ + 24576, tm_q, ld_bar, 64, qh, tt);
+      tma_load_3d(sm + B_V, tm_v, ld_bar, 0, h, tt);
+      tma_load_3d(sm + B_V + 8192, tm_v, ld_bar, 64, h, tt);
+    }
+    // zero past the chunk's end: beta = 0 keeps those rows out of every result, g = 0 keeps
+    // the decays of the real rows
+    if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
+    else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
+  };
   if (tid == 0) {
     mbar_init(ld_bar, 1);
     mbar_init(mma_bar, 1);
     fence_mbar_init();
+    claim_unit(p, total, ucur);
   }
   bar();
+  if (ucur[U_VALID] > 0) issue_loads(ucur);
   uint32_t ldp = 0, mp = 0;
-  const int64_t total = (int64_t)p.n_chain * (int64_t)p.ctl->maxN;
+  int pend_ci = -1, pend_slot = 0, pend_pos = 0;  // record written, its ready flag not yet released
+  // thread 0 releases the pending record once its bulk stores have completed
+  auto release_pending = [&]() {
+    if (tid == 0 && pend_ci >= 0) {
+      bulk_wait_all();
+      fence_proxy_async_all();
+      __threadfence();
+      st_release(p.ready + (size_t)pend_ci * p.R + pend_slot, pend_pos + 1);
+    }
+    pend_ci = -1;
+  };
   // wait (thread 0) on an mbarrier phase; every thread learns the outcome
   auto lane_wait = [&](uint64_t *b, uint32_t &ph) -> bool {
     bool ok = true;
@@ -315,57 +377,20 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
     ++ph;
     return true;
   };
+  bool failed = false;
 #pragma unroll 1
   for (;;) {
-    // ---- claim a unit
-    if (tid == 0) {
-      int valid = -1;
-      if (!*(volatile int32_t *)&p.ctl->abort) {
-        const int u = atomicAdd(&p.ctl->counter, 1);
-        if ((int64_t)u < total) {
-          const int ci = u % p.n_chain, pos = u / p.n_chain;
-          Unit un;
-          valid = decode_unit(p, ci, pos, un) ? 1 : 0;
-          misc[1] = ci;
-          misc[2] = pos;
-          misc[3] = un.s;
-          misc[4] = un.h;
-          misc[5] = un.c;
-          misc[6] = un.last;
-          misc[7] = (int)un.t0;
-          misc[8] = un.n;
-        }
-      }
-      misc[0] = valid;
-    }
     bar();
-    const int valid = misc[0];
-    if (valid < 0) break;
-    if (valid == 0) {
-      bar();  // misc is rewritten by the next claim only after every thread read it
-      continue;
-    }
-    const int ci = misc[1], pos = misc[2], h = misc[4], n = misc[8];
-    const int64_t t0 = misc[7];
-    const int qh = h / (p.Hv / p.Hqk);
+    if (ucur[U_VALID] <= 0) break;
+    const int ci = ucur[U_CI], pos = ucur[U_POS], n = ucur[U_N];
     const int slot = pos % p.R;
     uint8_t *rec = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES;
-
-    // ---- k, q, v tiles by TMA; gates (zero past the chunk's end: beta = 0 keeps those
-    //      rows out of every result, g = 0 keeps the decays of the real rows)
-    if (tid == 0) {
-      const int32_t tt = (int32_t)t0;
-      mbar_arrive_expect_tx(ld_bar, 6 * 8192);
-      tma_load_3d(sm + B_KQ, tm_k, ld_bar, 0, qh, tt);
-      tma_load_3d(sm + B_KQ + 16384, tm_k, ld_bar, 64, qh, tt);
-      tma_load_3d(sm + B_KQ + 8192, tm_q, ld_bar, 0, qh, tt);
-      tma_load_3d(sm + B_KQ + 24576, tm_q, ld_bar, 64, qh, tt);
-      tma_load_3d(sm + B_V, tm_v, ld_bar, 0, h, tt);
-      tma_load_3d(sm + B_V + 8192, tm_v, ld_bar, 64, h, tt);
+    // the next unit is claimed and decoded by another warp while this one is built
+    if (tid == 32) claim_unit(p, total, unext);
+    if (!lane_wait(ld_bar, ldp)) {
+      failed = true;
+      break;
     }
-    if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
-    else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
-    if (!lane_wait(ld_bar, ldp)) break;
 
     // ---- 1/|k| and 1/|q| (two threads per token)
     {
@@ -415,8 +440,6 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
       }
       const float last = __shfl_sync(0xffffffffu, incl, 31);
       const float ga = incl - g1, gb = incl;
-      gam[2 * lane] = ga;
-      gam[2 * lane + 1] = gb;
       bex[2 * lane] = expf(ga);
       bex[2 * lane + 1] = expf(gb);
       dec[2 * lane] = expf(last - ga);
@@ -424,11 +447,15 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
       alf[2 * lane] = expf(g0);
       alf[2 * lane + 1] = expf(g1);
       if (lane == 31) {
-        smf[SM_MISC + 16] = expf(last);  // b_last
+        *blast_s = expf(last);
         alf[C] = 1.f;
       }
     }
-    if (!lane_wait(mma_bar, mp)) break;
+    release_pending();  // the previous unit's record: its stores have had a whole phase to land
+    if (!lane_wait(mma_bar, mp)) {
+      failed = true;
+      break;
+    }
     tc_fence_after();
     if (tid < C) {
       alpha[tid] = p.scale * bex[tid] * qinv[tid];
@@ -449,7 +476,7 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
         const float aj = alf[j + 1], kj = kinv[j];
         if (j < i) gprod *= aj;
         const bool keep = isq ? (j <= i) : (j < i);
-        r64[j] = keep ? bi * kj * ((j == i) ? 1.f : gprod) * r64[j] : 0.f;
+        r64[j] = keep ? bi * kj * gprod * r64[j] : 0.f;
       }
       if (!isq) {
         float4 *xr = reinterpret_cast<float4 *>(X + i * kXP);
@@ -517,28 +544,16 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
                   id, ks > 0);
       umma_commit(mma_bar);
     }
-    {
-      // the ring slot must be free (its previous record consumed) before anything is written
-      bool ok = true;
-      if (tid == 0) {
-        ok = mbar_wait(mma_bar, mp & 1, p.spin);
-        if (ok) ok = wait_flag_ge(p.consumed + ci, pos - p.R + 1, p.spin, p.ctl);
-      }
-      if (named_bar_any(bid, 128, !ok)) {
-        if (tid == 0) {
-          give_up(p, nullptr);
-          (void)mbar_wait(mma_bar, mp & 1, kSpinDefault);
-        }
-        break;
-      }
-      ++mp;
+    if (!lane_wait(mma_bar, mp)) {
+      failed = true;
+      break;
     }
     tc_fence_after();
-    // ---- rows of U and W (an M = 64 result: lanes 0-15 of each quarter)
+    // ---- rows of U (hi + lo) and W (bf16) into shared memory (an M = 64 result: lanes 0-15
+    //      of each quarter); k rows become diag(d/|k|) k for What = W^T diag(d/|k|) K
     {
       const int rr = wq * 16 + lane;
       const bool has_row = lane < 16;
-      const float dki = has_row ? dk[rr] : 0.f;
 #pragma unroll 1
       for (int hv = 0; hv < 2; ++hv) {
         float u[64];
@@ -547,31 +562,24 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
         if (has_row) {
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 8) {
-            uint32_t uh[4], ul[4], th[4], tl[4];
+            uint32_t uh[4], ul[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              split2(u[c0 + 2 * e], u[c0 + 2 * e + 1], uh[e], ul[e]);
-              split2(dki * u[c0 + 2 * e], dki * u[c0 + 2 * e + 1], th[e], tl[e]);
-            }
+            for (int e = 0; e < 4; ++e) split2(u[c0 + 2 * e], u[c0 + 2 * e + 1], uh[e], ul[e]);
             const uint32_t off = hv * 8192 + sw128_off(rr, c0);
             *reinterpret_cast<uint4 *>(sm + B_V + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
             *reinterpret_cast<uint4 *>(sm + B_X + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
-            *reinterpret_cast<uint4 *>(rec + REC_UTH + off) = make_uint4(th[0], th[1], th[2], th[3]);
-            *reinterpret_cast<uint4 *>(rec + REC_UTL + off) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
           }
         }
-        float w[64];
-        tmem_ld64(R1 + lq + hv * 64, w);
+        tmem_ld64(R1 + lq + hv * 64, u);
         tmem_wait_ld();
         if (has_row) {
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 8)
             *reinterpret_cast<uint4 *>(sm + B_TH + hv * 8192 + sw128_off(rr, c0)) =
-                make_uint4(pack_bf16(w[c0], w[c0 + 1]), pack_bf16(w[c0 + 2], w[c0 + 3]),
-                           pack_bf16(w[c0 + 4], w[c0 + 5]), pack_bf16(w[c0 + 6], w[c0 + 7]));
+                make_uint4(pack_bf16(u[c0], u[c0 + 1]), pack_bf16(u[c0 + 2], u[c0 + 3]),
+                           pack_bf16(u[c0 + 4], u[c0 + 5]), pack_bf16(u[c0 + 6], u[c0 + 7]));
         }
       }
-      // k rows become diag(d/|k|) k (bf16) for What = W^T diag(d/|k|) K
       {
         const int r = tid >> 1, hf = tid & 1;
         const float s = dk[r];
@@ -613,21 +621,61 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
                   id_w, ks > 0);
       umma_commit(mma_bar);
     }
-    if (!lane_wait(mma_bar, mp)) break;
-    tc_fence_after();
-    // ---- the record: (P U)^T, Qt^T = alpha Q^T - (P W)^T, -What, b_last
     {
-      const int m = wq * 32 + lane;  // TMEM lane: v for (P U)^T, key feature for the others
-      float x[64];
-      tmem_ld64(R0 + lq, x);
-      tmem_wait_ld();
-      float4 *opr = reinterpret_cast<float4 *>(rec + REC_OP + (size_t)m * 256);
+      // the MMAs, and the ring slot free (its previous record consumed) before any record store
+      bool ok = true;
+      if (tid == 0) {
+        ok = wait_flag_ge(p.consumed + ci, pos - p.R + 1, p.spin, p.ctl);
+        ok = mbar_wait(mma_bar, mp & 1, ok ? p.spin : kSpinDefault) && ok;
+      }
+      if (named_bar_any(bid, 128, !ok)) {
+        if (tid == 0) give_up(p, nullptr);
+        failed = true;
+        break;
+      }
+      ++mp;
+    }
+    tc_fence_after();
+    // ---- the record, staged in shared memory and written by bulk copies:
+    // (1) Ut = diag(d/|k|) U as hi + lo, in place over the U images (16-byte pieces)
+#pragma unroll 2
+    for (int c16 = tid; c16 < 1024; c16 += 128) {
+      const uint32_t off = (uint32_t)c16 * 16;
+      const float s = dk[(off & 8191) >> 7];
+      uint4 *ph = reinterpret_cast<uint4 *>(sm + B_V + off), *pl = reinterpret_cast<uint4 *>(sm + B_X + off);
+      const uint4 h4 = *ph, l4 = *pl;
+      const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, lw[4] = {l4.x, l4.y, l4.z, l4.w};
+      uint32_t oh[4], ol[4];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) opr[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+      for (int e = 0; e < 4; ++e) {
+        const float2 a = unpack_bf16(hw[e]), b = unpack_bf16(lw[e]);
+        split2(s * (a.x + b.x), s * (a.y + b.y), oh[e], ol[e]);
+      }
+      *ph = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+      *pl = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+    }
+    const int m = wq * 32 + lane;  // TMEM lane: v for (P U)^T, key feature for the others
+    // (2) -What from R1 into the free T and P images (rows m, [2 f-halves][128 rows][128 B])
+#pragma unroll 1
+    for (int fh = 0; fh < 2; ++fh) {
+      float x[64];
+      tmem_ld64(R1 + lq + fh * 64, x);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 8)
+        *reinterpret_cast<uint4 *>(sm + B_TH + fh * 16384 + sw128_off(m, c0)) =
+            make_uint4(pack_bf16(-x[c0], -x[c0 + 1]), pack_bf16(-x[c0 + 2], -x[c0 + 3]),
+                       pack_bf16(-x[c0 + 4], -x[c0 + 5]), pack_bf16(-x[c0 + 6], -x[c0 + 7]));
+    }
+    // (3) Qt^T = alpha Q^T - (P W)^T into the k rows (rows 0-63 of the image in the first
+    //     half's k rows, rows 64-127 in the second half's)
+    {
+      float x[64];
       tmem_ld64(R0 + lq + 64, x);
       tmem_wait_ld();
       const uint8_t *qcol = sm + B_KQ + (m >> 6) * 16384;
       const int f = m & 63;
+      uint8_t *dst = sm + B_KQ + (m >> 6) * 16384;
 #pragma unroll
       for (int t8 = 0; t8 < 64; t8 += 8) {
         uint32_t w4[4];
@@ -638,27 +686,56 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
           const float q1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qcol + sw128_off(65 + t, f)));
           w4[e] = pack_bf16(fmaf(alpha[t], q0, -x[t]), fmaf(alpha[t + 1], q1, -x[t + 1]));
         }
-        *reinterpret_cast<uint4 *>(rec + REC_QT + sw128_off(m, t8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        *reinterpret_cast<uint4 *>(dst + sw128_off(f, t8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-#pragma unroll 1
-      for (int fh = 0; fh < 2; ++fh) {
-        tmem_ld64(R1 + lq + fh * 64, x);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 8)
-          *reinterpret_cast<uint4 *>(rec + REC_WN + fh * 16384 + sw128_off(m, c0)) =
-              make_uint4(pack_bf16(-x[c0], -x[c0 + 1]), pack_bf16(-x[c0 + 2], -x[c0 + 3]),
-                         pack_bf16(-x[c0 + 4], -x[c0 + 5]), pack_bf16(-x[c0 + 6], -x[c0 + 7]));
-      }
-      if (tid == 0) *reinterpret_cast<float *>(rec + REC_VEC) = smf[SM_MISC + 16];
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     bar();
     if (tid == 0) {
-      __threadfence();
-      st_release(p.ready + (size_t)ci * p.R + slot, pos + 1);
+      bulk_store(rec + REC_UTH, sm + B_V, 16384);
+      bulk_store(rec + REC_UTL, sm + B_X, 16384);
+      bulk_commit();
+      bulk_store(rec + REC_WN, sm + B_TH, 32768);
+      bulk_store(rec + REC_QT, sm + B_KQ, 8192);
+      bulk_store(rec + REC_QT + 8192, sm + B_KQ + 16384, 8192);
+      bulk_commit();
+      *reinterpret_cast<float *>(rec + REC_VEC) = *blast_s;
+      bulk_wait_read1();  // the U images have been read: they take (P U)^T next
     }
+    bar();
+    // (4) (P U)^T fp32, row v = m: 16-byte piece j at (j ^ (v % 16)) of its 256-byte row
+    {
+      float x[64];
+      tmem_ld64(R0 + lq, x);
+      tmem_wait_ld();
+      uint8_t *row = sm + B_V + (size_t)m * 256;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        *reinterpret_cast<float4 *>(row + ((j ^ (m & 15)) << 4)) =
+            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    bar();
+    if (tid == 0) {
+      bulk_store(rec + REC_OP, sm + B_V, 32768);
+      bulk_commit();
+    }
+    pend_ci = ci;
+    pend_slot = slot;
+    pend_pos = pos;
+    // ---- the next unit: its tiles go where this record was staged once the copies have read it
+    bar();  // unext is written
+    if (tid == 0) bulk_wait_read0();
+    bar();
+    if (tid == 0)
+      for (int w = 0; w < U_WORDS; ++w) ucur[w] = unext[w];
+    bar();
+    if (ucur[U_VALID] > 0) issue_loads(ucur);
   }
+  if (!failed) release_pending();
+  if (tid == 0) bulk_wait_all();  // no copy may still read shared memory when the CTA exits
 }
 
 // ============================================================ chain CTA
@@ -671,6 +748,9 @@ struct ChainShared {
   uint32_t mma_par;
 };
 
+constexpr int kEpiWarps = 16;        // state and output warps of a chain CTA
+constexpr uint32_t CH_TILE = kStages * kStage;  // bf16 [64 tokens][128 v] output tile
+
 __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uint32_t tm, ChainShared &sh,
                           int ci) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -678,7 +758,7 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
   volatile int *abort_flag = &sh.abort;
   const int n_r = (p.n_items - ci + p.n_chain - 1) / p.n_chain;
 
-  if (warp == 12) {
+  if (warp == kEpiWarps) {
     // ===================================================== loads
     if (lane == 0) {
       tma_prefetch_desc(tm_k);
@@ -686,9 +766,10 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
       bool ok = true;
       for (int r = 0; r < n_r && ok; ++r) {
         const int j = ci + r * p.n_chain, s = j / p.Hv, h = j % p.Hv, qh = h / (p.Hv / p.Hqk);
+        const int nc = p.nch[j];
         int64_t start, end;
         seq_range(p.cu, p.row_T, s, start, end);
-        for (int c = 0; c < p.nch[j]; ++c, ++pos) {
+        for (int c = 0; c < nc; ++c, ++pos) {
           const int st = pos % kStages;
           if (pos >= kStages && !mbar_wait_spin(&sh.empty[st], ((pos - kStages) / kStages) & 1, p.spin, abort_flag)) {
             ok = false;
@@ -702,8 +783,11 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
           fence_proxy_async_all();
           uint8_t *sg = sm + st * kStage;
           const uint8_t *rec = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES;
-          mbar_arrive_expect_tx(&sh.full[st], REC_SMEM + 16384);
-          bulk_load(sg, rec, REC_SMEM, &sh.full[st]);
+          const bool last = c == nc - 1;  // Ut lo is only read on a sequence's last chunk
+          mbar_arrive_expect_tx(&sh.full[st], REC_UTL + (REC_SMEM - REC_QT) + (last ? 16384u : 0u) + 16384);
+          bulk_load(sg, rec, REC_UTL, &sh.full[st]);
+          bulk_load(sg + REC_QT, rec + REC_QT, REC_SMEM - REC_QT, &sh.full[st]);
+          if (last) bulk_load(sg + REC_UTL, rec + REC_UTL, 16384, &sh.full[st]);
           const int32_t tt = (int32_t)(start + (int64_t)c * C);
           tma_load_3d(sg + ST_K, tm_k, &sh.full[st], 0, qh, tt);
           tma_load_3d(sg + ST_K + 8192, tm_k, &sh.full[st], 64, qh, tt);
@@ -712,7 +796,7 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
       }
       if (!ok) give_up(p, abort_flag);
     }
-  } else if (warp == 13) {
+  } else if (warp == kEpiWarps + 1) {
     // ===================================================== MMAs
     if (lane == 0) {
       const uint32_t id_u = idesc_bf16(128, 128, true, true);
@@ -756,7 +840,7 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
           umma_commit(&sh.chain_done[b]);
           sh.mma_bar = &sh.chain_done[b];
           sh.mma_par = (pos >> 1) & 1;
-          // O^T = S Qt^T once the output warps are done with this accumulator (chunk pos - 2)
+          // O^T = S Qt^T once the epilogue warps are done with this accumulator (chunk pos - 2)
           if (pos >= 2 && !mbar_wait_spin(&sh.out_free[b], ((pos - 2) >> 1) & 1, p.spin, abort_flag)) {
             ok = false;
             break;
@@ -773,20 +857,23 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
       }
       if (!ok) give_up(p, abort_flag);
     }
-  } else if (warp < 8) {
-    // ===================================================== state (warps 0-7)
-    // thread: value row v = 32 (warp % 4) + lane, key features [64 (warp / 4), +64)
-    const int quarter = warp & 3, half = warp >> 2;
-    const int v = quarter * 32 + lane, k0 = half * 64;
+  } else {
+    // ===================================================== state and outputs (warps 0-15)
+    // thread: value row v = 32 (warp % 4) + lane; key features [32 g, +32) of the state and
+    // tokens [16 g, +16) of the output, g = warp / 4
+    const int quarter = warp & 3, g = warp >> 2;
+    const int v = quarter * 32 + lane;
     const uint32_t lq = (uint32_t)(quarter * 32) << 16;
-    float S[64];
+    const size_t o_tok = (size_t)p.Hv * VD;
+    __nv_bfloat16 *tile = reinterpret_cast<__nv_bfloat16 *>(sm + CH_TILE);
+    float S[32];
     int pos = 0;
     bool ok = true;
     auto write_shi = [&](int b) {
-      uint32_t pk[32];
+      float pk[16];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16(S[2 * jj], S[2 * jj + 1]);
-      tmem_st32(tm + lq + T_SHI + b * 64 + half * 32, pk);
+      for (int jj = 0; jj < 16; ++jj) pk[jj] = __uint_as_float(pack_bf16(S[2 * jj], S[2 * jj + 1]));
+      tmem_st16(tm + lq + T_SHI + b * 64 + g * 16, pk);
       tmem_wait_st();
       tc_fence_before();
       warp_arrive(&sh.s_ready);
@@ -795,11 +882,13 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
       const int j = ci + r * p.n_chain, s = j / p.Hv, h = j % p.Hv;
       const int nc = p.nch[j];
       if (nc == 0) continue;
-      const size_t srow = (((size_t)s * p.Hv + h) * VD + v) * KD + k0;
+      int64_t start, end;
+      seq_range(p.cu, p.row_T, s, start, end);
+      const size_t srow = (((size_t)s * p.Hv + h) * VD + v) * KD + g * 32;
       if (p.h0) {
         const float4 *src = reinterpret_cast<const float4 *>(p.h0 + srow);
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
+        for (int m = 0; m < 8; ++m) {
           const float4 a = src[m];
           S[4 * m] = a.x;
           S[4 * m + 1] = a.y;
@@ -808,27 +897,29 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
         }
       } else {
 #pragma unroll
-        for (int m = 0; m < 64; ++m) S[m] = 0.f;
+        for (int m = 0; m < 32; ++m) S[m] = 0.f;
       }
       write_shi(pos & 1);
       for (int c = 0; c < nc; ++c, ++pos) {
-        const int b = pos & 1, st = pos % kStages;
-        // the warp's lanes agree on the outcome: the TMEM loads below need the whole warp
-        const bool got = mbar_wait_spin(&sh.chain_done[b], (pos >> 1) & 1, p.spin, abort_flag) &&
-                         mbar_wait_spin(&sh.full[st], (pos / kStages) & 1, p.spin, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
+        const int b = pos & 1, st = pos % kStages, slot = pos % p.R;
+        // ---- the state: S <- b_last S + D
+        {
+          // the warp's lanes agree on the outcome: the TMEM loads below need the whole warp
+          const bool got = mbar_wait_spin(&sh.chain_done[b], (pos >> 1) & 1, p.spin, abort_flag) &&
+                           mbar_wait_spin(&sh.full[st], (pos / kStages) & 1, p.spin, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
         }
         const float bl = *reinterpret_cast<const float *>(sm + st * kStage + REC_VEC);
         tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        {
           float D[32];
-          tmem_ld32(tm + lq + T_DCH + b * 128 + k0 + hh * 32, D);
+          tmem_ld32(tm + lq + T_DCH + b * 128 + g * 32, D);
           tmem_wait_ld();
 #pragma unroll
-          for (int m = 0; m < 32; ++m) S[hh * 32 + m] = fmaf(bl, S[hh * 32 + m], D[m]);
+          for (int m = 0; m < 32; ++m) S[m] = fmaf(bl, S[m], D[m]);
         }
         tc_fence_before();
         warp_arrive(&sh.empty[st]);
@@ -837,77 +928,71 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
         } else if (p.hT) {
           float4 *dst = reinterpret_cast<float4 *>(p.hT + srow);
 #pragma unroll
-          for (int m = 0; m < 16; ++m) dst[m] = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
+          for (int m = 0; m < 8; ++m) dst[m] = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
         }
-      }
-    }
-    if (!ok && lane == 0) give_up(p, abort_flag);
-  } else {
-    // ===================================================== outputs (warps 8-11)
-    const int quarter = warp - 8;
-    const int v = quarter * 32 + lane;
-    const uint32_t lq = (uint32_t)(quarter * 32) << 16;
-    const size_t o_tok = (size_t)p.Hv * VD;
-    int pos = 0;
-    bool ok = true;
-    for (int r = 0; r < n_r && ok; ++r) {
-      const int j = ci + r * p.n_chain, s = j / p.Hv, h = j % p.Hv;
-      const int nc = p.nch[j];
-      int64_t start, end;
-      seq_range(p.cu, p.row_T, s, start, end);
-      for (int c = 0; c < nc; ++c, ++pos) {
-        const int b = pos & 1, slot = pos % p.R;
-        const bool got = mbar_wait_spin(&sh.out_done[b], (pos >> 1) & 1, p.spin, abort_flag) &&
-                         wait_flag_ge(p.ready + (size_t)ci * p.R + slot, pos + 1, p.spin, p.ctl);
-        // the four output warps agree before any of them leaves: a warp that left alone
-        // would strand the others at the named barrier below
-        if (named_bar_any(3, 128, !got)) {
+        // ---- the output of this chunk: o[t][v] = O^T[v][t] + (P U)^T[v][t] for tokens [16 g, +16)
+        const bool got = wait_flag_ge(p.ready + (size_t)ci * p.R + slot, pos + 1, p.spin, p.ctl) &&
+                         mbar_wait_spin(&sh.out_done[b], (pos >> 1) & 1, p.spin, abort_flag);
+        // the sixteen warps agree before any of them leaves: one that left alone would
+        // strand the others at the named barriers below
+        if (named_bar_any(3, 32 * kEpiWarps, !got)) {
           ok = false;
           break;
         }
-        const float4 *opr =
-            reinterpret_cast<const float4 *>(p.ring + ((size_t)ci * p.R + slot) * REC_BYTES + REC_OP + (size_t)v * 256);
-        const int64_t t0 = start + (int64_t)c * C;
-        const int n = (int)min((int64_t)C, end - t0);
-        const size_t base = (size_t)t0 * o_tok + (size_t)h * VD + v;
+        float x[16];
+        {
+          const uint8_t *prow = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES + REC_OP + (size_t)v * 256;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(prow + (((g * 4 + jj) ^ (v & 15)) << 4)));
+            x[4 * jj] = a.x;
+            x[4 * jj + 1] = a.y;
+            x[4 * jj + 2] = a.z;
+            x[4 * jj + 3] = a.w;
+          }
+        }
         tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float x[32], d[32];
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float4 a = __ldcg(opr + hh * 8 + m);
-            x[4 * m] = a.x;
-            x[4 * m + 1] = a.y;
-            x[4 * m + 2] = a.z;
-            x[4 * m + 3] = a.w;
-          }
-          tmem_ld32(tm + lq + T_DOUT + b * 64 + hh * 32, d);
+        {
+          float d[16];
+          tmem_ld16(tm + lq + T_DOUT + b * 64 + g * 16, d);
           tmem_wait_ld();
-          if (p.o_f32) {
-            float *o = reinterpret_cast<float *>(p.o) + base;
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
-              if (hh * 32 + t < n) o[(size_t)(hh * 32 + t) * o_tok] = x[t] + d[t];
-          } else {
-            __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o) + base;
-#pragma unroll
-            for (int t = 0; t < 32; ++t)
-              if (hh * 32 + t < n) o[(size_t)(hh * 32 + t) * o_tok] = __float2bfloat16_rn(x[t] + d[t]);
-          }
+          for (int i = 0; i < 16; ++i) x[i] += d[i];
         }
         tc_fence_before();
         warp_arrive(&sh.out_free[b]);
-        // every output lane has read the slot: it may take the next record
-        named_bar_sync(3, 128);
-        if (warp == 8 && lane == 0) st_release(p.consumed + ci, pos + 1);
+        const int64_t t0 = start + (int64_t)c * C;
+        const int n = (int)min((int64_t)C, end - t0);
+        const size_t base = (size_t)t0 * o_tok + (size_t)h * VD;
+        if (p.o_f32) {
+          float *o = reinterpret_cast<float *>(p.o) + base + v;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (g * 16 + i < n) o[(size_t)(g * 16 + i) * o_tok] = x[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) tile[(g * 16 + i) * VD + v] = __float2bfloat16_rn(x[i]);
+          named_bar_sync(3, 32 * kEpiWarps);
+          // rows of 256 bytes: 16 threads per row, 32 rows per pass
+          const int tr = tid >> 4, tc = tid & 15;
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass) {
+            const int t = pass * 32 + tr;
+            if (t < n)
+              *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + base + (size_t)t * o_tok + tc * 8) =
+                  *reinterpret_cast<const uint4 *>(tile + t * VD + tc * 8);
+          }
+        }
+        // every epilogue thread has read the slot and the tile: both may be reused
+        named_bar_sync(3, 32 * kEpiWarps);
+        if (tid == 0) st_release(p.consumed + ci, pos + 1);
       }
     }
     if (!ok && lane == 0) give_up(p, abort_flag);
   }
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __maxnreg__(112)
     chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, FfParams p) {
   extern __shared__ uint8_t smraw[];
@@ -921,14 +1006,14 @@ __global__ void __launch_bounds__(NT, 1)
     if (is_chain) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(&sh.full[i], 1);
-        mbar_init(&sh.empty[i], 1 + 8);  // the MMA commit and the 8 state warps (b_last read)
+        mbar_init(&sh.empty[i], 1 + kEpiWarps);  // the MMA commit and the warps that read b_last
         sh.fills[i] = 0;
       }
-      mbar_init(&sh.s_ready, 8);
+      mbar_init(&sh.s_ready, kEpiWarps);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&sh.chain_done[i], 1);
         mbar_init(&sh.out_done[i], 1);
-        mbar_init(&sh.out_free[i], 4);
+        mbar_init(&sh.out_free[i], kEpiWarps);
       }
     }
     sh.abort = 0;
@@ -1040,7 +1125,7 @@ FfLayout ff_layout(int n_chain, int R, int n_items) {
 }
 
 constexpr int kMaxChains = 32;  // chains at once; the other SMs build
-constexpr int kMaxRing = 6;     // records per chain in flight
+constexpr int kMaxRing = 12;    // records per chain in flight
 
 }  // namespace
 
