@@ -381,18 +381,25 @@ def time_chunk_paths(crg, q, k, v, g, beta, h0, cu, B, scale, stream, flush, rep
     """gdn_chunk_fwd on the fused kernel and on the two-kernel split path (GDN_FLAG_SPLIT),
     same inputs, L2 flushed before each call; median ms of each."""
     out = {}
+    sh = crg.make_shape(q, k, v, cu, B)
     for name, split in (("fused", False), ("split", True)):
+        nb = crg.gdn_chunk_fwd_workspace_bytes(sh)
+        if split:
+            nb = max(nb, crg.split_workspace_bytes(sh))
+        ws = crg.Workspace(nb, q.device)
+        ws.reset()
         ts = []
         for it in range(reps + 3):
             flush.fill_(1)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            crg.gdn_chunk_fwd(q, k, v, g, beta, h0, cu, scale, True, B=B, split=split)
+            crg.gdn_chunk_fwd(q, k, v, g, beta, h0, cu, scale, True, B=B, split=split, workspace=ws)
             e1.record(stream)
             torch.cuda.synchronize()
             if it >= 3:
                 ts.append(e0.elapsed_time(e1))
         out[name + "_ms"] = round(statistics.median(ts), 5)
+        out[name + "_path_word"] = ws.path()  # GDN_PATH_FUSED (1) when the fused kernel ran
     out["speedup"] = round(out["split_ms"] / out["fused_ms"], 3)
     return out
 

@@ -20,6 +20,7 @@ from . import build as _build
 
 GDN_OK = 0
 GDN_ERR_TIMEOUT, GDN_ERR_BOUNDS = 4, 6  # device-side statuses read from a workspace
+GDN_PATH_FUSED = 1                      # path word of a workspace after the fused kernel ran
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_SIMT = 2
@@ -53,6 +54,7 @@ _SIGS = {
     "gdn_segment_summary_workspace_bytes": ([ctypes.POINTER(GdnShape), _I32], _SZ),
     "gdn_workspace_reset": ([_P, _SZ, _P], ctypes.c_int),
     "gdn_workspace_status": ([_P, ctypes.POINTER(_I32), _P], ctypes.c_int),
+    "gdn_workspace_path": ([_P, ctypes.POINTER(_I32), _P], ctypes.c_int),
     "gdn_gate_prep": ([_P, _P, _I32, _P, _P, _I64, _I32, _P, _P, _P], ctypes.c_int),
     "gdn_conv1d_varlen": ([_P, _P, _P, _I32, _P, _I32, _I64, _I32, _I32, _I32, _P, _P],
                           ctypes.c_int),
@@ -277,6 +279,13 @@ class Workspace:
         out = ctypes.c_int32(0)
         _check(load().gdn_workspace_status(self.ptr(), ctypes.byref(out), _stream(self.buf, stream)),
                "gdn_workspace_status")
+        return out.value
+
+    def path(self, stream=None) -> int:
+        """The path word: GDN_PATH_FUSED after the fused kernel ran in this workspace."""
+        out = ctypes.c_int32(0)
+        _check(load().gdn_workspace_path(self.ptr(), ctypes.byref(out), _stream(self.buf, stream)),
+               "gdn_workspace_path")
         return out.value
 
     def reset(self, stream=None):

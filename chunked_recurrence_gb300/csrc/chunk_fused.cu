@@ -56,7 +56,7 @@ namespace {
 constexpr int C = kChunk;  // 64 tokens per chunk
 constexpr int KD = 128;    // key width
 constexpr int VD = 128;    // value width
-constexpr int NT = 576;    // threads per CTA: 18 warps
+constexpr int NT = 320;    // threads per CTA: 10 warps
 constexpr uint32_t kSpinDefault = 1u << 22;
 constexpr size_t kHeader = 256;  // status word + padding
 
@@ -170,6 +170,19 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit data to TMEM (thread i of the warp writes lane quarter + i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 
@@ -748,7 +761,7 @@ struct ChainShared {
   uint32_t mma_par;
 };
 
-constexpr int kEpiWarps = 16;        // state and output warps of a chain CTA
+constexpr int kEpiWarps = 8;         // state and output warps of a chain CTA
 constexpr uint32_t CH_TILE = kStages * kStage;  // bf16 [64 tokens][128 v] output tile
 
 __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uint32_t tm, ChainShared &sh,
@@ -858,22 +871,22 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
       if (!ok) give_up(p, abort_flag);
     }
   } else {
-    // ===================================================== state and outputs (warps 0-15)
-    // thread: value row v = 32 (warp % 4) + lane; key features [32 g, +32) of the state and
-    // tokens [16 g, +16) of the output, g = warp / 4
+    // ===================================================== state and outputs (warps 0-7)
+    // thread: value row v = 32 (warp % 4) + lane; key features [64 g, +64) of the state and
+    // tokens [32 g, +32) of the output, g = warp / 4
     const int quarter = warp & 3, g = warp >> 2;
     const int v = quarter * 32 + lane;
     const uint32_t lq = (uint32_t)(quarter * 32) << 16;
     const size_t o_tok = (size_t)p.Hv * VD;
     __nv_bfloat16 *tile = reinterpret_cast<__nv_bfloat16 *>(sm + CH_TILE);
-    float S[32];
+    float S[64];
     int pos = 0;
     bool ok = true;
     auto write_shi = [&](int b) {
-      float pk[16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) pk[jj] = __uint_as_float(pack_bf16(S[2 * jj], S[2 * jj + 1]));
-      tmem_st16(tm + lq + T_SHI + b * 64 + g * 16, pk);
+      for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16(S[2 * jj], S[2 * jj + 1]);
+      tmem_st32(tm + lq + T_SHI + b * 64 + g * 32, pk);
       tmem_wait_st();
       tc_fence_before();
       warp_arrive(&sh.s_ready);
@@ -884,11 +897,11 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
       if (nc == 0) continue;
       int64_t start, end;
       seq_range(p.cu, p.row_T, s, start, end);
-      const size_t srow = (((size_t)s * p.Hv + h) * VD + v) * KD + g * 32;
+      const size_t srow = (((size_t)s * p.Hv + h) * VD + v) * KD + g * 64;
       if (p.h0) {
         const float4 *src = reinterpret_cast<const float4 *>(p.h0 + srow);
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
+        for (int m = 0; m < 16; ++m) {
           const float4 a = src[m];
           S[4 * m] = a.x;
           S[4 * m + 1] = a.y;
@@ -897,7 +910,7 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
         }
       } else {
 #pragma unroll
-        for (int m = 0; m < 32; ++m) S[m] = 0.f;
+        for (int m = 0; m < 64; ++m) S[m] = 0.f;
       }
       write_shi(pos & 1);
       for (int c = 0; c < nc; ++c, ++pos) {
@@ -915,11 +928,11 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
         const float bl = *reinterpret_cast<const float *>(sm + st * kStage + REC_VEC);
         tc_fence_after();
         {
-          float D[32];
-          tmem_ld32(tm + lq + T_DCH + b * 128 + g * 32, D);
+          float D[64];
+          tmem_ld64(tm + lq + T_DCH + b * 128 + g * 64, D);
           tmem_wait_ld();
 #pragma unroll
-          for (int m = 0; m < 32; ++m) S[m] = fmaf(bl, S[m], D[m]);
+          for (int m = 0; m < 64; ++m) S[m] = fmaf(bl, S[m], D[m]);
         }
         tc_fence_before();
         warp_arrive(&sh.empty[st]);
@@ -928,23 +941,23 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
         } else if (p.hT) {
           float4 *dst = reinterpret_cast<float4 *>(p.hT + srow);
 #pragma unroll
-          for (int m = 0; m < 8; ++m) dst[m] = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
+          for (int m = 0; m < 16; ++m) dst[m] = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
         }
-        // ---- the output of this chunk: o[t][v] = O^T[v][t] + (P U)^T[v][t] for tokens [16 g, +16)
+        // ---- the output of this chunk: o[t][v] = O^T[v][t] + (P U)^T[v][t] for tokens [32 g, +32)
         const bool got = wait_flag_ge(p.ready + (size_t)ci * p.R + slot, pos + 1, p.spin, p.ctl) &&
                          mbar_wait_spin(&sh.out_done[b], (pos >> 1) & 1, p.spin, abort_flag);
-        // the sixteen warps agree before any of them leaves: one that left alone would
+        // the epilogue warps agree before any of them leaves: one that left alone would
         // strand the others at the named barriers below
         if (named_bar_any(3, 32 * kEpiWarps, !got)) {
           ok = false;
           break;
         }
-        float x[16];
+        float x[32];
         {
           const uint8_t *prow = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES + REC_OP + (size_t)v * 256;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const float4 a = __ldcg(reinterpret_cast<const float4 *>(prow + (((g * 4 + jj) ^ (v & 15)) << 4)));
+          for (int jj = 0; jj < 8; ++jj) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(prow + (((g * 8 + jj) ^ (v & 15)) << 4)));
             x[4 * jj] = a.x;
             x[4 * jj + 1] = a.y;
             x[4 * jj + 2] = a.z;
@@ -953,11 +966,11 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
         }
         tc_fence_after();
         {
-          float d[16];
-          tmem_ld16(tm + lq + T_DOUT + b * 64 + g * 16, d);
+          float d[32];
+          tmem_ld32(tm + lq + T_DOUT + b * 64 + g * 32, d);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[i] += d[i];
+          for (int i = 0; i < 32; ++i) x[i] += d[i];
         }
         tc_fence_before();
         warp_arrive(&sh.out_free[b]);
@@ -967,17 +980,17 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
         if (p.o_f32) {
           float *o = reinterpret_cast<float *>(p.o) + base + v;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (g * 16 + i < n) o[(size_t)(g * 16 + i) * o_tok] = x[i];
+          for (int i = 0; i < 32; ++i)
+            if (g * 32 + i < n) o[(size_t)(g * 32 + i) * o_tok] = x[i];
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) tile[(g * 16 + i) * VD + v] = __float2bfloat16_rn(x[i]);
+          for (int i = 0; i < 32; ++i) tile[(g * 32 + i) * VD + v] = __float2bfloat16_rn(x[i]);
           named_bar_sync(3, 32 * kEpiWarps);
-          // rows of 256 bytes: 16 threads per row, 32 rows per pass
+          // rows of 256 bytes: 16 threads per row, 16 rows per pass
           const int tr = tid >> 4, tc = tid & 15;
 #pragma unroll
-          for (int pass = 0; pass < 2; ++pass) {
-            const int t = pass * 32 + tr;
+          for (int pass = 0; pass < 4; ++pass) {
+            const int t = pass * 16 + tr;
             if (t < n)
               *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + base + (size_t)t * o_tok + tc * 8) =
                   *reinterpret_cast<const uint4 *>(tile + t * VD + tc * 8);
@@ -992,7 +1005,7 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
   }
 }
 
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(NT, 1)
     chunk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, FfParams p) {
   extern __shared__ uint8_t smraw[];
@@ -1058,6 +1071,7 @@ __global__ void chunk_fused_setup_kernel(FfParams p) {
     mx = 0;
     p.ctl->counter = 0;
     p.ctl->abort = 0;
+    p.status[1] = GDN_PATH_FUSED;  // the workspace header's path word
   }
   for (int i = tid; i < p.n_chain * p.R; i += blockDim.x) p.ready[i] = 0;
   for (int i = tid; i < p.n_chain; i += blockDim.x) p.consumed[i] = 0;

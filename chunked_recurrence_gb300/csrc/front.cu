@@ -30,8 +30,19 @@ extern "C" int32_t gdn_version(void) { return (1 << 16) | 2; }
 
 extern "C" gdn_status gdn_workspace_reset(void *workspace, size_t workspace_bytes, void *stream) {
   if (!workspace || workspace_bytes < sizeof(int32_t)) return GDN_ERR_WORKSPACE;
-  if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), (cudaStream_t)stream) != cudaSuccess)
+  const size_t n = workspace_bytes >= 2 * sizeof(int32_t) ? 2 * sizeof(int32_t) : sizeof(int32_t);
+  if (cudaMemsetAsync(workspace, 0, n, (cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+extern "C" gdn_status gdn_workspace_path(const void *workspace, int32_t *path_out, void *stream) {
+  if (!workspace || !path_out) return GDN_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, (const int32_t *)workspace + 1, sizeof(v), cudaMemcpyDeviceToHost,
+                      (cudaStream_t)stream) != cudaSuccess ||
+      cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
     return GDN_ERR_CUDA;
+  *path_out = v;
   return GDN_OK;
 }
 

@@ -95,8 +95,19 @@ size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape);
  * shape. */
 size_t gdn_chunk_fwd_min_workspace_bytes(const gdn_shape *shape);
 
-/* Zero the status word at the start of `workspace` (stream-ordered). */
+/* Zero the status word and the path word at the start of `workspace` (stream-ordered). */
 gdn_status gdn_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
+
+/* The second 32-bit word of a workspace records which kernel path the last
+ * gdn_chunk_fwd that ran in it took, when that path writes it:
+ * GDN_PATH_FUSED for the fused persistent kernel (bf16, K = V = 128).  The other
+ * paths leave the word as they found it, and gdn_workspace_reset clears it, so
+ * after a reset a value of 0 means another path ran. */
+#define GDN_PATH_FUSED 1
+
+/* Copy the path word (see GDN_PATH_FUSED) of `workspace` to *path_out (host) and
+ * synchronise `stream`. */
+gdn_status gdn_workspace_path(const void *workspace, int32_t *path_out, void *stream);
 
 /* Copy the status word at the start of `workspace` to *status_out (host) and
  * synchronise `stream`.  *status_out is a gdn_status: GDN_OK when no device

@@ -62,11 +62,22 @@ def make_case(lengths, Hqk, Hv, K, V, dtype, gates="paper", h0=False, seed=0, B=
 
 
 def run_gpu(crg, c, simt=False, l2norm=True, o_f32=False, split=False):
+    """gdn_chunk_fwd in a fresh workspace; checks that bf16 K = V = 128 calls (without
+    simt / split) really ran the fused kernel and that no other call did."""
     d = lambda t: None if t is None else t.to(DEV)
-    o, hT = crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]),
-                              d(c["cu"]), c["scale"], l2norm, B=c["B"], simt=simt, o_f32=o_f32,
-                              split=split)
+    q, k, v = d(c["q"]), d(c["k"]), d(c["v"])
+    sh = crg.make_shape(q, k, v, d(c["cu"]), c["B"])
+    nb = crg.gdn_chunk_fwd_workspace_bytes(sh)
+    if split:
+        nb = max(nb, crg.split_workspace_bytes(sh))
+    ws = crg.Workspace(nb, DEV)
+    ws.reset()
+    o, hT = crg.gdn_chunk_fwd(q, k, v, d(c["g"]), d(c["beta"]), d(c["h0"]), d(c["cu"]), c["scale"],
+                              l2norm, B=c["B"], simt=simt, o_f32=o_f32, split=split, workspace=ws)
     torch.cuda.synchronize()
+    fused_shape = c["dtype"] == "bf16" and q.shape[-1] == 128 and v.shape[-1] == 128
+    assert (ws.path() == crg.GDN_PATH_FUSED) == (fused_shape and not simt and not split)
+    assert ws.status() == 0
     return o.cpu(), hT.cpu()
 
 
@@ -521,11 +532,12 @@ def test_fused_timeout_reported_then_context_usable(crg):
     ws.reset()
     crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]), d(c["cu"]),
                       c["scale"], True, workspace=ws, _test_no_wait=True)
+    assert ws.path() == crg.GDN_PATH_FUSED
     assert ws.status() == crg.GDN_ERR_TIMEOUT
     ws.reset()
     o, hT = crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]),
                               d(c["cu"]), c["scale"], True, workspace=ws)
-    assert ws.status() == 0
+    assert ws.status() == 0 and ws.path() == crg.GDN_PATH_FUSED
     ro, rh = run_oracle(c)
     assert_close(o.cpu(), ro, "bf16", "o after a timeout")
     assert_close(hT.cpu(), rh, "bf16", "h_T after a timeout")
