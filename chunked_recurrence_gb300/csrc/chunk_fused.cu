@@ -142,6 +142,9 @@ __device__ __forceinline__ int ld_acquire(const int32_t *p) {
 __device__ __forceinline__ void st_release(int32_t *p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed(int32_t *p, int v) {
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // Waits until *flag >= want (acquire), polling at most `limit` times; gives up early when
@@ -256,8 +259,12 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid, Bar bar) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) y[m][c] = (rg + 8 * m == 4 * cg + c) ? 1.f : 0.f;
   const float *xr = X + rg * kXP;
+  // Y_kj = 0 for j > k: the warp's 16 columns (16 w .. 16 w + 15) take no update from the
+  // steps before its first column (a warp-uniform skip)
+  const int k0 = (tid >> 5) * 16;
 #pragma unroll
   for (int k = 0; k < C - 1; ++k) {
+    if (k < k0) continue;
     float yk[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) yk[c] = __shfl_sync(0xffffffffu, y[k >> 3][c], (k & 7) | (lane & 24));
@@ -291,9 +298,12 @@ __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.
 // every committed group has completed its writes
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// decoded unit in the lane's small region (ints): valid (1) or none left (-1), chain, position,
-// v-head, tokens, first token
+// decoded unit (ints): valid (1) or none left (-1), chain, position, v-head, tokens, first token
 constexpr int U_VALID = 0, U_CI = 1, U_POS = 2, U_H = 3, U_N = 4, U_T0 = 5, U_WORDS = 8;
+// mbarriers of a builder lane (in its small region, 8-byte aligned)
+constexpr int BB_LD = 0, BB_MMA = 1, BB_CLAIMED = 2 /* two: even and odd units */, BB_STAGED_A = 4,
+              BB_UFREE = 5, BB_STAGED_B = 6, BB_COUNT = 7;
+static_assert(SM_BAR * 4 + BB_COUNT * 8 <= 3072, "lane barriers fit the small region");
 
 // Claims units until one is real (a chain's stream can be shorter than the longest).
 __device__ __forceinline__ void claim_unit(const FfParams &p, int64_t total, int *u_out) {
@@ -318,92 +328,152 @@ __device__ __forceinline__ void claim_unit(const FfParams &p, int64_t total, int
   u_out[U_VALID] = valid;
 }
 
-__device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                             FfParams &p, uint8_t *sm, uint32_t tm, int lane_id) {
+// A bounded wait that also gives up once any CTA has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint32_t limit, const FfCtl *ctl) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && *(volatile const int32_t *)&ctl->abort) return false;
+    if (i > 64) __nanosleep(32);
+  }
+  return false;
+}
+
+struct LaneRefs {
+  float *smf;
+  int *ring;  // [2][U_WORDS]: units 2 i and 2 i + 1 alternate
+  float *blast;
+  uint64_t *bars;
+};
+__device__ __forceinline__ LaneRefs lane_refs(uint8_t *sm) {
+  LaneRefs r;
+  r.smf = reinterpret_cast<float *>(sm + B_SMALL);
+  r.ring = reinterpret_cast<int *>(r.smf + SM_MISC);
+  r.blast = r.smf + SM_MISC + 2 * U_WORDS;
+  r.bars = reinterpret_cast<uint64_t *>(r.smf + SM_BAR);
+  return r;
+}
+
+// The helper of a builder lane (one thread): claims units two ahead, loads each unit's
+// k, q, v tiles by TMA, writes each staged record to its ring slot by bulk copies (after the
+// chain has consumed the slot's previous record) and releases the slot's ready flag once the
+// copies have landed.  The lane itself only computes and stages.
+__device__ void builder_helper(const CUtensorMap *tm_q, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                               FfParams &p, uint8_t *sm) {
+  LaneRefs L = lane_refs(sm);
+  uint64_t *ld_bar = L.bars + BB_LD;
+  const int64_t total = (int64_t)p.n_chain * (int64_t)p.ctl->maxN;
+  auto issue_tma = [&](const int *u) {
+    const int h = u[U_H], qh = h / (p.Hv / p.Hqk);
+    const int32_t tt = u[U_T0];
+    mbar_arrive_expect_tx(ld_bar, 6 * 8192);
+    tma_load_3d(sm + B_KQ, tm_k, ld_bar, 0, qh, tt);
+    tma_load_3d(sm + B_KQ + 16384, tm_k, ld_bar, 64, qh, tt);
+    tma_load_3d(sm + B_KQ + 8192, tm_q, ld_bar, 0, qh, tt);
+    tma_load_3d(sm + B_KQ + 24576, tm_q, ld_bar, 64, qh, tt);
+    tma_load_3d(sm + B_V, tm_v, ld_bar, 0, h, tt);
+    tma_load_3d(sm + B_V + 8192, tm_v, ld_bar, 64, h, tt);
+  };
+  claim_unit(p, total, L.ring);
+  mbar_arrive(L.bars + BB_CLAIMED);
+  claim_unit(p, total, L.ring + U_WORDS);
+  mbar_arrive(L.bars + BB_CLAIMED + 1);
+  int tma_issued = 0;
+  if (L.ring[U_VALID] > 0) {
+    issue_tma(L.ring);
+    tma_issued = 1;
+  }
+  bool ok = true;
+  for (int i = 0;; ++i) {
+    int *u = L.ring + (i & 1) * U_WORDS;
+    if (u[U_VALID] <= 0) break;
+    const int ci = u[U_CI], pos = u[U_POS], slot = pos % p.R;
+    uint8_t *rec = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES;
+    ok = wait_bar(L.bars + BB_STAGED_A, i & 1, p.spin, p.ctl) &&
+         wait_flag_ge(p.consumed + ci, pos - p.R + 1, p.spin, p.ctl);
+    if (!ok) break;
+    bulk_store(rec + REC_UTH, sm + B_V, 16384);
+    bulk_store(rec + REC_UTL, sm + B_X, 16384);
+    bulk_commit();
+    bulk_store(rec + REC_WN, sm + B_TH, 32768);
+    bulk_store(rec + REC_QT, sm + B_KQ, 8192);
+    bulk_store(rec + REC_QT + 8192, sm + B_KQ + 16384, 8192);
+    bulk_commit();
+    *reinterpret_cast<float *>(rec + REC_VEC) = *L.blast;
+    bulk_wait_read1();  // the U images have been read: the lane may put (P U)^T there
+    mbar_arrive(L.bars + BB_UFREE);
+    claim_unit(p, total, u);  // unit i + 2 into the entry unit i used
+    mbar_arrive(L.bars + BB_CLAIMED + (i & 1));
+    if (!wait_bar(L.bars + BB_STAGED_B, i & 1, p.spin, p.ctl)) {
+      ok = false;
+      break;
+    }
+    bulk_store(rec + REC_OP, sm + B_V, 32768);
+    bulk_commit();
+    bulk_wait_read0();  // the lane's tiles are free for the next unit
+    const int *un = L.ring + ((i + 1) & 1) * U_WORDS;
+    if (un[U_VALID] > 0) {
+      issue_tma(un);
+      ++tma_issued;
+    }
+    bulk_wait_all();
+    fence_proxy_async_all();
+    __threadfence();
+    st_release(p.ready + (size_t)ci * p.R + slot, pos + 1);
+  }
+  if (!ok) give_up(p, nullptr);
+  bulk_wait_all();  // no copy may still read shared memory when the CTA exits
+  if (tma_issued > 0) (void)mbar_wait(ld_bar, (tma_issued - 1) & 1, kSpinDefault);
+}
+
+__device__ void builder_lane(FfParams &p, uint8_t *sm, uint32_t tm, int lane_id) {
   const int tid = threadIdx.x - 128 * lane_id;  // 0..127 inside the lane
   const int lane = tid & 31, wq = tid >> 5;      // wq = TMEM lane quarter of this warp
   const uint32_t bid = 1 + lane_id;              // named barrier of the lane
   auto bar = [&]() { named_bar_sync(bid, 128); };
-  float *smf = reinterpret_cast<float *>(sm + B_SMALL);
+  LaneRefs L = lane_refs(sm);
+  float *smf = L.smf;
   float *gam = smf + SM_GAM, *bex = smf + SM_BEX, *dec = smf + SM_DEC, *alf = smf + SM_ALF;
   float *kinv = smf + SM_KINV, *qinv = smf + SM_QINV, *bet = smf + SM_BET, *alpha = smf + SM_ALPHA;
   float *dk = smf + SM_DK;
-  int *ucur = reinterpret_cast<int *>(smf + SM_MISC), *unext = ucur + U_WORDS;
-  float *blast_s = smf + SM_MISC + 2 * U_WORDS;
-  uint64_t *ld_bar = reinterpret_cast<uint64_t *>(smf + SM_BAR), *mma_bar = ld_bar + 1;
+  uint64_t *ld_bar = L.bars + BB_LD, *mma_bar = L.bars + BB_MMA;
   float *X = reinterpret_cast<float *>(sm + B_X);
   const uint32_t sb = smem_u32(sm);
   const uint32_t lq = (uint32_t)(wq * 32) << 16;
   const uint32_t R0 = tm, R1 = tm + 128;
-  const int64_t total = (int64_t)p.n_chain * (int64_t)p.ctl->maxN;
-  // TMA of a unit's k, q, v tiles (thread 0) and its gates (every thread)
-  auto issue_loads = [&](const int *u) {
-    const int h = u[U_H], n = u[U_N], qh = h / (p.Hv / p.Hqk);
-    const int64_t t0 = u[U_T0];
-    if (tid == 0) {
-      const int32_t tt = (int32_t)t0;
-      mbar_arrive_expect_tx(ld_bar, 6 * 8192);
-      tma_load_3d(sm + B_KQ, tm_k, ld_bar, 0, qh, tt);
-      tma_load_3d(sm + B_KQ + 16384, tm_k, ld_bar, 64, qh, tt);
-      tma_load_3d(sm + B_KQ + 8192, tm_q, ld_bar, 0, qh, tt);
-      tma_load_3d(sm + B_KQ + 24576, tm_q, ld_bar, 64, qh, tt);
-      tma_load_3d(sm + B_V, tm_v, ld_bar, 0, h, tt);
-      tma_load_3d(sm + B_V + 8192, tm_v, ld_bar, 64, h, tt);
-    }
-    // zero past the chunk's end: beta = 0 keeps those rows out of every result, g = 0 keeps
-    // the decays of the real rows
-    if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
-    else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
-  };
-  if (tid == 0) {
-    mbar_init(ld_bar, 1);
-    mbar_init(mma_bar, 1);
-    fence_mbar_init();
-    claim_unit(p, total, ucur);
-  }
-  bar();
-  if (ucur[U_VALID] > 0) issue_loads(ucur);
-  uint32_t ldp = 0, mp = 0;
-  int pend_ci = -1, pend_slot = 0, pend_pos = 0;  // record written, its ready flag not yet released
-  // thread 0 releases the pending record once its bulk stores have completed
-  auto release_pending = [&]() {
-    if (tid == 0 && pend_ci >= 0) {
-      bulk_wait_all();
-      fence_proxy_async_all();
-      __threadfence();
-      st_release(p.ready + (size_t)pend_ci * p.R + pend_slot, pend_pos + 1);
-    }
-    pend_ci = -1;
-  };
-  // wait (thread 0) on an mbarrier phase; every thread learns the outcome
-  auto lane_wait = [&](uint64_t *b, uint32_t &ph) -> bool {
+  uint32_t mp = 0;
+  // thread 0 waits on an mbarrier phase; every thread learns the outcome.  An MMA or copy
+  // still in flight after a give-up lands before the lane leaves.
+  auto lane_wait = [&](uint64_t *b, uint32_t parity, bool drain) -> bool {
     bool ok = true;
-    if (tid == 0) ok = mbar_wait(b, ph & 1, p.spin);
-    const bool bad = named_bar_any(bid, 128, !ok);
-    if (bad) {
+    if (tid == 0) ok = wait_bar(b, parity, p.spin, p.ctl);
+    if (named_bar_any(bid, 128, !ok)) {
       if (tid == 0) {
         give_up(p, nullptr);
-        (void)mbar_wait(b, ph & 1, kSpinDefault);  // copies / MMAs in flight land first
+        if (drain) (void)mbar_wait(b, parity, kSpinDefault);
       }
       return false;
     }
-    ++ph;
     return true;
   };
-  bool failed = false;
+  // gates of a unit: zero past the chunk's end (beta = 0 keeps those rows out of every result,
+  // g = 0 keeps the decays of the real rows)
+  auto gate_of = [&](const int *u) -> float {
+    const int n = u[U_N], h = u[U_H];
+    const int64_t t0 = u[U_T0];
+    if (tid < C) return (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
+    return (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
+  };
+  float gnext = 0.f;
 #pragma unroll 1
-  for (;;) {
-    bar();
-    if (ucur[U_VALID] <= 0) break;
-    const int ci = ucur[U_CI], pos = ucur[U_POS], n = ucur[U_N];
-    const int slot = pos % p.R;
-    uint8_t *rec = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES;
-    // the next unit is claimed and decoded by another warp while this one is built
-    if (tid == 32) claim_unit(p, total, unext);
-    if (!lane_wait(ld_bar, ldp)) {
-      failed = true;
-      break;
-    }
+  for (int i = 0;; ++i) {
+    if (!lane_wait(L.bars + BB_CLAIMED + (i & 1), (i >> 1) & 1, false)) break;
+    const int *u = L.ring + (i & 1) * U_WORDS;
+    if (u[U_VALID] <= 0) break;
+    const int n = u[U_N];
+    const float gv = i == 0 ? gate_of(u) : gnext;
+    if (tid < C) gam[tid] = gv;
+    else bet[tid - C] = gv;
+    if (!lane_wait(ld_bar, i & 1, false)) break;
 
     // ---- 1/|k| and 1/|q| (two threads per token)
     {
@@ -448,8 +518,8 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
       float incl = g0 + g1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
+        const float uu = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += uu;
       }
       const float last = __shfl_sync(0xffffffffu, incl, 31);
       const float ga = incl - g1, gb = incl;
@@ -460,15 +530,12 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
       alf[2 * lane] = expf(g0);
       alf[2 * lane + 1] = expf(g1);
       if (lane == 31) {
-        *blast_s = expf(last);
+        *L.blast = expf(last);
         alf[C] = 1.f;
       }
     }
-    release_pending();  // the previous unit's record: its stores have had a whole phase to land
-    if (!lane_wait(mma_bar, mp)) {
-      failed = true;
-      break;
-    }
+    if (!lane_wait(mma_bar, mp & 1, true)) break;
+    ++mp;
     tc_fence_after();
     if (tid < C) {
       alpha[tid] = p.scale * bex[tid] * qinv[tid];
@@ -476,23 +543,23 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
     }
     // ---- rows of K K^T (lanes 0-63) become rows of A; rows of Q K^T (lanes 64-127) rows of P
     {
-      const int i = tid & 63;
+      const int ii = tid & 63;
       const bool isq = tid >= 64;
       float r64[64];
       tmem_ld64(R0 + lq, r64);
       tmem_wait_ld();
-      const float bi = isq ? p.scale * qinv[i] : bet[i] * kinv[i];
+      const float bi = isq ? p.scale * qinv[ii] : bet[ii] * kinv[ii];
       // Gamma_ij = prod_{m=j+1..i} exp(g_m) for j < i: a running product walking j down
       float gprod = 1.f;
 #pragma unroll
       for (int j = C - 1; j >= 0; --j) {
         const float aj = alf[j + 1], kj = kinv[j];
-        if (j < i) gprod *= aj;
-        const bool keep = isq ? (j <= i) : (j < i);
+        if (j < ii) gprod *= aj;
+        const bool keep = isq ? (j <= ii) : (j < ii);
         r64[j] = keep ? bi * kj * gprod * r64[j] : 0.f;
       }
       if (!isq) {
-        float4 *xr = reinterpret_cast<float4 *>(X + i * kXP);
+        float4 *xr = reinterpret_cast<float4 *>(X + ii * kXP);
 #pragma unroll
         for (int m = 0; m < C / 4; ++m) xr[m] = make_float4(r64[4 * m], r64[4 * m + 1], r64[4 * m + 2], r64[4 * m + 3]);
       } else {
@@ -501,8 +568,8 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) split2(r64[c0 + 2 * e], r64[c0 + 2 * e + 1], hw[e], lw[e]);
-          *reinterpret_cast<uint4 *>(sm + B_PH + sw128_off(i, c0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4 *>(sm + B_PL + sw128_off(i, c0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4 *>(sm + B_PH + sw128_off(ii, c0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4 *>(sm + B_PL + sw128_off(ii, c0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
     }
@@ -557,10 +624,8 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
                   id, ks > 0);
       umma_commit(mma_bar);
     }
-    if (!lane_wait(mma_bar, mp)) {
-      failed = true;
-      break;
-    }
+    if (!lane_wait(mma_bar, mp & 1, true)) break;
+    ++mp;
     tc_fence_after();
     // ---- rows of U (hi + lo) and W (bf16) into shared memory (an M = 64 result: lanes 0-15
     //      of each quarter); k rows become diag(d/|k|) k for What = W^T diag(d/|k|) K
@@ -569,40 +634,40 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
       const bool has_row = lane < 16;
 #pragma unroll 1
       for (int hv = 0; hv < 2; ++hv) {
-        float u[64];
-        tmem_ld64(R0 + lq + hv * 64, u);
+        float uu[64];
+        tmem_ld64(R0 + lq + hv * 64, uu);
         tmem_wait_ld();
         if (has_row) {
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 8) {
             uint32_t uh[4], ul[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) split2(u[c0 + 2 * e], u[c0 + 2 * e + 1], uh[e], ul[e]);
+            for (int e = 0; e < 4; ++e) split2(uu[c0 + 2 * e], uu[c0 + 2 * e + 1], uh[e], ul[e]);
             const uint32_t off = hv * 8192 + sw128_off(rr, c0);
             *reinterpret_cast<uint4 *>(sm + B_V + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
             *reinterpret_cast<uint4 *>(sm + B_X + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
           }
         }
-        tmem_ld64(R1 + lq + hv * 64, u);
+        tmem_ld64(R1 + lq + hv * 64, uu);
         tmem_wait_ld();
         if (has_row) {
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 8)
             *reinterpret_cast<uint4 *>(sm + B_TH + hv * 8192 + sw128_off(rr, c0)) =
-                make_uint4(pack_bf16(u[c0], u[c0 + 1]), pack_bf16(u[c0 + 2], u[c0 + 3]),
-                           pack_bf16(u[c0 + 4], u[c0 + 5]), pack_bf16(u[c0 + 6], u[c0 + 7]));
+                make_uint4(pack_bf16(uu[c0], uu[c0 + 1]), pack_bf16(uu[c0 + 2], uu[c0 + 3]),
+                           pack_bf16(uu[c0 + 4], uu[c0 + 5]), pack_bf16(uu[c0 + 6], uu[c0 + 7]));
         }
       }
       {
         const int r = tid >> 1, hf = tid & 1;
-        const float s = dk[r];
+        const float sc = dk[r];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint4 *ptr = reinterpret_cast<uint4 *>(sm + B_KQ + hf * 16384 + sw128_off(r, j * 8));
           const uint4 kr = *ptr;
           const float2 a = unpack_bf16(kr.x), b = unpack_bf16(kr.y), c = unpack_bf16(kr.z), d = unpack_bf16(kr.w);
-          *ptr = make_uint4(pack_bf16(s * a.x, s * a.y), pack_bf16(s * b.x, s * b.y), pack_bf16(s * c.x, s * c.y),
-                            pack_bf16(s * d.x, s * d.y));
+          *ptr = make_uint4(pack_bf16(sc * a.x, sc * a.y), pack_bf16(sc * b.x, sc * b.y), pack_bf16(sc * c.x, sc * c.y),
+                            pack_bf16(sc * d.x, sc * d.y));
         }
       }
     }
@@ -634,27 +699,24 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
                   id_w, ks > 0);
       umma_commit(mma_bar);
     }
-    {
-      // the MMAs, and the ring slot free (its previous record consumed) before any record store
-      bool ok = true;
-      if (tid == 0) {
-        ok = wait_flag_ge(p.consumed + ci, pos - p.R + 1, p.spin, p.ctl);
-        ok = mbar_wait(mma_bar, mp & 1, ok ? p.spin : kSpinDefault) && ok;
-      }
-      if (named_bar_any(bid, 128, !ok)) {
-        if (tid == 0) give_up(p, nullptr);
-        failed = true;
-        break;
-      }
-      ++mp;
+    // the next unit's gates, loaded while the MMAs run (its claim was made a unit earlier)
+    if (!lane_wait(L.bars + BB_CLAIMED + ((i + 1) & 1), ((i + 1) >> 1) & 1, false)) {
+      if (tid == 0) (void)mbar_wait(mma_bar, mp & 1, kSpinDefault);
+      break;
     }
+    {
+      const int *un = L.ring + ((i + 1) & 1) * U_WORDS;
+      if (un[U_VALID] > 0) gnext = gate_of(un);
+    }
+    if (!lane_wait(mma_bar, mp & 1, true)) break;
+    ++mp;
     tc_fence_after();
-    // ---- the record, staged in shared memory and written by bulk copies:
+    // ---- the record, staged in shared memory for the helper's bulk copies:
     // (1) Ut = diag(d/|k|) U as hi + lo, in place over the U images (16-byte pieces)
 #pragma unroll 2
     for (int c16 = tid; c16 < 1024; c16 += 128) {
       const uint32_t off = (uint32_t)c16 * 16;
-      const float s = dk[(off & 8191) >> 7];
+      const float sc = dk[(off & 8191) >> 7];
       uint4 *ph = reinterpret_cast<uint4 *>(sm + B_V + off), *pl = reinterpret_cast<uint4 *>(sm + B_X + off);
       const uint4 h4 = *ph, l4 = *pl;
       const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, lw[4] = {l4.x, l4.y, l4.z, l4.w};
@@ -662,7 +724,7 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 a = unpack_bf16(hw[e]), b = unpack_bf16(lw[e]);
-        split2(s * (a.x + b.x), s * (a.y + b.y), oh[e], ol[e]);
+        split2(sc * (a.x + b.x), sc * (a.y + b.y), oh[e], ol[e]);
       }
       *ph = make_uint4(oh[0], oh[1], oh[2], oh[3]);
       *pl = make_uint4(ol[0], ol[1], ol[2], ol[3]);
@@ -705,19 +767,10 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
     fence_proxy_async_smem();
     tc_fence_before();
     bar();
-    if (tid == 0) {
-      bulk_store(rec + REC_UTH, sm + B_V, 16384);
-      bulk_store(rec + REC_UTL, sm + B_X, 16384);
-      bulk_commit();
-      bulk_store(rec + REC_WN, sm + B_TH, 32768);
-      bulk_store(rec + REC_QT, sm + B_KQ, 8192);
-      bulk_store(rec + REC_QT + 8192, sm + B_KQ + 16384, 8192);
-      bulk_commit();
-      *reinterpret_cast<float *>(rec + REC_VEC) = *blast_s;
-      bulk_wait_read1();  // the U images have been read: they take (P U)^T next
-    }
-    bar();
-    // (4) (P U)^T fp32, row v = m: 16-byte piece j at (j ^ (v % 16)) of its 256-byte row
+    if (tid == 0) mbar_arrive(L.bars + BB_STAGED_A);
+    // (4) (P U)^T fp32, row v = m: 16-byte piece j at (j ^ (v % 16)) of its 256-byte row, over
+    //     the U images once the helper's copies have read them
+    if (!lane_wait(L.bars + BB_UFREE, i & 1, false)) break;
     {
       float x[64];
       tmem_ld64(R0 + lq, x);
@@ -731,24 +784,8 @@ __device__ void builder_lane(const CUtensorMap *tm_q, const CUtensorMap *tm_k, c
     fence_proxy_async_smem();
     tc_fence_before();
     bar();
-    if (tid == 0) {
-      bulk_store(rec + REC_OP, sm + B_V, 32768);
-      bulk_commit();
-    }
-    pend_ci = ci;
-    pend_slot = slot;
-    pend_pos = pos;
-    // ---- the next unit: its tiles go where this record was staged once the copies have read it
-    bar();  // unext is written
-    if (tid == 0) bulk_wait_read0();
-    bar();
-    if (tid == 0)
-      for (int w = 0; w < U_WORDS; ++w) ucur[w] = unext[w];
-    bar();
-    if (ucur[U_VALID] > 0) issue_loads(ucur);
+    if (tid == 0) mbar_arrive(L.bars + BB_STAGED_B);
   }
-  if (!failed) release_pending();
-  if (tid == 0) bulk_wait_all();  // no copy may still read shared memory when the CTA exits
 }
 
 // ============================================================ chain CTA
@@ -943,15 +980,9 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
 #pragma unroll
           for (int m = 0; m < 16; ++m) dst[m] = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
         }
-        // ---- the output of this chunk: o[t][v] = O^T[v][t] + (P U)^T[v][t] for tokens [32 g, +32)
-        const bool got = wait_flag_ge(p.ready + (size_t)ci * p.R + slot, pos + 1, p.spin, p.ctl) &&
-                         mbar_wait_spin(&sh.out_done[b], (pos >> 1) & 1, p.spin, abort_flag);
-        // the epilogue warps agree before any of them leaves: one that left alone would
-        // strand the others at the named barriers below
-        if (named_bar_any(3, 32 * kEpiWarps, !got)) {
-          ok = false;
-          break;
-        }
+        // (P U)^T of this chunk from the ring slot, loaded now so that the loads overlap the
+        // wait for the output MMA.  The slot's ready flag was acquired by the loader before its
+        // copies, whose completion these warps observed on full[st]: the reads see the record.
         float x[32];
         {
           const uint8_t *prow = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES + REC_OP + (size_t)v * 256;
@@ -963,6 +994,14 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
             x[4 * jj + 2] = a.z;
             x[4 * jj + 3] = a.w;
           }
+        }
+        // ---- the output of this chunk: o[t][v] = O^T[v][t] + (P U)^T[v][t] for tokens [32 g, +32)
+        const bool got = mbar_wait_spin(&sh.out_done[b], (pos >> 1) & 1, p.spin, abort_flag);
+        // the epilogue warps agree before any of them leaves: one that left alone would
+        // strand the others at the named barriers below
+        if (named_bar_any(3, 32 * kEpiWarps, !got)) {
+          ok = false;
+          break;
         }
         tc_fence_after();
         {
@@ -996,9 +1035,11 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
                   *reinterpret_cast<const uint4 *>(tile + t * VD + tc * 8);
           }
         }
-        // every epilogue thread has read the slot and the tile: both may be reused
+        // every epilogue thread has read the slot and the tile: both may be reused.  The
+        // flag orders nothing but loads that have returned, so it needs no release fence
+        // (which would wait for the output stores above).
         named_bar_sync(3, 32 * kEpiWarps);
-        if (tid == 0) st_release(p.consumed + ci, pos + 1);
+        if (tid == 0) st_relaxed(p.consumed + ci, pos + 1);
       }
     }
     if (!ok && lane == 0) give_up(p, abort_flag);
@@ -1029,6 +1070,12 @@ __global__ void __launch_bounds__(NT, 1)
         mbar_init(&sh.out_free[i], kEpiWarps);
       }
     }
+    if (!is_chain) {
+      for (int l = 0; l < 2; ++l) {
+        uint64_t *bars = lane_refs(sm + l * kLane).bars;
+        for (int b = 0; b < BB_COUNT; ++b) mbar_init(bars + b, 1);
+      }
+    }
     sh.abort = 0;
     sh.mma_bar = nullptr;
     sh.mma_par = 0;
@@ -1046,7 +1093,9 @@ __global__ void __launch_bounds__(NT, 1)
     chain_cta(&tm_k, p, sm, tm, sh, blockIdx.x);
   } else if (warp < 8) {
     const int lane_id = warp >> 2;
-    builder_lane(&tm_q, &tm_k, &tm_v, p, sm + lane_id * kLane, tm + lane_id * 256, lane_id);
+    builder_lane(p, sm + lane_id * kLane, tm + lane_id * 256, lane_id);
+  } else if ((tid & 31) == 0) {  // warps 8 and 9: the helpers of lanes 0 and 1
+    builder_helper(&tm_q, &tm_k, &tm_v, p, sm + (warp - 8) * kLane);
   }
   __syncthreads();
   if (is_chain && tid == 0 && sh.abort) {
