@@ -69,13 +69,14 @@ constexpr uint32_t REC_UTH = 32768;   // Ut hi: [2 v-halves][64 token rows][128 
 constexpr uint32_t REC_UTL = 49152;   // Ut lo, same layout
 constexpr uint32_t REC_QT = 65536;    // Qt^T: [128 k rows][128 B = 64 tokens] (B operand, N-major)
 constexpr uint32_t REC_VEC = 81920;   // b_last (fp32) and padding
-constexpr uint32_t REC_SMEM = 82944;  // bytes the chain copies to shared memory
-constexpr uint32_t REC_OP = 82944;    // (P U)^T: [128 v][64 tokens] fp32, read by the chain's output warps
-constexpr uint32_t REC_BYTES = 115712;
+constexpr uint32_t REC_K = 82944;     // raw k: [2 f-halves][64 token rows][128 B] (B operand, N-major)
+constexpr uint32_t REC_SMEM = 99328;  // bytes the chain copies to shared memory
+constexpr uint32_t REC_OP = 99328;    // (P U)^T: [128 v][64 tokens] fp32, read by the chain's output warps
+constexpr uint32_t REC_BYTES = 132096;
 
-// chain stage in shared memory: the record's first REC_SMEM bytes, then the raw k tile
-constexpr uint32_t ST_K = REC_SMEM;   // [2 f-halves][64 token rows][128 B]
-constexpr uint32_t kStage = REC_SMEM + 16384;
+// chain stage in shared memory: the record's first REC_SMEM bytes
+constexpr uint32_t ST_K = REC_K;
+constexpr uint32_t kStage = REC_SMEM;
 constexpr int kStages = 2;
 // chain TMEM columns
 constexpr uint32_t T_DCH = 0;    // 2 x 128: D = Ut^T K - S What, lane = v, column = key feature
@@ -302,7 +303,7 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 constexpr int U_VALID = 0, U_CI = 1, U_POS = 2, U_H = 3, U_N = 4, U_T0 = 5, U_WORDS = 8;
 // mbarriers of a builder lane (in its small region, 8-byte aligned)
 constexpr int BB_LD = 0, BB_MMA = 1, BB_CLAIMED = 2 /* two: even and odd units */, BB_STAGED_A = 4,
-              BB_UFREE = 5, BB_STAGED_B = 6, BB_COUNT = 7;
+              BB_UFREE = 5, BB_STAGED_B = 6, BB_KSAVED = 7, BB_COUNT = 8;
 static_assert(SM_BAR * 4 + BB_COUNT * 8 <= 3072, "lane barriers fit the small region");
 
 // Claims units until one is real (a chain's stream can be shorter than the longest).
@@ -388,9 +389,19 @@ __device__ void builder_helper(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
     if (u[U_VALID] <= 0) break;
     const int ci = u[U_CI], pos = u[U_POS], slot = pos % p.R;
     uint8_t *rec = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES;
-    ok = wait_bar(L.bars + BB_STAGED_A, i & 1, p.spin, p.ctl) &&
-         wait_flag_ge(p.consumed + ci, pos - p.R + 1, p.spin, p.ctl);
+    // the slot is free and the unit's tiles have landed: the raw k rows go to the record
+    // before the lane scales them in place
+    ok = wait_flag_ge(p.consumed + ci, pos - p.R + 1, p.spin, p.ctl) && wait_bar(ld_bar, i & 1, p.spin, p.ctl);
     if (!ok) break;
+    bulk_store(rec + REC_K, sm + B_KQ, 8192);
+    bulk_store(rec + REC_K + 8192, sm + B_KQ + 16384, 8192);
+    bulk_commit();
+    bulk_wait_read0();
+    mbar_arrive(L.bars + BB_KSAVED);
+    if (!wait_bar(L.bars + BB_STAGED_A, i & 1, p.spin, p.ctl)) {
+      ok = false;
+      break;
+    }
     bulk_store(rec + REC_UTH, sm + B_V, 16384);
     bulk_store(rec + REC_UTL, sm + B_X, 16384);
     bulk_commit();
@@ -464,6 +475,7 @@ __device__ void builder_lane(FfParams &p, uint8_t *sm, uint32_t tm, int lane_id)
     return (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
   };
   float gnext = 0.f;
+  bool failed_mid = false;
 #pragma unroll 1
   for (int i = 0;; ++i) {
     if (!lane_wait(L.bars + BB_CLAIMED + (i & 1), (i >> 1) & 1, false)) break;
@@ -523,6 +535,8 @@ __device__ void builder_lane(FfParams &p, uint8_t *sm, uint32_t tm, int lane_id)
       }
       const float last = __shfl_sync(0xffffffffu, incl, 31);
       const float ga = incl - g1, gb = incl;
+      gam[2 * lane] = ga;  // the inclusive cumulative sum from here on
+      gam[2 * lane + 1] = gb;
       bex[2 * lane] = expf(ga);
       bex[2 * lane + 1] = expf(gb);
       dec[2 * lane] = expf(last - ga);
@@ -549,14 +563,12 @@ __device__ void builder_lane(FfParams &p, uint8_t *sm, uint32_t tm, int lane_id)
       tmem_ld64(R0 + lq, r64);
       tmem_wait_ld();
       const float bi = isq ? p.scale * qinv[ii] : bet[ii] * kinv[ii];
-      // Gamma_ij = prod_{m=j+1..i} exp(g_m) for j < i: a running product walking j down
-      float gprod = 1.f;
+      const float gi = gam[ii];
+      // Gamma_ij = exp(gamma_i - gamma_j) <= 1 for j <= i (every g <= 0), each independent
 #pragma unroll
-      for (int j = C - 1; j >= 0; --j) {
-        const float aj = alf[j + 1], kj = kinv[j];
-        if (j < ii) gprod *= aj;
+      for (int j = 0; j < C; ++j) {
         const bool keep = isq ? (j <= ii) : (j < ii);
-        r64[j] = keep ? bi * kj * gprod * r64[j] : 0.f;
+        r64[j] = keep ? bi * kinv[j] * expf(gi - gam[j]) * r64[j] : 0.f;
       }
       if (!isq) {
         float4 *xr = reinterpret_cast<float4 *>(X + ii * kXP);
@@ -658,7 +670,9 @@ __device__ void builder_lane(FfParams &p, uint8_t *sm, uint32_t tm, int lane_id)
                            pack_bf16(uu[c0 + 4], uu[c0 + 5]), pack_bf16(uu[c0 + 6], uu[c0 + 7]));
         }
       }
-      {
+      if (!lane_wait(L.bars + BB_KSAVED, i & 1, false)) {
+        failed_mid = true;
+      } else {
         const int r = tid >> 1, hf = tid & 1;
         const float sc = dk[r];
 #pragma unroll
@@ -671,6 +685,7 @@ __device__ void builder_lane(FfParams &p, uint8_t *sm, uint32_t tm, int lane_id)
         }
       }
     }
+    if (failed_mid) break;
     fence_proxy_async_smem();
     tc_fence_before();
     bar();
@@ -801,8 +816,7 @@ struct ChainShared {
 constexpr int kEpiWarps = 8;         // state and output warps of a chain CTA
 constexpr uint32_t CH_TILE = kStages * kStage;  // bf16 [64 tokens][128 v] output tile
 
-__device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uint32_t tm, ChainShared &sh,
-                          int ci) {
+__device__ void chain_cta(FfParams &p, uint8_t *sm, uint32_t tm, ChainShared &sh, int ci) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sb = smem_u32(sm);
   volatile int *abort_flag = &sh.abort;
@@ -811,22 +825,17 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
   if (warp == kEpiWarps) {
     // ===================================================== loads
     if (lane == 0) {
-      tma_prefetch_desc(tm_k);
       int pos = 0;
       bool ok = true;
       for (int r = 0; r < n_r && ok; ++r) {
-        const int j = ci + r * p.n_chain, s = j / p.Hv, h = j % p.Hv, qh = h / (p.Hv / p.Hqk);
-        const int nc = p.nch[j];
-        int64_t start, end;
-        seq_range(p.cu, p.row_T, s, start, end);
+        const int nc = p.nch[ci + r * p.n_chain];
         for (int c = 0; c < nc; ++c, ++pos) {
           const int st = pos % kStages;
-          if (pos >= kStages && !mbar_wait_spin(&sh.empty[st], ((pos - kStages) / kStages) & 1, p.spin, abort_flag)) {
-            ok = false;
-            break;
-          }
           const int slot = pos % p.R;
-          if (!wait_flag_ge(p.ready + (size_t)ci * p.R + slot, pos + 1, p.spin, p.ctl)) {
+          // the record's flag first (usually set long before), then the stage
+          if (!wait_flag_ge(p.ready + (size_t)ci * p.R + slot, pos + 1, p.spin, p.ctl) ||
+              (pos >= kStages &&
+               !mbar_wait_spin(&sh.empty[st], ((pos - kStages) / kStages) & 1, p.spin, abort_flag))) {
             ok = false;
             break;
           }
@@ -834,13 +843,10 @@ __device__ void chain_cta(const CUtensorMap *tm_k, FfParams &p, uint8_t *sm, uin
           uint8_t *sg = sm + st * kStage;
           const uint8_t *rec = p.ring + ((size_t)ci * p.R + slot) * REC_BYTES;
           const bool last = c == nc - 1;  // Ut lo is only read on a sequence's last chunk
-          mbar_arrive_expect_tx(&sh.full[st], REC_UTL + (REC_SMEM - REC_QT) + (last ? 16384u : 0u) + 16384);
+          mbar_arrive_expect_tx(&sh.full[st], REC_UTL + (REC_SMEM - REC_QT) + (last ? 16384u : 0u));
           bulk_load(sg, rec, REC_UTL, &sh.full[st]);
           bulk_load(sg + REC_QT, rec + REC_QT, REC_SMEM - REC_QT, &sh.full[st]);
           if (last) bulk_load(sg + REC_UTL, rec + REC_UTL, 16384, &sh.full[st]);
-          const int32_t tt = (int32_t)(start + (int64_t)c * C);
-          tma_load_3d(sg + ST_K, tm_k, &sh.full[st], 0, qh, tt);
-          tma_load_3d(sg + ST_K + 8192, tm_k, &sh.full[st], 64, qh, tt);
           sh.fills[st] += 1;
         }
       }
@@ -1090,7 +1096,7 @@ __global__ void __launch_bounds__(NT, 1)
   tc_fence_after();
   const uint32_t tm = tbase;
   if (is_chain) {
-    chain_cta(&tm_k, p, sm, tm, sh, blockIdx.x);
+    chain_cta(p, sm, tm, sh, blockIdx.x);
   } else if (warp < 8) {
     const int lane_id = warp >> 2;
     builder_lane(p, sm + lane_id * kLane, tm + lane_id * 256, lane_id);
