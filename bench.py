@@ -11,11 +11,11 @@ gates, conv with the carried inputs, L2 norm, recurrence) for a batch
 of 64 sequences of the same layer continuing from fp32 states, and the gated
 RMSNorm of the layer's o.
 
-gdn_chunk_fwd runs as two launches: a one-block set-up kernel (the ring flags
-and each chain's schedule) and chunk_fused_kernel, a persistent kernel in which
-per-head state chains are fed by chunk builders through an L2-resident ring; a
+gdn_chunk_fwd runs as two kernels (chunk_operand_kernel: every chunk's
+state-independent operands at once; chunk_scan_kernel: the state chain), so a
 step is four launches.  The roofline is reported for the gdn_chunk_fwd call.
-The two-kernel split path (GDN_FLAG_SPLIT) is timed beside it on the same inputs.
+The fused persistent kernel (GDN_FLAG_FUSED: per-head state chains fed by chunk
+builders through an L2-resident ring) is timed beside it on the same inputs.
 
 Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
 on the host cores instead, on a bounded sample of the same workload.
@@ -161,11 +161,11 @@ class ClockSampler:
 
 
 def _kernel_sha() -> str:
-    """Hash of the sources chunk_fused_kernel compiles from: a stored ncu traffic figure is
-    valid for these only."""
+    """Hash of the sources chunk_operand_kernel and chunk_scan_kernel compile from: a stored
+    ncu traffic figure is valid for these only."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_recurrence_gb300", "csrc")
-    for fn in ("chunk_common.cuh", "chunk_fused.cu", "common.cuh", "sm100.cuh"):
+    for fn in ("chunk_common.cuh", "chunk_scan.cu", "common.cuh", "sm100.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
@@ -300,7 +300,7 @@ def run_gpu_arm(args, ws, rank, local):
     sha = _kernel_sha()
     traffic = _stored_traffic(sha)
     roofline = roofline_entry(cb, cf, chunk_ms, peaks, traffic)
-    roofline.update({"kernel": "gdn_chunk_fwd (chunk_fused_setup_kernel + chunk_fused_kernel)",
+    roofline.update({"kernel": "gdn_chunk_fwd (chunk_operand_kernel + chunk_scan_kernel)",
                      "ms_mean": round(chunk_ms, 5), "ms_median": round(chunk_ms_median, 5),
                      "kernel_sha": sha})
     kernels = {
@@ -328,7 +328,7 @@ def run_gpu_arm(args, ws, rank, local):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
 
-    launches_per_step = 4  # gate prep, conv1d, and gdn_chunk_fwd's set-up + fused kernels
+    launches_per_step = 4  # gate prep, conv1d, and gdn_chunk_fwd's operand + scan kernels
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -378,29 +378,26 @@ def roofline_entry(nbytes, flops, ms, peaks, traffic=None):
 
 
 def time_chunk_paths(crg, q, k, v, g, beta, h0, cu, B, scale, stream, flush, reps=30):
-    """gdn_chunk_fwd on the fused kernel and on the two-kernel split path (GDN_FLAG_SPLIT),
-    same inputs, L2 flushed before each call; median ms of each."""
+    """gdn_chunk_fwd on the default two-kernel path and on the fused persistent kernel
+    (GDN_FLAG_FUSED), same inputs, L2 flushed before each call; median ms of each and the
+    workspace path word (GDN_PATH_FUSED = 1 when the fused kernel ran)."""
     out = {}
     sh = crg.make_shape(q, k, v, cu, B)
-    for name, split in (("fused", False), ("split", True)):
-        nb = crg.gdn_chunk_fwd_workspace_bytes(sh)
-        if split:
-            nb = max(nb, crg.split_workspace_bytes(sh))
-        ws = crg.Workspace(nb, q.device)
+    for name, fused in (("split", False), ("fused", True)):
+        ws = crg.Workspace(crg.gdn_chunk_fwd_workspace_bytes(sh), q.device)
         ws.reset()
         ts = []
         for it in range(reps + 3):
             flush.fill_(1)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            crg.gdn_chunk_fwd(q, k, v, g, beta, h0, cu, scale, True, B=B, split=split, workspace=ws)
+            crg.gdn_chunk_fwd(q, k, v, g, beta, h0, cu, scale, True, B=B, fused=fused, workspace=ws)
             e1.record(stream)
             torch.cuda.synchronize()
             if it >= 3:
                 ts.append(e0.elapsed_time(e1))
         out[name + "_ms"] = round(statistics.median(ts), 5)
-        out[name + "_path_word"] = ws.path()  # GDN_PATH_FUSED (1) when the fused kernel ran
-    out["speedup"] = round(out["split_ms"] / out["fused_ms"], 3)
+        out[name + "_path_word"] = ws.path()
     return out
 
 

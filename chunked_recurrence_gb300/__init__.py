@@ -25,7 +25,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_SIMT = 2
 GDN_FLAG_O_F32 = 4
-GDN_FLAG_SPLIT = 8
+GDN_FLAG_FUSED = 8
 GDN_FLAG_TEST_NO_WAIT = 16
 CHUNK = 64
 
@@ -312,22 +312,14 @@ def gdn_chunk_fwd_min_workspace_bytes(shape: GdnShape) -> int:
     return int(load().gdn_chunk_fwd_min_workspace_bytes(ctypes.byref(shape)))
 
 
-def split_workspace_bytes(shape: GdnShape) -> int:
-    """Workspace of the two-kernel split path (GDN_FLAG_SPLIT): a status header and one
-    operand record of 25600 + 256 V bytes per chunk slot and v-head."""
-    n_tok = shape.T if shape.B == 1 else shape.B * shape.T
-    slots = shape.n_seqs + (n_tok + CHUNK - 1) // CHUNK
-    return 256 + slots * shape.Hv * (25600 + 256 * shape.V)
-
-
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm_qk=True,
                   B=None, simt=False, o=None, h_T=None, want_h_T=True, workspace=None,
-                  stream=None, o_f32=False, split=False, _test_no_wait=False):
+                  stream=None, o_f32=False, fused=False, _test_no_wait=False):
     """Chunked gated delta rule forward; returns (o [n_tok, Hv, V], h_T [n_seqs, Hv, V, K] or None).
 
-    bf16 with K = V = 128 runs the fused persistent kernel; split=True takes the two-kernel
-    split path instead.  _test_no_wait (tests only) makes every bounded wait of the fused
-    kernel give up at once, so the call ends with GDN_ERR_TIMEOUT in the workspace status."""
+    fused=True (bf16, K = V = 128) runs the fused persistent kernel instead of the two-kernel
+    split path.  _test_no_wait (tests only, with fused=True) makes every bounded wait of the
+    fused kernel give up at once, so the call ends with GDN_ERR_TIMEOUT in the workspace status."""
     _need_cuda(q, k, v, g, beta, h0, cu_seqlens)
     for n, t in (("g", g), ("beta", beta), ("h0", h0)):
         _contig(n, t)
@@ -338,7 +330,7 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm
     if scale is None:
         scale = sh.K ** -0.5
     flags = ((GDN_FLAG_QK_L2NORM if l2norm_qk else 0) | (GDN_FLAG_SIMT if simt else 0)
-             | (GDN_FLAG_O_F32 if o_f32 else 0) | (GDN_FLAG_SPLIT if split else 0)
+             | (GDN_FLAG_O_F32 if o_f32 else 0) | (GDN_FLAG_FUSED if fused else 0)
              | (GDN_FLAG_TEST_NO_WAIT if _test_no_wait else 0))
     o_dtype = torch.float32 if o_f32 else v.dtype
     if o is None:
@@ -349,10 +341,7 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm
     if h0 is not None:
         assert h0.dtype == torch.float32 and tuple(h0.shape) == (sh.n_seqs, sh.Hv, sh.V, sh.K)
     if workspace is None:
-        nb = gdn_chunk_fwd_workspace_bytes(sh)
-        if split:
-            nb = max(nb, split_workspace_bytes(sh))
-        workspace = _workspace_for(nb, v.device)
+        workspace = _workspace_for(gdn_chunk_fwd_workspace_bytes(sh), v.device)
     ws = workspace
     _check(load().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                 _ptr(cu_seqlens), ctypes.byref(sh), float(scale), flags, _ptr(o),

@@ -81,10 +81,11 @@ bool fused_shape(const gdn_shape &s) { return s.dtype == GDN_BF16 && s.K == 128 
 extern "C" size_t gdn_chunk_fwd_workspace_bytes(const gdn_shape *shape) {
   gdn_shape s;
   if (normalise_shape(shape, &s) != GDN_OK) return 0;
-  // the fused kernel's ring, or the compact pair's T matrices should the fused kernel decline
-  if (fused_shape(s))
-    return std::max(chunk_fused_workspace_bytes(s), chunk_tc_workspace_bytes(s, (int64_t)s.B * s.T));
-  if (scan_shape(s)) return chunk_scan_workspace_bytes(s, (int64_t)s.B * s.T);
+  // the split path's records; they also hold the fused kernel's ring (GDN_FLAG_FUSED)
+  if (scan_shape(s)) {
+    const size_t split = chunk_scan_workspace_bytes(s, (int64_t)s.B * s.T);
+    return fused_shape(s) ? std::max(split, chunk_fused_workspace_bytes(s)) : split;
+  }
   if (tc_shape(s)) return chunk_tc_workspace_bytes(s, (int64_t)s.B * s.T);
   return kWorkspaceBase;
 }
@@ -115,7 +116,7 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   gdn_shape s;
   gdn_status st = normalise_shape(shape, &s);
   if (st != GDN_OK) return st;
-  if (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_SIMT | GDN_FLAG_O_F32 | GDN_FLAG_SPLIT |
+  if (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_SIMT | GDN_FLAG_O_F32 | GDN_FLAG_FUSED |
                 GDN_FLAG_TEST_NO_WAIT))
     return GDN_ERR_INVALID_ARG;
   if (cu_seqlens) {
@@ -129,9 +130,9 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   if (s.n_seqs == 0) return GDN_OK;
   if (n_tok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
   if (n_tok == 0 && !h_T) return GDN_OK;
-  if (!(flags & (GDN_FLAG_SIMT | GDN_FLAG_SPLIT)) && n_tok > 0 && chunk_fused_supported(q, k, v, s)) {
+  if ((flags & GDN_FLAG_FUSED) && !(flags & GDN_FLAG_SIMT) && n_tok > 0 && chunk_fused_supported(q, k, v, s)) {
     // the fused kernel; it declines (before launching anything) when the device cannot hold
-    // its grid at once or the workspace is too small for its ring, and the split path runs
+    // its grid at once or the workspace is too small for its ring, and another path runs
     const gdn_status fs = chunk_fwd_fused(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
                                           workspace, workspace_bytes, (cudaStream_t)stream);
     if (fs != GDN_ERR_UNSUPPORTED) return fs;

@@ -1,5 +1,5 @@
-// chunk_fused.cu -- gdn_chunk_fwd (bf16, K = V = 128) as one persistent kernel in
-// which per-head state chains are fed by chunk builders running beside them.
+// chunk_fused.cu -- gdn_chunk_fwd (bf16, K = V = 128, GDN_FLAG_FUSED) as one persistent
+// kernel in which per-head state chains are fed by chunk builders running beside them.
 //
 // The chunk form of the gated delta rule ("Gated Delta Networks", chunkwise
 // algorithm with the UT/WY transform), per chunk of C = 64 tokens and v-head,

@@ -56,9 +56,9 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_FLAG_QK_L2NORM 1u  /* normalise q and k to unit L2 norm on load (eps 1e-6 inside the sqrt) */
 #define GDN_FLAG_SIMT 2u       /* force the fp32 CUDA-core kernel (the tensor-core kernel is the default for bf16) */
 #define GDN_FLAG_O_F32 4u      /* write o as fp32 whatever the input dtype (default: o has the input dtype) */
-#define GDN_FLAG_SPLIT 8u      /* gdn_chunk_fwd: take the two-kernel split path even where the fused kernel applies */
-#define GDN_FLAG_TEST_NO_WAIT 16u /* test only: every bounded wait of the fused kernel gives up at its first
-                                   * check, so the call ends with GDN_ERR_TIMEOUT in the status word */
+#define GDN_FLAG_FUSED 8u      /* gdn_chunk_fwd (bf16, K = V = 128): the fused persistent kernel instead of the two-kernel path */
+#define GDN_FLAG_TEST_NO_WAIT 16u /* test only, with GDN_FLAG_FUSED: every bounded wait of the fused kernel gives
+                                   * up at its first check, so the call ends with GDN_ERR_TIMEOUT in the status word */
 
 /* Problem shape of the recurrence. */
 typedef struct {
@@ -149,7 +149,7 @@ gdn_status gdn_conv1d_varlen(const void *x, const void *w, const void *bias, int
  *   h0:   [n_seqs, Hv, V, K] fp32 start states, or NULL for zero
  *   cu_seqlens: see the conventions above, or NULL
  *   scale: multiplies o (1/sqrt(K) in Qwen3.5)
- *   flags: GDN_FLAG_QK_L2NORM, GDN_FLAG_SIMT, GDN_FLAG_O_F32, GDN_FLAG_SPLIT,
+ *   flags: GDN_FLAG_QK_L2NORM, GDN_FLAG_SIMT, GDN_FLAG_O_F32, GDN_FLAG_FUSED,
  *          GDN_FLAG_TEST_NO_WAIT
  *   o:    [tokens, Hv, V] (dense) of shape->dtype, or fp32 with GDN_FLAG_O_F32; every token written
  *   h_T:  [n_seqs, Hv, V, K] fp32 final states, or NULL

@@ -155,30 +155,22 @@ def _select_heads(inp, g, beta, heads, r):
             to64(beta.index_select(1, vh)))
 
 
-def _fresh_workspace(crg, inp):
-    sh = crg.make_shape(inp["q"], inp["k"], inp["v"], None, 1)
-    ws = crg.Workspace(crg.gdn_chunk_fwd_workspace_bytes(sh), DEV)
-    ws.reset()
-    return ws
-
-
 def _windows(starts, n_tok, width):
     idx = [t for s in starts for t in range(int(s), min(int(s) + width, n_tok))]
     return np.unique(np.array(idx, dtype=np.int64))
 
 
-@pytest.mark.parametrize("o_f32", [False, True])
-def test_qwen35_4b_layer_mild_gates_full(crg, o_f32):
-    """T = 8192, 16 q/k and 32 v heads: 128 chunks of carried state per head."""
+@pytest.mark.parametrize("o_f32,fused", [(False, False), (True, False), (False, True)])
+def test_qwen35_4b_layer_mild_gates_full(crg, o_f32, fused):
+    """T = 8192, 16 q/k and 32 v heads: 128 chunks of carried state per head (the default
+    path with bf16 and fp32 o, and the fused kernel)."""
     wl = synth.WORKLOADS["qwen35_4b_layer"]
     inp = synth.make_inputs(wl, device=DEV, with_front_end=False)
     n = inp["n_tok"]
     g, beta = synth.mild_gates(n, wl.Hv, wl.seed, device=DEV)
-    ws = _fresh_workspace(crg, inp)
     o, hT = crg.gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], g, beta, None, None, inp["scale"],
-                              True, B=1, o_f32=o_f32, workspace=ws)
+                              True, B=1, o_f32=o_f32, fused=fused)
     torch.cuda.synchronize()
-    assert ws.path() == crg.GDN_PATH_FUSED and ws.status() == 0
     heads = [0, 7, 18, 31]
     ro, rh = oracle.gdn_fwd(*_select_heads(inp, g, beta, heads, wl.Hv // wl.Hqk), None, None,
                             inp["scale"], True)
@@ -198,11 +190,8 @@ def test_long_segments_mild_gates_full(crg):
     n = inp["n_tok"]
     g, beta = synth.mild_gates(n, wl.Hv, wl.seed, device=DEV)
     bounds = inp["seg_bounds"]
-    ws = _fresh_workspace(crg, inp)
     o1, h1 = crg.gdn_chunk_fwd(inp["q"], inp["k"], inp["v"], g, beta, None, None, inp["scale"],
-                               True, B=1, workspace=ws)
-    torch.cuda.synchronize()
-    assert ws.path() == crg.GDN_PATH_FUSED and ws.status() == 0
+                               True, B=1)
     o2, h2 = crg.segment_parallel_fwd(inp["q"], inp["k"], inp["v"], g, beta, bounds,
                                       scale=inp["scale"])
     torch.cuda.synchronize()

@@ -61,22 +61,19 @@ def make_case(lengths, Hqk, Hv, K, V, dtype, gates="paper", h0=False, seed=0, B=
                 scale=K ** -0.5)
 
 
-def run_gpu(crg, c, simt=False, l2norm=True, o_f32=False, split=False):
-    """gdn_chunk_fwd in a fresh workspace; checks that bf16 K = V = 128 calls (without
-    simt / split) really ran the fused kernel and that no other call did."""
+def run_gpu(crg, c, simt=False, l2norm=True, o_f32=False, fused=False):
+    """gdn_chunk_fwd in a fresh workspace; checks that a fused=True call on bf16 K = V = 128
+    really ran the fused kernel and that no other call did."""
     d = lambda t: None if t is None else t.to(DEV)
     q, k, v = d(c["q"]), d(c["k"]), d(c["v"])
     sh = crg.make_shape(q, k, v, d(c["cu"]), c["B"])
-    nb = crg.gdn_chunk_fwd_workspace_bytes(sh)
-    if split:
-        nb = max(nb, crg.split_workspace_bytes(sh))
-    ws = crg.Workspace(nb, DEV)
+    ws = crg.Workspace(crg.gdn_chunk_fwd_workspace_bytes(sh), DEV)
     ws.reset()
     o, hT = crg.gdn_chunk_fwd(q, k, v, d(c["g"]), d(c["beta"]), d(c["h0"]), d(c["cu"]), c["scale"],
-                              l2norm, B=c["B"], simt=simt, o_f32=o_f32, split=split, workspace=ws)
+                              l2norm, B=c["B"], simt=simt, o_f32=o_f32, fused=fused, workspace=ws)
     torch.cuda.synchronize()
     fused_shape = c["dtype"] == "bf16" and q.shape[-1] == 128 and v.shape[-1] == 128
-    assert (ws.path() == crg.GDN_PATH_FUSED) == (fused_shape and not simt and not split)
+    assert (ws.path() == crg.GDN_PATH_FUSED) == (fused_shape and fused and not simt)
     assert ws.status() == 0
     return o.cpu(), hT.cpu()
 
@@ -88,8 +85,8 @@ def run_oracle(c, l2norm=True):
                           c["scale"], l2norm, B=c["B"] or 1)
 
 
-def check_case(crg, c, simt=False, l2norm=True, what="", o_f32=False, split=False):
-    o, hT = run_gpu(crg, c, simt, l2norm, o_f32, split)
+def check_case(crg, c, simt=False, l2norm=True, what="", o_f32=False, fused=False):
+    o, hT = run_gpu(crg, c, simt, l2norm, o_f32, fused)
     ro, rh = run_oracle(c, l2norm)
     mo = assert_close(o, ro, c["dtype"], f"{what} o")
     mh = assert_close(hT, rh, c["dtype"], f"{what} h_T")
@@ -218,24 +215,25 @@ SMALL = [
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{c[5]}-L{len(c[0])}-K{c[3]}-V{c[4]}")
 @pytest.mark.parametrize("gates", ["paper", "mild"])
 @pytest.mark.parametrize("h0", [False, True])
-@pytest.mark.parametrize("path", ["default", "split", "simt"])
+@pytest.mark.parametrize("path", ["default", "fused", "simt"])
 def test_chunk_fwd_small(crg, case, gates, h0, path):
-    """Every path against the oracle; "default" is the fused kernel for bf16 K = V = 128."""
+    """Every path against the oracle; "fused" is the fused kernel for bf16 K = V = 128 (other
+    shapes take the default path with it)."""
     lengths, Hqk, Hv, K, V, dtype = case
     c = make_case(lengths, Hqk, Hv, K, V, dtype, gates, h0, seed=len(lengths) * 31 + K + V)
-    mo, mh, o, _, ro, _ = check_case(crg, c, simt=path == "simt", split=path == "split",
+    mo, mh, o, _, ro, _ = check_case(crg, c, simt=path == "simt", fused=path == "fused",
                                      what=f"{case} {path}")
     if gates == "mild" and c["cu"] is not None:
         idx = boundary_windows(c["cu"].numpy())
         assert_close(o[idx], ro[idx], dtype, "boundary windows")
 
 
-@pytest.mark.parametrize("path", ["default", "split", "simt"])
+@pytest.mark.parametrize("path", ["default", "fused", "simt"])
 def test_chunk_fwd_fp32_output_strict_bar(crg, path):
     """bf16 inputs, o written in fp32: the 2e-2 * rms max-abs bar with no storage allowance."""
     for seed, gates in ((287, "paper"), (288, "mild")):
         c = make_case([300, 65], 2, 4, 128, 128, "bf16", gates, True, seed=seed)
-        o, _ = run_gpu(crg, c, simt=path == "simt", o_f32=True, split=path == "split")
+        o, _ = run_gpu(crg, c, simt=path == "simt", o_f32=True, fused=path == "fused")
         assert o.dtype == torch.float32
         ro, _ = run_oracle(c)
         assert_close(o, ro, "bf16", f"fp32-o {gates}")
@@ -508,8 +506,8 @@ def test_fused_against_oracle_and_split(crg, case, gates):
     kernel code), with h0, on the tail lengths and item counts that exercise its ring."""
     lengths, Hqk, Hv, B = case
     c = make_case(lengths, Hqk, Hv, 128, 128, "bf16", gates, True, seed=90 + len(lengths) + Hv, B=B)
-    o, hT = run_gpu(crg, c)
-    os_, hs = run_gpu(crg, c, split=True)
+    o, hT = run_gpu(crg, c, fused=True)
+    os_, hs = run_gpu(crg, c)
     ro, rh = run_oracle(c)
     assert_close(o, ro, "bf16", "fused o")
     assert_close(hT, rh, "bf16", "fused h_T")
@@ -531,12 +529,12 @@ def test_fused_timeout_reported_then_context_usable(crg):
     ws = crg.Workspace(crg.gdn_chunk_fwd_workspace_bytes(sh), DEV)
     ws.reset()
     crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]), d(c["cu"]),
-                      c["scale"], True, workspace=ws, _test_no_wait=True)
+                      c["scale"], True, workspace=ws, fused=True, _test_no_wait=True)
     assert ws.path() == crg.GDN_PATH_FUSED
     assert ws.status() == crg.GDN_ERR_TIMEOUT
     ws.reset()
     o, hT = crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]),
-                              d(c["cu"]), c["scale"], True, workspace=ws)
+                              d(c["cu"]), c["scale"], True, workspace=ws, fused=True)
     assert ws.status() == 0 and ws.path() == crg.GDN_PATH_FUSED
     ro, rh = run_oracle(c)
     assert_close(o.cpu(), ro, "bf16", "o after a timeout")
