@@ -107,12 +107,8 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) y[m][c] = (rg + 8 * m == 4 * cg + c) ? 1.f : 0.f;
   const float *xr = X + rg * kXP;
-  // Y_kj = 0 for j > k: the warp's 16 columns (16 w .. 16 w + 15) take no update from the
-  // steps before its first column (a warp-uniform skip)
-  const int k0 = (tid >> 5) * 16;
 #pragma unroll
   for (int k = 0; k < C - 1; ++k) {
-    if (k < k0) continue;
     float yk[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) yk[c] = __shfl_sync(0xffffffffu, y[k >> 3][c], (k & 7) | (lane & 24));
@@ -139,7 +135,7 @@ __global__ void __launch_bounds__(128, 4)
   constexpr uint32_t kCols = (V <= 128) ? 128u : 256u;
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-  __shared__ float gam[C], bex[C], dec[C], kinv[C], qinv[C], bet[C];
+  __shared__ float gam[C], bex[C], dec[C], alf[C + 1], kinv[C], qinv[C], bet[C];
   __shared__ float blast_s;
   __shared__ uint64_t bar, ld_bar;
   __shared__ uint32_t tbase;
@@ -263,7 +259,12 @@ __global__ void __launch_bounds__(128, 4)
     bex[2 * lane + 1] = expf(gb);
     dec[2 * lane] = expf(last - ga);
     dec[2 * lane + 1] = expf(last - gb);
-    if (lane == 31) blast_s = expf(last);
+    alf[2 * lane] = expf(g0);
+    alf[2 * lane + 1] = expf(g1);
+    if (lane == 31) {
+      blast_s = expf(last);
+      alf[C] = 1.f;
+    }
   }
   __syncthreads();
   if (tid < C) {
@@ -292,15 +293,16 @@ __global__ void __launch_bounds__(128, 4)
     tmem_ld64(tm + ((uint32_t)(warp * 32) << 16), r64);
     tmem_wait_ld();
     const float bi = isq ? p.scale * qinv[i] : bet[i] * kinv[i];
-    // Gamma_ij = exp(gamma_i - gamma_j) <= 1 for j < i (every g <= 0), each term independent.
+    // Gamma_ij = prod_{m=j+1..i} exp(g_m) for j < i: a running product walking j down.
     // Every shared load comes before the stores below (interleaved, each load would wait for
     // the previous store: the compiler cannot rule out aliasing).
-    const float gi = gam[i];
-    float vd = 0.f;
+    float gprod = 1.f, vd = 0.f;
 #pragma unroll
-    for (int j = 0; j < C; ++j) {
+    for (int j = C - 1; j >= 0; --j) {
+      const float aj = alf[j + 1], kj = kinv[j];
       vd = (j == i) ? r64[j] : vd;
-      r64[j] = (j < i) ? bi * kinv[j] * expf(gi - gam[j]) * r64[j] : 0.f;
+      if (j < i) gprod *= aj;
+      r64[j] = (j < i) ? bi * kj * gprod * r64[j] : 0.f;
     }
     if (!isq) {
       float4 *xr = reinterpret_cast<float4 *>(X + i * kXP);
