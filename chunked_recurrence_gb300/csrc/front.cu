@@ -609,9 +609,19 @@ extern "C" gdn_status gdn_cu_seqlens_from_position_ids(const int64_t *position_i
 
 // S_start[0] = h0; S_start[i+1] = S_start[i] M_i + S_local_i, in fp32 FFMA.
 // Rows of S evolve independently (row a: s_a <- s_a M + l_a), so a block owns
-// kChainRows rows of one head's state and walks the segments in order, with
-// the segment's K x K transition staged in shared memory.
-constexpr int kChainRows = 8;
+// kChainRows rows of one head's state and walks the segments in order.  Each thread
+// keeps a 2-row x 4-column tile of the product (8 independent sums; one float4 of M
+// feeds 8 FMAs), and the next segment's K x K transition streams into the second of two
+// shared-memory buffers (cp.async) while the current one is used.
+constexpr int kChainRows = 16;
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __global__ void __launch_bounds__(256) chain_reduce_kernel(const float *__restrict__ M,
                                                            const float *__restrict__ S_local,
@@ -619,41 +629,75 @@ __global__ void __launch_bounds__(256) chain_reduce_kernel(const float *__restri
                                                            int Hv, int K, int V,
                                                            float *__restrict__ S_start,
                                                            float *__restrict__ h_T) {
-  extern __shared__ float sm[];
-  float *Ms = sm;                   // K * K
-  float *Sr = Ms + (size_t)K * K;   // kChainRows * K
+  extern __shared__ float4 sm4[];
+  float *Ms = reinterpret_cast<float *>(sm4);  // 2 x K * K
+  float *Sr = Ms + 2 * (size_t)K * K;         // kChainRows * K
+  const int tid = threadIdx.x;
   const int h = blockIdx.y, r0 = blockIdx.x * kChainRows;
   const int rows = min(kChainRows, V - r0);
-  for (int idx = threadIdx.x; idx < kChainRows * K; idx += blockDim.x) {
+  const int cg = tid & 31, rg = tid >> 5;     // columns 4 cg .. 4 cg + 3, rows 2 rg, 2 rg + 1
+  const int c0 = 4 * cg;
+  const bool col_ok = c0 < K;                  // K is a multiple of 4 (32, 64 or 128)
+  const int n4 = K * K / 4;
+  auto prefetch = [&](int i, int buf) {
+    const float4 *src = reinterpret_cast<const float4 *>(M + ((size_t)i * Hv + h) * K * K);
+    float4 *dst = reinterpret_cast<float4 *>(Ms + (size_t)buf * K * K);
+    for (int idx = tid; idx < n4; idx += blockDim.x) cp_async16(dst + idx, src + idx);
+    cp_async_commit();
+  };
+  if (n_seg > 0) prefetch(0, 0);
+  for (int idx = tid; idx < kChainRows * K; idx += blockDim.x) {
     const int r = idx / K, c = idx % K;
     Sr[idx] = (r < rows && h0) ? h0[((size_t)h * V + r0 + r) * K + c] : 0.f;
   }
-  __syncthreads();
   for (int i = 0; i < n_seg; ++i) {
-    const float *Mi = M + ((size_t)i * Hv + h) * K * K;
-    for (int idx = threadIdx.x; idx < K * K; idx += blockDim.x) Ms[idx] = Mi[idx];
     const size_t base = ((size_t)i * Hv + h) * V * K;
-    for (int idx = threadIdx.x; idx < rows * K; idx += blockDim.x) {
+    cp_async_wait_all();
+    __syncthreads();  // M_i and the rows are in place; the other buffer is free
+    if (i + 1 < n_seg) prefetch(i + 1, (i + 1) & 1);
+    for (int idx = tid; idx < rows * K; idx += blockDim.x) {
       const int r = idx / K, c = idx % K;
       S_start[base + (size_t)(r0 + r) * K + c] = Sr[idx];
     }
-    __syncthreads();
-    float acc[(kChainRows * 128 + 255) / 256];
-    int n_out = 0;
-    for (int idx = threadIdx.x; idx < rows * K; idx += blockDim.x, ++n_out) {
-      const int r = idx / K, c = idx % K;
-      float a = S_local[base + (size_t)(r0 + r) * K + c];
-      const float *srow = Sr + r * K;
-      for (int m = 0; m < K; ++m) a = fmaf(srow[m], Ms[m * K + c], a);
-      acc[n_out] = a;
+    const float *Mi = Ms + (size_t)(i & 1) * K * K;
+    float acc[2][4];
+    const int ra = 2 * rg, rb = 2 * rg + 1;
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) acc[e][cc] = 0.f;
+    if (col_ok && ra < rows) {
+      const float4 la = *reinterpret_cast<const float4 *>(S_local + base + (size_t)(r0 + ra) * K + c0);
+      acc[0][0] = la.x; acc[0][1] = la.y; acc[0][2] = la.z; acc[0][3] = la.w;
+      if (rb < rows) {
+        const float4 lb = *reinterpret_cast<const float4 *>(S_local + base + (size_t)(r0 + rb) * K + c0);
+        acc[1][0] = lb.x; acc[1][1] = lb.y; acc[1][2] = lb.z; acc[1][3] = lb.w;
+      }
+      const float *sa = Sr + ra * K, *sb = Sr + rb * K;
+#pragma unroll 8
+      for (int m = 0; m < K; ++m) {
+        const float4 mv = *reinterpret_cast<const float4 *>(Mi + (size_t)m * K + c0);
+        const float xa = sa[m], xb = sb[m];
+        acc[0][0] = fmaf(xa, mv.x, acc[0][0]);
+        acc[0][1] = fmaf(xa, mv.y, acc[0][1]);
+        acc[0][2] = fmaf(xa, mv.z, acc[0][2]);
+        acc[0][3] = fmaf(xa, mv.w, acc[0][3]);
+        acc[1][0] = fmaf(xb, mv.x, acc[1][0]);
+        acc[1][1] = fmaf(xb, mv.y, acc[1][1]);
+        acc[1][2] = fmaf(xb, mv.z, acc[1][2]);
+        acc[1][3] = fmaf(xb, mv.w, acc[1][3]);
+      }
     }
-    __syncthreads();
-    n_out = 0;
-    for (int idx = threadIdx.x; idx < rows * K; idx += blockDim.x, ++n_out) Sr[idx] = acc[n_out];
-    __syncthreads();
+    __syncthreads();  // every read of Sr is done
+    if (col_ok && ra < rows) {
+      *reinterpret_cast<float4 *>(Sr + ra * K + c0) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+      if (rb < rows)
+        *reinterpret_cast<float4 *>(Sr + rb * K + c0) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+    }
   }
+  __syncthreads();
   if (h_T)
-    for (int idx = threadIdx.x; idx < rows * K; idx += blockDim.x) {
+    for (int idx = tid; idx < rows * K; idx += blockDim.x) {
       const int r = idx / K, c = idx % K;
       h_T[((size_t)h * V + r0 + r) * K + c] = Sr[idx];
     }
@@ -666,7 +710,9 @@ extern "C" gdn_status gdn_chain_reduce(const float *M, const float *S_local, con
   if (K > 128) return GDN_ERR_UNSUPPORTED;
   if (n_seg > 0 && (!M || !S_local || !S_start)) return GDN_ERR_INVALID_ARG;
   if (n_seg == 0 && !h_T) return GDN_OK;
-  const size_t smem = ((size_t)K * K + (size_t)kChainRows * K) * sizeof(float);
+  if (K % 4 != 0) return GDN_ERR_UNSUPPORTED;
+  if (!aligned(M, 16) || !aligned(S_local, 16) || !aligned(S_start, 16)) return GDN_ERR_INVALID_ARG;
+  const size_t smem = (2 * (size_t)K * K + (size_t)kChainRows * K) * sizeof(float);
   if (cudaFuncSetAttribute(chain_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return GDN_ERR_CUDA;

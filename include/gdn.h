@@ -273,8 +273,10 @@ gdn_status gdn_gated_rmsnorm(const void *o, const void *z, const void *w, int32_
  * Architecture: (b, M) chain reduce, fp32):
  *     S_start[0] = h0 (or 0);  S_start[i+1] = S_start[i] M[i] + S_local[i];  h_T = S_start[n_seg]
  * M: [n_seg, Hv, K, K], S_local: [n_seg, Hv, V, K], h0: [Hv, V, K] or NULL,
- * S_start: [n_seg, Hv, V, K] out, h_T: [Hv, V, K] out or NULL; all fp32.
- * Pass 2 is gdn_chunk_fwd with cu_seqlens = seg_bounds and h0 = S_start. */
+ * S_start: [n_seg, Hv, V, K] out, h_T: [Hv, V, K] out or NULL; all fp32, 16-byte aligned
+ * (GDN_ERR_INVALID_ARG otherwise).  K a multiple of 4, at most 128 (else
+ * GDN_ERR_UNSUPPORTED).  Pass 2 is gdn_chunk_fwd with cu_seqlens = seg_bounds and
+ * h0 = S_start. */
 gdn_status gdn_chain_reduce(const float *M, const float *S_local, const float *h0, int32_t n_seg,
                             int32_t Hv, int32_t K, int32_t V, float *S_start, float *h_T,
                             void *stream);

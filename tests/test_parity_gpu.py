@@ -355,6 +355,22 @@ def test_chain_reduce_no_h0(crg):
     np.testing.assert_allclose(to64(hT), rh, rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("n_seg,Hv,K,V", [(8, 16, 128, 128), (5, 3, 64, 40), (1, 2, 32, 96), (4, 1, 128, 17 * 4)])
+def test_chain_reduce_shapes(crg, n_seg, Hv, K, V):
+    """The fp32 chain reduce against the oracle's fp64 one on the same fp32 inputs: the
+    long-context size (8 segments x 16 heads, K = V = 128), and row counts that leave a
+    block partly empty."""
+    gen = _cpu_gen(13 + n_seg + V)
+    M = (torch.eye(K) * 0.6 + torch.randn((n_seg, Hv, K, K), generator=gen) * (0.3 / K ** 0.5)).float()
+    L = torch.randn((n_seg, Hv, V, K), generator=gen)
+    h0 = torch.randn((Hv, V, K), generator=gen) * 0.1
+    S_start, hT = crg.gdn_chain_reduce(M.to(DEV), L.to(DEV), h0.to(DEV))
+    rSs, rh = oracle.chain_reduce(to64(M), to64(L), to64(h0))
+    scale = np.abs(rSs).max()
+    np.testing.assert_allclose(to64(S_start), rSs, rtol=1e-5, atol=1e-5 * scale)
+    np.testing.assert_allclose(to64(hT), rh, rtol=1e-5, atol=1e-5 * np.abs(rh).max())
+
+
 # ------------------------------------------------- the whole layer chain
 
 def _layer_case(wl, device="cpu"):
