@@ -319,6 +319,10 @@ def run_gpu_arm(args, ws, rank, local):
     seg = None
     if not args.no_segment:
         seg = run_segment_leg(crg, args, dev, stream, peaks)
+    bwd = None
+    if not args.no_backward:
+        bwd = run_backward_leg(crg, args, dev, stream, peaks)
+        bwd["vs_forward"] = round(bwd["ms"] / chunk_ms, 1)
     dec = None
     if not args.no_decode:
         dec = run_decode_leg(crg, args, dev, stream, peaks)
@@ -352,6 +356,8 @@ def run_gpu_arm(args, ws, rank, local):
         out["segment_parallel"] = seg
     if dec is not None:
         out["decode"] = dec
+    if bwd is not None:
+        out["backward"] = bwd
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out
@@ -466,6 +472,47 @@ def run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws):
     return {"value": round(tok / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "pipeline": "3 streams (H2D, compute, D2H), 2 buffer slots"}
+
+
+def bwd_bytes(wl, n_tok, n_seq):
+    """HBM bytes one gdn_chunk_bwd must move, per token and v-head: q and k once per q/k
+    head (2 K 2 B Hqk/Hv), v (2 V), g and beta (8), d_o in fp32 (4 V), dq and dk out in fp32
+    (2 K 4 B Hqk/Hv), dv (4 V), dg and dbeta (8); plus dh0 per sequence and head."""
+    eb = 2 if wl.dtype == "bf16" else 4
+    per_tok = (wl.Hqk * wl.K * eb * 2 + wl.Hv * wl.V * eb + wl.Hv * 8 + wl.Hv * wl.V * 4
+               + wl.Hqk * wl.K * 4 * 2 + wl.Hv * wl.V * 4 + wl.Hv * 8)
+    return n_tok * per_tok + n_seq * wl.Hv * wl.V * wl.K * 4
+
+
+def run_backward_leg(crg, args, dev, stream, peaks):
+    """gdn_chunk_bwd on the 4B-shaped layer (same q, k, v, gates as the forward leg; d_o ~
+    N(0, 1) fp32, no loss on h_T), timed with CUDA events on the launching stream, L2
+    flushed before each call."""
+    wl = synth.WORKLOADS["qwen35_4b_layer"]
+    inp = synth.make_inputs(wl, device=dev, with_front_end=False)
+    g, beta = crg.gdn_gate_prep(inp["a"], inp["b"], inp["A_log"], inp["dt_bias"])
+    n_tok = inp["n_tok"]
+    d_o = synth.upstream_grads(n_tok, wl.Hv, wl.V, wl.seed, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ts = []
+    reps = 3
+    for it in range(reps + 1):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        crg.gdn_chunk_bwd(inp["q"], inp["k"], inp["v"], g, beta, d_o, None, None, B=1,
+                          scale=inp["scale"], l2norm_qk=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it > 0:
+            ts.append(e0.elapsed_time(e1))
+    ms = statistics.median(ts)
+    nb = bwd_bytes(wl, n_tok, 1)
+    return {"workload": wl.name, "kernel": "gdn_chunk_bwd (chunk_bwd_kernel + l2_back_kernel, fp32 CUDA cores)",
+            "ms": round(ms, 3), "tokens_per_s": round(n_tok / (ms * 1e-3), 1), "bytes": nb,
+            "achieved_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5),
+            "vs_forward": None, "steps": len(ts)}
 
 
 def run_decode_leg(crg, args, dev, stream, peaks, B=64):
@@ -669,6 +716,7 @@ def main(argv=None):
     ap.add_argument("--no-segment", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

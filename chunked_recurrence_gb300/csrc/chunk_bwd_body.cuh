@@ -74,7 +74,7 @@ struct Params {
 // shared memory of one block, in floats
 GDN_BWD_HD size_t smem_floats(int K) {
   const size_t KP = (size_t)K + 1;
-  return 2 * C * KP + 2 * BV * KP + 7 * (size_t)C * VP + 6 * (size_t)C * CP + 8 * C;
+  return 2 * C * KP + 2 * BV * KP + 7 * (size_t)C * VP + 7 * (size_t)C * CP + 8 * C;
 }
 
 // ld(ptr, i): element i of a q / k / v array as float
@@ -106,6 +106,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
   float *dd = db + C;          // [C] dL/dd
   float *dbt = dd + C;         // [C] dL/dbeta
   float *dgm = dbt + C;        // [C] scratch of the inversion, then dL/dgamma
+  float *Gm = dgm + C;         // [C][CP]  Gamma_ij = exp(gamma_i - gamma_j), j <= i (once per chunk)
 
   const int qh = h / (Hv / p.Hqk), row0 = tile * BV;
   int64_t start, end;
@@ -123,7 +124,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
   const int64_t slot0 = (int64_t)s + start / C;
   const int n_chunks = (int)((end - start + C - 1) / C);
   const size_t VK = (size_t)V * K;
-  auto G = [&](int i, int j) { return expf(gam[i] - gam[j]); };  // j <= i
+  auto G = [&](int i, int j) { return Gm[i * CP + j]; };  // j <= i
 
   // ---- the chunk's inputs and its state-independent matrices (with_q: Q, dO, Q K^T too)
   auto prep = [&](int64_t t0, int n, bool with_q) {
@@ -168,8 +169,10 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         for (int c = 0; c < K; ++c) kk = fmaf(Ks[i * KP + c], Ks[j * KP + c], kk);
       if (with_q && j <= i)
         for (int c = 0; c < K; ++c) qk = fmaf(Qs[i * KP + c], Ks[j * KP + c], qk);
+      const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
+      Gm[i * CP + j] = gij;
       KKm[i * CP + j] = kk;
-      Zm[i * CP + j] = j < i ? bet[i] * expf(gam[i] - gam[j]) * kk : 0.f;
+      Zm[i * CP + j] = j < i ? bet[i] * gij * kk : 0.f;
       if (with_q) QKm[i * CP + j] = qk;
     });
     x.sync();

@@ -172,6 +172,12 @@ def mild_gates(n_tok: int, Hv: int, seed: int, device="cpu"):
     return gg, bb
 
 
+def upstream_grads(n_tok: int, Hv: int, V: int, seed: int, device="cpu"):
+    """Upstream gradient of o for the backward: d_o [n_tok, Hv, V] fp32 ~ N(0, 1)."""
+    g = _gen(seed + 65537, torch.device(device))
+    return torch.randn((n_tok, Hv, V), generator=g, device=device)
+
+
 def decode_inputs(B: int, Hqk: int, Hv: int, K: int, V: int, width: int, dtype: str, seed: int,
                   device="cpu", with_bias: bool = False, state_std: float = 0.1) -> dict:
     """Inputs of one decode step for B sequences: the new token's Q|K|V projections x [B, C],

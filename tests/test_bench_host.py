@@ -79,3 +79,11 @@ def test_roofline_frac_uses_the_bound_that_applies():
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 100.0
     assert r["frac"] == pytest.approx(0.5) and r["achieved"] == pytest.approx(50.0)
     assert r["hbm_frac"] == pytest.approx(0.025)
+
+
+def test_backward_work_matches_the_hand_count():
+    """gdn_chunk_bwd at the 4B layer: per token and v-head, q and k (2 x 128 x 2 B / 2), v
+    (256), g and beta (8), d_o fp32 (512), dq and dk fp32 (2 x 128 x 4 B / 2), dv (512), dg and
+    dbeta (8) = 2064 B; plus dh0 (V K 4 B per head)."""
+    wl = synth.WORKLOADS["qwen35_4b_layer"]
+    assert bench.bwd_bytes(wl, 8192, 1) == 8192 * 32 * 2064 + 32 * 128 * 128 * 4

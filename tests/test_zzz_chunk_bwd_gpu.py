@@ -22,7 +22,7 @@ def crg():
     return m
 
 
-def _check(got, ref, what, tol=5e-5):
+def _check(got, ref, what, tol=1e-5):
     for name, a, b in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], got, ref):
         a = a.detach().cpu().double().numpy().reshape(np.shape(b))
         err = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
