@@ -161,11 +161,11 @@ class ClockSampler:
 
 
 def _kernel_sha() -> str:
-    """Hash of the sources chunk_operand_kernel and chunk_scan_kernel compile from: a stored
-    ncu traffic figure is valid for these only."""
+    """Hash of the sources chunk_operand_kernel (with its front end) and chunk_scan_kernel
+    compile from: a stored ncu traffic figure is valid for these only."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_recurrence_gb300", "csrc")
-    for fn in ("chunk_common.cuh", "chunk_scan.cu", "common.cuh", "sm100.cuh"):
+    for fn in ("chunk_common.cuh", "chunk_scan.cu", "common.cuh", "conv_tap.cuh", "gates.cuh", "sm100.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
@@ -204,6 +204,17 @@ def chunk_flops(wl, n_tok, C=64):
     return n_tok * wl.Hv * (6 * C * wl.K + 4 * C * wl.V + 6 * wl.K * wl.V)
 
 
+def layer_bytes(wl, n_tok, n_seq, with_h0=False):
+    """HBM bytes one gdn_layer_fwd must move: x (every Q|K|V channel once), a and b, the
+    conv weights and the per-head gate parameters in; o and h_T (and h0) as for the chunk
+    form."""
+    eb = 2 if wl.dtype == "bf16" else 4
+    per_tok = wl.C * eb + wl.Hv * 2 * eb + wl.Hv * wl.V * eb
+    params = wl.C * wl.conv_width * eb + wl.Hv * 8
+    state = n_seq * wl.Hv * wl.V * wl.K * 4 * (2 if with_h0 else 1)
+    return n_tok * per_tok + params + state
+
+
 def conv_bytes(wl, n_tok):
     eb = 2 if wl.dtype == "bf16" else 4
     return n_tok * wl.C * eb * 2 + wl.C * wl.conv_width * eb
@@ -235,10 +246,10 @@ def run_gpu_arm(args, ws, rank, local):
         cu_full, cnt = crg.gdn_cu_seqlens_from_position_ids(inp["position_ids"])
         cu = cu_full[: int(cnt.item()) + 1]
     bufs = dict(
-        g=torch.empty((n_tok, wl.Hv), device=dev), beta=torch.empty((n_tok, wl.Hv), device=dev),
-        y=torch.empty_like(inp["x"]),
         o=torch.empty((n_tok, wl.Hv, wl.V), device=dev, dtype=wl.torch_dtype),
         h_T=torch.empty((n_seq, wl.Hv, wl.V, wl.K), device=dev))
+    lsh = crg.layer_shape(inp["x"], wl.Hqk, wl.Hv, wl.K, wl.V, cu, wl.B)
+    bufs["workspace"] = crg.Workspace(crg.gdn_layer_fwd_workspace_bytes(lsh, wl.conv_width, 0), dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -246,28 +257,22 @@ def run_gpu_arm(args, ws, rank, local):
     marks = {}
 
     def step(record=False):
+        # one gdn_layer_fwd: gates, conv + SiLU, q/k L2 norm and the chunked rule (its default
+        # path: separate launches, the faster as measured)
         if record:
-            e = [ev() for _ in range(4)]
+            e = [ev(), ev()]
             e[0].record(stream)
-        g, beta = crg.gdn_gate_prep(inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
-                                    bufs["g"], bufs["beta"])
+        crg.layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
+                      wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"], bufs=bufs)
         if record:
             e[1].record(stream)
-        y = crg.gdn_conv1d_varlen(inp["x"], inp["conv_w"], None, cu,
-                                  None if cu is not None else wl.B, 1, bufs["y"])
-        if record:
-            e[2].record(stream)
-        q, k, v = crg.split_qkv(y, wl.Hqk, wl.Hv, wl.K, wl.V)
-        crg.gdn_chunk_fwd(q, k, v, g, beta, inp["h0"], cu, inp["scale"], True,
-                          B=None if cu is not None else wl.B, o=bufs["o"], h_T=bufs["h_T"])
-        if record:
-            e[3].record(stream)
             marks.setdefault("ev", []).append(e)
 
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
+    bufs["workspace"].reset()
 
     clocks = ClockSampler(local) if rank == 0 or True else None
     clocks.start()
@@ -281,11 +286,9 @@ def run_gpu_arm(args, ws, rank, local):
     _barrier(ws)
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
+    layer_path = bufs["workspace"].path()
 
-    per_step = [e[0].elapsed_time(e[3]) for e in marks["ev"]]
-    t_gate = [e[0].elapsed_time(e[1]) for e in marks["ev"]]
-    t_conv = [e[1].elapsed_time(e[2]) for e in marks["ev"]]
-    t_chunk = [e[2].elapsed_time(e[3]) for e in marks["ev"]]
+    per_step = [e[0].elapsed_time(e[1]) for e in marks["ev"]]
     step_ms_local = sum(per_step) / len(per_step)
     step_ms_median = statistics.median(per_step)
     step_ms = _max_over_ranks(step_ms_local, ws, dev)
@@ -293,25 +296,39 @@ def run_gpu_arm(args, ws, rank, local):
     value = tokens_all / (step_ms * 1e-3)
 
     peaks = _peaks()
-    chunk_ms = sum(t_chunk) / len(t_chunk)
-    chunk_ms_median = statistics.median(t_chunk)
-    cb = chunk_bytes(wl, n_tok, n_seq, inp["h0"] is not None)
+    lb = layer_bytes(wl, n_tok, n_seq, inp["h0"] is not None)
     cf = chunk_flops(wl, n_tok)
     sha = _kernel_sha()
     traffic = _stored_traffic(sha)
-    roofline = roofline_entry(cb, cf, chunk_ms, peaks, traffic)
-    roofline.update({"kernel": "gdn_chunk_fwd (chunk_operand_kernel + chunk_scan_kernel)",
-                     "ms_mean": round(chunk_ms, 5), "ms_median": round(chunk_ms_median, 5),
-                     "kernel_sha": sha})
+    roofline = roofline_entry(lb, cf, step_ms_local, peaks, traffic)
+    roofline.update({"kernel": "gdn_layer_fwd (gate_prep_kernel, conv1d_staged_kernel<4>, "
+                               "chunk_operand_kernel<128>, chunk_scan_kernel)",
+                     "ms_mean": round(step_ms_local, 5), "ms_median": round(step_ms_median, 5),
+                     "path_word": layer_path, "kernel_sha": sha})
+
+    # ---- the same launches called one by one (gate prep, conv1d, gdn_chunk_fwd), kernel by kernel
+    unf = time_unfused_layer(crg, wl, inp, cu, stream, flush)
+    cb = chunk_bytes(wl, n_tok, n_seq, inp["h0"] is not None)
+    chunk_ms = unf["chunk_ms"]
     kernels = {
-        "gdn_gate_prep": _kinfo(sum(t_gate) / len(t_gate), gate_bytes(wl, n_tok), peaks),
-        "gdn_conv1d_varlen": _kinfo(sum(t_conv) / len(t_conv), conv_bytes(wl, n_tok), peaks),
+        "gdn_layer_fwd": _kinfo(step_ms_local, lb, peaks),
+        "gdn_gate_prep": _kinfo(unf["gate_ms"], gate_bytes(wl, n_tok), peaks),
+        "gdn_conv1d_varlen": _kinfo(unf["conv_ms"], conv_bytes(wl, n_tok), peaks),
         "gdn_chunk_fwd": _kinfo(chunk_ms, cb, peaks),
     }
+    chunk_roofline = roofline_entry(cb, cf, chunk_ms, peaks)
+    front = time_front_layer(crg, wl, inp, cu, stream, flush)
+    layer_paths = {"separate_launches_ms_median": round(step_ms_median, 5),
+                   "separate_launches_unwrapped_ms_median": round(unf["total_ms"], 5),
+                   "fused_front_ms_median": round(front["ms"], 5),
+                   "fused_front_path_word": front["path_word"],
+                   "fused_front_workspace_bytes": front["workspace_bytes"],
+                   "separate_launches_workspace_bytes": bufs["workspace"].nbytes}
 
-    q_, k_, v_ = crg.split_qkv(bufs["y"], wl.Hqk, wl.Hv, wl.K, wl.V)
-    paths = time_chunk_paths(crg, q_, k_, v_, bufs["g"], bufs["beta"], inp["h0"], cu,
+    q_, k_, v_ = crg.split_qkv(unf["y"], wl.Hqk, wl.Hv, wl.K, wl.V)
+    paths = time_chunk_paths(crg, q_, k_, v_, unf["g"], unf["beta"], inp["h0"], cu,
                              None if cu is not None else wl.B, inp["scale"], stream, flush)
+    del unf
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws)
@@ -332,7 +349,7 @@ def run_gpu_arm(args, ws, rank, local):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
 
-    launches_per_step = 4  # gate prep, conv1d, and gdn_chunk_fwd's operand + scan kernels
+    launches_per_step = 4  # gdn_layer_fwd: gate prep, conv1d, and the chunk operand and scan kernels
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -342,10 +359,12 @@ def run_gpu_arm(args, ws, rank, local):
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Hqk": wl.Hqk, "Hv": wl.Hv,
                    "K": wl.K, "V": wl.V, "conv_channels": wl.C, "conv_width": wl.conv_width,
                    "chunk": 64, "state": "fp32", "parallelism": f"replicas x{ws}",
-                   "step": "gate_prep + conv1d(SiLU) + chunk_fwd(L2 norm fused)",
+                   "step": "gdn_layer_fwd: conv1d(SiLU) + gates + q/k L2 norm + chunked rule in one call",
                    "l2": "flushed between steps (512 MiB fill outside the per-step events)"},
         "roofline": roofline,
         "kernels": kernels,
+        "chunk_fwd_roofline": chunk_roofline,
+        "layer_paths": layer_paths,
         "chunk_fwd_paths": paths,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -407,6 +426,64 @@ def time_chunk_paths(crg, q, k, v, g, beta, h0, cu, B, scale, stream, flush, rep
     return out
 
 
+def time_front_layer(crg, wl, inp, cu, stream, flush, reps=30):
+    """gdn_layer_fwd with the fused front end (GDN_FLAG_LAYER_FRONT), L2 flushed before each
+    call: median ms, the path word and the workspace it needs."""
+    sh = crg.layer_shape(inp["x"], wl.Hqk, wl.Hv, wl.K, wl.V, cu, wl.B)
+    ws = crg.Workspace(crg.gdn_layer_fwd_workspace_bytes(sh, wl.conv_width, crg.GDN_FLAG_LAYER_FRONT),
+                       inp["x"].device)
+    ws.reset()
+    bufs = {"workspace": ws}
+    ts = []
+    for it in range(reps + 3):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        crg.layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
+                      wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"], bufs=bufs, front=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= 3:
+            ts.append(e0.elapsed_time(e1))
+    return {"ms": statistics.median(ts), "path_word": ws.path(), "workspace_bytes": ws.nbytes}
+
+
+def time_unfused_layer(crg, wl, inp, cu, stream, flush, reps=30):
+    """The layer as separate launches (gdn_gate_prep, gdn_conv1d_varlen, gdn_chunk_fwd), L2
+    flushed before each step; median ms of each call and of the whole, and the intermediates
+    (y, g, beta) of the last step."""
+    n_tok = inp["n_tok"]
+    dev = inp["x"].device
+    g = torch.empty((n_tok, wl.Hv), device=dev)
+    beta = torch.empty_like(g)
+    y = torch.empty_like(inp["x"])
+    o = torch.empty((n_tok, wl.Hv, wl.V), device=dev, dtype=wl.torch_dtype)
+    h_T = torch.empty((inp["n_seq"], wl.Hv, wl.V, wl.K), device=dev)
+    B = None if cu is not None else wl.B
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    t = {"gate": [], "conv": [], "chunk": [], "total": []}
+    for it in range(reps + 3):
+        flush.fill_(1)
+        e = [ev() for _ in range(4)]
+        e[0].record(stream)
+        crg.gdn_gate_prep(inp["a"], inp["b"], inp["A_log"], inp["dt_bias"], g, beta)
+        e[1].record(stream)
+        crg.gdn_conv1d_varlen(inp["x"], inp["conv_w"], None, cu, B, 1, y)
+        e[2].record(stream)
+        q, k, v = crg.split_qkv(y, wl.Hqk, wl.Hv, wl.K, wl.V)
+        crg.gdn_chunk_fwd(q, k, v, g, beta, inp["h0"], cu, inp["scale"], True, B=B, o=o, h_T=h_T)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        if it >= 3:
+            t["gate"].append(e[0].elapsed_time(e[1]))
+            t["conv"].append(e[1].elapsed_time(e[2]))
+            t["chunk"].append(e[2].elapsed_time(e[3]))
+            t["total"].append(e[0].elapsed_time(e[3]))
+    out = {k2 + "_ms": statistics.median(v2) for k2, v2 in t.items()}
+    out.update(y=y, g=g, beta=beta)
+    return out
+
+
 def _kinfo(ms, nbytes, peaks):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"ms": round(ms, 5), "bytes": nbytes, "achieved_gbs": round(gbs, 1),
@@ -423,8 +500,8 @@ def run_e2e(crg, args, wl, inp, cu, bufs, dev, stream, ws):
     host_in = {k: inp[k].cpu().pin_memory() for k in keys}
     slots = 2
     dev_in = [{k: torch.empty_like(inp[k]) for k in keys} for _ in range(slots)]
-    outs = [dict(g=bufs["g"], beta=bufs["beta"], y=bufs["y"], o=torch.empty_like(bufs["o"]),
-                 h_T=torch.empty_like(bufs["h_T"])) for _ in range(slots)]
+    outs = [dict(o=torch.empty_like(bufs["o"]), h_T=torch.empty_like(bufs["h_T"]),
+                 workspace=bufs["workspace"]) for _ in range(slots)]
     host_out = [(torch.empty(bufs["o"].shape, dtype=bufs["o"].dtype).pin_memory(),
                  torch.empty(bufs["h_T"].shape, dtype=torch.float32).pin_memory()) for _ in range(slots)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())

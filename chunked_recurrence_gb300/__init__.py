@@ -21,12 +21,14 @@ from . import build as _build
 GDN_OK = 0
 GDN_ERR_TIMEOUT, GDN_ERR_BOUNDS = 4, 6  # device-side statuses read from a workspace
 GDN_PATH_FUSED = 1                      # path word of a workspace after the fused kernel ran
+GDN_PATH_FRONT = 2                      # ... after gdn_layer_fwd's fused front end ran
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_SIMT = 2
 GDN_FLAG_O_F32 = 4
 GDN_FLAG_FUSED = 8
 GDN_FLAG_TEST_NO_WAIT = 16
+GDN_FLAG_LAYER_FRONT = 32
 CHUNK = 64
 
 _lib = None
@@ -69,6 +71,9 @@ _SIGS = {
     "gdn_decode_step": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                          _I32, _F32, _U32, _P, _P], ctypes.c_int),
     "gdn_cu_seqlens_from_position_ids": ([_P, _I64, _P, _P, _P], ctypes.c_int),
+    "gdn_layer_fwd_workspace_bytes": ([ctypes.POINTER(GdnShape), _I32, _U32], _SZ),
+    "gdn_layer_fwd": ([_P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, ctypes.POINTER(GdnShape), _F32, _U32, _P, _P,
+                       _F32, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "gdn_chunk_bwd_workspace_bytes": ([ctypes.POINTER(GdnShape)], _SZ),
     "gdn_chunk_bwd": ([_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(GdnShape), _F32, _U32, _P, _P, _P, _P, _P,
                        _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
@@ -457,18 +462,75 @@ def split_qkv(y, Hqk, Hv, K, V):
 
 
 def layer_fwd(x, conv_w, a, b, A_log, dt_bias, Hqk, Hv, K, V, h0=None, cu_seqlens=None, B=1,
-              scale=None, stream=None, bufs=None):
-    """The GDN layer forward hot path: gate prep, conv1d+SiLU over Q|K|V, then the
-    chunked rule with in-kernel q/k L2 norm.  Returns dict(o, h_T, y, g, beta)."""
+              scale=None, stream=None, bufs=None, front=False):
+    """The GDN layer forward hot path through gdn_layer_fwd: conv1d+SiLU over Q|K|V, gates,
+    then the chunked rule with q/k L2 norm (front=True: the fused front end).
+    Returns dict(o, h_T)."""
     bufs = bufs if bufs is not None else {}
-    g, beta = gdn_gate_prep(a, b, A_log, dt_bias, bufs.get("g"), bufs.get("beta"), stream)
-    n_seqs = None if cu_seqlens is not None else B
-    y = gdn_conv1d_varlen(x, conv_w, None, cu_seqlens, n_seqs, 1, bufs.get("y"), stream)
-    q, k, v = split_qkv(y, Hqk, Hv, K, V)
-    o, h_T = gdn_chunk_fwd(q, k, v, g, beta, h0, cu_seqlens, scale, True,
-                           B=None if cu_seqlens is not None else B, o=bufs.get("o"),
-                           h_T=bufs.get("h_T"), stream=stream)
-    return dict(o=o, h_T=h_T, y=y, g=g, beta=beta)
+    o, h_T = gdn_layer_fwd(x, conv_w, a, b, A_log, dt_bias, Hqk, Hv, K, V, h0, cu_seqlens, B, scale,
+                           o=bufs.get("o"), h_T=bufs.get("h_T"), front=front,
+                           workspace=bufs.get("workspace"), stream=stream)
+    return dict(o=o, h_T=h_T)
+
+
+def layer_shape(x, Hqk, Hv, K, V, cu_seqlens=None, B=1, n_seqs=None) -> GdnShape:
+    """Shape of a gdn_layer_fwd call on x [n_tok, 2*Hqk*K + Hv*V] (dense)."""
+    n_tok = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != 2 * Hqk * K + Hv * V:
+        raise ValueError("x must be [n_tok, 2*Hqk*K + Hv*V]")
+    if cu_seqlens is not None:
+        Bv, T, ns = 1, n_tok, (cu_seqlens.numel() - 1 if n_seqs is None else n_seqs)
+    else:
+        assert n_tok % B == 0
+        Bv, T, ns = B, n_tok // B, B
+    return GdnShape(Bv, T, ns, Hqk, Hv, K, V, _dtype_code(x.dtype), 0, 0, 0)
+
+
+def gdn_layer_fwd_workspace_bytes(shape: GdnShape, width: int, flags: int = 0) -> int:
+    return int(load().gdn_layer_fwd_workspace_bytes(ctypes.byref(shape), int(width), int(flags)))
+
+
+def gdn_layer_fwd(x, conv_w, a, b, A_log, dt_bias, Hqk, Hv, K, V, h0=None, cu_seqlens=None, B=1,
+                  scale=None, conv_bias=None, z=None, norm_w=None, norm_eps=1e-6, o=None, h_T=None,
+                  want_h_T=True, o_f32=False, simt=False, front=False, workspace=None, stream=None):
+    """The layer's forward in one call: conv1d+SiLU over x's Q|K|V channels, gates, the
+    chunked rule with q/k L2 norm and, with z, the gated RMS norm of o.  Returns (o, h_T).
+
+    By default gate prep, conv and gdn_chunk_fwd run as separate launches; front=True (bf16,
+    K = V = 128, conv width <= 4) runs the fused front end instead (conv and gates inside the
+    chunk operand kernel, same results bit for bit)."""
+    _need_cuda(x, conv_w, a, b, A_log, dt_bias, h0, cu_seqlens, z, norm_w, conv_bias)
+    for n, t in (("x", x), ("conv_w", conv_w), ("a", a), ("b", b), ("A_log", A_log),
+                 ("dt_bias", dt_bias), ("h0", h0), ("z", z), ("norm_w", norm_w), ("conv_bias", conv_bias)):
+        _contig(n, t)
+    sh = layer_shape(x, Hqk, Hv, K, V, cu_seqlens, B)
+    n_tok = x.shape[0]
+    width = conv_w.shape[1]
+    assert conv_w.dtype == a.dtype == b.dtype == x.dtype
+    assert A_log.dtype == dt_bias.dtype == torch.float32
+    if scale is None:
+        scale = K ** -0.5
+    flags = ((GDN_FLAG_O_F32 if o_f32 else 0) | (GDN_FLAG_SIMT if simt else 0)
+             | (GDN_FLAG_LAYER_FRONT if front else 0))
+    o_dtype = torch.float32 if o_f32 else x.dtype
+    if o is None:
+        o = torch.empty((n_tok, Hv, V), device=x.device, dtype=o_dtype)
+    assert o.dtype == o_dtype and o.is_contiguous()
+    if h_T is None and want_h_T:
+        h_T = torch.empty((sh.n_seqs, Hv, V, K), device=x.device, dtype=torch.float32)
+    if h0 is not None:
+        assert h0.dtype == torch.float32 and tuple(h0.shape) == (sh.n_seqs, Hv, V, K)
+    if z is not None:
+        assert z.dtype == x.dtype and tuple(z.shape) == (n_tok, Hv, V)
+    if workspace is None:
+        workspace = _workspace_for(gdn_layer_fwd_workspace_bytes(sh, width, flags), x.device)
+    ws = workspace
+    _check(load().gdn_layer_fwd(_ptr(x), _ptr(conv_w), _ptr(conv_bias), int(width), _ptr(a), _ptr(b),
+                                _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens), ctypes.byref(sh),
+                                float(scale), flags, _ptr(z), _ptr(norm_w), float(norm_eps), _ptr(o),
+                                _ptr(h_T), ws.ptr(), ws.nbytes, _stream(x, stream)),
+           "gdn_layer_fwd")
+    return o, h_T
 
 
 def segment_parallel_fwd(q, k, v, g, beta, seg_bounds, h0=None, scale=None, l2norm_qk=True,

@@ -1,4 +1,5 @@
-// api.cu -- argument checking and dispatch of gdn_chunk_fwd / gdn_segment_summary.
+// api.cu -- argument checking and dispatch of gdn_chunk_fwd, gdn_segment_summary and
+// gdn_layer_fwd.
 #include <algorithm>
 
 #include "common.cuh"
@@ -34,6 +35,11 @@ gdn_status chunk_fwd_fused(const void *q, const void *k, const void *v, const fl
                            const float *beta, const float *h0, const int32_t *cu,
                            const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
                            void *workspace, size_t ws_bytes, cudaStream_t st);
+bool chunk_front_supported(const void *x, const void *w, int width, const gdn_shape &sh);
+size_t chunk_front_workspace_bytes(const gdn_shape &sh, int64_t n_tok);
+gdn_status chunk_fwd_front(const FrontArgs &fr, const float *h0, const int32_t *cu, const gdn_shape &sh,
+                           float scale, uint32_t flags, void *o, float *h_T, void *workspace,
+                           size_t ws_bytes, cudaStream_t st);
 gdn_status summary_tc(const void *k, const void *v, const float *g, const float *beta,
                       const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
                       float *M, float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st);
@@ -176,4 +182,104 @@ extern "C" gdn_status gdn_segment_summary(const void *k, const void *v, const fl
   }
   return segment_summary_simt(k, v, g, beta, seg_bounds, n_seg, s, flags, M, S_local,
                               (int32_t *)workspace, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ layer forward
+
+namespace {
+
+constexpr uint32_t kLayerFlags = GDN_FLAG_O_F32 | GDN_FLAG_SIMT | GDN_FLAG_LAYER_FRONT;
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+bool front_applies(const gdn_shape &s, int width, uint32_t flags) {
+  return (flags & GDN_FLAG_LAYER_FRONT) && !(flags & GDN_FLAG_SIMT) && s.dtype == GDN_BF16 && s.K == 128 &&
+         s.V == 128 && width >= 1 && width <= 4;
+}
+
+// The chunk shape of the unfused sequence: q, k and v are views of the conv output y.
+gdn_shape chunk_view(const gdn_shape &s) {
+  gdn_shape c = s;
+  const int64_t Cx = 2LL * s.Hqk * s.K + (int64_t)s.Hv * s.V;
+  c.q_stride = c.k_stride = c.v_stride = Cx;
+  return c;
+}
+
+// Unfused layout: [gdn_chunk_fwd's workspace][y][g][beta].
+size_t unfused_bytes(const gdn_shape &s, int64_t n_tok) {
+  const int64_t Cx = 2LL * s.Hqk * s.K + (int64_t)s.Hv * s.V;
+  const size_t es = s.dtype == GDN_BF16 ? 2 : 4;
+  gdn_shape c = chunk_view(s);
+  return align256(gdn_chunk_fwd_workspace_bytes(&c)) + align256((size_t)n_tok * Cx * es) +
+         2 * align256((size_t)n_tok * s.Hv * 4);
+}
+
+gdn_status layer_shape(const gdn_shape *shape, int32_t width, gdn_shape *s) {
+  if (!shape || shape->q_stride || shape->k_stride || shape->v_stride) return GDN_ERR_INVALID_ARG;
+  if (width < 1 || width > 8) return GDN_ERR_INVALID_ARG;
+  return normalise_shape(shape, s);
+}
+
+}  // namespace
+
+extern "C" size_t gdn_layer_fwd_workspace_bytes(const gdn_shape *shape, int32_t width, uint32_t flags) {
+  gdn_shape s;
+  if (layer_shape(shape, width, &s) != GDN_OK || (flags & ~kLayerFlags)) return 0;
+  const int64_t n_tok = (int64_t)s.B * s.T;
+  if (front_applies(s, width, flags)) return chunk_front_workspace_bytes(s, n_tok);
+  return unfused_bytes(s, n_tok);
+}
+
+extern "C" gdn_status gdn_layer_fwd(const void *x, const void *conv_w, const void *conv_bias, int32_t width,
+                                    const void *a, const void *b, const float *A_log, const float *dt_bias,
+                                    const float *h0, const int32_t *cu_seqlens, const gdn_shape *shape,
+                                    float scale, uint32_t flags, const void *z, const void *norm_w,
+                                    float norm_eps, void *o, float *h_T, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+  gdn_shape s;
+  gdn_status st = layer_shape(shape, width, &s);
+  if (st != GDN_OK) return st;
+  if (flags & ~kLayerFlags) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens) {
+    if (s.B != 1) return GDN_ERR_INVALID_ARG;
+  } else if (s.n_seqs != s.B) {
+    return GDN_ERR_INVALID_ARG;
+  }
+  if (z && ((flags & GDN_FLAG_O_F32) || !(norm_eps >= 0.f))) return GDN_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return GDN_ERR_WORKSPACE;
+  const int64_t n_tok = cu_seqlens ? s.T : (int64_t)s.B * s.T;
+  if (s.n_seqs == 0) return GDN_OK;
+  if (n_tok > 0 && (!x || !conv_w || !a || !b || !A_log || !dt_bias || !o)) return GDN_ERR_INVALID_ARG;
+  if (n_tok > 0 && !aligned(x, s.dtype == GDN_BF16 ? 16 : 4)) return GDN_ERR_INVALID_ARG;
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (n_tok == 0) {  // only h_T = h0 (or 0) per sequence
+    const gdn_shape c = chunk_view(s);
+    return gdn_chunk_fwd(x, x, x, nullptr, nullptr, h0, cu_seqlens, &c, scale, GDN_FLAG_QK_L2NORM, o, h_T,
+                         workspace, workspace_bytes, stream);
+  }
+  if (front_applies(s, width, flags) && chunk_front_supported(x, conv_w, width, s)) {
+    if (workspace_bytes < chunk_front_workspace_bytes(s, n_tok)) return GDN_ERR_WORKSPACE;
+    const FrontArgs fr{x, conv_w, conv_bias, width, a, b, A_log, dt_bias};
+    st = chunk_fwd_front(fr, h0, cu_seqlens, s, scale, flags, o, h_T, workspace, workspace_bytes, cs);
+  } else {
+    if (workspace_bytes < unfused_bytes(s, n_tok)) return GDN_ERR_WORKSPACE;
+    const gdn_shape c = chunk_view(s);
+    const int64_t Cx = c.q_stride;
+    const size_t es = s.dtype == GDN_BF16 ? 2 : 4;
+    const size_t ws_chunk = align256(gdn_chunk_fwd_workspace_bytes(&c));
+    uint8_t *ws = (uint8_t *)workspace;
+    uint8_t *y = ws + ws_chunk;
+    float *g = (float *)(y + align256((size_t)n_tok * Cx * es));
+    float *beta = (float *)((uint8_t *)g + align256((size_t)n_tok * s.Hv * 4));
+    st = gdn_gate_prep(a, b, s.dtype, A_log, dt_bias, n_tok, s.Hv, g, beta, stream);
+    if (st != GDN_OK) return st;
+    st = gdn_conv1d_varlen(x, conv_w, conv_bias, s.dtype, cu_seqlens, s.n_seqs, n_tok, (int32_t)Cx, width, 1,
+                           y, stream);
+    if (st != GDN_OK) return st;
+    st = gdn_chunk_fwd(y, y + (size_t)s.Hqk * s.K * es, y + (size_t)2 * s.Hqk * s.K * es, g, beta, h0, cu_seqlens,
+                       &c, scale, GDN_FLAG_QK_L2NORM | (flags & (GDN_FLAG_O_F32 | GDN_FLAG_SIMT)), o, h_T,
+                       workspace, ws_chunk, stream);
+  }
+  if (st != GDN_OK || !z) return st;
+  return gdn_gated_rmsnorm(o, z, norm_w, s.dtype, n_tok * s.Hv, s.V, norm_eps, o, stream);
 }

@@ -37,6 +37,8 @@
 
 #include "chunk_common.cuh"
 #include "common.cuh"
+#include "conv_tap.cuh"
+#include "gates.cuh"
 #include "sm100.cuh"
 
 using namespace gdn;
@@ -75,6 +77,17 @@ struct OpParams {
   size_t rec_bytes;
   int64_t n_items;  // chunk slots x v-heads
   int32_t *status;
+  // Fused front end (the layer's Q|K|V projections x before the conv): the maps read the
+  // raw q, k and v channels of x, the tiles are conv'd (+ SiLU) in place in shared memory,
+  // the gates come from a and b, and the first v-head of every q/k head writes the conv'd
+  // q and k rows that the scan reads.
+  int front, width;                   // width 1..4 (taps before the last W zero-padded)
+  const __nv_bfloat16 *x, *cw, *cbias;  // x [n_tok][Cx]; weights [Cx][width]; bias [Cx] or null
+  int64_t Cx;
+  const __nv_bfloat16 *ga, *gb;       // a, b [n_tok][Hv]
+  const float *A_log, *dt_bias;       // [Hv]
+  __nv_bfloat16 *qc, *kc;             // conv'd q, k [n_tok][Hqk][128]
+  unsigned long long *claim;          // front end: item-group counter, zero at launch
 };
 
 constexpr int kXP = C + 4;  // fp32 row of A, padded (rows stay 16-byte aligned)
@@ -90,6 +103,24 @@ __host__ __device__ constexpr uint32_t op_vt_stride(int V) { return op_late_v(V)
 // A, then (I + A)^-1, both row-major (row stride kXP), then the T diag(b/|k|) hi / lo tiles
 __host__ __device__ constexpr uint32_t op_x(int V) { return op_late_v(V) ? 32768u : 32768u + (uint32_t)V * 128; }
 __host__ __device__ constexpr uint32_t op_smem(int V) { return op_x(V) + 17408u + 1024; }
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const __nv_bfloat16 *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+// Conv taps of channels chan .. chan + 7 as four taps of fp32 pairs: a width below 4 leaves
+// the first 4 - width taps zero (they multiply finite history rows, so the sums are those of
+// the narrower conv).
+__device__ __forceinline__ void front_weights(const OpParams &p, int64_t chan, uint64_t (&wt)[4][4], uint64_t (&bs)[4]) {
+  const int W = p.width;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t ca = chan + 2 * i, cb = ca + 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      wt[j][i] = (j >= 4 - W) ? f2_pack(__bfloat162float(p.cw[ca * W + j - (4 - W)]),
+                                                     __bfloat162float(p.cw[cb * W + j - (4 - W)]))
+                                           : 0ull;
+    bs[i] = p.cbias ? f2_pack(__bfloat162float(p.cbias[ca]), __bfloat162float(p.cbias[cb])) : 0ull;
+  }
+}
 
 // Y = (I + A)^-1 for the strictly lower 64 x 64 A in X, by forward substitution swept
 // by columns of A: y_i = delta_ij - sum_{k<i} A_ik y_k, and once row k of Y is final every
@@ -130,7 +161,8 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
 template <int V>
 __global__ void __launch_bounds__(128, 4)
     chunk_operand_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const OpParams p) {
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qc,
+                         const __grid_constant__ CUtensorMap tm_kc, const OpParams p) {
   constexpr int NVB = V / 64;                       // 64-column blocks of v
   constexpr uint32_t kCols = (V <= 128) ? 128u : 256u;
   extern __shared__ uint8_t smraw[];
@@ -139,6 +171,11 @@ __global__ void __launch_bounds__(128, 4)
   __shared__ float blast_s;
   __shared__ uint64_t bar, ld_bar;
   __shared__ uint32_t tbase;
+  // front end: the conv history rows of the chunk's first tokens, as 8-channel pieces:
+  // [row][0-15 k, 16-31 q, 32-47 v]
+  __shared__ uint4 halo[3][48];
+  __shared__ int64_t claim_s[2];
+  constexpr bool kFront = V == 128;  // the only width the front end takes
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // A resident block walks the (chunk slot, v-head) items with the grid's stride: TMEM and
   // the barriers are set up once, and the phases of the barriers are counted across items.
@@ -156,8 +193,35 @@ __global__ void __launch_bounds__(128, 4)
   tc_fence_after();
   const uint32_t tm = tbase;
   uint32_t ldp = 0, mp = 0;  // completed phases of ld_bar and bar
+  if (kFront && p.front && blockIdx.x == 0 && tid == 0) p.status[1] = GDN_PATH_FRONT;
+  // In front mode blocks claim groups of G consecutive items from a counter (G = the v-heads
+  // of one q/k head) and walk each group in order: the group's first item convs the q/k
+  // head's tiles and writes them out, and the later items load them back.
+  // Each claim is made one group ahead (thread 32, into the other of two slots), so its
+  // latency overlaps the current group's work.
+  const int G = (kFront && p.front) ? p.Hv / p.Hqk : 1;
+  int64_t group = 0;
+  int jg = G, slot_par = 0;  // item of the current group to run next; slot of its claim
+  // Without the front end (G = 1) the blocks stride over the items instead.
+  if (G > 1 && tid == 32) claim_s[0] = (int64_t)atomicAdd(p.claim, 1ull);
+  bool first = true;
 #pragma unroll 1
-  for (int64_t item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+  for (;;) {
+  if (jg == G) {
+    if (G == 1) {
+      group = first ? (int64_t)blockIdx.x : group + gridDim.x;
+      first = false;
+    } else {
+      __syncthreads();  // this group's claim is stored; the slot the next claim reuses is read
+      group = claim_s[slot_par];
+      slot_par ^= 1;
+      if (tid == 32) claim_s[slot_par] = (int64_t)atomicAdd(p.claim, 1ull);
+    }
+    jg = 0;
+    if (group * G >= p.n_items) break;
+  }
+  const int jv = jg++;  // this item's place in its group
+  const int64_t item = group * G + jv;
   const int h = (int)(item % p.Hv);
   const int64_t slot = item / p.Hv;
   const int qh = h / (p.Hv / p.Hqk);
@@ -186,16 +250,38 @@ __global__ void __launch_bounds__(128, 4)
   if (tid == 0) {
     const int32_t tt = (int32_t)t0;
     mbar_arrive_expect_tx(&ld_bar, (4 + (op_late_v(V) ? 0 : NVB)) * 8192);
-    tma_load_3d(sm + OP_KQ, &tm_k, &ld_bar, 0, qh, tt);
-    tma_load_3d(sm + OP_KQ + 16384, &tm_k, &ld_bar, 64, qh, tt);
-    tma_load_3d(sm + OP_KQ + 8192, &tm_q, &ld_bar, 0, qh, tt);
-    tma_load_3d(sm + OP_KQ + 24576, &tm_q, &ld_bar, 64, qh, tt);
+    const CUtensorMap *mk = jv ? &tm_kc : &tm_k, *mq = jv ? &tm_qc : &tm_q;
+    tma_load_3d(sm + OP_KQ, mk, &ld_bar, 0, qh, tt);
+    tma_load_3d(sm + OP_KQ + 16384, mk, &ld_bar, 64, qh, tt);
+    tma_load_3d(sm + OP_KQ + 8192, mq, &ld_bar, 0, qh, tt);
+    tma_load_3d(sm + OP_KQ + 24576, mq, &ld_bar, 64, qh, tt);
     if (!op_late_v(V))
 #pragma unroll
       for (int nb = 0; nb < NVB; ++nb) tma_load_3d(sm + op_vt(V) + nb * 8192, &tm_v, &ld_bar, nb * 64, h, tt);
   }
-  if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
-  else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
+  if (!kFront || !p.front) {
+    if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
+    else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
+  } else {
+    // gates of the chunk's tokens (gdn_gate_prep's arithmetic), and the conv history rows
+    // of the chunk's first tokens: zero at the sequence's start, else x's previous rows
+    if (tid < C) {
+      float gg = 0.f, bb = 0.f;
+      if (tid < n) {
+        const int64_t ai = (t0 + tid) * p.Hv + h;
+        gdn_gates(__bfloat162float(p.ga[ai]), __bfloat162float(p.gb[ai]), p.A_log[h], p.dt_bias[h], gg, bb);
+      }
+      gam[tid] = gg;
+      bet[tid] = bb;
+    }
+    for (int e = tid + (jv ? 96 : 0); e < 3 * 48; e += 128) {  // later items: v pieces only
+      const int j = (jv ? e - 96 : e) / (jv ? 16 : 48), pc = jv ? 32 + (e - 96) % 16 : e % 48;
+      const int64_t chan = pc < 16 ? (int64_t)(p.Hqk + qh) * KD + pc * 8
+                         : pc < 32 ? (int64_t)qh * KD + (pc - 16) * 8
+                                   : (int64_t)2 * p.Hqk * KD + (int64_t)h * V + (pc - 32) * 8;
+      halo[j][pc] = (c > 0) ? ldg_nc_v4(p.x + (t0 - 3 + j) * p.Cx + chan) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   {
     const bool ok = tid != 0 || mbar_wait(&ld_bar, ldp & 1, kSpin);
     if (__syncthreads_or(!ok)) {
@@ -204,6 +290,51 @@ __global__ void __launch_bounds__(128, 4)
       break;
     }
     ++ldp;
+  }
+  if (kFront && p.front && jv == 0) {
+    // ---- conv (+ SiLU) of the k and q tiles in place: warp w takes rows 16 w .. 16 w + 15,
+    //      lanes 0-15 the k tile and 16-31 the q tile, eight channels a lane
+    const int tile = lane >> 4, pc = lane & 15;
+    const int64_t chan = (int64_t)(tile ? qh : p.Hqk + qh) * KD + pc * 8;
+    uint8_t *base = sm + OP_KQ + (pc >> 3) * 16384 + tile * 8192;
+    const int cin = (pc & 7) * 8;
+    uint64_t wt[4][4], bs[4], hist[3][4];
+    front_weights(p, chan, wt, bs);
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+      unpack8p(warp == 0 ? halo[j][(tile ? 16 : 0) + pc]
+                         : *reinterpret_cast<const uint4 *>(base + sw128_off(16 * warp - 3 + j, cin)),
+               hist[j]);
+    __syncthreads();  // every history row is read before any row is overwritten
+    // the conv'd rows this item owns go to the scan's q / k arrays (past the last
+    // sequence's end, the chunk's remaining rows too)
+    const int64_t last_end = p.cu ? (int64_t)p.cu[p.n_seqs] : p.n_tok;
+    const int64_t lim = (end >= last_end) ? p.n_tok : end;
+    __nv_bfloat16 *dst = (tile ? p.qc : p.kc) + (int64_t)qh * KD + pc * 8;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int row = 16 * warp + r;
+      uint4 *cell = reinterpret_cast<uint4 *>(base + sw128_off(row, cin));
+      uint64_t cur[4], out[4];
+      unpack8p(*cell, cur);
+      conv_row8p<4, 3>(wt, bs, hist, cur, true, out);
+      const uint4 y = pack8p(out);
+      *cell = y;
+      if (t0 + row < lim) *reinterpret_cast<uint4 *>(dst + (t0 + row) * (int64_t)p.Hqk * KD) = y;
+      conv_shift8p<3>(hist, cur);
+    }
+    // the MMAs read the conv'd tiles, and the group's later items load the written rows
+    fence_proxy_async_all();
+    __syncthreads();
+  } else if (kFront && p.front && n < C) {
+    // ---- rows past this sequence's end in tiles loaded back: they may not be written yet
+    for (int e = tid; e < (C - n) * 32; e += 128) {
+      const int r = n + (e >> 5), pcs = e & 31;  // 32 pieces of 16 bytes: k and q, both halves
+      *reinterpret_cast<uint4 *>(sm + OP_KQ + (pcs >> 4) * 16384 + ((pcs >> 3) & 1) * 8192 +
+                                 sw128_off(r, (pcs & 7) * 8)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
   }
   // ---- 1/|k| and 1/|q| from the tiles (two threads per token)
   {
@@ -388,6 +519,31 @@ __global__ void __launch_bounds__(128, 4)
         break;
       }
       ++ldp;
+      if (kFront && p.front) {
+        // ---- conv (+ SiLU) of the v tile in place: rows 8 (tid / 16) .. + 7, eight
+        //      channels (tid % 16) a thread; the first row group's history from halo
+        const int rg = tid >> 4, pc = tid & 15;
+        uint8_t *base = sm + op_vt(V) + (pc >> 3) * op_vt_stride(V);
+        const int cin = (pc & 7) * 8;
+        uint64_t wt[4][4], bs[4], hist[3][4];
+        front_weights(p, (int64_t)2 * p.Hqk * KD + (int64_t)h * V + pc * 8, wt, bs);
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+          unpack8p(rg == 0 ? halo[j][32 + pc] : *reinterpret_cast<const uint4 *>(base + sw128_off(8 * rg - 3 + j, cin)),
+                   hist[j]);
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          uint4 *cell = reinterpret_cast<uint4 *>(base + sw128_off(8 * rg + r, cin));
+          uint64_t cur[4], out[4];
+          unpack8p(*cell, cur);
+          conv_row8p<4, 3>(wt, bs, hist, cur, true, out);
+          *cell = pack8p(out);
+          conv_shift8p<3>(hist, cur);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+      }
     }
     if (tid == 0) {
       if (pass == 0) {
@@ -945,7 +1101,8 @@ namespace {
 
 template <int V>
 gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const OpParams &op, size_t slots, cudaStream_t st) {
+                           const CUtensorMap &mqc, const CUtensorMap &mkc, const OpParams &op, size_t slots,
+                           cudaStream_t st) {
   const size_t smem = op_smem(V);
   if (cudaFuncSetAttribute(chunk_operand_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess ||
@@ -966,7 +1123,8 @@ gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const C
   const size_t grid = std::min(items, (size_t)sms * (size_t)per_sm);
   OpParams q = op;
   q.n_items = (int64_t)items;
-  chunk_operand_kernel<V><<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, q);
+  if (q.front && cudaMemsetAsync(q.claim, 0, sizeof(*q.claim), st) != cudaSuccess) return GDN_ERR_CUDA;
+  chunk_operand_kernel<V><<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, mqc, mkc, q);
   return launch_status();
 }
 
@@ -987,18 +1145,35 @@ size_t chunk_scan_workspace_bytes(const gdn_shape &sh, int64_t n_tok) {
   return kHeader + n_slots(n_tok, sh.n_seqs) * (size_t)sh.Hv * rec_bytes(sh.V);
 }
 
+// The fused front end applies to the Qwen3.5 layer's shape on this path: bf16, K = V = 128,
+// conv width up to 4, and x, the weights, a and b 16-byte aligned (bias and a/b rows any).
+bool chunk_front_supported(const void *x, const void *w, int width, const gdn_shape &sh) {
+  if (sh.dtype != GDN_BF16 || sh.K != KD || sh.V != 128 || width < 1 || width > 4) return false;
+  if (!aligned(x, 16) || !aligned(w, 2)) return false;
+  const int64_t n_tok = (int64_t)sh.B * sh.T;
+  return n_tok < (1LL << 31);
+}
+
+size_t chunk_front_workspace_bytes(const gdn_shape &sh, int64_t n_tok) {
+  return chunk_scan_workspace_bytes(sh, n_tok) + 2 * front_qk_bytes(sh, n_tok);
+}
+
+
 // Both kernels of the split path over `n_seqs` sequences (cu_seqlens `cu`, or rows of
 // sh.T tokens): the operand records, then the state scan over (value-column blocks,
 // v-heads, sequences).  Summary mode scans the K + V columns of [M; S_local] instead.
+// With `fr` (the fused front end) q, k and v are unused: the operand kernel reads x, and the
+// conv'd q and k it writes after the records feed the scan.
 static gdn_status run_scan(const void *q, const void *k, const void *v, const float *g,
                            const float *beta, const float *h0, const int32_t *cu, int n_seqs,
                            int64_t n_tok, const gdn_shape &sh, int64_t q_stride, float scale,
                            uint32_t flags, void *o, float *h_T, bool summary, float *M,
-                           float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st) {
-  gdn_shape rs = sh;
-  rs.n_seqs = n_seqs;
+                           float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st,
+                           const FrontArgs *fr = nullptr) {
   const size_t slots = n_slots(n_tok, n_seqs);
-  if (ws_bytes < kHeader + slots * (size_t)sh.Hv * rec_bytes(sh.V)) return GDN_ERR_WORKSPACE;
+  const size_t rec_end = kHeader + slots * (size_t)sh.Hv * rec_bytes(sh.V);
+  const size_t qk_bytes = fr ? front_qk_bytes(sh, n_tok) : 0;
+  if (ws_bytes < rec_end + 2 * qk_bytes) return GDN_ERR_WORKSPACE;
   int32_t *status = (int32_t *)workspace;
   OpParams op{};
   op.q = (const __nv_bfloat16 *)q;
@@ -1020,17 +1195,43 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
   op.rec = (uint8_t *)workspace + kHeader;
   op.rec_bytes = rec_bytes(sh.V);
   op.status = status;
+  op.claim = reinterpret_cast<unsigned long long *>((uint8_t *)workspace + 8);  // header bytes 8-15
   CUtensorMap mq, mk, mv;
-  if (!make_tile_map(&mq, q, KD, sh.Hqk, n_tok, q_stride) ||
-      !make_tile_map(&mk, k, KD, sh.Hqk, n_tok, sh.k_stride) ||
-      !make_tile_map(&mv, v, sh.V, sh.Hv, n_tok, sh.v_stride))
+  if (fr) {
+    const __nv_bfloat16 *x = (const __nv_bfloat16 *)fr->x;
+    const int64_t Cx = (int64_t)2 * sh.Hqk * KD + (int64_t)sh.Hv * sh.V;
+    op.front = 1;
+    op.width = fr->width;
+    op.x = x;
+    op.cw = (const __nv_bfloat16 *)fr->w;
+    op.cbias = (const __nv_bfloat16 *)fr->bias;
+    op.Cx = Cx;
+    op.ga = (const __nv_bfloat16 *)fr->a;
+    op.gb = (const __nv_bfloat16 *)fr->b;
+    op.A_log = fr->A_log;
+    op.dt_bias = fr->dt_bias;
+    op.qc = (__nv_bfloat16 *)((uint8_t *)workspace + rec_end);
+    op.kc = (__nv_bfloat16 *)((uint8_t *)workspace + rec_end + qk_bytes);
+    if (!make_tile_map(&mq, x, KD, sh.Hqk, n_tok, Cx) ||
+        !make_tile_map(&mk, x + (int64_t)sh.Hqk * KD, KD, sh.Hqk, n_tok, Cx) ||
+        !make_tile_map(&mv, x + (int64_t)2 * sh.Hqk * KD, sh.V, sh.Hv, n_tok, Cx))
+      return GDN_ERR_CUDA;
+  } else if (!make_tile_map(&mq, q, KD, sh.Hqk, n_tok, q_stride) ||
+             !make_tile_map(&mk, k, KD, sh.Hqk, n_tok, sh.k_stride) ||
+             !make_tile_map(&mv, v, sh.V, sh.Hv, n_tok, sh.v_stride)) {
+    return GDN_ERR_CUDA;
+  }
+  // the front end's later items load the conv'd q and k back from the workspace
+  CUtensorMap mqc = mq, mkc = mk;
+  if (fr && (!make_tile_map(&mqc, op.qc, KD, sh.Hqk, n_tok, (int64_t)sh.Hqk * KD) ||
+             !make_tile_map(&mkc, op.kc, KD, sh.Hqk, n_tok, (int64_t)sh.Hqk * KD)))
     return GDN_ERR_CUDA;
   gdn_status r;
   switch (sh.V) {
-    case 64: r = launch_operands<64>(mq, mk, mv, op, slots, st); break;
-    case 128: r = launch_operands<128>(mq, mk, mv, op, slots, st); break;
-    case 192: r = launch_operands<192>(mq, mk, mv, op, slots, st); break;
-    case 256: r = launch_operands<256>(mq, mk, mv, op, slots, st); break;
+    case 64: r = launch_operands<64>(mq, mk, mv, mqc, mkc, op, slots, st); break;
+    case 128: r = launch_operands<128>(mq, mk, mv, mqc, mkc, op, slots, st); break;
+    case 192: r = launch_operands<192>(mq, mk, mv, mqc, mkc, op, slots, st); break;
+    case 256: r = launch_operands<256>(mq, mk, mv, mqc, mkc, op, slots, st); break;
     default: return GDN_ERR_UNSUPPORTED;
   }
   if (r != GDN_OK) return r;
@@ -1055,6 +1256,10 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
                            (int)kScanSmem) != cudaSuccess)
     return GDN_ERR_CUDA;
   const int cols = summary ? KD + sh.V : sh.V;
+  if (fr) {
+    mq = mqc;
+    mk = mkc;
+  }
   chunk_scan_kernel<<<dim3(cols / VS, sh.Hv, n_seqs), NTS, kScanSmem, st>>>(mq, mk, sp);
   return launch_status();
 }
@@ -1075,6 +1280,15 @@ gdn_status summary_scan(const void *k, const void *v, const float *g, const floa
                         cudaStream_t st) {
   return run_scan(k, k, v, g, beta, nullptr, bounds, n_seg, sh.T, sh, sh.k_stride, 1.f, flags,
                   nullptr, nullptr, true, M, S_local, workspace, ws_bytes, st);
+}
+
+// gdn_layer_fwd's fused front end: conv, SiLU and gates inside the operand kernel.
+gdn_status chunk_fwd_front(const FrontArgs &fr, const float *h0, const int32_t *cu, const gdn_shape &sh,
+                           float scale, uint32_t flags, void *o, float *h_T, void *workspace,
+                           size_t ws_bytes, cudaStream_t st) {
+  const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
+  return run_scan(nullptr, nullptr, nullptr, nullptr, nullptr, h0, cu, sh.n_seqs, n_tok, sh, 0, scale,
+                  flags | GDN_FLAG_QK_L2NORM, o, h_T, false, nullptr, nullptr, workspace, ws_bytes, st, &fr);
 }
 
 }  // namespace gdn

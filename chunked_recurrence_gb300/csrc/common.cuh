@@ -48,4 +48,18 @@ inline gdn_status launch_status() {
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Inputs of the fused front end of gdn_layer_fwd: the conv over x's Q|K|V channels and the
+// gates, computed inside the chunk operand kernel.
+struct FrontArgs {
+  const void *x, *w, *bias;
+  int width;
+  const void *a, *b;
+  const float *A_log, *dt_bias;
+};
+
+// bytes of one conv'd q (or k) array [n_tok][Hqk][K] bf16 in the front end's workspace
+inline size_t front_qk_bytes(const gdn_shape &sh, int64_t n_tok) {
+  return ((size_t)n_tok * sh.Hqk * sh.K * 2 + 255) & ~(size_t)255;
+}
+
 }  // namespace gdn

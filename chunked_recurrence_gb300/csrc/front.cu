@@ -6,6 +6,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "conv_tap.cuh"
 #include "gates.cuh"
 #include "sm100.cuh"
 
@@ -264,48 +265,13 @@ __global__ void __launch_bounds__(128, 4) conv1d_kernel(const T *__restrict__ x,
 // mbarrier, so three stages of loads stay in flight while the block computes on the fourth.
 // The run starts W-1 tokens early (at most back to its sequence's start) so the history
 // comes through the same ring.  Runs are sized so that the grid is about one wave of
-// resident blocks.  The conv taps are packed fp32x2 FMAs, in the same order as the scalar
-// chain, and SiLU(x) = x / (1 + e^-x) takes e^-x as 2^(-x log2 e) on the hardware base-2
-// exponential and the division as a hardware reciprocal (both with flush to zero: the
-// results round to bf16 right after).  A wait that gives up (only a failed copy can make it)
+// resident blocks.  Each row's arithmetic is conv_row8 (packed fp32x2 taps in the scalar
+// chain's order, SiLU on the hardware exponential and reciprocal), which the chunk operand
+// kernel's fused front end shares.  A wait that gives up (only a failed copy can make it)
 // leaves NaN in the outputs the block did not compute.
 constexpr int kStageRows = 8, kStages = 4, kStagedCols = 1024;
 constexpr uint32_t kStagedSmem = kStages * kStageRows * kStagedCols * 2;
 constexpr uint32_t kConvSpin = 1u << 22;
-
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t r, float &a, float &b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ float hw_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float hw_rcp(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 template <int W>
 __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat16 *__restrict__ x,
@@ -316,7 +282,6 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
                                                                int act, __nv_bfloat16 *__restrict__ y) {
   using namespace gdn::sm100;
   constexpr int VEC = 8, HW = W > 1 ? W - 1 : 1;
-  constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ __align__(128) uint4 ring[];  // [kStages][kStageRows][kStagedCols / 8]
   __shared__ __align__(8) uint64_t full[kStages];
   const int tid = threadIdx.x;
@@ -355,14 +320,17 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
   };
   if (tid == 0)
     for (int k = 0; k < min(kStages, nst); ++k) issue(k);
-  float wt[W][VEC], bs[VEC], hist[HW][VEC];
+  // taps, bias and history as fp32 pairs (channels c0 + 2i, c0 + 2i + 1)
+  uint64_t wt[W][VEC / 2], bs[VEC / 2], hist[HW][VEC / 2];
 #pragma unroll
-  for (int v = 0; v < VEC; ++v) {
+  for (int i = 0; i < VEC / 2; ++i) {
+    const int64_t ca = c0 + 2 * i, cb = ca + 1;
 #pragma unroll
-    for (int j = 0; j < W; ++j) wt[j][v] = mine ? to_f32(w[(int64_t)(c0 + v) * W + j]) : 0.f;
-    bs[v] = (mine && bias) ? to_f32(bias[c0 + v]) : 0.f;
+    for (int j = 0; j < W; ++j)
+      wt[j][i] = mine ? f2_pack(to_f32(w[ca * W + j]), to_f32(w[cb * W + j])) : 0ull;
+    bs[i] = (mine && bias) ? f2_pack(to_f32(bias[ca]), to_f32(bias[cb])) : 0ull;
 #pragma unroll
-    for (int j = 0; j < HW; ++j) hist[j][v] = 0.f;
+    for (int j = 0; j < HW; ++j) hist[j][i] = 0ull;
   }
   int k = 0;
   for (; k < nst; ++k) {
@@ -374,35 +342,14 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
     const uint4 *rows = ring + st * kStageRows * (kStagedCols / 8) + tid;
     // one token row: its conv output (when `emit`) and the history shift
     auto conv_row = [&](const uint4 &raw, int64_t t, bool emit) {
-      float cur[VEC];
-      Vec<__nv_bfloat16, VEC>::cvt(raw, cur);
+      uint64_t cur[VEC / 2];
+      unpack8p(raw, cur);
       if (emit) {
-        float out[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; v += 2) {
-          uint64_t acc = f2_pack(bs[v], bs[v + 1]);
-#pragma unroll
-          for (int j = 0; j < W - 1; ++j)
-            acc = f2_fma(f2_pack(wt[j][v], wt[j][v + 1]), f2_pack(hist[j][v], hist[j][v + 1]), acc);
-          acc = f2_fma(f2_pack(wt[W - 1][v], wt[W - 1][v + 1]), f2_pack(cur[v], cur[v + 1]), acc);
-          if (act) {
-            float e0, e1, d0, d1;
-            f2_unpack(f2_mul(acc, f2_pack(-kLog2e, -kLog2e)), e0, e1);
-            f2_unpack(f2_add(f2_pack(hw_exp2(e0), hw_exp2(e1)), f2_pack(1.f, 1.f)), d0, d1);
-            acc = f2_mul(acc, f2_pack(hw_rcp(d0), hw_rcp(d1)));
-          }
-          f2_unpack(acc, out[v], out[v + 1]);
-        }
-        Vec<__nv_bfloat16, VEC>::store(y + t * C + c0, out);
+        uint64_t out[VEC / 2];
+        conv_row8p<W, HW>(wt, bs, hist, cur, act != 0, out);
+        *reinterpret_cast<uint4 *>(y + t * C + c0) = pack8p(out);
       }
-      if (W > 1) {
-#pragma unroll
-        for (int j = 0; j + 1 < HW; ++j)
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) hist[j][v] = hist[j + 1][v];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) hist[HW - 1][v] = cur[v];
-      }
+      if (W > 1) conv_shift8p<HW>(hist, cur);
     };
     if (m == kStageRows && a >= t0 && a + kStageRows <= end && mine) {
       // the whole stage lies inside one sequence and past the history rows: straight-line
@@ -429,7 +376,7 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
 #pragma unroll
           for (int j = 0; j < HW; ++j)
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) hist[j][v] = 0.f;
+            for (int v = 0; v < VEC / 2; ++v) hist[j][v] = 0ull;
         }
         conv_row(rows[i * (kStagedCols / 8)], t, t >= t0 && mine);
       }

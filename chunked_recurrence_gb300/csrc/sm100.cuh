@@ -133,6 +133,11 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// the same for generic-proxy writes to shared and global memory (a later TMA load of rows
+// this CTA stored)
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
 
 // -------------------------------------------------------------- tcgen05
 

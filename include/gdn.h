@@ -59,6 +59,8 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_FLAG_FUSED 8u      /* gdn_chunk_fwd (bf16, K = V = 128): the fused persistent kernel instead of the two-kernel path */
 #define GDN_FLAG_TEST_NO_WAIT 16u /* test only, with GDN_FLAG_FUSED: every bounded wait of the fused kernel gives
                                    * up at its first check, so the call ends with GDN_ERR_TIMEOUT in the status word */
+#define GDN_FLAG_LAYER_FRONT 32u /* gdn_layer_fwd: the fused front end (conv and gates inside the chunk operand
+                                  * kernel) instead of separate launches, where the shape allows it */
 
 /* Problem shape of the recurrence. */
 typedef struct {
@@ -104,6 +106,7 @@ gdn_status gdn_workspace_reset(void *workspace, size_t workspace_bytes, void *st
  * paths leave the word as they found it, and gdn_workspace_reset clears it, so
  * after a reset a value of 0 means another path ran. */
 #define GDN_PATH_FUSED 1
+#define GDN_PATH_FRONT 2 /* gdn_layer_fwd's fused front end (conv and gates inside the operand kernel) */
 
 /* Copy the path word (see GDN_PATH_FUSED) of `workspace` to *path_out (host) and
  * synchronise `stream`. */
@@ -268,6 +271,42 @@ gdn_status gdn_decode_step(const void *x, const void *conv_state_in, void *conv_
  *   overlap y.  n_rows may be 0. */
 gdn_status gdn_gated_rmsnorm(const void *o, const void *z, const void *w, int32_t dtype, int64_t n_rows,
                              int32_t V, float eps, void *y, void *stream);
+
+/* The layer's forward in one call ("[v1] support GDN Ulysses cp", What This PR Does and
+ * Key decisions 5: the causal conv over the concatenated Q|K|V projections, given cu_seqlens
+ * so that packed samples never read each other's tokens, then chunk_gated_delta_rule, then
+ * the norm):
+ *   y     = SiLU(conv1d(x))            (gdn_conv1d_varlen with act = 1, y rounded to dtype)
+ *   q, k, v = y's channels [0, Hqk K), [Hqk K, 2 Hqk K), [2 Hqk K, C); q and k L2-normalised
+ *   g, beta = gdn_gate_prep(a, b, A_log, dt_bias)
+ *   o, h_T  = gdn_chunk_fwd(q, k, v, g, beta, h0, cu_seqlens, scale)
+ *   o      <- gdn_gated_rmsnorm(o, z, norm_w, norm_eps)  when z is not NULL
+ * Arguments:
+ *   x:          [tokens, C] of shape->dtype, C = 2 Hqk K + Hv V, dense, 16-byte aligned
+ *   conv_w:     [C, width] of shape->dtype, 1 <= width <= 8;  conv_bias: [C] or NULL
+ *   a, b:       [tokens, Hv] of shape->dtype;  A_log, dt_bias: [Hv] fp32
+ *   h0, cu_seqlens, scale, o, h_T: as for gdn_chunk_fwd (shape's strides must be 0)
+ *   flags:      GDN_FLAG_O_F32, GDN_FLAG_SIMT, GDN_FLAG_LAYER_FRONT
+ *   z:          [tokens, Hv, V] of shape->dtype or NULL (no norm);  norm_w: [V] or NULL
+ *               (ones); norm_eps >= 0.  With z, GDN_FLAG_O_F32 is GDN_ERR_INVALID_ARG.
+ *   workspace:  at least gdn_layer_fwd_workspace_bytes(shape, width, flags), 256-byte aligned
+ * By default the four steps run as their own launches, with y, g and beta in the workspace.
+ * GDN_FLAG_LAYER_FRONT with bf16, K = V = 128 and width <= 4 takes the fused front end
+ * instead: the chunk operand kernel reads x's rows (a chunk and the 3 rows before it, zero
+ * before the sample's start), applies the conv and SiLU in shared memory and computes the
+ * gates, so neither y nor g and beta go to memory (only the conv'd q and k, which the state
+ * scan reads again, sit in the workspace: about n_tok * C * 2 bytes less of it).  Its y
+ * values are those of gdn_conv1d_varlen's staged bf16 kernel bit for bit, so the results
+ * equal the default path's.  It sets the path word to GDN_PATH_FRONT.  (On a GB300 at the
+ * Qwen3.5-4B layer's shape it measures a few percent slower than the separate launches: the
+ * conv's arithmetic lengthens the latency-bound operand kernel by more than the separate
+ * conv costs.)  x, o and z must not overlap; o may not alias the workspace. */
+size_t gdn_layer_fwd_workspace_bytes(const gdn_shape *shape, int32_t width, uint32_t flags);
+gdn_status gdn_layer_fwd(const void *x, const void *conv_w, const void *conv_bias, int32_t width,
+                         const void *a, const void *b, const float *A_log, const float *dt_bias,
+                         const float *h0, const int32_t *cu_seqlens, const gdn_shape *shape, float scale,
+                         uint32_t flags, const void *z, const void *norm_w, float norm_eps, void *o,
+                         float *h_T, void *workspace, size_t workspace_bytes, void *stream);
 
 /* fp32 chain reduce of the segment summaries ("Qwen3.5 cp - #1",
  * Architecture: (b, M) chain reduce, fp32):

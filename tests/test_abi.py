@@ -205,8 +205,43 @@ def test_flag_values_match_header_and_test_mode_is_off_by_default():
     import chunked_recurrence_gb300 as crg
     hdr = open(os.path.join(ROOT, "include", "gdn.h")).read()
     defs = {k: int(v) for k, v in re.findall(r"#define (GDN_FLAG_\w+) (\d+)u", hdr)}
+    defs.update({k: int(v) for k, v in re.findall(r"#define (GDN_PATH_\w+) (\d+)", hdr)})
+    assert "GDN_FLAG_LAYER_FRONT" in defs and "GDN_PATH_FRONT" in defs
     for name, val in defs.items():
         assert getattr(crg, name) == val, name
     assert inspect.signature(crg.gdn_chunk_fwd).parameters["_test_no_wait"].default is False
     src = inspect.getsource(crg)
     assert src.count("GDN_FLAG_TEST_NO_WAIT if _test_no_wait") == 1
+
+
+def test_layer_fwd_argument_errors_return_before_launch(lib):
+    """gdn_layer_fwd checks the conv width, the flags, dense strides, the norm's arguments, the
+    alignment of x and the workspace before anything runs."""
+    P = ctypes.c_void_p
+    fake, ws = P(0x10000), P(0x20000)  # never dereferenced
+    sh = _shape()
+    sz = lambda s, w, f: lib.gdn_layer_fwd_workspace_bytes(ctypes.byref(s), w, f)
+    assert sz(sh, 4, 0) > 0 and sz(sh, 4, 32) > 0
+    assert sz(sh, 0, 0) == 0 and sz(sh, 9, 0) == 0       # width 1..8
+    assert sz(sh, 4, 1) == 0 and sz(sh, 4, 8) == 0       # flags the layer call does not take
+    assert sz(_shape(q_stride=512), 4, 0) == 0           # x is dense: strides must be 0
+    # the fused front end needs no room for y, g and beta
+    assert sz(sh, 4, 32) < sz(sh, 4, 0)
+
+    def call(x=fake, w=fake, width=4, shape=sh, flags=0, z=None, eps=1e-6, o_ptr=fake, ws_ptr=ws, nbytes=1 << 30):
+        return lib.gdn_layer_fwd(x, w, None, width, fake, fake, fake, fake, None, None, ctypes.byref(shape),
+                                 1.0, flags, z, None, eps, o_ptr, None, ws_ptr, nbytes, None)
+    assert call(width=9) == 1
+    assert call(flags=8) == 1
+    assert call(z=fake, flags=4) == 1                    # the norm writes o in the input dtype
+    assert call(z=fake, eps=-1.0) == 1
+    assert call(x=P(0x10008)) == 1                       # x not 16-byte aligned
+    assert call(x=None) == 1
+    assert call(ws_ptr=None) == 5
+    assert call(ws_ptr=P(0x20040)) == 5                  # workspace not 256-byte aligned
+    assert call(nbytes=256) == 5                         # too small
+    assert call(nbytes=256, flags=32) == 5              # too small for the front end
+    # zero sequences (cu_seqlens of one entry) is a no-op
+    assert lib.gdn_layer_fwd(None, None, None, 4, None, None, None, None, None, fake,
+                             ctypes.byref(_shape(n_seqs=0, T=0)), 1.0, 0, None, None, 1e-6, None, None, ws,
+                             256, None) == 0

@@ -25,6 +25,17 @@ def test_headline_work_matches_the_hand_count():
     assert bench.conv_bytes(wl, n_tok) == 8192 * 8192 * 2 * 2 + 8192 * 4 * 2
 
 
+def test_layer_work_matches_the_hand_count():
+    """gdn_layer_fwd on the 4B-shaped layer, by hand: per token x's 8192 channels (16 KiB
+    bf16), a and b (32 v-heads x 2 x 2 B) and o (32 x 128 x 2 B); the conv weights
+    (8192 x 4 bf16) and A_log, dt_bias (32 x 2 fp32) once; h_T (32 x 128 x 128 fp32)."""
+    wl = synth.WORKLOADS["qwen35_4b_layer"]
+    per_tok = 8192 * 2 + 32 * 4 + 32 * 128 * 2
+    assert bench.layer_bytes(wl, 8192, 1) == 8192 * per_tok + 8192 * 4 * 2 + 32 * 8 + 32 * 128 * 128 * 4
+    assert bench.layer_bytes(wl, 8192, 1) == 204_538_112  # 8192 x 24,704 + 65,536 + 256 + 2,097,152
+    assert bench.layer_bytes(wl, 10, 2, True) - bench.layer_bytes(wl, 10, 2) == 2 * 32 * 128 * 128 * 4
+
+
 def test_chunk_bytes_counts_h0_when_given():
     wl = synth.WORKLOADS["qwen35_4b_layer"]
     assert bench.chunk_bytes(wl, 100, 3, True) - bench.chunk_bytes(wl, 100, 3, False) == 3 * 32 * 128 * 128 * 4

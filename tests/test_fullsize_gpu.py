@@ -67,11 +67,18 @@ def _oracle_layer(inp, cu_host, seqs, heads, n_threads=None):
     return out
 
 
-def _run_layer(crg, inp, cu):
+def _run_layer(crg, inp, cu, front=False):
+    """gdn_layer_fwd as bench.py calls it (front=True: the fused front end, checked to have run)."""
     wl = inp["workload"]
+    sh = crg.layer_shape(inp["x"], wl.Hqk, wl.Hv, wl.K, wl.V, cu, wl.B)
+    flags = crg.GDN_FLAG_LAYER_FRONT if front else 0
+    ws = crg.Workspace(crg.gdn_layer_fwd_workspace_bytes(sh, wl.conv_width, flags), DEV)
     r = crg.layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
-                      wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"])
+                      wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"],
+                      bufs={"workspace": ws}, front=front)
     torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert ws.path() == (crg.GDN_PATH_FRONT if front else 0)
     return r
 
 
@@ -82,22 +89,24 @@ def _check(r, ref, cu_host, what):
         assert_close(r["h_T"][s, h].cpu(), rh, "bf16", f"{what} h_T seq {s} head {h}")
 
 
-def test_qwen35_4b_layer_full(crg):
+@pytest.mark.parametrize("front", [False, True])
+def test_qwen35_4b_layer_full(crg, front):
     inp = synth.make_inputs("qwen35_4b_layer", device=DEV, with_direct=False)
-    r = _run_layer(crg, inp, None)
+    r = _run_layer(crg, inp, None, front)
     cu = np.array([0, inp["n_tok"]])
     ref = _oracle_layer(inp, cu, [0], [0, 13, 31])
     _check(r, ref, cu, "4B layer")
 
 
-def test_packed_full(crg):
+@pytest.mark.parametrize("front", [False, True])
+def test_packed_full(crg, front):
     inp = synth.make_inputs("packed", device=DEV, with_direct=False)
     cu_full, cnt = crg.gdn_cu_seqlens_from_position_ids(inp["position_ids"])
     n = int(cnt.item())
     cu = cu_full[: n + 1]
     cu_host = cu.cpu().numpy()
     assert n == 12 and np.array_equal(cu_host, inp["cu_seqlens"].cpu().numpy())
-    r = _run_layer(crg, inp, cu)
+    r = _run_layer(crg, inp, cu, front)
     ref = _oracle_layer(inp, cu_host, [0, 5, 11], [1, 30])
     _check(r, ref, cu_host, "packed")
 
