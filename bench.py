@@ -318,6 +318,7 @@ def run_gpu_arm(args, ws, rank, local):
     }
     chunk_roofline = roofline_entry(cb, cf, chunk_ms, peaks)
     front = time_front_layer(crg, wl, inp, cu, stream, flush)
+    with_norm = time_norm_layer(crg, wl, inp, cu, stream, flush)
     layer_paths = {"separate_launches_ms_median": round(step_ms_median, 5),
                    "separate_launches_unwrapped_ms_median": round(unf["total_ms"], 5),
                    "fused_front_ms_median": round(front["ms"], 5),
@@ -365,6 +366,7 @@ def run_gpu_arm(args, ws, rank, local):
         "kernels": kernels,
         "chunk_fwd_roofline": chunk_roofline,
         "layer_paths": layer_paths,
+        "layer_with_norm": with_norm,
         "chunk_fwd_paths": paths,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -446,6 +448,45 @@ def time_front_layer(crg, wl, inp, cu, stream, flush, reps=30):
         if it >= 3:
             ts.append(e0.elapsed_time(e1))
     return {"ms": statistics.median(ts), "path_word": ws.path(), "workspace_bytes": ws.nbytes}
+
+
+def time_norm_layer(crg, wl, inp, cu, stream, flush, reps=30):
+    """The layer with its gated norm ("+ norm"): z and the norm weight from synth.norm_inputs.
+    gdn_layer_fwd with z and GDN_FLAG_LAYER_NORM_EPILOGUE (the norm in the scan's output
+    epilogue) against gdn_layer_fwd followed by gdn_gated_rmsnorm; L2 flushed before each,
+    medians."""
+    n_tok = inp["n_tok"]
+    nz = synth.norm_inputs((n_tok, wl.Hv), wl.V, wl.dtype, seed=40606, device=inp["x"].device)
+    sh = crg.layer_shape(inp["x"], wl.Hqk, wl.Hv, wl.K, wl.V, cu, wl.B)
+    ws = crg.Workspace(crg.gdn_layer_fwd_workspace_bytes(sh, wl.conv_width, 0), inp["x"].device)
+    o = torch.empty((n_tok, wl.Hv, wl.V), device=inp["x"].device, dtype=wl.torch_dtype)
+    h_T = torch.empty((inp["n_seq"], wl.Hv, wl.V, wl.K), device=inp["x"].device)
+    B = None if cu is not None else wl.B
+    out = {}
+    for name in ("epilogue", "separate"):
+        ws.reset()
+        ts = []
+        for it in range(reps + 3):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if name == "epilogue":
+                crg.gdn_layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
+                                  wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"], z=nz["z"],
+                                  norm_w=nz["w"], o=o, h_T=h_T, workspace=ws, norm_epilogue=True)
+            else:
+                crg.gdn_layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
+                                  wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"], o=o, h_T=h_T,
+                                  workspace=ws)
+                crg.gdn_gated_rmsnorm(o, nz["z"], nz["w"], y=o)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 3:
+                ts.append(e0.elapsed_time(e1))
+        out[name + "_ms_median"] = round(statistics.median(ts), 5)
+        out[name + "_path_word"] = ws.path()
+    del B
+    return out
 
 
 def time_unfused_layer(crg, wl, inp, cu, stream, flush, reps=30):

@@ -21,7 +21,8 @@ from . import build as _build
 GDN_OK = 0
 GDN_ERR_TIMEOUT, GDN_ERR_BOUNDS = 4, 6  # device-side statuses read from a workspace
 GDN_PATH_FUSED = 1                      # path word of a workspace after the fused kernel ran
-GDN_PATH_FRONT = 2                      # ... after gdn_layer_fwd's fused front end ran
+GDN_PATH_FRONT = 2                      # bit: gdn_layer_fwd's fused front end ran
+GDN_PATH_NORM = 4                       # bit: gdn_layer_fwd's norm ran in the scan's epilogue
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_SIMT = 2
@@ -29,6 +30,7 @@ GDN_FLAG_O_F32 = 4
 GDN_FLAG_FUSED = 8
 GDN_FLAG_TEST_NO_WAIT = 16
 GDN_FLAG_LAYER_FRONT = 32
+GDN_FLAG_LAYER_NORM_EPILOGUE = 64
 CHUNK = 64
 
 _lib = None
@@ -492,13 +494,15 @@ def gdn_layer_fwd_workspace_bytes(shape: GdnShape, width: int, flags: int = 0) -
 
 def gdn_layer_fwd(x, conv_w, a, b, A_log, dt_bias, Hqk, Hv, K, V, h0=None, cu_seqlens=None, B=1,
                   scale=None, conv_bias=None, z=None, norm_w=None, norm_eps=1e-6, o=None, h_T=None,
-                  want_h_T=True, o_f32=False, simt=False, front=False, workspace=None, stream=None):
+                  want_h_T=True, o_f32=False, simt=False, front=False, norm_epilogue=False, workspace=None,
+                  stream=None):
     """The layer's forward in one call: conv1d+SiLU over x's Q|K|V channels, gates, the
     chunked rule with q/k L2 norm and, with z, the gated RMS norm of o.  Returns (o, h_T).
 
     By default gate prep, conv and gdn_chunk_fwd run as separate launches; front=True (bf16,
     K = V = 128, conv width <= 4) runs the fused front end instead (conv and gates inside the
-    chunk operand kernel, same results bit for bit)."""
+    chunk operand kernel, same results bit for bit).  With z the gated norm runs as the
+    standalone kernel, or with norm_epilogue=True in the state scan's output epilogue."""
     _need_cuda(x, conv_w, a, b, A_log, dt_bias, h0, cu_seqlens, z, norm_w, conv_bias)
     for n, t in (("x", x), ("conv_w", conv_w), ("a", a), ("b", b), ("A_log", A_log),
                  ("dt_bias", dt_bias), ("h0", h0), ("z", z), ("norm_w", norm_w), ("conv_bias", conv_bias)):
@@ -511,7 +515,8 @@ def gdn_layer_fwd(x, conv_w, a, b, A_log, dt_bias, Hqk, Hv, K, V, h0=None, cu_se
     if scale is None:
         scale = K ** -0.5
     flags = ((GDN_FLAG_O_F32 if o_f32 else 0) | (GDN_FLAG_SIMT if simt else 0)
-             | (GDN_FLAG_LAYER_FRONT if front else 0))
+             | (GDN_FLAG_LAYER_FRONT if front else 0)
+             | (GDN_FLAG_LAYER_NORM_EPILOGUE if norm_epilogue else 0))
     o_dtype = torch.float32 if o_f32 else x.dtype
     if o is None:
         o = torch.empty((n_tok, Hv, V), device=x.device, dtype=o_dtype)

@@ -20,7 +20,8 @@ size_t chunk_scan_workspace_bytes(const gdn_shape &sh, int64_t n_tok);
 gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, const int32_t *cu,
                           const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
-                          void *workspace, size_t ws_bytes, cudaStream_t st);
+                          void *workspace, size_t ws_bytes, cudaStream_t st, const NormArgs *nm);
+bool chunk_norm_supported(const gdn_shape &sh, uint32_t flags, const NormArgs &nm);
 gdn_status chunk_fwd_tc(const void *q, const void *k, const void *v, const float *g,
                         const float *beta, const float *h0, const int32_t *cu,
                         const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
@@ -39,7 +40,7 @@ bool chunk_front_supported(const void *x, const void *w, int width, const gdn_sh
 size_t chunk_front_workspace_bytes(const gdn_shape &sh, int64_t n_tok);
 gdn_status chunk_fwd_front(const FrontArgs &fr, const float *h0, const int32_t *cu, const gdn_shape &sh,
                            float scale, uint32_t flags, void *o, float *h_T, void *workspace,
-                           size_t ws_bytes, cudaStream_t st);
+                           size_t ws_bytes, cudaStream_t st, const NormArgs *nm);
 gdn_status summary_tc(const void *k, const void *v, const float *g, const float *beta,
                       const int32_t *bounds, int n_seg, const gdn_shape &sh, uint32_t flags,
                       float *M, float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st);
@@ -114,11 +115,14 @@ extern "C" size_t gdn_segment_summary_workspace_bytes(const gdn_shape *shape, in
   return kWorkspaceBase;
 }
 
-extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
-                                    const float *beta, const float *h0, const int32_t *cu_seqlens,
-                                    const gdn_shape *shape, float scale, uint32_t flags, void *o,
-                                    float *h_T, void *workspace, size_t workspace_bytes,
-                                    void *stream) {
+// gdn_chunk_fwd's dispatch.  With nm (gdn_layer_fwd's gated norm), the split scan applies the
+// norm in its output epilogue where it can and sets *norm_done; other paths leave it false.
+static gdn_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const float *h0, const int32_t *cu_seqlens,
+                                 const gdn_shape *shape, float scale, uint32_t flags, void *o,
+                                 float *h_T, void *workspace, size_t workspace_bytes, void *stream,
+                                 const NormArgs *nm, bool *norm_done) {
+  if (norm_done) *norm_done = false;
   gdn_shape s;
   gdn_status st = normalise_shape(shape, &s);
   if (st != GDN_OK) return st;
@@ -145,14 +149,28 @@ extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
   }
   if (!(flags & GDN_FLAG_SIMT) && n_tok > 0 && tc_shape(s) && chunk_tc_supported(q, k, v, s)) {
     if (scan_shape(s) && chunk_scan_supported(q, k, v, s) &&
-        workspace_bytes >= chunk_scan_workspace_bytes(s, n_tok))
-      return chunk_fwd_scan(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T, workspace,
-                            workspace_bytes, (cudaStream_t)stream);
+        workspace_bytes >= chunk_scan_workspace_bytes(s, n_tok)) {
+      const bool fuse_norm = nm && chunk_norm_supported(s, flags, *nm);
+      const gdn_status r = chunk_fwd_scan(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
+                                          workspace, workspace_bytes, (cudaStream_t)stream,
+                                          fuse_norm ? nm : nullptr);
+      if (norm_done) *norm_done = fuse_norm && r == GDN_OK;
+      return r;
+    }
     return chunk_fwd_tc(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T, workspace,
                         workspace_bytes, (cudaStream_t)stream);
   }
   return chunk_fwd_simt(q, k, v, g, beta, h0, cu_seqlens, s, scale, flags, o, h_T,
                         (int32_t *)workspace, (cudaStream_t)stream);
+}
+
+extern "C" gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, const float *h0, const int32_t *cu_seqlens,
+                                    const gdn_shape *shape, float scale, uint32_t flags, void *o,
+                                    float *h_T, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+  return chunk_fwd_impl(q, k, v, g, beta, h0, cu_seqlens, shape, scale, flags, o, h_T, workspace,
+                        workspace_bytes, stream, nullptr, nullptr);
 }
 
 extern "C" gdn_status gdn_segment_summary(const void *k, const void *v, const float *g,
@@ -188,7 +206,8 @@ extern "C" gdn_status gdn_segment_summary(const void *k, const void *v, const fl
 
 namespace {
 
-constexpr uint32_t kLayerFlags = GDN_FLAG_O_F32 | GDN_FLAG_SIMT | GDN_FLAG_LAYER_FRONT;
+constexpr uint32_t kLayerFlags =
+    GDN_FLAG_O_F32 | GDN_FLAG_SIMT | GDN_FLAG_LAYER_FRONT | GDN_FLAG_LAYER_NORM_EPILOGUE;
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
@@ -257,10 +276,16 @@ extern "C" gdn_status gdn_layer_fwd(const void *x, const void *conv_w, const voi
     return gdn_chunk_fwd(x, x, x, nullptr, nullptr, h0, cu_seqlens, &c, scale, GDN_FLAG_QK_L2NORM, o, h_T,
                          workspace, workspace_bytes, stream);
   }
+  const NormArgs nm{z, norm_w, norm_eps};
+  const bool want_epilogue = z && (flags & GDN_FLAG_LAYER_NORM_EPILOGUE);
+  bool norm_done = false;
   if (front_applies(s, width, flags) && chunk_front_supported(x, conv_w, width, s)) {
     if (workspace_bytes < chunk_front_workspace_bytes(s, n_tok)) return GDN_ERR_WORKSPACE;
     const FrontArgs fr{x, conv_w, conv_bias, width, a, b, A_log, dt_bias};
-    st = chunk_fwd_front(fr, h0, cu_seqlens, s, scale, flags, o, h_T, workspace, workspace_bytes, cs);
+    const bool fuse_norm = want_epilogue && chunk_norm_supported(s, flags, nm);
+    st = chunk_fwd_front(fr, h0, cu_seqlens, s, scale, flags, o, h_T, workspace, workspace_bytes, cs,
+                         fuse_norm ? &nm : nullptr);
+    norm_done = fuse_norm;
   } else {
     if (workspace_bytes < unfused_bytes(s, n_tok)) return GDN_ERR_WORKSPACE;
     const gdn_shape c = chunk_view(s);
@@ -276,10 +301,10 @@ extern "C" gdn_status gdn_layer_fwd(const void *x, const void *conv_w, const voi
     st = gdn_conv1d_varlen(x, conv_w, conv_bias, s.dtype, cu_seqlens, s.n_seqs, n_tok, (int32_t)Cx, width, 1,
                            y, stream);
     if (st != GDN_OK) return st;
-    st = gdn_chunk_fwd(y, y + (size_t)s.Hqk * s.K * es, y + (size_t)2 * s.Hqk * s.K * es, g, beta, h0, cu_seqlens,
-                       &c, scale, GDN_FLAG_QK_L2NORM | (flags & (GDN_FLAG_O_F32 | GDN_FLAG_SIMT)), o, h_T,
-                       workspace, ws_chunk, stream);
+    st = chunk_fwd_impl(y, y + (size_t)s.Hqk * s.K * es, y + (size_t)2 * s.Hqk * s.K * es, g, beta, h0,
+                        cu_seqlens, &c, scale, GDN_FLAG_QK_L2NORM | (flags & (GDN_FLAG_O_F32 | GDN_FLAG_SIMT)), o,
+                        h_T, workspace, ws_chunk, stream, want_epilogue ? &nm : nullptr, &norm_done);
   }
-  if (st != GDN_OK || !z) return st;
+  if (st != GDN_OK || !z || norm_done) return st;
   return gdn_gated_rmsnorm(o, z, norm_w, s.dtype, n_tok * s.Hv, s.V, norm_eps, o, stream);
 }

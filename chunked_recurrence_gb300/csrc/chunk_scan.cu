@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(128, 4)
   tc_fence_after();
   const uint32_t tm = tbase;
   uint32_t ldp = 0, mp = 0;  // completed phases of ld_bar and bar
-  if (kFront && p.front && blockIdx.x == 0 && tid == 0) p.status[1] = GDN_PATH_FRONT;
+  if (kFront && p.front && blockIdx.x == 0 && tid == 0) atomicOr(p.status + 1, GDN_PATH_FRONT);
   // In front mode blocks claim groups of G consecutive items from a counter (G = the v-heads
   // of one q/k head) and walk each group in order: the group's first item convs the q/k
   // head's tiles and writes them out, and the later items load them back.
@@ -647,6 +647,11 @@ struct ScanParams {
   // S_local (start 0); no output, q unused
   int summary;
   float *M, *S_local;
+  // gated RMS norm of o in the output epilogue: the V / 32 blocks of one (v-head, sequence)
+  // form a cluster and exchange each token's partial sum of squares
+  int norm;
+  const __nv_bfloat16 *z, *nw;  // z [n_tok][Hv][V]; the norm weight [V] or null (ones)
+  float eps;
 };
 
 // warps 0-7: state path; 8, 9, 12, 13: outputs; 10: copies; 11: MMAs
@@ -664,7 +669,9 @@ constexpr int kStages = 3;                 // chunks of operands in flight
 constexpr uint32_t SC_ST = kStages * kStage;  // S^T bf16 [128 features][32 values] SW64
 constexpr uint32_t SC_UP = SC_ST + 8192;      // [U'_hi | U'_lo] [64 tokens][64] SW128
 constexpr uint32_t SC_DU = SC_UP + 8192;      // [dU'_hi | dU'_lo] [64 tokens][64] SW128
-constexpr uint32_t kScanSmem = SC_DU + 8192 + 1024;
+constexpr uint32_t SC_NP = SC_DU + 8192;      // norm: [2 chunk slots][4 ranks][2 halves][64 tokens] fp32
+constexpr int kNormRanks = 4;                 // the norm epilogue takes V <= 128
+constexpr uint32_t kScanSmem = SC_NP + 2 * kNormRanks * 2 * 64 * 4 + 1024;
 // TMEM columns
 constexpr uint32_t TC_A = 0;    // 3 x 32: q S^T in lanes 0-63, -W S^T in lanes 64-127
 constexpr uint32_t TC_O = 96;   // 64: [P U'_hi | P U'_lo] in lanes 0-63
@@ -672,7 +679,7 @@ constexpr uint32_t TC_S = 160;  // 64: [K^T dU'_hi | K^T dU'_lo], one lane per k
 constexpr uint32_t kScanCols = 256;
 
 struct ScanShared {
-  uint64_t full[kStages], empty[kStages], ga, b1, b2, epa, epa2, epb, outd;
+  uint64_t full[kStages], empty[kStages], ga, b1, b2, epa, epa2, epb, outd, nbar[2];
   uint32_t tbase;
   int abort;
   int fills[kStages];    // loads issued into each stage
@@ -736,6 +743,10 @@ __global__ void __launch_bounds__(NTS, 1)
     mbar_init(&sh.epa2, 4);
     mbar_init(&sh.epb, 8);
     mbar_init(&sh.outd, 4);
+    if (p.norm) {  // one local arrival a chunk (with the bytes the cluster's partials bring)
+      mbar_init(&sh.nbar[0], 1);
+      mbar_init(&sh.nbar[1], 1);
+    }
     sh.abort = 0;
     sh.mma_bar = nullptr;
     sh.mma_par = 0;
@@ -748,6 +759,9 @@ __global__ void __launch_bounds__(NTS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (p.norm) cluster_sync_all();  // the peers' barriers are initialised before any remote arrival
+  if (p.norm && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0)
+    atomicOr(p.status + 1, GDN_PATH_NORM);
   const uint32_t tm = sh.tbase;
   auto fail = [&]() {
     *abort_flag = 1;
@@ -987,6 +1001,22 @@ __global__ void __launch_bounds__(NTS, 1)
     const int cb = hc * 16;
     const int i = quarter * 32 + lane;
     const size_t o_tok = (size_t)p.Hv * p.V;
+    const uint32_t rank = p.norm ? cluster_ctarank() : 0u, n_ranks = gridDim.x;
+    float wv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) wv[j] = (p.norm && p.nw) ? __bfloat162float(p.nw[v0 + cb + j]) : 1.f;
+    // the norm's z of this token's 16 columns, loaded a chunk ahead of its use
+    auto load_z = [&](int cj, uint4 &za, uint4 &zb) {
+      za = zb = make_uint4(0u, 0u, 0u, 0u);
+      const int64_t tj = start + (int64_t)cj * C + i;
+      if (cj < n_chunks && tj < end) {
+        const uint4 *zp = reinterpret_cast<const uint4 *>(p.z + (size_t)tj * o_tok + (size_t)h * p.V + v0 + cb);
+        za = __ldg(zp);
+        zb = __ldg(zp + 1);
+      }
+    };
+    uint4 zc0 = make_uint4(0u, 0u, 0u, 0u), zc1 = zc0;
+    if (p.norm && !summary) load_z(0, zc0, zc1);
     bool ok = true;
     for (int ci = 0; ci < n_chunks; ++ci) {
       const int st = ci % kStages;
@@ -1006,6 +1036,8 @@ __global__ void __launch_bounds__(NTS, 1)
         break;
       }
       tc_fence_after();
+      uint4 zn0 = zc0, zn1 = zc1;
+      if (p.norm) load_z(ci + 1, zn0, zn1);
       float qs[16], ph[16], pl[16];
       tmem_ld16(tm + lq + TC_A + (ci % 3) * 32 + cb, qs);
       tmem_ld16(tm + lq + TC_O + cb, ph);
@@ -1031,6 +1063,42 @@ __global__ void __launch_bounds__(NTS, 1)
       float ov[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) ov[j] = fmaf(al, qs[j], fmaf(pd, uo[j], ph[j] + pl[j]));
+      // o is in registers: the accumulator columns, the U' tile and the stage are free
+      tc_fence_before();
+      warp_arrive(&sh.outd);
+      warp_arrive(&sh.empty[st]);
+      if (p.norm) {
+        // ---- y = o / sqrt(mean_v o^2 + eps) * w * silu(z): this thread's 16 columns' sum of
+        //      squares goes to every block of the cluster (slot ci % 2), whose barrier for that
+        //      slot completes once all of a token's partials are in
+        const uint4 zr0 = zc0, zr1 = zc1;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ss = fmaf(ov[j], ov[j], ss);
+        const int slot = ci & 1;
+        const uint32_t np_mine = sb + SC_NP + (uint32_t)((((slot * kNormRanks + (int)rank) * 2 + hc) * 64 + i) * 4);
+        const uint32_t bar_mine = smem_u32(&sh.nbar[slot]);
+        // this block's barrier for the slot expects every partial of the cluster: 128 output
+        // threads a block, 4 bytes each (one arrival, by warp 8's lane 0)
+        if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&sh.nbar[slot], 128u * 4u * n_ranks);
+        for (uint32_t r = 0; r < n_ranks; ++r) st_async_cluster_f32(mapa_shared(np_mine, r), ss, mapa_shared(bar_mine, r));
+        const bool got = mbar_wait_cluster_spin(&sh.nbar[slot], (uint32_t)(ci >> 1) & 1, kSpin, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const float *np = reinterpret_cast<const float *>(sm + SC_NP) + slot * kNormRanks * 2 * 64 + i;
+        float tot = 0.f;  // the same order in every block
+        for (uint32_t r = 0; r < n_ranks; ++r) tot += np[(r * 2) * 64] + np[(r * 2 + 1) * 64];
+        const float inv = 1.f / sqrtf(tot * (1.f / (float)p.V) + p.eps);
+        const uint32_t zw[8] = {zr0.x, zr0.y, zr0.z, zr0.w, zr1.x, zr1.y, zr1.z, zr1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 zz = unpack_bf16(zw[e]);
+          ov[2 * e] = ov[2 * e] * inv * wv[2 * e] * __fdividef(zz.x, 1.f + __expf(-zz.x));
+          ov[2 * e + 1] = ov[2 * e + 1] * inv * wv[2 * e + 1] * __fdividef(zz.y, 1.f + __expf(-zz.y));
+        }
+      }
       if (i < nv) {
         const size_t off = (size_t)(t0 + i) * o_tok + (size_t)h * p.V + v0 + cb;
         if (p.o_f32) {
@@ -1045,9 +1113,8 @@ __global__ void __launch_bounds__(NTS, 1)
                                 pack_bf16(ov[8 * m + 4], ov[8 * m + 5]), pack_bf16(ov[8 * m + 6], ov[8 * m + 7]));
         }
       }
-      tc_fence_before();
-      warp_arrive(&sh.outd);
-      warp_arrive(&sh.empty[st]);
+      zc0 = zn0;
+      zc1 = zn1;
     }
     if (!ok && lane == 0) fail();
   }
@@ -1061,6 +1128,7 @@ __global__ void __launch_bounds__(NTS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tm, kScanCols);
+  if (p.norm) cluster_sync_all();  // no block leaves while a peer may still write into it
 }
 
 // ============================================================ host side
@@ -1169,7 +1237,7 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
                            int64_t n_tok, const gdn_shape &sh, int64_t q_stride, float scale,
                            uint32_t flags, void *o, float *h_T, bool summary, float *M,
                            float *S_local, void *workspace, size_t ws_bytes, cudaStream_t st,
-                           const FrontArgs *fr = nullptr) {
+                           const FrontArgs *fr = nullptr, const NormArgs *nm = nullptr) {
   const size_t slots = n_slots(n_tok, n_seqs);
   const size_t rec_end = kHeader + slots * (size_t)sh.Hv * rec_bytes(sh.V);
   const size_t qk_bytes = fr ? front_qk_bytes(sh, n_tok) : 0;
@@ -1260,17 +1328,76 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
     mq = mqc;
     mk = mkc;
   }
-  chunk_scan_kernel<<<dim3(cols / VS, sh.Hv, n_seqs), NTS, kScanSmem, st>>>(mq, mk, sp);
+  const dim3 grid(cols / VS, sh.Hv, n_seqs);
+  if (nm && !summary) {
+    // the norm epilogue: the blocks of one (v-head, sequence) as one cluster
+    sp.norm = 1;
+    sp.z = (const __nv_bfloat16 *)nm->z;
+    sp.nw = (const __nv_bfloat16 *)nm->w;
+    sp.eps = nm->eps;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NTS);
+    cfg.dynamicSmemBytes = kScanSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, chunk_scan_kernel, mq, mk, sp) != cudaSuccess) return GDN_ERR_CUDA;
+    return launch_status();
+  }
+  chunk_scan_kernel<<<grid, NTS, kScanSmem, st>>>(mq, mk, sp);
   return launch_status();
+}
+
+// Whether a cluster of `ranks` scan blocks can be resident at once on the current device
+// (asked once per device and cluster size).
+static bool scan_cluster_fits(int ranks) {
+  static int cached[8][kNormRanks + 1] = {};  // 0 unknown, 1 fits, 2 does not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8 || ranks < 1 || ranks > kNormRanks) return false;
+  if (cached[dev][ranks] == 0) {
+    bool fits = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kScanSmem) == cudaSuccess;
+    if (fits) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(ranks, 1, 1);
+      cfg.blockDim = dim3(NTS);
+      cfg.dynamicSmemBytes = kScanSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = ranks;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      fits = cudaOccupancyMaxActiveClusters(&n, chunk_scan_kernel, &cfg) == cudaSuccess && n >= 1;
+    }
+    (void)cudaGetLastError();  // a refused query is an answer, not an error to report later
+    cached[dev][ranks] = fits ? 1 : 2;
+  }
+  return cached[dev][ranks] == 1;
+}
+
+// The norm epilogue applies to the split scan's bf16 output with V <= 128 (V / 32 blocks of a
+// head in one cluster, at most four) where such a cluster fits the device.
+bool chunk_norm_supported(const gdn_shape &sh, uint32_t flags, const NormArgs &nm) {
+  return sh.dtype == GDN_BF16 && sh.V % 64 == 0 && sh.V / VS <= kNormRanks && !(flags & GDN_FLAG_O_F32) &&
+         aligned(nm.z, 16) && scan_cluster_fits(sh.V / VS);
 }
 
 gdn_status chunk_fwd_scan(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, const float *h0, const int32_t *cu,
                           const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
-                          void *workspace, size_t ws_bytes, cudaStream_t st) {
+                          void *workspace, size_t ws_bytes, cudaStream_t st, const NormArgs *nm) {
   const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
   return run_scan(q, k, v, g, beta, h0, cu, sh.n_seqs, n_tok, sh, sh.q_stride, scale, flags, o,
-                  h_T, false, nullptr, nullptr, workspace, ws_bytes, st);
+                  h_T, false, nullptr, nullptr, workspace, ws_bytes, st, nullptr, nm);
 }
 
 // gdn_segment_summary on the split path: k stands in for q (no output is formed).
@@ -1285,10 +1412,11 @@ gdn_status summary_scan(const void *k, const void *v, const float *g, const floa
 // gdn_layer_fwd's fused front end: conv, SiLU and gates inside the operand kernel.
 gdn_status chunk_fwd_front(const FrontArgs &fr, const float *h0, const int32_t *cu, const gdn_shape &sh,
                            float scale, uint32_t flags, void *o, float *h_T, void *workspace,
-                           size_t ws_bytes, cudaStream_t st) {
+                           size_t ws_bytes, cudaStream_t st, const NormArgs *nm) {
   const int64_t n_tok = cu ? sh.T : (int64_t)sh.B * sh.T;
   return run_scan(nullptr, nullptr, nullptr, nullptr, nullptr, h0, cu, sh.n_seqs, n_tok, sh, 0, scale,
-                  flags | GDN_FLAG_QK_L2NORM, o, h_T, false, nullptr, nullptr, workspace, ws_bytes, st, &fr);
+                  flags | GDN_FLAG_QK_L2NORM, o, h_T, false, nullptr, nullptr, workspace, ws_bytes, st, &fr,
+                  nm);
 }
 
 }  // namespace gdn

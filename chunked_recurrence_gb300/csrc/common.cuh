@@ -57,6 +57,12 @@ struct FrontArgs {
   const float *A_log, *dt_bias;
 };
 
+// The gated RMS norm applied in the state scan's output epilogue (gdn_layer_fwd with z).
+struct NormArgs {
+  const void *z, *w;
+  float eps;
+};
+
 // bytes of one conv'd q (or k) array [n_tok][Hqk][K] bf16 in the front end's workspace
 inline size_t front_qk_bytes(const gdn_shape &sh, int64_t n_tok) {
   return ((size_t)n_tok * sh.Hqk * sh.K * 2 + 255) & ~(size_t)255;

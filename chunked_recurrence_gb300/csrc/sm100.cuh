@@ -86,6 +86,53 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, u
 }
 
 // Barrier among `count` threads (a multiple of 32) using hardware barrier `id` (1..15).
+// ---- thread-block clusters: distributed shared memory and remote transaction bytes
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the address of the same shared-memory location in cluster block `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// an asynchronous 4-byte store into a (possibly remote) cluster block's shared memory that
+// completes 4 transaction bytes on that block's mbarrier: no fence, and the value is visible
+// to whoever observes the barrier's phase complete
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t addr, float v, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+               "r"(bar_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait_spin for a barrier that other blocks of the cluster complete (acquire at cluster
+// scope, so their remote writes are visible once it returns true)
+__device__ __forceinline__ bool mbar_wait_cluster_spin(uint64_t *bar, uint32_t parity, uint32_t max_iters,
+                                                       volatile int *abort) {
+  for (uint32_t i = 0; i < max_iters; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 31) == 31 && *abort) return false;
+  }
+  return false;
+}
+// every thread of every block of the cluster (all threads must call it)
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }

@@ -61,6 +61,8 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
                                    * up at its first check, so the call ends with GDN_ERR_TIMEOUT in the status word */
 #define GDN_FLAG_LAYER_FRONT 32u /* gdn_layer_fwd: the fused front end (conv and gates inside the chunk operand
                                   * kernel) instead of separate launches, where the shape allows it */
+#define GDN_FLAG_LAYER_NORM_EPILOGUE 64u /* gdn_layer_fwd with z: the gated norm in the state scan's output
+                                          * epilogue instead of the standalone norm kernel, where it applies */
 
 /* Problem shape of the recurrence. */
 typedef struct {
@@ -101,12 +103,14 @@ size_t gdn_chunk_fwd_min_workspace_bytes(const gdn_shape *shape);
 gdn_status gdn_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
 
 /* The second 32-bit word of a workspace records which kernel path the last
- * gdn_chunk_fwd that ran in it took, when that path writes it:
- * GDN_PATH_FUSED for the fused persistent kernel (bf16, K = V = 128).  The other
- * paths leave the word as they found it, and gdn_workspace_reset clears it, so
- * after a reset a value of 0 means another path ran. */
+ * gdn_chunk_fwd or gdn_layer_fwd that ran in it took, when that path writes it:
+ * GDN_PATH_FUSED for the fused persistent kernel (bf16, K = V = 128); the bits
+ * GDN_PATH_FRONT and GDN_PATH_NORM for gdn_layer_fwd's fused front end and its norm
+ * epilogue.  The other paths leave the word as they found it, and gdn_workspace_reset
+ * clears it, so after a reset a value of 0 means another path ran. */
 #define GDN_PATH_FUSED 1
 #define GDN_PATH_FRONT 2 /* gdn_layer_fwd's fused front end (conv and gates inside the operand kernel) */
+#define GDN_PATH_NORM 4  /* gdn_layer_fwd's gated norm applied in the state scan's output epilogue */
 
 /* Copy the path word (see GDN_PATH_FUSED) of `workspace` to *path_out (host) and
  * synchronise `stream`. */
@@ -280,13 +284,17 @@ gdn_status gdn_gated_rmsnorm(const void *o, const void *z, const void *w, int32_
  *   q, k, v = y's channels [0, Hqk K), [Hqk K, 2 Hqk K), [2 Hqk K, C); q and k L2-normalised
  *   g, beta = gdn_gate_prep(a, b, A_log, dt_bias)
  *   o, h_T  = gdn_chunk_fwd(q, k, v, g, beta, h0, cu_seqlens, scale)
- *   o      <- gdn_gated_rmsnorm(o, z, norm_w, norm_eps)  when z is not NULL
+ *   o      <- gdn_gated_rmsnorm(o, z, norm_w, norm_eps)  when z is not NULL (by default the
+ *             standalone kernel on the stored o; with GDN_FLAG_LAYER_NORM_EPILOGUE, bf16 and
+ *             V <= 128 a multiple of 64, the split scan's output epilogue on its fp32 o, the
+ *             V / 32 scan blocks of a head exchanging each token's sum of squares as one
+ *             thread-block cluster; the path word then has GDN_PATH_NORM)
  * Arguments:
  *   x:          [tokens, C] of shape->dtype, C = 2 Hqk K + Hv V, dense, 16-byte aligned
  *   conv_w:     [C, width] of shape->dtype, 1 <= width <= 8;  conv_bias: [C] or NULL
  *   a, b:       [tokens, Hv] of shape->dtype;  A_log, dt_bias: [Hv] fp32
  *   h0, cu_seqlens, scale, o, h_T: as for gdn_chunk_fwd (shape's strides must be 0)
- *   flags:      GDN_FLAG_O_F32, GDN_FLAG_SIMT, GDN_FLAG_LAYER_FRONT
+ *   flags:      GDN_FLAG_O_F32, GDN_FLAG_SIMT, GDN_FLAG_LAYER_FRONT, GDN_FLAG_LAYER_NORM_EPILOGUE
  *   z:          [tokens, Hv, V] of shape->dtype or NULL (no norm);  norm_w: [V] or NULL
  *               (ones); norm_eps >= 0.  With z, GDN_FLAG_O_F32 is GDN_ERR_INVALID_ARG.
  *   workspace:  at least gdn_layer_fwd_workspace_bytes(shape, width, flags), 256-byte aligned

@@ -28,12 +28,12 @@ def crg():
     return m
 
 
-def _case(lengths, width=4, Hqk=2, Hv=4, seed=31, h0_std=0.1, B=1, with_bias=False, n_tok=None):
+def _case(lengths, width=4, Hqk=2, Hv=4, seed=31, h0_std=0.1, B=1, with_bias=False, n_tok=None, V=128):
     """Layer inputs for packed samples of the given lengths (B = 1), or B rows of lengths[0]
     tokens; n_tok may exceed the samples' total (rows that belong to no sample)."""
     total = sum(lengths) if B == 1 else B * lengths[0]
     n_tok = total if n_tok is None else n_tok
-    wl = synth.Workload("layer_case", B=B, T=n_tok // B, Hqk=Hqk, Hv=Hv, K=128, V=128, dtype="bf16",
+    wl = synth.Workload("layer_case", B=B, T=n_tok // B, Hqk=Hqk, Hv=Hv, K=128, V=V, dtype="bf16",
                         seed=seed, conv_width=width, h0_std=0.0)
     inp = synth.make_inputs(wl, device=DEV, with_direct=False)
     n_seq = len(lengths) if B == 1 else B
@@ -41,20 +41,21 @@ def _case(lengths, width=4, Hqk=2, Hv=4, seed=31, h0_std=0.1, B=1, with_bias=Fal
     inp["n_seq"] = n_seq
     g = torch.Generator(device=DEV)
     g.manual_seed(seed + 1)
-    inp["h0"] = (torch.randn((n_seq, Hv, 128, 128), generator=g, device=DEV) * h0_std) if h0_std else None
+    inp["h0"] = (torch.randn((n_seq, Hv, V, 128), generator=g, device=DEV) * h0_std) if h0_std else None
     inp["conv_bias"] = ((torch.randn((wl.C,), generator=g, device=DEV) * 0.1).to(torch.bfloat16)
                         if with_bias else None)
     return inp
 
 
-def _run(crg, inp, front, z=None, norm_w=None):
+def _run(crg, inp, front, z=None, norm_w=None, o_f32=False, epi=False):
     wl = inp["workload"]
     sh = crg.layer_shape(inp["x"], wl.Hqk, wl.Hv, wl.K, wl.V, inp["cu_seqlens"], wl.B)
-    flags = crg.GDN_FLAG_LAYER_FRONT if front else 0
+    flags = (crg.GDN_FLAG_LAYER_FRONT if front else 0) | (crg.GDN_FLAG_LAYER_NORM_EPILOGUE if epi else 0)
     ws = crg.Workspace(crg.gdn_layer_fwd_workspace_bytes(sh, wl.conv_width, flags), DEV)
     o, hT = crg.gdn_layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
                               wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], inp["cu_seqlens"], wl.B, inp["scale"],
-                              conv_bias=inp.get("conv_bias"), z=z, norm_w=norm_w, front=front,
+                              conv_bias=inp.get("conv_bias"), z=z, norm_w=norm_w, front=front, o_f32=o_f32,
+                              norm_epilogue=epi,
                               workspace=ws)
     torch.cuda.synchronize()
     assert ws.status() == 0
@@ -102,29 +103,41 @@ def test_front_end_against_oracle(crg):
         assert_close(hT[:, h].cpu(), rh, "bf16", f"fused layer h_T head {h}")
 
 
-def test_layer_with_gated_norm(crg):
-    """z given: o is rmsnorm(o) * w * silu(z), the same bits as gdn_gated_rmsnorm on the
-    un-normed output; within the bf16 bar of the oracle's norm of that output; and within the
-    relative-L2 bar of the oracle's norm of the oracle's o (the per-row normalisation divides
-    each row's error by the row's own rms, so the max-abs bar, relative to the whole output's
-    rms, applies to the norm step alone; the core's o meets it in the test above)."""
-    inp = _case([300, 77], seed=53)
+@pytest.mark.parametrize("front,V,epi", [(False, 128, True), (True, 128, True), (False, 64, True),
+                                         (False, 256, True), (False, 128, False), (True, 128, False)])
+def test_layer_with_gated_norm(crg, front, V, epi):
+    """z given: o is rmsnorm(o) * w * silu(z).  With GDN_FLAG_LAYER_NORM_EPILOGUE and V <= 128
+    the scan applies it in its output epilogue (its V / 32 blocks of a head exchanging each
+    token's sum of squares as one cluster; the path word's GDN_PATH_NORM bit says so), on the
+    kernel's fp32 o: checked at the bf16 bar against the oracle's norm of that fp32 o (the
+    same call with GDN_FLAG_O_F32 and no z).  Otherwise (V = 256, or no flag) the standalone
+    norm kernel runs on the stored o, the same bits as calling it after the layer.  Both are
+    also held to the relative-L2 bar against the oracle's norm of the oracle's o (the
+    per-row normalisation divides a row's error by the row's own rms, so the max-abs bar,
+    relative to the whole output's rms, applies to the norm step alone)."""
+    inp = _case([300, 77], seed=53, V=V)
     n_tok, Hv = inp["x"].shape[0], inp["workload"].Hv
-    nz = synth.norm_inputs((n_tok, Hv), 128, "bf16", seed=59, device=DEV)
+    nz = synth.norm_inputs((n_tok, Hv), V, "bf16", seed=59, device=DEV)
     z, w = nz["z"], nz["w"]
-    o_plain, _, _ = _run(crg, inp, front=True)
-    o_norm, _, path = _run(crg, inp, front=True, z=z, norm_w=w)
-    assert path == crg.GDN_PATH_FRONT
-    expect = crg.gdn_gated_rmsnorm(o_plain, z, w, eps=1e-6)
-    torch.cuda.synchronize()
-    assert torch.equal(o_norm, expect)
+    o_norm, _, path = _run(crg, inp, front=front, z=z, norm_w=w, epi=epi)
+    fused = epi and V <= 128
+    assert bool(path & crg.GDN_PATH_NORM) == fused and bool(path & crg.GDN_PATH_FRONT) == front
+    if fused:
+        o32, _, _ = _run(crg, inp, front=front, o_f32=True)
+        base = o32
+    else:
+        base, _, _ = _run(crg, inp, front=front)
+        expect = crg.gdn_gated_rmsnorm(base, z, w, eps=1e-6)
+        torch.cuda.synchronize()
+        assert torch.equal(o_norm, expect)
     inp_cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
-    ref = _oracle_layer_heads(inp_cpu, range(Hv))
-    for h, (ro, _) in ref.items():
+    heads = range(Hv)
+    ref = _oracle_layer_heads(inp_cpu, heads)
+    for h in heads:
         zh, wh = to64(z[:, h].cpu()), to64(w.cpu())
-        own = oracle.gated_rmsnorm(to64(o_plain[:, h].cpu()), zh, wh)
+        own = oracle.gated_rmsnorm(to64(base[:, h].cpu()), zh, wh)
         assert_close(o_norm[:, h].cpu(), own, "bf16", f"norm of the layer's o, head {h}")
-        chain = oracle.gated_rmsnorm(ro, zh, wh)
+        chain = oracle.gated_rmsnorm(ref[h][0], zh, wh)
         m = metrics(o_norm[:, h].cpu(), chain)
         assert m["rel_l2"] <= BF16_REL_L2, f"normed o head {h} vs the oracle chain: rel-L2 {m['rel_l2']:.3e}"
 
