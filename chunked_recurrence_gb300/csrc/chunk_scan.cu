@@ -158,7 +158,7 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
   __syncthreads();
 }
 
-template <int V>
+template <int V, bool FRONT>
 __global__ void __launch_bounds__(128, 4)
     chunk_operand_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qc,
@@ -175,7 +175,9 @@ __global__ void __launch_bounds__(128, 4)
   // [row][0-15 k, 16-31 q, 32-47 v]
   __shared__ uint4 halo[3][48];
   __shared__ int64_t claim_s[2];
-  constexpr bool kFront = V == 128;  // the only width the front end takes
+  // the front end's code lives only in its own instantiation (V = 128), so that the plain
+  // kernel's instruction footprint stays small
+  constexpr bool kFront = FRONT && V == 128;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // A resident block walks the (chunk slot, v-head) items with the grid's stride: TMEM and
   // the barriers are set up once, and the phases of the barriers are counted across items.
@@ -193,13 +195,13 @@ __global__ void __launch_bounds__(128, 4)
   tc_fence_after();
   const uint32_t tm = tbase;
   uint32_t ldp = 0, mp = 0;  // completed phases of ld_bar and bar
-  if (kFront && p.front && blockIdx.x == 0 && tid == 0) atomicOr(p.status + 1, GDN_PATH_FRONT);
+  if (kFront && blockIdx.x == 0 && tid == 0) atomicOr(p.status + 1, GDN_PATH_FRONT);
   // In front mode blocks claim groups of G consecutive items from a counter (G = the v-heads
   // of one q/k head) and walk each group in order: the group's first item convs the q/k
   // head's tiles and writes them out, and the later items load them back.
   // Each claim is made one group ahead (thread 32, into the other of two slots), so its
   // latency overlaps the current group's work.
-  const int G = (kFront && p.front) ? p.Hv / p.Hqk : 1;
+  const int G = kFront ? p.Hv / p.Hqk : 1;
   int64_t group = 0;
   int jg = G, slot_par = 0;  // item of the current group to run next; slot of its claim
   // Without the front end (G = 1) the blocks stride over the items instead.
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(128, 4)
 #pragma unroll
       for (int nb = 0; nb < NVB; ++nb) tma_load_3d(sm + op_vt(V) + nb * 8192, &tm_v, &ld_bar, nb * 64, h, tt);
   }
-  if (!kFront || !p.front) {
+  if (!kFront) {
     if (tid < C) gam[tid] = (tid < n) ? p.g[(t0 + tid) * p.Hv + h] : 0.f;
     else bet[tid - C] = (tid - C < n) ? p.beta[(t0 + tid - C) * p.Hv + h] : 0.f;
   } else {
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(128, 4)
     }
     ++ldp;
   }
-  if (kFront && p.front && jv == 0) {
+  if (kFront && jv == 0) {
     // ---- conv (+ SiLU) of the k and q tiles in place: warp w takes rows 16 w .. 16 w + 15,
     //      lanes 0-15 the k tile and 16-31 the q tile, eight channels a lane
     const int tile = lane >> 4, pc = lane & 15;
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(128, 4)
     // the MMAs read the conv'd tiles, and the group's later items load the written rows
     fence_proxy_async_all();
     __syncthreads();
-  } else if (kFront && p.front && n < C) {
+  } else if (kFront && n < C) {
     // ---- rows past this sequence's end in tiles loaded back: they may not be written yet
     for (int e = tid; e < (C - n) * 32; e += 128) {
       const int r = n + (e >> 5), pcs = e & 31;  // 32 pieces of 16 bytes: k and q, both halves
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(128, 4)
         break;
       }
       ++ldp;
-      if (kFront && p.front) {
+      if (kFront) {
         // ---- conv (+ SiLU) of the v tile in place: rows 8 (tid / 16) .. + 7, eight
         //      channels (tid % 16) a thread; the first row group's history from halo
         const int rg = tid >> 4, pc = tid & 15;
@@ -708,6 +710,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+// NORM: the gated-norm epilogue (its code only in that instantiation; NORM is set with it)
+template <bool NORM>
 __global__ void __launch_bounds__(NTS, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const ScanParams p) {
@@ -743,7 +747,7 @@ __global__ void __launch_bounds__(NTS, 1)
     mbar_init(&sh.epa2, 4);
     mbar_init(&sh.epb, 8);
     mbar_init(&sh.outd, 4);
-    if (p.norm) {  // one local arrival a chunk (with the bytes the cluster's partials bring)
+    if (NORM) {  // one local arrival a chunk (with the bytes the cluster's partials bring)
       mbar_init(&sh.nbar[0], 1);
       mbar_init(&sh.nbar[1], 1);
     }
@@ -759,8 +763,8 @@ __global__ void __launch_bounds__(NTS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (p.norm) cluster_sync_all();  // the peers' barriers are initialised before any remote arrival
-  if (p.norm && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0)
+  if (NORM) cluster_sync_all();  // the peers' barriers are initialised before any remote arrival
+  if (NORM && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0)
     atomicOr(p.status + 1, GDN_PATH_NORM);
   const uint32_t tm = sh.tbase;
   auto fail = [&]() {
@@ -1001,10 +1005,10 @@ __global__ void __launch_bounds__(NTS, 1)
     const int cb = hc * 16;
     const int i = quarter * 32 + lane;
     const size_t o_tok = (size_t)p.Hv * p.V;
-    const uint32_t rank = p.norm ? cluster_ctarank() : 0u, n_ranks = gridDim.x;
+    const uint32_t rank = NORM ? cluster_ctarank() : 0u, n_ranks = gridDim.x;
     float wv[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) wv[j] = (p.norm && p.nw) ? __bfloat162float(p.nw[v0 + cb + j]) : 1.f;
+    for (int j = 0; j < 16; ++j) wv[j] = (NORM && p.nw) ? __bfloat162float(p.nw[v0 + cb + j]) : 1.f;
     // the norm's z of this token's 16 columns, loaded a chunk ahead of its use
     auto load_z = [&](int cj, uint4 &za, uint4 &zb) {
       za = zb = make_uint4(0u, 0u, 0u, 0u);
@@ -1016,7 +1020,7 @@ __global__ void __launch_bounds__(NTS, 1)
       }
     };
     uint4 zc0 = make_uint4(0u, 0u, 0u, 0u), zc1 = zc0;
-    if (p.norm && !summary) load_z(0, zc0, zc1);
+    if (NORM && !summary) load_z(0, zc0, zc1);
     bool ok = true;
     for (int ci = 0; ci < n_chunks; ++ci) {
       const int st = ci % kStages;
@@ -1037,7 +1041,7 @@ __global__ void __launch_bounds__(NTS, 1)
       }
       tc_fence_after();
       uint4 zn0 = zc0, zn1 = zc1;
-      if (p.norm) load_z(ci + 1, zn0, zn1);
+      if (NORM) load_z(ci + 1, zn0, zn1);
       float qs[16], ph[16], pl[16];
       tmem_ld16(tm + lq + TC_A + (ci % 3) * 32 + cb, qs);
       tmem_ld16(tm + lq + TC_O + cb, ph);
@@ -1067,7 +1071,7 @@ __global__ void __launch_bounds__(NTS, 1)
       tc_fence_before();
       warp_arrive(&sh.outd);
       warp_arrive(&sh.empty[st]);
-      if (p.norm) {
+      if (NORM) {
         // ---- y = o / sqrt(mean_v o^2 + eps) * w * silu(z): this thread's 16 columns' sum of
         //      squares goes to every block of the cluster (slot ci % 2), whose barrier for that
         //      slot completes once all of a token's partials are in
@@ -1128,7 +1132,7 @@ __global__ void __launch_bounds__(NTS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tm, kScanCols);
-  if (p.norm) cluster_sync_all();  // no block leaves while a peer may still write into it
+  if (NORM) cluster_sync_all();  // no block leaves while a peer may still write into it
 }
 
 // ============================================================ host side
@@ -1167,14 +1171,14 @@ bool make_tile_map(CUtensorMap *m, const void *base, int width, int heads, int64
 
 namespace {
 
-template <int V>
+template <int V, bool FRONT = false>
 gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const CUtensorMap &mqc, const CUtensorMap &mkc, const OpParams &op, size_t slots,
                            cudaStream_t st) {
   const size_t smem = op_smem(V);
-  if (cudaFuncSetAttribute(chunk_operand_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(chunk_operand_kernel<V, FRONT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(chunk_operand_kernel<V>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaFuncSetAttribute(chunk_operand_kernel<V, FRONT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return GDN_ERR_CUDA;
   const size_t items = slots * (size_t)op.Hv;
@@ -1192,7 +1196,7 @@ gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const C
   OpParams q = op;
   q.n_items = (int64_t)items;
   if (q.front && cudaMemsetAsync(q.claim, 0, sizeof(*q.claim), st) != cudaSuccess) return GDN_ERR_CUDA;
-  chunk_operand_kernel<V><<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, mqc, mkc, q);
+  chunk_operand_kernel<V, FRONT><<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, mqc, mkc, q);
   return launch_status();
 }
 
@@ -1297,7 +1301,10 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
   gdn_status r;
   switch (sh.V) {
     case 64: r = launch_operands<64>(mq, mk, mv, mqc, mkc, op, slots, st); break;
-    case 128: r = launch_operands<128>(mq, mk, mv, mqc, mkc, op, slots, st); break;
+    case 128:
+      r = fr ? launch_operands<128, true>(mq, mk, mv, mqc, mkc, op, slots, st)
+             : launch_operands<128>(mq, mk, mv, mqc, mkc, op, slots, st);
+      break;
     case 192: r = launch_operands<192>(mq, mk, mv, mqc, mkc, op, slots, st); break;
     case 256: r = launch_operands<256>(mq, mk, mv, mqc, mkc, op, slots, st); break;
     default: return GDN_ERR_UNSUPPORTED;
@@ -1320,7 +1327,9 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
   sp.summary = summary ? 1 : 0;
   sp.M = M;
   sp.S_local = S_local;
-  if (cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(chunk_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kScanSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(chunk_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kScanSmem) != cudaSuccess)
     return GDN_ERR_CUDA;
   const int cols = summary ? KD + sh.V : sh.V;
@@ -1347,10 +1356,10 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, chunk_scan_kernel, mq, mk, sp) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, chunk_scan_kernel<true>, mq, mk, sp) != cudaSuccess) return GDN_ERR_CUDA;
     return launch_status();
   }
-  chunk_scan_kernel<<<grid, NTS, kScanSmem, st>>>(mq, mk, sp);
+  chunk_scan_kernel<false><<<grid, NTS, kScanSmem, st>>>(mq, mk, sp);
   return launch_status();
 }
 
@@ -1361,7 +1370,7 @@ static bool scan_cluster_fits(int ranks) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8 || ranks < 1 || ranks > kNormRanks) return false;
   if (cached[dev][ranks] == 0) {
-    bool fits = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    bool fits = cudaFuncSetAttribute(chunk_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kScanSmem) == cudaSuccess;
     if (fits) {
       cudaLaunchConfig_t cfg{};
@@ -1376,7 +1385,7 @@ static bool scan_cluster_fits(int ranks) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      fits = cudaOccupancyMaxActiveClusters(&n, chunk_scan_kernel, &cfg) == cudaSuccess && n >= 1;
+      fits = cudaOccupancyMaxActiveClusters(&n, chunk_scan_kernel<true>, &cfg) == cudaSuccess && n >= 1;
     }
     (void)cudaGetLastError();  // a refused query is an answer, not an error to report later
     cached[dev][ranks] = fits ? 1 : 2;
