@@ -161,27 +161,30 @@ class ClockSampler:
 
 
 def _kernel_sha() -> str:
-    """Hash of the sources chunk_operand_kernel (with its front end) and chunk_scan_kernel
-    compile from: a stored ncu traffic figure is valid for these only."""
+    """Hash of the sources the layer call's kernels compile from (gate prep, the conv, the
+    chunk operand and scan kernels, and the host code that launches them): a stored ncu
+    traffic figure is valid for these only."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_recurrence_gb300", "csrc")
-    for fn in ("chunk_common.cuh", "chunk_scan.cu", "common.cuh", "conv_tap.cuh", "gates.cuh", "sm100.cuh"):
+    for fn in ("api.cu", "chunk_common.cuh", "chunk_scan.cu", "common.cuh", "conv_tap.cuh", "front.cu",
+               "gates.cuh", "sm100.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def _stored_traffic(sha: str):
-    """dram read+write bytes per chunk-kernel launch from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "chunk_fwd_qwen35_4b_layer.md")
+def _stored_traffic(sha: str, key: str = "traffic_bytes_per_launch"):
+    """DRAM read + write bytes of one call from the committed ncu summary of the layer step,
+    if it was taken on the current kernel sources (else None).  key: the layer call's four
+    kernels (traffic_bytes_per_launch) or the chunk pair alone (chunk_traffic_bytes_per_launch)."""
+    path = os.path.join(ROOT, "profiles", "layer_fwd_qwen35_4b_layer.md")
     try:
         txt = open(path).read()
     except OSError:
         return None
     m_sha = re.search(r"kernel_sha:\s*([0-9a-f]+)", txt)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m_tr = re.search(key + r":\s*([0-9.eE+]+)", txt)
     if m_sha and m_tr and m_sha.group(1) == sha:
         return float(m_tr.group(1))
     return None
@@ -316,7 +319,7 @@ def run_gpu_arm(args, ws, rank, local):
         "gdn_conv1d_varlen": _kinfo(unf["conv_ms"], conv_bytes(wl, n_tok), peaks),
         "gdn_chunk_fwd": _kinfo(chunk_ms, cb, peaks),
     }
-    chunk_roofline = roofline_entry(cb, cf, chunk_ms, peaks)
+    chunk_roofline = roofline_entry(cb, cf, chunk_ms, peaks, _stored_traffic(sha, "chunk_traffic_bytes_per_launch"))
     front = time_front_layer(crg, wl, inp, cu, stream, flush)
     with_norm = time_norm_layer(crg, wl, inp, cu, stream, flush)
     layer_paths = {"separate_launches_ms_median": round(step_ms_median, 5),
