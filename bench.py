@@ -304,7 +304,7 @@ def run_gpu_arm(args, ws, rank, local):
     sha = _kernel_sha()
     traffic = _stored_traffic(sha)
     layer_roofline = roofline_entry(lb, cf, step_ms_local, peaks, traffic)
-    layer_roofline.update({"kernel": "gdn_layer_fwd (gate_prep_kernel, conv1d_staged_kernel<4>, "
+    layer_roofline.update({"kernel": "gdn_layer_fwd (conv1d_staged_kernel<4> with the gates, "
                                      "chunk_operand_kernel<128>, chunk_scan_kernel)",
                            "ms_mean": round(step_ms_local, 5), "ms_median": round(step_ms_median, 5),
                            "path_word": layer_path, "kernel_sha": sha})
@@ -358,7 +358,7 @@ def run_gpu_arm(args, ws, rank, local):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
 
-    launches_per_step = 4  # gdn_layer_fwd: gate prep, conv1d, and the chunk operand and scan kernels
+    launches_per_step = 3  # gdn_layer_fwd: the conv (with the gates), the chunk operand and scan kernels
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),

@@ -37,6 +37,10 @@ gdn_status chunk_fwd_fused(const void *q, const void *k, const void *v, const fl
                            const gdn_shape &sh, float scale, uint32_t flags, void *o, float *h_T,
                            void *workspace, size_t ws_bytes, cudaStream_t st);
 bool chunk_front_supported(const void *x, const void *w, int width, const gdn_shape &sh);
+gdn_status layer_conv_and_gates(const void *x, const void *w, const void *bias, int32_t dtype,
+                                const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t C,
+                                int32_t width, void *y, const void *a, const void *b, const float *A_log,
+                                const float *dt_bias, int32_t Hv, float *g, float *beta, void *stream);
 size_t chunk_front_workspace_bytes(const gdn_shape &sh, int64_t n_tok);
 gdn_status chunk_fwd_front(const FrontArgs &fr, const float *h0, const int32_t *cu, const gdn_shape &sh,
                            float scale, uint32_t flags, void *o, float *h_T, void *workspace,
@@ -296,10 +300,8 @@ extern "C" gdn_status gdn_layer_fwd(const void *x, const void *conv_w, const voi
     uint8_t *y = ws + ws_chunk;
     float *g = (float *)(y + align256((size_t)n_tok * Cx * es));
     float *beta = (float *)((uint8_t *)g + align256((size_t)n_tok * s.Hv * 4));
-    st = gdn_gate_prep(a, b, s.dtype, A_log, dt_bias, n_tok, s.Hv, g, beta, stream);
-    if (st != GDN_OK) return st;
-    st = gdn_conv1d_varlen(x, conv_w, conv_bias, s.dtype, cu_seqlens, s.n_seqs, n_tok, (int32_t)Cx, width, 1,
-                           y, stream);
+    st = layer_conv_and_gates(x, conv_w, conv_bias, s.dtype, cu_seqlens, s.n_seqs, n_tok, (int32_t)Cx, width, y,
+                              a, b, A_log, dt_bias, s.Hv, g, beta, stream);
     if (st != GDN_OK) return st;
     st = chunk_fwd_impl(y, y + (size_t)s.Hqk * s.K * es, y + (size_t)2 * s.Hqk * s.K * es, g, beta, h0,
                         cu_seqlens, &c, scale, GDN_FLAG_QK_L2NORM | (flags & (GDN_FLAG_O_F32 | GDN_FLAG_SIMT)), o,

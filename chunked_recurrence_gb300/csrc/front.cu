@@ -273,13 +273,23 @@ constexpr int kStageRows = 8, kStages = 4, kStagedCols = 1024;
 constexpr uint32_t kStagedSmem = kStages * kStageRows * kStagedCols * 2;
 constexpr uint32_t kConvSpin = 1u << 22;
 
+// The layer's gates, computed by the conv's first channel block over its run of tokens
+// (gdn_layer_fwd): the same values as gdn_gate_prep, one launch fewer.
+struct ConvGates {
+  const __nv_bfloat16 *a, *b;  // [n_tok][Hv]
+  const float *A_log, *dt_bias;
+  float *g, *beta;
+  int Hv;
+};
+
 template <int W>
 __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat16 *__restrict__ x,
                                                                const __nv_bfloat16 *__restrict__ w,
                                                                const __nv_bfloat16 *__restrict__ bias,
                                                                const int32_t *__restrict__ cu, int n_seqs,
                                                                int64_t row_T, int64_t n_tok, int C, int run,
-                                                               int act, __nv_bfloat16 *__restrict__ y) {
+                                                               int act, __nv_bfloat16 *__restrict__ y,
+                                                               const ConvGates gates) {
   using namespace gdn::sm100;
   constexpr int VEC = 8, HW = W > 1 ? W - 1 : 1;
   extern __shared__ __align__(128) uint4 ring[];  // [kStages][kStageRows][kStagedCols / 8]
@@ -291,6 +301,15 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
   const int64_t t0 = (int64_t)blockIdx.x * run;
   if (t0 >= n_tok) return;
   const int64_t t1 = min(t0 + (int64_t)run, n_tok);
+  if (gates.g && blockIdx.y == 0) {
+    const int64_t n_g = (t1 - t0) * gates.Hv;
+    for (int64_t e = tid; e < n_g; e += blockDim.x) {
+      const int64_t i = t0 * gates.Hv + e;
+      const int hh = (int)(i % gates.Hv);
+      gdn_gates(__bfloat162float(gates.a[i]), __bfloat162float(gates.b[i]), gates.A_log[hh], gates.dt_bias[hh],
+                gates.g[i], gates.beta[i]);
+    }
+  }
   int s = 0;
   int64_t start, end;
   if (cu) {
@@ -400,7 +419,8 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
 // Launches the staged bf16 conv; returns false (nothing launched) where it does not apply.
 static bool launch_conv_staged(int W, cudaStream_t st, const __nv_bfloat16 *x, const __nv_bfloat16 *w,
                                const __nv_bfloat16 *bias, const int32_t *cu, int n_seqs, int64_t row_T,
-                               int64_t n_tok, int C, int act, __nv_bfloat16 *y, gdn_status *status) {
+                               int64_t n_tok, int C, int act, __nv_bfloat16 *y, gdn_status *status,
+                               const ConvGates &gates = ConvGates{}) {
   int dev = 0, sms = 0, smem_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -423,7 +443,7 @@ static bool launch_conv_staged(int W, cudaStream_t st, const __nv_bfloat16 *x, c
       return true;                                                                                   \
     }                                                                                                \
     conv1d_staged_kernel<WW><<<grid, 128, kStagedSmem, st>>>(x, w, bias, cu, n_seqs, row_T, n_tok, C, \
-                                                             (int)run, act, y);                      \
+                                                             (int)run, act, y, gates);               \
     break;
   switch (W) {
     GDN_STAGED_CASE(1) GDN_STAGED_CASE(2) GDN_STAGED_CASE(3) GDN_STAGED_CASE(4)
@@ -451,6 +471,33 @@ static void launch_conv_w(int W, dim3 grid, dim3 block, cudaStream_t st, const T
   }
 #undef GDN_CONV_CASE
 }
+
+namespace gdn {
+
+// gdn_layer_fwd's front steps: the conv (SiLU) and the gates.  bf16 with the staged conv
+// takes both in one launch; otherwise gdn_gate_prep and gdn_conv1d_varlen run.
+gdn_status layer_conv_and_gates(const void *x, const void *w, const void *bias, int32_t dtype,
+                                const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t C,
+                                int32_t width, void *y, const void *a, const void *b, const float *A_log,
+                                const float *dt_bias, int32_t Hv, float *g, float *beta, void *stream) {
+  const bool staged = dtype == GDN_BF16 && n_tokens > 0 && width >= 1 && width <= 6 && C % 8 == 0 &&
+                      aligned(x, 16) && aligned(y, 16) && n_seqs >= 1 && (cu_seqlens || n_tokens % n_seqs == 0) &&
+                      a && b && A_log && dt_bias && g && beta && Hv > 0;
+  if (staged) {
+    const int64_t row_T = cu_seqlens ? 0 : n_tokens / n_seqs;
+    const ConvGates gates{(const __nv_bfloat16 *)a, (const __nv_bfloat16 *)b, A_log, dt_bias, g, beta, Hv};
+    gdn_status st = GDN_OK;
+    if (launch_conv_staged(width, (cudaStream_t)stream, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w,
+                           (const __nv_bfloat16 *)bias, cu_seqlens, n_seqs, row_T, n_tokens, C, 1,
+                           (__nv_bfloat16 *)y, &st, gates))
+      return st;
+  }
+  gdn_status st = gdn_gate_prep(a, b, dtype, A_log, dt_bias, n_tokens, Hv, g, beta, stream);
+  if (st != GDN_OK) return st;
+  return gdn_conv1d_varlen(x, w, bias, dtype, cu_seqlens, n_seqs, n_tokens, C, width, 1, y, stream);
+}
+
+}  // namespace gdn
 
 extern "C" gdn_status gdn_conv1d_varlen(const void *x, const void *w, const void *bias, int32_t dtype,
                                         const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
