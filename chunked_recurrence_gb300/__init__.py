@@ -325,8 +325,9 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None, l2norm
     """Chunked gated delta rule forward; returns (o [n_tok, Hv, V], h_T [n_seqs, Hv, V, K] or None).
 
     fused=True (bf16, K = V = 128) runs the fused persistent kernel instead of the two-kernel
-    split path.  _test_no_wait (tests only, with fused=True) makes every bounded wait of the
-    fused kernel give up at once, so the call ends with GDN_ERR_TIMEOUT in the workspace status."""
+    split path.  _test_no_wait (tests only) makes every bounded wait of the tensor-core kernels
+    (split, or fused) give up at once, so the call ends with GDN_ERR_TIMEOUT in the workspace
+    status."""
     _need_cuda(q, k, v, g, beta, h0, cu_seqlens)
     for n, t in (("g", g), ("beta", beta), ("h0", h0)):
         _contig(n, t)

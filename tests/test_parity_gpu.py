@@ -535,23 +535,26 @@ def test_fused_against_oracle_and_split(crg, case, gates):
         assert_close(o[idx], ro[idx], "bf16", "fused chunk-start windows")
 
 
-def test_fused_timeout_reported_then_context_usable(crg):
-    """With every bounded wait told to give up at once, the fused kernel stops and reports
-    GDN_ERR_TIMEOUT in the status word (no trap, no hang); the same context then runs a
-    normal call that matches the oracle."""
+@pytest.mark.parametrize("fused", [False, True], ids=["split", "fused"])
+def test_timeout_reported_then_context_usable(crg, fused):
+    """With every bounded wait told to give up at once (GDN_FLAG_TEST_NO_WAIT), the kernels
+    stop and report GDN_ERR_TIMEOUT in the status word (no trap, no hang; the waits that let
+    copies and MMAs in flight land keep their full bound); the same context then runs a
+    normal call that matches the oracle.  Split: the default operand and scan kernels."""
     c = make_case([300, 65], 2, 4, 128, 128, "bf16", "mild", True, seed=77)
     d = lambda t: None if t is None else t.to(DEV)
     sh = crg.make_shape(d(c["q"]), d(c["k"]), d(c["v"]), d(c["cu"]))
     ws = crg.Workspace(crg.gdn_chunk_fwd_workspace_bytes(sh), DEV)
     ws.reset()
     crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]), d(c["cu"]),
-                      c["scale"], True, workspace=ws, fused=True, _test_no_wait=True)
-    assert ws.path() == crg.GDN_PATH_FUSED
+                      c["scale"], True, workspace=ws, fused=fused, _test_no_wait=True)
+    want_path = crg.GDN_PATH_FUSED if fused else 0
+    assert ws.path() == want_path
     assert ws.status() == crg.GDN_ERR_TIMEOUT
     ws.reset()
     o, hT = crg.gdn_chunk_fwd(d(c["q"]), d(c["k"]), d(c["v"]), d(c["g"]), d(c["beta"]), d(c["h0"]),
-                              d(c["cu"]), c["scale"], True, workspace=ws, fused=True)
-    assert ws.status() == 0 and ws.path() == crg.GDN_PATH_FUSED
+                              d(c["cu"]), c["scale"], True, workspace=ws, fused=fused)
+    assert ws.status() == 0 and ws.path() == want_path
     ro, rh = run_oracle(c)
     assert_close(o.cpu(), ro, "bf16", "o after a timeout")
     assert_close(hT.cpu(), rh, "bf16", "h_T after a timeout")
