@@ -162,18 +162,41 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       bex[i] = expf(gam[i]);
       dec[i] = expf(gam[C - 1] - gam[i]);
     });
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      float kk = 0.f, qk = 0.f;
-      if (j < i)
-        for (int c = 0; c < K; ++c) kk = fmaf(Ks[i * KP + c], Ks[j * KP + c], kk);
-      if (with_q && j <= i)
-        for (int c = 0; c < K; ++c) qk = fmaf(Qs[i * KP + c], Ks[j * KP + c], qk);
-      const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
-      Gm[i * CP + j] = gij;
-      KKm[i * CP + j] = kk;
-      Zm[i * CP + j] = j < i ? bet[i] * gij * kk : 0.f;
-      if (with_q) QKm[i * CP + j] = qk;
+    // K K^T (strictly lower) and Q K^T (lower), 4 x 4 tiles of (i, j) a thread: every loaded
+    // k or q value feeds four products
+    x.par((C / 4) * (C / 4), [&](int t) {
+      const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
+      float kk[4][4] = {}, qk[4][4] = {};
+      if (j0 <= i0 + 3) {  // tiles wholly above the diagonal hold zeros
+        for (int c = 0; c < K; ++c) {
+          float ki[4], kj[4], qi[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            ki[r] = Ks[(i0 + r) * KP + c];
+            kj[r] = Ks[(j0 + r) * KP + c];
+            qi[r] = with_q ? Qs[(i0 + r) * KP + c] : 0.f;
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              kk[a][b] = fmaf(ki[a], kj[b], kk[a][b]);
+              qk[a][b] = fmaf(qi[a], kj[b], qk[a][b]);
+            }
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int i = i0 + a, j = j0 + b;
+          const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
+          const float kv = j < i ? kk[a][b] : 0.f;
+          Gm[i * CP + j] = gij;
+          KKm[i * CP + j] = kv;
+          Zm[i * CP + j] = j < i ? bet[i] * gij * kv : 0.f;
+          if (with_q) QKm[i * CP + j] = j <= i ? qk[a][b] : 0.f;
+        }
     });
     x.sync();
     // Z = (I + A)^-1 by forward substitution, a row at a time: row i of Z (left of the
@@ -189,16 +212,32 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       x.sync();
     }
     x.par(C, [&](int i) { Zm[i * CP + i] = 1.f; });
-    // K S^T (and Q S^T)
-    x.par(C * BV, [&](int idx) {
-      const int i = idx / BV, v = idx % BV;
-      float ks = 0.f, qs = 0.f;
-      for (int c = 0; c < K; ++c) ks = fmaf(Ks[i * KP + c], Ss[v * KP + c], ks);
-      KSs[i * VP + v] = ks;
-      if (with_q) {
-        for (int c = 0; c < K; ++c) qs = fmaf(Qs[i * KP + c], Ss[v * KP + c], qs);
-        QSs[i * VP + v] = qs;
+    // K S^T (and Q S^T), 2 x 2 tiles of (i, v) a thread
+    x.par((C / 2) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
+      float ks[2][2] = {}, qs[2][2] = {};
+      for (int c = 0; c < K; ++c) {
+        const float k0 = Ks[i0 * KP + c], k1 = Ks[(i0 + 1) * KP + c];
+        const float s0 = Ss[v0 * KP + c], s1 = Ss[(v0 + 1) * KP + c];
+        ks[0][0] = fmaf(k0, s0, ks[0][0]);
+        ks[0][1] = fmaf(k0, s1, ks[0][1]);
+        ks[1][0] = fmaf(k1, s0, ks[1][0]);
+        ks[1][1] = fmaf(k1, s1, ks[1][1]);
+        if (with_q) {
+          const float q0 = Qs[i0 * KP + c], q1 = Qs[(i0 + 1) * KP + c];
+          qs[0][0] = fmaf(q0, s0, qs[0][0]);
+          qs[0][1] = fmaf(q0, s1, qs[0][1]);
+          qs[1][0] = fmaf(q1, s0, qs[1][0]);
+          qs[1][1] = fmaf(q1, s1, qs[1][1]);
+        }
       }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          KSs[(i0 + a) * VP + v0 + b] = ks[a][b];
+          if (with_q) QSs[(i0 + a) * VP + v0 + b] = qs[a][b];
+        }
     });
     x.sync();
     // U' = Z diag(beta) (V - diag(b) K S^T)
@@ -224,12 +263,26 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
     float *dst = p.states + ((size_t)(slot0 + ci) * Hv + h) * VK + (size_t)row0 * K;
     x.par(BV * K, [&](int idx) { dst[(idx / K) * (size_t)K + idx % K] = Ss[(idx / K) * KP + idx % K]; });
     prep(t0, n, false);
-    // S1 = b_last S + U'^T diag(d) K
-    x.par(BV * K, [&](int idx) {
-      const int v = idx / K, c = idx % K;
-      float acc = 0.f;
-      for (int j = 0; j < C; ++j) acc = fmaf(Us[j * VP + v] * dec[j], Ks[j * KP + c], acc);
-      Ss[v * KP + c] = fmaf(bex[C - 1], Ss[v * KP + c], acc);
+    // S1 = b_last S + U'^T diag(d) K, 2 x 4 tiles of (v, c) a thread
+    x.par((BV / 2) * (K / 4), [&](int t) {
+      const int v0 = (t / (K / 4)) * 2, c0 = (t % (K / 4)) * 4;
+      float acc[2][4] = {};
+      for (int j = 0; j < C; ++j) {
+        const float u0 = Us[j * VP + v0] * dec[j], u1 = Us[j * VP + v0 + 1] * dec[j];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float kv = Ks[j * KP + c0 + b];
+          acc[0][b] = fmaf(u0, kv, acc[0][b]);
+          acc[1][b] = fmaf(u1, kv, acc[1][b]);
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float *sp = Ss + (v0 + a) * KP + c0 + b;
+          *sp = fmaf(bex[C - 1], *sp, acc[a][b]);
+        }
     });
     x.sync();
   }
@@ -246,12 +299,22 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
     x.par(BV * K, [&](int idx) { Ss[(idx / K) * KP + idx % K] = src[(idx / K) * (size_t)K + idx % K]; });
     x.sync();
     prep(t0, n, true);
-    // K dS1^T; dP = Ot U'^T (lower incl. diagonal)
-    x.par(C * BV, [&](int idx) {
-      const int i = idx / BV, v = idx % BV;
-      float acc = 0.f;
-      for (int c = 0; c < K; ++c) acc = fmaf(Ks[i * KP + c], dSs[v * KP + c], acc);
-      dUs[i * VP + v] = acc;
+    // K dS1^T (2 x 2 tiles of (i, v) a thread); dP = Ot U'^T (lower incl. diagonal)
+    x.par((C / 2) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
+      float acc[2][2] = {};
+      for (int c = 0; c < K; ++c) {
+        const float k0 = Ks[i0 * KP + c], k1 = Ks[(i0 + 1) * KP + c];
+        const float d0 = dSs[v0 * KP + c], d1 = dSs[(v0 + 1) * KP + c];
+        acc[0][0] = fmaf(k0, d0, acc[0][0]);
+        acc[0][1] = fmaf(k0, d1, acc[0][1]);
+        acc[1][0] = fmaf(k1, d0, acc[1][0]);
+        acc[1][1] = fmaf(k1, d1, acc[1][1]);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) dUs[(i0 + a) * VP + v0 + b] = acc[a][b];
     });
     x.par(C * C, [&](int idx) {
       const int i = idx / C, j = idx % C;
@@ -355,33 +418,119 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       dTm[i * CP + j] = j < i ? bet[i] * dTm[i * CP + j] * G(i, j) : 0.f;
     });
     x.sync();
-    // dq and dk of the chunk's tokens
-    x.par(C * K, [&](int idx) {
-      const int i = idx / K, c = idx % K;
-      if (i >= n) return;
-      float sq = 0.f, sk = 0.f, sv = 0.f;
-      for (int v = 0; v < BV; ++v) {
-        sq = fmaf(Os[i * VP + v], Ss[v * KP + c], sq);
-        sk = fmaf(Us[i * VP + v], dSs[v * KP + c], sk);
-        sv = fmaf(dVs[i * VP + v], Ss[v * KP + c], sv);
-      }
-      float dq = bex[i] * sq, dk = dec[i] * sk - bex[i] * sv;
-      for (int j = 0; j <= i; ++j) dq = fmaf(dPm[i * CP + j] * G(i, j), Ks[j * KP + c], dq);
-      for (int j = i; j < C; ++j) dk = fmaf(dPm[j * CP + i] * G(j, i), Qs[j * KP + c], dk);
-      for (int j = 0; j < i; ++j) dk = fmaf(dTm[i * CP + j], Ks[j * KP + c], dk);
-      for (int j = i + 1; j < C; ++j) dk = fmaf(dTm[j * CP + i], Ks[j * KP + c], dk);
-      const size_t off = ((size_t)(t0 + i) * p.Hqk + qh) * K + c;
-      x.add(p.dqn + off, dq);
-      x.add(p.dkn + off, dk);
+    // M1 = dP * Gamma (lower, in dP's place) and D = dKK + dKK^T (symmetric, zero diagonal,
+    // in Y's place, free since dA), so that dq and dk are tiled products
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      dPm[i * CP + j] = dPm[i * CP + j] * Gm[i * CP + j];
+      Ym[i * CP + j] = j < i ? dTm[i * CP + j] : (j > i ? dTm[j * CP + i] : 0.f);
     });
     x.sync();
-    // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K
-    x.par(BV * K, [&](int idx) {
-      const int v = idx / K, c = idx % K;
-      float acc = bex[C - 1] * dSs[v * KP + c];
-      for (int i = 0; i < C; ++i)
-        acc = fmaf(bex[i], Os[i * VP + v] * Qs[i * KP + c] - dVs[i * VP + v] * Ks[i * KP + c], acc);
-      dSs[v * KP + c] = acc;
+    // dq and dk of the chunk's tokens, 4 x 8 tiles of (i, c) a thread:
+    //   dq = diag(b) Ot S + M1 K,  dk = diag(d) U' dS1 - diag(b) dV S + M1^T Q + D K
+    x.par((C / 4) * (K / 8), [&](int t) {
+      const int i0 = (t / (K / 8)) * 4, c0 = (t % (K / 8)) * 8;
+      float sq[4][8] = {}, sk[4][8] = {}, sv[4][8] = {};
+      for (int v = 0; v < BV; ++v) {
+        float o[4], u[4], w[4], sr[8], dr[8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          o[a] = Os[(i0 + a) * VP + v];
+          u[a] = Us[(i0 + a) * VP + v];
+          w[a] = dVs[(i0 + a) * VP + v];
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          sr[b] = Ss[v * KP + c0 + b];
+          dr[b] = dSs[v * KP + c0 + b];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            sq[a][b] = fmaf(o[a], sr[b], sq[a][b]);
+            sk[a][b] = fmaf(u[a], dr[b], sk[a][b]);
+            sv[a][b] = fmaf(w[a], sr[b], sv[a][b]);
+          }
+      }
+      float dq[4][8], dk[4][8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          dq[a][b] = bex[i0 + a] * sq[a][b];
+          dk[a][b] = dec[i0 + a] * sk[a][b] - bex[i0 + a] * sv[a][b];
+        }
+      // M1 is zero above the diagonal: row i needs j <= i, column i needs j >= i
+      for (int j = 0; j < i0 + 4; ++j) {
+        float m[4], kr[8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) m[a] = dPm[(i0 + a) * CP + j];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 8; ++b) dq[a][b] = fmaf(m[a], kr[b], dq[a][b]);
+      }
+      for (int j = i0; j < C; ++j) {
+        float m[4], qr[8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) m[a] = dPm[j * CP + i0 + a];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) qr[b] = Qs[j * KP + c0 + b];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 8; ++b) dk[a][b] = fmaf(m[a], qr[b], dk[a][b]);
+      }
+      for (int j = 0; j < C; ++j) {
+        float m[4], kr[8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) m[a] = Ym[(i0 + a) * CP + j];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 8; ++b) dk[a][b] = fmaf(m[a], kr[b], dk[a][b]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int i = i0 + a;
+        if (i >= n) continue;
+        const size_t off = ((size_t)(t0 + i) * p.Hqk + qh) * K + c0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          x.add(p.dqn + off + b, dq[a][b]);
+          x.add(p.dkn + off + b, dk[a][b]);
+        }
+      }
+    });
+    x.sync();
+    // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K, 2 x 4 tiles of (v, c) a thread
+    x.par((BV / 2) * (K / 4), [&](int t) {
+      const int v0 = (t / (K / 4)) * 2, c0 = (t % (K / 4)) * 4;
+      float acc[2][4];
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = bex[C - 1] * dSs[(v0 + a) * KP + c0 + b];
+      for (int i = 0; i < C; ++i) {
+        const float bi = bex[i];
+        const float o0 = Os[i * VP + v0], o1 = Os[i * VP + v0 + 1];
+        const float w0 = dVs[i * VP + v0], w1 = dVs[i * VP + v0 + 1];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float qv = Qs[i * KP + c0 + b], kv = Ks[i * KP + c0 + b];
+          acc[0][b] = fmaf(bi, o0 * qv - w0 * kv, acc[0][b]);
+          acc[1][b] = fmaf(bi, o1 * qv - w1 * kv, acc[1][b]);
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) dSs[(v0 + a) * KP + c0 + b] = acc[a][b];
     });
     x.sync();
   }
