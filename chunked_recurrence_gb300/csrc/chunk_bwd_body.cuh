@@ -199,19 +199,26 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         }
     });
     x.sync();
-    // Z = (I + A)^-1 by forward substitution, a row at a time: row i of Z (left of the
-    // diagonal) is -(A_ij + sum_{j<m<i} A_im Z_mj); rows above i already hold Z.
-    for (int i = 1; i < C; ++i) {
-      x.par(i, [&](int j) {
-        float acc = Zm[i * CP + j];
-        for (int m = j + 1; m < i; ++m) acc = fmaf(Zm[i * CP + m], Zm[m * CP + j], acc);
-        dgm[j] = acc;
+    // Z = (I + A)^-1 by a row sweep: once row m of Z is final (every row above it applied),
+    // each row i below it takes -A_im Z_m.  A stays in Zm while Z builds in Ym (free until the
+    // backward step's dT), then Z replaces A.  One barrier a step, a few FMAs a thread.
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      Ym[i * CP + j] = i == j ? 1.f : 0.f;
+    });
+    x.sync();
+    for (int m = 0; m < C - 1; ++m) {
+      const int cols = m + 1;  // row m of Z is zero right of its diagonal
+      x.par((C - 1 - m) * cols, [&](int idx) {
+        const int i = m + 1 + idx / cols, j = idx % cols;
+        Ym[i * CP + j] = fmaf(-Zm[i * CP + m], Ym[m * CP + j], Ym[i * CP + j]);
       });
       x.sync();
-      x.par(i, [&](int j) { Zm[i * CP + j] = -dgm[j]; });
-      x.sync();
     }
-    x.par(C, [&](int i) { Zm[i * CP + i] = 1.f; });
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      Zm[i * CP + j] = Ym[i * CP + j];
+    });
     // K S^T (and Q S^T), 2 x 2 tiles of (i, v) a thread
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
