@@ -247,13 +247,28 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         }
     });
     x.sync();
-    // U' = Z diag(beta) (V - diag(b) K S^T)
+    // U' = Z diag(beta) (V - diag(b) K S^T): the right factor first (into dV's place, free
+    // until the backward step's dV), then 2 x 2 tiles of (i, v) a thread
     x.par(C * BV, [&](int idx) {
-      const int i = idx / BV, v = idx % BV;
-      float acc = 0.f;
-      for (int j = 0; j <= i; ++j)
-        acc = fmaf(Zm[i * CP + j] * bet[j], Vs[j * VP + v] - bex[j] * KSs[j * VP + v], acc);
-      Us[i * VP + v] = acc;
+      const int j = idx / BV, v = idx % BV;
+      dVs[j * VP + v] = Vs[j * VP + v] - bex[j] * KSs[j * VP + v];
+    });
+    x.sync();
+    x.par((C / 2) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
+      float acc[2][2] = {};
+      for (int j = 0; j <= i0 + 1; ++j) {  // Z is zero right of its diagonal
+        const float z0 = Zm[i0 * CP + j] * bet[j], z1 = Zm[(i0 + 1) * CP + j] * bet[j];
+        const float w0 = dVs[j * VP + v0], w1 = dVs[j * VP + v0 + 1];
+        acc[0][0] = fmaf(z0, w0, acc[0][0]);
+        acc[0][1] = fmaf(z0, w1, acc[0][1]);
+        acc[1][0] = fmaf(z1, w0, acc[1][0]);
+        acc[1][1] = fmaf(z1, w1, acc[1][1]);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) Us[(i0 + a) * VP + v0 + b] = acc[a][b];
     });
     x.sync();
   };
@@ -362,6 +377,14 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       dTm[i * CP + j] = acc;
     });
     x.sync();
+    // b_last's gradient takes <S, dS1> over the block's rows: 64 partial sums (in dgm's
+    // place, free until dgamma) instead of one thread's 2048-term chain
+    x.par(C, [&](int r) {
+      float acc = 0.f;
+      for (int idx = r; idx < BV * K; idx += C) acc = fmaf(Ss[(idx / K) * KP + idx % K], dSs[(idx / K) * KP + idx % K], acc);
+      dgm[r] = acc;
+    });
+    x.sync();
     // dbeta from T = Z diag(beta); db; Y = (dT diag(beta)) Z^T
     x.par(C, [&](int j) {
       float acc = 0.f;
@@ -371,24 +394,56 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       for (int v = 0; v < BV; ++v)
         b += Os[j * VP + v] * QSs[j * VP + v] - dVs[j * VP + v] * KSs[j * VP + v];
       if (j == C - 1)
-        for (int idx = 0; idx < BV * K; ++idx) b = fmaf(Ss[(idx / K) * KP + idx % K], dSs[(idx / K) * KP + idx % K], b);
+        for (int r = 0; r < C; ++r) b += dgm[r];
       db[j] = b;
     });
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      const int mm = i < j ? i : j;
-      float acc = 0.f;
-      for (int m = 0; m <= mm; ++m) acc = fmaf(dTm[i * CP + m] * bet[m], Zm[j * CP + m], acc);
-      Ym[i * CP + j] = acc;
+    // Y, 4 x 4 tiles of (i, j) a thread: dT is zero right of its diagonal and Z too, so the
+    // terms past min(i, j) add zeros
+    x.par((C / 4) * (C / 4), [&](int t) {
+      const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
+      const int mend = (i0 < j0 ? i0 : j0) + 4;
+      float acc[4][4] = {};
+      for (int m = 0; m < mend; ++m) {
+        const float bm = bet[m];
+        float tr[4], zr[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          tr[a] = dTm[(i0 + a) * CP + m] * bm;
+          zr[a] = Zm[(j0 + a) * CP + m];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(tr[a], zr[b], acc[a][b]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) Ym[(i0 + a) * CP + j0 + b] = acc[a][b];
     });
     x.sync();
-    // dA = -Z^T Y, strictly lower (into dT's place)
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      float acc = 0.f;
-      if (j < i)
-        for (int m = i; m < C; ++m) acc = fmaf(Zm[m * CP + i], Ym[m * CP + j], acc);
-      dTm[i * CP + j] = -acc;
+    // dA = -Z^T Y, strictly lower (into dT's place), 4 x 4 tiles: Z^T's column i is zero
+    // above row i, so every row of a tile can start at the tile's first row
+    x.par((C / 4) * (C / 4), [&](int t) {
+      const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
+      float acc[4][4] = {};
+      if (j0 < i0 + 3)
+        for (int m = i0; m < C; ++m) {
+          float zr[4], yr[4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            zr[a] = Zm[m * CP + i0 + a];
+            yr[a] = Ym[m * CP + j0 + a];
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(zr[a], yr[b], acc[a][b]);
+        }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) dTm[(i0 + a) * CP + j0 + b] = j0 + b < i0 + a ? -acc[a][b] : 0.f;
     });
     x.sync();
     // dgamma (through Gamma in A and P, b and d) and the rest of dbeta
