@@ -32,6 +32,22 @@ struct DevLoad {
   __device__ __forceinline__ float operator()(const void *p, int64_t i) const {
     return to_f32<T>(reinterpret_cast<const T *>(p)[i]);
   }
+  __device__ __forceinline__ void vec8(const void *p, int64_t i, float *out) const {
+    if constexpr (sizeof(T) == 2) {
+      const uint4 r = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p) + i));
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        out[2 * e] = __uint_as_float(w[e] << 16);
+        out[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+      }
+    } else {
+      const float4 *q = reinterpret_cast<const float4 *>(reinterpret_cast<const T *>(p) + i);
+      const float4 a = __ldg(q), b = __ldg(q + 1);
+      out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+      out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    }
+  }
 };
 
 template <typename T>
@@ -120,6 +136,8 @@ extern "C" gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v,
   p.qs = qs; p.ks = ks; p.vs = vs;
   p.scale = scale;
   p.l2norm = (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0;
+  p.vec8 = aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && qs % 8 == 0 && ks % 8 == 0 && vs % 8 == 0 &&
+           (sh.dtype == GDN_BF16 || (qs % 4 == 0 && ks % 4 == 0 && vs % 4 == 0));
   p.states = (float *)(ws + kHeader);
   p.dqn = (float *)(ws + kHeader + states_bytes);
   p.dkn = (float *)(ws + kHeader + states_bytes + acc_bytes);

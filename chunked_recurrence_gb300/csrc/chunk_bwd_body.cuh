@@ -63,6 +63,7 @@ struct Params {
   int64_t qs, ks, vs;
   float scale;
   int l2norm;
+  int vec8;         // q, k, v load as 8-element vectors (16-byte aligned rows and strides)
   float *states;    // [slot][Hv][V][K]: chunk-start states (chunk c of sequence s: slot s + start/C + c)
   float *dqn, *dkn; // [n_tok][Hqk][K]: gradients of the unit-norm (or raw) q and k, accumulated
   float *dv;        // [n_tok][Hv][V]
@@ -77,7 +78,8 @@ GDN_BWD_HD size_t smem_floats(int K) {
   return 2 * C * KP + 2 * BV * KP + 7 * (size_t)C * VP + 7 * (size_t)C * CP + 8 * C;
 }
 
-// ld(ptr, i): element i of a q / k / v array as float
+// ld(ptr, i): element i of a q / k / v array as float; ld.vec8(ptr, i, out): elements
+// i .. i + 7 (i a multiple of 8, the array 16-byte aligned), used when p.vec8 is set
 template <class X, class LD>
 GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, int s) {
   const int K = p.K, KP = K + 1, V = p.V, Hv = p.Hv;
@@ -128,18 +130,55 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
 
   // ---- the chunk's inputs and its state-independent matrices (with_q: Q, dO, Q K^T too)
   auto prep = [&](int64_t t0, int n, bool with_q) {
-    x.par(C * K, [&](int idx) {
-      const int r = idx / K, c = idx % K;
-      const bool in = r < n;
-      Ks[r * KP + c] = in ? ld(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c) : 0.f;
-      if (with_q) Qs[r * KP + c] = in ? ld(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c) : 0.f;
-    });
-    x.par(C * BV, [&](int idx) {
-      const int r = idx / BV, j = idx % BV;
-      const bool in = r < n;
-      Vs[r * VP + j] = in ? ld(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j) : 0.f;
-      if (with_q) Os[r * VP + j] = in ? p.scale * p.dout[((t0 + r) * Hv + h) * V + row0 + j] : 0.f;
-    });
+    if (p.vec8) {
+      // 8 consecutive elements an item (one or two vector loads), so that each thread has
+      // several loads in flight instead of one
+      x.par(C * (K / 8), [&](int idx) {
+        const int r = idx / (K / 8), c = (idx % (K / 8)) * 8;
+        const bool in = r < n;
+        float kv[8] = {}, qv[8] = {};
+        if (in) {
+          ld.vec8(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c, kv);
+          if (with_q) ld.vec8(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c, qv);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          Ks[r * KP + c + e] = kv[e];
+          if (with_q) Qs[r * KP + c + e] = qv[e];
+        }
+      });
+      x.par(C * (BV / 8), [&](int idx) {
+        const int r = idx / (BV / 8), j = (idx % (BV / 8)) * 8;
+        const bool in = r < n;
+        float vv[8] = {}, ov[8] = {};
+        if (in) {
+          ld.vec8(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j, vv);
+          if (with_q) {
+            const float *src = p.dout + ((t0 + r) * Hv + h) * V + row0 + j;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ov[e] = p.scale * src[e];
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          Vs[r * VP + j + e] = vv[e];
+          if (with_q) Os[r * VP + j + e] = ov[e];
+        }
+      });
+    } else {
+      x.par(C * K, [&](int idx) {
+        const int r = idx / K, c = idx % K;
+        const bool in = r < n;
+        Ks[r * KP + c] = in ? ld(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c) : 0.f;
+        if (with_q) Qs[r * KP + c] = in ? ld(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c) : 0.f;
+      });
+      x.par(C * BV, [&](int idx) {
+        const int r = idx / BV, j = idx % BV;
+        const bool in = r < n;
+        Vs[r * VP + j] = in ? ld(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j) : 0.f;
+        if (with_q) Os[r * VP + j] = in ? p.scale * p.dout[((t0 + r) * Hv + h) * V + row0 + j] : 0.f;
+      });
+    }
     x.par(C, [&](int i) {
       const bool in = i < n;
       gam[i] = in ? p.g[(t0 + i) * Hv + h] : 0.f;

@@ -24,6 +24,9 @@ struct HostExec {
 
 struct HostLoad {
   float operator()(const void *p, int64_t i) const { return reinterpret_cast<const float *>(p)[i]; }
+  void vec8(const void *p, int64_t i, float *out) const {
+    for (int e = 0; e < 8; ++e) out[e] = reinterpret_cast<const float *>(p)[i + e];
+  }
 };
 
 }  // namespace
@@ -47,6 +50,7 @@ extern "C" int emu_chunk_bwd(const float *q, const float *k, const float *v, con
   p.Hqk = Hqk; p.Hv = Hv; p.K = K; p.V = V;
   p.qs = (int64_t)Hqk * K; p.ks = (int64_t)Hqk * K; p.vs = (int64_t)Hv * V;
   p.scale = scale; p.l2norm = l2norm;
+  p.vec8 = (K % 8 == 0 && V % 8 == 0) ? 1 : 0;
   p.states = states.data(); p.dqn = dqn.data(); p.dkn = dkn.data();
   p.dv = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0; p.status = &status;
   HostExec x;
