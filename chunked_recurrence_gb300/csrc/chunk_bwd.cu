@@ -50,11 +50,29 @@ struct DevLoad {
   }
 };
 
-template <typename T>
+template <typename T, int KD>
 __global__ void __launch_bounds__(kThreads) chunk_bwd_kernel(const gdn_bwd::Params p) {
   extern __shared__ float sm[];
   DevExec x{(int)threadIdx.x};
-  gdn_bwd::block(x, p, DevLoad<T>{}, sm, blockIdx.x, blockIdx.y, blockIdx.z);
+  gdn_bwd::block<KD>(x, p, DevLoad<T>{}, sm, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+template <typename T, int KD>
+gdn_status launch_bwd(const gdn_bwd::Params &p, dim3 grid, size_t smem, cudaStream_t st) {
+  if (cudaFuncSetAttribute(chunk_bwd_kernel<T, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return GDN_ERR_CUDA;
+  chunk_bwd_kernel<T, KD><<<grid, kThreads, smem, st>>>(p);
+  return GDN_OK;
+}
+
+template <typename T>
+gdn_status launch_bwd_k(const gdn_bwd::Params &p, dim3 grid, size_t smem, cudaStream_t st) {
+  switch (p.K) {
+    case 32: return launch_bwd<T, 32>(p, grid, smem, st);
+    case 64: return launch_bwd<T, 64>(p, grid, smem, st);
+    default: return launch_bwd<T, 128>(p, grid, smem, st);
+  }
 }
 
 template <typename T>
@@ -156,18 +174,14 @@ extern "C" gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v,
   const int64_t rows = n_tok * sh.Hqk;
   const unsigned lgrid = (unsigned)((2 * rows + 255) / 256);
   if (sh.dtype == GDN_BF16) {
-    if (cudaFuncSetAttribute(chunk_bwd_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return GDN_ERR_CUDA;
-    chunk_bwd_kernel<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p);
+    const gdn_status r = launch_bwd_k<__nv_bfloat16>(p, grid, smem, st);
+    if (r != GDN_OK) return r;
     if (rows > 0)
       l2_back_kernel<__nv_bfloat16><<<lgrid, 256, 0, st>>>(q, k, qs, ks, sh.Hqk, sh.K, p.l2norm, p.dqn, p.dkn, dq,
                                                            dk, rows);
   } else {
-    if (cudaFuncSetAttribute(chunk_bwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return GDN_ERR_CUDA;
-    chunk_bwd_kernel<float><<<grid, kThreads, smem, st>>>(p);
+    const gdn_status r = launch_bwd_k<float>(p, grid, smem, st);
+    if (r != GDN_OK) return r;
     if (rows > 0)
       l2_back_kernel<float><<<lgrid, 256, 0, st>>>(q, k, qs, ks, sh.Hqk, sh.K, p.l2norm, p.dqn, p.dkn, dq, dk, rows);
   }

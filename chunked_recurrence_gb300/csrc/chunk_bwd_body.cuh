@@ -80,9 +80,12 @@ GDN_BWD_HD size_t smem_floats(int K) {
 
 // ld(ptr, i): element i of a q / k / v array as float; ld.vec8(ptr, i, out): elements
 // i .. i + 7 (i a multiple of 8, the array 16-byte aligned), used when p.vec8 is set
-template <class X, class LD>
+// KD: the key width (p.K) as a compile-time constant (32, 64 or 128), so that the loops over
+// features unroll and row addresses fold into constants.
+template <int KD, class X, class LD>
 GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, int s) {
-  const int K = p.K, KP = K + 1, V = p.V, Hv = p.Hv;
+  constexpr int K = KD, KP = KD + 1;
+  const int V = p.V, Hv = p.Hv;
   float *Ks = sm;              // [C][KP]  k of the chunk (unit-norm when l2norm)
   float *Qs = Ks + C * KP;     // [C][KP]  q
   float *Ss = Qs + C * KP;     // [BV][KP] this block's rows of the chunk-start state
@@ -207,6 +210,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
       float kk[4][4] = {}, qk[4][4] = {};
       if (j0 <= i0 + 3) {  // tiles wholly above the diagonal hold zeros
+#pragma unroll 4
         for (int c = 0; c < K; ++c) {
           float ki[4], kj[4], qi[4];
 #pragma unroll
@@ -262,6 +266,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
       float ks[2][2] = {}, qs[2][2] = {};
+#pragma unroll 4
       for (int c = 0; c < K; ++c) {
         const float k0 = Ks[i0 * KP + c], k1 = Ks[(i0 + 1) * KP + c];
         const float s0 = Ss[v0 * KP + c], s1 = Ss[(v0 + 1) * KP + c];
@@ -364,6 +369,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
       float acc[2][2] = {};
+#pragma unroll 4
       for (int c = 0; c < K; ++c) {
         const float k0 = Ks[i0 * KP + c], k1 = Ks[(i0 + 1) * KP + c];
         const float d0 = dSs[v0 * KP + c], d1 = dSs[(v0 + 1) * KP + c];

@@ -56,7 +56,11 @@ extern "C" int emu_chunk_bwd(const float *q, const float *k, const float *v, con
   HostExec x;
   for (int s = 0; s < n_seqs; ++s)
     for (int h = 0; h < Hv; ++h)
-      for (int tile = 0; tile < V / gdn_bwd::BV; ++tile) gdn_bwd::block(x, p, HostLoad{}, sm.data(), tile, h, s);
+      for (int tile = 0; tile < V / gdn_bwd::BV; ++tile) {
+        if (K == 32) gdn_bwd::block<32>(x, p, HostLoad{}, sm.data(), tile, h, s);
+        else if (K == 64) gdn_bwd::block<64>(x, p, HostLoad{}, sm.data(), tile, h, s);
+        else gdn_bwd::block<128>(x, p, HostLoad{}, sm.data(), tile, h, s);
+      }
   for (int64_t r = 0; r < n_tok * Hqk; ++r) {
     gdn_bwd::l2_back_row(q, p.qs, Hqk, K, l2norm, HostLoad{}, dqn.data(), dq, r);
     gdn_bwd::l2_back_row(k, p.ks, Hqk, K, l2norm, HostLoad{}, dkn.data(), dk, r);
