@@ -329,15 +329,16 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
     float *dst = p.states + ((size_t)(slot0 + ci) * Hv + h) * VK + (size_t)row0 * K;
     x.par(BV * K, [&](int idx) { dst[(idx / K) * (size_t)K + idx % K] = Ss[(idx / K) * KP + idx % K]; });
     prep(t0, n, false);
-    // S1 = b_last S + U'^T diag(d) K, 2 x 4 tiles of (v, c) a thread
+    // S1 = b_last S + U'^T diag(d) K, 2 x 4 tiles of (v, c) a thread (columns c0 + b K / 4,
+    // so that neighbouring threads read neighbouring features)
     x.par((BV / 2) * (K / 4), [&](int t) {
-      const int v0 = (t / (K / 4)) * 2, c0 = (t % (K / 4)) * 4;
+      const int v0 = (t / (K / 4)) * 2, c0 = t % (K / 4);
       float acc[2][4] = {};
       for (int j = 0; j < C; ++j) {
         const float u0 = Us[j * VP + v0] * dec[j], u1 = Us[j * VP + v0 + 1] * dec[j];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const float kv = Ks[j * KP + c0 + b];
+          const float kv = Ks[j * KP + c0 + b * (K / 4)];
           acc[0][b] = fmaf(u0, kv, acc[0][b]);
           acc[1][b] = fmaf(u1, kv, acc[1][b]);
         }
@@ -346,7 +347,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          float *sp = Ss + (v0 + a) * KP + c0 + b;
+          float *sp = Ss + (v0 + a) * KP + c0 + b * (K / 4);
           *sp = fmaf(bex[C - 1], *sp, acc[a][b]);
         }
     });
@@ -533,10 +534,10 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       Ym[i * CP + j] = j < i ? dTm[i * CP + j] : (j > i ? dTm[j * CP + i] : 0.f);
     });
     x.sync();
-    // dq and dk of the chunk's tokens, 4 x 8 tiles of (i, c) a thread:
+    // dq and dk of the chunk's tokens, 4 x 8 tiles of (i, c) a thread (columns c0 + b K / 8):
     //   dq = diag(b) Ot S + M1 K,  dk = diag(d) U' dS1 - diag(b) dV S + M1^T Q + D K
     x.par((C / 4) * (K / 8), [&](int t) {
-      const int i0 = (t / (K / 8)) * 4, c0 = (t % (K / 8)) * 8;
+      const int i0 = (t / (K / 8)) * 4, c0 = t % (K / 8);
       float sq[4][8] = {}, sk[4][8] = {}, sv[4][8] = {};
       for (int v = 0; v < BV; ++v) {
         float o[4], u[4], w[4], sr[8], dr[8];
@@ -548,8 +549,8 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-          sr[b] = Ss[v * KP + c0 + b];
-          dr[b] = dSs[v * KP + c0 + b];
+          sr[b] = Ss[v * KP + c0 + b * (K / 8)];
+          dr[b] = dSs[v * KP + c0 + b * (K / 8)];
         }
 #pragma unroll
         for (int a = 0; a < 4; ++a)
@@ -574,7 +575,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
 #pragma unroll
         for (int a = 0; a < 4; ++a) m[a] = dPm[(i0 + a) * CP + j];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b];
+        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -585,7 +586,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
 #pragma unroll
         for (int a = 0; a < 4; ++a) m[a] = dPm[j * CP + i0 + a];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) qr[b] = Qs[j * KP + c0 + b];
+        for (int b = 0; b < 8; ++b) qr[b] = Qs[j * KP + c0 + b * (K / 8)];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -596,7 +597,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
 #pragma unroll
         for (int a = 0; a < 4; ++a) m[a] = Ym[(i0 + a) * CP + j];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b];
+        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -609,27 +610,28 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         const size_t off = ((size_t)(t0 + i) * p.Hqk + qh) * K + c0;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-          x.add(p.dqn + off + b, dq[a][b]);
-          x.add(p.dkn + off + b, dk[a][b]);
+          x.add(p.dqn + off + b * (K / 8), dq[a][b]);
+          x.add(p.dkn + off + b * (K / 8), dk[a][b]);
         }
       }
     });
     x.sync();
     // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K, 2 x 4 tiles of (v, c) a thread
+    // (columns c0 + b K / 4)
     x.par((BV / 2) * (K / 4), [&](int t) {
-      const int v0 = (t / (K / 4)) * 2, c0 = (t % (K / 4)) * 4;
+      const int v0 = (t / (K / 4)) * 2, c0 = t % (K / 4);
       float acc[2][4];
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = bex[C - 1] * dSs[(v0 + a) * KP + c0 + b];
+        for (int b = 0; b < 4; ++b) acc[a][b] = bex[C - 1] * dSs[(v0 + a) * KP + c0 + b * (K / 4)];
       for (int i = 0; i < C; ++i) {
         const float bi = bex[i];
         const float o0 = Os[i * VP + v0], o1 = Os[i * VP + v0 + 1];
         const float w0 = dVs[i * VP + v0], w1 = dVs[i * VP + v0 + 1];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const float qv = Qs[i * KP + c0 + b], kv = Ks[i * KP + c0 + b];
+          const float qv = Qs[i * KP + c0 + b * (K / 4)], kv = Ks[i * KP + c0 + b * (K / 4)];
           acc[0][b] = fmaf(bi, o0 * qv - w0 * kv, acc[0][b]);
           acc[1][b] = fmaf(bi, o1 * qv - w1 * kv, acc[1][b]);
         }
@@ -637,7 +639,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) dSs[(v0 + a) * KP + c0 + b] = acc[a][b];
+        for (int b = 0; b < 4; ++b) dSs[(v0 + a) * KP + c0 + b * (K / 4)] = acc[a][b];
     });
     x.sync();
   }
