@@ -384,12 +384,30 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
 #pragma unroll
         for (int b = 0; b < 2; ++b) dUs[(i0 + a) * VP + v0 + b] = acc[a][b];
     });
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      float acc = 0.f;
-      if (j <= i)
-        for (int v = 0; v < BV; ++v) acc = fmaf(Os[i * VP + v], Us[j * VP + v], acc);
-      dPm[i * CP + j] = acc;
+    // (4 x 4 tiles of (i, j): rows i0 .. i0 + 3, columns tj + 16 b)
+    x.par((C / 4) * 16, [&](int t) {
+      const int i0 = (t / 16) * 4, tj = t % 16;
+      float acc[4][4] = {};
+      if (tj <= i0 + 3)
+        for (int v = 0; v < BV; ++v) {
+          float o[4], u[4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            o[a] = Os[(i0 + a) * VP + v];
+            u[a] = Us[(tj + 16 * a) * VP + v];
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(o[a], u[b], acc[a][b]);
+        }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int i = i0 + a, j = tj + 16 * b;
+          dPm[i * CP + j] = j <= i ? acc[a][b] : 0.f;
+        }
     });
     x.sync();
     // dd_i = U'_i . (K dS1^T)_i;  dU' = diag(d) K dS1^T + P^T Ot
@@ -399,28 +417,76 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       dd[i] = acc;
     });
     x.sync();
-    x.par(C * BV, [&](int idx) {
-      const int i = idx / BV, v = idx % BV;
-      float acc = dec[i] * dUs[i * VP + v];
-      for (int j = i; j < C; ++j) acc = fmaf(QKm[j * CP + i] * G(j, i), Os[j * VP + v], acc);
-      dUs[i * VP + v] = acc;
+    // (2 x 2 tiles of (i, v); row i0 + 1's term at j = i0 has a zero factor, P being lower)
+    x.par((C / 2) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
+      float acc[2][2];
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) acc[a][b] = dec[i0 + a] * dUs[(i0 + a) * VP + v0 + b];
+      for (int j = i0; j < C; ++j) {
+        const float m0 = QKm[j * CP + i0] * G(j, i0), m1 = QKm[j * CP + i0 + 1] * G(j, i0 + 1);
+        const float o0 = Os[j * VP + v0], o1 = Os[j * VP + v0 + 1];
+        acc[0][0] = fmaf(m0, o0, acc[0][0]);
+        acc[0][1] = fmaf(m0, o1, acc[0][1]);
+        acc[1][0] = fmaf(m1, o0, acc[1][0]);
+        acc[1][1] = fmaf(m1, o1, acc[1][1]);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) dUs[(i0 + a) * VP + v0 + b] = acc[a][b];
     });
     x.sync();
     // dV = T^T dU' (complete for these rows); dT = dU' (V - diag(b) K S^T)^T (lower)
-    x.par(C * BV, [&](int idx) {
-      const int i = idx / BV, v = idx % BV;
-      float acc = 0.f;
-      for (int j = i; j < C; ++j) acc = fmaf(Zm[j * CP + i], dUs[j * VP + v], acc);
-      acc *= bet[i];
-      dVs[i * VP + v] = acc;
-      if (i < n) p.dv[((t0 + i) * Hv + h) * V + row0 + v] = acc;
+    // (dV in 2 x 2 tiles of (i, v), Z being lower; dT in 4 x 4 tiles of (i, j), columns tj + 16 b)
+    x.par((C / 2) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
+      float acc[2][2] = {};
+      for (int j = i0; j < C; ++j) {
+        const float z0 = Zm[j * CP + i0], z1 = Zm[j * CP + i0 + 1];
+        const float d0 = dUs[j * VP + v0], d1 = dUs[j * VP + v0 + 1];
+        acc[0][0] = fmaf(z0, d0, acc[0][0]);
+        acc[0][1] = fmaf(z0, d1, acc[0][1]);
+        acc[1][0] = fmaf(z1, d0, acc[1][0]);
+        acc[1][1] = fmaf(z1, d1, acc[1][1]);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int i = i0 + a;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const float r = acc[a][b] * bet[i];
+          dVs[i * VP + v0 + b] = r;
+          if (i < n) p.dv[((t0 + i) * Hv + h) * V + row0 + v0 + b] = r;
+        }
+      }
     });
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      float acc = 0.f;
-      if (j <= i)
-        for (int v = 0; v < BV; ++v) acc = fmaf(dUs[i * VP + v], Vs[j * VP + v] - bex[j] * KSs[j * VP + v], acc);
-      dTm[i * CP + j] = acc;
+    x.par((C / 4) * 16, [&](int t) {
+      const int i0 = (t / 16) * 4, tj = t % 16;
+      float acc[4][4] = {};
+      if (tj <= i0 + 3)
+        for (int v = 0; v < BV; ++v) {
+          float du[4], w[4];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            du[a] = dUs[(i0 + a) * VP + v];
+            const int j = tj + 16 * a;
+            w[a] = Vs[j * VP + v] - bex[j] * KSs[j * VP + v];
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(du[a], w[b], acc[a][b]);
+        }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int i = i0 + a, j = tj + 16 * b;
+          dTm[i * CP + j] = j <= i ? acc[a][b] : 0.f;
+        }
     });
     x.sync();
     // b_last's gradient takes <S, dS1> over the block's rows: 64 partial sums (in dgm's
