@@ -635,7 +635,7 @@ def run_backward_leg(crg, args, dev, stream, peaks):
             ts.append(e0.elapsed_time(e1))
     ms = statistics.median(ts)
     nb = bwd_bytes(wl, n_tok, 1)
-    return {"workload": wl.name, "kernel": "gdn_chunk_bwd (chunk_bwd_kernel + l2_back_kernel, fp32 CUDA cores)",
+    return {"workload": wl.name, "kernel": "gdn_chunk_bwd (chunk_bwd_prep_kernel, chunk_bwd_walk_kernel, chunk_bwd_grad_kernel, l2_back_kernel; fp32 CUDA cores)",
             "ms": round(ms, 3), "tokens_per_s": round(n_tok / (ms * 1e-3), 1), "bytes": nb,
             "achieved_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
             "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5),

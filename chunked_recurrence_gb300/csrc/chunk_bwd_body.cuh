@@ -1,4 +1,4 @@
-// chunk_bwd_body.cuh -- the block body of the fp32 backward of the chunked gated delta rule.
+// chunk_bwd_body.cuh -- the block bodies of the fp32 backward of the chunked gated delta rule.
 //
 // Training runs backward through the layer ("[v1] support GDN Ulysses cp", Testing: loss
 // alignment over training steps; "feat: hybrid CP for Qwen3.5 MoE (DeltaNet + attention)",
@@ -19,16 +19,25 @@
 //   dbeta = colsum(dT * Z) + rowsum(dA * KK * Gamma)
 //   dgamma from Gamma (row sums minus column sums of dGamma * Gamma), b and d; dg is the
 //   reverse cumulative sum of dgamma.
-// Each row of the state evolves on its own given k, g, beta and its column of v, and so
-// does each row of dS.  So a block owns BV rows of one v-head's state: it recomputes its
-// rows' chunk-start states in a forward sweep, then walks the chunks backward carrying its
-// rows of dS.  dv and dh0 of its rows are complete in the block; dq, dk, dg and dbeta are
-// sums over the blocks of a head (and over the v-heads of a q/k head) and are added
-// atomically.
+// The work runs as three kernels:
+//   prep  one block per (chunk, v-head), all in parallel: the chunk's state-independent
+//         matrices Z = (I + A)^-1, KG = (K K^T) * Gamma (strictly lower) and
+//         QG = (Q K^T) * Gamma (lower incl. the diagonal), stored once;
+//   walk  one block per (BV state rows, v-head, sequence).  Each row of the state evolves on
+//         its own given k, g, beta and its column of v, and so does each row of dS.  A block
+//         recomputes its rows' chunk-start states in a forward sweep, then walks the chunks
+//         backward carrying its rows of dS.  It completes dv and dh0 of its rows and adds
+//         the parts of dq and dk that take S or dS.  dP, dT, dd and db are sums over all
+//         state rows: each block adds its rows' share into per-chunk sums;
+//   grad  one block per (chunk, v-head), in parallel: from the summed dP, dT, dd and db,
+//         everything that is linear in them: dbeta, dgamma and so dg, and the (dP * Gamma)
+//         and dKK parts of dq and dk.
+// So the C x C work (K K^T, Q K^T, the inversion, Y, dA and the C x C x K products of dq
+// and dk) runs once per chunk and head, not once per block of state rows.
 //
-// The body is written against an executor X with three operations: x.par(n, f) runs f(i)
+// The bodies are written against an executor X with three operations: x.par(n, f) runs f(i)
 // for i in [0, n), the items independent of each other; x.sync() is a block barrier;
-// x.add(p, v) adds v to *p atomically.  The CUDA kernel runs items on threads with
+// x.add(p, v) adds v to *p atomically.  The CUDA kernels run items on threads with
 // __syncthreads(); a host harness runs the same code with plain loops.
 #pragma once
 
@@ -46,10 +55,11 @@
 
 namespace gdn_bwd {
 
-constexpr int C = 64;   // tokens per chunk
-constexpr int BV = 16;  // state rows per block
-constexpr int CP = C + 1, VP = BV + 1;
+constexpr int C = 64;  // tokens per chunk
+constexpr int CP = C + 1;
 constexpr float kEps = 1e-6f;  // q/k L2 norm: x / sqrt(sum x^2 + eps)
+constexpr size_t kPrep = 3 * (size_t)C * C;         // floats per (chunk, v-head): Z, KG, QG
+constexpr size_t kSums = 2 * (size_t)C * C + 2 * C;  // floats per (chunk, v-head): dP, dT, dd, db
 
 struct Params {
   const void *q, *k, *v;  // q, k [n_tok][Hqk][K] (token strides qs, ks), v [n_tok][Hv][V] (vs)
@@ -59,260 +69,270 @@ struct Params {
   const float *dhT;       // [n_seq][Hv][V][K] or null
   const int32_t *cu;      // sequence bounds, or null: rows of row_T tokens
   int64_t row_T, n_tok;
+  int n_seqs;
   int Hqk, Hv, K, V;
   int64_t qs, ks, vs;
   float scale;
   int l2norm;
   int vec8;         // q, k, v load as 8-element vectors (16-byte aligned rows and strides)
-  float *states;    // [slot][Hv][V][K]: chunk-start states (chunk c of sequence s: slot s + start/C + c)
+  // chunk slots: chunk c of sequence s is slot s + start_s / C + c (distinct for every chunk)
+  float *states;    // [slot][Hv][V][K]: chunk-start states
+  float *fw;        // [slot][Hv][3][C][V]: the forward sweep's U', V - diag(b) K S^T and K S^T
+  float *prep;      // [slot][Hv][kPrep]: Z, KG, QG, each [C][C] row-major
+  float *sums;      // [slot][Hv][kSums]: dP [C][C], dT [C][C], dd [C], db [C]; zero before the walk
   float *dqn, *dkn; // [n_tok][Hqk][K]: gradients of the unit-norm (or raw) q and k, accumulated
   float *dv;        // [n_tok][Hv][V]
-  float *dg, *dbeta;  // [n_tok][Hv], accumulated
+  float *dg, *dbeta;  // [n_tok][Hv]
   float *dh0;       // [n_seq][Hv][V][K] or null
   int32_t *status;  // set to GDN_ERR_BOUNDS on a bad sequence range
 };
 
 // shared memory of one block, in floats
-GDN_BWD_HD size_t smem_floats(int K) {
-  const size_t KP = (size_t)K + 1;
-  return 2 * C * KP + 2 * BV * KP + 7 * (size_t)C * VP + 7 * (size_t)C * CP + 8 * C;
+GDN_BWD_HD size_t prep_smem_floats(int K) { return 2 * (size_t)C * (K + 1) + 2 * (size_t)C * CP + 4 * C; }
+GDN_BWD_HD size_t walk_smem_floats(int K, int BV) {
+  return 2 * (size_t)C * (K + 1) + 2 * (size_t)BV * (K + 1) + 8 * (size_t)C * (BV + 1) + 2 * (size_t)C * CP + 8 * C;
+}
+GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 1) + 6 * (size_t)C * CP + 8 * C; }
+
+GDN_BWD_FN int64_t seq_start(const Params &p, int s) { return p.cu ? (int64_t)p.cu[s] : (int64_t)s * p.row_T; }
+
+GDN_BWD_FN bool seq_bounds(const Params &p, int s, int64_t &start, int64_t &end) {
+  start = seq_start(p, s);
+  end = p.cu ? (int64_t)p.cu[s + 1] : start + p.row_T;
+  return start >= 0 && end >= start && end <= p.n_tok;
 }
 
-// ld(ptr, i): element i of a q / k / v array as float; ld.vec8(ptr, i, out): elements
-// i .. i + 7 (i a multiple of 8, the array 16-byte aligned), used when p.vec8 is set
-// KD: the key width (p.K) as a compile-time constant (32, 64 or 128), so that the loops over
-// features unroll and row addresses fold into constants.
+// The chunk held by a slot: its first token t0 and length n.  False for a slot that no chunk
+// uses (slots are distinct, not dense) and for a sequence whose bounds are bad (the walk
+// reports those).  Slot s + start_s / C is the first of sequence s, rising with s.
+GDN_BWD_FN bool slot_chunk(const Params &p, int64_t slot, int64_t &t0, int &n) {
+  int lo = 0, hi = p.n_seqs - 1;
+  while (lo < hi) {  // the last sequence whose first slot is at or before this one
+    const int mid = (lo + hi + 1) / 2;
+    if (mid + seq_start(p, mid) / C <= slot) lo = mid;
+    else hi = mid - 1;
+  }
+  int64_t start, end;
+  if (!seq_bounds(p, lo, start, end)) return false;
+  const int64_t ci = slot - (lo + start / C);
+  if (ci < 0 || ci * C >= end - start) return false;
+  t0 = start + ci * C;
+  n = (int)(end - t0 < C ? end - t0 : C);
+  return true;
+}
+
+// Rows t0 .. t0 + n - 1 of k (and of q, when Qs is given) of q/k head qh into [C][K + 1]
+// tiles, zero past n.  The L2 norm follows in norm_and_cumsum, after a barrier.
+template <int K, class X, class LD>
+GDN_BWD_FN void load_keys(X &x, const Params &p, LD ld, float *Ks, float *Qs, int64_t t0, int n, int qh) {
+  constexpr int KP = K + 1;
+  const bool with_q = Qs != nullptr;
+  if (p.vec8) {
+    // 8 consecutive elements an item (one or two vector loads), so that each thread has
+    // several loads in flight instead of one
+    x.par(C * (K / 8), [&](int idx) {
+      const int r = idx / (K / 8), c = (idx % (K / 8)) * 8;
+      float kv[8] = {}, qv[8] = {};
+      if (r < n) {
+        ld.vec8(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c, kv);
+        if (with_q) ld.vec8(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c, qv);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        Ks[r * KP + c + e] = kv[e];
+        if (with_q) Qs[r * KP + c + e] = qv[e];
+      }
+    });
+  } else {
+    x.par(C * K, [&](int idx) {
+      const int r = idx / K, c = idx % K;
+      const bool in = r < n;
+      Ks[r * KP + c] = in ? ld(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c) : 0.f;
+      if (with_q) Qs[r * KP + c] = in ? ld(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c) : 0.f;
+    });
+  }
+}
+
+template <class X>
+GDN_BWD_FN void load_gates(X &x, const Params &p, float *gam, float *bet, int64_t t0, int n, int h) {
+  x.par(C, [&](int i) {
+    const bool in = i < n;
+    gam[i] = in ? p.g[(t0 + i) * p.Hv + h] : 0.f;
+    bet[i] = in ? p.beta[(t0 + i) * p.Hv + h] : 0.f;
+  });
+}
+
+// After the loads' barrier: unit-norm rows of k (and q), gamma = the inclusive cumsum of g.
+// The rows past n are zero and stay zero; gamma past n repeats the last token's.
+template <int K, class X>
+GDN_BWD_FN void norm_and_cumsum(X &x, const Params &p, float *Ks, float *Qs, float *gam) {
+  constexpr int KP = K + 1;
+  if (p.l2norm) {
+    x.par(Qs ? 2 * C : C, [&](int r) {
+      float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
+      float ss = 0.f;
+      for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
+      const float inv = 1.f / sqrtf(ss + kEps);
+      for (int c = 0; c < K; ++c) row[c] *= inv;
+    });
+  }
+  if (x.leader())
+    for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
+}
+
+// ---- prep: Z, KG and QG of one (chunk, v-head)
 template <int KD, class X, class LD>
-GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, int s) {
+GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot, int h) {
   constexpr int K = KD, KP = KD + 1;
+  int64_t t0;
+  int n;
+  if (!slot_chunk(p, slot, t0, n)) return;
+  float *Ks = sm;             // [C][KP]
+  float *Qs = Ks + C * KP;    // [C][KP]
+  float *Am = Qs + C * KP;    // [C][CP]  A (strictly lower)
+  float *Zb = Am + C * CP;    // [C][CP]  Z, built row by row
+  float *gam = Zb + C * CP;   // [C]
+  float *bet = gam + C;       // [C]
+  float *out = p.prep + ((size_t)slot * p.Hv + h) * kPrep;
+  float *KGo = out + C * C, *QGo = out + 2 * C * C;
+  load_keys<K>(x, p, ld, Ks, Qs, t0, n, h / (p.Hv / p.Hqk));
+  load_gates(x, p, gam, bet, t0, n, h);
+  x.sync();
+  norm_and_cumsum<K>(x, p, Ks, Qs, gam);
+  x.sync();
+  // K K^T and Q K^T, 4 x 4 tiles of (i, j) a thread: every loaded k or q value feeds four
+  // products.  Gamma, KG, QG and A = diag(beta) KG follow in the tile's epilogue.
+  x.par((C / 4) * (C / 4), [&](int t) {
+    const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
+    float kk[4][4] = {}, qk[4][4] = {};
+    if (j0 <= i0 + 3) {  // tiles wholly above the diagonal hold zeros
+#pragma unroll 4
+      for (int c = 0; c < K; ++c) {
+        float ki[4], kj[4], qi[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          ki[r] = Ks[(i0 + r) * KP + c];
+          kj[r] = Ks[(j0 + r) * KP + c];
+          qi[r] = Qs[(i0 + r) * KP + c];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            kk[a][b] = fmaf(ki[a], kj[b], kk[a][b]);
+            qk[a][b] = fmaf(qi[a], kj[b], qk[a][b]);
+          }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int i = i0 + a, j = j0 + b;
+        const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
+        const float kg = j < i ? kk[a][b] * gij : 0.f;
+        Am[i * CP + j] = bet[i] * kg;
+        KGo[i * C + j] = kg;
+        QGo[i * C + j] = j <= i ? qk[a][b] * gij : 0.f;
+      }
+  });
+  x.par(C * C, [&](int idx) {
+    const int i = idx / C, j = idx % C;
+    Zb[i * CP + j] = i == j ? 1.f : 0.f;
+  });
+  x.sync();
+  // Z = (I + A)^-1 by a row sweep: once row m of Z is final (every row above it applied),
+  // each row i below it takes -A_im Z_m.  One barrier a step, a few FMAs a thread.
+  for (int m = 0; m < C - 1; ++m) {
+    const int cols = m + 1;  // row m of Z is zero right of its diagonal
+    x.par((C - 1 - m) * cols, [&](int idx) {
+      const int i = m + 1 + idx / cols, j = idx % cols;
+      Zb[i * CP + j] = fmaf(-Am[i * CP + m], Zb[m * CP + j], Zb[i * CP + j]);
+    });
+    x.sync();
+  }
+  x.par(C * C, [&](int idx) { out[idx] = Zb[(idx / C) * CP + idx % C]; });
+}
+
+// ---- walk: the state-dependent steps of BV state rows of one v-head, chunk by chunk
+template <int KD, int BV, class X, class LD>
+GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, int h, int s) {
+  constexpr int K = KD, KP = KD + 1, VP = BV + 1;
   const int V = p.V, Hv = p.Hv;
   float *Ks = sm;              // [C][KP]  k of the chunk (unit-norm when l2norm)
   float *Qs = Ks + C * KP;     // [C][KP]  q
   float *Ss = Qs + C * KP;     // [BV][KP] this block's rows of the chunk-start state
   float *dSs = Ss + BV * KP;   // [BV][KP] their gradient, carried from the chunk's end
-  float *Vs = dSs + BV * KP;   // [C][VP]  v columns of the block's rows
+  float *Vs = dSs + BV * KP;   // [C][VP]  v columns of the block's rows (forward sweep)
   float *Os = Vs + C * VP;     // [C][VP]  scale * dO
   float *Us = Os + C * VP;     // [C][VP]  U'
-  float *dUs = Us + C * VP;    // [C][VP]  K dS1^T, then dU'
-  float *dVs = dUs + C * VP;   // [C][VP]  dV
-  float *KSs = dVs + C * VP;   // [C][VP]  K S^T
+  float *KdS = Us + C * VP;    // [C][VP]  K dS1^T
+  float *dUs = KdS + C * VP;   // [C][VP]  dU'
+  float *Ws = dUs + C * VP;    // [C][VP]  V - diag(b) K S^T, then dV
+  float *KSs = Ws + C * VP;    // [C][VP]  K S^T
   float *QSs = KSs + C * VP;   // [C][VP]  Q S^T
-  float *Zm = QSs + C * VP;    // [C][CP]  A, then Z = (I + A)^-1 (unit lower)
-  float *QKm = Zm + C * CP;    // [C][CP]  Q K^T (lower incl. diagonal)
-  float *KKm = QKm + C * CP;   // [C][CP]  K K^T (strictly lower)
-  float *dPm = KKm + C * CP;   // [C][CP]  dP (lower incl. diagonal)
-  float *dTm = dPm + C * CP;   // [C][CP]  dT, then dA, then dKK
-  float *Ym = dTm + C * CP;    // [C][CP]  (dT diag(beta)) Z^T
-  float *gam = Ym + C * CP;    // [C] gamma
+  float *Zm = QSs + C * VP;    // [C][CP]  Z (from prep)
+  float *QGm = Zm + C * CP;    // [C][CP]  QG (from prep)
+  float *gam = QGm + C * CP;   // [C] gamma
   float *bet = gam + C;        // [C] beta
   float *bex = bet + C;        // [C] exp(gamma)
   float *dec = bex + C;        // [C] exp(gamma_last - gamma)
-  float *db = dec + C;         // [C] dL/db
-  float *dd = db + C;          // [C] dL/dd
-  float *dbt = dd + C;         // [C] dL/dbeta
-  float *dgm = dbt + C;        // [C] scratch of the inversion, then dL/dgamma
-  float *Gm = dgm + C;         // [C][CP]  Gamma_ij = exp(gamma_i - gamma_j), j <= i (once per chunk)
+  float *prt = dec + C;        // [C] partial sums of <S, dS1>
 
   const int qh = h / (Hv / p.Hqk), row0 = tile * BV;
   int64_t start, end;
-  if (p.cu) {
-    start = p.cu[s];
-    end = p.cu[s + 1];
-  } else {
-    start = (int64_t)s * p.row_T;
-    end = start + p.row_T;
-  }
-  if (start < 0 || end < start || end > p.n_tok) {
+  if (!seq_bounds(p, s, start, end)) {
     x.fail(p.status);
     return;
   }
   const int64_t slot0 = (int64_t)s + start / C;
   const int n_chunks = (int)((end - start + C - 1) / C);
-  const size_t VK = (size_t)V * K;
-  auto G = [&](int i, int j) { return Gm[i * CP + j]; };  // j <= i
+  const size_t VK = (size_t)V * K, CV = (size_t)C * V;
+  // the forward sweep's U', V - diag(b) K S^T and K S^T of the block's columns, [C][V] each
+  auto fw_of = [&](int64_t slot) { return p.fw + ((size_t)slot * Hv + h) * 3 * CV + row0; };
 
-  // ---- the chunk's inputs and its state-independent matrices (with_q: Q, dO, Q K^T too)
-  auto prep = [&](int64_t t0, int n, bool with_q) {
+  // the chunk's inputs: k (and q), the block's v columns (forward) or scale * dO (backward),
+  // the gates, and Z (and QG) from prep; then the norm, gamma, b and d.  Ends on a barrier.
+  auto load = [&](int64_t slot, int64_t t0, int n, bool bwd) {
+    load_keys<K>(x, p, ld, Ks, bwd ? Qs : nullptr, t0, n, qh);
     if (p.vec8) {
-      // 8 consecutive elements an item (one or two vector loads), so that each thread has
-      // several loads in flight instead of one
-      x.par(C * (K / 8), [&](int idx) {
-        const int r = idx / (K / 8), c = (idx % (K / 8)) * 8;
-        const bool in = r < n;
-        float kv[8] = {}, qv[8] = {};
-        if (in) {
-          ld.vec8(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c, kv);
-          if (with_q) ld.vec8(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c, qv);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          Ks[r * KP + c + e] = kv[e];
-          if (with_q) Qs[r * KP + c + e] = qv[e];
-        }
-      });
       x.par(C * (BV / 8), [&](int idx) {
         const int r = idx / (BV / 8), j = (idx % (BV / 8)) * 8;
-        const bool in = r < n;
-        float vv[8] = {}, ov[8] = {};
-        if (in) {
-          ld.vec8(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j, vv);
-          if (with_q) {
+        float vv[8] = {};
+        if (r < n) {
+          if (bwd) {
             const float *src = p.dout + ((t0 + r) * Hv + h) * V + row0 + j;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ov[e] = p.scale * src[e];
+            for (int e = 0; e < 8; ++e) vv[e] = p.scale * src[e];
+          } else {
+            ld.vec8(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j, vv);
           }
         }
+        float *dst = (bwd ? Os : Vs) + r * VP + j;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          Vs[r * VP + j + e] = vv[e];
-          if (with_q) Os[r * VP + j + e] = ov[e];
-        }
+        for (int e = 0; e < 8; ++e) dst[e] = vv[e];
       });
     } else {
-      x.par(C * K, [&](int idx) {
-        const int r = idx / K, c = idx % K;
-        const bool in = r < n;
-        Ks[r * KP + c] = in ? ld(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c) : 0.f;
-        if (with_q) Qs[r * KP + c] = in ? ld(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c) : 0.f;
-      });
       x.par(C * BV, [&](int idx) {
         const int r = idx / BV, j = idx % BV;
         const bool in = r < n;
-        Vs[r * VP + j] = in ? ld(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j) : 0.f;
-        if (with_q) Os[r * VP + j] = in ? p.scale * p.dout[((t0 + r) * Hv + h) * V + row0 + j] : 0.f;
+        if (bwd) Os[r * VP + j] = in ? p.scale * p.dout[((t0 + r) * Hv + h) * V + row0 + j] : 0.f;
+        else Vs[r * VP + j] = in ? ld(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j) : 0.f;
       });
     }
-    x.par(C, [&](int i) {
-      const bool in = i < n;
-      gam[i] = in ? p.g[(t0 + i) * Hv + h] : 0.f;
-      bet[i] = in ? p.beta[(t0 + i) * Hv + h] : 0.f;
+    load_gates(x, p, gam, bet, t0, n, h);
+    const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
+    x.par(C * C, [&](int idx) {
+      const int i = idx / C, j = idx % C;
+      Zm[i * CP + j] = pr[idx];
+      if (bwd) QGm[i * CP + j] = pr[2 * C * C + idx];
     });
     x.sync();
-    if (p.l2norm) {
-      x.par(with_q ? 2 * C : C, [&](int r) {
-        float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
-        float ss = 0.f;
-        for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
-        const float inv = 1.f / sqrtf(ss + kEps);
-        for (int c = 0; c < K; ++c) row[c] *= inv;
-      });
-    }
-    if (x.leader())
-      for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
+    norm_and_cumsum<K>(x, p, Ks, bwd ? Qs : nullptr, gam);
     x.sync();
     x.par(C, [&](int i) {
       bex[i] = expf(gam[i]);
       dec[i] = expf(gam[C - 1] - gam[i]);
-    });
-    // K K^T (strictly lower) and Q K^T (lower), 4 x 4 tiles of (i, j) a thread: every loaded
-    // k or q value feeds four products
-    x.par((C / 4) * (C / 4), [&](int t) {
-      const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
-      float kk[4][4] = {}, qk[4][4] = {};
-      if (j0 <= i0 + 3) {  // tiles wholly above the diagonal hold zeros
-#pragma unroll 4
-        for (int c = 0; c < K; ++c) {
-          float ki[4], kj[4], qi[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            ki[r] = Ks[(i0 + r) * KP + c];
-            kj[r] = Ks[(j0 + r) * KP + c];
-            qi[r] = with_q ? Qs[(i0 + r) * KP + c] : 0.f;
-          }
-#pragma unroll
-          for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              kk[a][b] = fmaf(ki[a], kj[b], kk[a][b]);
-              qk[a][b] = fmaf(qi[a], kj[b], qk[a][b]);
-            }
-        }
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int i = i0 + a, j = j0 + b;
-          const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
-          const float kv = j < i ? kk[a][b] : 0.f;
-          Gm[i * CP + j] = gij;
-          KKm[i * CP + j] = kv;
-          Zm[i * CP + j] = j < i ? bet[i] * gij * kv : 0.f;
-          if (with_q) QKm[i * CP + j] = j <= i ? qk[a][b] : 0.f;
-        }
-    });
-    x.sync();
-    // Z = (I + A)^-1 by a row sweep: once row m of Z is final (every row above it applied),
-    // each row i below it takes -A_im Z_m.  A stays in Zm while Z builds in Ym (free until the
-    // backward step's dT), then Z replaces A.  One barrier a step, a few FMAs a thread.
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      Ym[i * CP + j] = i == j ? 1.f : 0.f;
-    });
-    x.sync();
-    for (int m = 0; m < C - 1; ++m) {
-      const int cols = m + 1;  // row m of Z is zero right of its diagonal
-      x.par((C - 1 - m) * cols, [&](int idx) {
-        const int i = m + 1 + idx / cols, j = idx % cols;
-        Ym[i * CP + j] = fmaf(-Zm[i * CP + m], Ym[m * CP + j], Ym[i * CP + j]);
-      });
-      x.sync();
-    }
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      Zm[i * CP + j] = Ym[i * CP + j];
-    });
-    // K S^T (and Q S^T), 2 x 2 tiles of (i, v) a thread
-    x.par((C / 2) * (BV / 2), [&](int t) {
-      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
-      float ks[2][2] = {}, qs[2][2] = {};
-#pragma unroll 4
-      for (int c = 0; c < K; ++c) {
-        const float k0 = Ks[i0 * KP + c], k1 = Ks[(i0 + 1) * KP + c];
-        const float s0 = Ss[v0 * KP + c], s1 = Ss[(v0 + 1) * KP + c];
-        ks[0][0] = fmaf(k0, s0, ks[0][0]);
-        ks[0][1] = fmaf(k0, s1, ks[0][1]);
-        ks[1][0] = fmaf(k1, s0, ks[1][0]);
-        ks[1][1] = fmaf(k1, s1, ks[1][1]);
-        if (with_q) {
-          const float q0 = Qs[i0 * KP + c], q1 = Qs[(i0 + 1) * KP + c];
-          qs[0][0] = fmaf(q0, s0, qs[0][0]);
-          qs[0][1] = fmaf(q0, s1, qs[0][1]);
-          qs[1][0] = fmaf(q1, s0, qs[1][0]);
-          qs[1][1] = fmaf(q1, s1, qs[1][1]);
-        }
-      }
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          KSs[(i0 + a) * VP + v0 + b] = ks[a][b];
-          if (with_q) QSs[(i0 + a) * VP + v0 + b] = qs[a][b];
-        }
-    });
-    x.sync();
-    // U' = Z diag(beta) (V - diag(b) K S^T): the right factor first (into dV's place, free
-    // until the backward step's dV), then 2 x 2 tiles of (i, v) a thread
-    x.par(C * BV, [&](int idx) {
-      const int j = idx / BV, v = idx % BV;
-      dVs[j * VP + v] = Vs[j * VP + v] - bex[j] * KSs[j * VP + v];
-    });
-    x.sync();
-    x.par((C / 2) * (BV / 2), [&](int t) {
-      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
-      float acc[2][2] = {};
-      for (int j = 0; j <= i0 + 1; ++j) {  // Z is zero right of its diagonal
-        const float z0 = Zm[i0 * CP + j] * bet[j], z1 = Zm[(i0 + 1) * CP + j] * bet[j];
-        const float w0 = dVs[j * VP + v0], w1 = dVs[j * VP + v0 + 1];
-        acc[0][0] = fmaf(z0, w0, acc[0][0]);
-        acc[0][1] = fmaf(z0, w1, acc[0][1]);
-        acc[1][0] = fmaf(z1, w0, acc[1][0]);
-        acc[1][1] = fmaf(z1, w1, acc[1][1]);
-      }
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 2; ++b) Us[(i0 + a) * VP + v0 + b] = acc[a][b];
     });
     x.sync();
   };
@@ -324,27 +344,79 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
   });
   x.sync();
   for (int ci = 0; ci < n_chunks; ++ci) {
-    const int64_t t0 = start + (int64_t)ci * C;
+    const int64_t t0 = start + (int64_t)ci * C, slot = slot0 + ci;
     const int n = (int)(end - t0 < C ? end - t0 : C);
-    float *dst = p.states + ((size_t)(slot0 + ci) * Hv + h) * VK + (size_t)row0 * K;
+    float *dst = p.states + ((size_t)slot * Hv + h) * VK + (size_t)row0 * K;
     x.par(BV * K, [&](int idx) { dst[(idx / K) * (size_t)K + idx % K] = Ss[(idx / K) * KP + idx % K]; });
-    prep(t0, n, false);
-    // S1 = b_last S + U'^T diag(d) K, 2 x 4 tiles of (v, c) a thread (columns c0 + b K / 4,
-    // so that neighbouring threads read neighbouring features)
-    x.par((BV / 2) * (K / 4), [&](int t) {
-      const int v0 = (t / (K / 4)) * 2, c0 = t % (K / 4);
-      float acc[2][4] = {};
-      for (int j = 0; j < C; ++j) {
-        const float u0 = Us[j * VP + v0] * dec[j], u1 = Us[j * VP + v0 + 1] * dec[j];
+    load(slot, t0, n, false);
+    float *fw = fw_of(slot);
+    // K S^T, 4 x 2 tiles of (i, v) a thread; the epilogue forms V - diag(b) K S^T, and both
+    // go to the backward sweep
+    x.par((C / 4) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 4, v0 = (t % (BV / 2)) * 2;
+      float ks[4][2] = {};
+#pragma unroll 4
+      for (int c = 0; c < K; ++c) {
+        const float s0 = Ss[v0 * KP + c], s1 = Ss[(v0 + 1) * KP + c];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float kv = Ks[j * KP + c0 + b * (K / 4)];
-          acc[0][b] = fmaf(u0, kv, acc[0][b]);
-          acc[1][b] = fmaf(u1, kv, acc[1][b]);
+        for (int a = 0; a < 4; ++a) {
+          const float kv = Ks[(i0 + a) * KP + c];
+          ks[a][0] = fmaf(kv, s0, ks[a][0]);
+          ks[a][1] = fmaf(kv, s1, ks[a][1]);
         }
       }
 #pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int i = i0 + a, v = v0 + b;
+          const float w = Vs[i * VP + v] - bex[i] * ks[a][b];
+          Ws[i * VP + v] = w;
+          fw[CV + (size_t)i * V + v] = w;
+          fw[2 * CV + (size_t)i * V + v] = ks[a][b];
+        }
+    });
+    x.sync();
+    // U' = Z diag(beta) (V - diag(b) K S^T), 2 x 2 tiles of (i, v) a thread
+    x.par((C / 2) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
+      float acc[2][2] = {};
+      for (int j = 0; j <= i0 + 1; ++j) {  // Z is zero right of its diagonal
+        const float z0 = Zm[i0 * CP + j] * bet[j], z1 = Zm[(i0 + 1) * CP + j] * bet[j];
+        const float w0 = Ws[j * VP + v0], w1 = Ws[j * VP + v0 + 1];
+        acc[0][0] = fmaf(z0, w0, acc[0][0]);
+        acc[0][1] = fmaf(z0, w1, acc[0][1]);
+        acc[1][0] = fmaf(z1, w0, acc[1][0]);
+        acc[1][1] = fmaf(z1, w1, acc[1][1]);
+      }
+#pragma unroll
       for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          Us[(i0 + a) * VP + v0 + b] = acc[a][b];
+          fw[(size_t)(i0 + a) * V + v0 + b] = acc[a][b];
+        }
+    });
+    x.sync();
+    // S1 = b_last S + U'^T diag(d) K, 4 x 4 tiles of (v, c) a thread (columns c0 + b K / 4,
+    // so that neighbouring threads read neighbouring features)
+    x.par((BV / 4) * (K / 4), [&](int t) {
+      const int v0 = (t / (K / 4)) * 4, c0 = t % (K / 4);
+      float acc[4][4] = {};
+      for (int j = 0; j < C; ++j) {
+        const float dj = dec[j];
+        float u[4], kv[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) u[a] = Us[j * VP + v0 + a] * dj;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) kv[b] = Ks[j * KP + c0 + b * (K / 4)];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(u[a], kv[b], acc[a][b]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           float *sp = Ss + (v0 + a) * KP + c0 + b * (K / 4);
@@ -360,73 +432,88 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
     dSs[r * KP + c] = p.dhT ? p.dhT[((size_t)s * Hv + h) * VK + (size_t)(row0 + r) * K + c] : 0.f;
   });
   for (int ci = n_chunks - 1; ci >= 0; --ci) {
-    const int64_t t0 = start + (int64_t)ci * C;
+    const int64_t t0 = start + (int64_t)ci * C, slot = slot0 + ci;
     const int n = (int)(end - t0 < C ? end - t0 : C);
-    const float *src = p.states + ((size_t)(slot0 + ci) * Hv + h) * VK + (size_t)row0 * K;
+    const float *src = p.states + ((size_t)slot * Hv + h) * VK + (size_t)row0 * K;
+    const float *fw = fw_of(slot);
+    float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
+    float *dPsum = sums, *dTsum = sums + C * C, *ddsum = sums + 2 * C * C, *dbsum = ddsum + C;
     x.par(BV * K, [&](int idx) { Ss[(idx / K) * KP + idx % K] = src[(idx / K) * (size_t)K + idx % K]; });
-    x.sync();
-    prep(t0, n, true);
-    // K dS1^T (2 x 2 tiles of (i, v) a thread); dP = Ot U'^T (lower incl. diagonal)
-    x.par((C / 2) * (BV / 2), [&](int t) {
-      const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
-      float acc[2][2] = {};
-#pragma unroll 4
+    x.par(C * BV, [&](int idx) {
+      const int i = idx / BV, v = idx % BV;
+      Us[i * VP + v] = fw[(size_t)i * V + v];
+      Ws[i * VP + v] = fw[CV + (size_t)i * V + v];
+      KSs[i * VP + v] = fw[2 * CV + (size_t)i * V + v];
+    });
+    load(slot, t0, n, true);
+    // Q S^T and K dS1^T, 4 x 2 tiles of (i, v) a thread
+    x.par((C / 4) * (BV / 2), [&](int t) {
+      const int i0 = (t / (BV / 2)) * 4, v0 = (t % (BV / 2)) * 2;
+      float qs[4][2] = {}, kd[4][2] = {};
+#pragma unroll 2
       for (int c = 0; c < K; ++c) {
-        const float k0 = Ks[i0 * KP + c], k1 = Ks[(i0 + 1) * KP + c];
+        const float s0 = Ss[v0 * KP + c], s1 = Ss[(v0 + 1) * KP + c];
         const float d0 = dSs[v0 * KP + c], d1 = dSs[(v0 + 1) * KP + c];
-        acc[0][0] = fmaf(k0, d0, acc[0][0]);
-        acc[0][1] = fmaf(k0, d1, acc[0][1]);
-        acc[1][0] = fmaf(k1, d0, acc[1][0]);
-        acc[1][1] = fmaf(k1, d1, acc[1][1]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float qv = Qs[(i0 + a) * KP + c], kv = Ks[(i0 + a) * KP + c];
+          qs[a][0] = fmaf(qv, s0, qs[a][0]);
+          qs[a][1] = fmaf(qv, s1, qs[a][1]);
+          kd[a][0] = fmaf(kv, d0, kd[a][0]);
+          kd[a][1] = fmaf(kv, d1, kd[a][1]);
+        }
       }
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 2; ++b) dUs[(i0 + a) * VP + v0 + b] = acc[a][b];
+        for (int b = 0; b < 2; ++b) {
+          QSs[(i0 + a) * VP + v0 + b] = qs[a][b];
+          KdS[(i0 + a) * VP + v0 + b] = kd[a][b];
+        }
     });
-    // (4 x 4 tiles of (i, j): rows i0 .. i0 + 3, columns tj + 16 b)
+    x.sync();
+    // this block's share of dP = Ot U'^T (lower incl. the diagonal; 4 x 4 tiles of (i, j):
+    // rows i0 .. i0 + 3, columns tj + 16 b) and of dd_i = U'_i . (K dS1^T)_i;
+    // dU' = diag(d) K dS1^T + QG^T Ot (2 x 2 tiles of (i, v); row i0 + 1's term at j = i0 has
+    // a zero factor, QG being lower)
     x.par((C / 4) * 16, [&](int t) {
       const int i0 = (t / 16) * 4, tj = t % 16;
+      if (tj > i0 + 3) return;
       float acc[4][4] = {};
-      if (tj <= i0 + 3)
-        for (int v = 0; v < BV; ++v) {
-          float o[4], u[4];
+      for (int v = 0; v < BV; ++v) {
+        float o[4], u[4];
 #pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            o[a] = Os[(i0 + a) * VP + v];
-            u[a] = Us[(tj + 16 * a) * VP + v];
-          }
-#pragma unroll
-          for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(o[a], u[b], acc[a][b]);
+        for (int a = 0; a < 4; ++a) {
+          o[a] = Os[(i0 + a) * VP + v];
+          u[a] = Us[(tj + 16 * a) * VP + v];
         }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(o[a], u[b], acc[a][b]);
+      }
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const int i = i0 + a, j = tj + 16 * b;
-          dPm[i * CP + j] = j <= i ? acc[a][b] : 0.f;
+          if (j <= i) x.add(dPsum + i * C + j, acc[a][b]);
         }
     });
-    x.sync();
-    // dd_i = U'_i . (K dS1^T)_i;  dU' = diag(d) K dS1^T + P^T Ot
     x.par(C, [&](int i) {
       float acc = 0.f;
-      for (int v = 0; v < BV; ++v) acc = fmaf(Us[i * VP + v], dUs[i * VP + v], acc);
-      dd[i] = acc;
+      for (int v = 0; v < BV; ++v) acc = fmaf(Us[i * VP + v], KdS[i * VP + v], acc);
+      x.add(ddsum + i, acc);
     });
-    x.sync();
-    // (2 x 2 tiles of (i, v); row i0 + 1's term at j = i0 has a zero factor, P being lower)
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
       float acc[2][2];
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int b = 0; b < 2; ++b) acc[a][b] = dec[i0 + a] * dUs[(i0 + a) * VP + v0 + b];
+        for (int b = 0; b < 2; ++b) acc[a][b] = dec[i0 + a] * KdS[(i0 + a) * VP + v0 + b];
       for (int j = i0; j < C; ++j) {
-        const float m0 = QKm[j * CP + i0] * G(j, i0), m1 = QKm[j * CP + i0 + 1] * G(j, i0 + 1);
+        const float m0 = QGm[j * CP + i0], m1 = QGm[j * CP + i0 + 1];
         const float o0 = Os[j * VP + v0], o1 = Os[j * VP + v0 + 1];
         acc[0][0] = fmaf(m0, o0, acc[0][0]);
         acc[0][1] = fmaf(m0, o1, acc[0][1]);
@@ -439,8 +526,41 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         for (int b = 0; b < 2; ++b) dUs[(i0 + a) * VP + v0 + b] = acc[a][b];
     });
     x.sync();
-    // dV = T^T dU' (complete for these rows); dT = dU' (V - diag(b) K S^T)^T (lower)
-    // (dV in 2 x 2 tiles of (i, v), Z being lower; dT in 4 x 4 tiles of (i, j), columns tj + 16 b)
+    // this block's share of dT = dU' (V - diag(b) K S^T)^T (lower; 4 x 4 tiles, columns
+    // tj + 16 b); dV = diag(beta) Z^T dU' (complete for these rows; 2 x 2 tiles, Z being
+    // lower), written over V - diag(b) K S^T once dT has read it (after the barrier below)
+    x.par((C / 4) * 16, [&](int t) {
+      const int i0 = (t / 16) * 4, tj = t % 16;
+      if (tj > i0 + 3) return;
+      float acc[4][4] = {};
+      for (int v = 0; v < BV; ++v) {
+        float du[4], w[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          du[a] = dUs[(i0 + a) * VP + v];
+          w[a] = Ws[(tj + 16 * a) * VP + v];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(du[a], w[b], acc[a][b]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int i = i0 + a, j = tj + 16 * b;
+          if (j <= i) x.add(dTsum + i * C + j, acc[a][b]);
+        }
+    });
+    // b_last's gradient takes <S, dS1> over the block's rows: 64 partial sums
+    x.par(C, [&](int r) {
+      float acc = 0.f;
+      for (int idx = r; idx < BV * K; idx += C)
+        acc = fmaf(Ss[(idx / K) * KP + idx % K], dSs[(idx / K) * KP + idx % K], acc);
+      prt[r] = acc;
+    });
+    x.sync();
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
       float acc[2][2] = {};
@@ -458,150 +578,22 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const float r = acc[a][b] * bet[i];
-          dVs[i * VP + v0 + b] = r;
+          Ws[i * VP + v0 + b] = r;
           if (i < n) p.dv[((t0 + i) * Hv + h) * V + row0 + v0 + b] = r;
         }
       }
     });
-    x.par((C / 4) * 16, [&](int t) {
-      const int i0 = (t / 16) * 4, tj = t % 16;
-      float acc[4][4] = {};
-      if (tj <= i0 + 3)
-        for (int v = 0; v < BV; ++v) {
-          float du[4], w[4];
-#pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            du[a] = dUs[(i0 + a) * VP + v];
-            const int j = tj + 16 * a;
-            w[a] = Vs[j * VP + v] - bex[j] * KSs[j * VP + v];
-          }
-#pragma unroll
-          for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(du[a], w[b], acc[a][b]);
-        }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int i = i0 + a, j = tj + 16 * b;
-          dTm[i * CP + j] = j <= i ? acc[a][b] : 0.f;
-        }
-    });
     x.sync();
-    // b_last's gradient takes <S, dS1> over the block's rows: 64 partial sums (in dgm's
-    // place, free until dgamma) instead of one thread's 2048-term chain
-    x.par(C, [&](int r) {
-      float acc = 0.f;
-      for (int idx = r; idx < BV * K; idx += C) acc = fmaf(Ss[(idx / K) * KP + idx % K], dSs[(idx / K) * KP + idx % K], acc);
-      dgm[r] = acc;
-    });
-    x.sync();
-    // dbeta from T = Z diag(beta); db; Y = (dT diag(beta)) Z^T
+    // this block's share of db_j = Ot_j . (Q S^T)_j - dV_j . (K S^T)_j (+ <S, dS1> at the
+    // chunk's last row); the S and dS1 parts of dq and dk, 4 x 8 tiles of (i, c) a thread
+    // (columns c0 + b K / 8): dq = diag(b) Ot S, dk = diag(d) U' dS1 - diag(b) dV S
     x.par(C, [&](int j) {
-      float acc = 0.f;
-      for (int i = j; i < C; ++i) acc = fmaf(dTm[i * CP + j], Zm[i * CP + j], acc);
-      dbt[j] = acc;
       float b = 0.f;
-      for (int v = 0; v < BV; ++v)
-        b += Os[j * VP + v] * QSs[j * VP + v] - dVs[j * VP + v] * KSs[j * VP + v];
+      for (int v = 0; v < BV; ++v) b += Os[j * VP + v] * QSs[j * VP + v] - Ws[j * VP + v] * KSs[j * VP + v];
       if (j == C - 1)
-        for (int r = 0; r < C; ++r) b += dgm[r];
-      db[j] = b;
+        for (int r = 0; r < C; ++r) b += prt[r];
+      x.add(dbsum + j, b);
     });
-    // Y, 4 x 4 tiles of (i, j) a thread: dT is zero right of its diagonal and Z too, so the
-    // terms past min(i, j) add zeros
-    x.par((C / 4) * (C / 4), [&](int t) {
-      const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
-      const int mend = (i0 < j0 ? i0 : j0) + 4;
-      float acc[4][4] = {};
-      for (int m = 0; m < mend; ++m) {
-        const float bm = bet[m];
-        float tr[4], zr[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          tr[a] = dTm[(i0 + a) * CP + m] * bm;
-          zr[a] = Zm[(j0 + a) * CP + m];
-        }
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(tr[a], zr[b], acc[a][b]);
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) Ym[(i0 + a) * CP + j0 + b] = acc[a][b];
-    });
-    x.sync();
-    // dA = -Z^T Y, strictly lower (into dT's place), 4 x 4 tiles: Z^T's column i is zero
-    // above row i, so every row of a tile can start at the tile's first row
-    x.par((C / 4) * (C / 4), [&](int t) {
-      const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
-      float acc[4][4] = {};
-      if (j0 < i0 + 3)
-        for (int m = i0; m < C; ++m) {
-          float zr[4], yr[4];
-#pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            zr[a] = Zm[m * CP + i0 + a];
-            yr[a] = Ym[m * CP + j0 + a];
-          }
-#pragma unroll
-          for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(zr[a], yr[b], acc[a][b]);
-        }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) dTm[(i0 + a) * CP + j0 + b] = j0 + b < i0 + a ? -acc[a][b] : 0.f;
-    });
-    x.sync();
-    // dgamma (through Gamma in A and P, b and d) and the rest of dbeta
-    x.par(C, [&](int i) {
-      float rA = 0.f, cA = 0.f, rP = 0.f, cP = 0.f, bA = 0.f;
-      for (int j = 0; j < i; ++j) {
-        const float t = dTm[i * CP + j] * KKm[i * CP + j] * G(i, j);
-        bA += t;
-        rA = fmaf(bet[i], t, rA);
-      }
-      for (int m = i + 1; m < C; ++m) cA = fmaf(bet[m], dTm[m * CP + i] * KKm[m * CP + i] * G(m, i), cA);
-      for (int j = 0; j <= i; ++j) rP = fmaf(dPm[i * CP + j], QKm[i * CP + j] * G(i, j), rP);
-      for (int m = i; m < C; ++m) cP = fmaf(dPm[m * CP + i], QKm[m * CP + i] * G(m, i), cP);
-      dbt[i] += bA;
-      dgm[i] = rP - cP + rA - cA + db[i] * bex[i] - dd[i] * dec[i];
-    });
-    x.sync();
-    if (x.leader()) {
-      float sdd = 0.f;
-      for (int i = 0; i < C; ++i) sdd = fmaf(dd[i], dec[i], sdd);
-      dgm[C - 1] += sdd;
-      for (int i = C - 2; i >= 0; --i) dgm[i] += dgm[i + 1];  // dg = reverse cumsum of dgamma
-    }
-    x.sync();
-    x.par(C, [&](int i) {
-      if (i < n) {
-        x.add(p.dg + (t0 + i) * Hv + h, dgm[i]);
-        x.add(p.dbeta + (t0 + i) * Hv + h, dbt[i]);
-      }
-    });
-    // dKK = diag(beta) dA * Gamma (strictly lower)
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      dTm[i * CP + j] = j < i ? bet[i] * dTm[i * CP + j] * G(i, j) : 0.f;
-    });
-    x.sync();
-    // M1 = dP * Gamma (lower, in dP's place) and D = dKK + dKK^T (symmetric, zero diagonal,
-    // in Y's place, free since dA), so that dq and dk are tiled products
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      dPm[i * CP + j] = dPm[i * CP + j] * Gm[i * CP + j];
-      Ym[i * CP + j] = j < i ? dTm[i * CP + j] : (j > i ? dTm[j * CP + i] : 0.f);
-    });
-    x.sync();
-    // dq and dk of the chunk's tokens, 4 x 8 tiles of (i, c) a thread (columns c0 + b K / 8):
-    //   dq = diag(b) Ot S + M1 K,  dk = diag(d) U' dS1 - diag(b) dV S + M1^T Q + D K
     x.par((C / 4) * (K / 8), [&](int t) {
       const int i0 = (t / (K / 8)) * 4, c0 = t % (K / 8);
       float sq[4][8] = {}, sk[4][8] = {}, sv[4][8] = {};
@@ -611,7 +603,7 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         for (int a = 0; a < 4; ++a) {
           o[a] = Os[(i0 + a) * VP + v];
           u[a] = Us[(i0 + a) * VP + v];
-          w[a] = dVs[(i0 + a) * VP + v];
+          w[a] = Ws[(i0 + a) * VP + v];
         }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
@@ -627,48 +619,6 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
             sv[a][b] = fmaf(w[a], sr[b], sv[a][b]);
           }
       }
-      float dq[4][8], dk[4][8];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          dq[a][b] = bex[i0 + a] * sq[a][b];
-          dk[a][b] = dec[i0 + a] * sk[a][b] - bex[i0 + a] * sv[a][b];
-        }
-      // M1 is zero above the diagonal: row i needs j <= i, column i needs j >= i
-      for (int j = 0; j < i0 + 4; ++j) {
-        float m[4], kr[8];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) m[a] = dPm[(i0 + a) * CP + j];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int b = 0; b < 8; ++b) dq[a][b] = fmaf(m[a], kr[b], dq[a][b]);
-      }
-      for (int j = i0; j < C; ++j) {
-        float m[4], qr[8];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) m[a] = dPm[j * CP + i0 + a];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) qr[b] = Qs[j * KP + c0 + b * (K / 8)];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int b = 0; b < 8; ++b) dk[a][b] = fmaf(m[a], qr[b], dk[a][b]);
-      }
-      for (int j = 0; j < C; ++j) {
-        float m[4], kr[8];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) m[a] = Ym[(i0 + a) * CP + j];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int b = 0; b < 8; ++b) dk[a][b] = fmaf(m[a], kr[b], dk[a][b]);
-      }
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const int i = i0 + a;
@@ -676,34 +626,41 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
         const size_t off = ((size_t)(t0 + i) * p.Hqk + qh) * K + c0;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-          x.add(p.dqn + off + b * (K / 8), dq[a][b]);
-          x.add(p.dkn + off + b * (K / 8), dk[a][b]);
+          x.add(p.dqn + off + b * (K / 8), bex[i] * sq[a][b]);
+          x.add(p.dkn + off + b * (K / 8), dec[i] * sk[a][b] - bex[i] * sv[a][b]);
         }
       }
     });
     x.sync();
-    // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K, 2 x 4 tiles of (v, c) a thread
+    // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K, 4 x 4 tiles of (v, c) a thread
     // (columns c0 + b K / 4)
-    x.par((BV / 2) * (K / 4), [&](int t) {
-      const int v0 = (t / (K / 4)) * 2, c0 = t % (K / 4);
-      float acc[2][4];
+    x.par((BV / 4) * (K / 4), [&](int t) {
+      const int v0 = (t / (K / 4)) * 4, c0 = t % (K / 4);
+      float acc[4][4];
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = bex[C - 1] * dSs[(v0 + a) * KP + c0 + b * (K / 4)];
       for (int i = 0; i < C; ++i) {
         const float bi = bex[i];
-        const float o0 = Os[i * VP + v0], o1 = Os[i * VP + v0 + 1];
-        const float w0 = dVs[i * VP + v0], w1 = dVs[i * VP + v0 + 1];
+        float bo[4], bw[4], qv[4], kv[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          bo[a] = bi * Os[i * VP + v0 + a];
+          bw[a] = -bi * Ws[i * VP + v0 + a];
+        }
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const float qv = Qs[i * KP + c0 + b * (K / 4)], kv = Ks[i * KP + c0 + b * (K / 4)];
-          acc[0][b] = fmaf(bi, o0 * qv - w0 * kv, acc[0][b]);
-          acc[1][b] = fmaf(bi, o1 * qv - w1 * kv, acc[1][b]);
+          qv[b] = Qs[i * KP + c0 + b * (K / 4)];
+          kv[b] = Ks[i * KP + c0 + b * (K / 4)];
         }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(bw[a], kv[b], fmaf(bo[a], qv[b], acc[a][b]));
       }
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) dSs[(v0 + a) * KP + c0 + b * (K / 4)] = acc[a][b];
     });
@@ -714,6 +671,202 @@ GDN_BWD_FN void block(X &x, const Params &p, LD ld, float *sm, int tile, int h, 
       const int r = idx / K, c = idx % K;
       p.dh0[((size_t)s * Hv + h) * VK + (size_t)(row0 + r) * K + c] = dSs[r * KP + c];
     });
+}
+
+// ---- grad: the gradients linear in the summed dP, dT, dd and db of one (chunk, v-head)
+template <int KD, class X, class LD>
+GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot, int h) {
+  constexpr int K = KD, KP = KD + 1;
+  int64_t t0;
+  int n;
+  if (!slot_chunk(p, slot, t0, n)) return;
+  const int Hv = p.Hv, qh = h / (Hv / p.Hqk);
+  float *Ks = sm;              // [C][KP]  k (unit-norm when l2norm)
+  float *Qs = Ks + C * KP;     // [C][KP]  q
+  float *Zm = Qs + C * KP;     // [C][CP]  Z
+  float *KGm = Zm + C * CP;    // [C][CP]  KG
+  float *QGm = KGm + C * CP;   // [C][CP]  QG
+  float *dPm = QGm + C * CP;   // [C][CP]  dP, then M1 = dP * Gamma
+  float *dTm = dPm + C * CP;   // [C][CP]  dT, then dA, then dKK
+  float *Ym = dTm + C * CP;    // [C][CP]  Y = (dT diag(beta)) Z^T, then D = dKK + dKK^T
+  float *gam = Ym + C * CP;    // [C] gamma
+  float *bet = gam + C;        // [C] beta
+  float *bex = bet + C;        // [C] exp(gamma)
+  float *dec = bex + C;        // [C] exp(gamma_last - gamma)
+  float *dd = dec + C;         // [C] dL/dd
+  float *db = dd + C;          // [C] dL/db
+  float *dbt = db + C;         // [C] dL/dbeta
+  float *dgm = dbt + C;        // [C] dL/dgamma, then dg
+  const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
+  const float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
+  load_keys<K>(x, p, ld, Ks, Qs, t0, n, qh);
+  load_gates(x, p, gam, bet, t0, n, h);
+  x.par(C * C, [&](int idx) {
+    const int o = (idx / C) * CP + idx % C;
+    Zm[o] = pr[idx];
+    KGm[o] = pr[C * C + idx];
+    QGm[o] = pr[2 * C * C + idx];
+    dPm[o] = sums[idx];
+    dTm[o] = sums[C * C + idx];
+  });
+  x.par(C, [&](int i) {
+    dd[i] = sums[2 * C * C + i];
+    db[i] = sums[2 * C * C + C + i];
+  });
+  x.sync();
+  norm_and_cumsum<K>(x, p, Ks, Qs, gam);
+  x.sync();
+  x.par(C, [&](int i) {
+    bex[i] = expf(gam[i]);
+    dec[i] = expf(gam[C - 1] - gam[i]);
+  });
+  // dbeta from T = Z diag(beta): colsum(dT * Z)
+  x.par(C, [&](int j) {
+    float acc = 0.f;
+    for (int i = j; i < C; ++i) acc = fmaf(dTm[i * CP + j], Zm[i * CP + j], acc);
+    dbt[j] = acc;
+  });
+  // Y = (dT diag(beta)) Z^T, 4 x 4 tiles of (i, j) a thread: dT is zero right of its
+  // diagonal and Z too, so the terms past min(i, j) add zeros
+  x.par((C / 4) * (C / 4), [&](int t) {
+    const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
+    const int mend = (i0 < j0 ? i0 : j0) + 4;
+    float acc[4][4] = {};
+    for (int m = 0; m < mend; ++m) {
+      const float bm = bet[m];
+      float tr[4], zr[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        tr[a] = dTm[(i0 + a) * CP + m] * bm;
+        zr[a] = Zm[(j0 + a) * CP + m];
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(tr[a], zr[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) Ym[(i0 + a) * CP + j0 + b] = acc[a][b];
+  });
+  x.sync();
+  // dA = -Z^T Y, strictly lower (into dT's place), 4 x 4 tiles: Z^T's column i is zero
+  // above row i, so every row of a tile can start at the tile's first row
+  x.par((C / 4) * (C / 4), [&](int t) {
+    const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
+    float acc[4][4] = {};
+    if (j0 < i0 + 3)
+      for (int m = i0; m < C; ++m) {
+        float zr[4], yr[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          zr[a] = Zm[m * CP + i0 + a];
+          yr[a] = Ym[m * CP + j0 + a];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(zr[a], yr[b], acc[a][b]);
+      }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) dTm[(i0 + a) * CP + j0 + b] = j0 + b < i0 + a ? -acc[a][b] : 0.f;
+  });
+  x.sync();
+  // dgamma (through Gamma in A and P, b and d) and the rest of dbeta
+  x.par(C, [&](int i) {
+    float rA = 0.f, cA = 0.f, rP = 0.f, cP = 0.f, bA = 0.f;
+    for (int j = 0; j < i; ++j) {
+      const float t = dTm[i * CP + j] * KGm[i * CP + j];
+      bA += t;
+      rA = fmaf(bet[i], t, rA);
+    }
+    for (int m = i + 1; m < C; ++m) cA = fmaf(bet[m], dTm[m * CP + i] * KGm[m * CP + i], cA);
+    for (int j = 0; j <= i; ++j) rP = fmaf(dPm[i * CP + j], QGm[i * CP + j], rP);
+    for (int m = i; m < C; ++m) cP = fmaf(dPm[m * CP + i], QGm[m * CP + i], cP);
+    dbt[i] += bA;
+    dgm[i] = rP - cP + rA - cA + db[i] * bex[i] - dd[i] * dec[i];
+  });
+  x.sync();
+  if (x.leader()) {
+    float sdd = 0.f;
+    for (int i = 0; i < C; ++i) sdd = fmaf(dd[i], dec[i], sdd);
+    dgm[C - 1] += sdd;
+    for (int i = C - 2; i >= 0; --i) dgm[i] += dgm[i + 1];  // dg = reverse cumsum of dgamma
+  }
+  // dKK = diag(beta) dA * Gamma (strictly lower); M1 = dP * Gamma (lower)
+  x.par(C * C, [&](int idx) {
+    const int i = idx / C, j = idx % C;
+    const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
+    dTm[i * CP + j] = j < i ? bet[i] * dTm[i * CP + j] * gij : 0.f;
+    dPm[i * CP + j] *= gij;
+  });
+  x.sync();
+  x.par(C, [&](int i) {
+    if (i < n) {
+      p.dg[(t0 + i) * Hv + h] = dgm[i];
+      p.dbeta[(t0 + i) * Hv + h] = dbt[i];
+    }
+  });
+  // D = dKK + dKK^T (symmetric, zero diagonal, in Y's place, free since dA)
+  x.par(C * C, [&](int idx) {
+    const int i = idx / C, j = idx % C;
+    Ym[i * CP + j] = j < i ? dTm[i * CP + j] : (j > i ? dTm[j * CP + i] : 0.f);
+  });
+  x.sync();
+  // the C x C parts of dq and dk, 4 x 8 tiles of (i, c) a thread (columns c0 + b K / 8):
+  //   dq += M1 K,  dk += M1^T Q + D K
+  x.par((C / 4) * (K / 8), [&](int t) {
+    const int i0 = (t / (K / 8)) * 4, c0 = t % (K / 8);
+    float dq[4][8] = {}, dk[4][8] = {};
+    // M1 is zero above the diagonal: row i needs j <= i, column i needs j >= i
+    for (int j = 0; j < i0 + 4; ++j) {
+      float m[4], kr[8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) m[a] = dPm[(i0 + a) * CP + j];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) dq[a][b] = fmaf(m[a], kr[b], dq[a][b]);
+    }
+    for (int j = i0; j < C; ++j) {
+      float m[4], qr[8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) m[a] = dPm[j * CP + i0 + a];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) qr[b] = Qs[j * KP + c0 + b * (K / 8)];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) dk[a][b] = fmaf(m[a], qr[b], dk[a][b]);
+    }
+    for (int j = 0; j < C; ++j) {
+      float m[4], kr[8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) m[a] = Ym[(i0 + a) * CP + j];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) dk[a][b] = fmaf(m[a], kr[b], dk[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int i = i0 + a;
+      if (i >= n) continue;
+      const size_t off = ((size_t)(t0 + i) * p.Hqk + qh) * K + c0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        x.add(p.dqn + off + b * (K / 8), dq[a][b]);
+        x.add(p.dkn + off + b * (K / 8), dk[a][b]);
+      }
+    }
+  });
 }
 
 // Row r of q or k (token t = r / Hqk, head r % Hqk): the gradient of the unit-norm row taken

@@ -273,8 +273,9 @@ constexpr int kStageRows = 8, kStages = 4, kStagedCols = 1024;
 constexpr uint32_t kStagedSmem = kStages * kStageRows * kStagedCols * 2;
 constexpr uint32_t kConvSpin = 1u << 22;
 
-// The layer's gates, computed by the conv's first channel block over its run of tokens
-// (gdn_layer_fwd): the same values as gdn_gate_prep, one launch fewer.
+// The layer's gates, computed by the conv's blocks over their run of tokens, the elements of
+// a run spread over its channel blocks (gdn_layer_fwd): the same values as gdn_gate_prep, one
+// launch fewer.
 struct ConvGates {
   const __nv_bfloat16 *a, *b;  // [n_tok][Hv]
   const float *A_log, *dt_bias;
@@ -301,9 +302,9 @@ __global__ void __launch_bounds__(128, 3) conv1d_staged_kernel(const __nv_bfloat
   const int64_t t0 = (int64_t)blockIdx.x * run;
   if (t0 >= n_tok) return;
   const int64_t t1 = min(t0 + (int64_t)run, n_tok);
-  if (gates.g && blockIdx.y == 0) {
+  if (gates.g) {  // the run's gates, spread over its channel blocks
     const int64_t n_g = (t1 - t0) * gates.Hv;
-    for (int64_t e = tid; e < n_g; e += blockDim.x) {
+    for (int64_t e = (int64_t)blockIdx.y * blockDim.x + tid; e < n_g; e += (int64_t)gridDim.y * blockDim.x) {
       const int64_t i = t0 * gates.Hv + e;
       const int hh = (int)(i % gates.Hv);
       gdn_gates(__bfloat162float(gates.a[i]), __bfloat162float(gates.b[i]), gates.A_log[hh], gates.dt_bias[hh],

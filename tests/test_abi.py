@@ -175,8 +175,12 @@ def test_chunk_bwd_argument_errors_return_before_launch(lib):
     ws = P(0x20000)    # 256-byte aligned
     sh = _shape()
     need = lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(sh))
-    # states of (1 + 2) chunk slots x 4 heads x 128 x 128 fp32, two q/k accumulators of 128 x 2 x 128
-    assert need == 256 + 3 * 4 * 128 * 128 * 4 + 2 * 128 * 2 * 128 * 4
+    # over (1 + 2) chunk slots x 4 heads: states of 128 x 128 fp32, the forward sweep's three
+    # 64 x 128 fp32 tiles, prep's Z, KG and QG (3 x 64 x 64 fp32), the walk's sums dP, dT
+    # (2 x 64 x 64) and dd, db (2 x 64); then two q/k accumulators of 128 x 2 x 128
+    slots_h = 3 * 4
+    assert need == (256 + slots_h * 128 * 128 * 4 + slots_h * 3 * 64 * 128 * 4 + slots_h * 3 * 64 * 64 * 4
+                    + slots_h * (2 * 64 * 64 + 2 * 64) * 4 + 2 * 128 * 2 * 128 * 4)
     assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(K=96))) == 0
     assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(V=40))) == 0
     assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(V=48))) > 0

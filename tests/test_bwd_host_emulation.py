@@ -102,3 +102,15 @@ def test_host_body_rows_no_start_state(emu):
     ref = oracle.gdn_bwd(q, k, v, g, beta, do, None, None, B=2, scale=0.125, l2norm_qk=True)
     got = run_emu(emu, q, k, v, g, beta, None, None, 2, 0.125, True, do, None)
     _check(got, ref, "rows")
+
+
+def test_host_body_empty_sequences_and_three_row_tiles(emu):
+    """Empty sequences between and after two that end on and just past a chunk boundary
+    (64 and 65 tokens), two v-heads on each of two q/k heads, K = 64, and V = 48: three
+    16-row tiles a head (the walk takes 32 rows a block only when V allows)."""
+    lens = [64, 0, 0, 65, 0]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v, g, beta, h0, do, dhT = _case(83, int(cu[-1]), 2, 4, 64, 48, len(lens))
+    ref = oracle.gdn_bwd(q, k, v, g, beta, do, dhT, h0, cu_seqlens=cu, scale=0.3, l2norm_qk=True)
+    got = run_emu(emu, q, k, v, g, beta, h0, cu, 1, 0.3, True, do, dhT)
+    _check(got, ref, "empty sequences, V = 48")
