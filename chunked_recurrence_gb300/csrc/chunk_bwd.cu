@@ -238,8 +238,8 @@ extern "C" gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v,
   p.qs = qs; p.ks = ks; p.vs = vs;
   p.scale = scale;
   p.l2norm = (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0;
-  p.vec8 = aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && qs % 8 == 0 && ks % 8 == 0 && vs % 8 == 0 &&
-           (sh.dtype == GDN_BF16 || (qs % 4 == 0 && ks % 4 == 0 && vs % 4 == 0));
+  p.vec8 = aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(d_o, 16) && qs % 8 == 0 && ks % 8 == 0 &&
+           vs % 8 == 0 && (sh.dtype == GDN_BF16 || (qs % 4 == 0 && ks % 4 == 0 && vs % 4 == 0));
   uint8_t *cur = ws + kHeader;
   p.states = (float *)cur;
   p.fw = (float *)(cur += L.states);

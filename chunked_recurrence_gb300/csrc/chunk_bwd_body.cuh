@@ -74,7 +74,8 @@ struct Params {
   int64_t qs, ks, vs;
   float scale;
   int l2norm;
-  int vec8;         // q, k, v load as 8-element vectors (16-byte aligned rows and strides)
+  int vec8;         // q, k, v load as 8-element vectors and d_o as 4-element ones (16-byte aligned
+                    // rows and strides)
   // chunk slots: chunk c of sequence s is slot s + start_s / C + c (distinct for every chunk)
   float *states;    // [slot][Hv][V][K]: chunk-start states
   float *fw;        // [slot][Hv][3][C][V]: the forward sweep's U', V - diag(b) K S^T and K S^T
@@ -121,6 +122,44 @@ GDN_BWD_FN bool slot_chunk(const Params &p, int64_t slot, int64_t &t0, int &n) {
   return true;
 }
 
+// Four consecutive floats (16-byte aligned on the device).
+GDN_BWD_FN void ld4(const float *p, float *o) {
+#if defined(__CUDACC__)
+  const float4 v = *reinterpret_cast<const float4 *>(p);
+  o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+#else
+  for (int e = 0; e < 4; ++e) o[e] = p[e];
+#endif
+}
+
+// Groups of float4 an item for a copy of nf float4: enough that each thread has several
+// loads in flight before its first store (an item's loads all issue before its stores).
+GDN_BWD_HD constexpr int per_item(int nf) { return nf >= 1024 ? 4 : (nf >= 512 ? 2 : 1); }
+
+// dst[r][c] = scale * src[r * src_ld + c] for a ROWS x COLS fp32 block (COLS a multiple of 4,
+// src and src_ld 16-byte aligned); rows r >= n read as zero when n < ROWS.
+template <int ROWS, int COLS, class X>
+GDN_BWD_FN void copy_block(X &x, const float *src, size_t src_ld, float *dst, int dst_ld, int n = ROWS,
+                           float scale = 1.f) {
+  constexpr int NF = ROWS * COLS / 4, PER = per_item(NF), NI = NF / PER;
+  static_assert(NF % PER == 0, "whole items");
+  x.par(NI, [&](int t) {
+    float v[PER][4];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int f = t + u * NI, r = f / (COLS / 4), c = (f % (COLS / 4)) * 4;
+      if (r < n) ld4(src + r * src_ld + c, v[u]);
+      else v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int f = t + u * NI, r = f / (COLS / 4), c = (f % (COLS / 4)) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[r * dst_ld + c + e] = scale * v[u][e];
+    }
+  });
+}
+
 // Rows t0 .. t0 + n - 1 of k (and of q, when Qs is given) of q/k head qh into [C][K + 1]
 // tiles, zero past n.  The L2 norm follows in norm_and_cumsum, after a barrier.
 template <int K, class X, class LD>
@@ -128,19 +167,28 @@ GDN_BWD_FN void load_keys(X &x, const Params &p, LD ld, float *Ks, float *Qs, in
   constexpr int KP = K + 1;
   const bool with_q = Qs != nullptr;
   if (p.vec8) {
-    // 8 consecutive elements an item (one or two vector loads), so that each thread has
-    // several loads in flight instead of one
-    x.par(C * (K / 8), [&](int idx) {
-      const int r = idx / (K / 8), c = (idx % (K / 8)) * 8;
-      float kv[8] = {}, qv[8] = {};
-      if (r < n) {
-        ld.vec8(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c, kv);
-        if (with_q) ld.vec8(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c, qv);
+    // 8-element vectors, PER of them (of k and of q) an item, all loads before the stores
+    constexpr int NV = C * (K / 8), PER = per_item(NV), NI = NV / PER;
+    x.par(NI, [&](int t) {
+      float kv[PER][8], qv[PER][8];
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int idx = t + u * NI, r = idx / (K / 8), c = (idx % (K / 8)) * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kv[u][e] = qv[u][e] = 0.f;
+        if (r < n) {
+          ld.vec8(p.k, (t0 + r) * p.ks + (int64_t)qh * K + c, kv[u]);
+          if (with_q) ld.vec8(p.q, (t0 + r) * p.qs + (int64_t)qh * K + c, qv[u]);
+        }
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        Ks[r * KP + c + e] = kv[e];
-        if (with_q) Qs[r * KP + c + e] = qv[e];
+      for (int u = 0; u < PER; ++u) {
+        const int idx = t + u * NI, r = idx / (K / 8), c = (idx % (K / 8)) * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          Ks[r * KP + c + e] = kv[u][e];
+          if (with_q) Qs[r * KP + c + e] = qv[u][e];
+        }
       }
     });
   } else {
@@ -295,22 +343,15 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
   // the gates, and Z (and QG) from prep; then the norm, gamma, b and d.  Ends on a barrier.
   auto load = [&](int64_t slot, int64_t t0, int n, bool bwd) {
     load_keys<K>(x, p, ld, Ks, bwd ? Qs : nullptr, t0, n, qh);
-    if (p.vec8) {
+    if (p.vec8 && bwd) {
+      copy_block<C, BV>(x, p.dout + (t0 * Hv + h) * V + row0, (size_t)Hv * V, Os, VP, n, p.scale);
+    } else if (p.vec8) {
       x.par(C * (BV / 8), [&](int idx) {
         const int r = idx / (BV / 8), j = (idx % (BV / 8)) * 8;
         float vv[8] = {};
-        if (r < n) {
-          if (bwd) {
-            const float *src = p.dout + ((t0 + r) * Hv + h) * V + row0 + j;
+        if (r < n) ld.vec8(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j, vv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) vv[e] = p.scale * src[e];
-          } else {
-            ld.vec8(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j, vv);
-          }
-        }
-        float *dst = (bwd ? Os : Vs) + r * VP + j;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dst[e] = vv[e];
+        for (int e = 0; e < 8; ++e) Vs[r * VP + j + e] = vv[e];
       });
     } else {
       x.par(C * BV, [&](int idx) {
@@ -322,11 +363,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     }
     load_gates(x, p, gam, bet, t0, n, h);
     const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
-    x.par(C * C, [&](int idx) {
-      const int i = idx / C, j = idx % C;
-      Zm[i * CP + j] = pr[idx];
-      if (bwd) QGm[i * CP + j] = pr[2 * C * C + idx];
-    });
+    copy_block<C, C>(x, pr, C, Zm, CP);
+    if (bwd) copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
     x.sync();
     norm_and_cumsum<K>(x, p, Ks, bwd ? Qs : nullptr, gam);
     x.sync();
@@ -438,13 +476,10 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     const float *fw = fw_of(slot);
     float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
     float *dPsum = sums, *dTsum = sums + C * C, *ddsum = sums + 2 * C * C, *dbsum = ddsum + C;
-    x.par(BV * K, [&](int idx) { Ss[(idx / K) * KP + idx % K] = src[(idx / K) * (size_t)K + idx % K]; });
-    x.par(C * BV, [&](int idx) {
-      const int i = idx / BV, v = idx % BV;
-      Us[i * VP + v] = fw[(size_t)i * V + v];
-      Ws[i * VP + v] = fw[CV + (size_t)i * V + v];
-      KSs[i * VP + v] = fw[2 * CV + (size_t)i * V + v];
-    });
+    copy_block<BV, K>(x, src, K, Ss, KP);
+    copy_block<C, BV>(x, fw, V, Us, VP);
+    copy_block<C, BV>(x, fw + CV, V, Ws, VP);
+    copy_block<C, BV>(x, fw + 2 * CV, V, KSs, VP);
     load(slot, t0, n, true);
     // Q S^T and K dS1^T, 4 x 2 tiles of (i, v) a thread
     x.par((C / 4) * (BV / 2), [&](int t) {
@@ -701,14 +736,11 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   const float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
   load_keys<K>(x, p, ld, Ks, Qs, t0, n, qh);
   load_gates(x, p, gam, bet, t0, n, h);
-  x.par(C * C, [&](int idx) {
-    const int o = (idx / C) * CP + idx % C;
-    Zm[o] = pr[idx];
-    KGm[o] = pr[C * C + idx];
-    QGm[o] = pr[2 * C * C + idx];
-    dPm[o] = sums[idx];
-    dTm[o] = sums[C * C + idx];
-  });
+  copy_block<C, C>(x, pr, C, Zm, CP);
+  copy_block<C, C>(x, pr + C * C, C, KGm, CP);
+  copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
+  copy_block<C, C>(x, sums, C, dPm, CP);
+  copy_block<C, C>(x, sums + C * C, C, dTm, CP);
   x.par(C, [&](int i) {
     dd[i] = sums[2 * C * C + i];
     db[i] = sums[2 * C * C + C + i];
