@@ -225,12 +225,16 @@ gdn_status gdn_segment_summary(const void *k, const void *v, const float *g, con
  * d_o [tokens, Hv, V] and dh_T [n_seqs, Hv, V, K] (NULL: no loss on h_T) are fp32,
  * as are all outputs; q, k, v are of shape->dtype with the strides of gdn_shape.
  * K is 32, 64 or 128; V a multiple of 16 up to 256 (else GDN_ERR_UNSUPPORTED).
- * fp32 CUDA-core kernel: one block per (16 state rows, v-head, sequence) recomputes
- * its rows' chunk-start states, then walks the chunks backward.  The workspace
- * (gdn_chunk_bwd_workspace_bytes, 256-byte aligned) holds the status word, the
- * chunk-start states and the q/k gradient accumulators; a bad cu_seqlens range
- * sets GDN_ERR_BOUNDS in the status word (gdn_workspace_status).  dq, dk, dg and
- * dbeta are summed with atomic adds, so their last bits depend on the order. */
+ * fp32 CUDA-core kernels, all on the stream: a chunk-parallel prep of each chunk's
+ * state-independent matrices; a walk, one block per (32 or 16 state rows, v-head,
+ * sequence), that recomputes its rows' chunk-start states and then walks the chunks
+ * backward; a chunk-parallel pass for the gradients linear in the walk's per-chunk
+ * sums; the L2-norm backward.  The workspace (gdn_chunk_bwd_workspace_bytes,
+ * 256-byte aligned, caller-owned) holds the status word, the chunk-start states, the
+ * walk's per-chunk tiles, the prep matrices, the per-chunk sums and the q/k gradient
+ * accumulators; a bad cu_seqlens range sets GDN_ERR_BOUNDS in the status word
+ * (gdn_workspace_status).  dq, dk and the per-chunk sums are added atomically, so
+ * the last bits of dq, dk, dg and dbeta depend on the order. */
 size_t gdn_chunk_bwd_workspace_bytes(const gdn_shape *shape);
 gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          const float *h0, const int32_t *cu_seqlens, const gdn_shape *shape, float scale,
