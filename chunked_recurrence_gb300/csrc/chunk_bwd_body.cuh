@@ -160,6 +160,59 @@ GDN_BWD_FN void copy_block(X &x, const float *src, size_t src_ld, float *dst, in
   });
 }
 
+// One item's share of a ROWS x COLS fp32 block copy: float4 pieces t, t + NI, ... of it.
+// load() issues the item's loads and store() writes them, so that an item can hold the
+// loads of several fills in flight before its first store.  Rows r >= n read as zero.
+template <int ROWS, int COLS, int NI>
+struct Fill4 {
+  static constexpr int NF = ROWS * COLS / 4, PER = (NF + NI - 1) / NI;
+  float v[PER][4];
+  GDN_BWD_FN void load(int t, const float *src, size_t src_ld, int n) {
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int f = t + u * NI, r = f / (COLS / 4), c = (f % (COLS / 4)) * 4;
+      if (f < NF && r < n) ld4(src + r * src_ld + c, v[u]);
+      else v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.f;
+    }
+  }
+  GDN_BWD_FN void store(int t, float *dst, int dst_ld, float scale = 1.f) const {
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int f = t + u * NI, r = f / (COLS / 4), c = (f % (COLS / 4)) * 4;
+      if (f < NF)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[r * dst_ld + c + e] = scale * v[u][e];
+    }
+  }
+};
+
+// The same for rows of q, k or v read as 8-element vectors through LD::vec8: element
+// (r, c) of the block is src[base + r * row_stride + c].
+template <int ROWS, int COLS, int NI>
+struct Fill8 {
+  static constexpr int NV = ROWS * COLS / 8, PER = (NV + NI - 1) / NI;
+  float v[PER][8];
+  template <class LD>
+  GDN_BWD_FN void load(LD ld, int t, const void *src, int64_t base, int64_t row_stride, int n) {
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int f = t + u * NI, r = f / (COLS / 8), c = (f % (COLS / 8)) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[u][e] = 0.f;
+      if (f < NV && r < n) ld.vec8(src, base + r * row_stride + c, v[u]);
+    }
+  }
+  GDN_BWD_FN void store(int t, float *dst, int dst_ld) const {
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int f = t + u * NI, r = f / (COLS / 8), c = (f % (COLS / 8)) * 8;
+      if (f < NV)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dst[r * dst_ld + c + e] = v[u][e];
+    }
+  }
+};
+
 // Rows t0 .. t0 + n - 1 of k (and of q, when Qs is given) of q/k head qh into [C][K + 1]
 // tiles, zero past n.  The L2 norm follows in norm_and_cumsum, after a barrier.
 template <int K, class X, class LD>
@@ -340,31 +393,85 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
   auto fw_of = [&](int64_t slot) { return p.fw + ((size_t)slot * Hv + h) * 3 * CV + row0; };
 
   // the chunk's inputs: k (and q), the block's v columns (forward) or scale * dO (backward),
-  // the gates, and Z (and QG) from prep; then the norm, gamma, b and d.  Ends on a barrier.
+  // the gates, Z (and QG) from prep, and in the backward sweep the block's chunk-start
+  // state and the forward sweep's tiles; then the norm, gamma, b and d.  Ends on a
+  // barrier.  With vector loads every fill of a phase is in flight at once (two phases
+  // backward, one forward).
   auto load = [&](int64_t slot, int64_t t0, int n, bool bwd) {
-    load_keys<K>(x, p, ld, Ks, bwd ? Qs : nullptr, t0, n, qh);
+    const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
+    const float *st = p.states + ((size_t)slot * Hv + h) * VK + (size_t)row0 * K;
+    const float *fw = fw_of(slot);
+    const int64_t kb = t0 * p.ks + (int64_t)qh * K, qb = t0 * p.qs + (int64_t)qh * K;
+    constexpr int NI = 256;
     if (p.vec8 && bwd) {
-      copy_block<C, BV>(x, p.dout + (t0 * Hv + h) * V + row0, (size_t)Hv * V, Os, VP, n, p.scale);
+      x.par(NI, [&](int t) {
+        Fill4<BV, K, NI> fs;
+        Fill4<C, BV, NI> fu, fwv, fks, fo;
+        Fill4<C, C, NI> fz, fq;
+        fs.load(t, st, K, BV);
+        fu.load(t, fw, V, C);
+        fwv.load(t, fw + CV, V, C);
+        fks.load(t, fw + 2 * CV, V, C);
+        fo.load(t, p.dout + (t0 * Hv + h) * V + row0, (size_t)Hv * V, n);
+        fz.load(t, pr, C, C);
+        fq.load(t, pr + 2 * C * C, C, C);
+        fs.store(t, Ss, KP);
+        fu.store(t, Us, VP);
+        fwv.store(t, Ws, VP);
+        fks.store(t, KSs, VP);
+        fo.store(t, Os, VP, p.scale);
+        fz.store(t, Zm, CP);
+        fq.store(t, QGm, CP);
+      });
+      x.par(NI, [&](int t) {
+        Fill8<C, K, NI> fk, fq;
+        fk.load(ld, t, p.k, kb, p.ks, n);
+        fq.load(ld, t, p.q, qb, p.qs, n);
+        const bool gi = t < C && t < n;
+        const float gv = gi ? p.g[(t0 + t) * Hv + h] : 0.f, bv = gi ? p.beta[(t0 + t) * Hv + h] : 0.f;
+        fk.store(t, Ks, KP);
+        fq.store(t, Qs, KP);
+        if (t < C) {
+          gam[t] = gv;
+          bet[t] = bv;
+        }
+      });
     } else if (p.vec8) {
-      x.par(C * (BV / 8), [&](int idx) {
-        const int r = idx / (BV / 8), j = (idx % (BV / 8)) * 8;
-        float vv[8] = {};
-        if (r < n) ld.vec8(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j, vv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) Vs[r * VP + j + e] = vv[e];
+      x.par(NI, [&](int t) {
+        Fill8<C, K, NI> fk;
+        Fill8<C, BV, NI> fv;
+        Fill4<C, C, NI> fz;
+        fk.load(ld, t, p.k, kb, p.ks, n);
+        fv.load(ld, t, p.v, t0 * p.vs + (int64_t)h * V + row0, p.vs, n);
+        fz.load(t, pr, C, C);
+        const bool gi = t < C && t < n;
+        const float gv = gi ? p.g[(t0 + t) * Hv + h] : 0.f, bv = gi ? p.beta[(t0 + t) * Hv + h] : 0.f;
+        fk.store(t, Ks, KP);
+        fv.store(t, Vs, VP);
+        fz.store(t, Zm, CP);
+        if (t < C) {
+          gam[t] = gv;
+          bet[t] = bv;
+        }
       });
     } else {
+      load_keys<K>(x, p, ld, Ks, bwd ? Qs : nullptr, t0, n, qh);
       x.par(C * BV, [&](int idx) {
         const int r = idx / BV, j = idx % BV;
         const bool in = r < n;
         if (bwd) Os[r * VP + j] = in ? p.scale * p.dout[((t0 + r) * Hv + h) * V + row0 + j] : 0.f;
         else Vs[r * VP + j] = in ? ld(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j) : 0.f;
       });
+      load_gates(x, p, gam, bet, t0, n, h);
+      copy_block<C, C>(x, pr, C, Zm, CP);
+      if (bwd) {
+        copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
+        copy_block<BV, K>(x, st, K, Ss, KP);
+        copy_block<C, BV>(x, fw, V, Us, VP);
+        copy_block<C, BV>(x, fw + CV, V, Ws, VP);
+        copy_block<C, BV>(x, fw + 2 * CV, V, KSs, VP);
+      }
     }
-    load_gates(x, p, gam, bet, t0, n, h);
-    const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
-    copy_block<C, C>(x, pr, C, Zm, CP);
-    if (bwd) copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
     x.sync();
     norm_and_cumsum<K>(x, p, Ks, bwd ? Qs : nullptr, gam);
     x.sync();
@@ -472,14 +579,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
   for (int ci = n_chunks - 1; ci >= 0; --ci) {
     const int64_t t0 = start + (int64_t)ci * C, slot = slot0 + ci;
     const int n = (int)(end - t0 < C ? end - t0 : C);
-    const float *src = p.states + ((size_t)slot * Hv + h) * VK + (size_t)row0 * K;
-    const float *fw = fw_of(slot);
     float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
     float *dPsum = sums, *dTsum = sums + C * C, *ddsum = sums + 2 * C * C, *dbsum = ddsum + C;
-    copy_block<BV, K>(x, src, K, Ss, KP);
-    copy_block<C, BV>(x, fw, V, Us, VP);
-    copy_block<C, BV>(x, fw + CV, V, Ws, VP);
-    copy_block<C, BV>(x, fw + 2 * CV, V, KSs, VP);
     load(slot, t0, n, true);
     // Q S^T and K dS1^T, 4 x 2 tiles of (i, v) a thread
     x.par((C / 4) * (BV / 2), [&](int t) {
@@ -734,17 +835,52 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   float *dgm = dbt + C;        // [C] dL/dgamma, then dg
   const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
   const float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
-  load_keys<K>(x, p, ld, Ks, Qs, t0, n, qh);
-  load_gates(x, p, gam, bet, t0, n, h);
-  copy_block<C, C>(x, pr, C, Zm, CP);
-  copy_block<C, C>(x, pr + C * C, C, KGm, CP);
-  copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
-  copy_block<C, C>(x, sums, C, dPm, CP);
-  copy_block<C, C>(x, sums + C * C, C, dTm, CP);
-  x.par(C, [&](int i) {
-    dd[i] = sums[2 * C * C + i];
-    db[i] = sums[2 * C * C + C + i];
-  });
+  if (p.vec8) {  // every fill of a phase in flight at once
+    constexpr int NI = 256;
+    x.par(NI, [&](int t) {
+      Fill4<C, C, NI> fz, fkg, fqg, fdp, fdt;
+      fz.load(t, pr, C, C);
+      fkg.load(t, pr + C * C, C, C);
+      fqg.load(t, pr + 2 * C * C, C, C);
+      fdp.load(t, sums, C, C);
+      fdt.load(t, sums + C * C, C, C);
+      const float dv = t < C ? sums[2 * C * C + t] : 0.f, bv = t < C ? sums[2 * C * C + C + t] : 0.f;
+      fz.store(t, Zm, CP);
+      fkg.store(t, KGm, CP);
+      fqg.store(t, QGm, CP);
+      fdp.store(t, dPm, CP);
+      fdt.store(t, dTm, CP);
+      if (t < C) {
+        dd[t] = dv;
+        db[t] = bv;
+      }
+    });
+    x.par(NI, [&](int t) {
+      Fill8<C, K, NI> fk, fq;
+      fk.load(ld, t, p.k, t0 * p.ks + (int64_t)qh * K, p.ks, n);
+      fq.load(ld, t, p.q, t0 * p.qs + (int64_t)qh * K, p.qs, n);
+      const bool gi = t < C && t < n;
+      const float gv = gi ? p.g[(t0 + t) * Hv + h] : 0.f, bv = gi ? p.beta[(t0 + t) * Hv + h] : 0.f;
+      fk.store(t, Ks, KP);
+      fq.store(t, Qs, KP);
+      if (t < C) {
+        gam[t] = gv;
+        bet[t] = bv;
+      }
+    });
+  } else {
+    load_keys<K>(x, p, ld, Ks, Qs, t0, n, qh);
+    load_gates(x, p, gam, bet, t0, n, h);
+    copy_block<C, C>(x, pr, C, Zm, CP);
+    copy_block<C, C>(x, pr + C * C, C, KGm, CP);
+    copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
+    copy_block<C, C>(x, sums, C, dPm, CP);
+    copy_block<C, C>(x, sums + C * C, C, dTm, CP);
+    x.par(C, [&](int i) {
+      dd[i] = sums[2 * C * C + i];
+      db[i] = sums[2 * C * C + C + i];
+    });
+  }
   x.sync();
   norm_and_cumsum<K>(x, p, Ks, Qs, gam);
   x.sync();

@@ -50,6 +50,11 @@ void run_all(gdn_bwd::Params &p, int n_seqs, int64_t n_slots) {
     for (int h = 0; h < p.Hv; ++h) gdn_bwd::grad_block<K>(x, p, HostLoad{}, sm.data(), slot, h);
 }
 
+// -1: vector loads where the shapes allow them (as the library decides for aligned inputs);
+// 0: the element-wise loads the library takes for unaligned inputs
+static int g_vec8 = -1;
+extern "C" void emu_set_vec8(int mode) { g_vec8 = mode; }
+
 extern "C" int emu_chunk_bwd(const float *q, const float *k, const float *v, const float *g, const float *beta,
                              const float *h0, const int32_t *cu, int n_seqs, int64_t row_T, int64_t n_tok, int Hqk,
                              int Hv, int K, int V, float scale, int l2norm, const float *dout, const float *dhT,
@@ -70,7 +75,7 @@ extern "C" int emu_chunk_bwd(const float *q, const float *k, const float *v, con
   p.Hqk = Hqk; p.Hv = Hv; p.K = K; p.V = V;
   p.qs = (int64_t)Hqk * K; p.ks = (int64_t)Hqk * K; p.vs = (int64_t)Hv * V;
   p.scale = scale; p.l2norm = l2norm;
-  p.vec8 = (K % 8 == 0 && V % 8 == 0) ? 1 : 0;
+  p.vec8 = (g_vec8 != 0 && K % 8 == 0 && V % 8 == 0) ? 1 : 0;
   p.states = states.data(); p.fw = fw.data(); p.prep = prep.data(); p.sums = sums.data();
   p.dqn = dqn.data(); p.dkn = dkn.data();
   p.dv = dv; p.dg = dg; p.dbeta = dbeta; p.dh0 = dh0; p.status = &status;

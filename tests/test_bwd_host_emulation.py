@@ -31,6 +31,7 @@ def emu(tmp_path_factory):
     lib.emu_chunk_bwd.argtypes = [d, d, d, d, d, d, d, i32, i64, i64, i32, i32, i32, i32, f32, i32, d, d,
                                   d, d, d, d, d, d]
     lib.emu_chunk_bwd.restype = i32
+    lib.emu_set_vec8.argtypes = [i32]
     return lib
 
 
@@ -114,3 +115,18 @@ def test_host_body_empty_sequences_and_three_row_tiles(emu):
     ref = oracle.gdn_bwd(q, k, v, g, beta, do, dhT, h0, cu_seqlens=cu, scale=0.3, l2norm_qk=True)
     got = run_emu(emu, q, k, v, g, beta, h0, cu, 1, 0.3, True, do, dhT)
     _check(got, ref, "empty sequences, V = 48")
+
+
+def test_host_body_elementwise_loads(emu):
+    """The element-wise load path (what the library takes when q, k, v or d_o are not 16-byte
+    aligned) on the varlen case: the same gradients as the vector path."""
+    lens = [1, 40, 150]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v, g, beta, h0, do, dhT = _case(84, int(cu[-1]), 1, 2, 32, 32, len(lens))
+    ref = oracle.gdn_bwd(q, k, v, g, beta, do, dhT, h0, cu_seqlens=cu, scale=0.4, l2norm_qk=True)
+    emu.emu_set_vec8(0)
+    try:
+        got = run_emu(emu, q, k, v, g, beta, h0, cu, 1, 0.4, True, do, dhT)
+    finally:
+        emu.emu_set_vec8(-1)
+    _check(got, ref, "element-wise loads")
