@@ -88,7 +88,7 @@ struct OpParams {
   const float *A_log, *dt_bias;       // [Hv]
   __nv_bfloat16 *qc, *kc;             // conv'd q, k [n_tok][Hqk][128]
   unsigned long long *claim;          // front end: item-group counter, zero at launch
-  uint32_t spin;                      // polls before a wait gives up (0 under GDN_FLAG_TEST_NO_WAIT)
+  int quit;                           // GDN_FLAG_TEST_NO_WAIT: a wait that misses its first poll gives up
 };
 
 constexpr int kXP = C + 4;  // fp32 row of A, padded (rows stay 16-byte aligned)
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(128, 4)
     }
   }
   {
-    const bool ok = tid != 0 || mbar_wait(&ld_bar, ldp & 1, p.spin);
+    const bool ok = tid != 0 || mbar_wait_q(&ld_bar, ldp & 1, kSpin, p.quit != 0);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
       (void)mbar_wait(&ld_bar, ldp & 1, kSpin);  // the copies land before shared memory is released
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(128, 4)
     }
   }
   {
-    const bool ok = tid != 0 || mbar_wait(&bar, mp & 1, p.spin);
+    const bool ok = tid != 0 || mbar_wait_q(&bar, mp & 1, kSpin, p.quit != 0);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
       (void)mbar_wait(&bar, mp & 1, kSpin);  // an MMA still in flight lands before TMEM is freed
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(128, 4)
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     if (op_late_v(V) && pass == 1) {
-      const bool ok = tid != 0 || mbar_wait(&ld_bar, ldp & 1, p.spin);
+      const bool ok = tid != 0 || mbar_wait_q(&ld_bar, ldp & 1, kSpin, p.quit != 0);
       if (__syncthreads_or(!ok)) {
         if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
         (void)mbar_wait(&ld_bar, ldp & 1, kSpin);  // the copy lands before shared memory is released
@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(128, 4)
     }
     {
       const uint32_t par = mp & 1;
-      bool ok = tid != 0 || mbar_wait(&bar, par, p.spin);
+      bool ok = tid != 0 || mbar_wait_q(&bar, par, kSpin, p.quit != 0);
       if (op_late_v(V) && pass == 0 && tid == 0 && ok) {
         // W has read the k rows: v goes there while -W drains
         const int32_t tt = (int32_t)t0;
@@ -655,7 +655,8 @@ struct ScanParams {
   int norm;
   const __nv_bfloat16 *z, *nw;  // z [n_tok][Hv][V]; the norm weight [V] or null (ones)
   float eps;
-  uint32_t spin;  // polls before a wait gives up (0 under GDN_FLAG_TEST_NO_WAIT); drains keep kSpin
+  int quit;  // GDN_FLAG_TEST_NO_WAIT: the abort flag starts set, so waits give up after 32 polls;
+             // drains keep the full bound
 };
 
 // warps 0-7: state path; 8, 9, 12, 13: outputs; 10: copies; 11: MMAs
@@ -753,7 +754,7 @@ __global__ void __launch_bounds__(NTS, 1)
       mbar_init(&sh.nbar[0], 1);
       mbar_init(&sh.nbar[1], 1);
     }
-    sh.abort = 0;
+    sh.abort = p.quit ? 1 : 0;  // test mode: every wait gives up after 32 polls
     sh.mma_bar = nullptr;
     sh.mma_par = 0;
     fence_mbar_init();
@@ -781,7 +782,7 @@ __global__ void __launch_bounds__(NTS, 1)
       tma_prefetch_desc(&tm_k);
       for (int ci = 0; ci < n_chunks; ++ci) {
         const int st = ci % kStages;
-        if (ci >= kStages && !mbar_wait_spin(&sh.empty[st], ((ci - kStages) / kStages) & 1, p.spin, abort_flag)) {
+        if (ci >= kStages && !mbar_wait_spin(&sh.empty[st], ((ci - kStages) / kStages) & 1, kSpin, abort_flag)) {
           fail();
           break;
         }
@@ -820,14 +821,14 @@ __global__ void __launch_bounds__(NTS, 1)
       int outd_seen = 0;  // outputs known to be done; out_done phases are consumed in order
       auto outputs_done = [&](int need) {
         while (outd_seen < need) {
-          if (!mbar_wait_spin(&sh.outd, outd_seen & 1, p.spin, abort_flag)) return false;
+          if (!mbar_wait_spin(&sh.outd, outd_seen & 1, kSpin, abort_flag)) return false;
           ++outd_seen;
         }
         return true;
       };
       // [P; -] [U'_hi | U'_lo] of chunk cj: the output path, one chunk behind the state path
       auto issue_b2 = [&](int cj) {
-        if (!mbar_wait_spin(&sh.epa2, cj & 1, p.spin, abort_flag) || !outputs_done(cj)) return false;
+        if (!mbar_wait_spin(&sh.epa2, cj & 1, kSpin, abort_flag) || !outputs_done(cj)) return false;
         tc_fence_after();
         const uint64_t sj = (uint64_t)((cj % kStages) * kStage) >> 4;
 #pragma unroll
@@ -843,8 +844,8 @@ __global__ void __launch_bounds__(NTS, 1)
         const int st = ci % kStages;
         // chunk ci's operands, the state after chunk ci-1, and the output of chunk ci-3
         // (whose accumulator columns [q; -W] S^T reuses) done
-        if (!mbar_wait_spin(&sh.full[st], (ci / kStages) & 1, p.spin, abort_flag) ||
-            !mbar_wait_spin(&sh.epb, ci & 1, p.spin, abort_flag) || (!summary && !outputs_done(ci - 2))) {
+        if (!mbar_wait_spin(&sh.full[st], (ci / kStages) & 1, kSpin, abort_flag) ||
+            !mbar_wait_spin(&sh.epb, ci & 1, kSpin, abort_flag) || (!summary && !outputs_done(ci - 2))) {
           mok = false;
           break;
         }
@@ -858,7 +859,7 @@ __global__ void __launch_bounds__(NTS, 1)
         umma_commit(&sh.ga);
         sh.mma_bar = &sh.ga;
         sh.mma_par = ci & 1;
-        if ((!summary && ci > 0 && !issue_b2(ci - 1)) || !mbar_wait_spin(&sh.epa, ci & 1, p.spin, abort_flag)) {
+        if ((!summary && ci > 0 && !issue_b2(ci - 1)) || !mbar_wait_spin(&sh.epa, ci & 1, kSpin, abort_flag)) {
           mok = false;
           break;
         }
@@ -905,7 +906,7 @@ __global__ void __launch_bounds__(NTS, 1)
       const int st = ci % kStages;
       const uint8_t *sg = sm + st * kStage;
       const float *vec = reinterpret_cast<const float *>(sg + ST_VEC);
-      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, p.spin, abort_flag)) {
+      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, kSpin, abort_flag)) {
         ok = false;
         break;
       }
@@ -913,7 +914,7 @@ __global__ void __launch_bounds__(NTS, 1)
       float x[16];
       if (quarter >= 2) {
         // ---- U' = U - W S^T for tokens i: diag(d/|k|) U' hi/lo for the state path
-        if (!warp_wait(&sh.ga, ci & 1, p.spin, abort_flag)) {
+        if (!warp_wait(&sh.ga, ci & 1, kSpin, abort_flag)) {
           ok = false;
           break;
         }
@@ -949,7 +950,7 @@ __global__ void __launch_bounds__(NTS, 1)
         warp_arrive(&sh.epa);
       }
       // ---- S <- b_last S + dS (fp32), and its bf16 copy for the next chunk's MMAs
-      if (!warp_wait(&sh.b1, ci & 1, p.spin, abort_flag)) {
+      if (!warp_wait(&sh.b1, ci & 1, kSpin, abort_flag)) {
         ok = false;
         break;
       }
@@ -969,7 +970,7 @@ __global__ void __launch_bounds__(NTS, 1)
       }
       if (quarter >= 2 && !summary) {
         // ---- U' hi/lo for the output path, once the previous chunk's output has read its tile
-        if (ci > 0 && !warp_wait(&sh.outd, (ci - 1) & 1, p.spin, abort_flag)) {
+        if (ci > 0 && !warp_wait(&sh.outd, (ci - 1) & 1, kSpin, abort_flag)) {
           ok = false;
           break;
         }
@@ -1028,7 +1029,7 @@ __global__ void __launch_bounds__(NTS, 1)
       const int st = ci % kStages;
       const uint8_t *sg = sm + st * kStage;
       const float *vec = reinterpret_cast<const float *>(sg + ST_VEC);
-      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, p.spin, abort_flag)) {
+      if (!warp_wait(&sh.full[st], (ci / kStages) & 1, kSpin, abort_flag)) {
         ok = false;
         break;
       }
@@ -1037,7 +1038,7 @@ __global__ void __launch_bounds__(NTS, 1)
         warp_arrive(&sh.empty[st]);
         continue;
       }
-      if (!warp_wait(&sh.b2, ci & 1, p.spin, abort_flag)) {
+      if (!warp_wait(&sh.b2, ci & 1, kSpin, abort_flag)) {
         ok = false;
         break;
       }
@@ -1088,7 +1089,7 @@ __global__ void __launch_bounds__(NTS, 1)
         // threads a block, 4 bytes each (one arrival, by warp 8's lane 0)
         if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&sh.nbar[slot], 128u * 4u * n_ranks);
         for (uint32_t r = 0; r < n_ranks; ++r) st_async_cluster_f32(mapa_shared(np_mine, r), ss, mapa_shared(bar_mine, r));
-        const bool got = mbar_wait_cluster_spin(&sh.nbar[slot], (uint32_t)(ci >> 1) & 1, p.spin, abort_flag);
+        const bool got = mbar_wait_cluster_spin(&sh.nbar[slot], (uint32_t)(ci >> 1) & 1, kSpin, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -1270,7 +1271,7 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
   op.rec_bytes = rec_bytes(sh.V);
   op.status = status;
   op.claim = reinterpret_cast<unsigned long long *>((uint8_t *)workspace + 8);  // header bytes 8-15
-  op.spin = (flags & GDN_FLAG_TEST_NO_WAIT) ? 0u : kSpin;
+  op.quit = (flags & GDN_FLAG_TEST_NO_WAIT) ? 1 : 0;
   CUtensorMap mq, mk, mv;
   if (fr) {
     const __nv_bfloat16 *x = (const __nv_bfloat16 *)fr->x;
@@ -1328,7 +1329,7 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
   sp.hT = h_T;
   sp.status = status;
   sp.summary = summary ? 1 : 0;
-  sp.spin = op.spin;
+  sp.quit = op.quit;
   sp.M = M;
   sp.S_local = S_local;
   if (cudaFuncSetAttribute(chunk_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -62,6 +62,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   return false;
 }
 
+// Like mbar_wait (call it with a compile-time max_iters), but a wait that misses its first
+// poll gives up at once when `quit` is set (a test mode).  The flag is read only on that
+// slow path, so a wait whose phase has completed costs what mbar_wait does.
+__device__ __forceinline__ bool mbar_wait_q(uint64_t *bar, uint32_t parity, uint32_t max_iters, bool quit) {
+  for (uint32_t i = 0; i < max_iters; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (quit) return false;
+    if (i > 64) __nanosleep(32);
+  }
+  return false;
+}
+
 // Like mbar_wait, but also gives up as soon as *abort (set by another warp
 // that hit a failure) becomes non-zero.
 __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t parity, uint32_t max_iters,

@@ -57,10 +57,11 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_FLAG_SIMT 2u       /* force the fp32 CUDA-core kernel (the tensor-core kernel is the default for bf16) */
 #define GDN_FLAG_O_F32 4u      /* write o as fp32 whatever the input dtype (default: o has the input dtype) */
 #define GDN_FLAG_FUSED 8u      /* gdn_chunk_fwd (bf16, K = V = 128): the fused persistent kernel instead of the two-kernel path */
-#define GDN_FLAG_TEST_NO_WAIT 16u /* test only: every bounded wait of the tensor-core split kernels (or, with
-                                   * GDN_FLAG_FUSED, the fused kernel) gives up at its first check, so the call
-                                   * ends with GDN_ERR_TIMEOUT in the status word; only the waits that let copies
-                                   * and MMAs in flight land before memory is released keep their bound */
+#define GDN_FLAG_TEST_NO_WAIT 16u /* test only: every bounded wait of the tensor-core split kernels gives up
+                                   * at its first missed poll (the state scan's after 32 polls), and with
+                                   * GDN_FLAG_FUSED every wait of the fused kernel at its first check, so the
+                                   * call ends with GDN_ERR_TIMEOUT in the status word; only the waits that let
+                                   * copies and MMAs in flight land before memory is released keep their bound */
 #define GDN_FLAG_LAYER_FRONT 32u /* gdn_layer_fwd: the fused front end (conv and gates inside the chunk operand
                                   * kernel) instead of separate launches, where the shape allows it */
 #define GDN_FLAG_LAYER_NORM_EPILOGUE 64u /* gdn_layer_fwd with z: the gated norm in the state scan's output
