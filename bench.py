@@ -161,8 +161,8 @@ class ClockSampler:
 
 
 def _kernel_sha() -> str:
-    """Hash of the sources the layer call's kernels compile from (gate prep, the conv, the
-    chunk operand and scan kernels, and the host code that launches them): a stored ncu
+    """Hash of the sources the layer call's kernels compile from (the conv with the gates,
+    the chunk operand and scan kernels, and the host code that launches them): a stored ncu
     traffic figure is valid for these only."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_recurrence_gb300", "csrc")
@@ -176,7 +176,7 @@ def _kernel_sha() -> str:
 
 def _stored_traffic(sha: str, key: str = "traffic_bytes_per_launch"):
     """DRAM read + write bytes of one call from the committed ncu summary of the layer step,
-    if it was taken on the current kernel sources (else None).  key: the layer call's four
+    if it was taken on the current kernel sources (else None).  key: the layer call's three
     kernels (traffic_bytes_per_launch) or the chunk pair alone (chunk_traffic_bytes_per_launch)."""
     path = os.path.join(ROOT, "profiles", "layer_fwd_qwen35_4b_layer.md")
     try:
