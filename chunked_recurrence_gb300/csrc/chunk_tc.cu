@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(NT2, 1)
         }
       }
       tc_fence_after();
-      // ---- round 1: U' = U - W S^T ; Q S^T
+      // ---- MMA group 1: U' = U - W S^T ; Q S^T
       if (wt == 0) {
         const uint32_t id = idesc_bf16(64, BVT, false, true);
 #pragma unroll
@@ -738,7 +738,7 @@ __global__ void __launch_bounds__(NT2, 1)
       tc_fence_before();
       named_bar_sync(2, 128);
       tc_fence_after();
-      // ---- round 2: P U' (hi + lo) ; dS^T = K^T diag(d/|k|) U' (hi + lo)
+      // ---- MMA group 2: P U' (hi + lo) ; dS^T = K^T diag(d/|k|) U' (hi + lo)
       if (wt == 0) {
         const uint32_t id_o = idesc_bf16(64, BVT, false, true);
         const uint32_t id_s = idesc_bf16(128, BVT, true, true);
