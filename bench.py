@@ -2,8 +2,10 @@
 
 One step = one pass of the forward hot path over one batch of the
 Qwen3.5-4B-shaped GDN layer workload (B=1, T=8192, 16 q/k heads, 32 v heads,
-K=V=128, bf16 inputs, fp32 state): gdn_gate_prep -> gdn_conv1d_varlen (+SiLU,
-Q|K|V channels) -> gdn_chunk_fwd (q/k L2 norm fused).  The segment-parallel
+K=V=128, bf16 inputs, fp32 state): one gdn_layer_fwd call, i.e. the gates and the
+conv1d (+SiLU, Q|K|V channels) in one launch, then gdn_chunk_fwd's two kernels (q/k
+L2 norm fused).  The same launches called one by one (gdn_gate_prep,
+gdn_conv1d_varlen, gdn_chunk_fwd) give the per-call times.  The segment-parallel
 two-pass (gdn_segment_summary -> gdn_chain_reduce -> gdn_chunk_fwd per
 segment) is measured on the long-context workload (T=131072, 16 heads,
 8 segments) and reported beside it, and one decode step (gdn_decode_step:
@@ -13,7 +15,9 @@ RMSNorm of the layer's o.
 
 gdn_chunk_fwd runs as two kernels (chunk_operand_kernel: every chunk's
 state-independent operands at once; chunk_scan_kernel: the state chain), so a
-step is four launches.  The roofline is reported for the gdn_chunk_fwd call.
+step is three launches.  The roofline is reported for the gdn_chunk_fwd call.
+The backward (gdn_chunk_bwd) at the same shape, and warm-L2 times of
+gdn_chunk_fwd and the step, are reported beside it.
 The fused persistent kernel (GDN_FLAG_FUSED: per-head state chains fed by chunk
 builders through an L2-resident ring) is timed beside it on the same inputs.
 
@@ -309,7 +313,7 @@ def run_gpu_arm(args, ws, rank, local):
                            "ms_mean": round(step_ms_local, 5), "ms_median": round(step_ms_median, 5),
                            "path_word": layer_path, "kernel_sha": sha})
 
-    # ---- the same launches called one by one (gate prep, conv1d, gdn_chunk_fwd), kernel by kernel
+    # ---- the same work as calls one by one (gate prep, conv1d, gdn_chunk_fwd), call by call
     unf = time_unfused_layer(crg, wl, inp, cu, stream, flush)
     cb = chunk_bytes(wl, n_tok, n_seq, inp["h0"] is not None)
     chunk_ms = unf["chunk_ms"]
@@ -337,6 +341,7 @@ def run_gpu_arm(args, ws, rank, local):
     q_, k_, v_ = crg.split_qkv(unf["y"], wl.Hqk, wl.Hv, wl.K, wl.V)
     paths = time_chunk_paths(crg, q_, k_, v_, unf["g"], unf["beta"], inp["h0"], cu,
                              None if cu is not None else wl.B, inp["scale"], stream, flush)
+    hot = time_hot_l2(crg, wl, inp, cu, bufs, q_, k_, v_, unf["g"], unf["beta"], stream)
     del unf
 
     # ---- end to end through the public API with host buffers
@@ -376,6 +381,7 @@ def run_gpu_arm(args, ws, rank, local):
         "layer_paths": layer_paths,
         "layer_with_norm": with_norm,
         "chunk_fwd_paths": paths,
+        "hot_l2": hot,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -531,6 +537,33 @@ def time_unfused_layer(crg, wl, inp, cu, stream, flush, reps=30):
     out = {k2 + "_ms": statistics.median(v2) for k2, v2 in t.items()}
     out["chunk_ms_mean"] = sum(t["chunk"]) / len(t["chunk"])
     out.update(y=y, g=g, beta=beta)
+    return out
+
+
+def time_hot_l2(crg, wl, inp, cu, bufs, q, k, v, g, beta, stream, reps=50):
+    """Secondary figures with a warm L2: gdn_chunk_fwd and the layer step called back to back
+    with no flush between calls (mean over reps calls between two events).  The inputs are
+    larger than L2, so they are only partly resident."""
+    n_tok = inp["n_tok"]
+    o = torch.empty((n_tok, wl.Hv, wl.V), device=q.device, dtype=wl.torch_dtype)
+    h_T = torch.empty((inp["n_seq"], wl.Hv, wl.V, wl.K), device=q.device)
+    B = None if cu is not None else wl.B
+    chunk = lambda: crg.gdn_chunk_fwd(q, k, v, g, beta, inp["h0"], cu, inp["scale"], True, B=B, o=o, h_T=h_T)
+    layer = lambda: crg.layer_fwd(inp["x"], inp["conv_w"], inp["a"], inp["b"], inp["A_log"], inp["dt_bias"],
+                                  wl.Hqk, wl.Hv, wl.K, wl.V, inp["h0"], cu, wl.B, inp["scale"], bufs=bufs)
+    out = {}
+    for name, fn in (("gdn_chunk_fwd_ms", chunk), ("gdn_layer_fwd_ms", layer)):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = round(e0.elapsed_time(e1) / reps, 5)
+    out["calls"] = reps
+    out["l2"] = "not flushed: back-to-back calls on the same inputs (larger than L2, so partly resident)"
     return out
 
 
