@@ -56,3 +56,41 @@ def test_chunk_bwd_bf16_head_dims(crg):
                             l2norm_qk=True)
     torch.cuda.synchronize()
     _check(got, ref, "bf16 rows")
+
+
+def test_chunk_bwd_fp32_16_row_walk_blocks(crg):
+    """V = 48 (three 16-row walk blocks a v-head), K = 64, two v-heads on each of two q/k
+    heads, empty sequences between and after two that end on and just past a chunk
+    boundary."""
+    lens = [64, 0, 0, 65, 0]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v, g, beta, h0, do, dhT = _case(93, int(cu[-1]), 2, 4, 64, 48, len(lens))
+    ref = oracle.gdn_bwd(q, k, v, g, beta, do, dhT, h0, cu_seqlens=cu, scale=0.3, l2norm_qk=True)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV)
+    got = crg.gdn_chunk_bwd(t(q), t(k), t(v), t(g), t(beta), t(do), t(dhT), t(h0),
+                            cu_seqlens=torch.from_numpy(cu).to(DEV), scale=0.3, l2norm_qk=True)
+    torch.cuda.synchronize()
+    _check(got, ref, "fp32 V = 48")
+
+
+def test_chunk_bwd_fp32_unaligned_inputs(crg):
+    """q, k, v and d_o 4 bytes off a 16-byte boundary: the kernels take their element-wise
+    loads instead of the vector ones, with the same gradients."""
+    lens = [1, 40, 150]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v, g, beta, h0, do, dhT = _case(94, int(cu[-1]), 1, 2, 32, 32, len(lens))
+    ref = oracle.gdn_bwd(q, k, v, g, beta, do, dhT, h0, cu_seqlens=cu, scale=0.4, l2norm_qk=True)
+
+    def off(x):  # the same values in a buffer that starts one float past an aligned address
+        a = np.ascontiguousarray(x, dtype=np.float32)
+        buf = torch.empty(a.size + 1, dtype=torch.float32, device=DEV)
+        view = buf[1:].view(a.shape)
+        view.copy_(torch.from_numpy(a))
+        assert view.data_ptr() % 16 != 0
+        return view
+
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV)
+    got = crg.gdn_chunk_bwd(off(q), off(k), off(v), t(g), t(beta), off(do), t(dhT), t(h0),
+                            cu_seqlens=torch.from_numpy(cu).to(DEV), scale=0.4, l2norm_qk=True)
+    torch.cuda.synchronize()
+    _check(got, ref, "fp32 unaligned")
