@@ -46,6 +46,7 @@
 #include <stdint.h>
 
 #if defined(__CUDACC__)
+#include "chunk_bwd_mma.cuh"
 #define GDN_BWD_FN __device__ __forceinline__
 #define GDN_BWD_HD __host__ __device__ inline
 #else
@@ -91,7 +92,7 @@ struct Params {
 // shared memory of one block, in floats
 GDN_BWD_HD size_t prep_smem_floats(int K) { return 2 * (size_t)C * (K + 1) + 2 * (size_t)C * CP + 4 * C; }
 GDN_BWD_HD size_t walk_smem_floats(int K, int BV) {
-  return 2 * (size_t)C * (K + 1) + 2 * (size_t)BV * (K + 1) + 8 * (size_t)C * (BV + 1) + 2 * (size_t)C * CP + 8 * C;
+  return 2 * (size_t)C * (K + 4) + 2 * (size_t)BV * (K + 4) + 8 * (size_t)C * (BV + 4) + 2 * (size_t)C * CP + 8 * C;
 }
 GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 1) + 6 * (size_t)C * CP + 8 * C; }
 
@@ -213,11 +214,10 @@ struct Fill8 {
   }
 };
 
-// Rows t0 .. t0 + n - 1 of k (and of q, when Qs is given) of q/k head qh into [C][K + 1]
+// Rows t0 .. t0 + n - 1 of k (and of q, when Qs is given) of q/k head qh into [C][KP]
 // tiles, zero past n.  The L2 norm follows in norm_and_cumsum, after a barrier.
-template <int K, class X, class LD>
+template <int K, int KP = K + 1, class X, class LD>
 GDN_BWD_FN void load_keys(X &x, const Params &p, LD ld, float *Ks, float *Qs, int64_t t0, int n, int qh) {
-  constexpr int KP = K + 1;
   const bool with_q = Qs != nullptr;
   if (p.vec8) {
     // 8-element vectors, PER of them (of k and of q) an item, all loads before the stores
@@ -265,9 +265,8 @@ GDN_BWD_FN void load_gates(X &x, const Params &p, float *gam, float *bet, int64_
 
 // After the loads' barrier: unit-norm rows of k (and q), gamma = the inclusive cumsum of g.
 // The rows past n are zero and stay zero; gamma past n repeats the last token's.
-template <int K, class X>
+template <int K, int KP = K + 1, class X>
 GDN_BWD_FN void norm_and_cumsum(X &x, const Params &p, float *Ks, float *Qs, float *gam) {
-  constexpr int KP = K + 1;
   if (p.l2norm) {
     x.par(Qs ? 2 * C : C, [&](int r) {
       float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
@@ -358,7 +357,9 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
 // ---- walk: the state-dependent steps of BV state rows of one v-head, chunk by chunk
 template <int KD, int BV, class X, class LD>
 GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, int h, int s) {
-  constexpr int K = KD, KP = KD + 1, VP = BV + 1;
+  // rows padded by 4 floats: the tensor-core fragments' loads (lane 4 g + t reads row g,
+  // column t) then fall in distinct banks
+  constexpr int K = KD, KP = KD + 4, VP = BV + 4;
   const int V = p.V, Hv = p.Hv;
   float *Ks = sm;              // [C][KP]  k of the chunk (unit-norm when l2norm)
   float *Qs = Ks + C * KP;     // [C][KP]  q
@@ -455,7 +456,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         }
       });
     } else {
-      load_keys<K>(x, p, ld, Ks, bwd ? Qs : nullptr, t0, n, qh);
+      load_keys<K, KP>(x, p, ld, Ks, bwd ? Qs : nullptr, t0, n, qh);
       x.par(C * BV, [&](int idx) {
         const int r = idx / BV, j = idx % BV;
         const bool in = r < n;
@@ -473,7 +474,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       }
     }
     x.sync();
-    norm_and_cumsum<K>(x, p, Ks, bwd ? Qs : nullptr, gam);
+    norm_and_cumsum<K, KP>(x, p, Ks, bwd ? Qs : nullptr, gam);
     x.sync();
     x.par(C, [&](int i) {
       bex[i] = expf(gam[i]);
@@ -495,8 +496,29 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     x.par(BV * K, [&](int idx) { dst[(idx / K) * (size_t)K + idx % K] = Ss[(idx / K) * KP + idx % K]; });
     load(slot, t0, n, false);
     float *fw = fw_of(slot);
-    // K S^T, 4 x 2 tiles of (i, v) a thread; the epilogue forms V - diag(b) K S^T, and both
-    // go to the backward sweep
+    // K S^T; the epilogue forms V - diag(b) K S^T, and both go to the backward sweep (on the
+    // device a tensor-core product, on the host 4 x 2 tiles of (i, v) a thread)
+#if defined(__CUDA_ARCH__)
+    {
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, BV> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, BV>::NTW;
+      if (tl.any) {
+        float d[NTW][4] = {};
+        tc::mma_nt<K, NTW>(lane, Ks, KP, Ss, KP, tl.m0, tl.n0, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), v = tc::frag_col(lane, tl.n0, j, e);
+            const float w = Vs[i * VP + v] - bex[i] * d[j][e];
+            Ws[i * VP + v] = w;
+            fw[CV + (size_t)i * V + v] = w;
+            fw[2 * CV + (size_t)i * V + v] = d[j][e];
+          }
+      }
+    }
+#else
     x.par((C / 4) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 4, v0 = (t % (BV / 2)) * 2;
       float ks[4][2] = {};
@@ -521,6 +543,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
           fw[2 * CV + (size_t)i * V + v] = ks[a][b];
         }
     });
+#endif
     x.sync();
     // U' = Z diag(beta) (V - diag(b) K S^T), 2 x 2 tiles of (i, v) a thread
     x.par((C / 2) * (BV / 2), [&](int t) {
@@ -543,8 +566,29 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         }
     });
     x.sync();
-    // S1 = b_last S + U'^T diag(d) K, 4 x 4 tiles of (v, c) a thread (columns c0 + b K / 4,
-    // so that neighbouring threads read neighbouring features)
+    // S1 = b_last S + U'^T diag(d) K (on the device a tensor-core product, on the host 4 x 4
+    // tiles of (v, c) a thread, columns c0 + b K / 4)
+#if defined(__CUDA_ARCH__)
+    {
+      const int lane = x.tid & 31;
+      const tc::Tiles<BV, K> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<BV, K>::NTW;
+      if (tl.any) {
+        float d[NTW][4];
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d[j][e] = bex[C - 1] * Ss[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)];
+        tc::mma_tn<C, NTW>(lane, Us, VP, dec, 1.f, Ks, KP, tl.m0, tl.n0, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            Ss[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)] = d[j][e];
+      }
+    }
+#else
     x.par((BV / 4) * (K / 4), [&](int t) {
       const int v0 = (t / (K / 4)) * 4, c0 = t % (K / 4);
       float acc[4][4] = {};
@@ -568,6 +612,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
           *sp = fmaf(bex[C - 1], *sp, acc[a][b]);
         }
     });
+#endif
     x.sync();
   }
 
@@ -582,7 +627,28 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
     float *dPsum = sums, *dTsum = sums + C * C, *ddsum = sums + 2 * C * C, *dbsum = ddsum + C;
     load(slot, t0, n, true);
-    // Q S^T and K dS1^T, 4 x 2 tiles of (i, v) a thread
+    // Q S^T and K dS1^T (on the device tensor-core products, on the host 4 x 2 tiles of
+    // (i, v) a thread)
+#if defined(__CUDA_ARCH__)
+    {
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, BV> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, BV>::NTW;
+      if (tl.any) {
+        float dq[NTW][4] = {}, dk[NTW][4] = {};
+        tc::mma_nt<K, NTW>(lane, Qs, KP, Ss, KP, tl.m0, tl.n0, dq);
+        tc::mma_nt<K, NTW>(lane, Ks, KP, dSs, KP, tl.m0, tl.n0, dk);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), v = tc::frag_col(lane, tl.n0, j, e);
+            QSs[i * VP + v] = dq[j][e];
+            KdS[i * VP + v] = dk[j][e];
+          }
+      }
+    }
+#else
     x.par((C / 4) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 4, v0 = (t % (BV / 2)) * 2;
       float qs[4][2] = {}, kd[4][2] = {};
@@ -607,6 +673,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
           KdS[(i0 + a) * VP + v0 + b] = kd[a][b];
         }
     });
+#endif
     x.sync();
     // this block's share of dP = Ot U'^T (lower incl. the diagonal; 4 x 4 tiles of (i, j):
     // rows i0 .. i0 + 3, columns tj + 16 b) and of dd_i = U'_i . (K dS1^T)_i;
@@ -721,8 +788,9 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     });
     x.sync();
     // this block's share of db_j = Ot_j . (Q S^T)_j - dV_j . (K S^T)_j (+ <S, dS1> at the
-    // chunk's last row); the S and dS1 parts of dq and dk, 4 x 8 tiles of (i, c) a thread
-    // (columns c0 + b K / 8): dq = diag(b) Ot S, dk = diag(d) U' dS1 - diag(b) dV S
+    // chunk's last row); the S and dS1 parts of dq and dk, dq = diag(b) Ot S,
+    // dk = diag(d) U' dS1 - diag(b) dV S (on the device tensor-core products, on the host
+    // 4 x 8 tiles of (i, c) a thread, columns c0 + b K / 8)
     x.par(C, [&](int j) {
       float b = 0.f;
       for (int v = 0; v < BV; ++v) b += Os[j * VP + v] * QSs[j * VP + v] - Ws[j * VP + v] * KSs[j * VP + v];
@@ -730,6 +798,34 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         for (int r = 0; r < C; ++r) b += prt[r];
       x.add(dbsum + j, b);
     });
+#if defined(__CUDA_ARCH__)
+    {
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, K> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, K>::NTW;
+      if (tl.any) {
+        float d[NTW][4] = {};
+        tc::mma_nn<BV, NTW>(lane, Os, VP, bex, 1.f, Ss, KP, tl.m0, tl.n0, d);  // diag(b) Ot S
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            if (i < n) x.add(p.dqn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
+            d[j][e] = 0.f;
+          }
+        tc::mma_nn<BV, NTW>(lane, Us, VP, dec, 1.f, dSs, KP, tl.m0, tl.n0, d);   // diag(d) U' dS1
+        tc::mma_nn<BV, NTW>(lane, Ws, VP, bex, -1.f, Ss, KP, tl.m0, tl.n0, d);   // - diag(b) dV S
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            if (i < n) x.add(p.dkn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
+          }
+      }
+    }
+#else
     x.par((C / 4) * (K / 8), [&](int t) {
       const int i0 = (t / (K / 8)) * 4, c0 = t % (K / 8);
       float sq[4][8] = {}, sk[4][8] = {}, sv[4][8] = {};
@@ -767,9 +863,32 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         }
       }
     });
+#endif
     x.sync();
-    // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K, 4 x 4 tiles of (v, c) a thread
-    // (columns c0 + b K / 4)
+    // dS = b_last dS1 + Ot^T diag(b) Q - (diag(b) dV)^T K (on the device tensor-core products,
+    // on the host 4 x 4 tiles of (v, c) a thread, columns c0 + b K / 4)
+#if defined(__CUDA_ARCH__)
+    {
+      const int lane = x.tid & 31;
+      const tc::Tiles<BV, K> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<BV, K>::NTW;
+      if (tl.any) {
+        float d[NTW][4];
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d[j][e] = bex[C - 1] * dSs[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)];
+        tc::mma_tn<C, NTW>(lane, Os, VP, bex, 1.f, Qs, KP, tl.m0, tl.n0, d);
+        tc::mma_tn<C, NTW>(lane, Ws, VP, bex, -1.f, Ks, KP, tl.m0, tl.n0, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dSs[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)] = d[j][e];
+      }
+    }
+#else
     x.par((BV / 4) * (K / 4), [&](int t) {
       const int v0 = (t / (K / 4)) * 4, c0 = t % (K / 4);
       float acc[4][4];
@@ -800,6 +919,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 #pragma unroll
         for (int b = 0; b < 4; ++b) dSs[(v0 + a) * KP + c0 + b * (K / 4)] = acc[a][b];
     });
+#endif
     x.sync();
   }
   if (p.dh0)

@@ -1,0 +1,152 @@
+// chunk_bwd_mma.cuh -- the walk's state products on the tensor cores: warp-level
+// mma.sync m16n8k8 with TF32 operands and fp32 accumulation.  Each fp32 operand x is split
+// into x = hi + lo, both TF32 (round to nearest), and a product takes three MMAs,
+// lo*hi + hi*lo + hi*hi (the dropped lo*lo term is about 2^-22 of the product), which keeps
+// the products at fp32-level accuracy.
+//
+// The operands stay where the walk keeps them, fp32 rows in shared memory; the split
+// happens in registers as the fragments are loaded (tcgen05 would need the split parts
+// staged in shared memory, three times the walk's tiles, which do not fit beside them).
+//
+// Fragment layout of m16n8k8 (TF32), lane = 4 g + t:
+//   A (16 x 8, row-major): a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
+//   B (8 x 8, k x n):      b0 (t, g), b1 (t + 4, g)
+//   D (16 x 8):            d0 (g, 2t), d1 (g, 2t + 1), d2 (g + 8, 2t), d3 (g + 8, 2t + 1)
+//
+// Tiles: a product of M x N (M, N multiples of 16 and 8) has MT = M / 16 row tiles and
+// NT = N / 8 column tiles.  Warp w takes row tile w % MT and NTW consecutive column tiles
+// from (w / MT) NTW, NTW = max(1, MT NT / 8), so that the eight warps cover every tile
+// once; with fewer than eight tiles the warps past them idle.  Device code only.
+#pragma once
+
+#include <stdint.h>
+
+namespace gdn_bwd {
+namespace tc {
+
+struct FragA {
+  uint32_t h[4], l[4];
+};
+struct FragB {
+  uint32_t h[2], l[2];
+};
+
+__device__ __forceinline__ void split(float x, uint32_t &hi, uint32_t &lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+__device__ __forceinline__ void frag_a(FragA &f, float a0, float a1, float a2, float a3) {
+  split(a0, f.h[0], f.l[0]);
+  split(a1, f.h[1], f.l[1]);
+  split(a2, f.h[2], f.l[2]);
+  split(a3, f.h[3], f.l[3]);
+}
+
+__device__ __forceinline__ void frag_b(FragB &f, float b0, float b1) {
+  split(b0, f.h[0], f.l[0]);
+  split(b1, f.h[1], f.l[1]);
+}
+
+__device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// d += a b in three MMAs, the small terms first
+__device__ __forceinline__ void mma3(float (&d)[4], const FragA &a, const FragB &b) {
+  mma(d, a.l, b.h);
+  mma(d, a.h, b.l);
+  mma(d, a.h, b.h);
+}
+
+// The warp's tiles of an M x N product (see above): its row tile m0, its first column tile
+// n0, and whether it has any.
+template <int M, int N>
+struct Tiles {
+  static constexpr int MT = M / 16, NT = N / 8, NTW = (MT * NT) / 8 > 0 ? (MT * NT) / 8 : 1;
+  int m0, n0;
+  bool any;
+  __device__ __forceinline__ explicit Tiles(int warp) {
+    m0 = (warp % MT) * 16;
+    n0 = (warp / MT) * NTW * 8;
+    any = (warp / MT) * NTW < NT;
+  }
+};
+
+// D[m][n] += sum_k A[m][k] B[n][k] for k < KL: A rows m0 .., B rows n0 + 8 j .. (j < NTW),
+// both fp32 rows in shared memory with strides lda, ldb.
+template <int KL, int NTW>
+__device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const float *B, int ldb, int m0, int n0,
+                                       float (&d)[NTW][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float *a = A + (m0 + g) * lda + t;
+  const float *b = B + (n0 + g) * ldb + t;
+#pragma unroll 2
+  for (int k0 = 0; k0 < KL; k0 += 8) {
+    FragA fa;
+    frag_a(fa, a[k0], a[8 * lda + k0], a[k0 + 4], a[8 * lda + k0 + 4]);
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) {
+      FragB fb;
+      frag_b(fb, b[8 * j * ldb + k0], b[8 * j * ldb + k0 + 4]);
+      mma3(d[j], fa, fb);
+    }
+  }
+}
+
+// D[m][n] += sum_k mult r_m A[m][k] B[k][n] for k < KL: A rows m0 .. (stride lda) scaled by
+// r (per row m), B rows k (stride ldb), columns n0 + 8 j ..
+template <int KL, int NTW>
+__device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const float *r, float mult, const float *B,
+                                       int ldb, int m0, int n0, float (&d)[NTW][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float *a = A + (m0 + g) * lda + t;
+  const float *b = B + t * ldb + n0 + g;
+  const float r0 = mult * r[m0 + g], r1 = mult * r[m0 + g + 8];
+#pragma unroll 2
+  for (int k0 = 0; k0 < KL; k0 += 8) {
+    FragA fa;
+    frag_a(fa, r0 * a[k0], r1 * a[8 * lda + k0], r0 * a[k0 + 4], r1 * a[8 * lda + k0 + 4]);
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) {
+      FragB fb;
+      frag_b(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
+      mma3(d[j], fa, fb);
+    }
+  }
+}
+
+// D[m][n] += sum_k mult s_k A[k][m] B[k][n] for k < KL: A stored by rows k (stride lda), so
+// that the operand is its transpose, row k scaled by s[k]; B rows k (stride ldb), columns
+// n0 + 8 j ..
+template <int KL, int NTW>
+__device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const float *s, float mult, const float *B,
+                                       int ldb, int m0, int n0, float (&d)[NTW][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float *a = A + t * lda + m0 + g;
+  const float *b = B + t * ldb + n0 + g;
+#pragma unroll 2
+  for (int k0 = 0; k0 < KL; k0 += 8) {
+    const float s0 = mult * s[k0 + t], s1 = mult * s[k0 + t + 4];
+    FragA fa;
+    frag_a(fa, s0 * a[k0 * lda], s0 * a[k0 * lda + 8], s1 * a[(k0 + 4) * lda], s1 * a[(k0 + 4) * lda + 8]);
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) {
+      FragB fb;
+      frag_b(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
+      mma3(d[j], fa, fb);
+    }
+  }
+}
+
+// The element of tile j that fragment slot e of this lane holds: row m0 + g (+ 8 for e >= 2),
+// column n0 + 8 j + 2 t (+ 1 for odd e).
+__device__ __forceinline__ int frag_row(int lane, int m0, int e) { return m0 + (lane >> 2) + ((e >> 1) << 3); }
+__device__ __forceinline__ int frag_col(int lane, int n0, int j, int e) { return n0 + 8 * j + 2 * (lane & 3) + (e & 1); }
+
+}  // namespace tc
+}  // namespace gdn_bwd
