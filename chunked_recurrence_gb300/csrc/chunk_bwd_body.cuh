@@ -380,6 +380,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
   float *bex = bet + C;        // [C] exp(gamma)
   float *dec = bex + C;        // [C] exp(gamma_last - gamma)
   float *prt = dec + C;        // [C] partial sums of <S, dS1>
+  float *one = prt + C;        // [C] ones (a unit scale for the tensor-core products)
 
   const int qh = h / (Hv / p.Hqk), row0 = tile * BV;
   int64_t start, end;
@@ -488,6 +489,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     const int r = idx / K, c = idx % K;
     Ss[r * KP + c] = p.h0 ? p.h0[((size_t)s * Hv + h) * VK + (size_t)(row0 + r) * K + c] : 0.f;
   });
+  x.par(C, [&](int i) { one[i] = 1.f; });
   x.sync();
   for (int ci = 0; ci < n_chunks; ++ci) {
     const int64_t t0 = start + (int64_t)ci * C, slot = slot0 + ci;
@@ -505,7 +507,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float d[NTW][4] = {};
-        tc::mma_nt<K, NTW>(lane, Ks, KP, Ss, KP, tl.m0, tl.n0, d);
+        tc::mma_nt<NTW>(lane, Ks, KP, Ss, KP, tl.m0, tl.n0, 0, K, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -545,7 +547,27 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     });
 #endif
     x.sync();
-    // U' = Z diag(beta) (V - diag(b) K S^T), 2 x 2 tiles of (i, v) a thread
+    // U' = Z diag(beta) (V - diag(b) K S^T) (on the device a tensor-core product, on the host
+    // 2 x 2 tiles of (i, v) a thread)
+#if defined(__CUDA_ARCH__)
+    {  // Z is zero right of its diagonal: rows i < m0 + 16 take j < m0 + 16
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, BV> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, BV>::NTW;
+      if (tl.any) {
+        float d[NTW][4] = {};
+        tc::mma_nn<NTW>(lane, Zm, CP, one, 1.f, Ws, VP, bet, tl.m0, tl.n0, 0, tl.m0 + 16, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            Us[i * VP + c] = d[j][e];
+            fw[(size_t)i * V + c] = d[j][e];
+          }
+      }
+    }
+#else
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
       float acc[2][2] = {};
@@ -565,6 +587,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
           fw[(size_t)(i0 + a) * V + v0 + b] = acc[a][b];
         }
     });
+#endif
     x.sync();
     // S1 = b_last S + U'^T diag(d) K (on the device a tensor-core product, on the host 4 x 4
     // tiles of (v, c) a thread, columns c0 + b K / 4)
@@ -580,7 +603,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             d[j][e] = bex[C - 1] * Ss[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)];
-        tc::mma_tn<C, NTW>(lane, Us, VP, dec, 1.f, Ks, KP, tl.m0, tl.n0, d);
+        tc::mma_tn<NTW>(lane, Us, VP, dec, 1.f, Ks, KP, tl.m0, tl.n0, 0, C, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -636,8 +659,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float dq[NTW][4] = {}, dk[NTW][4] = {};
-        tc::mma_nt<K, NTW>(lane, Qs, KP, Ss, KP, tl.m0, tl.n0, dq);
-        tc::mma_nt<K, NTW>(lane, Ks, KP, dSs, KP, tl.m0, tl.n0, dk);
+        tc::mma_nt<NTW>(lane, Qs, KP, Ss, KP, tl.m0, tl.n0, 0, K, dq);
+        tc::mma_nt<NTW>(lane, Ks, KP, dSs, KP, tl.m0, tl.n0, 0, K, dk);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -679,6 +702,24 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     // rows i0 .. i0 + 3, columns tj + 16 b) and of dd_i = U'_i . (K dS1^T)_i;
     // dU' = diag(d) K dS1^T + QG^T Ot (2 x 2 tiles of (i, v); row i0 + 1's term at j = i0 has
     // a zero factor, QG being lower)
+#if defined(__CUDA_ARCH__)
+    {  // tiles wholly above the diagonal skipped
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, C> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, C>::NTW;
+      if (tl.any && tl.n0 <= tl.m0 + 15) {
+        float d[NTW][4] = {};
+        tc::mma_nt<NTW>(lane, Os, VP, Us, VP, tl.m0, tl.n0, 0, BV, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            if (c <= i) x.add(dPsum + i * C + c, d[j][e]);
+          }
+      }
+    }
+#else
     x.par((C / 4) * 16, [&](int t) {
       const int i0 = (t / 16) * 4, tj = t % 16;
       if (tj > i0 + 3) return;
@@ -703,11 +744,37 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
           if (j <= i) x.add(dPsum + i * C + j, acc[a][b]);
         }
     });
+#endif
     x.par(C, [&](int i) {
       float acc = 0.f;
       for (int v = 0; v < BV; ++v) acc = fmaf(Us[i * VP + v], KdS[i * VP + v], acc);
       x.add(ddsum + i, acc);
     });
+#if defined(__CUDA_ARCH__)
+    {  // QG[j][i] is zero for j < i: rows i >= m0 take j >= m0
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, BV> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, BV>::NTW;
+      if (tl.any) {
+        float d[NTW][4];
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            d[j][e] = dec[i] * KdS[i * VP + c];
+          }
+        tc::mma_tn<NTW>(lane, QGm, CP, one, 1.f, Os, VP, tl.m0, tl.n0, tl.m0, C, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            dUs[i * VP + c] = d[j][e];
+          }
+      }
+    }
+#else
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
       float acc[2][2];
@@ -728,10 +795,29 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 #pragma unroll
         for (int b = 0; b < 2; ++b) dUs[(i0 + a) * VP + v0 + b] = acc[a][b];
     });
+#endif
     x.sync();
     // this block's share of dT = dU' (V - diag(b) K S^T)^T (lower; 4 x 4 tiles, columns
     // tj + 16 b); dV = diag(beta) Z^T dU' (complete for these rows; 2 x 2 tiles, Z being
     // lower), written over V - diag(b) K S^T once dT has read it (after the barrier below)
+#if defined(__CUDA_ARCH__)
+    {  // tiles wholly above the diagonal skipped
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, C> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, C>::NTW;
+      if (tl.any && tl.n0 <= tl.m0 + 15) {
+        float d[NTW][4] = {};
+        tc::mma_nt<NTW>(lane, dUs, VP, Ws, VP, tl.m0, tl.n0, 0, BV, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            if (c <= i) x.add(dTsum + i * C + c, d[j][e]);
+          }
+      }
+    }
+#else
     x.par((C / 4) * 16, [&](int t) {
       const int i0 = (t / 16) * 4, tj = t % 16;
       if (tj > i0 + 3) return;
@@ -756,6 +842,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
           if (j <= i) x.add(dTsum + i * C + j, acc[a][b]);
         }
     });
+#endif
     // b_last's gradient takes <S, dS1> over the block's rows: 64 partial sums
     x.par(C, [&](int r) {
       float acc = 0.f;
@@ -764,6 +851,26 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       prt[r] = acc;
     });
     x.sync();
+#if defined(__CUDA_ARCH__)
+    {  // Z[j][i] is zero for j < i: rows i >= m0 take j >= m0
+      const int lane = x.tid & 31;
+      const tc::Tiles<C, BV> tl(x.tid >> 5);
+      constexpr int NTW = tc::Tiles<C, BV>::NTW;
+      if (tl.any) {
+        float d[NTW][4] = {};
+        tc::mma_tn<NTW>(lane, Zm, CP, one, 1.f, dUs, VP, tl.m0, tl.n0, tl.m0, C, d);
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            const float r = d[j][e] * bet[i];
+            Ws[i * VP + c] = r;
+            if (i < n) p.dv[((t0 + i) * Hv + h) * V + row0 + c] = r;
+          }
+      }
+    }
+#else
     x.par((C / 2) * (BV / 2), [&](int t) {
       const int i0 = (t / (BV / 2)) * 2, v0 = (t % (BV / 2)) * 2;
       float acc[2][2] = {};
@@ -786,6 +893,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         }
       }
     });
+#endif
     x.sync();
     // this block's share of db_j = Ot_j . (Q S^T)_j - dV_j . (K S^T)_j (+ <S, dS1> at the
     // chunk's last row); the S and dS1 parts of dq and dk, dq = diag(b) Ot S,
@@ -805,7 +913,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, K>::NTW;
       if (tl.any) {
         float d[NTW][4] = {};
-        tc::mma_nn<BV, NTW>(lane, Os, VP, bex, 1.f, Ss, KP, tl.m0, tl.n0, d);  // diag(b) Ot S
+        tc::mma_nn<NTW>(lane, Os, VP, bex, 1.f, Ss, KP, one, tl.m0, tl.n0, 0, BV, d);  // diag(b) Ot S
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -814,8 +922,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
             if (i < n) x.add(p.dqn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
             d[j][e] = 0.f;
           }
-        tc::mma_nn<BV, NTW>(lane, Us, VP, dec, 1.f, dSs, KP, tl.m0, tl.n0, d);   // diag(d) U' dS1
-        tc::mma_nn<BV, NTW>(lane, Ws, VP, bex, -1.f, Ss, KP, tl.m0, tl.n0, d);   // - diag(b) dV S
+        tc::mma_nn<NTW>(lane, Us, VP, dec, 1.f, dSs, KP, one, tl.m0, tl.n0, 0, BV, d);   // diag(d) U' dS1
+        tc::mma_nn<NTW>(lane, Ws, VP, bex, -1.f, Ss, KP, one, tl.m0, tl.n0, 0, BV, d);   // - diag(b) dV S
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -879,8 +987,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             d[j][e] = bex[C - 1] * dSs[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)];
-        tc::mma_tn<C, NTW>(lane, Os, VP, bex, 1.f, Qs, KP, tl.m0, tl.n0, d);
-        tc::mma_tn<C, NTW>(lane, Ws, VP, bex, -1.f, Ks, KP, tl.m0, tl.n0, d);
+        tc::mma_tn<NTW>(lane, Os, VP, bex, 1.f, Qs, KP, tl.m0, tl.n0, 0, C, d);
+        tc::mma_tn<NTW>(lane, Ws, VP, bex, -1.f, Ks, KP, tl.m0, tl.n0, 0, C, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll

@@ -77,16 +77,18 @@ struct Tiles {
   }
 };
 
-// D[m][n] += sum_k A[m][k] B[n][k] for k < KL: A rows m0 .., B rows n0 + 8 j .. (j < NTW),
-// both fp32 rows in shared memory with strides lda, ldb.
-template <int KL, int NTW>
+// The three forms below add to D, over k in [kbeg, kend) (multiples of 8), the products of
+// fp32 rows in shared memory; a triangular factor passes the range where it is nonzero.
+
+// D[m][n] += sum_k A[m][k] B[n][k]: A rows m0 .. (stride lda), B rows n0 + 8 j .. (ldb).
+template <int NTW>
 __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const float *B, int ldb, int m0, int n0,
-                                       float (&d)[NTW][4]) {
+                                       int kbeg, int kend, float (&d)[NTW][4]) {
   const int g = lane >> 2, t = lane & 3;
   const float *a = A + (m0 + g) * lda + t;
   const float *b = B + (n0 + g) * ldb + t;
 #pragma unroll 2
-  for (int k0 = 0; k0 < KL; k0 += 8) {
+  for (int k0 = kbeg; k0 < kend; k0 += 8) {
     FragA fa;
     frag_a(fa, a[k0], a[8 * lda + k0], a[k0 + 4], a[8 * lda + k0 + 4]);
 #pragma unroll
@@ -98,40 +100,41 @@ __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const 
   }
 }
 
-// D[m][n] += sum_k mult r_m A[m][k] B[k][n] for k < KL: A rows m0 .. (stride lda) scaled by
-// r (per row m), B rows k (stride ldb), columns n0 + 8 j ..
-template <int KL, int NTW>
-__device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const float *r, float mult, const float *B,
-                                       int ldb, int m0, int n0, float (&d)[NTW][4]) {
+// D[m][n] += sum_k mult ra_m A[m][k] kb_k B[k][n]: A rows m0 .. (stride lda) scaled by ra (per
+// row), B rows k (stride ldb) scaled by kb (per row k), columns n0 + 8 j ..
+template <int NTW>
+__device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const float *ra, float mult, const float *B,
+                                       int ldb, const float *kb, int m0, int n0, int kbeg, int kend,
+                                       float (&d)[NTW][4]) {
   const int g = lane >> 2, t = lane & 3;
   const float *a = A + (m0 + g) * lda + t;
   const float *b = B + t * ldb + n0 + g;
-  const float r0 = mult * r[m0 + g], r1 = mult * r[m0 + g + 8];
+  const float r0 = mult * ra[m0 + g], r1 = mult * ra[m0 + g + 8];
 #pragma unroll 2
-  for (int k0 = 0; k0 < KL; k0 += 8) {
+  for (int k0 = kbeg; k0 < kend; k0 += 8) {
     FragA fa;
     frag_a(fa, r0 * a[k0], r1 * a[8 * lda + k0], r0 * a[k0 + 4], r1 * a[8 * lda + k0 + 4]);
+    const float s0 = kb[k0 + t], s1 = kb[k0 + t + 4];
 #pragma unroll
     for (int j = 0; j < NTW; ++j) {
       FragB fb;
-      frag_b(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
+      frag_b(fb, s0 * b[k0 * ldb + 8 * j], s1 * b[(k0 + 4) * ldb + 8 * j]);
       mma3(d[j], fa, fb);
     }
   }
 }
 
-// D[m][n] += sum_k mult s_k A[k][m] B[k][n] for k < KL: A stored by rows k (stride lda), so
-// that the operand is its transpose, row k scaled by s[k]; B rows k (stride ldb), columns
-// n0 + 8 j ..
-template <int KL, int NTW>
-__device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const float *s, float mult, const float *B,
-                                       int ldb, int m0, int n0, float (&d)[NTW][4]) {
+// D[m][n] += sum_k mult ks_k A[k][m] B[k][n]: A stored by rows k (stride lda), so that the
+// operand is its transpose, row k scaled by ks[k]; B rows k (stride ldb), columns n0 + 8 j ..
+template <int NTW>
+__device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const float *ks, float mult, const float *B,
+                                       int ldb, int m0, int n0, int kbeg, int kend, float (&d)[NTW][4]) {
   const int g = lane >> 2, t = lane & 3;
   const float *a = A + t * lda + m0 + g;
   const float *b = B + t * ldb + n0 + g;
 #pragma unroll 2
-  for (int k0 = 0; k0 < KL; k0 += 8) {
-    const float s0 = mult * s[k0 + t], s1 = mult * s[k0 + t + 4];
+  for (int k0 = kbeg; k0 < kend; k0 += 8) {
+    const float s0 = mult * ks[k0 + t], s1 = mult * ks[k0 + t + 4];
     FragA fa;
     frag_a(fa, s0 * a[k0 * lda], s0 * a[k0 * lda + 8], s1 * a[(k0 + 4) * lda], s1 * a[(k0 + 4) * lda + 8]);
 #pragma unroll
