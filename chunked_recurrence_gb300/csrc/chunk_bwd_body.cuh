@@ -90,11 +90,11 @@ struct Params {
 };
 
 // shared memory of one block, in floats
-GDN_BWD_HD size_t prep_smem_floats(int K) { return 2 * (size_t)C * (K + 1) + 2 * (size_t)C * CP + 4 * C; }
+GDN_BWD_HD size_t prep_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 2 * (size_t)C * CP + 4 * C; }
 GDN_BWD_HD size_t walk_smem_floats(int K, int BV) {
   return 2 * (size_t)C * (K + 4) + 2 * (size_t)BV * (K + 4) + 8 * (size_t)C * (BV + 4) + 2 * (size_t)C * CP + 8 * C;
 }
-GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 1) + 6 * (size_t)C * CP + 8 * C; }
+GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 6 * (size_t)C * (C + 4) + 9 * C; }
 
 GDN_BWD_FN int64_t seq_start(const Params &p, int s) { return p.cu ? (int64_t)p.cu[s] : (int64_t)s * p.row_T; }
 
@@ -283,7 +283,7 @@ GDN_BWD_FN void norm_and_cumsum(X &x, const Params &p, float *Ks, float *Qs, flo
 // ---- prep: Z, KG and QG of one (chunk, v-head)
 template <int KD, class X, class LD>
 GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot, int h) {
-  constexpr int K = KD, KP = KD + 1;
+  constexpr int K = KD, KP = KD + 4;  // rows padded for the tensor-core fragments' loads
   int64_t t0;
   int n;
   if (!slot_chunk(p, slot, t0, n)) return;
@@ -295,13 +295,39 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   float *bet = gam + C;       // [C]
   float *out = p.prep + ((size_t)slot * p.Hv + h) * kPrep;
   float *KGo = out + C * C, *QGo = out + 2 * C * C;
-  load_keys<K>(x, p, ld, Ks, Qs, t0, n, h / (p.Hv / p.Hqk));
+  load_keys<K, KP>(x, p, ld, Ks, Qs, t0, n, h / (p.Hv / p.Hqk));
   load_gates(x, p, gam, bet, t0, n, h);
   x.sync();
-  norm_and_cumsum<K>(x, p, Ks, Qs, gam);
+  norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
   x.sync();
-  // K K^T and Q K^T, 4 x 4 tiles of (i, j) a thread: every loaded k or q value feeds four
-  // products.  Gamma, KG, QG and A = diag(beta) KG follow in the tile's epilogue.
+  // K K^T and Q K^T (on the device tensor-core products, on the host 4 x 4 tiles of (i, j) a
+  // thread).  Gamma, KG, QG and A = diag(beta) KG follow in the tile's epilogue, which also
+  // writes the zeros above the diagonal.
+#if defined(__CUDA_ARCH__)
+  {
+    const int lane = x.tid & 31;
+    const tc::Tiles<C, C> tl(x.tid >> 5);
+    constexpr int NTW = tc::Tiles<C, C>::NTW;
+    if (tl.any) {
+      float kk[NTW][4] = {}, qk[NTW][4] = {};
+      if (tl.n0 <= tl.m0 + 15) {  // tiles wholly above the diagonal hold zeros
+        tc::mma_nt<NTW>(lane, Ks, KP, nullptr, Ks, KP, tl.m0, tl.n0, 0, K, kk);
+        tc::mma_nt<NTW>(lane, Qs, KP, nullptr, Ks, KP, tl.m0, tl.n0, 0, K, qk);
+      }
+#pragma unroll
+      for (int jt = 0; jt < NTW; ++jt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = tc::frag_row(lane, tl.m0, e), j = tc::frag_col(lane, tl.n0, jt, e);
+          const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
+          const float kg = j < i ? kk[jt][e] * gij : 0.f;
+          Am[i * CP + j] = bet[i] * kg;
+          KGo[i * C + j] = kg;
+          QGo[i * C + j] = j <= i ? qk[jt][e] * gij : 0.f;
+        }
+    }
+  }
+#else
   x.par((C / 4) * (C / 4), [&](int t) {
     const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
     float kk[4][4] = {}, qk[4][4] = {};
@@ -336,6 +362,7 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
         QGo[i * C + j] = j <= i ? qk[a][b] * gij : 0.f;
       }
   });
+#endif
   x.par(C * C, [&](int idx) {
     const int i = idx / C, j = idx % C;
     Zb[i * CP + j] = i == j ? 1.f : 0.f;
@@ -507,7 +534,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float d[NTW][4] = {};
-        tc::mma_nt<NTW>(lane, Ks, KP, Ss, KP, tl.m0, tl.n0, 0, K, d);
+        tc::mma_nt<NTW>(lane, Ks, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -659,8 +686,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float dq[NTW][4] = {}, dk[NTW][4] = {};
-        tc::mma_nt<NTW>(lane, Qs, KP, Ss, KP, tl.m0, tl.n0, 0, K, dq);
-        tc::mma_nt<NTW>(lane, Ks, KP, dSs, KP, tl.m0, tl.n0, 0, K, dk);
+        tc::mma_nt<NTW>(lane, Qs, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, dq);
+        tc::mma_nt<NTW>(lane, Ks, KP, nullptr, dSs, KP, tl.m0, tl.n0, 0, K, dk);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -709,7 +736,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, C>::NTW;
       if (tl.any && tl.n0 <= tl.m0 + 15) {
         float d[NTW][4] = {};
-        tc::mma_nt<NTW>(lane, Os, VP, Us, VP, tl.m0, tl.n0, 0, BV, d);
+        tc::mma_nt<NTW>(lane, Os, VP, nullptr, Us, VP, tl.m0, tl.n0, 0, BV, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -807,7 +834,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, C>::NTW;
       if (tl.any && tl.n0 <= tl.m0 + 15) {
         float d[NTW][4] = {};
-        tc::mma_nt<NTW>(lane, dUs, VP, Ws, VP, tl.m0, tl.n0, 0, BV, d);
+        tc::mma_nt<NTW>(lane, dUs, VP, nullptr, Ws, VP, tl.m0, tl.n0, 0, BV, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -1040,20 +1067,21 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 // ---- grad: the gradients linear in the summed dP, dT, dd and db of one (chunk, v-head)
 template <int KD, class X, class LD>
 GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot, int h) {
-  constexpr int K = KD, KP = KD + 1;
+  // rows padded by 4 floats, so that the tensor-core fragments' loads fall in distinct banks
+  constexpr int K = KD, KP = KD + 4, MP = C + 4;
   int64_t t0;
   int n;
   if (!slot_chunk(p, slot, t0, n)) return;
   const int Hv = p.Hv, qh = h / (Hv / p.Hqk);
   float *Ks = sm;              // [C][KP]  k (unit-norm when l2norm)
   float *Qs = Ks + C * KP;     // [C][KP]  q
-  float *Zm = Qs + C * KP;     // [C][CP]  Z
-  float *KGm = Zm + C * CP;    // [C][CP]  KG
-  float *QGm = KGm + C * CP;   // [C][CP]  QG
-  float *dPm = QGm + C * CP;   // [C][CP]  dP, then M1 = dP * Gamma
-  float *dTm = dPm + C * CP;   // [C][CP]  dT, then dA, then dKK
-  float *Ym = dTm + C * CP;    // [C][CP]  Y = (dT diag(beta)) Z^T, then D = dKK + dKK^T
-  float *gam = Ym + C * CP;    // [C] gamma
+  float *Zm = Qs + C * KP;     // [C][MP]  Z
+  float *KGm = Zm + C * MP;    // [C][MP]  KG
+  float *QGm = KGm + C * MP;   // [C][MP]  QG
+  float *dPm = QGm + C * MP;   // [C][MP]  dP, then M1 = dP * Gamma
+  float *dTm = dPm + C * MP;   // [C][MP]  dT, then dA, then dKK
+  float *Ym = dTm + C * MP;    // [C][MP]  Y = (dT diag(beta)) Z^T, then D = dKK + dKK^T
+  float *gam = Ym + C * MP;    // [C] gamma
   float *bet = gam + C;        // [C] beta
   float *bex = bet + C;        // [C] exp(gamma)
   float *dec = bex + C;        // [C] exp(gamma_last - gamma)
@@ -1061,6 +1089,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   float *db = dd + C;          // [C] dL/db
   float *dbt = db + C;         // [C] dL/dbeta
   float *dgm = dbt + C;        // [C] dL/dgamma, then dg
+  float *one = dgm + C;        // [C] ones (a unit scale for the tensor-core products)
   const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
   const float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
   if (p.vec8) {  // every fill of a phase in flight at once
@@ -1073,11 +1102,11 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
       fdp.load(t, sums, C, C);
       fdt.load(t, sums + C * C, C, C);
       const float dv = t < C ? sums[2 * C * C + t] : 0.f, bv = t < C ? sums[2 * C * C + C + t] : 0.f;
-      fz.store(t, Zm, CP);
-      fkg.store(t, KGm, CP);
-      fqg.store(t, QGm, CP);
-      fdp.store(t, dPm, CP);
-      fdt.store(t, dTm, CP);
+      fz.store(t, Zm, MP);
+      fkg.store(t, KGm, MP);
+      fqg.store(t, QGm, MP);
+      fdp.store(t, dPm, MP);
+      fdt.store(t, dTm, MP);
       if (t < C) {
         dd[t] = dv;
         db[t] = bv;
@@ -1097,33 +1126,54 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
       }
     });
   } else {
-    load_keys<K>(x, p, ld, Ks, Qs, t0, n, qh);
+    load_keys<K, KP>(x, p, ld, Ks, Qs, t0, n, qh);
     load_gates(x, p, gam, bet, t0, n, h);
-    copy_block<C, C>(x, pr, C, Zm, CP);
-    copy_block<C, C>(x, pr + C * C, C, KGm, CP);
-    copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
-    copy_block<C, C>(x, sums, C, dPm, CP);
-    copy_block<C, C>(x, sums + C * C, C, dTm, CP);
+    copy_block<C, C>(x, pr, C, Zm, MP);
+    copy_block<C, C>(x, pr + C * C, C, KGm, MP);
+    copy_block<C, C>(x, pr + 2 * C * C, C, QGm, MP);
+    copy_block<C, C>(x, sums, C, dPm, MP);
+    copy_block<C, C>(x, sums + C * C, C, dTm, MP);
     x.par(C, [&](int i) {
       dd[i] = sums[2 * C * C + i];
       db[i] = sums[2 * C * C + C + i];
     });
   }
   x.sync();
-  norm_and_cumsum<K>(x, p, Ks, Qs, gam);
+  norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
   x.sync();
   x.par(C, [&](int i) {
     bex[i] = expf(gam[i]);
     dec[i] = expf(gam[C - 1] - gam[i]);
+    one[i] = 1.f;
   });
   // dbeta from T = Z diag(beta): colsum(dT * Z)
   x.par(C, [&](int j) {
     float acc = 0.f;
-    for (int i = j; i < C; ++i) acc = fmaf(dTm[i * CP + j], Zm[i * CP + j], acc);
+    for (int i = j; i < C; ++i) acc = fmaf(dTm[i * MP + j], Zm[i * MP + j], acc);
     dbt[j] = acc;
   });
-  // Y = (dT diag(beta)) Z^T, 4 x 4 tiles of (i, j) a thread: dT is zero right of its
-  // diagonal and Z too, so the terms past min(i, j) add zeros
+  // Y = (dT diag(beta)) Z^T (on the device a tensor-core product, on the host 4 x 4 tiles of
+  // (i, j) a thread): dT is zero right of its diagonal and Z too, so the terms past min(i, j)
+  // add zeros
+#if defined(__CUDA_ARCH__)
+  {  // terms past min(i, j) are zero: the tile takes m < min(m0 + 16, n0 + its width)
+    const int lane = x.tid & 31;
+    const tc::Tiles<C, C> tl(x.tid >> 5);
+    constexpr int NTW = tc::Tiles<C, C>::NTW;
+    if (tl.any) {
+      float d[NTW][4] = {};
+      const int kend = (tl.m0 + 16 < tl.n0 + 8 * NTW) ? tl.m0 + 16 : tl.n0 + 8 * NTW;
+      tc::mma_nt<NTW, true>(lane, dTm, MP, bet, Zm, MP, tl.m0, tl.n0, 0, kend, d);
+#pragma unroll
+      for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            Ym[i * MP + c] = d[j][e];
+          }
+    }
+  }
+#else
   x.par((C / 4) * (C / 4), [&](int t) {
     const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
     const int mend = (i0 < j0 ? i0 : j0) + 4;
@@ -1133,8 +1183,8 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
       float tr[4], zr[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
-        tr[a] = dTm[(i0 + a) * CP + m] * bm;
-        zr[a] = Zm[(j0 + a) * CP + m];
+        tr[a] = dTm[(i0 + a) * MP + m] * bm;
+        zr[a] = Zm[(j0 + a) * MP + m];
       }
 #pragma unroll
       for (int a = 0; a < 4; ++a)
@@ -1144,11 +1194,30 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) Ym[(i0 + a) * CP + j0 + b] = acc[a][b];
+      for (int b = 0; b < 4; ++b) Ym[(i0 + a) * MP + j0 + b] = acc[a][b];
   });
+#endif
   x.sync();
-  // dA = -Z^T Y, strictly lower (into dT's place), 4 x 4 tiles: Z^T's column i is zero
-  // above row i, so every row of a tile can start at the tile's first row
+  // dA = -Z^T Y, strictly lower (into dT's place; on the host 4 x 4 tiles): Z^T's column i
+  // is zero above row i, so every row of a tile can start at the tile's first row
+#if defined(__CUDA_ARCH__)
+  {  // Z[m][i] is zero for m < i: rows i >= m0 take m >= m0; tiles above the diagonal write zeros
+    const int lane = x.tid & 31;
+    const tc::Tiles<C, C> tl(x.tid >> 5);
+    constexpr int NTW = tc::Tiles<C, C>::NTW;
+    if (tl.any) {
+      float d[NTW][4] = {};
+      if (tl.n0 <= tl.m0 + 15) tc::mma_tn<NTW>(lane, Zm, MP, one, 1.f, Ym, MP, tl.m0, tl.n0, tl.m0, C, d);
+#pragma unroll
+      for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            dTm[i * MP + c] = c < i ? -d[j][e] : 0.f;
+          }
+    }
+  }
+#else
   x.par((C / 4) * (C / 4), [&](int t) {
     const int i0 = (t / (C / 4)) * 4, j0 = (t % (C / 4)) * 4;
     float acc[4][4] = {};
@@ -1157,8 +1226,8 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
         float zr[4], yr[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-          zr[a] = Zm[m * CP + i0 + a];
-          yr[a] = Ym[m * CP + j0 + a];
+          zr[a] = Zm[m * MP + i0 + a];
+          yr[a] = Ym[m * MP + j0 + a];
         }
 #pragma unroll
         for (int a = 0; a < 4; ++a)
@@ -1168,20 +1237,21 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) dTm[(i0 + a) * CP + j0 + b] = j0 + b < i0 + a ? -acc[a][b] : 0.f;
+      for (int b = 0; b < 4; ++b) dTm[(i0 + a) * MP + j0 + b] = j0 + b < i0 + a ? -acc[a][b] : 0.f;
   });
+#endif
   x.sync();
   // dgamma (through Gamma in A and P, b and d) and the rest of dbeta
   x.par(C, [&](int i) {
     float rA = 0.f, cA = 0.f, rP = 0.f, cP = 0.f, bA = 0.f;
     for (int j = 0; j < i; ++j) {
-      const float t = dTm[i * CP + j] * KGm[i * CP + j];
+      const float t = dTm[i * MP + j] * KGm[i * MP + j];
       bA += t;
       rA = fmaf(bet[i], t, rA);
     }
-    for (int m = i + 1; m < C; ++m) cA = fmaf(bet[m], dTm[m * CP + i] * KGm[m * CP + i], cA);
-    for (int j = 0; j <= i; ++j) rP = fmaf(dPm[i * CP + j], QGm[i * CP + j], rP);
-    for (int m = i; m < C; ++m) cP = fmaf(dPm[m * CP + i], QGm[m * CP + i], cP);
+    for (int m = i + 1; m < C; ++m) cA = fmaf(bet[m], dTm[m * MP + i] * KGm[m * MP + i], cA);
+    for (int j = 0; j <= i; ++j) rP = fmaf(dPm[i * MP + j], QGm[i * MP + j], rP);
+    for (int m = i; m < C; ++m) cP = fmaf(dPm[m * MP + i], QGm[m * MP + i], cP);
     dbt[i] += bA;
     dgm[i] = rP - cP + rA - cA + db[i] * bex[i] - dd[i] * dec[i];
   });
@@ -1196,8 +1266,8 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   x.par(C * C, [&](int idx) {
     const int i = idx / C, j = idx % C;
     const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
-    dTm[i * CP + j] = j < i ? bet[i] * dTm[i * CP + j] * gij : 0.f;
-    dPm[i * CP + j] *= gij;
+    dTm[i * MP + j] = j < i ? bet[i] * dTm[i * MP + j] * gij : 0.f;
+    dPm[i * MP + j] *= gij;
   });
   x.sync();
   x.par(C, [&](int i) {
@@ -1209,11 +1279,39 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   // D = dKK + dKK^T (symmetric, zero diagonal, in Y's place, free since dA)
   x.par(C * C, [&](int idx) {
     const int i = idx / C, j = idx % C;
-    Ym[i * CP + j] = j < i ? dTm[i * CP + j] : (j > i ? dTm[j * CP + i] : 0.f);
+    Ym[i * MP + j] = j < i ? dTm[i * MP + j] : (j > i ? dTm[j * MP + i] : 0.f);
   });
   x.sync();
-  // the C x C parts of dq and dk, 4 x 8 tiles of (i, c) a thread (columns c0 + b K / 8):
-  //   dq += M1 K,  dk += M1^T Q + D K
+  // the C x C parts of dq and dk (on the device tensor-core products, on the host 4 x 8 tiles
+  // of (i, c) a thread, columns c0 + b K / 8):  dq += M1 K,  dk += M1^T Q + D K
+#if defined(__CUDA_ARCH__)
+  {  // M1 is zero above the diagonal: rows i < m0 + 16 take j < m0 + 16 in dq, j >= m0 in dk
+    const int lane = x.tid & 31;
+    const tc::Tiles<C, K> tl(x.tid >> 5);
+    constexpr int NTW = tc::Tiles<C, K>::NTW;
+    if (tl.any) {
+      float d[NTW][4] = {};
+      tc::mma_nn<NTW>(lane, dPm, MP, one, 1.f, Ks, KP, one, tl.m0, tl.n0, 0, tl.m0 + 16, d);
+#pragma unroll
+      for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            if (i < n) x.add(p.dqn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
+            d[j][e] = 0.f;
+          }
+      tc::mma_tn<NTW>(lane, dPm, MP, one, 1.f, Qs, KP, tl.m0, tl.n0, tl.m0, C, d);
+      tc::mma_nn<NTW>(lane, Ym, MP, one, 1.f, Ks, KP, one, tl.m0, tl.n0, 0, C, d);
+#pragma unroll
+      for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
+            if (i < n) x.add(p.dkn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
+          }
+    }
+  }
+#else
   x.par((C / 4) * (K / 8), [&](int t) {
     const int i0 = (t / (K / 8)) * 4, c0 = t % (K / 8);
     float dq[4][8] = {}, dk[4][8] = {};
@@ -1221,7 +1319,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     for (int j = 0; j < i0 + 4; ++j) {
       float m[4], kr[8];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) m[a] = dPm[(i0 + a) * CP + j];
+      for (int a = 0; a < 4; ++a) m[a] = dPm[(i0 + a) * MP + j];
 #pragma unroll
       for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
 #pragma unroll
@@ -1232,7 +1330,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     for (int j = i0; j < C; ++j) {
       float m[4], qr[8];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) m[a] = dPm[j * CP + i0 + a];
+      for (int a = 0; a < 4; ++a) m[a] = dPm[j * MP + i0 + a];
 #pragma unroll
       for (int b = 0; b < 8; ++b) qr[b] = Qs[j * KP + c0 + b * (K / 8)];
 #pragma unroll
@@ -1243,7 +1341,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     for (int j = 0; j < C; ++j) {
       float m[4], kr[8];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) m[a] = Ym[(i0 + a) * CP + j];
+      for (int a = 0; a < 4; ++a) m[a] = Ym[(i0 + a) * MP + j];
 #pragma unroll
       for (int b = 0; b < 8; ++b) kr[b] = Ks[j * KP + c0 + b * (K / 8)];
 #pragma unroll
@@ -1263,6 +1361,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
       }
     }
   });
+#endif
 }
 
 // Row r of q or k (token t = r / Hqk, head r % Hqk): the gradient of the unit-norm row taken

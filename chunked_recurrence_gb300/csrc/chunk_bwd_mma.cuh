@@ -80,17 +80,20 @@ struct Tiles {
 // The three forms below add to D, over k in [kbeg, kend) (multiples of 8), the products of
 // fp32 rows in shared memory; a triangular factor passes the range where it is nonzero.
 
-// D[m][n] += sum_k A[m][k] B[n][k]: A rows m0 .. (stride lda), B rows n0 + 8 j .. (ldb).
-template <int NTW>
-__device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const float *B, int ldb, int m0, int n0,
-                                       int kbeg, int kend, float (&d)[NTW][4]) {
+// D[m][n] += sum_k A[m][k] ka_k B[n][k]: A rows m0 .. (stride lda), with KA its column k
+// scaled by ka[k] (ka then holds kend entries; without KA it is not read); B rows n0 + 8 j ..
+// (ldb).
+template <int NTW, bool KA = false>
+__device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const float *ka, const float *B, int ldb,
+                                       int m0, int n0, int kbeg, int kend, float (&d)[NTW][4]) {
   const int g = lane >> 2, t = lane & 3;
   const float *a = A + (m0 + g) * lda + t;
   const float *b = B + (n0 + g) * ldb + t;
 #pragma unroll 2
   for (int k0 = kbeg; k0 < kend; k0 += 8) {
+    const float s0 = KA ? ka[k0 + t] : 1.f, s1 = KA ? ka[k0 + t + 4] : 1.f;
     FragA fa;
-    frag_a(fa, a[k0], a[8 * lda + k0], a[k0 + 4], a[8 * lda + k0 + 4]);
+    frag_a(fa, s0 * a[k0], s0 * a[8 * lda + k0], s1 * a[k0 + 4], s1 * a[8 * lda + k0 + 4]);
 #pragma unroll
     for (int j = 0; j < NTW; ++j) {
       FragB fb;
