@@ -30,6 +30,7 @@ struct DevExec {
 
 template <typename T>
 struct DevLoad {
+  static constexpr bool kRawTf32 = sizeof(T) == 2;  // bf16 values are exact in TF32
   __device__ __forceinline__ float operator()(const void *p, int64_t i) const {
     return to_f32<T>(reinterpret_cast<const T *>(p)[i]);
   }

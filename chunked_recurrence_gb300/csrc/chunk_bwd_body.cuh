@@ -92,7 +92,7 @@ struct Params {
 // shared memory of one block, in floats
 GDN_BWD_HD size_t prep_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 2 * (size_t)C * CP + 4 * C; }
 GDN_BWD_HD size_t walk_smem_floats(int K, int BV) {
-  return 2 * (size_t)C * (K + 4) + 2 * (size_t)BV * (K + 4) + 8 * (size_t)C * (BV + 4) + 2 * (size_t)C * CP + 8 * C;
+  return 2 * (size_t)C * (K + 4) + 2 * (size_t)BV * (K + 4) + 8 * (size_t)C * (BV + 4) + 2 * (size_t)C * CP + 12 * C;
 }
 GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 6 * (size_t)C * (C + 4) + 9 * C; }
 
@@ -408,6 +408,15 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
   float *dec = bex + C;        // [C] exp(gamma_last - gamma)
   float *prt = dec + C;        // [C] partial sums of <S, dS1>
   float *one = prt + C;        // [C] ones (a unit scale for the tensor-core products)
+  // with raw keys (below): 1/|k|, 1/|q| and the row scales that carry them
+  float *kin = one + C, *qin = kin + C, *dkn = qin + C, *bkn = dkn + C, *bqn = bkn + C;
+#if defined(__CUDA_ARCH__)
+  // bf16 inputs widened to fp32 are exact in TF32: the device keeps k and q raw and folds
+  // their norms into the tensor-core products' scales, which then need no split of k or q
+  constexpr bool RAW = LD::kRawTf32;
+#else
+  constexpr bool RAW = false;
+#endif
 
   const int qh = h / (Hv / p.Hqk), row0 = tile * BV;
   int64_t start, end;
@@ -502,11 +511,27 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       }
     }
     x.sync();
-    norm_and_cumsum<K, KP>(x, p, Ks, bwd ? Qs : nullptr, gam);
+    if constexpr (RAW) {  // the inverse norms, the rows left raw
+      x.par(bwd ? 2 * C : C, [&](int r) {
+        const float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
+        float ss = 0.f;
+        for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
+        (r < C ? kin : qin)[r % C] = p.l2norm ? 1.f / sqrtf(ss + kEps) : 1.f;
+      });
+      if (x.leader())
+        for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
+    } else {
+      norm_and_cumsum<K, KP>(x, p, Ks, bwd ? Qs : nullptr, gam);
+    }
     x.sync();
     x.par(C, [&](int i) {
       bex[i] = expf(gam[i]);
       dec[i] = expf(gam[C - 1] - gam[i]);
+      if (RAW) {
+        dkn[i] = dec[i] * kin[i];
+        bkn[i] = bex[i] * kin[i];
+        if (bwd) bqn[i] = bex[i] * qin[i];
+      }
     });
     x.sync();
   };
@@ -534,16 +559,17 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float d[NTW][4] = {};
-        tc::mma_nt<NTW>(lane, Ks, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, d);
+        tc::mma_nt<NTW, false, RAW>(lane, Ks, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = tc::frag_row(lane, tl.m0, e), v = tc::frag_col(lane, tl.n0, j, e);
-            const float w = Vs[i * VP + v] - bex[i] * d[j][e];
+            const float ks = RAW ? d[j][e] * kin[i] : d[j][e];
+            const float w = Vs[i * VP + v] - bex[i] * ks;
             Ws[i * VP + v] = w;
             fw[CV + (size_t)i * V + v] = w;
-            fw[2 * CV + (size_t)i * V + v] = d[j][e];
+            fw[2 * CV + (size_t)i * V + v] = ks;
           }
       }
     }
@@ -630,7 +656,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             d[j][e] = bex[C - 1] * Ss[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)];
-        tc::mma_tn<NTW>(lane, Us, VP, dec, 1.f, Ks, KP, tl.m0, tl.n0, 0, C, d);
+        tc::mma_tn<NTW, RAW>(lane, Us, VP, RAW ? dkn : dec, 1.f, Ks, KP, tl.m0, tl.n0, 0, C, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -686,15 +712,15 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float dq[NTW][4] = {}, dk[NTW][4] = {};
-        tc::mma_nt<NTW>(lane, Qs, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, dq);
-        tc::mma_nt<NTW>(lane, Ks, KP, nullptr, dSs, KP, tl.m0, tl.n0, 0, K, dk);
+        tc::mma_nt<NTW, false, RAW>(lane, Qs, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, dq);
+        tc::mma_nt<NTW, false, RAW>(lane, Ks, KP, nullptr, dSs, KP, tl.m0, tl.n0, 0, K, dk);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = tc::frag_row(lane, tl.m0, e), v = tc::frag_col(lane, tl.n0, j, e);
-            QSs[i * VP + v] = dq[j][e];
-            KdS[i * VP + v] = dk[j][e];
+            QSs[i * VP + v] = RAW ? dq[j][e] * qin[i] : dq[j][e];
+            KdS[i * VP + v] = RAW ? dk[j][e] * kin[i] : dk[j][e];
           }
       }
     }
@@ -1014,8 +1040,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             d[j][e] = bex[C - 1] * dSs[tc::frag_row(lane, tl.m0, e) * KP + tc::frag_col(lane, tl.n0, j, e)];
-        tc::mma_tn<NTW>(lane, Os, VP, bex, 1.f, Qs, KP, tl.m0, tl.n0, 0, C, d);
-        tc::mma_tn<NTW>(lane, Ws, VP, bex, -1.f, Ks, KP, tl.m0, tl.n0, 0, C, d);
+        tc::mma_tn<NTW, RAW>(lane, Os, VP, RAW ? bqn : bex, 1.f, Qs, KP, tl.m0, tl.n0, 0, C, d);
+        tc::mma_tn<NTW, RAW>(lane, Ws, VP, RAW ? bkn : bex, -1.f, Ks, KP, tl.m0, tl.n0, 0, C, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll

@@ -63,6 +63,25 @@ __device__ __forceinline__ void mma3(float (&d)[4], const FragA &a, const FragB 
   mma(d, a.h, b.h);
 }
 
+// An operand whose values are exact in TF32 (bf16 inputs widened to fp32: 8 significant bits)
+// needs no low part, and its product takes two MMAs.
+__device__ __forceinline__ void frag_a_exact(FragA &f, float a0, float a1, float a2, float a3) {
+  f.h[0] = __float_as_uint(a0);
+  f.h[1] = __float_as_uint(a1);
+  f.h[2] = __float_as_uint(a2);
+  f.h[3] = __float_as_uint(a3);
+}
+__device__ __forceinline__ void frag_b_exact(FragB &f, float b0, float b1) {
+  f.h[0] = __float_as_uint(b0);
+  f.h[1] = __float_as_uint(b1);
+}
+template <bool AX, bool BX>
+__device__ __forceinline__ void mma_x(float (&d)[4], const FragA &a, const FragB &b) {
+  if (!AX) mma(d, a.l, b.h);
+  if (!BX) mma(d, a.h, b.l);
+  mma(d, a.h, b.h);
+}
+
 // The warp's tiles of an M x N product (see above): its row tile m0, its first column tile
 // n0, and whether it has any.
 template <int M, int N>
@@ -83,9 +102,11 @@ struct Tiles {
 // D[m][n] += sum_k A[m][k] ka_k B[n][k]: A rows m0 .. (stride lda), with KA its column k
 // scaled by ka[k] (ka then holds kend entries; without KA it is not read); B rows n0 + 8 j ..
 // (ldb).
-template <int NTW, bool KA = false>
+// AX: A's values are exact in TF32 (no split; KA must then be off).
+template <int NTW, bool KA = false, bool AX = false>
 __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const float *ka, const float *B, int ldb,
                                        int m0, int n0, int kbeg, int kend, float (&d)[NTW][4]) {
+  static_assert(!(KA && AX), "a scaled operand is not exact");
   const int g = lane >> 2, t = lane & 3;
   const float *a = A + (m0 + g) * lda + t;
   const float *b = B + (n0 + g) * ldb + t;
@@ -93,12 +114,13 @@ __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const 
   for (int k0 = kbeg; k0 < kend; k0 += 8) {
     const float s0 = KA ? ka[k0 + t] : 1.f, s1 = KA ? ka[k0 + t + 4] : 1.f;
     FragA fa;
-    frag_a(fa, s0 * a[k0], s0 * a[8 * lda + k0], s1 * a[k0 + 4], s1 * a[8 * lda + k0 + 4]);
+    if (AX) frag_a_exact(fa, a[k0], a[8 * lda + k0], a[k0 + 4], a[8 * lda + k0 + 4]);
+    else frag_a(fa, s0 * a[k0], s0 * a[8 * lda + k0], s1 * a[k0 + 4], s1 * a[8 * lda + k0 + 4]);
 #pragma unroll
     for (int j = 0; j < NTW; ++j) {
       FragB fb;
       frag_b(fb, b[8 * j * ldb + k0], b[8 * j * ldb + k0 + 4]);
-      mma3(d[j], fa, fb);
+      mma_x<AX, false>(d[j], fa, fb);
     }
   }
 }
@@ -129,7 +151,8 @@ __device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const 
 
 // D[m][n] += sum_k mult ks_k A[k][m] B[k][n]: A stored by rows k (stride lda), so that the
 // operand is its transpose, row k scaled by ks[k]; B rows k (stride ldb), columns n0 + 8 j ..
-template <int NTW>
+// BX: B's values are exact in TF32 (no split).
+template <int NTW, bool BX = false>
 __device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const float *ks, float mult, const float *B,
                                        int ldb, int m0, int n0, int kbeg, int kend, float (&d)[NTW][4]) {
   const int g = lane >> 2, t = lane & 3;
@@ -143,8 +166,9 @@ __device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const 
 #pragma unroll
     for (int j = 0; j < NTW; ++j) {
       FragB fb;
-      frag_b(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
-      mma3(d[j], fa, fb);
+      if (BX) frag_b_exact(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
+      else frag_b(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
+      mma_x<false, BX>(d[j], fa, fb);
     }
   }
 }

@@ -24,6 +24,7 @@ struct HostExec {
 };
 
 struct HostLoad {
+  static constexpr bool kRawTf32 = false;
   float operator()(const void *p, int64_t i) const { return reinterpret_cast<const float *>(p)[i]; }
   void vec8(const void *p, int64_t i, float *out) const {
     for (int e = 0; e < 8; ++e) out[e] = reinterpret_cast<const float *>(p)[i + e];
