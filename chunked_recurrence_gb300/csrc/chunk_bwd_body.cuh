@@ -94,7 +94,7 @@ GDN_BWD_HD size_t prep_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 2 *
 GDN_BWD_HD size_t walk_smem_floats(int K, int BV) {
   return 2 * (size_t)C * (K + 4) + 2 * (size_t)BV * (K + 4) + 8 * (size_t)C * (BV + 4) + 2 * (size_t)C * CP + 12 * C;
 }
-GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 6 * (size_t)C * (C + 4) + 9 * C; }
+GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 6 * (size_t)C * (C + 4) + 11 * C; }
 
 GDN_BWD_FN int64_t seq_start(const Params &p, int s) { return p.cu ? (int64_t)p.cu[s] : (int64_t)s * p.row_T; }
 
@@ -293,12 +293,29 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   float *Zb = Am + C * CP;    // [C][CP]  Z, built row by row
   float *gam = Zb + C * CP;   // [C]
   float *bet = gam + C;       // [C]
+  float *kin = bet + C, *qin = kin + C;  // [C] each: 1/|k|, 1/|q| with raw keys
+#if defined(__CUDA_ARCH__)
+  constexpr bool RAW = LD::kRawTf32;  // k and q kept raw, their norms in kin / qin
+#else
+  constexpr bool RAW = false;
+#endif
   float *out = p.prep + ((size_t)slot * p.Hv + h) * kPrep;
   float *KGo = out + C * C, *QGo = out + 2 * C * C;
   load_keys<K, KP>(x, p, ld, Ks, Qs, t0, n, h / (p.Hv / p.Hqk));
   load_gates(x, p, gam, bet, t0, n, h);
   x.sync();
-  norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
+  if constexpr (RAW) {  // the inverse norms, the rows left raw
+    x.par(2 * C, [&](int r) {
+      const float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
+      float ss = 0.f;
+      for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
+      (r < C ? kin : qin)[r % C] = p.l2norm ? 1.f / sqrtf(ss + kEps) : 1.f;
+    });
+    if (x.leader())
+      for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
+  } else {
+    norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
+  }
   x.sync();
   // K K^T and Q K^T (on the device tensor-core products, on the host 4 x 4 tiles of (i, j) a
   // thread).  Gamma, KG, QG and A = diag(beta) KG follow in the tile's epilogue, which also
@@ -311,8 +328,8 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     if (tl.any) {
       float kk[NTW][4] = {}, qk[NTW][4] = {};
       if (tl.n0 <= tl.m0 + 15) {  // tiles wholly above the diagonal hold zeros
-        tc::mma_nt<NTW>(lane, Ks, KP, nullptr, Ks, KP, tl.m0, tl.n0, 0, K, kk);
-        tc::mma_nt<NTW>(lane, Qs, KP, nullptr, Ks, KP, tl.m0, tl.n0, 0, K, qk);
+        tc::mma_nt<NTW, false, RAW, RAW>(lane, Ks, KP, nullptr, Ks, KP, tl.m0, tl.n0, 0, K, kk);
+        tc::mma_nt<NTW, false, RAW, RAW>(lane, Qs, KP, nullptr, Ks, KP, tl.m0, tl.n0, 0, K, qk);
       }
 #pragma unroll
       for (int jt = 0; jt < NTW; ++jt)
@@ -320,10 +337,12 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
         for (int e = 0; e < 4; ++e) {
           const int i = tc::frag_row(lane, tl.m0, e), j = tc::frag_col(lane, tl.n0, jt, e);
           const float gij = j <= i ? expf(gam[i] - gam[j]) : 0.f;
-          const float kg = j < i ? kk[jt][e] * gij : 0.f;
+          const float kkv = RAW ? kk[jt][e] * kin[i] * kin[j] : kk[jt][e];
+          const float qkv = RAW ? qk[jt][e] * qin[i] * kin[j] : qk[jt][e];
+          const float kg = j < i ? kkv * gij : 0.f;
           Am[i * CP + j] = bet[i] * kg;
           KGo[i * C + j] = kg;
-          QGo[i * C + j] = j <= i ? qk[jt][e] * gij : 0.f;
+          QGo[i * C + j] = j <= i ? qkv * gij : 0.f;
         }
     }
   }
@@ -1116,6 +1135,12 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   float *dbt = db + C;         // [C] dL/dbeta
   float *dgm = dbt + C;        // [C] dL/dgamma, then dg
   float *one = dgm + C;        // [C] ones (a unit scale for the tensor-core products)
+  float *kin = one + C, *qin = kin + C;  // [C] each: 1/|k|, 1/|q| with raw keys
+#if defined(__CUDA_ARCH__)
+  constexpr bool RAW = LD::kRawTf32;  // k and q kept raw, their norms in kin / qin
+#else
+  constexpr bool RAW = false;
+#endif
   const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
   const float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
   if (p.vec8) {  // every fill of a phase in flight at once
@@ -1165,7 +1190,18 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     });
   }
   x.sync();
-  norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
+  if constexpr (RAW) {  // the inverse norms, the rows left raw
+    x.par(2 * C, [&](int r) {
+      const float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
+      float ss = 0.f;
+      for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
+      (r < C ? kin : qin)[r % C] = p.l2norm ? 1.f / sqrtf(ss + kEps) : 1.f;
+    });
+    if (x.leader())
+      for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
+  } else {
+    norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
+  }
   x.sync();
   x.par(C, [&](int i) {
     bex[i] = expf(gam[i]);
@@ -1317,7 +1353,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     constexpr int NTW = tc::Tiles<C, K>::NTW;
     if (tl.any) {
       float d[NTW][4] = {};
-      tc::mma_nn<NTW>(lane, dPm, MP, one, 1.f, Ks, KP, one, tl.m0, tl.n0, 0, tl.m0 + 16, d);
+      tc::mma_nn<NTW, RAW>(lane, dPm, MP, one, 1.f, Ks, KP, RAW ? kin : one, tl.m0, tl.n0, 0, tl.m0 + 16, d);
 #pragma unroll
       for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -1326,8 +1362,8 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
             if (i < n) x.add(p.dqn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
             d[j][e] = 0.f;
           }
-      tc::mma_tn<NTW>(lane, dPm, MP, one, 1.f, Qs, KP, tl.m0, tl.n0, tl.m0, C, d);
-      tc::mma_nn<NTW>(lane, Ym, MP, one, 1.f, Ks, KP, one, tl.m0, tl.n0, 0, C, d);
+      tc::mma_tn<NTW, RAW>(lane, dPm, MP, RAW ? qin : one, 1.f, Qs, KP, tl.m0, tl.n0, tl.m0, C, d);
+      tc::mma_nn<NTW, RAW>(lane, Ym, MP, one, 1.f, Ks, KP, RAW ? kin : one, tl.m0, tl.n0, 0, C, d);
 #pragma unroll
       for (int j = 0; j < NTW; ++j)
 #pragma unroll

@@ -102,8 +102,8 @@ struct Tiles {
 // D[m][n] += sum_k A[m][k] ka_k B[n][k]: A rows m0 .. (stride lda), with KA its column k
 // scaled by ka[k] (ka then holds kend entries; without KA it is not read); B rows n0 + 8 j ..
 // (ldb).
-// AX: A's values are exact in TF32 (no split; KA must then be off).
-template <int NTW, bool KA = false, bool AX = false>
+// AX, BX: A's (B's) values are exact in TF32 (no split; KA must then be off for A).
+template <int NTW, bool KA = false, bool AX = false, bool BX = false>
 __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const float *ka, const float *B, int ldb,
                                        int m0, int n0, int kbeg, int kend, float (&d)[NTW][4]) {
   static_assert(!(KA && AX), "a scaled operand is not exact");
@@ -119,15 +119,18 @@ __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const 
 #pragma unroll
     for (int j = 0; j < NTW; ++j) {
       FragB fb;
-      frag_b(fb, b[8 * j * ldb + k0], b[8 * j * ldb + k0 + 4]);
-      mma_x<AX, false>(d[j], fa, fb);
+      if (BX) frag_b_exact(fb, b[8 * j * ldb + k0], b[8 * j * ldb + k0 + 4]);
+      else frag_b(fb, b[8 * j * ldb + k0], b[8 * j * ldb + k0 + 4]);
+      mma_x<AX, BX>(d[j], fa, fb);
     }
   }
 }
 
 // D[m][n] += sum_k mult ra_m A[m][k] kb_k B[k][n]: A rows m0 .. (stride lda) scaled by ra (per
-// row), B rows k (stride ldb) scaled by kb (per row k), columns n0 + 8 j ..
-template <int NTW>
+// row), B rows k (stride ldb) scaled by kb (per row k), columns n0 + 8 j ..  BX: B's values
+// are exact in TF32 and unscaled (kb is not read), its k-scale then carried by A's columns
+// through kb instead.
+template <int NTW, bool BX = false>
 __device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const float *ra, float mult, const float *B,
                                        int ldb, const float *kb, int m0, int n0, int kbeg, int kend,
                                        float (&d)[NTW][4]) {
@@ -137,14 +140,16 @@ __device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const 
   const float r0 = mult * ra[m0 + g], r1 = mult * ra[m0 + g + 8];
 #pragma unroll 2
   for (int k0 = kbeg; k0 < kend; k0 += 8) {
-    FragA fa;
-    frag_a(fa, r0 * a[k0], r1 * a[8 * lda + k0], r0 * a[k0 + 4], r1 * a[8 * lda + k0 + 4]);
     const float s0 = kb[k0 + t], s1 = kb[k0 + t + 4];
+    FragA fa;
+    if (BX) frag_a(fa, r0 * s0 * a[k0], r1 * s0 * a[8 * lda + k0], r0 * s1 * a[k0 + 4], r1 * s1 * a[8 * lda + k0 + 4]);
+    else frag_a(fa, r0 * a[k0], r1 * a[8 * lda + k0], r0 * a[k0 + 4], r1 * a[8 * lda + k0 + 4]);
 #pragma unroll
     for (int j = 0; j < NTW; ++j) {
       FragB fb;
-      frag_b(fb, s0 * b[k0 * ldb + 8 * j], s1 * b[(k0 + 4) * ldb + 8 * j]);
-      mma3(d[j], fa, fb);
+      if (BX) frag_b_exact(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
+      else frag_b(fb, s0 * b[k0 * ldb + 8 * j], s1 * b[(k0 + 4) * ldb + 8 * j]);
+      mma_x<false, BX>(d[j], fa, fb);
     }
   }
 }
