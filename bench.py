@@ -353,7 +353,7 @@ def run_gpu_arm(args, ws, rank, local):
     bwd = None
     if not args.no_backward:
         bwd = run_backward_leg(crg, args, dev, stream, peaks)
-        bwd["vs_forward"] = round(bwd["ms"] / chunk_ms, 1)
+        bwd["vs_forward"] = round(bwd["ms"] / chunk_ms, 1) if bwd["T"] == wl.T else None
     dec = None
     if not args.no_decode:
         dec = run_decode_leg(crg, args, dev, stream, peaks)
@@ -647,8 +647,10 @@ def bwd_bytes(wl, n_tok, n_seq):
 def run_backward_leg(crg, args, dev, stream, peaks):
     """gdn_chunk_bwd on the 4B-shaped layer (same q, k, v, gates as the forward leg; d_o ~
     N(0, 1) fp32, no loss on h_T), timed with CUDA events on the launching stream, L2
-    flushed before each call."""
+    flushed before each call.  --bwd-tokens cuts the sequence (a small case for ncu)."""
     wl = synth.WORKLOADS["qwen35_4b_layer"]
+    if args.bwd_tokens != wl.T:
+        wl = wl.scaled(T=args.bwd_tokens)
     inp = synth.make_inputs(wl, device=dev, with_front_end=False)
     g, beta = crg.gdn_gate_prep(inp["a"], inp["b"], inp["A_log"], inp["dt_bias"])
     n_tok = inp["n_tok"]
@@ -668,7 +670,9 @@ def run_backward_leg(crg, args, dev, stream, peaks):
             ts.append(e0.elapsed_time(e1))
     ms = statistics.median(ts)
     nb = bwd_bytes(wl, n_tok, 1)
-    return {"workload": wl.name, "kernel": "gdn_chunk_bwd (chunk_bwd_prep_kernel, chunk_bwd_walk_kernel, chunk_bwd_grad_kernel, l2_back_kernel; fp32 CUDA cores)",
+    return {"workload": wl.name, "T": wl.T,
+            "kernel": "gdn_chunk_bwd (chunk_bwd_prep_kernel, chunk_bwd_walk_kernel, chunk_bwd_grad_kernel, "
+                      "l2_back_kernel; fp32 state, 3xTF32 mma.sync products)",
             "ms": round(ms, 3), "tokens_per_s": round(n_tok / (ms * 1e-3), 1), "bytes": nb,
             "achieved_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
             "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 5),
@@ -877,6 +881,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--bwd-tokens", type=int, default=8192, help="tokens of the backward leg (default: the full layer)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
