@@ -197,6 +197,9 @@ __global__ void __launch_bounds__(128, 4)
   const uint32_t tm = tbase;
   uint32_t ldp = 0, mp = 0;  // completed phases of ld_bar and bar
   if (kFront && blockIdx.x == 0 && tid == 0) atomicOr(p.status + 1, GDN_PATH_FRONT);
+  // every block is resident (the grid is one wave): the state scan may start its prologue
+  // on SMs this grid leaves, and waits for the whole grid before reading what it wrote
+  launch_dependents();
   // In front mode blocks claim groups of G consecutive items from a counter (G = the v-heads
   // of one q/k head) and walk each group in order: the group's first item convs the q/k
   // head's tiles and writes them out, and the later items load them back.
@@ -767,6 +770,7 @@ __global__ void __launch_bounds__(NTS, 1)
   __syncthreads();
   tc_fence_after();
   if (NORM) cluster_sync_all();  // the peers' barriers are initialised before any remote arrival
+  grid_dependency_wait();  // the operand kernel's records (and conv'd q, k) are complete and visible
   if (NORM && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0)
     atomicOr(p.status + 1, GDN_PATH_NORM);
   const uint32_t tm = sh.tbase;
@@ -1343,6 +1347,9 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
     mk = mkc;
   }
   const dim3 grid(cols / VS, sh.Hv, n_seqs);
+  // a programmatic dependent of the operand kernel only when that kernel ran (no items: no
+  // launch, and the previous kernel on the stream is someone else's)
+  const bool pdl = slots * (size_t)sh.Hv > 0;
   if (nm && !summary) {
     // the norm epilogue: the blocks of one (v-head, sequence) as one cluster
     sp.norm = 1;
@@ -1354,17 +1361,31 @@ static gdn_status run_scan(const void *q, const void *k, const void *v, const fl
     cfg.blockDim = dim3(NTS);
     cfg.dynamicSmemBytes = kScanSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = grid.x;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, chunk_scan_kernel<true>, mq, mk, sp) != cudaSuccess) return GDN_ERR_CUDA;
     return launch_status();
   }
-  chunk_scan_kernel<false><<<grid, NTS, kScanSmem, st>>>(mq, mk, sp);
+  // launched as a programmatic dependent of the operand kernel: its launch and prologue overlap
+  // that kernel's last items
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NTS);
+  cfg.dynamicSmemBytes = kScanSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, chunk_scan_kernel<false>, mq, mk, sp) != cudaSuccess) return GDN_ERR_CUDA;
   return launch_status();
 }
 

@@ -62,6 +62,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   return false;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on the stream, when
+// it was launched with programmatic stream serialization, start once every block of this
+// grid has issued it; grid_dependency_wait (in that next kernel) returns once the previous
+// grid has completed and its memory operations are visible.  Without the launch attribute
+// the wait returns at once.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Like mbar_wait (call it with a compile-time max_iters), but a wait that misses its first
 // poll gives up at once when `quit` is set (a test mode).  The flag is read only on that
 // slow path, so a wait whose phase has completed costs what mbar_wait does.
