@@ -226,7 +226,8 @@ gdn_status gdn_segment_summary(const void *k, const void *v, const float *g, con
  * d_o [tokens, Hv, V] and dh_T [n_seqs, Hv, V, K] (NULL: no loss on h_T) are fp32,
  * as are all outputs; q, k, v are of shape->dtype with the strides of gdn_shape.
  * K is 32, 64 or 128; V a multiple of 16 up to 256 (else GDN_ERR_UNSUPPORTED).
- * fp32 CUDA-core kernels, all on the stream: a chunk-parallel prep of each chunk's
+ * fp32 state and gradients, products on the tensor cores (TF32 with each fp32 operand split
+ * in two, fp32-level accuracy); kernels, all on the stream: a chunk-parallel prep of each chunk's
  * state-independent matrices; a walk, one block per (32 or 16 state rows, v-head,
  * sequence), that recomputes its rows' chunk-start states and then walks the chunks
  * backward; a chunk-parallel pass for the gradients linear in the walk's per-chunk
