@@ -59,7 +59,8 @@ namespace gdn_bwd {
 constexpr int C = 64;  // tokens per chunk
 constexpr int CP = C + 1;
 constexpr float kEps = 1e-6f;  // q/k L2 norm: x / sqrt(sum x^2 + eps)
-constexpr size_t kPrep = 3 * (size_t)C * C;         // floats per (chunk, v-head): Z, KG, QG
+constexpr size_t kPrep = 3 * (size_t)C * C + 5 * C;  // floats per (chunk, v-head): Z, KG, QG; 5 vectors
+constexpr size_t kPrepVec = 3 * (size_t)C * C;       // offset of the vectors gamma, b, d, 1/|k|, 1/|q|
 constexpr size_t kSums = 2 * (size_t)C * C + 2 * C;  // floats per (chunk, v-head): dP, dT, dd, db
 
 struct Params {
@@ -80,7 +81,8 @@ struct Params {
   // chunk slots: chunk c of sequence s is slot s + start_s / C + c (distinct for every chunk)
   float *states;    // [slot][Hv][V][K]: chunk-start states
   float *fw;        // [slot][Hv][3][C][V]: the forward sweep's U', V - diag(b) K S^T and K S^T
-  float *prep;      // [slot][Hv][kPrep]: Z, KG, QG, each [C][C] row-major
+  float *prep;      // [slot][Hv][kPrep]: Z, KG, QG ([C][C] row-major each), then gamma, b = exp(gamma),
+                    // d = exp(gamma_last - gamma), 1/|k|, 1/|q| ([C] each)
   float *sums;      // [slot][Hv][kSums]: dP [C][C], dT [C][C], dd [C], db [C]; zero before the walk
   float *dqn, *dkn; // [n_tok][Hqk][K]: gradients of the unit-norm (or raw) q and k, accumulated
   float *dv;        // [n_tok][Hv][V]
@@ -265,8 +267,9 @@ GDN_BWD_FN void load_gates(X &x, const Params &p, float *gam, float *bet, int64_
 
 // After the loads' barrier: unit-norm rows of k (and q), gamma = the inclusive cumsum of g.
 // The rows past n are zero and stay zero; gamma past n repeats the last token's.
+// rin (optional, 2 C floats): the rows' inverse norms, k rows then q rows (1 without the norm).
 template <int K, int KP = K + 1, class X>
-GDN_BWD_FN void norm_and_cumsum(X &x, const Params &p, float *Ks, float *Qs, float *gam) {
+GDN_BWD_FN void norm_and_cumsum(X &x, const Params &p, float *Ks, float *Qs, float *gam, float *rin = nullptr) {
   if (p.l2norm) {
     x.par(Qs ? 2 * C : C, [&](int r) {
       float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
@@ -274,7 +277,10 @@ GDN_BWD_FN void norm_and_cumsum(X &x, const Params &p, float *Ks, float *Qs, flo
       for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
       const float inv = 1.f / sqrtf(ss + kEps);
       for (int c = 0; c < K; ++c) row[c] *= inv;
+      if (rin) rin[r] = inv;
     });
+  } else if (rin) {
+    x.par(Qs ? 2 * C : C, [&](int r) { rin[r] = 1.f; });
   }
   if (x.leader())
     for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
@@ -293,7 +299,7 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   float *Zb = Am + C * CP;    // [C][CP]  Z, built row by row
   float *gam = Zb + C * CP;   // [C]
   float *bet = gam + C;       // [C]
-  float *kin = bet + C, *qin = kin + C;  // [C] each: 1/|k|, 1/|q| with raw keys
+  float *kin = bet + C, *qin = kin + C;  // [C] each: 1/|k|, 1/|q|
 #if defined(__CUDA_ARCH__)
   constexpr bool RAW = LD::kRawTf32;  // k and q kept raw, their norms in kin / qin
 #else
@@ -314,7 +320,7 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     if (x.leader())
       for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
   } else {
-    norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
+    norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam, kin);  // qin follows kin
   }
   x.sync();
   // K K^T and Q K^T (on the device tensor-core products, on the host 4 x 4 tiles of (i, j) a
@@ -398,6 +404,15 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     x.sync();
   }
   x.par(C * C, [&](int idx) { out[idx] = Zb[(idx / C) * CP + idx % C]; });
+  // gamma, b, d and the inverse norms, for the walk and grad
+  x.par(C, [&](int i) {
+    float *vo = out + kPrepVec;
+    vo[i] = gam[i];
+    vo[C + i] = expf(gam[i]);
+    vo[2 * C + i] = expf(gam[C - 1] - gam[i]);
+    vo[3 * C + i] = kin[i];
+    vo[4 * C + i] = qin[i];
+  });
 }
 
 // ---- walk: the state-dependent steps of BV state rows of one v-head, chunk by chunk
@@ -451,8 +466,8 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 
   // the chunk's inputs: k (and q), the block's v columns (forward) or scale * dO (backward),
   // the gates, Z (and QG) from prep, and in the backward sweep the block's chunk-start
-  // state and the forward sweep's tiles; then the norm, gamma, b and d.  Ends on a
-  // barrier.  With vector loads every fill of a phase is in flight at once (two phases
+  // state and the forward sweep's tiles; then the norm, gamma, b and d (with raw keys b, d and
+  // the inverse norms come from prep).  Everything but the raw-key scales is ready on return.  With vector loads every fill of a phase is in flight at once (two phases
   // backward, one forward).
   auto load = [&](int64_t slot, int64_t t0, int n, bool bwd) {
     const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
@@ -486,11 +501,21 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         fq.load(ld, t, p.q, qb, p.qs, n);
         const bool gi = t < C && t < n;
         const float gv = gi ? p.g[(t0 + t) * Hv + h] : 0.f, bv = gi ? p.beta[(t0 + t) * Hv + h] : 0.f;
+        float pv[4] = {};  // with raw keys: b, d, 1/|k|, 1/|q| from prep
+        if (RAW && t < C)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pv[u] = pr[kPrepVec + (u + 1) * C + t];
         fk.store(t, Ks, KP);
         fq.store(t, Qs, KP);
         if (t < C) {
           gam[t] = gv;
           bet[t] = bv;
+          if (RAW) {
+            bex[t] = pv[0];
+            dec[t] = pv[1];
+            kin[t] = pv[2];
+            qin[t] = pv[3];
+          }
         }
       });
     } else if (p.vec8) {
@@ -503,12 +528,21 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         fz.load(t, pr, C, C);
         const bool gi = t < C && t < n;
         const float gv = gi ? p.g[(t0 + t) * Hv + h] : 0.f, bv = gi ? p.beta[(t0 + t) * Hv + h] : 0.f;
+        float pv[3] = {};  // with raw keys: b, d, 1/|k| from prep
+        if (RAW && t < C)
+#pragma unroll
+          for (int u = 0; u < 3; ++u) pv[u] = pr[kPrepVec + (u + 1) * C + t];
         fk.store(t, Ks, KP);
         fv.store(t, Vs, VP);
         fz.store(t, Zm, CP);
         if (t < C) {
           gam[t] = gv;
           bet[t] = bv;
+          if (RAW) {
+            bex[t] = pv[0];
+            dec[t] = pv[1];
+            kin[t] = pv[2];
+          }
         }
       });
     } else {
@@ -520,6 +554,13 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
         else Vs[r * VP + j] = in ? ld(p.v, (t0 + r) * p.vs + (int64_t)h * V + row0 + j) : 0.f;
       });
       load_gates(x, p, gam, bet, t0, n, h);
+      if (RAW)
+        x.par(C, [&](int i) {
+          bex[i] = pr[kPrepVec + C + i];
+          dec[i] = pr[kPrepVec + 2 * C + i];
+          kin[i] = pr[kPrepVec + 3 * C + i];
+          qin[i] = pr[kPrepVec + 4 * C + i];
+        });
       copy_block<C, C>(x, pr, C, Zm, CP);
       if (bwd) {
         copy_block<C, C>(x, pr + 2 * C * C, C, QGm, CP);
@@ -530,29 +571,24 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       }
     }
     x.sync();
-    if constexpr (RAW) {  // the inverse norms, the rows left raw
-      x.par(bwd ? 2 * C : C, [&](int r) {
-        const float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
-        float ss = 0.f;
-        for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
-        (r < C ? kin : qin)[r % C] = p.l2norm ? 1.f / sqrtf(ss + kEps) : 1.f;
-      });
-      if (x.leader())
-        for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
-    } else {
-      norm_and_cumsum<K, KP>(x, p, Ks, bwd ? Qs : nullptr, gam);
-    }
-    x.sync();
-    x.par(C, [&](int i) {
-      bex[i] = expf(gam[i]);
-      dec[i] = expf(gam[C - 1] - gam[i]);
-      if (RAW) {
+    if constexpr (RAW) {
+      // b, d and the inverse norms came with the fill (prep computed them once per chunk and
+      // head); the scales that carry the norms into the state updates are read two phases on,
+      // past the next barrier
+      x.par(C, [&](int i) {
         dkn[i] = dec[i] * kin[i];
         bkn[i] = bex[i] * kin[i];
         if (bwd) bqn[i] = bex[i] * qin[i];
-      }
-    });
-    x.sync();
+      });
+    } else {
+      norm_and_cumsum<K, KP>(x, p, Ks, bwd ? Qs : nullptr, gam);
+      x.sync();
+      x.par(C, [&](int i) {
+        bex[i] = expf(gam[i]);
+        dec[i] = expf(gam[C - 1] - gam[i]);
+      });
+      x.sync();
+    }
   };
 
   // ---- forward sweep: the chunk-start state of every chunk, for this block's rows
@@ -1169,16 +1205,34 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
       fq.load(ld, t, p.q, t0 * p.qs + (int64_t)qh * K, p.qs, n);
       const bool gi = t < C && t < n;
       const float gv = gi ? p.g[(t0 + t) * Hv + h] : 0.f, bv = gi ? p.beta[(t0 + t) * Hv + h] : 0.f;
+      float pv[5] = {};  // with raw keys: gamma, b, d, 1/|k|, 1/|q| from prep
+      if (RAW && t < C)
+#pragma unroll
+        for (int u = 0; u < 5; ++u) pv[u] = pr[kPrepVec + u * C + t];
       fk.store(t, Ks, KP);
       fq.store(t, Qs, KP);
       if (t < C) {
-        gam[t] = gv;
+        gam[t] = RAW ? pv[0] : gv;
         bet[t] = bv;
+        if (RAW) {
+          bex[t] = pv[1];
+          dec[t] = pv[2];
+          kin[t] = pv[3];
+          qin[t] = pv[4];
+        }
       }
     });
   } else {
     load_keys<K, KP>(x, p, ld, Ks, Qs, t0, n, qh);
     load_gates(x, p, gam, bet, t0, n, h);
+    if (RAW)  // after load_gates' raw g, by the same item
+      x.par(C, [&](int i) {
+        gam[i] = pr[kPrepVec + i];
+        bex[i] = pr[kPrepVec + C + i];
+        dec[i] = pr[kPrepVec + 2 * C + i];
+        kin[i] = pr[kPrepVec + 3 * C + i];
+        qin[i] = pr[kPrepVec + 4 * C + i];
+      });
     copy_block<C, C>(x, pr, C, Zm, MP);
     copy_block<C, C>(x, pr + C * C, C, KGm, MP);
     copy_block<C, C>(x, pr + 2 * C * C, C, QGm, MP);
@@ -1190,22 +1244,15 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     });
   }
   x.sync();
-  if constexpr (RAW) {  // the inverse norms, the rows left raw
-    x.par(2 * C, [&](int r) {
-      const float *row = r < C ? Ks + r * KP : Qs + (r - C) * KP;
-      float ss = 0.f;
-      for (int c = 0; c < K; ++c) ss = fmaf(row[c], row[c], ss);
-      (r < C ? kin : qin)[r % C] = p.l2norm ? 1.f / sqrtf(ss + kEps) : 1.f;
-    });
-    if (x.leader())
-      for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
-  } else {
+  if constexpr (!RAW) {  // with raw keys gamma, b, d and the inverse norms came from prep
     norm_and_cumsum<K, KP>(x, p, Ks, Qs, gam);
+    x.sync();
   }
-  x.sync();
   x.par(C, [&](int i) {
-    bex[i] = expf(gam[i]);
-    dec[i] = expf(gam[C - 1] - gam[i]);
+    if (!RAW) {
+      bex[i] = expf(gam[i]);
+      dec[i] = expf(gam[C - 1] - gam[i]);
+    }
     one[i] = 1.f;
   });
   // dbeta from T = Z diag(beta): colsum(dT * Z)

@@ -176,10 +176,13 @@ def test_chunk_bwd_argument_errors_return_before_launch(lib):
     sh = _shape()
     need = lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(sh))
     # over (1 + 2) chunk slots x 4 heads: states of 128 x 128 fp32, the forward sweep's three
-    # 64 x 128 fp32 tiles, prep's Z, KG and QG (3 x 64 x 64 fp32), the walk's sums dP, dT
-    # (2 x 64 x 64) and dd, db (2 x 64); then two q/k accumulators of 128 x 2 x 128
+    # 64 x 128 fp32 tiles, prep's Z, KG and QG (3 x 64 x 64 fp32) and five 64-vectors, the
+    # walk's sums dP, dT (2 x 64 x 64) and dd, db (2 x 64); then two q/k accumulators of
+    # 128 x 2 x 128 (each part rounded up to 256 bytes)
     slots_h = 3 * 4
-    assert need == (256 + slots_h * 128 * 128 * 4 + slots_h * 3 * 64 * 128 * 4 + slots_h * 3 * 64 * 64 * 4
+    r256 = lambda b: (b + 255) // 256 * 256
+    assert need == (256 + slots_h * 128 * 128 * 4 + slots_h * 3 * 64 * 128 * 4
+                    + r256(slots_h * (3 * 64 * 64 + 5 * 64) * 4)
                     + slots_h * (2 * 64 * 64 + 2 * 64) * 4 + 2 * 128 * 2 * 128 * 4)
     assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(K=96))) == 0
     assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_shape(V=40))) == 0

@@ -94,3 +94,26 @@ def test_chunk_bwd_fp32_unaligned_inputs(crg):
                             cu_seqlens=torch.from_numpy(cu).to(DEV), scale=0.4, l2norm_qk=True)
     torch.cuda.synchronize()
     _check(got, ref, "fp32 unaligned")
+
+
+def test_chunk_bwd_bf16_unaligned_inputs(crg):
+    """bf16 q, k, v one element (2 bytes) off a 16-byte boundary and d_o 4 bytes off: the
+    element-wise loads with raw bf16 keys, against the oracle on the same bf16 values."""
+    q, k, v, g, beta, h0, do, dhT = _case(95, 150, 2, 4, 64, 32, 1)
+    bf = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    qb, kb, vb = bf(q), bf(k), bf(v)
+    f64 = lambda x: x.double().numpy()
+    ref = oracle.gdn_bwd(f64(qb), f64(kb), f64(vb), g, beta, do, dhT, h0, B=1, scale=0.2, l2norm_qk=True)
+
+    def off(x):  # the same values in a buffer that starts one element past an aligned address
+        buf = torch.empty(x.numel() + 1, dtype=x.dtype, device=DEV)
+        view = buf[1:].view(x.shape)
+        view.copy_(x.to(DEV))
+        assert view.data_ptr() % 16 != 0
+        return view
+
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV)
+    got = crg.gdn_chunk_bwd(off(qb), off(kb), off(vb), t(g), t(beta), off(t(do)), t(dhT), t(h0), B=1, scale=0.2,
+                            l2norm_qk=True)
+    torch.cuda.synchronize()
+    _check(got, ref, "bf16 unaligned")
