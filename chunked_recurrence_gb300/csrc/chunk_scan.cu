@@ -126,36 +126,41 @@ __device__ __forceinline__ void front_weights(const OpParams &p, int64_t chan, u
 // Y = (I + A)^-1 for the strictly lower 64 x 64 A in X, by forward substitution swept
 // by columns of A: y_i = delta_ij - sum_{k<i} A_ik y_k, and once row k of Y is final every
 // row below it takes the rank-1 term -A_ik Y_kj.  Each thread keeps an 8 x 4 tile of Y in
-// registers: rows rg + 8 m (m = 0..7) and columns 4 cg + c (c = 0..3), with rg = lane % 8
-// and cg = 4 warp + lane / 8, so the eight owners of one column group sit in one warp.
-// Step k reads row k's four values from their owner (lane k % 8 of the group) by shuffle
-// and A_ik for the thread's rows below k (one shared load each, shared by its 4 columns).
-// No barrier between steps.  Y is left in X, row-major, zero above the diagonal.
+// registers: rows rg + 8 m (m = 0..7) and columns 16 a + cj (a = 0..3), one in each
+// 16-column block, with rg = lane % 8 and cj = 4 warp + lane / 8, so the eight owners of
+// one column set sit in one warp.  Step k reads row k's values from their owner (lane k % 8
+// of the group) by shuffle and A_ik for the thread's rows below k (one shared load each,
+// shared by its columns).  Row k of Y is zero right of column k, so step k touches only
+// the column blocks a <= k / 16: with the loop unrolled that bound, like the row bound,
+// is fixed at compile time, the same for every warp (about half the FMAs of all four
+// columns at every step).  No barrier between steps.  Y is left in X, row-major, zero
+// above the diagonal.
 __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
-  const int lane = tid & 31, rg = lane & 7, cg = (tid >> 5) * 4 + (lane >> 3);
+  const int lane = tid & 31, rg = lane & 7, cj = (tid >> 5) * 4 + (lane >> 3);
   float y[8][4];
 #pragma unroll
   for (int m = 0; m < 8; ++m)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) y[m][c] = (rg + 8 * m == 4 * cg + c) ? 1.f : 0.f;
+    for (int a = 0; a < 4; ++a) y[m][a] = (rg + 8 * m == 16 * a + cj) ? 1.f : 0.f;
   const float *xr = X + rg * kXP;
 #pragma unroll
   for (int k = 0; k < C - 1; ++k) {
     float yk[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) yk[c] = __shfl_sync(0xffffffffu, y[k >> 3][c], (k & 7) | (lane & 24));
+    for (int a = 0; a <= (k >> 4); ++a) yk[a] = __shfl_sync(0xffffffffu, y[k >> 3][a], (k & 7) | (lane & 24));
     // rows rg + 8 m with m < k / 8 lie above row k: A_ik = 0 there (and A_kk = 0)
 #pragma unroll
     for (int m = k >> 3; m < 8; ++m) {
-      const float a = xr[8 * m * kXP + k];
+      const float av = xr[8 * m * kXP + k];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) y[m][c] = fmaf(-a, yk[c], y[m][c]);
+      for (int a = 0; a <= (k >> 4); ++a) y[m][a] = fmaf(-av, yk[a], y[m][a]);
     }
   }
   __syncthreads();  // every read of A is done
 #pragma unroll
   for (int m = 0; m < 8; ++m)
-    *reinterpret_cast<float4 *>(X + (rg + 8 * m) * kXP + 4 * cg) = make_float4(y[m][0], y[m][1], y[m][2], y[m][3]);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) X[(rg + 8 * m) * kXP + 16 * a + cj] = y[m][a];
   __syncthreads();
 }
 
