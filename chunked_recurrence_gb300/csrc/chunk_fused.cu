@@ -249,37 +249,36 @@ __device__ __forceinline__ bool decode_unit(const FfParams &p, int ci, int pos, 
 
 // Y = (I + A)^-1 for the strictly lower 64 x 64 A in X (row stride kXP), by forward
 // substitution swept over the columns of A; each of the lane's 128 threads keeps an
-// 8 x 4 tile of Y (rows rg + 8 m, columns 4 cg + c) and reads row k of Y from its owner by
-// shuffle.  Y is left in X, zero above the diagonal.  `bar` syncs the lane's threads.
+// 8 x 4 tile of Y (rows rg + 8 m, columns 16 a + cj: one in each 16-column block) and reads
+// row k of Y from its owner by shuffle.  Row k is zero right of column k, so step k updates
+// only the blocks a <= k / 16, a bound fixed at compile time and the same for every warp.
+// Y is left in X, zero above the diagonal.  `bar` syncs the lane's threads.
 template <typename Bar>
 __device__ __forceinline__ void invert_unit_lower(float *X, int tid, Bar bar) {
-  const int lane = tid & 31, rg = lane & 7, cg = (tid >> 5) * 4 + (lane >> 3);
+  const int lane = tid & 31, rg = lane & 7, cj = (tid >> 5) * 4 + (lane >> 3);
   float y[8][4];
 #pragma unroll
   for (int m = 0; m < 8; ++m)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) y[m][c] = (rg + 8 * m == 4 * cg + c) ? 1.f : 0.f;
+    for (int a = 0; a < 4; ++a) y[m][a] = (rg + 8 * m == 16 * a + cj) ? 1.f : 0.f;
   const float *xr = X + rg * kXP;
-  // Y_kj = 0 for j > k: the warp's 16 columns (16 w .. 16 w + 15) take no update from the
-  // steps before its first column (a warp-uniform skip)
-  const int k0 = (tid >> 5) * 16;
 #pragma unroll
   for (int k = 0; k < C - 1; ++k) {
-    if (k < k0) continue;
     float yk[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) yk[c] = __shfl_sync(0xffffffffu, y[k >> 3][c], (k & 7) | (lane & 24));
+    for (int a = 0; a <= (k >> 4); ++a) yk[a] = __shfl_sync(0xffffffffu, y[k >> 3][a], (k & 7) | (lane & 24));
 #pragma unroll
     for (int m = k >> 3; m < 8; ++m) {
-      const float a = xr[8 * m * kXP + k];
+      const float av = xr[8 * m * kXP + k];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) y[m][c] = fmaf(-a, yk[c], y[m][c]);
+      for (int a = 0; a <= (k >> 4); ++a) y[m][a] = fmaf(-av, yk[a], y[m][a]);
     }
   }
   bar();
 #pragma unroll
   for (int m = 0; m < 8; ++m)
-    *reinterpret_cast<float4 *>(X + (rg + 8 * m) * kXP + 4 * cg) = make_float4(y[m][0], y[m][1], y[m][2], y[m][3]);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) X[(rg + 8 * m) * kXP + 16 * a + cj] = y[m][a];
   bar();
 }
 

@@ -128,13 +128,16 @@ __device__ __forceinline__ void front_weights(const OpParams &p, int64_t chan, u
 // row below it takes the rank-1 term -A_ik Y_kj.  Each thread keeps an 8 x 4 tile of Y in
 // registers: rows rg + 8 m (m = 0..7) and columns 16 a + cj (a = 0..3), one in each
 // 16-column block, with rg = lane % 8 and cj = 4 warp + lane / 8, so the eight owners of
-// one column set sit in one warp.  Step k reads row k's values from their owner (lane k % 8
-// of the group) by shuffle and A_ik for the thread's rows below k (one shared load each,
-// shared by its columns).  Row k of Y is zero right of column k, so step k touches only
-// the column blocks a <= k / 16: with the loop unrolled that bound, like the row bound,
-// is fixed at compile time, the same for every warp (about half the FMAs of all four
-// columns at every step).  No barrier between steps.  Y is left in X, row-major, zero
-// above the diagonal.
+// one column set sit in one warp.
+// The sweep takes the rows four at a time, k = 4 b .. 4 b + 3: every thread reads those
+// rows (updated through row k - 1) from their owners by shuffle, finishes them among
+// themselves (rows k + 1 .. k + 3 take the terms of rows k .. k + 2: six FMAs a column),
+// and then applies all four to its own rows as y_i -= sum_j A_ij Y_j, with A_i,k..k+3 one
+// 16-byte load.  A_ij = 0 for j >= i, so the same update leaves rows <= k unchanged and
+// turns rows k + 1 .. k + 3 into their final values.  Rows of Y are zero right of their
+// diagonal, so block b touches only the column blocks a <= k / 16, a bound fixed at compile
+// time with the loop unrolled, the same for every warp.  No barrier between steps.  Y is
+// left in X, row-major, zero above the diagonal.
 __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
   const int lane = tid & 31, rg = lane & 7, cj = (tid >> 5) * 4 + (lane >> 3);
   float y[8][4];
@@ -144,16 +147,28 @@ __device__ __forceinline__ void invert_unit_lower(float *X, int tid) {
     for (int a = 0; a < 4; ++a) y[m][a] = (rg + 8 * m == 16 * a + cj) ? 1.f : 0.f;
   const float *xr = X + rg * kXP;
 #pragma unroll
-  for (int k = 0; k < C - 1; ++k) {
-    float yk[4];
+  for (int k = 0; k < C; k += 4) {
+    const int m0 = k >> 3, na = (k >> 4) + 1;
+    float z[4][4];
 #pragma unroll
-    for (int a = 0; a <= (k >> 4); ++a) yk[a] = __shfl_sync(0xffffffffu, y[k >> 3][a], (k & 7) | (lane & 24));
-    // rows rg + 8 m with m < k / 8 lie above row k: A_ik = 0 there (and A_kk = 0)
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int m = k >> 3; m < 8; ++m) {
-      const float av = xr[8 * m * kXP + k];
+      for (int a = 0; a < na; ++a) z[j][a] = __shfl_sync(0xffffffffu, y[m0][a], ((k + j) & 7) | (lane & 24));
+    const float4 r1 = *reinterpret_cast<const float4 *>(X + (k + 1) * kXP + k);
+    const float4 r2 = *reinterpret_cast<const float4 *>(X + (k + 2) * kXP + k);
+    const float4 r3 = *reinterpret_cast<const float4 *>(X + (k + 3) * kXP + k);
 #pragma unroll
-      for (int a = 0; a <= (k >> 4); ++a) y[m][a] = fmaf(-av, yk[a], y[m][a]);
+    for (int a = 0; a < na; ++a) {
+      z[1][a] = fmaf(-r1.x, z[0][a], z[1][a]);
+      z[2][a] = fmaf(-r2.y, z[1][a], fmaf(-r2.x, z[0][a], z[2][a]));
+      z[3][a] = fmaf(-r3.z, z[2][a], fmaf(-r3.y, z[1][a], fmaf(-r3.x, z[0][a], z[3][a])));
+    }
+#pragma unroll
+    for (int m = m0; m < 8; ++m) {
+      const float4 av = *reinterpret_cast<const float4 *>(xr + 8 * m * kXP + k);
+#pragma unroll
+      for (int a = 0; a < na; ++a)
+        y[m][a] = fmaf(-av.w, z[3][a], fmaf(-av.z, z[2][a], fmaf(-av.y, z[1][a], fmaf(-av.x, z[0][a], y[m][a]))));
     }
   }
   __syncthreads();  // every read of A is done
@@ -173,7 +188,9 @@ __global__ void __launch_bounds__(128, 4)
   constexpr uint32_t kCols = (V <= 128) ? 128u : 256u;
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-  __shared__ float gam[C], bex[C], dec[C], alf[C + 1], kinv[C], qinv[C], bet[C];
+  // per-token vectors, 16-byte aligned so that runs of four load as one: gam, then
+  // bex = b, dec = d, als[j] = exp(g_{j+1}) (1 at j = C - 1), 1/|k|, 1/|q|, beta, b/|k|
+  __shared__ __align__(16) float gam[C], bex[C], dec[C], als[C], kinv[C], qinv[C], bet[C], bk[C];
   __shared__ float blast_s;
   __shared__ uint64_t bar, ld_bar;
   __shared__ uint32_t tbase;
@@ -233,8 +250,16 @@ __global__ void __launch_bounds__(128, 4)
   }
   const int jv = jg++;  // this item's place in its group
   const int64_t item = group * G + jv;
-  const int h = (int)(item % p.Hv);
-  const int64_t slot = item / p.Hv;
+  int h;
+  int64_t slot;
+  if (p.n_items <= 0x7fffffff) {  // 32-bit division (the 64-bit one is a long software routine)
+    const uint32_t it = (uint32_t)item, hv = (uint32_t)p.Hv;
+    slot = it / hv;
+    h = (int)(it - (uint32_t)slot * hv);
+  } else {
+    h = (int)(item % p.Hv);
+    slot = item / p.Hv;
+  }
   const int qh = h / (p.Hv / p.Hqk);
   int lo = 0, hi = p.n_seqs - 1;  // sequence of this slot: largest s with slot_base(s) <= slot
   while (lo < hi) {
@@ -401,11 +426,13 @@ __global__ void __launch_bounds__(128, 4)
     bex[2 * lane + 1] = expf(gb);
     dec[2 * lane] = expf(last - ga);
     dec[2 * lane + 1] = expf(last - gb);
-    alf[2 * lane] = expf(g0);
-    alf[2 * lane + 1] = expf(g1);
+    if (lane > 0) als[2 * lane - 1] = expf(g0);
+    als[2 * lane] = expf(g1);
+    bk[2 * lane] = bex[2 * lane] * kinv[2 * lane];
+    bk[2 * lane + 1] = bex[2 * lane + 1] * kinv[2 * lane + 1];
     if (lane == 31) {
       blast_s = expf(last);
-      alf[C] = 1.f;
+      als[C - 1] = 1.f;
     }
   }
   __syncthreads();
@@ -441,7 +468,7 @@ __global__ void __launch_bounds__(128, 4)
     float gprod = 1.f, vd = 0.f;
 #pragma unroll
     for (int j = C - 1; j >= 0; --j) {
-      const float aj = alf[j + 1], kj = kinv[j];
+      const float aj = als[j], kj = kinv[j];
       vd = (j == i) ? r64[j] : vd;
       if (j < i) gprod *= aj;
       r64[j] = (j < i) ? bi * kj * gprod * r64[j] : 0.f;
@@ -479,10 +506,15 @@ __global__ void __launch_bounds__(128, 4)
       t[4 * m + 3] = a.w;
     }
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      const float bu = bet[cb + u];
-      t[u] = (cb + u <= r) ? t[u] * bu : 0.f;
-      cf[u] = bex[cb + u] * kinv[cb + u];
+    for (int m = 0; m < 8; ++m) {
+      const float4 b4 = reinterpret_cast<const float4 *>(bet + cb)[m], c4 = reinterpret_cast<const float4 *>(bk + cb)[m];
+      const float bu[4] = {b4.x, b4.y, b4.z, b4.w}, cu[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int u = 4 * m + e;
+        t[u] = (cb + u <= r) ? t[u] * bu[e] : 0.f;
+        cf[u] = cu[e];
+      }
     }
     __syncthreads();  // X is free
     uint8_t *TP = reinterpret_cast<uint8_t *>(X);
