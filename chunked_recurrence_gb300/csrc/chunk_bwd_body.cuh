@@ -286,6 +286,58 @@ GDN_BWD_FN void norm_and_cumsum(X &x, const Params &p, float *Ks, float *Qs, flo
     for (int i = 1; i < C; ++i) gam[i] += gam[i - 1];
 }
 
+#if defined(__CUDA_ARCH__)
+// Z = (I + A)^-1 for the strictly lower C x C A (row stride lda; zero on and above the
+// diagonal), by forward substitution swept by columns of A, in registers and without a
+// barrier: threads 0-127 each keep an 8 x 4 tile of Z, rows rg + 8 m and columns 16 a + cj
+// (one in each 16-column block; rg = lane % 8, cj = 4 warp + lane / 8).  Rows are taken four
+// at a time: every thread reads rows k .. k + 3 (updated through row k - 1) from their owners
+// by shuffle, finishes them among themselves, and applies all four to its own rows as
+// z_i -= sum_j A_ij Z_j; A_ij = 0 for j >= i leaves rows <= k unchanged and makes rows
+// k + 1 .. k + 3 final.  Rows of Z are zero right of their diagonal, so rows k .. k + 3 touch
+// only the column blocks a <= k / 16 (fixed at compile time).  Writes all of Z, zeros above
+// the diagonal included, to Y (row stride ldy); the caller syncs before Y is read.
+__device__ __forceinline__ void invert_unit_lower_rt(const float *A, int lda, float *Y, int ldy, int tid) {
+  static_assert(C == 64, "the register tiles cover 64 x 64");
+  const int lane = tid & 31, rg = lane & 7, cj = (tid >> 5) * 4 + (lane >> 3);
+  float y[8][4];
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+#pragma unroll
+    for (int a = 0; a < 4; ++a) y[m][a] = (rg + 8 * m == 16 * a + cj) ? 1.f : 0.f;
+  const float *ar = A + rg * lda;
+#pragma unroll
+  for (int k = 0; k < C; k += 4) {
+    const int m0 = k >> 3, na = (k >> 4) + 1;
+    float z[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int a = 0; a < na; ++a) z[j][a] = __shfl_sync(0xffffffffu, y[m0][a], ((k + j) & 7) | (lane & 24));
+    const float a10 = A[(k + 1) * lda + k], a20 = A[(k + 2) * lda + k], a21 = A[(k + 2) * lda + k + 1];
+    const float a30 = A[(k + 3) * lda + k], a31 = A[(k + 3) * lda + k + 1], a32 = A[(k + 3) * lda + k + 2];
+#pragma unroll
+    for (int a = 0; a < na; ++a) {
+      z[1][a] = fmaf(-a10, z[0][a], z[1][a]);
+      z[2][a] = fmaf(-a21, z[1][a], fmaf(-a20, z[0][a], z[2][a]));
+      z[3][a] = fmaf(-a32, z[2][a], fmaf(-a31, z[1][a], fmaf(-a30, z[0][a], z[3][a])));
+    }
+#pragma unroll
+    for (int m = m0; m < 8; ++m) {
+      const float *row = ar + 8 * m * lda + k;
+      const float v0 = row[0], v1 = row[1], v2 = row[2], v3 = row[3];
+#pragma unroll
+      for (int a = 0; a < na; ++a)
+        y[m][a] = fmaf(-v3, z[3][a], fmaf(-v2, z[2][a], fmaf(-v1, z[1][a], fmaf(-v0, z[0][a], y[m][a]))));
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+#pragma unroll
+    for (int a = 0; a < 4; ++a) Y[(rg + 8 * m) * ldy + 16 * a + cj] = y[m][a];
+}
+#endif
+
 // ---- prep: Z, KG and QG of one (chunk, v-head)
 template <int KD, class X, class LD>
 GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot, int h) {
@@ -388,6 +440,11 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
       }
   });
 #endif
+#if defined(__CUDA_ARCH__)
+  x.sync();  // A is complete
+  if (x.tid < 128) invert_unit_lower_rt(Am, CP, Zb, CP, x.tid);
+  x.sync();
+#else
   x.par(C * C, [&](int idx) {
     const int i = idx / C, j = idx % C;
     Zb[i * CP + j] = i == j ? 1.f : 0.f;
@@ -403,6 +460,7 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     });
     x.sync();
   }
+#endif
   x.par(C * C, [&](int idx) { out[idx] = Zb[(idx / C) * CP + idx % C]; });
   // gamma, b, d and the inverse norms, for the walk and grad
   x.par(C, [&](int i) {
