@@ -473,6 +473,41 @@ GDN_BWD_FN void prep_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   });
 }
 
+#if defined(__CUDA_ARCH__)
+// Adds the warp's NTW tiles of a C x C product at (m0, n0) into a row-major C x C fp32 sum
+// (16-byte aligned), its lower triangle with the diagonal only, as 16-byte vector atomics
+// (a quarter of the scalar ones): the elements above the diagonal in a quad add zero.
+template <int NTW>
+__device__ __forceinline__ void add_lower_quads(int lane, const float (&d)[NTW][4], float *sum, int m0, int n0) {
+#pragma unroll
+  for (int j = 0; j < NTW; ++j) {
+    int r, cb;
+    float4 v;
+    tc::frag_quad(lane, d[j], r, cb, v);
+    const int i = m0 + r, c = n0 + 8 * j + cb;
+    if (c > i) continue;  // the quad lies wholly above the diagonal
+    v.y = c + 1 <= i ? v.y : 0.f;
+    v.z = c + 2 <= i ? v.z : 0.f;
+    v.w = c + 3 <= i ? v.w : 0.f;
+    atomicAdd(reinterpret_cast<float4 *>(sum + i * C + c), v);
+  }
+}
+// Adds the warp's NTW tiles of a C x K product at (m0, n0) into rows of a global fp32 array
+// (row i at base + i * stride, 16-byte aligned), rows i < n only, as 16-byte vector atomics.
+template <int NTW>
+__device__ __forceinline__ void add_row_quads(int lane, const float (&d)[NTW][4], float *base, size_t stride, int n,
+                                              int m0, int n0) {
+#pragma unroll
+  for (int j = 0; j < NTW; ++j) {
+    int r, cb;
+    float4 v;
+    tc::frag_quad(lane, d[j], r, cb, v);
+    const int i = m0 + r;
+    if (i < n) atomicAdd(reinterpret_cast<float4 *>(base + (size_t)i * stride + n0 + 8 * j + cb), v);
+  }
+}
+#endif
+
 // ---- walk: the state-dependent steps of BV state rows of one v-head, chunk by chunk
 template <int KD, int BV, class X, class LD>
 GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, int h, int s) {
@@ -876,13 +911,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       if (tl.any && tl.n0 <= tl.m0 + 15) {
         float d[NTW][4] = {};
         tc::mma_nt<NTW>(lane, Os, VP, nullptr, Us, VP, tl.m0, tl.n0, 0, BV, d);
-#pragma unroll
-        for (int j = 0; j < NTW; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
-            if (c <= i) x.add(dPsum + i * C + c, d[j][e]);
-          }
+        add_lower_quads<NTW>(lane, d, dPsum, tl.m0, tl.n0);
       }
     }
 #else
@@ -974,13 +1003,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       if (tl.any && tl.n0 <= tl.m0 + 15) {
         float d[NTW][4] = {};
         tc::mma_nt<NTW>(lane, dUs, VP, nullptr, Ws, VP, tl.m0, tl.n0, 0, BV, d);
-#pragma unroll
-        for (int j = 0; j < NTW; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
-            if (c <= i) x.add(dTsum + i * C + c, d[j][e]);
-          }
+        add_lower_quads<NTW>(lane, d, dTsum, tl.m0, tl.n0);
       }
     }
 #else
@@ -1080,23 +1103,14 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       if (tl.any) {
         float d[NTW][4] = {};
         tc::mma_nn<NTW>(lane, Os, VP, bex, 1.f, Ss, KP, one, tl.m0, tl.n0, 0, BV, d);  // diag(b) Ot S
+        add_row_quads<NTW>(lane, d, p.dqn + ((size_t)t0 * p.Hqk + qh) * K, (size_t)p.Hqk * K, n, tl.m0, tl.n0);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
-            if (i < n) x.add(p.dqn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
-            d[j][e] = 0.f;
-          }
+          for (int e = 0; e < 4; ++e) d[j][e] = 0.f;
         tc::mma_nn<NTW>(lane, Us, VP, dec, 1.f, dSs, KP, one, tl.m0, tl.n0, 0, BV, d);   // diag(d) U' dS1
         tc::mma_nn<NTW>(lane, Ws, VP, bex, -1.f, Ss, KP, one, tl.m0, tl.n0, 0, BV, d);   // - diag(b) dV S
-#pragma unroll
-        for (int j = 0; j < NTW; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
-            if (i < n) x.add(p.dkn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
-          }
+        add_row_quads<NTW>(lane, d, p.dkn + ((size_t)t0 * p.Hqk + qh) * K, (size_t)p.Hqk * K, n, tl.m0, tl.n0);
       }
     }
 #else

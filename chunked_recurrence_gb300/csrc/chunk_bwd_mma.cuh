@@ -183,5 +183,19 @@ __device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const 
 __device__ __forceinline__ int frag_row(int lane, int m0, int e) { return m0 + (lane >> 2) + ((e >> 1) << 3); }
 __device__ __forceinline__ int frag_col(int lane, int n0, int j, int e) { return n0 + 8 * j + 2 * (lane & 3) + (e & 1); }
 
+// Four adjacent elements of tile j for one 16-byte vector store or atomic add: lanes t and
+// t ^ 1 swap half their fragment, so that an even-t lane holds row g, columns 2t .. 2t + 3 and
+// an odd-t lane row g + 8, columns 2t - 2 .. 2t + 1 of the 16 x 8 tile.  row and col are the
+// quad's first element within the tile.  Every lane of the warp takes part.
+__device__ __forceinline__ void frag_quad(int lane, const float (&d)[4], int &row, int &col, float4 &v) {
+  const int t = lane & 3;
+  const bool odd = (t & 1) != 0;
+  const float r0 = __shfl_xor_sync(0xffffffffu, odd ? d[0] : d[2], 1);
+  const float r1 = __shfl_xor_sync(0xffffffffu, odd ? d[1] : d[3], 1);
+  row = (lane >> 2) + (odd ? 8 : 0);
+  col = odd ? 2 * t - 2 : 2 * t;
+  v = odd ? make_float4(r0, r1, d[2], d[3]) : make_float4(d[0], d[1], r0, r1);
+}
+
 }  // namespace tc
 }  // namespace gdn_bwd
