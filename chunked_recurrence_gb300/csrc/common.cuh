@@ -41,6 +41,17 @@ __device__ __forceinline__ int seq_of_token(const int32_t *cu, int n_seqs, int64
   return lo;
 }
 
+// 16-byte asynchronous global -> shared copies (both addresses 16-byte aligned), tracked in
+// commit groups of the issuing thread; waiting on them is the hardware's own wait, no poll
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// every committed group has landed
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 inline gdn_status launch_status() {
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

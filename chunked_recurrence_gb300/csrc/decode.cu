@@ -10,16 +10,21 @@
 // The update is done as S <- a S + u k^T with a = exp(g) and u = beta (v - a S k), and
 // o = scale (a S q + u (k^T q)): every row of S is read once and written once.
 //
-// decode_kernel: one block per (32 rows of S, v-head, sequence), one launch per step.  The
-// block computes its head's gates, forms the conv outputs of its head's q, k and v channels
-// (q and k are shared by Hv / Hqk v-heads and by the V / 32 row blocks; each block
-// recomputes them from the same inputs), rounds them to the storage dtype as the prefill
-// conv stores them, normalises q and k, then each warp streams 8 rows of S: lane l holds
-// S[v][l + 32 j] (coalesced), the two dot products are warp reductions.  The conv state is
-// double-buffered: the block that owns a channel (its v channels; q and k channels by the
-// first v-head of the group and row block 0) writes that channel's shifted inputs to the
-// output buffer, so no block overwrites what another still reads.  State traffic is
-// 2 V K 4 bytes per (sequence, v-head).
+// The work is cut into units of (32 rows of S, v-head, sequence).  A unit computes its head's
+// gates, forms the conv outputs of its head's q, k and v channels (q and k are shared by
+// Hv / Hqk v-heads and by the V / 32 row blocks; each unit recomputes them from the same
+// inputs), rounds them to the storage dtype as the prefill conv stores them, normalises q and
+// k, then each warp takes 8 rows of S: lane l holds S[v][l + 32 j] (coalesced), the two dot
+// products are warp reductions.  The conv state is double-buffered: the unit that owns a
+// channel (its v channels; q and k channels by the first v-head of the group and row block 0)
+// writes that channel's shifted inputs to the output buffer, so no unit overwrites what
+// another still reads.  State traffic is 2 V K 4 bytes per (sequence, v-head).
+//
+// decode_kernel: one block per unit, one launch per step.  A block issues the loads of its
+// rows of S first, then those of its gates, so that their latency overlaps the conv.  (Resident
+// blocks walking the units with the next unit's rows staged into shared memory by cp.async
+// measured slower, 72.9 against 59.6 us at B = 64 on the 4B layer: each unit's prologue then
+// runs in series inside a block, with fewer blocks an SM.)
 #include "common.cuh"
 #include "gates.cuh"
 
@@ -27,47 +32,61 @@ using namespace gdn;
 
 namespace {
 
-constexpr int kDecRows = 32;  // rows of S per block: 4 warps x 8
+constexpr int kDecRows = 32;                   // rows of S per unit: 4 warps x 8
+constexpr int kRowsPerWarp = kDecRows / 4;
 
 template <typename T>
 __device__ __forceinline__ float round_to(float x) {
   return to_f32<T>(from_f32<T>(x));
 }
 
+struct DecArgs {
+  const void *x, *cs_in;
+  void *cs_out;
+  const void *w, *bias;
+  int act;
+  const void *a, *b;
+  const float *A_log, *dt_bias;
+  float *state;
+  int B, Hqk, Hv, V, l2norm, o_f32;
+  float scale;
+  void *o;
+};
+
+// Per-unit values the rows need, after the prologue.
+template <int KPL>
+struct UnitIn {
+  float kr[KPL], qr[KPL];  // this lane's unit-norm k and q features lane + 32 j
+  float kq_n, a, bt;       // k.q of the normed vectors, exp(g), beta
+};
+
+// The prologue of unit (vb, h, b): conv (+ SiLU) of the head's q and k channels and of the
+// unit's v rows into qs, ks, vs; the shifted conv inputs of the channels the unit owns; the
+// q/k norms and the gates.  Ends with the block synced; qs, ks, vs stay in use until the rows
+// are done.
 template <typename T, int KPL, int W>
-__global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, const T *__restrict__ conv_state,
-                                                     T *__restrict__ conv_out, const T *__restrict__ w,
-                                                     const T *__restrict__ bias, int act, const T *__restrict__ ga,
-                                                     const T *__restrict__ gb, const float *__restrict__ A_log,
-                                                     const float *__restrict__ dt_bias, float *__restrict__ S,
-                                                     int Hqk, int Hv, int V, int l2norm, float scale,
-                                                     int o_f32, void *__restrict__ o) {
+__device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h, int b, float *qs, float *ks,
+                                                float *vs, float (*red)[4], UnitIn<KPL> &u) {
   constexpr int K = KPL * 32;
-  const int vb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int qh = h / (Hv / Hqk);
+  const T *x = (const T *)d.x, *cs = (const T *)d.cs_in, *w = (const T *)d.w, *bias = (const T *)d.bias;
+  T *cs_out = (T *)d.cs_out;
+  const int Hqk = d.Hqk, Hv = d.Hv, V = d.V, qh = h / (Hv / Hqk);
   const int C = 2 * Hqk * K + Hv * V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ float qs[K], ks[K], vs[kDecRows];
-  __shared__ float red[3][4];
-  // this warp's 8 rows of S, loaded first so that their latency overlaps the conv below
-  constexpr int kRowsPerWarp = kDecRows / 4;
-  float sr[kRowsPerWarp][KPL];
-  float *Sh = S + ((size_t)b * Hv + h) * V * K;
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int v = vb * kDecRows + warp * kRowsPerWarp + r;
-#pragma unroll
-    for (int j = 0; j < KPL; ++j) sr[r][j] = v < V ? Sh[(size_t)v * K + lane + 32 * j] : 0.f;
+  {  // the gates first: their loads then overlap the conv's
+    float gv;
+    gdn_gates(to_f32<T>(((const T *)d.a)[(size_t)b * Hv + h]), to_f32<T>(((const T *)d.b)[(size_t)b * Hv + h]),
+              d.A_log[h], d.dt_bias[h], gv, u.bt);
+    u.a = __expf(gv);
   }
-
   // conv1d (+ SiLU) of channel c at the sequence's next token, in the prefill conv's order
   auto conv = [&](int c) -> float {
     float acc = bias ? to_f32<T>(bias[c]) : 0.f;
 #pragma unroll
     for (int j = 0; j < W - 1; ++j)
-      acc = fmaf(to_f32<T>(w[(size_t)c * W + j]), to_f32<T>(conv_state[((size_t)b * (W - 1) + j) * C + c]), acc);
+      acc = fmaf(to_f32<T>(w[(size_t)c * W + j]), to_f32<T>(cs[((size_t)b * (W - 1) + j) * C + c]), acc);
     acc = fmaf(to_f32<T>(w[(size_t)c * W + W - 1]), to_f32<T>(x[(size_t)b * C + c]), acc);
-    if (act) acc = __fdividef(acc, 1.f + __expf(-acc));
+    if (d.act) acc = __fdividef(acc, 1.f + __expf(-acc));
     return round_to<T>(acc);
   };
   for (int i = tid; i < K; i += 128) {
@@ -78,13 +97,13 @@ __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, co
     const int v = vb * kDecRows + tid;
     vs[tid] = v < V ? conv(2 * Hqk * K + h * V + v) : 0.f;
   }
-  // shifted conv inputs of the channels this block owns, into the output buffer
+  // shifted conv inputs of the channels this unit owns, into the output buffer
   if (W > 1) {
     auto shift = [&](int c) {
 #pragma unroll
       for (int j = 0; j + 1 < W - 1; ++j)
-        conv_out[((size_t)b * (W - 1) + j) * C + c] = conv_state[((size_t)b * (W - 1) + j + 1) * C + c];
-      conv_out[((size_t)b * (W - 1) + W - 2) * C + c] = x[(size_t)b * C + c];
+        cs_out[((size_t)b * (W - 1) + j) * C + c] = cs[((size_t)b * (W - 1) + j + 1) * C + c];
+      cs_out[((size_t)b * (W - 1) + W - 2) * C + c] = x[(size_t)b * C + c];
     };
     if (tid < kDecRows && vb * kDecRows + tid < V) shift(2 * Hqk * K + h * V + vb * kDecRows + tid);
     if (vb == 0 && h % (Hv / Hqk) == 0)
@@ -116,80 +135,91 @@ __global__ void __launch_bounds__(128) decode_kernel(const T *__restrict__ x, co
   sq = red[0][0] + red[0][1] + red[0][2] + red[0][3];
   sk = red[1][0] + red[1][1] + red[1][2] + red[1][3];
   kq = red[2][0] + red[2][1] + red[2][2] + red[2][3];
-  const float qn = l2norm ? 1.f / sqrtf(sq + kL2Eps) : 1.f;
-  const float kn = l2norm ? 1.f / sqrtf(sk + kL2Eps) : 1.f;
-  const float kq_n = kq * qn * kn;
-  float kr[KPL], qr[KPL];
+  const float qn = d.l2norm ? 1.f / sqrtf(sq + kL2Eps) : 1.f;
+  const float kn = d.l2norm ? 1.f / sqrtf(sk + kL2Eps) : 1.f;
+  u.kq_n = kq * qn * kn;
 #pragma unroll
   for (int j = 0; j < KPL; ++j) {
-    kr[j] = ks[lane + 32 * j] * kn;
-    qr[j] = qs[lane + 32 * j] * qn;
+    u.kr[j] = ks[lane + 32 * j] * kn;
+    u.qr[j] = qs[lane + 32 * j] * qn;
   }
-  float gv, bt;
-  gdn_gates(to_f32<T>(ga[(size_t)b * Hv + h]), to_f32<T>(gb[(size_t)b * Hv + h]), A_log[h], dt_bias[h], gv, bt);
-  const float a = __expf(gv);
-  // rows of S: warp w takes rows 8 w .. 8 w + 7 of this block's 32
+}
+
+// The unit's rows of S: warp w takes rows 8 w .. 8 w + 7 of its 32, held in sr.  Writes the
+// new rows to the state and their outputs to o.
+template <typename T, int KPL>
+__device__ __forceinline__ void decode_rows(const DecArgs &d, int vb, int h, int b, const float (&sr)[kRowsPerWarp][KPL],
+                                            const float *vs, const UnitIn<KPL> &u) {
+  constexpr int K = KPL * 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float *Sh = d.state + ((size_t)b * d.Hv + h) * d.V * K;
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
     const int vr = warp * kRowsPerWarp + r, v = vb * kDecRows + vr;
     float dk = 0.f, dq = 0.f;
 #pragma unroll
     for (int j = 0; j < KPL; ++j) {
-      dk = fmaf(sr[r][j], kr[j], dk);
-      dq = fmaf(sr[r][j], qr[j], dq);
+      dk = fmaf(sr[r][j], u.kr[j], dk);
+      dq = fmaf(sr[r][j], u.qr[j], dq);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       dk += __shfl_xor_sync(0xffffffffu, dk, off);
       dq += __shfl_xor_sync(0xffffffffu, dq, off);
     }
-    if (v >= V) continue;
-    const float u = bt * (vs[vr] - a * dk);
+    if (v >= d.V) continue;
+    const float uu = u.bt * (vs[vr] - u.a * dk);
 #pragma unroll
-    for (int j = 0; j < KPL; ++j) Sh[(size_t)v * K + lane + 32 * j] = fmaf(a, sr[r][j], u * kr[j]);
+    for (int j = 0; j < KPL; ++j) Sh[(size_t)v * K + lane + 32 * j] = fmaf(u.a, sr[r][j], uu * u.kr[j]);
     if (lane == 0) {
-      const float ov = scale * fmaf(a, dq, u * kq_n);
-      const size_t oi = ((size_t)b * Hv + h) * V + v;
-      if (o_f32) reinterpret_cast<float *>(o)[oi] = ov;
-      else reinterpret_cast<T *>(o)[oi] = from_f32<T>(ov);
+      const float ov = d.scale * fmaf(u.a, dq, uu * u.kq_n);
+      const size_t oi = ((size_t)b * d.Hv + h) * d.V + v;
+      if (d.o_f32) reinterpret_cast<float *>(d.o)[oi] = ov;
+      else reinterpret_cast<T *>(d.o)[oi] = from_f32<T>(ov);
     }
   }
 }
 
-struct DecArgs {
-  const void *x, *cs_in;
-  void *cs_out;
-  const void *w, *bias;
-  int act;
-  const void *a, *b;
-  const float *A_log, *dt_bias;
-  float *state;
-  int B, Hqk, Hv, V, l2norm, o_f32;
-  float scale;
-  void *o;
-};
+// one block per unit (vb, h, b) = (blockIdx.x, .y, .z); rows loaded into registers first, so
+// that their latency overlaps the prologue
+template <typename T, int KPL, int W>
+__global__ void __launch_bounds__(128) decode_kernel(const DecArgs d) {
+  constexpr int K = KPL * 32;
+  const int vb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ float qs[K], ks[K], vs[kDecRows];
+  __shared__ float red[3][4];
+  float sr[kRowsPerWarp][KPL];
+  const float *Sh = d.state + ((size_t)b * d.Hv + h) * d.V * K;
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int v = vb * kDecRows + warp * kRowsPerWarp + r;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) sr[r][j] = v < d.V ? Sh[(size_t)v * K + lane + 32 * j] : 0.f;
+  }
+  UnitIn<KPL> u;
+  decode_prologue<T, KPL, W>(d, vb, h, b, qs, ks, vs, red, u);
+  decode_rows<T, KPL>(d, vb, h, b, sr, vs, u);
+}
 
 template <typename T, int KPL, int W>
-void launch_decode(const DecArgs &d, cudaStream_t st) {
-  const dim3 grid((unsigned)((d.V + kDecRows - 1) / kDecRows), (unsigned)d.Hv, (unsigned)d.B);
-  decode_kernel<T, KPL, W><<<grid, 128, 0, st>>>((const T *)d.x, (const T *)d.cs_in, (T *)d.cs_out, (const T *)d.w,
-                                                 (const T *)d.bias, d.act, (const T *)d.a, (const T *)d.b, d.A_log,
-                                                 d.dt_bias, d.state, d.Hqk, d.Hv, d.V, d.l2norm, d.scale, d.o_f32,
-                                                 d.o);
+gdn_status launch_decode(const DecArgs &d, cudaStream_t st) {
+  const int nvb = (d.V + kDecRows - 1) / kDecRows;
+  const dim3 grid((unsigned)nvb, (unsigned)d.Hv, (unsigned)d.B);
+  decode_kernel<T, KPL, W><<<grid, 128, 0, st>>>(d);
+  return launch_status();
 }
 
 template <typename T, int KPL>
 gdn_status dispatch_w(int W, const DecArgs &d, cudaStream_t st) {
   switch (W) {
-#define GDN_DEC_W(WW)                   \
-  case WW:                              \
-    launch_decode<T, KPL, WW>(d, st);   \
-    break;
+#define GDN_DEC_W(WW) \
+  case WW:            \
+    return launch_decode<T, KPL, WW>(d, st);
     GDN_DEC_W(1) GDN_DEC_W(2) GDN_DEC_W(3) GDN_DEC_W(4) GDN_DEC_W(5) GDN_DEC_W(6) GDN_DEC_W(7) GDN_DEC_W(8)
 #undef GDN_DEC_W
     default: return GDN_ERR_UNSUPPORTED;
   }
-  return launch_status();
 }
 
 template <typename T>

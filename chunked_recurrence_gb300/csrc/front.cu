@@ -610,14 +610,6 @@ extern "C" gdn_status gdn_cu_seqlens_from_position_ids(const int64_t *position_i
 // shared-memory buffers (cp.async) while the current one is used.
 constexpr int kChainRows = 16;
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
 __global__ void __launch_bounds__(256) chain_reduce_kernel(const float *__restrict__ M,
                                                            const float *__restrict__ S_local,
                                                            const float *__restrict__ h0, int n_seg,

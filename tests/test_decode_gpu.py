@@ -137,3 +137,27 @@ def test_decode_step_empty_batch(crg):
                                d["b"][:0].to(DEV), d["A_log"].to(DEV), d["dt_bias"].to(DEV),
                                torch.zeros((0, 1, 32, 32), device=DEV), 1, 1, 32, 32)
     assert o.shape == (0, 1, 32)
+
+
+@pytest.mark.parametrize("shift", [0, 1])
+def test_decode_state_alignment_paths(crg, shift):
+    """The state 16-byte aligned and 4 bytes off a 16-byte boundary (the ABI takes any float
+    pointer): the same values as the oracle, and bit for bit the same as each other."""
+    Hqk, Hv, K, V, width = 2, 4, 64, 80, 4  # V = 80: a partial third row block of S
+    d = synth.decode_inputs(3, Hqk, Hv, K, V, width, "f32", seed=31777)
+    o_ref, s_ref = oracle_step(d, Hqk, Hv, K, V, width, 1, "f32")
+    outs = []
+    for sh in (0, shift):
+        on = {key: (t.to(DEV) if isinstance(t, torch.Tensor) else t) for key, t in d.items()}
+        n = on["state"].numel()
+        buf = torch.zeros(n + 4, device=DEV)
+        st = buf[sh: sh + n].view(on["state"].shape)
+        st.copy_(on["state"])
+        assert (st.data_ptr() % 16 == 0) == (sh == 0)
+        o, _ = crg.gdn_decode_step(on["x"], on["conv_state"].clone(), on["conv_w"], on["a"], on["b"], on["A_log"],
+                                   on["dt_bias"], st, Hqk, Hv, K, V, act=1, scale=d["scale"])
+        torch.cuda.synchronize()
+        assert_close(o, o_ref, "f32", f"decode o (state offset {sh})")
+        assert_close(st, s_ref, "f32", f"decode state (state offset {sh})")
+        outs.append((o.clone(), st.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
