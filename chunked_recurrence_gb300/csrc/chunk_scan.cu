@@ -1236,7 +1236,11 @@ gdn_status launch_operands(const CUtensorMap &mq, const CUtensorMap &mk, const C
   // blocks an SM holds: shared memory (dynamic + 2 KB static + 1 KB reserved), at most 4
   // (128 registers x 128 threads each)
   const int per_sm = std::max(1, std::min(4, smem_sm / (int)(smem + 3072)));
-  const size_t grid = std::min(items, (size_t)sms * (size_t)per_sm);
+  size_t grid = std::min(items, (size_t)sms * (size_t)per_sm);
+  if (!op.front) {  // as few blocks as give the same number of rounds (strided items)
+    const size_t rounds = (items + grid - 1) / grid;
+    grid = (items + rounds - 1) / rounds;
+  }
   OpParams q = op;
   q.n_items = (int64_t)items;
   if (q.front && cudaMemsetAsync(q.claim, 0, sizeof(*q.claim), st) != cudaSuccess) return GDN_ERR_CUDA;

@@ -14,8 +14,8 @@
 // gates, forms the conv outputs of its head's q, k and v channels (q and k are shared by
 // Hv / Hqk v-heads and by the V / 32 row blocks; each unit recomputes them from the same
 // inputs), rounds them to the storage dtype as the prefill conv stores them, normalises q and
-// k, then each warp takes 8 rows of S: lane l holds S[v][l + 32 j] (coalesced), the two dot
-// products are warp reductions.  The conv state is double-buffered: the unit that owns a
+// k, then each of 4 warps takes 8 rows of S: lane l holds S[v][l + 32 j] (coalesced), the two
+// dot products are warp reductions.  The conv state is double-buffered: the unit that owns a
 // channel (its v channels; q and k channels by the first v-head of the group and row block 0)
 // writes that channel's shifted inputs to the output buffer, so no unit overwrites what
 // another still reads.  State traffic is 2 V K 4 bytes per (sequence, v-head).
@@ -24,7 +24,8 @@
 // rows of S first, then those of its gates, so that their latency overlaps the conv.  (Resident
 // blocks walking the units with the next unit's rows staged into shared memory by cp.async
 // measured slower, 72.9 against 59.6 us at B = 64 on the 4B layer: each unit's prologue then
-// runs in series inside a block, with fewer blocks an SM.)
+// runs in series inside a block, with fewer blocks an SM.  So were units of 128 rows, one per
+// head and sequence, the q/k conv done once (75.5 us), and of 16 rows (78.1 us).)
 #include "common.cuh"
 #include "gates.cuh"
 
@@ -32,8 +33,10 @@ using namespace gdn;
 
 namespace {
 
-constexpr int kDecRows = 32;                   // rows of S per unit: 4 warps x 8
-constexpr int kRowsPerWarp = kDecRows / 4;
+constexpr int kRowsPerWarp = 8;
+constexpr int kDecWarps = 4;
+constexpr int kDecThreads = 32 * kDecWarps;
+constexpr int kDecRows = kRowsPerWarp * kDecWarps;  // rows of S per unit: 16 warps x 8
 
 template <typename T>
 __device__ __forceinline__ float round_to(float x) {
@@ -66,7 +69,7 @@ struct UnitIn {
 // are done.
 template <typename T, int KPL, int W>
 __device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h, int b, float *qs, float *ks,
-                                                float *vs, float (*red)[4], UnitIn<KPL> &u) {
+                                                float *vs, float (*red)[kDecWarps], UnitIn<KPL> &u) {
   constexpr int K = KPL * 32;
   const T *x = (const T *)d.x, *cs = (const T *)d.cs_in, *w = (const T *)d.w, *bias = (const T *)d.bias;
   T *cs_out = (T *)d.cs_out;
@@ -89,7 +92,7 @@ __device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h,
     if (d.act) acc = __fdividef(acc, 1.f + __expf(-acc));
     return round_to<T>(acc);
   };
-  for (int i = tid; i < K; i += 128) {
+  for (int i = tid; i < K; i += kDecThreads) {
     qs[i] = conv(qh * K + i);
     ks[i] = conv(Hqk * K + qh * K + i);
   }
@@ -107,7 +110,7 @@ __device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h,
     };
     if (tid < kDecRows && vb * kDecRows + tid < V) shift(2 * Hqk * K + h * V + vb * kDecRows + tid);
     if (vb == 0 && h % (Hv / Hqk) == 0)
-      for (int i = tid; i < K; i += 128) {
+      for (int i = tid; i < K; i += kDecThreads) {
         shift(qh * K + i);
         shift(Hqk * K + qh * K + i);
       }
@@ -115,7 +118,7 @@ __device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h,
   __syncthreads();
   // |q|^2, |k|^2 and k.q over the head's K features
   float sq = 0.f, sk = 0.f, kq = 0.f;
-  for (int i = tid; i < K; i += 128) {
+  for (int i = tid; i < K; i += kDecThreads) {
     sq = fmaf(qs[i], qs[i], sq);
     sk = fmaf(ks[i], ks[i], sk);
     kq = fmaf(qs[i], ks[i], kq);
@@ -132,9 +135,13 @@ __device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h,
     red[2][warp] = kq;
   }
   __syncthreads();
-  sq = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-  sk = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  kq = red[2][0] + red[2][1] + red[2][2] + red[2][3];
+  sq = sk = kq = 0.f;
+#pragma unroll
+  for (int i = 0; i < kDecWarps; ++i) {
+    sq += red[0][i];
+    sk += red[1][i];
+    kq += red[2][i];
+  }
   const float qn = d.l2norm ? 1.f / sqrtf(sq + kL2Eps) : 1.f;
   const float kn = d.l2norm ? 1.f / sqrtf(sk + kL2Eps) : 1.f;
   u.kq_n = kq * qn * kn;
@@ -183,12 +190,12 @@ __device__ __forceinline__ void decode_rows(const DecArgs &d, int vb, int h, int
 // one block per unit (vb, h, b) = (blockIdx.x, .y, .z); rows loaded into registers first, so
 // that their latency overlaps the prologue
 template <typename T, int KPL, int W>
-__global__ void __launch_bounds__(128) decode_kernel(const DecArgs d) {
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecArgs d) {
   constexpr int K = KPL * 32;
   const int vb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ float qs[K], ks[K], vs[kDecRows];
-  __shared__ float red[3][4];
+  __shared__ float red[3][kDecWarps];
   float sr[kRowsPerWarp][KPL];
   const float *Sh = d.state + ((size_t)b * d.Hv + h) * d.V * K;
 #pragma unroll
@@ -206,7 +213,7 @@ template <typename T, int KPL, int W>
 gdn_status launch_decode(const DecArgs &d, cudaStream_t st) {
   const int nvb = (d.V + kDecRows - 1) / kDecRows;
   const dim3 grid((unsigned)nvb, (unsigned)d.Hv, (unsigned)d.B);
-  decode_kernel<T, KPL, W><<<grid, 128, 0, st>>>(d);
+  decode_kernel<T, KPL, W><<<grid, kDecThreads, 0, st>>>(d);
   return launch_status();
 }
 
