@@ -36,7 +36,7 @@ namespace {
 constexpr int kRowsPerWarp = 8;
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = 32 * kDecWarps;
-constexpr int kDecRows = kRowsPerWarp * kDecWarps;  // rows of S per unit: 16 warps x 8
+constexpr int kDecRows = kRowsPerWarp * kDecWarps;  // rows of S per unit: 4 warps x 8
 
 template <typename T>
 __device__ __forceinline__ float round_to(float x) {
