@@ -20,8 +20,7 @@
 // writes that channel's shifted inputs to the output buffer, so no unit overwrites what
 // another still reads.  State traffic is 2 V K 4 bytes per (sequence, v-head).
 //
-// decode_kernel: one block per unit, one launch per step.  A block issues the loads of its
-// rows of S first, then those of its gates, so that their latency overlaps the conv.  (Resident
+// decode_kernel: one block per unit, one launch per step.  (Resident
 // blocks walking the units with the next unit's rows staged into shared memory by cp.async
 // measured slower, 72.9 against 59.6 us at B = 64 on the 4B layer: each unit's prologue then
 // runs in series inside a block, with fewer blocks an SM.  So were units of 128 rows, one per
@@ -63,13 +62,13 @@ struct UnitIn {
   float kq_n, a, bt;       // k.q of the normed vectors, exp(g), beta
 };
 
-// The prologue of unit (vb, h, b): conv (+ SiLU) of the head's q and k channels and of the
-// unit's v rows into qs, ks, vs; the shifted conv inputs of the channels the unit owns; the
-// q/k norms and the gates.  Ends with the block synced; qs, ks, vs stay in use until the rows
+// The first half of unit (vb, h, b)'s prologue: the gates; conv (+ SiLU) of the head's q and
+// k channels and of the unit's v rows into qs, ks, vs; the shifted conv inputs of the
+// channels the unit owns.  Ends with the block synced; qs, ks, vs stay in use until the rows
 // are done.
 template <typename T, int KPL, int W>
-__device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h, int b, float *qs, float *ks,
-                                                float *vs, float (*red)[kDecWarps], UnitIn<KPL> &u) {
+__device__ __forceinline__ void decode_conv(const DecArgs &d, int vb, int h, int b, float *qs, float *ks, float *vs,
+                                            UnitIn<KPL> &u) {
   constexpr int K = KPL * 32;
   const T *x = (const T *)d.x, *cs = (const T *)d.cs_in, *w = (const T *)d.w, *bias = (const T *)d.bias;
   T *cs_out = (T *)d.cs_out;
@@ -116,6 +115,14 @@ __device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h,
       }
   }
   __syncthreads();
+}
+
+// The second half: the q/k norms from qs and ks, and this lane's normed features.
+template <int KPL>
+__device__ __forceinline__ void decode_norms(const DecArgs &d, const float *qs, const float *ks,
+                                             float (*red)[kDecWarps], UnitIn<KPL> &u) {
+  constexpr int K = KPL * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // |q|^2, |k|^2 and k.q over the head's K features
   float sq = 0.f, sk = 0.f, kq = 0.f;
   for (int i = tid; i < K; i += kDecThreads) {
@@ -152,34 +159,60 @@ __device__ __forceinline__ void decode_prologue(const DecArgs &d, int vb, int h,
   }
 }
 
+// The 16 per-lane partial sums v[0..15] of a warp, each summed over the 32 lanes by one
+// butterfly: at offsets 16, 8, 4, 2 a lane keeps the half of its values that its offset bit
+// selects and adds its partner's copy of that half, then offset 1 adds the last pair.  Lanes
+// 2 m and 2 m + 1 end with the total of value m.  16 shuffles instead of 5 a value, and the
+// same additions, pair by pair, as one xor reduction per value (so the same sums bit for bit).
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = up ? v[i + n / 2] : v[i], send = up ? v[i] : v[i + n / 2];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 // The unit's rows of S: warp w takes rows 8 w .. 8 w + 7 of its 32, held in sr.  Writes the
 // new rows to the state and their outputs to o.
 template <typename T, int KPL>
 __device__ __forceinline__ void decode_rows(const DecArgs &d, int vb, int h, int b, const float (&sr)[kRowsPerWarp][KPL],
                                             const float *vs, const UnitIn<KPL> &u) {
+  static_assert(kRowsPerWarp == 8, "two dot products of 8 rows fill the 16-value butterfly");
   constexpr int K = KPL * 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float *Sh = d.state + ((size_t)b * d.Hv + h) * d.V * K;
+  // this lane's parts of S k (values 0-7) and S q (values 8-15) of the warp's eight rows
+  float part[16];
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int vr = warp * kRowsPerWarp + r, v = vb * kDecRows + vr;
     float dk = 0.f, dq = 0.f;
 #pragma unroll
     for (int j = 0; j < KPL; ++j) {
       dk = fmaf(sr[r][j], u.kr[j], dk);
       dq = fmaf(sr[r][j], u.qr[j], dq);
     }
+    part[r] = dk;
+    part[kRowsPerWarp + r] = dq;
+  }
+  // lanes 2 r, 2 r + 1 hold (S k)_r, lanes 16 + 2 r, 17 + 2 r hold (S q)_r
+  const float tot = warp_sum16(part, lane);
+  const int rl = (lane >> 1) & 7;  // the row whose sum this lane holds
+  const int vr0 = warp * kRowsPerWarp;
+  const float uu_l = u.bt * (vs[vr0 + rl] - u.a * tot);  // u of row rl (lanes 0-15)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      dk += __shfl_xor_sync(0xffffffffu, dk, off);
-      dq += __shfl_xor_sync(0xffffffffu, dq, off);
-    }
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int vr = vr0 + r, v = vb * kDecRows + vr;
+    const float uu = __shfl_sync(0xffffffffu, uu_l, 2 * r);
     if (v >= d.V) continue;
-    const float uu = u.bt * (vs[vr] - u.a * dk);
 #pragma unroll
     for (int j = 0; j < KPL; ++j) Sh[(size_t)v * K + lane + 32 * j] = fmaf(u.a, sr[r][j], uu * u.kr[j]);
-    if (lane == 0) {
-      const float ov = d.scale * fmaf(u.a, dq, uu * u.kq_n);
+    if (lane == 16 + 2 * r) {  // holds (S q)_r
+      const float ov = d.scale * fmaf(u.a, tot, uu * u.kq_n);
       const size_t oi = ((size_t)b * d.Hv + h) * d.V + v;
       if (d.o_f32) reinterpret_cast<float *>(d.o)[oi] = ov;
       else reinterpret_cast<T *>(d.o)[oi] = from_f32<T>(ov);
@@ -187,8 +220,10 @@ __device__ __forceinline__ void decode_rows(const DecArgs &d, int vb, int h, int
   }
 }
 
-// one block per unit (vb, h, b) = (blockIdx.x, .y, .z); rows loaded into registers first, so
-// that their latency overlaps the prologue
+// one block per unit (vb, h, b) = (blockIdx.x, .y, .z).  The conv's few loads go first and
+// the rows of S (16 KB a unit) after them: issued the other way round, the conv's loads, L2
+// hits, waited behind the rows' HBM misses, and the conv took 5.4 of a block's 7.7 us
+// (global-timer stamps at B = 64 on the 4B layer).  The norms then overlap the rows' loads.
 template <typename T, int KPL, int W>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecArgs d) {
   constexpr int K = KPL * 32;
@@ -196,6 +231,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecArgs d) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ float qs[K], ks[K], vs[kDecRows];
   __shared__ float red[3][kDecWarps];
+  UnitIn<KPL> u;
+  decode_conv<T, KPL, W>(d, vb, h, b, qs, ks, vs, u);
   float sr[kRowsPerWarp][KPL];
   const float *Sh = d.state + ((size_t)b * d.Hv + h) * d.V * K;
 #pragma unroll
@@ -204,8 +241,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecArgs d) {
 #pragma unroll
     for (int j = 0; j < KPL; ++j) sr[r][j] = v < d.V ? Sh[(size_t)v * K + lane + 32 * j] : 0.f;
   }
-  UnitIn<KPL> u;
-  decode_prologue<T, KPL, W>(d, vb, h, b, qs, ks, vs, red, u);
+  decode_norms<KPL>(d, qs, ks, red, u);
   decode_rows<T, KPL>(d, vb, h, b, sr, vs, u);
 }
 
