@@ -24,7 +24,9 @@
 // blocks walking the units with the next unit's rows staged into shared memory by cp.async
 // measured slower, 72.9 against 59.6 us at B = 64 on the 4B layer: each unit's prologue then
 // runs in series inside a block, with fewer blocks an SM.  So were units of 128 rows, one per
-// head and sequence, the q/k conv done once (75.5 us), and of 16 rows (78.1 us).)
+// head and sequence, the q/k conv done once (75.5 us), units of 16 rows (78.1 us), and the
+// conv inputs held in registers across the rows' loads (80 registers, 6 blocks an SM: 52.0
+// against 49.5 us).)
 #include "common.cuh"
 #include "gates.cuh"
 
