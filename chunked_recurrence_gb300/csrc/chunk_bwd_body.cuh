@@ -1102,14 +1102,11 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, K>::NTW;
       if (tl.any) {
         float d[NTW][4] = {};
-        tc::mma_nn<NTW>(lane, Os, VP, bex, 1.f, Ss, KP, one, tl.m0, tl.n0, 0, BV, d);  // diag(b) Ot S
-        add_row_quads<NTW>(lane, d, p.dqn + ((size_t)t0 * p.Hqk + qh) * K, (size_t)p.Hqk * K, n, tl.m0, tl.n0);
-#pragma unroll
-        for (int j = 0; j < NTW; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) d[j][e] = 0.f;
-        tc::mma_nn<NTW>(lane, Us, VP, dec, 1.f, dSs, KP, one, tl.m0, tl.n0, 0, BV, d);   // diag(d) U' dS1
-        tc::mma_nn<NTW>(lane, Ws, VP, bex, -1.f, Ss, KP, one, tl.m0, tl.n0, 0, BV, d);   // - diag(b) dV S
+        float dq[NTW][4] = {};
+        tc::mma_nn<NTW, false, false>(lane, Us, VP, dec, 1.f, dSs, KP, nullptr, tl.m0, tl.n0, 0, BV, d);  // diag(d) U' dS1
+        // diag(b) Ot S into dq and - diag(b) dV S into dk, S's fragments split once for both
+        tc::mma_nn_pair<NTW>(lane, Os, Ws, VP, bex, bex, -1.f, Ss, KP, tl.m0, tl.n0, 0, BV, dq, d);
+        add_row_quads<NTW>(lane, dq, p.dqn + ((size_t)t0 * p.Hqk + qh) * K, (size_t)p.Hqk * K, n, tl.m0, tl.n0);
         add_row_quads<NTW>(lane, d, p.dkn + ((size_t)t0 * p.Hqk + qh) * K, (size_t)p.Hqk * K, n, tl.m0, tl.n0);
       }
     }

@@ -129,8 +129,8 @@ __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const 
 // D[m][n] += sum_k mult ra_m A[m][k] kb_k B[k][n]: A rows m0 .. (stride lda) scaled by ra (per
 // row), B rows k (stride ldb) scaled by kb (per row k), columns n0 + 8 j ..  BX: B's values
 // are exact in TF32 and unscaled (kb is not read), its k-scale then carried by A's columns
-// through kb instead.
-template <int NTW, bool BX = false>
+// through kb instead.  KB = false: no k-scale (kb is not read; the same as kb all ones).
+template <int NTW, bool BX = false, bool KB = true>
 __device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const float *ra, float mult, const float *B,
                                        int ldb, const float *kb, int m0, int n0, int kbeg, int kend,
                                        float (&d)[NTW][4]) {
@@ -140,7 +140,7 @@ __device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const 
   const float r0 = mult * ra[m0 + g], r1 = mult * ra[m0 + g + 8];
 #pragma unroll 2
   for (int k0 = kbeg; k0 < kend; k0 += 8) {
-    const float s0 = kb[k0 + t], s1 = kb[k0 + t + 4];
+    const float s0 = KB ? kb[k0 + t] : 1.f, s1 = KB ? kb[k0 + t + 4] : 1.f;
     FragA fa;
     if (BX) frag_a(fa, r0 * s0 * a[k0], r1 * s0 * a[8 * lda + k0], r0 * s1 * a[k0 + 4], r1 * s1 * a[8 * lda + k0 + 4]);
     else frag_a(fa, r0 * a[k0], r1 * a[8 * lda + k0], r0 * a[k0 + 4], r1 * a[8 * lda + k0 + 4]);
@@ -150,6 +150,33 @@ __device__ __forceinline__ void mma_nn(int lane, const float *A, int lda, const 
       if (BX) frag_b_exact(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
       else frag_b(fb, s0 * b[k0 * ldb + 8 * j], s1 * b[(k0 + 4) * ldb + 8 * j]);
       mma_x<false, BX>(d[j], fa, fb);
+    }
+  }
+}
+
+// D1[m][n] += sum_k r1_m A1[m][k] B[k][n] and D2[m][n] += sum_k mult2 r2_m A2[m][k] B[k][n]: two
+// products of the mma_nn form (without a k-scale) that share B, whose fragments are loaded and
+// split once for both.  The same sums, term by term, as two mma_nn calls.
+template <int NTW>
+__device__ __forceinline__ void mma_nn_pair(int lane, const float *A1, const float *A2, int lda, const float *r1,
+                                            const float *r2, float mult2, const float *B, int ldb, int m0, int n0,
+                                            int kbeg, int kend, float (&d1)[NTW][4], float (&d2)[NTW][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float *a1 = A1 + (m0 + g) * lda + t, *a2 = A2 + (m0 + g) * lda + t;
+  const float *b = B + t * ldb + n0 + g;
+  const float p0 = r1[m0 + g], p1 = r1[m0 + g + 8];
+  const float q0 = mult2 * r2[m0 + g], q1 = mult2 * r2[m0 + g + 8];
+#pragma unroll 2
+  for (int k0 = kbeg; k0 < kend; k0 += 8) {
+    FragA f1, f2;
+    frag_a(f1, p0 * a1[k0], p1 * a1[8 * lda + k0], p0 * a1[k0 + 4], p1 * a1[8 * lda + k0 + 4]);
+    frag_a(f2, q0 * a2[k0], q1 * a2[8 * lda + k0], q0 * a2[k0 + 4], q1 * a2[8 * lda + k0 + 4]);
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) {
+      FragB fb;
+      frag_b(fb, b[k0 * ldb + 8 * j], b[(k0 + 4) * ldb + 8 * j]);
+      mma_x<false, false>(d1[j], f1, fb);
+      mma_x<false, false>(d2[j], f2, fb);
     }
   }
 }
