@@ -959,7 +959,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
             const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
             d[j][e] = dec[i] * KdS[i * VP + c];
           }
-        tc::mma_tn<NTW>(lane, QGm, CP, one, 1.f, Os, VP, tl.m0, tl.n0, tl.m0, C, d);
+        tc::mma_tn<NTW, false, false>(lane, QGm, CP, nullptr, 1.f, Os, VP, tl.m0, tl.n0, tl.m0, C, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -1047,7 +1047,7 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float d[NTW][4] = {};
-        tc::mma_tn<NTW>(lane, Zm, CP, one, 1.f, dUs, VP, tl.m0, tl.n0, tl.m0, C, d);
+        tc::mma_tn<NTW, false, false>(lane, Zm, CP, nullptr, 1.f, dUs, VP, tl.m0, tl.n0, tl.m0, C, d);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
@@ -1385,7 +1385,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     constexpr int NTW = tc::Tiles<C, C>::NTW;
     if (tl.any) {
       float d[NTW][4] = {};
-      if (tl.n0 <= tl.m0 + 15) tc::mma_tn<NTW>(lane, Zm, MP, one, 1.f, Ym, MP, tl.m0, tl.n0, tl.m0, C, d);
+      if (tl.n0 <= tl.m0 + 15) tc::mma_tn<NTW, false, false>(lane, Zm, MP, nullptr, 1.f, Ym, MP, tl.m0, tl.n0, tl.m0, C, d);
 #pragma unroll
       for (int j = 0; j < NTW; ++j)
 #pragma unroll

@@ -183,8 +183,9 @@ __device__ __forceinline__ void mma_nn_pair(int lane, const float *A1, const flo
 
 // D[m][n] += sum_k mult ks_k A[k][m] B[k][n]: A stored by rows k (stride lda), so that the
 // operand is its transpose, row k scaled by ks[k]; B rows k (stride ldb), columns n0 + 8 j ..
-// BX: B's values are exact in TF32 (no split).
-template <int NTW, bool BX = false>
+// BX: B's values are exact in TF32 (no split).  KS = false: no row scale (ks is not read;
+// the same as ks all ones).
+template <int NTW, bool BX = false, bool KS = true>
 __device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const float *ks, float mult, const float *B,
                                        int ldb, int m0, int n0, int kbeg, int kend, float (&d)[NTW][4]) {
   const int g = lane >> 2, t = lane & 3;
@@ -192,7 +193,7 @@ __device__ __forceinline__ void mma_tn(int lane, const float *A, int lda, const 
   const float *b = B + t * ldb + n0 + g;
 #pragma unroll 2
   for (int k0 = kbeg; k0 < kend; k0 += 8) {
-    const float s0 = mult * ks[k0 + t], s1 = mult * ks[k0 + t + 4];
+    const float s0 = KS ? mult * ks[k0 + t] : mult, s1 = KS ? mult * ks[k0 + t + 4] : mult;
     FragA fa;
     frag_a(fa, s0 * a[k0 * lda], s0 * a[k0 * lda + 8], s1 * a[(k0 + 4) * lda], s1 * a[(k0 + 4) * lda + 8]);
 #pragma unroll
