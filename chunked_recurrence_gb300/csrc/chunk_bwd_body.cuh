@@ -96,7 +96,7 @@ GDN_BWD_HD size_t prep_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 2 *
 GDN_BWD_HD size_t walk_smem_floats(int K, int BV) {
   return 2 * (size_t)C * (K + 4) + 2 * (size_t)BV * (K + 4) + 8 * (size_t)C * (BV + 4) + 2 * (size_t)C * CP + 12 * C;
 }
-GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 6 * (size_t)C * (C + 4) + 11 * C; }
+GDN_BWD_HD size_t grad_smem_floats(int K) { return 2 * (size_t)C * (K + 4) + 6 * (size_t)C * (C + 4) + 16 * C; }
 
 GDN_BWD_FN int64_t seq_start(const Params &p, int s) { return p.cu ? (int64_t)p.cu[s] : (int64_t)s * p.row_T; }
 
@@ -1241,6 +1241,7 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   float *dgm = dbt + C;        // [C] dL/dgamma, then dg
   float *one = dgm + C;        // [C] ones (a unit scale for the tensor-core products)
   float *kin = one + C, *qin = kin + C;  // [C] each: 1/|k|, 1/|q| with raw keys
+  float *gps = qin + C;        // [5][C] the dgamma phase's sums: rA, cA, rP, cP, bA
 #if defined(__CUDA_ARCH__)
   constexpr bool RAW = LD::kRawTf32;  // k and q kept raw, their norms in kin / qin
 #else
@@ -1419,18 +1420,31 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
   });
 #endif
   x.sync();
-  // dgamma (through Gamma in A and P, b and d) and the rest of dbeta
-  x.par(C, [&](int i) {
-    float rA = 0.f, cA = 0.f, rP = 0.f, cP = 0.f, bA = 0.f;
-    for (int j = 0; j < i; ++j) {
-      const float t = dTm[i * MP + j] * KGm[i * MP + j];
-      bA += t;
-      rA = fmaf(bet[i], t, rA);
+  // dgamma (through Gamma in A and P, b and d) and the rest of dbeta: the row and column sums
+  // of dA * KG and dP * QG, one sum kind per item group (a warp pair each on the device)
+  x.par(4 * C, [&](int idx) {
+    const int i = idx % C, part = idx / C;
+    float acc = 0.f, bA = 0.f;
+    if (part == 0) {
+      for (int j = 0; j < i; ++j) {
+        const float t = dTm[i * MP + j] * KGm[i * MP + j];
+        bA += t;
+        acc = fmaf(bet[i], t, acc);
+      }
+      gps[4 * C + i] = bA;
+    } else if (part == 1) {
+      for (int m = i + 1; m < C; ++m) acc = fmaf(bet[m], dTm[m * MP + i] * KGm[m * MP + i], acc);
+    } else if (part == 2) {
+      for (int j = 0; j <= i; ++j) acc = fmaf(dPm[i * MP + j], QGm[i * MP + j], acc);
+    } else {
+      for (int m = i; m < C; ++m) acc = fmaf(dPm[m * MP + i], QGm[m * MP + i], acc);
     }
-    for (int m = i + 1; m < C; ++m) cA = fmaf(bet[m], dTm[m * MP + i] * KGm[m * MP + i], cA);
-    for (int j = 0; j <= i; ++j) rP = fmaf(dPm[i * MP + j], QGm[i * MP + j], rP);
-    for (int m = i; m < C; ++m) cP = fmaf(dPm[m * MP + i], QGm[m * MP + i], cP);
-    dbt[i] += bA;
+    gps[part * C + i] = acc;
+  });
+  x.sync();
+  x.par(C, [&](int i) {
+    const float rA = gps[i], cA = gps[C + i], rP = gps[2 * C + i], cP = gps[3 * C + i];
+    dbt[i] += gps[4 * C + i];
     dgm[i] = rP - cP + rA - cA + db[i] * bex[i] - dd[i] * dec[i];
   });
   x.sync();
