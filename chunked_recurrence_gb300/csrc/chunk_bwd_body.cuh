@@ -1249,39 +1249,35 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
 #endif
   const float *pr = p.prep + ((size_t)slot * Hv + h) * kPrep;
   const float *sums = p.sums + ((size_t)slot * Hv + h) * kSums;
-  if (p.vec8) {  // every fill of a phase in flight at once
+  if (p.vec8) {  // every fill of the item in flight at once, then every store
     constexpr int NI = 256;
     x.par(NI, [&](int t) {
       Fill4<C, C, NI> fz, fkg, fqg, fdp, fdt;
+      Fill8<C, K, NI> fk, fq;
       fz.load(t, pr, C, C);
       fkg.load(t, pr + C * C, C, C);
       fqg.load(t, pr + 2 * C * C, C, C);
       fdp.load(t, sums, C, C);
       fdt.load(t, sums + C * C, C, C);
-      const float dv = t < C ? sums[2 * C * C + t] : 0.f, bv = t < C ? sums[2 * C * C + C + t] : 0.f;
-      fz.store(t, Zm, MP);
-      fkg.store(t, KGm, MP);
-      fqg.store(t, QGm, MP);
-      fdp.store(t, dPm, MP);
-      fdt.store(t, dTm, MP);
-      if (t < C) {
-        dd[t] = dv;
-        db[t] = bv;
-      }
-    });
-    x.par(NI, [&](int t) {
-      Fill8<C, K, NI> fk, fq;
       fk.load(ld, t, p.k, t0 * p.ks + (int64_t)qh * K, p.ks, n);
       fq.load(ld, t, p.q, t0 * p.qs + (int64_t)qh * K, p.qs, n);
+      const float dv = t < C ? sums[2 * C * C + t] : 0.f, sbv = t < C ? sums[2 * C * C + C + t] : 0.f;
       const bool gi = t < C && t < n;
       const float gv = gi ? p.g[(t0 + t) * Hv + h] : 0.f, bv = gi ? p.beta[(t0 + t) * Hv + h] : 0.f;
       float pv[5] = {};  // with raw keys: gamma, b, d, 1/|k|, 1/|q| from prep
       if (RAW && t < C)
 #pragma unroll
         for (int u = 0; u < 5; ++u) pv[u] = pr[kPrepVec + u * C + t];
+      fz.store(t, Zm, MP);
+      fkg.store(t, KGm, MP);
+      fqg.store(t, QGm, MP);
+      fdp.store(t, dPm, MP);
+      fdt.store(t, dTm, MP);
       fk.store(t, Ks, KP);
       fq.store(t, Qs, KP);
       if (t < C) {
+        dd[t] = dv;
+        db[t] = sbv;
         gam[t] = RAW ? pv[0] : gv;
         bet[t] = bv;
         if (RAW) {
