@@ -1479,24 +1479,16 @@ GDN_BWD_FN void grad_block(X &x, const Params &p, LD ld, float *sm, int64_t slot
     constexpr int NTW = tc::Tiles<C, K>::NTW;
     if (tl.any) {
       float d[NTW][4] = {};
-      tc::mma_nn<NTW, RAW>(lane, dPm, MP, one, 1.f, Ks, KP, RAW ? kin : one, tl.m0, tl.n0, 0, tl.m0 + 16, d);
+      // with raw keys the norms scale K's rows and Q's rows; without them there is no scale
+      tc::mma_nn<NTW, RAW, RAW>(lane, dPm, MP, one, 1.f, Ks, KP, RAW ? kin : nullptr, tl.m0, tl.n0, 0, tl.m0 + 16, d);
+      add_row_quads<NTW>(lane, d, p.dqn + ((size_t)t0 * p.Hqk + qh) * K, (size_t)p.Hqk * K, n, tl.m0, tl.n0);
 #pragma unroll
       for (int j = 0; j < NTW; ++j)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
-            if (i < n) x.add(p.dqn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
-            d[j][e] = 0.f;
-          }
-      tc::mma_tn<NTW, RAW>(lane, dPm, MP, RAW ? qin : one, 1.f, Qs, KP, tl.m0, tl.n0, tl.m0, C, d);
-      tc::mma_nn<NTW, RAW>(lane, Ym, MP, one, 1.f, Ks, KP, RAW ? kin : one, tl.m0, tl.n0, 0, C, d);
-#pragma unroll
-      for (int j = 0; j < NTW; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = tc::frag_row(lane, tl.m0, e), c = tc::frag_col(lane, tl.n0, j, e);
-            if (i < n) x.add(p.dkn + ((size_t)(t0 + i) * p.Hqk + qh) * K + c, d[j][e]);
-          }
+        for (int e = 0; e < 4; ++e) d[j][e] = 0.f;
+      tc::mma_tn<NTW, RAW, RAW>(lane, dPm, MP, RAW ? qin : nullptr, 1.f, Qs, KP, tl.m0, tl.n0, tl.m0, C, d);
+      tc::mma_nn<NTW, RAW, RAW>(lane, Ym, MP, one, 1.f, Ks, KP, RAW ? kin : nullptr, tl.m0, tl.n0, 0, C, d);
+      add_row_quads<NTW>(lane, d, p.dkn + ((size_t)t0 * p.Hqk + qh) * K, (size_t)p.Hqk * K, n, tl.m0, tl.n0);
     }
   }
 #else
