@@ -703,22 +703,39 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
 #if defined(__CUDA_ARCH__)
     {
       const int lane = x.tid & 31;
-      const tc::Tiles<C, BV> tl(x.tid >> 5);
-      constexpr int NTW = tc::Tiles<C, BV>::NTW;
-      if (tl.any) {
-        float d[NTW][4] = {};
-        tc::mma_nt<NTW, false, RAW>(lane, Ks, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, d);
+      // the tile's (i, v) and its K S^T value: the forms of the raw and the unit-norm keys
+      auto epi = [&](int i, int v, float ks) {
+        const float w = Vs[i * VP + v] - bex[i] * ks;
+        Ws[i * VP + v] = w;
+        fw[CV + (size_t)i * V + v] = w;
+        fw[2 * CV + (size_t)i * V + v] = ks;
+      };
+      if constexpr (RAW) {  // raw k exact: a warp takes one column tile, S's fragments split once
+        const tc::TilesM<C, BV> tl(x.tid >> 5);
+        constexpr int MTW = tc::TilesM<C, BV>::MTW;
+        if (tl.any) {
+          float d[MTW][4] = {};
+          tc::mma_nt_m<MTW>(lane, Ks, KP, Ss, KP, tl.m0, tl.n0, 0, K, d);
 #pragma unroll
-        for (int j = 0; j < NTW; ++j)
+          for (int r = 0; r < MTW; ++r)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = tc::frag_row(lane, tl.m0, e), v = tc::frag_col(lane, tl.n0, j, e);
-            const float ks = RAW ? d[j][e] * kin[i] : d[j][e];
-            const float w = Vs[i * VP + v] - bex[i] * ks;
-            Ws[i * VP + v] = w;
-            fw[CV + (size_t)i * V + v] = w;
-            fw[2 * CV + (size_t)i * V + v] = ks;
-          }
+            for (int e = 0; e < 4; ++e) {
+              const int i = tc::frag_row(lane, tl.m0 + 16 * r, e), v = tc::frag_col(lane, tl.n0, 0, e);
+              epi(i, v, d[r][e] * kin[i]);
+            }
+        }
+      } else {
+        const tc::Tiles<C, BV> tl(x.tid >> 5);
+        constexpr int NTW = tc::Tiles<C, BV>::NTW;
+        if (tl.any) {
+          float d[NTW][4] = {};
+          tc::mma_nt<NTW>(lane, Ks, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, d);
+#pragma unroll
+          for (int j = 0; j < NTW; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              epi(tc::frag_row(lane, tl.m0, e), tc::frag_col(lane, tl.n0, j, e), d[j][e]);
+        }
       }
     }
 #else
@@ -854,21 +871,38 @@ GDN_BWD_FN void walk_block(X &x, const Params &p, LD ld, float *sm, int tile, in
     // Q S^T and K dS1^T (on the device tensor-core products, on the host 4 x 2 tiles of
     // (i, v) a thread)
 #if defined(__CUDA_ARCH__)
-    {
+    if constexpr (RAW) {  // raw q, k exact: a warp takes one column tile, its S fragments split once
+      const int lane = x.tid & 31;
+      const tc::TilesM<C, BV> tl(x.tid >> 5);
+      constexpr int MTW = tc::TilesM<C, BV>::MTW;
+      if (tl.any) {
+        float dq[MTW][4] = {}, dk[MTW][4] = {};
+        tc::mma_nt_m<MTW>(lane, Qs, KP, Ss, KP, tl.m0, tl.n0, 0, K, dq);
+        tc::mma_nt_m<MTW>(lane, Ks, KP, dSs, KP, tl.m0, tl.n0, 0, K, dk);
+#pragma unroll
+        for (int r = 0; r < MTW; ++r)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = tc::frag_row(lane, tl.m0 + 16 * r, e), v = tc::frag_col(lane, tl.n0, 0, e);
+            QSs[i * VP + v] = dq[r][e] * qin[i];
+            KdS[i * VP + v] = dk[r][e] * kin[i];
+          }
+      }
+    } else {
       const int lane = x.tid & 31;
       const tc::Tiles<C, BV> tl(x.tid >> 5);
       constexpr int NTW = tc::Tiles<C, BV>::NTW;
       if (tl.any) {
         float dq[NTW][4] = {}, dk[NTW][4] = {};
-        tc::mma_nt<NTW, false, RAW>(lane, Qs, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, dq);
-        tc::mma_nt<NTW, false, RAW>(lane, Ks, KP, nullptr, dSs, KP, tl.m0, tl.n0, 0, K, dk);
+        tc::mma_nt<NTW>(lane, Qs, KP, nullptr, Ss, KP, tl.m0, tl.n0, 0, K, dq);
+        tc::mma_nt<NTW>(lane, Ks, KP, nullptr, dSs, KP, tl.m0, tl.n0, 0, K, dk);
 #pragma unroll
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = tc::frag_row(lane, tl.m0, e), v = tc::frag_col(lane, tl.n0, j, e);
-            QSs[i * VP + v] = RAW ? dq[j][e] * qin[i] : dq[j][e];
-            KdS[i * VP + v] = RAW ? dk[j][e] * kin[i] : dk[j][e];
+            QSs[i * VP + v] = dq[j][e];
+            KdS[i * VP + v] = dk[j][e];
           }
       }
     }

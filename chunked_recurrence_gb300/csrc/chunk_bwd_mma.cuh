@@ -96,6 +96,21 @@ struct Tiles {
   }
 };
 
+// The same tiles assigned the other way round: warp w takes column tile w % NT and MTW
+// consecutive row tiles from (w / NT) MTW, so that a B fragment serves MTW row tiles.  Better
+// where A is cheap to load (exact in TF32) and B must be split.
+template <int M, int N>
+struct TilesM {
+  static constexpr int MT = M / 16, NT = N / 8, MTW = (MT * NT) / 8 > 0 ? (MT * NT) / 8 : 1;
+  int m0, n0;
+  bool any;
+  __device__ __forceinline__ explicit TilesM(int warp) {
+    n0 = (warp % NT) * 8;
+    m0 = (warp / NT) * MTW * 16;
+    any = (warp / NT) * MTW < MT;
+  }
+};
+
 // The three forms below add to D, over k in [kbeg, kend) (multiples of 8), the products of
 // fp32 rows in shared memory; a triangular factor passes the range where it is nonzero.
 
@@ -122,6 +137,29 @@ __device__ __forceinline__ void mma_nt(int lane, const float *A, int lda, const 
       if (BX) frag_b_exact(fb, b[8 * j * ldb + k0], b[8 * j * ldb + k0 + 4]);
       else frag_b(fb, b[8 * j * ldb + k0], b[8 * j * ldb + k0 + 4]);
       mma_x<AX, BX>(d[j], fa, fb);
+    }
+  }
+}
+
+// mma_nt over MTW row tiles m0 + 16 i of one column tile n0 (TilesM): D[i][.] += A B^T with
+// A exact in TF32 (raw bf16 values, no split) and B split, its fragment loaded once for all
+// MTW row tiles.  The same products, in the same order for each tile, as mma_nt.
+template <int MTW>
+__device__ __forceinline__ void mma_nt_m(int lane, const float *A, int lda, const float *B, int ldb, int m0, int n0,
+                                         int kbeg, int kend, float (&d)[MTW][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float *a = A + (m0 + g) * lda + t;
+  const float *b = B + (n0 + g) * ldb + t;
+#pragma unroll 2
+  for (int k0 = kbeg; k0 < kend; k0 += 8) {
+    FragB fb;
+    frag_b(fb, b[k0], b[k0 + 4]);
+#pragma unroll
+    for (int i = 0; i < MTW; ++i) {
+      const float *ai = a + 16 * i * lda;
+      FragA fa;
+      frag_a_exact(fa, ai[k0], ai[8 * lda + k0], ai[k0 + 4], ai[8 * lda + k0 + 4]);
+      mma_x<true, false>(d[i], fa, fb);
     }
   }
 }
