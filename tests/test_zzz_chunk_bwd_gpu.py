@@ -117,3 +117,22 @@ def test_chunk_bwd_bf16_unaligned_inputs(crg):
                             l2norm_qk=True)
     torch.cuda.synchronize()
     _check(got, ref, "bf16 unaligned")
+
+
+def test_chunk_bwd_bf16_varlen_with_states(crg):
+    """bf16 q, k, v (the raw-key path) with a start state h0 and a loss on h_T, packed
+    sequences of 70, 0 and 130 tokens, two v-heads on each of two q/k heads, K = V = 128: the
+    walk's state products see nonzero S and dS1 from the first chunk on."""
+    lens = [70, 0, 130]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v, g, beta, h0, do, dhT = _case(96, int(cu[-1]), 2, 4, 128, 128, len(lens))
+    bf = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    qb, kb, vb = bf(q), bf(k), bf(v)
+    f64 = lambda x: x.double().numpy()
+    ref = oracle.gdn_bwd(f64(qb), f64(kb), f64(vb), g, beta, do, dhT, h0, cu_seqlens=cu, scale=128 ** -0.5,
+                         l2norm_qk=True)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DEV)
+    got = crg.gdn_chunk_bwd(qb.to(DEV), kb.to(DEV), vb.to(DEV), t(g), t(beta), t(do), t(dhT), t(h0),
+                            cu_seqlens=torch.from_numpy(cu).to(DEV), l2norm_qk=True)
+    torch.cuda.synchronize()
+    _check(got, ref, "bf16 varlen with h0 and dh_T")
