@@ -83,13 +83,24 @@ __device__ __forceinline__ void decode_conv(const DecArgs &d, int vb, int h, int
               d.A_log[h], d.dt_bias[h], gv, u.bt);
     u.a = __expf(gv);
   }
-  // conv1d (+ SiLU) of channel c at the sequence's next token, in the prefill conv's order
+  // conv1d (+ SiLU) of channel c at the sequence's next token, in the prefill conv's order;
+  // four bf16 taps, 8-byte aligned, come in one load
+  const bool w8 = W == 4 && sizeof(T) == 2 && (reinterpret_cast<uintptr_t>(w) & 7) == 0;
   auto conv = [&](int c) -> float {
+    float wt[W];
+    if (w8) {
+      const uint2 r = *reinterpret_cast<const uint2 *>(w + (size_t)c * W);
+      const uint32_t h[2] = {r.x, r.y};
+#pragma unroll
+      for (int j = 0; j < W; ++j) wt[j] = __uint_as_float(j & 1 ? h[(j >> 1) & 1] & 0xffff0000u : h[(j >> 1) & 1] << 16);
+    } else {
+#pragma unroll
+      for (int j = 0; j < W; ++j) wt[j] = to_f32<T>(w[(size_t)c * W + j]);
+    }
     float acc = bias ? to_f32<T>(bias[c]) : 0.f;
 #pragma unroll
-    for (int j = 0; j < W - 1; ++j)
-      acc = fmaf(to_f32<T>(w[(size_t)c * W + j]), to_f32<T>(cs[((size_t)b * (W - 1) + j) * C + c]), acc);
-    acc = fmaf(to_f32<T>(w[(size_t)c * W + W - 1]), to_f32<T>(x[(size_t)b * C + c]), acc);
+    for (int j = 0; j < W - 1; ++j) acc = fmaf(wt[j], to_f32<T>(cs[((size_t)b * (W - 1) + j) * C + c]), acc);
+    acc = fmaf(wt[W - 1], to_f32<T>(x[(size_t)b * C + c]), acc);
     if (d.act) acc = __fdividef(acc, 1.f + __expf(-acc));
     return round_to<T>(acc);
   };
