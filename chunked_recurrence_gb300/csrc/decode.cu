@@ -29,8 +29,10 @@
 // against 49.5 us).)
 #include "common.cuh"
 #include "gates.cuh"
+#include "sm100.cuh"
 
 using namespace gdn;
+using namespace gdn::sm100;
 
 namespace {
 
@@ -55,6 +57,7 @@ struct DecArgs {
   int B, Hqk, Hv, V, l2norm, o_f32;
   float scale;
   void *o;
+  int bulk;  // the conv inputs may come by bulk copies (bf16, W = 4, V % 32 == 0, 16-byte aligned)
 };
 
 // Per-unit values the rows need, after the prologue.
@@ -236,23 +239,103 @@ __device__ __forceinline__ void decode_rows(const DecArgs &d, int vb, int h, int
 // one block per unit (vb, h, b) = (blockIdx.x, .y, .z).  The conv's few loads go first and
 // the rows of S (16 KB a unit) after them: issued the other way round, the conv's loads, L2
 // hits, waited behind the rows' HBM misses, and the conv took 5.4 of a block's 7.7 us
-// (global-timer stamps at B = 64 on the 4B layer).  The norms then overlap the rows' loads.
+// (global-timer stamps at B = 64 on the 4B layer).  With bf16 inputs and W = 4 the conv's
+// inputs come instead by bulk async copies (the unit's channels are three contiguous runs in
+// the weights, the carried rows and x), which do not queue behind the rows' loads, so both
+// are in flight at once.  The norms then overlap the rows' loads.
 template <typename T, int KPL, int W>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecArgs d) {
   constexpr int K = KPL * 32;
+  constexpr bool kBulk = sizeof(T) == 2 && W == 4;
+  constexpr int NCH = 2 * K + kDecRows;  // the unit's conv channels: q, k, then its v rows
   const int vb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ float qs[K], ks[K], vs[kDecRows];
   __shared__ float red[3][kDecWarps];
+  __shared__ __align__(16) T cw[kBulk ? NCH * W : 1];   // the channels' taps
+  __shared__ __align__(16) T cin[kBulk ? W * NCH : 1];  // the W - 1 carried rows, then x
+  __shared__ __align__(8) uint64_t cbar;
+  const bool bulk = kBulk && d.bulk;
+  const int Hqk = d.Hqk, Hv = d.Hv, V = d.V, qh = h / (Hv / Hqk);
+  const int C = 2 * Hqk * K + Hv * V;
+  const int cq = qh * K, ck = Hqk * K + qh * K, cv = 2 * Hqk * K + h * V + vb * kDecRows;
+  if (bulk) {
+    if (tid == 0) {
+      mbar_init(&cbar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const T *w = (const T *)d.w, *cs = (const T *)d.cs_in, *x = (const T *)d.x;
+      constexpr uint32_t kb = sizeof(T);
+      mbar_arrive_expect_tx(&cbar, (uint32_t)(2 * NCH * W) * kb);
+      bulk_load(cw, w + (size_t)cq * W, K * W * kb, &cbar);
+      bulk_load(cw + K * W, w + (size_t)ck * W, K * W * kb, &cbar);
+      bulk_load(cw + 2 * K * W, w + (size_t)cv * W, kDecRows * W * kb, &cbar);
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const T *row = j < W - 1 ? cs + ((size_t)b * (W - 1) + j) * C : x + (size_t)b * C;
+        bulk_load(cin + j * NCH, row + cq, K * kb, &cbar);
+        bulk_load(cin + j * NCH + K, row + ck, K * kb, &cbar);
+        bulk_load(cin + j * NCH + 2 * K, row + cv, kDecRows * kb, &cbar);
+      }
+    }
+  }
   UnitIn<KPL> u;
-  decode_conv<T, KPL, W>(d, vb, h, b, qs, ks, vs, u);
   float sr[kRowsPerWarp][KPL];
   const float *Sh = d.state + ((size_t)b * d.Hv + h) * d.V * K;
+  auto load_rows = [&]() {
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int v = vb * kDecRows + warp * kRowsPerWarp + r;
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int v = vb * kDecRows + warp * kRowsPerWarp + r;
 #pragma unroll
-    for (int j = 0; j < KPL; ++j) sr[r][j] = v < d.V ? Sh[(size_t)v * K + lane + 32 * j] : 0.f;
+      for (int j = 0; j < KPL; ++j) sr[r][j] = v < d.V ? Sh[(size_t)v * K + lane + 32 * j] : 0.f;
+    }
+  };
+  bool staged = false;
+  if (bulk) {
+    float gv;
+    gdn_gates(to_f32<T>(((const T *)d.a)[(size_t)b * Hv + h]), to_f32<T>(((const T *)d.b)[(size_t)b * Hv + h]),
+              d.A_log[h], d.dt_bias[h], gv, u.bt);
+    load_rows();
+    u.a = __expf(gv);
+    staged = mbar_wait(&cbar, 0, 1u << 20);
+    if (!staged) (void)mbar_wait(&cbar, 0, 1u << 20);  // the copies land before the block moves on
+  }
+  if (staged) {
+    // conv (+ SiLU) of local channel c from the staged inputs: the prefill conv's order
+    const T *bias = (const T *)d.bias;
+    auto conv_s = [&](int c, int ch) -> float {
+      float acc = bias ? to_f32<T>(bias[ch]) : 0.f;
+#pragma unroll
+      for (int j = 0; j < W - 1; ++j) acc = fmaf(to_f32<T>(cw[c * W + j]), to_f32<T>(cin[j * NCH + c]), acc);
+      acc = fmaf(to_f32<T>(cw[c * W + W - 1]), to_f32<T>(cin[(W - 1) * NCH + c]), acc);
+      if (d.act) acc = __fdividef(acc, 1.f + __expf(-acc));
+      return round_to<T>(acc);
+    };
+    T *cs_out = (T *)d.cs_out;
+    auto shift = [&](int c, int ch) {
+#pragma unroll
+      for (int j = 0; j + 1 < W - 1; ++j) cs_out[((size_t)b * (W - 1) + j) * C + ch] = cin[(j + 1) * NCH + c];
+      cs_out[((size_t)b * (W - 1) + W - 2) * C + ch] = cin[(W - 1) * NCH + c];
+    };
+    for (int i = tid; i < K; i += kDecThreads) {
+      qs[i] = conv_s(i, cq + i);
+      ks[i] = conv_s(K + i, ck + i);
+    }
+    if (tid < kDecRows) vs[tid] = conv_s(2 * K + tid, cv + tid);
+    if (tid < kDecRows) shift(2 * K + tid, cv + tid);
+    if (vb == 0 && h % (Hv / Hqk) == 0)
+      for (int i = tid; i < K; i += kDecThreads) {
+        shift(i, cq + i);
+        shift(K + i, ck + i);
+      }
+    __syncthreads();
+  } else if (bulk) {
+    decode_conv<T, KPL, W>(d, vb, h, b, qs, ks, vs, u);  // (a copy that never landed)
+  } else {
+    decode_conv<T, KPL, W>(d, vb, h, b, qs, ks, vs, u);
+    load_rows();
   }
   decode_norms<KPL>(d, qs, ks, red, u);
   decode_rows<T, KPL>(d, vb, h, b, sr, vs, u);
@@ -308,8 +391,10 @@ extern "C" gdn_status gdn_decode_step(const void *x, const void *conv_state_in, 
     return GDN_ERR_INVALID_ARG;
   if ((int64_t)2 * Hqk * K + (int64_t)Hv * V > 2147483647LL || B > 65535 || Hv > 65535)
     return GDN_ERR_UNSUPPORTED;
+  const int bulk = dtype == GDN_BF16 && width == 4 && V % 32 == 0 && aligned(x, 16) && aligned(conv_state_in, 16) &&
+                   aligned(w, 16);
   DecArgs d{x, conv_state_in, conv_state_out, w, bias, act, a, b, A_log, dt_bias, state, B, Hqk, Hv, V,
-            (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, (flags & GDN_FLAG_O_F32) ? 1 : 0, scale, o};
+            (flags & GDN_FLAG_QK_L2NORM) ? 1 : 0, (flags & GDN_FLAG_O_F32) ? 1 : 0, scale, o, bulk};
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == GDN_BF16) return dispatch_k<__nv_bfloat16>(K, width, d, st);
   return dispatch_k<float>(K, width, d, st);
