@@ -64,6 +64,7 @@ CASES = [  # dtype, B, Hqk, Hv, K, V, width, act, bias
     ("f32", 1, 1, 1, 32, 32, 1, 0, False),        # no conv history, no activation
     ("bf16", 2, 2, 2, 256, 64, 3, 1, True),       # K = 256
     ("f32", 2, 1, 3, 96, 33, 8, 1, False),        # K = 96, V = 33, the widest conv
+    ("bf16", 3, 2, 2, 64, 32, 4, 1, True),        # the bulk-copied conv inputs at K = 64, V = 32, with bias
 ]
 
 
